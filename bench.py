@@ -1,0 +1,485 @@
+"""Benchmark of the 4-bit weight-quantized linear on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step = one Llama-3.2-1B-shaped decode token: 16 layers x {q, k, v, o, gate, up, down}
+plus lm_head, M = 1, group size 32, fp16 scales, every layer its own weight buffers
+(698.4 MB per token, far above the 129 MB L2, so each token streams the whole model from
+HBM and no L2 flush is needed).  The 113 q4lin_run calls of a token are captured once in
+a CUDA graph and replayed; steps are timed with CUDA events on the replay stream.
+
+Printed: one JSON line with the aggregate GB/s, ms/token, the roofline of the GEMV kernel,
+an end-to-end figure through the public C API with host copies, clocks sampled during the
+timed region, the oracle timed on the host cores (rank 0, N = 1), and extra measurements
+(8B decode token, per-shape GEMV bandwidth, prefill TFLOP/s).
+
+N > 1 (torchrun): replicas only -- each rank runs the same token on its own GPU with no
+collective on the data path; a barrier brackets the timed region and the slowest rank's
+time is reported; value = bytes of all ranks / that time ("scaling": "weak").
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode GEMV HBM GB/s & ms/token; prefill TFLOP/s; % roofline on 1 GB300"
+GROUP = 32
+
+# (name, N, K) per decoder layer, in layer order; lm_head last.
+LAYER_1B = [("q", 2048, 2048), ("k", 512, 2048), ("v", 512, 2048), ("o", 2048, 2048),
+            ("gate", 8192, 2048), ("up", 8192, 2048), ("down", 2048, 8192)]
+LAYER_8B = [("q", 4096, 4096), ("k", 1024, 4096), ("v", 1024, 4096), ("o", 4096, 4096),
+            ("gate", 14336, 4096), ("up", 14336, 4096), ("down", 4096, 14336)]
+MODELS = {
+    "1b": dict(layers=16, layer=LAYER_1B, head=("lm_head", 128256, 2048),
+               desc="Llama-3.2-1B-shaped decode token"),
+    "8b": dict(layers=32, layer=LAYER_8B, head=("lm_head", 128256, 4096),
+               desc="Llama-3.1-8B-shaped decode token"),
+}
+PREFILL_NK = [(2048, 2048), (512, 2048), (8192, 2048), (2048, 8192)]
+
+
+def gemv_bytes(N, K, gs=GROUP, scale_bytes=2, bias=False):
+    """Algorithmic bytes of one M=1 GEMV: packed weight + scales + x + out (+ bias)."""
+    return N * ((K + 1) // 2) + (-(-K // gs)) * N * scale_bytes + 4 * K + 4 * N + (4 * N if bias else 0)
+
+
+def token_shapes(model):
+    m = MODELS[model]
+    shapes = []
+    for layer in range(m["layers"]):
+        for name, N, K in m["layer"]:
+            shapes.append((f"{name}{layer}", N, K))
+    shapes.append(m["head"])
+    return shapes
+
+
+# ------------------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi clocks/throttle reasons every 200 ms while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(prefix="q4clk_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), smax=float(parts[2]),
+                                 power=float(parts[3]) if parts[3] not in ("[N/A]", "") else None,
+                                 hw=parts[5], hwt=parts[6], swt=parts[7], swp=parts[8]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        loaded = [r for r in rows if r["power"] is None or r["power"] > 0] or rows
+        reasons = set()
+        for r in loaded:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("swp", "sw_power_cap")):
+                if r[key].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in loaded),
+                "sm_max_mhz": max(r["smax"] for r in loaded),
+                "samples": len(loaded), "reasons": sorted(reasons)}
+
+
+# -------------------------------------------------------------------------- distributed
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(value, world, device=None):
+    """Largest value over all ranks (the slowest rank's time)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64,
+                     device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------------- our workload
+class DecodeToken:
+    """Device buffers of one model's decode token and the q4lin_run calls over them."""
+
+    def __init__(self, handle, model, device, seed_base=1000):
+        import torch
+        self.torch = torch
+        self.h = handle
+        self.shapes = token_shapes(model)
+        self.bufs = []
+        gen = torch.Generator(device=device)
+        for i, (name, N, K) in enumerate(self.shapes):
+            gen.manual_seed(seed_base * 1 + i)
+            w = torch.randint(0, 256, (N, (K + 1) // 2), dtype=torch.uint8, device=device,
+                              generator=gen)
+            s = (torch.rand((-(-K // GROUP), N), device=device, generator=gen) * 0.015
+                 + 0.005).to(torch.float16)
+            self.bufs.append((N, K, w, s))
+        # All activations of a token in one buffer, all outputs in another, so an
+        # end-to-end step is one host->device and one device->host copy.
+        self.x_offsets, self.out_offsets = [], []
+        xo = oo = 0
+        for N, K, _, _ in self.bufs:
+            self.x_offsets.append(xo)
+            self.out_offsets.append(oo)
+            xo += K
+            oo += N
+        self.x_all = torch.randn(xo, device=device, generator=gen)
+        self.out_all = torch.empty(oo, device=device)
+        self.bytes = sum(gemv_bytes(N, K) for N, K, _, _ in self.bufs)
+        self.launches = len(self.bufs)
+
+    def run(self, stream_ptr):
+        from bit_weight_quantized_int4_gb300 import q4lin as q
+        xb, ob = self.x_all.data_ptr(), self.out_all.data_ptr()
+        for (N, K, w, s), xo, oo in zip(self.bufs, self.x_offsets, self.out_offsets):
+            st = q.q4lin_run(self.h, xb + 4 * xo, w.data_ptr(), s.data_ptr(), None,
+                             ob + 4 * oo, 1, N, K, GROUP, q.Q4LIN_SCALE_F16, stream_ptr)
+            if st != q.Q4LIN_OK:
+                raise q.Q4LinError(st, "q4lin_run")
+
+    def head_output(self):
+        N = self.bufs[-1][0]
+        return self.out_all[self.out_offsets[-1]:self.out_offsets[-1] + N]
+
+    def capture(self):
+        torch = self.torch
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            self.run(side.cuda_stream)          # loads every kernel before capture
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.run(torch.cuda.current_stream().cuda_stream)
+        return g
+
+
+def time_graph(torch, graph, steps, warmup, world):
+    """ms per replay, CUDA events on the replay stream, barrier + sync on both sides."""
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            graph.replay()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(steps):
+            graph.replay()
+        end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    return start.elapsed_time(end) / steps
+
+
+def measure_e2e(torch, token, graph, steps, warmup):
+    """Per step: pinned host x -> device, the token's graph, lm_head logits -> pinned host."""
+    x_host = torch.empty(token.x_all.numel(), dtype=torch.float32, pin_memory=True)
+    x_host.copy_(token.x_all.cpu())
+    head = token.head_output()
+    out_host = torch.empty(head.numel(), dtype=torch.float32, pin_memory=True)
+    stream = torch.cuda.Stream()
+
+    def step():
+        token.x_all.copy_(x_host, non_blocking=True)
+        graph.replay()
+        out_host.copy_(head, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            step()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(steps):
+            step()
+        end.record(stream)
+    end.synchronize()
+    ms = start.elapsed_time(end) / steps
+    return ms, x_host.numel() * 4, out_host.numel() * 4
+
+
+def shape_bandwidth(torch, handle, N, K, reps=30, l2_bytes=129 << 20):
+    """GB/s of one GEMV shape in isolation: enough weight copies rotated that each launch
+    streams from HBM; CUDA events around `reps` launches."""
+    from bit_weight_quantized_int4_gb300 import q4lin as q
+    b = gemv_bytes(N, K)
+    copies = max(2, -(-3 * l2_bytes // b))
+    ws = [torch.randint(0, 256, (N, K // 2), dtype=torch.uint8, device="cuda") for _ in range(copies)]
+    ss = [(torch.rand((K // GROUP, N), device="cuda") * 0.015 + 0.005).half() for _ in range(copies)]
+    x = torch.randn(K, device="cuda")
+    out = torch.empty(N, device="cuda")
+    stream = torch.cuda.Stream()
+    sp = stream.cuda_stream
+
+    def launch(i):
+        st = q.q4lin_run(handle, x.data_ptr(), ws[i % copies].data_ptr(),
+                         ss[i % copies].data_ptr(), None, out.data_ptr(), 1, N, K, GROUP,
+                         q.Q4LIN_SCALE_F16, sp)
+        assert st == q.Q4LIN_OK
+
+    with torch.cuda.stream(stream):
+        for i in range(5):
+            launch(i)
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for i in range(reps):
+            launch(i)
+        end.record(stream)
+    end.synchronize()
+    us = start.elapsed_time(end) * 1000 / reps
+    del ws, ss
+    return {"N": N, "K": K, "us": round(us, 3), "GB_s": round(b / us / 1e3, 1)}
+
+
+def prefill_tflops(torch, handle, M, N, K, reps=10):
+    from bit_weight_quantized_int4_gb300 import q4lin as q
+    w = torch.randint(0, 256, (N, K // 2), dtype=torch.uint8, device="cuda")
+    s = torch.rand((K // GROUP, N), device="cuda") * 0.015 + 0.005
+    bias = torch.randn(N, device="cuda") * 0.1
+    x = torch.randn(M, K, device="cuda")
+    out = torch.empty(M, N, device="cuda")
+    st, path = q.q4lin_plan(handle, x.data_ptr(), w.data_ptr(), s.data_ptr(), bias.data_ptr(),
+                            out.data_ptr(), M, N, K, GROUP, q.Q4LIN_SCALE_F32)
+    stream = torch.cuda.Stream()
+
+    def launch():
+        r = q.q4lin_run(handle, x.data_ptr(), w.data_ptr(), s.data_ptr(), bias.data_ptr(),
+                        out.data_ptr(), M, N, K, GROUP, q.Q4LIN_SCALE_F32, stream.cuda_stream)
+        assert r == q.Q4LIN_OK
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            launch()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(reps):
+            launch()
+        end.record(stream)
+    end.synchronize()
+    ms = start.elapsed_time(end) / reps
+    return {"M": M, "N": N, "K": K, "path": q.PATH_NAMES[path], "us": round(ms * 1000, 2),
+            "TFLOP_s": round(2.0 * M * N * K / (ms * 1e-3) / 1e12, 2)}
+
+
+# ------------------------------------------------------------------------- CPU baseline
+def cpu_baseline(min_seconds=10.0, row_fraction=8):
+    """The fp64 oracle, as it stands, on the host cores: every matrix of a 1B decode
+    token restricted to its first N/row_fraction rows, repeated until min_seconds."""
+    import numpy as np
+    import oracle
+    rng = np.random.Generator(np.random.PCG64(7))
+    mats, nbytes = [], 0
+    for name, N, K in token_shapes("1b"):
+        n = max(1, N // row_fraction)
+        w = rng.integers(0, 256, size=(n, K // 2), dtype=np.uint8)
+        s = rng.uniform(0.005, 0.02, size=(K // GROUP, n)).astype(np.float16)
+        x = rng.standard_normal((1, K), dtype=np.float32)
+        mats.append((x, w, s, K))
+        nbytes += gemv_bytes(n, K)
+    oracle.build()
+    t0 = time.perf_counter()
+    passes = 0
+    while True:
+        for x, w, s, K in mats:
+            oracle.linear(x, w, s, None, K, GROUP)
+        passes += 1
+        if time.perf_counter() - t0 >= min_seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": round(nbytes * passes / dt / 1e9, 4), "unit": "GB/s",
+            "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": (f"1B decode token, first 1/{row_fraction} of the rows of each of the "
+                       f"113 matrices ({nbytes / 1e6:.1f} MB), {passes} passes, {dt:.1f} s"),
+            "ms_per_token_equiv": round(dt / passes * row_fraction * 1000, 1)}
+
+
+def run_reference(args, world, rank):
+    """The reference arm: the fp64 oracle on the host cores (no GPU work)."""
+    if rank != 0:
+        return 0
+    for _ in range(args.warmup):
+        cpu_baseline(min_seconds=0.0)
+    vals = [cpu_baseline(min_seconds=1.0) for _ in range(args.steps)]
+    gbs = statistics.median(v["value"] for v in vals)
+    line = {"impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": statistics.median(v["ms_per_token_equiv"] for v in vals),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config("1b"),
+            "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": vals[0]["cores"],
+                             "kind": "oracle", "sample": vals[0]["sample"]},
+            "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+def workload_config(model):
+    shapes = token_shapes(model)
+    b = sum(gemv_bytes(N, K) for _, N, K in shapes)
+    return {"workload": f"{MODELS[model]['desc']}: {len(shapes)} q4 GEMVs (M=1, group 32, "
+                        f"fp16 scales, distinct buffers per layer), {b / 1e6:.1f} MB per token",
+            "bytes_per_step": b, "launches_per_step": len(shapes),
+            "l2": "inputs larger than L2 (129 MB): every token streams from HBM; no flush",
+            "parallelism": "replicas"}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        p = json.load(open(path))
+        return p["hbm_gbs"], p.get("bf16_tflops"), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true")
+    args = ap.parse_args()
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+
+    import torch
+    torch.cuda.set_device(local)
+    from bit_weight_quantized_int4_gb300 import q4lin as q
+    h = q.q4lin_create(local)
+
+    token = DecodeToken(h, "1b", "cuda")
+    graph = token.capture()
+    with ClockSampler(local) as clk:
+        ms = time_graph(torch, graph, args.steps, args.warmup, world)
+    clocks = clk.summary()
+    ms_max = max_over_ranks(ms, world, device="cuda")
+    total_bytes = token.bytes * world
+    gbs = total_bytes / (ms_max * 1e-3) / 1e9
+    hbm_peak, bf16_peak, peak_src = load_peaks()
+    per_gpu_gbs = token.bytes / (ms * 1e-3) / 1e9
+
+    e2e_ms, h2d, d2h = measure_e2e(torch, token, graph, args.steps, args.warmup)
+    e2e_ms = max_over_ranks(e2e_ms, world, device="cuda")
+
+    extra = {}
+    if not args.no_extra and rank == 0:
+        tok8 = DecodeToken(h, "8b", "cuda", seed_base=2000)
+        g8 = tok8.capture()
+        ms8 = time_graph(torch, g8, max(5, args.steps // 4), 3, 1)
+        extra["decode_8b"] = {"ms_per_token": round(ms8, 4),
+                              "GB_s": round(tok8.bytes / (ms8 * 1e-3) / 1e9, 1),
+                              "bytes_per_token": tok8.bytes, "launches": tok8.launches}
+        del g8, tok8
+        torch.cuda.empty_cache()
+        seen, shapes = set(), []
+        for _, N, K in token_shapes("1b") + token_shapes("8b") + [("fused", 22016, 4096)]:
+            if (N, K) not in seen:
+                seen.add((N, K))
+                shapes.append(shape_bandwidth(torch, h, N, K))
+        extra["gemv_shapes"] = shapes
+        extra["prefill"] = [prefill_tflops(torch, h, M, N, K)
+                            for M in (128, 512, 2048) for N, K in PREFILL_NK]
+
+    line = {
+        "metric": METRIC, "value": round(gbs, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max, 4),
+        "ms_per_token": round(ms_max, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": workload_config("1b"),
+        "roofline": {"bound": "hbm", "achieved": round(per_gpu_gbs, 1), "peak": hbm_peak,
+                     "unit": "GB/s", "frac": round(per_gpu_gbs / hbm_peak, 4),
+                     "traffic": None,
+                     "kernel": "gemv_kernel (all 113 launches of a token; launch gaps "
+                               "included)", "peak_source": peak_src},
+        "e2e": {"value": round(token.bytes * world / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "clocks": clocks,
+        "gpu_launches": token.launches * args.steps,
+    }
+    if extra:
+        line["extra"] = extra
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline()
+    if rank == 0:
+        print(json.dumps(line))
+    q.q4lin_destroy(h)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,302 @@
+// q4lin.cpp -- C-ABI host layer: argument validation, path planning, dispatch, options.
+//
+// The guards mirror the fail-loud checks on the pages ("Add linear_qcs4w op",
+// Implementation: packed row length ceil(K/2), enough scales; the K == 0 guard of the
+// q4gsw training ops) and the "throw before any allocation" rule of "Add optimized
+// linear_fp32 op": every check runs before anything is enqueued.  The path choice
+// mirrors the pages' M-dispatch (M = 1 -> GEMV; M > 1 -> a GEMM chosen by a fail-closed
+// eligibility test, "Add 256-thread steel q4gsw prefill GEMM") with a crossover measured
+// on GB300 instead of shape thresholds.
+#include "../../include/q4lin.h"
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stdlib.h>
+
+#include <new>
+
+#include "q4lin_internal.h"
+
+struct q4lin_handle {
+    int device = 0;
+    int sm_count = 0;
+    int max_smem_optin = 0;
+    int force_path = Q4LIN_PATH_AUTO;
+    int even_high = 0;
+    int pdl = 0;
+    int64_t wait_limit = 0;  // 0: default
+    int* d_status = nullptr;
+};
+
+namespace {
+
+constexpr int64_t kDefaultWaitLimit = 1LL << 26;  // mbarrier polls before giving up
+
+// Crossover: at and above this M the tensor-core GEMM replaces the row-streaming
+// CUDA-core kernel (when both are eligible).  Measured on GB300; see plan().
+constexpr int64_t kTcMinM = 4;
+
+class DeviceGuard {
+   public:
+    explicit DeviceGuard(int device) {
+        if (cudaGetDevice(&prev_) != cudaSuccess) prev_ = -1;
+        if (prev_ != device) ok_ = cudaSetDevice(device) == cudaSuccess;
+    }
+    ~DeviceGuard() {
+        int cur = -1;
+        if (prev_ >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev_) cudaSetDevice(prev_);
+    }
+    bool ok() const { return ok_; }
+
+   private:
+    int prev_ = -1;
+    bool ok_ = true;
+};
+
+bool mul_ok(int64_t a, int64_t b, int64_t* r) { return !__builtin_mul_overflow(a, b, r); }
+
+bool overlaps(const void* a, int64_t abytes, const void* b, int64_t bbytes) {
+    if (!a || !b || abytes <= 0 || bbytes <= 0) return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + (uintptr_t)bbytes && b0 < a0 + (uintptr_t)abytes;
+}
+
+// Validation shared by q4lin_run and q4lin_plan.  On success fills `p` (except the
+// out pointer for plan) and returns Q4LIN_OK; M == 0 or N == 0 is reported via *empty.
+q4lin_status_t validate(q4lin_handle_t h, const float* x, const uint8_t* qweight,
+                        const void* scales, const float* bias, const void* out, int64_t M,
+                        int64_t N, int64_t K, int64_t group_size, int scale_dtype,
+                        q4lin::Problem* p, bool* empty) {
+    if (!h) return Q4LIN_ERR_INVALID_ARG;
+    if (M < 0 || N < 0 || K < 1 || group_size < 1) return Q4LIN_ERR_INVALID_ARG;
+    if (scale_dtype != Q4LIN_SCALE_F32 && scale_dtype != Q4LIN_SCALE_F16)
+        return Q4LIN_ERR_INVALID_ARG;
+    *empty = (M == 0 || N == 0);
+    if (*empty) return Q4LIN_OK;
+    if (!x || !qweight || !scales || !out) return Q4LIN_ERR_INVALID_ARG;
+    const int64_t esize = scale_dtype == Q4LIN_SCALE_F16 ? 2 : 4;
+    const int64_t Kp = (K + 1) / 2;
+    const int64_t G = (K + group_size - 1) / group_size;
+    int64_t xb, wb, sb, ob, t;
+    if (!mul_ok(M, K, &t) || !mul_ok(t, 4, &xb)) return Q4LIN_ERR_INVALID_ARG;
+    if (!mul_ok(N, Kp, &wb)) return Q4LIN_ERR_INVALID_ARG;
+    if (!mul_ok(G, N, &t) || !mul_ok(t, esize, &sb)) return Q4LIN_ERR_INVALID_ARG;
+    if (!mul_ok(M, N, &t) || !mul_ok(t, 4, &ob)) return Q4LIN_ERR_INVALID_ARG;
+    const int64_t bb = bias ? N * 4 : 0;
+    // Element alignment.
+    if (reinterpret_cast<uintptr_t>(x) % 4 || reinterpret_cast<uintptr_t>(out) % 4 ||
+        (bias && reinterpret_cast<uintptr_t>(bias) % 4) ||
+        reinterpret_cast<uintptr_t>(scales) % esize)
+        return Q4LIN_ERR_INVALID_ARG;
+    // The output must not alias any input.
+    if (overlaps(out, ob, x, xb) || overlaps(out, ob, qweight, wb) ||
+        overlaps(out, ob, scales, sb) || overlaps(out, ob, bias, bb))
+        return Q4LIN_ERR_INVALID_ARG;
+    p->x = x;
+    p->qweight = qweight;
+    p->scales = scales;
+    p->bias = bias;
+    p->out = static_cast<float*>(const_cast<void*>(out));
+    p->M = M;
+    p->N = N;
+    p->K = K;
+    p->group_size = group_size;
+    p->scale_f16 = scale_dtype == Q4LIN_SCALE_F16;
+    p->even_high = h->even_high;
+    return Q4LIN_OK;
+}
+
+q4lin::LaunchCtx make_ctx(q4lin_handle_t h, cudaStream_t stream) {
+    q4lin::LaunchCtx c;
+    c.stream = stream;
+    c.sm_count = h->sm_count;
+    c.max_smem_optin = h->max_smem_optin;
+    c.pdl = h->pdl;
+    c.status_word = h->d_status;
+    c.wait_limit = h->wait_limit > 0 ? h->wait_limit : kDefaultWaitLimit;
+    return c;
+}
+
+// Which kernel family runs the problem.
+q4lin_status_t plan(q4lin_handle_t h, const q4lin::Problem& p, const q4lin::LaunchCtx& c,
+                    int* path) {
+    const bool row_ok = q4lin::rowstream_eligible(p);
+    switch (h->force_path) {
+        case Q4LIN_PATH_GEMV:
+            if (!row_ok) return Q4LIN_ERR_UNSUPPORTED;
+            *path = Q4LIN_PATH_GEMV;
+            return Q4LIN_OK;
+        case Q4LIN_PATH_FFMA:
+            *path = Q4LIN_PATH_FFMA;
+            return Q4LIN_OK;
+        case Q4LIN_PATH_TC:
+            if (!q4lin::tc_eligible(p, c)) return Q4LIN_ERR_UNSUPPORTED;
+            *path = Q4LIN_PATH_TC;
+            return Q4LIN_OK;
+        default:
+            break;
+    }
+    if (p.M >= kTcMinM && q4lin::tc_eligible(p, c)) {
+        *path = Q4LIN_PATH_TC;
+    } else if (row_ok) {
+        *path = Q4LIN_PATH_GEMV;
+    } else {
+        *path = Q4LIN_PATH_FFMA;
+    }
+    return Q4LIN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+q4lin_status_t q4lin_create(q4lin_handle_t* handle, int device) {
+    if (!handle) return Q4LIN_ERR_INVALID_ARG;
+    *handle = nullptr;
+    int count = 0;
+    if (cudaGetDeviceCount(&count) != cudaSuccess || device < 0 || device >= count) {
+        cudaGetLastError();
+        return Q4LIN_ERR_NO_DEVICE;
+    }
+    int major = 0, minor = 0, sms = 0, smem = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, device) !=
+            cudaSuccess)
+        return Q4LIN_ERR_CUDA;
+    if (major != 10 || minor != 3) return Q4LIN_ERR_UNSUPPORTED;
+    q4lin_handle* h = new (std::nothrow) q4lin_handle();
+    if (!h) return Q4LIN_ERR_CUDA;
+    h->device = device;
+    h->sm_count = sms;
+    h->max_smem_optin = smem;
+    {
+        DeviceGuard g(device);
+        if (!g.ok() || cudaMalloc(&h->d_status, sizeof(int)) != cudaSuccess ||
+            cudaMemset(h->d_status, 0, sizeof(int)) != cudaSuccess) {
+            if (h->d_status) cudaFree(h->d_status);
+            delete h;
+            return Q4LIN_ERR_CUDA;
+        }
+    }
+    *handle = h;
+    return Q4LIN_OK;
+}
+
+q4lin_status_t q4lin_destroy(q4lin_handle_t h) {
+    if (!h) return Q4LIN_OK;
+    {
+        DeviceGuard g(h->device);
+        if (h->d_status) cudaFree(h->d_status);
+    }
+    delete h;
+    return Q4LIN_OK;
+}
+
+q4lin_status_t q4lin_plan(q4lin_handle_t h, const float* x, const uint8_t* qweight,
+                          const void* scales, const float* bias, const float* out,
+                          int64_t M, int64_t N, int64_t K, int64_t group_size,
+                          int scale_dtype, int* path_out) {
+    if (!path_out) return Q4LIN_ERR_INVALID_ARG;
+    q4lin::Problem p;
+    bool empty = false;
+    q4lin_status_t st = validate(h, x, qweight, scales, bias, out, M, N, K, group_size,
+                                 scale_dtype, &p, &empty);
+    if (st != Q4LIN_OK) return st;
+    if (empty) {
+        *path_out = Q4LIN_PATH_AUTO;
+        return Q4LIN_OK;
+    }
+    return plan(h, p, make_ctx(h, nullptr), path_out);
+}
+
+q4lin_status_t q4lin_run(q4lin_handle_t h, const float* x, const uint8_t* qweight,
+                         const void* scales, const float* bias, float* out, int64_t M,
+                         int64_t N, int64_t K, int64_t group_size, int scale_dtype,
+                         void* stream) {
+    q4lin::Problem p;
+    bool empty = false;
+    q4lin_status_t st = validate(h, x, qweight, scales, bias, out, M, N, K, group_size,
+                                 scale_dtype, &p, &empty);
+    if (st != Q4LIN_OK || empty) return st;
+    const q4lin::LaunchCtx c = make_ctx(h, static_cast<cudaStream_t>(stream));
+    int path = 0;
+    st = plan(h, p, c, &path);
+    if (st != Q4LIN_OK) return st;
+    DeviceGuard g(h->device);
+    if (!g.ok()) return Q4LIN_ERR_CUDA;
+    cudaError_t err;
+    switch (path) {
+        case Q4LIN_PATH_TC: err = q4lin::tc_launch(p, c); break;
+        case Q4LIN_PATH_GEMV: err = q4lin::rowstream_launch(p, c); break;
+        default: err = q4lin::generic_launch(p, c); break;
+    }
+    if (err == cudaSuccess) err = cudaGetLastError();
+    return err == cudaSuccess ? Q4LIN_OK : Q4LIN_ERR_CUDA;
+}
+
+q4lin_status_t q4lin_set_option(q4lin_handle_t h, int option, int64_t value) {
+    if (!h) return Q4LIN_ERR_INVALID_ARG;
+    switch (option) {
+        case Q4LIN_OPT_FORCE_PATH:
+            if (value < Q4LIN_PATH_AUTO || value > Q4LIN_PATH_TC) return Q4LIN_ERR_INVALID_ARG;
+            h->force_path = (int)value;
+            return Q4LIN_OK;
+        case Q4LIN_OPT_NIBBLE_EVEN_HIGH:
+            if (value != 0 && value != 1) return Q4LIN_ERR_INVALID_ARG;
+            h->even_high = (int)value;
+            return Q4LIN_OK;
+        case Q4LIN_OPT_WAIT_LIMIT:
+            h->wait_limit = value > 0 ? value : 0;
+            return Q4LIN_OK;
+        case Q4LIN_OPT_PDL:
+            if (value != 0 && value != 1) return Q4LIN_ERR_INVALID_ARG;
+            h->pdl = (int)value;
+            return Q4LIN_OK;
+        default:
+            return Q4LIN_ERR_INVALID_ARG;
+    }
+}
+
+q4lin_status_t q4lin_get_option(q4lin_handle_t h, int option, int64_t* value) {
+    if (!h || !value) return Q4LIN_ERR_INVALID_ARG;
+    switch (option) {
+        case Q4LIN_OPT_FORCE_PATH: *value = h->force_path; return Q4LIN_OK;
+        case Q4LIN_OPT_NIBBLE_EVEN_HIGH: *value = h->even_high; return Q4LIN_OK;
+        case Q4LIN_OPT_WAIT_LIMIT:
+            *value = h->wait_limit > 0 ? h->wait_limit : kDefaultWaitLimit;
+            return Q4LIN_OK;
+        case Q4LIN_OPT_PDL: *value = h->pdl; return Q4LIN_OK;
+        default: return Q4LIN_ERR_INVALID_ARG;
+    }
+}
+
+q4lin_status_t q4lin_check_device_status(q4lin_handle_t h, void* stream, int* code_out) {
+    if (!h || !code_out) return Q4LIN_ERR_INVALID_ARG;
+    DeviceGuard g(h->device);
+    if (!g.ok()) return Q4LIN_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int code = 0;
+    if (cudaMemcpyAsync(&code, h->d_status, sizeof(int), cudaMemcpyDeviceToHost, s) !=
+            cudaSuccess ||
+        cudaMemsetAsync(h->d_status, 0, sizeof(int), s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return Q4LIN_ERR_CUDA;
+    *code_out = code;
+    return code ? Q4LIN_ERR_TIMEOUT : Q4LIN_OK;
+}
+
+const char* q4lin_status_string(q4lin_status_t s) {
+    switch (s) {
+        case Q4LIN_OK: return "ok";
+        case Q4LIN_ERR_INVALID_ARG: return "invalid argument";
+        case Q4LIN_ERR_UNSUPPORTED: return "unsupported device or forced path";
+        case Q4LIN_ERR_CUDA: return "CUDA error";
+        case Q4LIN_ERR_TIMEOUT: return "device-side bounded wait ran out";
+        case Q4LIN_ERR_NO_DEVICE: return "no such CUDA device";
+        default: return "unknown status";
+    }
+}
+
+}  // extern "C"

@@ -1,0 +1,45 @@
+// Internal interface between the C-ABI host layer (q4lin.cpp) and the kernel files.
+// Not installed; the public interface is include/q4lin.h.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace q4lin {
+
+// One linear problem, already validated by the host layer.
+struct Problem {
+    const float* x;          // [M, K] fp32
+    const uint8_t* qweight;  // [N, ceil(K/2)] packed codes
+    const void* scales;      // [ceil(K/gs), N] fp32 or fp16
+    const float* bias;       // [N] or nullptr
+    float* out;              // [M, N] fp32
+    int64_t M, N, K, group_size;
+    int scale_f16;           // 1: binary16 scales, 0: fp32
+    int even_high;           // 1: even k in the high nibble
+};
+
+// Per-launch context from the handle.
+struct LaunchCtx {
+    cudaStream_t stream;
+    int sm_count;
+    int max_smem_optin;      // bytes of opt-in shared memory per block
+    int pdl;                 // launch with programmatic stream serialization
+    int* status_word;        // device int, first nonzero code a kernel records
+    int64_t wait_limit;      // iteration limit of bounded device-side waits
+};
+
+// Row-streaming CUDA-core kernel (decode GEMV, and small M with weight reuse across a
+// tile of up to 4 activation rows).  Needs K % 32 == 0, 16-byte aligned x and qweight,
+// and group_size % 32 == 0 or group_size >= K.
+bool rowstream_eligible(const Problem& p);
+cudaError_t rowstream_launch(const Problem& p, const LaunchCtx& c);
+
+// Generic CUDA-core kernel: any K (odd included), any group size, any alignment.
+cudaError_t generic_launch(const Problem& p, const LaunchCtx& c);
+
+// tcgen05 tensor-core GEMM.  Eligibility and launch live in tc_gemm.cu.
+bool tc_eligible(const Problem& p, const LaunchCtx& c);
+cudaError_t tc_launch(const Problem& p, const LaunchCtx& c);
+
+}  // namespace q4lin

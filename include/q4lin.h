@@ -1,0 +1,148 @@
+/*
+ * q4lin.h -- C ABI of the GB300 (sm_103a) 4-bit group-symmetric weight-quantized linear.
+ *
+ *   out[m,n] = bias[n] + sum_k x[m,k] * (nib(W)[n,k] - 8) * scale[k / group_size, n]
+ *
+ * Sources of the operation ("[ExecuTorch][WebGPU] ..." pull-request pages):
+ *   - "Add linear_qcs4w op (et_vk.linear_qcs4w)", Solution and Constraints (2)-(4): the
+ *     per-term formula in[m,k] * (unpack_int4(w) - 8) * scale, the grouped scale index
+ *     (k / group_size) * N + n, the +8-shifted signed int4, the packed [N, K/2] uint8
+ *     weight whose LOW nibble holds the even k (the q4gsw packer's "(odd << 4) | even"),
+ *     the per-output-channel case (one scale per n, i.e. group_size = K), and the
+ *     fail-loud argument guards (K_packed == ceil(K/2), enough scales).
+ *   - "Add fp32 matmul ops ... (linear_q4gsw_backward)", #20943: dequant = (code - 8) *
+ *     scale with [num_groups, N] scales; the K == 0 guard of the sibling ops.
+ *   - "Add optimized linear_fp32 op", Implementation: the optional bias (a dummy binding
+ *     when absent) added once in the epilogue, v = v + bias[n].
+ *   - "Add 256-thread steel q4gsw prefill GEMM", Solution/Implementation: M = 1 routes to
+ *     a GEMV, M > 1 to GEMM kernels chosen by a fail-closed eligibility check.
+ *
+ * Conventions for every entry point:
+ *   - Every buffer is owned by the caller.  q4lin_run allocates nothing, never
+ *     synchronizes the device and only enqueues kernels on the given stream.  A handle
+ *     owns its options and one small device status word, nothing else.
+ *   - Status codes, never exceptions, aborts or prints.  Arguments are validated before
+ *     any launch: a non-OK status from validation means nothing was enqueued.
+ *   - All device pointers must be device-accessible memory of the handle's device.
+ *   - Reentrant for distinct streams; q4lin_set_option must not race with q4lin_run on
+ *     the same handle.
+ */
+#ifndef Q4LIN_H
+#define Q4LIN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define Q4LIN_API __attribute__((visibility("default")))
+#else
+#define Q4LIN_API
+#endif
+
+typedef struct q4lin_handle* q4lin_handle_t;
+
+typedef enum {
+    Q4LIN_OK = 0,
+    Q4LIN_ERR_INVALID_ARG = 1, /* bad pointer, size, alignment, overlap or option     */
+    Q4LIN_ERR_UNSUPPORTED = 2, /* device is not sm_103, or a forced path cannot run   */
+    Q4LIN_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed                 */
+    Q4LIN_ERR_TIMEOUT = 4,     /* a bounded device-side wait gave up (see status word) */
+    Q4LIN_ERR_NO_DEVICE = 5    /* no CUDA device with that ordinal                     */
+} q4lin_status_t;
+
+/* Element type of the scales array. */
+typedef enum { Q4LIN_SCALE_F32 = 0, Q4LIN_SCALE_F16 = 1 } q4lin_scale_dtype_t;
+
+/* Kernel families.  AUTO picks by M and shape (measured crossover); the others force. */
+typedef enum {
+    Q4LIN_PATH_AUTO = 0,
+    Q4LIN_PATH_GEMV = 1,    /* row-streaming CUDA-core kernel (M = 1 decode, small M)  */
+    Q4LIN_PATH_FFMA = 2,    /* generic CUDA-core kernel: any K, group size, alignment  */
+    Q4LIN_PATH_TC = 3       /* tcgen05 tensor-core GEMM (TMEM accumulators)            */
+} q4lin_path_t;
+
+/* Options for q4lin_set_option / q4lin_get_option. */
+typedef enum {
+    /* q4lin_path_t; default AUTO.  A forced path that cannot run the shape makes
+     * q4lin_run return Q4LIN_ERR_UNSUPPORTED. */
+    Q4LIN_OPT_FORCE_PATH = 1,
+    /* 0 (default): the low nibble of byte j holds k = 2j (the q4gsw packer).
+     * 1: the high nibble holds k = 2j (the qcs4w AOT packer's "(even << 4) | odd"
+     * order, "Add linear_qcs4w op", Constraints (2)). */
+    Q4LIN_OPT_NIBBLE_EVEN_HIGH = 2,
+    /* Iteration limit of every bounded device-side wait (mbarrier polls) in the
+     * tensor-core kernel; <= 0 restores the default.  After the limit the kernel records
+     * a code in the handle's status word and returns without computing. */
+    Q4LIN_OPT_WAIT_LIMIT = 3,
+    /* 1: launch with programmatic dependent launch, so a kernel may start streaming
+     * its weights while the previous kernel on the stream drains (default 0). */
+    Q4LIN_OPT_PDL = 4
+} q4lin_option_t;
+
+/* Create a handle for CUDA device `device`.  Queries the SM count and shared-memory
+ * limit and allocates the 4-byte device status word.  Q4LIN_ERR_NO_DEVICE if the
+ * ordinal does not exist, Q4LIN_ERR_UNSUPPORTED if it is not compute capability 10.3.
+ * The caller's current device is left unchanged. */
+Q4LIN_API q4lin_status_t q4lin_create(q4lin_handle_t* handle, int device);
+
+/* Release the handle and its status word.  NULL is accepted (no-op). */
+Q4LIN_API q4lin_status_t q4lin_destroy(q4lin_handle_t handle);
+
+/* out = x @ dequant(W)^T (+ bias), enqueued on `stream` (a cudaStream_t; NULL = the
+ * legacy default stream).
+ *
+ *   x        float32 [M, K], row-major, contiguous, 4-byte aligned.
+ *   qweight  uint8 [N, ceil(K/2)], row-major: byte (n, j) holds codes for k = 2j and
+ *            k = 2j+1 (low/high nibble by default, see Q4LIN_OPT_NIBBLE_EVEN_HIGH);
+ *            signed weight = code - 8.  For odd K the last high nibble is never read.
+ *   scales   [ceil(K / group_size), N] row-major, float32 (scale_dtype 0, 4-byte
+ *            aligned) or IEEE binary16 (scale_dtype 1, 2-byte aligned).  Per-channel
+ *            (qcs4w) weights use group_size = K with a [1, N] (= [N]) array.
+ *   bias     float32 [N], 4-byte aligned, or NULL for no bias.
+ *   out      float32 [M, N], row-major, 4-byte aligned; must not overlap any input.
+ *   M >= 0, N >= 0, K >= 1, group_size >= 1.  M == 0 or N == 0 returns Q4LIN_OK and
+ *   launches nothing; K == 0 is Q4LIN_ERR_INVALID_ARG.
+ * Any K, group size and alignment beyond the element alignment above is accepted;
+ * shapes a fast kernel cannot take run on a slower one (never an error under AUTO).
+ * Accumulation is fp32.  Q4LIN_ERR_CUDA reports a failed launch
+ * (cudaGetLastError after enqueueing). */
+Q4LIN_API q4lin_status_t q4lin_run(q4lin_handle_t handle, const float* x,
+                                   const uint8_t* qweight, const void* scales,
+                                   const float* bias, float* out, int64_t M, int64_t N,
+                                   int64_t K, int64_t group_size, int scale_dtype,
+                                   void* stream);
+
+/* The path q4lin_run would take for these arguments (no launch, no device access);
+ * *path_out receives a q4lin_path_t other than AUTO.  Same validation and status codes
+ * as q4lin_run.  For M == 0 or N == 0, *path_out is Q4LIN_PATH_AUTO (nothing runs). */
+Q4LIN_API q4lin_status_t q4lin_plan(q4lin_handle_t handle, const float* x,
+                                    const uint8_t* qweight, const void* scales,
+                                    const float* bias, const float* out, int64_t M,
+                                    int64_t N, int64_t K, int64_t group_size,
+                                    int scale_dtype, int* path_out);
+
+/* Set / read one q4lin_option_t.  Q4LIN_ERR_INVALID_ARG for an unknown option or an
+ * out-of-range value. */
+Q4LIN_API q4lin_status_t q4lin_set_option(q4lin_handle_t handle, int option,
+                                          int64_t value);
+Q4LIN_API q4lin_status_t q4lin_get_option(q4lin_handle_t handle, int option,
+                                          int64_t* value);
+
+/* Read and clear the handle's device status word after synchronizing `stream`.
+ * *code_out = 0 if no kernel recorded a problem since the last call; otherwise the
+ * first recorded code (1 = a bounded wait of the tensor-core kernel ran out).
+ * Returns Q4LIN_ERR_TIMEOUT when the code is non-zero, Q4LIN_OK otherwise. */
+Q4LIN_API q4lin_status_t q4lin_check_device_status(q4lin_handle_t handle, void* stream,
+                                                   int* code_out);
+
+/* Static, never-NULL description of a status code. */
+Q4LIN_API const char* q4lin_status_string(q4lin_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* Q4LIN_H */

@@ -39,6 +39,8 @@ def _load():
     if _lib is None:
         lib = ctypes.CDLL(build())
         i64, i32, vp, dp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p
+        lib.q4o_num_threads.argtypes = []
+        lib.q4o_num_threads.restype = ctypes.c_int
         lib.q4o_f16_to_f64.argtypes = [ctypes.c_uint16]
         lib.q4o_f16_to_f64.restype = ctypes.c_double
         lib.q4o_linear.argtypes = [vp, vp, vp, i32, vp, i64, i64, i64, i64, i32, dp, dp]
@@ -77,6 +79,11 @@ def _prep(x, qweight, scales, bias, K):
     if qweight.shape[1] != (K + 1) // 2:
         raise ValueError("qweight must be [N, ceil(K/2)]")
     return x, qweight, scales, bias, M, N
+
+
+def num_threads() -> int:
+    """Threads the oracle's OpenMP loops use."""
+    return int(_load().q4o_num_threads())
 
 
 def f16_to_f64(bits: int) -> float:

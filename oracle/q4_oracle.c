@@ -37,9 +37,21 @@
 #include <math.h>
 #include <stddef.h>
 #include <stdint.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 
 #define Q4O_OK 0
 #define Q4O_BAD_ARG 1
+
+/* Threads an OpenMP loop of this library uses (1 without OpenMP). */
+int q4o_num_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
 
 /* IEEE 754 binary16 -> double, from the bit fields (1 sign, 5 exponent bias 15,
  * 10 fraction bits).  Written here so the oracle needs no half-precision library. */

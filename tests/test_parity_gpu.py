@@ -1,0 +1,262 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 CPU oracle.
+
+Every case is seeded and synthetic (bit_weight_quantized_int4_gb300.synth).  The output
+is NaN-poisoned with 64 guard slots after it; the tolerance per element is
+1e-5 * sum_k|x*w| + 1e-7 on the CUDA-core paths and 4e-3 * sum_k|x*w| + 1e-6 on the
+tensor-core path.  Dyadic inputs and all-8 codes must come out bit-exact on every path.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from bit_weight_quantized_int4_gb300 import synth
+from tests._golden import load_worked_example
+from tests._gpu import TOL_FP32, TOL_TC, assert_parity, run_q4lin
+
+pytestmark = pytest.mark.gpu
+
+GEMV, FFMA, TC, AUTO = 1, 2, 3, 0
+
+
+@pytest.fixture(scope="module")
+def handle():
+    import torch
+    from bit_weight_quantized_int4_gb300 import q4lin as q
+    assert torch.cuda.is_available()
+    h = q.q4lin_create(0)
+    yield h
+    q.q4lin_destroy(h)
+
+
+def tol_for(path):
+    return TOL_TC if path == TC else TOL_FP32
+
+
+def sample_rows(M, max_rows=24):
+    if M <= max_rows:
+        return np.arange(M)
+    step = -(-M // 16)
+    return np.unique(np.concatenate([[0, M - 1], np.arange(0, M, step)]))
+
+
+def check_case(handle, case, path=AUTO, even_high=False, rows=None):
+    out, used = run_q4lin(handle, case, path, even_high)
+    if rows is None:
+        rows = np.arange(case.M)
+    ref, mag = oracle.linear(case.x[rows], case.qweight, case.scales, case.bias, case.K,
+                             case.group_size, even_high=even_high)
+    assert_parity(out[rows], ref, mag, tol_for(used))
+    return out, used
+
+
+# ------------------------------------------------------------------------ worked example
+@pytest.mark.parametrize("path", [AUTO, FFMA])
+@pytest.mark.parametrize("f16", [False, True])
+def test_worked_example_exact(handle, path, f16):
+    ex = load_worked_example()
+    scales = ex["scales"].astype(np.float16 if f16 else np.float32)
+    c = synth.Case(2, 4, 8, 4, ex["x"], ex["qweight"], scales, ex["bias"])
+    out, _ = run_q4lin(handle, c, path)
+    np.testing.assert_array_equal(out.astype(np.float64), ex["out_bias"])
+
+
+# ---------------------------------------------------------------------------- tiny config
+@pytest.mark.parametrize("path", [AUTO, GEMV, FFMA])
+def test_tiny_config(handle, path):
+    c = synth.make_case(4, 128, 256, 32, scale_f16=False, bias=False, seed=0)
+    check_case(handle, c, path)
+
+
+# ----------------------------------------------------------------------- decode shapes
+DECODE_1B = [(2048, 2048), (512, 2048), (8192, 2048), (2048, 8192), (128256, 2048)]
+DECODE_8B = [(4096, 4096), (1024, 4096), (14336, 4096), (4096, 14336), (22016, 4096),
+             (128256, 4096)]
+
+
+@pytest.mark.parametrize("N,K", DECODE_1B + DECODE_8B)
+def test_decode_gemv_shapes(handle, N, K):
+    c = synth.make_case(1, N, K, 32, scale_f16=True, bias=False, seed=1 + N % 97 + K)
+    _, used = check_case(handle, c, AUTO)
+    assert used == GEMV
+
+
+# ------------------------------------------------------------------------ qcs4w edges
+@pytest.mark.parametrize("M", [1, 7, 64])
+def test_qcs4w_vocab_ragged(handle, M):
+    c = synth.make_case(M, 128257, 4096, 4096, scale_f16=False, bias=False, seed=4)
+    check_case(handle, c, AUTO, rows=sample_rows(M, 8))
+
+
+@pytest.mark.parametrize("M", [1, 33])
+def test_qcs4w_k2056(handle, M):
+    c = synth.make_case(M, 1000, 2056, 2056, scale_f16=False, bias=False, seed=4)
+    check_case(handle, c, AUTO)
+
+
+def test_qcs4w_fp16_scales(handle):
+    c = synth.make_case(3, 4097, 1024, 1024, scale_f16=True, bias=True, seed=41)
+    check_case(handle, c, AUTO)
+
+
+# --------------------------------------------------------------------- small M / ragged
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 7, 8, 9, 16])
+@pytest.mark.parametrize("path", [GEMV, FFMA])
+def test_small_m(handle, M, path):
+    c = synth.make_case(M, 300, 512, 32, scale_f16=True, bias=True, seed=M)
+    check_case(handle, c, path)
+
+
+@pytest.mark.parametrize("N", [1, 7, 15, 17, 33, 127, 129, 1000, 4097])
+def test_ragged_n_gemv(handle, N):
+    c = synth.make_case(1, N, 1024, 32, scale_f16=True, bias=True, seed=N)
+    check_case(handle, c, GEMV)
+
+
+@pytest.mark.parametrize("gs", [32, 64, 128, 96, 4096, 100000])
+def test_group_sizes_gemv(handle, gs):
+    K = 4096 if gs != 96 else 1056
+    G = -(-K // gs)
+    c = synth.make_case(2, 257, K, gs, scale_f16=False, bias=True, seed=gs)
+    assert c.scales.shape == (G, 257)
+    check_case(handle, c, GEMV)
+
+
+@pytest.mark.parametrize("K,gs", [(77, 8), (33, 33), (250, 1), (1000, 24), (2056, 8),
+                                  (96, 64), (1, 1)])
+def test_generic_shapes(handle, K, gs):
+    c = synth.make_case(3, 45, K, gs, scale_f16=K % 2 == 0, bias=True, seed=K)
+    _, used = check_case(handle, c, AUTO)
+    if K % 32:
+        assert used == FFMA
+
+
+# --------------------------------------------------------------------------- options
+@pytest.mark.parametrize("path", [GEMV, FFMA])
+def test_nibble_even_high(handle, path):
+    c = synth.make_case(3, 130, 512, 64, scale_f16=True, bias=True, seed=21)
+    check_case(handle, c, path, even_high=True)
+
+
+# ------------------------------------------------------------------------ exactness
+@pytest.mark.parametrize("path", [GEMV, FFMA, AUTO])
+@pytest.mark.parametrize("M", [1, 3, 6])
+def test_dyadic_bit_exact(handle, path, M):
+    c = synth.make_dyadic_case(M, 200, 1024, 32, scale_f16=(M % 2 == 1), bias=True, seed=M)
+    out, _ = run_q4lin(handle, c, path)
+    ref, _ = oracle.linear(c.x, c.qweight, c.scales, c.bias, c.K, c.group_size)
+    np.testing.assert_array_equal(out.astype(np.float64), ref)
+
+
+@pytest.mark.parametrize("path", [GEMV, FFMA, AUTO])
+def test_all_codes_eight_gives_bias(handle, path):
+    c = synth.make_case(2, 333, 2048, 32, scale_f16=True, bias=True, seed=9)
+    c.qweight = synth.fill_codes(333, 2048, 8)
+    out, _ = run_q4lin(handle, c, path)
+    np.testing.assert_array_equal(out, np.broadcast_to(c.bias, out.shape))
+
+
+def test_repeat_calls_identical(handle):
+    c = synth.make_case(1, 5000, 2048, 32, scale_f16=True, bias=True, seed=31)
+    a, _ = run_q4lin(handle, c, AUTO)
+    b, _ = run_q4lin(handle, c, AUTO)
+    np.testing.assert_array_equal(a, b)
+
+
+# ------------------------------------------------------------------- host-side checks
+def test_empty_problems_launch_nothing(handle):
+    import torch
+    from bit_weight_quantized_int4_gb300 import q4lin as q
+    out = torch.full((16,), 7.0, device="cuda")
+    x = torch.zeros(64, device="cuda")
+    w = torch.zeros(64, dtype=torch.uint8, device="cuda")
+    s = torch.zeros(64, device="cuda")
+    for M, N in [(0, 4), (4, 0), (0, 0)]:
+        st = q.q4lin_run(handle, x.data_ptr(), w.data_ptr(), s.data_ptr(), None,
+                         out.data_ptr(), M, N, 32, 32, 0, None)
+        assert st == q.Q4LIN_OK
+    torch.cuda.synchronize()
+    assert torch.all(out == 7.0)
+
+
+def test_invalid_arguments(handle):
+    import torch
+    from bit_weight_quantized_int4_gb300 import q4lin as q
+    x = torch.zeros(4 * 64, device="cuda")
+    w = torch.zeros(8 * 32, dtype=torch.uint8, device="cuda")
+    s = torch.zeros(2 * 8, device="cuda")
+    out = torch.zeros(4 * 8, device="cuda")
+    P = lambda t: t.data_ptr()
+    run = lambda *a: q.q4lin_run(handle, *a)
+    ok = (P(x), P(w), P(s), None, P(out), 4, 8, 64, 32, 0, None)
+    assert run(*ok) == q.Q4LIN_OK
+    bad = [
+        (P(x), P(w), P(s), None, P(out), 4, 8, 0, 32, 0, None),        # K == 0
+        (P(x), P(w), P(s), None, P(out), -1, 8, 64, 32, 0, None),      # M < 0
+        (P(x), P(w), P(s), None, P(out), 4, 8, 64, 0, 0, None),        # group_size 0
+        (P(x), P(w), P(s), None, P(out), 4, 8, 64, 32, 2, None),       # scale dtype
+        (None, P(w), P(s), None, P(out), 4, 8, 64, 32, 0, None),       # NULL x
+        (P(x), P(w), P(s), None, P(x), 4, 8, 64, 32, 0, None),         # out aliases x
+        (P(x), P(w), P(s), None, P(out) + 2, 4, 8, 64, 32, 0, None),   # misaligned out
+        (P(x), P(w), P(s) + 2, None, P(out), 4, 8, 64, 32, 0, None),   # misaligned f32 scales
+    ]
+    for args in bad:
+        assert run(*args) == q.Q4LIN_ERR_INVALID_ARG, args
+    assert q.q4lin_set_option(handle, q.Q4LIN_OPT_FORCE_PATH, 9) == q.Q4LIN_ERR_INVALID_ARG
+    assert q.q4lin_set_option(handle, 77, 0) == q.Q4LIN_ERR_INVALID_ARG
+
+
+def test_unaligned_x_falls_back(handle):
+    """x that is 4- but not 16-byte aligned: GEMV is ineligible, AUTO still correct."""
+    import torch
+    from bit_weight_quantized_int4_gb300 import q4lin as q
+    c = synth.make_case(2, 100, 256, 32, scale_f16=True, bias=False, seed=5)
+    big = torch.zeros(2 * 256 + 1, device="cuda")
+    big[1:] = torch.from_numpy(c.x.ravel()).cuda()
+    x_view = big[1:]
+    out, used = run_q4lin(handle, c, AUTO, x_dev=x_view)
+    assert used == FFMA
+    ref, mag = oracle.linear(c.x, c.qweight, c.scales, None, 256, 32)
+    assert_parity(out, ref, mag, TOL_FP32)
+    q.q4lin_set_option(handle, q.Q4LIN_OPT_FORCE_PATH, GEMV)
+    w = torch.from_numpy(c.qweight).cuda()
+    s = torch.from_numpy(c.scales).cuda()
+    o = torch.empty(200, device="cuda")
+    st = q.q4lin_run(handle, x_view.data_ptr(), w.data_ptr(), s.data_ptr(), None,
+                     o.data_ptr(), 2, 100, 256, 32, 1, None)
+    q.q4lin_set_option(handle, q.Q4LIN_OPT_FORCE_PATH, AUTO)
+    assert st == q.Q4LIN_ERR_UNSUPPORTED
+
+
+def test_side_stream(handle):
+    import torch
+    from bit_weight_quantized_int4_gb300 import q4lin as q
+    c = synth.make_case(1, 2048, 2048, 32, scale_f16=True, bias=True, seed=6)
+    x, w, s, b = (torch.from_numpy(a).cuda() for a in (c.x, c.qweight, c.scales, c.bias))
+    out = torch.full((1, 2048), float("nan"), device="cuda")
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    st = q.q4lin_run(handle, x.data_ptr(), w.data_ptr(), s.data_ptr(), b.data_ptr(),
+                     out.data_ptr(), 1, 2048, 2048, 32, 1, side.cuda_stream)
+    assert st == q.Q4LIN_OK
+    side.synchronize()
+    ref, mag = oracle.linear(c.x, c.qweight, c.scales, c.bias, 2048, 32)
+    assert_parity(out.cpu().numpy(), ref, mag, TOL_FP32)
+
+
+# -------------------------------------------------------------------- prefill shapes
+PREFILL_NK = [(2048, 2048), (512, 2048), (8192, 2048), (2048, 8192)]
+
+
+@pytest.mark.parametrize("M", [128, 512, 2048])
+@pytest.mark.parametrize("N,K", PREFILL_NK)
+def test_prefill_shapes(handle, M, N, K):
+    c = synth.make_case(M, N, K, 32, scale_f16=False, bias=(N != 512), seed=3)
+    check_case(handle, c, AUTO, rows=sample_rows(M))
+
+
+@pytest.mark.parametrize("M,K,N,gs", [(96, 2048, 256, 32), (70, 1024, 136, 32),
+                                      (96, 2048, 256, 64), (96, 2048, 256, 8),
+                                      (128, 8192, 2048, 32)])
+def test_extra_page_shapes(handle, M, K, N, gs):
+    c = synth.make_case(M, N, K, gs, scale_f16=False, bias=True, seed=12)
+    check_case(handle, c, AUTO, rows=sample_rows(M))
