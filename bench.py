@@ -400,6 +400,29 @@ def load_peaks():
     return 6800.0, 1900.0, "fallback"
 
 
+def profile(spec):
+    """A handful of launches of one op, nothing printed: a target for ncu."""
+    import torch
+    from bit_weight_quantized_int4_gb300 import q4lin as q
+    h = q.q4lin_create(0)
+    kind, *dims = spec.split(":")
+    if kind == "token":
+        token = DecodeToken(h, dims[0], "cuda")
+        for _ in range(3):
+            token.run(torch.cuda.current_stream().cuda_stream)
+    elif kind == "gemv":
+        N, K = int(dims[0]), int(dims[1])
+        shape_bandwidth(torch, h, N, K, reps=3)
+    elif kind == "prefill":
+        M, N, K = (int(d) for d in dims)
+        prefill_tflops(torch, h, M, N, K, reps=3)
+    else:
+        raise SystemExit(f"unknown profile spec {spec}")
+    torch.cuda.synchronize()
+    q.q4lin_destroy(h)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -408,7 +431,15 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true")
+    ap.add_argument("--pdl", type=int, default=1, choices=[0, 1],
+                    help="launch with programmatic dependent launch (kernels start "
+                         "streaming weights while the previous one drains)")
+    ap.add_argument("--profile", default=None,
+                    help="run a few launches of one op and exit (for ncu): gemv:N:K, "
+                         "prefill:M:N:K or token:1b|8b")
     args = ap.parse_args()
+    if args.profile:
+        return profile(args.profile)
     world, rank, local = dist_setup(args)
     if args.impl == "reference":
         return run_reference(args, world, rank)
@@ -417,6 +448,7 @@ def main():
     torch.cuda.set_device(local)
     from bit_weight_quantized_int4_gb300 import q4lin as q
     h = q.q4lin_create(local)
+    q.q4lin_set_option(h, q.Q4LIN_OPT_PDL, args.pdl)
 
     token = DecodeToken(h, "1b", "cuda")
     graph = token.capture()
@@ -456,7 +488,7 @@ def main():
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max, 4),
         "ms_per_token": round(ms_max, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": workload_config("1b"),
+        "config": dict(workload_config("1b"), pdl=bool(args.pdl)),
         "roofline": {"bound": "hbm", "achieved": round(per_gpu_gbs, 1), "peak": hbm_peak,
                      "unit": "GB/s", "frac": round(per_gpu_gbs / hbm_peak, 4),
                      "traffic": None,

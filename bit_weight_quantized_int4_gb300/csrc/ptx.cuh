@@ -1,0 +1,147 @@
+// ptx.cuh -- inline-PTX building blocks shared by the sm_103a kernels of this library:
+// mbarriers with time-bounded waits, TMA tensor copies, tcgen05 (tensor memory and MMA),
+// programmatic dependent launch, packed fp32x2 arithmetic and the 4-bit code widening.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+namespace q4lin {
+namespace ptx {
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ uint64_t global_timer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// ------------------------------------------------------------------------- mbarrier
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_init_fence() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Wait for the phase of `bar` with the given parity, for at most limit_ns of global time
+// and, when `failed` is given, only while no thread of the CTA has recorded a failure.
+__device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, int64_t limit_ns,
+                                          const volatile int* failed) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (failed && *failed) return false;
+        if ((int64_t)(global_timer() - t0) > limit_ns) return false;
+    }
+}
+__device__ __forceinline__ void record_failure(int* status, volatile int* failed) {
+    atomicCAS(status, 0, 1);
+    *failed = 1;
+}
+
+// ----------------------------------------------------------------------------- TMA
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ----------------------------------------------------------- programmatic dependent launch
+// Wait until the preceding grid on the stream has completed and its writes are visible
+// (a no-op when the kernel was launched without programmatic stream serialization).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Allow the next grid on the stream to begin launching.
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ------------------------------------------------------------------------- loads
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr));
+    return v;
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, float a, float b, float c, float d) {
+    asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "f"(a), "f"(b), "f"(c),
+                 "f"(d)
+                 : "memory");
+}
+
+// --------------------------------------------------------------- packed fp32x2 math
+__device__ __forceinline__ unsigned long long as_u64(float2 a) {
+    return *reinterpret_cast<unsigned long long*>(&a);
+}
+__device__ __forceinline__ float2 as_f2(unsigned long long a) { return *reinterpret_cast<float2*>(&a); }
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+    unsigned long long d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(as_u64(a)), "l"(as_u64(b)), "l"(as_u64(c)));
+    return as_f2(d);
+}
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+    unsigned long long d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(as_u64(a)), "l"(as_u64(b)));
+    return as_f2(d);
+}
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+    unsigned long long d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(as_u64(a)), "l"(as_u64(b)));
+    return as_f2(d);
+}
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
+// ------------------------------------------------------------- 4-bit code widening
+// The signed codes (c - 8) of one packed 32-bit word as exact fp32 pairs, in k order:
+// pair b holds (k = 2b, k = 2b + 1).  Byte b of the word holds k = 2b in its low nibble
+// and k = 2b + 1 in its high nibble (swapped when even_high).  A byte permute builds the
+// float 2^23 + c (bit pattern 0x4B0000cc); one packed add of -(2^23 + 8) then gives c - 8
+// exactly for both lanes of the pair.
+template <bool EH>
+__device__ __forceinline__ void codes_word(uint32_t w, float2 (&v)[4]) {
+    const uint32_t m = w & 0x0F0F0F0Fu, s = (w >> 4) & 0x0F0F0F0Fu;
+    const uint32_t lo = EH ? s : m, hi = EH ? m : s;
+    const float2 bias = make_float2(-8388616.0f, -8388616.0f);
+#pragma unroll
+    for (int b = 0; b < 4; ++b)
+        v[b] = fadd2(make_float2(__uint_as_float(prmt(lo, 0x4B000000u, 0x7440u | b)),
+                                 __uint_as_float(prmt(hi, 0x4B000000u, 0x7440u | b))),
+                     bias);
+}
+
+}  // namespace ptx
+}  // namespace q4lin

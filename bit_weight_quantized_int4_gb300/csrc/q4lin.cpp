@@ -24,13 +24,14 @@ struct q4lin_handle {
     int force_path = Q4LIN_PATH_AUTO;
     int even_high = 0;
     int pdl = 0;
-    int64_t wait_limit = 0;  // 0: default
+    int64_t wait_limit = 0;  // ns; 0: default
+    int tc_skip_first_copy = 0;
     int* d_status = nullptr;
 };
 
 namespace {
 
-constexpr int64_t kDefaultWaitLimit = 1LL << 26;  // mbarrier polls before giving up
+constexpr int64_t kDefaultWaitLimit = 2000000000LL;  // 2 s of GPU global time
 
 // Crossover: at and above this M the tensor-core GEMM replaces the row-streaming
 // CUDA-core kernel (when both are eligible).  Measured on GB300; see plan().
@@ -113,7 +114,8 @@ q4lin::LaunchCtx make_ctx(q4lin_handle_t h, cudaStream_t stream) {
     c.max_smem_optin = h->max_smem_optin;
     c.pdl = h->pdl;
     c.status_word = h->d_status;
-    c.wait_limit = h->wait_limit > 0 ? h->wait_limit : kDefaultWaitLimit;
+    c.wait_limit_ns = h->wait_limit > 0 ? h->wait_limit : kDefaultWaitLimit;
+    c.tc_skip_first_copy = h->tc_skip_first_copy;
     return c;
 }
 
@@ -229,7 +231,10 @@ q4lin_status_t q4lin_run(q4lin_handle_t h, const float* x, const uint8_t* qweigh
     cudaError_t err;
     switch (path) {
         case Q4LIN_PATH_TC: err = q4lin::tc_launch(p, c); break;
-        case Q4LIN_PATH_GEMV: err = q4lin::rowstream_launch(p, c); break;
+        case Q4LIN_PATH_GEMV:
+            err = q4lin::gemv_tma_eligible(p) ? q4lin::gemv_tma_launch(p, c)
+                                              : q4lin::rowstream_launch(p, c);
+            break;
         default: err = q4lin::generic_launch(p, c); break;
     }
     if (err == cudaSuccess) err = cudaGetLastError();
@@ -254,6 +259,10 @@ q4lin_status_t q4lin_set_option(q4lin_handle_t h, int option, int64_t value) {
             if (value != 0 && value != 1) return Q4LIN_ERR_INVALID_ARG;
             h->pdl = (int)value;
             return Q4LIN_OK;
+        case Q4LIN_OPT_TC_SKIP_FIRST_COPY:
+            if (value != 0 && value != 1) return Q4LIN_ERR_INVALID_ARG;
+            h->tc_skip_first_copy = (int)value;
+            return Q4LIN_OK;
         default:
             return Q4LIN_ERR_INVALID_ARG;
     }
@@ -268,6 +277,7 @@ q4lin_status_t q4lin_get_option(q4lin_handle_t h, int option, int64_t* value) {
             *value = h->wait_limit > 0 ? h->wait_limit : kDefaultWaitLimit;
             return Q4LIN_OK;
         case Q4LIN_OPT_PDL: *value = h->pdl; return Q4LIN_OK;
+        case Q4LIN_OPT_TC_SKIP_FIRST_COPY: *value = h->tc_skip_first_copy; return Q4LIN_OK;
         default: return Q4LIN_ERR_INVALID_ARG;
     }
 }

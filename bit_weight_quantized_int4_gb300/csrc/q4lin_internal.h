@@ -26,7 +26,8 @@ struct LaunchCtx {
     int max_smem_optin;      // bytes of opt-in shared memory per block
     int pdl;                 // launch with programmatic stream serialization
     int* status_word;        // device int, first nonzero code a kernel records
-    int64_t wait_limit;      // iteration limit of bounded device-side waits
+    int64_t wait_limit_ns;   // time limit of bounded device-side waits
+    int tc_skip_first_copy;  // test hook: the TC producer skips stage 0
 };
 
 // Row-streaming CUDA-core kernel (decode GEMV, and small M with weight reuse across a
@@ -34,6 +35,12 @@ struct LaunchCtx {
 // and group_size % 32 == 0 or group_size >= K.
 bool rowstream_eligible(const Problem& p);
 cudaError_t rowstream_launch(const Problem& p, const LaunchCtx& c);
+
+// TMA-fed decode GEMV (M = 1): persistent CTAs, a producer warp streams weight tiles
+// into a shared-memory ring.  Needs K % 32 == 0, K >= 512, N >= 16, 16-byte aligned x and
+// qweight, and group_size % 32 == 0 or group_size >= K.
+bool gemv_tma_eligible(const Problem& p);
+cudaError_t gemv_tma_launch(const Problem& p, const LaunchCtx& c);
 
 // Generic CUDA-core kernel: any K (odd included), any group size, any alignment.
 cudaError_t generic_launch(const Problem& p, const LaunchCtx& c);

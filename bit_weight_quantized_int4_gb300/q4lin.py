@@ -42,6 +42,7 @@ Q4LIN_OPT_FORCE_PATH = 1
 Q4LIN_OPT_NIBBLE_EVEN_HIGH = 2
 Q4LIN_OPT_WAIT_LIMIT = 3
 Q4LIN_OPT_PDL = 4
+Q4LIN_OPT_TC_SKIP_FIRST_COPY = 5
 
 _vp, _i64, _i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
 

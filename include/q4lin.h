@@ -73,13 +73,20 @@ typedef enum {
      * 1: the high nibble holds k = 2j (the qcs4w AOT packer's "(even << 4) | odd"
      * order, "Add linear_qcs4w op", Constraints (2)). */
     Q4LIN_OPT_NIBBLE_EVEN_HIGH = 2,
-    /* Iteration limit of every bounded device-side wait (mbarrier polls) in the
-     * tensor-core kernel; <= 0 restores the default.  After the limit the kernel records
-     * a code in the handle's status word and returns without computing. */
+    /* Time limit, in nanoseconds of the GPU's global timer, of every bounded
+     * device-side wait (mbarrier polls) of the tensor-core kernel; <= 0 restores the
+     * default (2 s).  When a wait runs out the kernel records code 1 in the handle's
+     * status word, stops issuing work, lets its own copies and MMAs in flight finish,
+     * frees its tensor memory and returns; its output is then undefined. */
     Q4LIN_OPT_WAIT_LIMIT = 3,
     /* 1: launch with programmatic dependent launch, so a kernel may start streaming
-     * its weights while the previous kernel on the stream drains (default 0). */
-    Q4LIN_OPT_PDL = 4
+     * its weights while the previous kernel on the stream drains (default 0).  The
+     * preceding kernel must not write this call's qweight or scales. */
+    Q4LIN_OPT_PDL = 4,
+    /* Test hook, default 0.  1: the tensor-core kernel's copy engine skips the first
+     * pipeline stage, so the barrier its consumers wait on is never completed and their
+     * bounded waits run out (exercises the timeout path without faulting the GPU). */
+    Q4LIN_OPT_TC_SKIP_FIRST_COPY = 5
 } q4lin_option_t;
 
 /* Create a handle for CUDA device `device`.  Queries the SM count and shared-memory
@@ -134,6 +141,7 @@ Q4LIN_API q4lin_status_t q4lin_get_option(q4lin_handle_t handle, int option,
 /* Read and clear the handle's device status word after synchronizing `stream`.
  * *code_out = 0 if no kernel recorded a problem since the last call; otherwise the
  * first recorded code (1 = a bounded wait of the tensor-core kernel ran out).
+ * The word is shared by every call on the handle.
  * Returns Q4LIN_ERR_TIMEOUT when the code is non-zero, Q4LIN_OK otherwise. */
 Q4LIN_API q4lin_status_t q4lin_check_device_status(q4lin_handle_t handle, void* stream,
                                                    int* code_out);

@@ -260,3 +260,112 @@ def test_prefill_shapes(handle, M, N, K):
 def test_extra_page_shapes(handle, M, K, N, gs):
     c = synth.make_case(M, N, K, gs, scale_f16=False, bias=True, seed=12)
     check_case(handle, c, AUTO, rows=sample_rows(M))
+
+
+# ------------------------------------------------------------------- tensor-core path
+TC_SHAPES = [
+    # (M, N, K, gs, f16, bias)
+    (4, 128, 256, 32, False, False),      # the tiny config
+    (1, 300, 512, 32, True, True),        # M = 1 through the tensor cores (bm = 16)
+    (17, 129, 96, 32, False, True),       # 3 k-stages (< pipeline depth), ragged M and N
+    (70, 136, 1024, 32, False, True),     # the pages' partial-M / partial-N edge shape
+    (96, 256, 2048, 64, True, False),
+    (256, 384, 512, 128, False, True),
+    (257, 200, 1024, 32, False, True),    # two M tiles
+    (600, 1000, 768, 32, True, True),     # three M tiles, ragged everything
+    (33, 1000, 4096, 4096, False, False), # per-channel
+    (64, 128257, 4096, 4096, False, False),
+]
+
+
+@pytest.mark.parametrize("M,N,K,gs,f16,bias", TC_SHAPES)
+def test_tc_parity(handle, M, N, K, gs, f16, bias):
+    c = synth.make_case(M, N, K, gs, scale_f16=f16, bias=bias, seed=M + N)
+    _, used = check_case(handle, c, TC, rows=sample_rows(M))
+    assert used == TC
+
+
+@pytest.mark.parametrize("M", [1, 5, 48, 300])
+def test_tc_dyadic_bit_exact(handle, M):
+    c = synth.make_dyadic_case(M, 260, 1024, 32, scale_f16=(M % 2 == 1), bias=True, seed=M)
+    out, used = run_q4lin(handle, c, TC)
+    assert used == TC
+    ref, _ = oracle.linear(c.x, c.qweight, c.scales, c.bias, c.K, c.group_size)
+    np.testing.assert_array_equal(out.astype(np.float64), ref)
+
+
+def test_tc_all_codes_eight_gives_bias(handle):
+    c = synth.make_case(40, 333, 2048, 32, scale_f16=True, bias=True, seed=9)
+    c.qweight = synth.fill_codes(333, 2048, 8)
+    out, _ = run_q4lin(handle, c, TC)
+    np.testing.assert_array_equal(out, np.broadcast_to(c.bias, out.shape))
+
+
+def test_tc_nibble_even_high(handle):
+    c = synth.make_case(20, 130, 512, 64, scale_f16=True, bias=True, seed=21)
+    check_case(handle, c, TC, even_high=True)
+
+
+def test_tc_bounded_wait_times_out_cleanly(handle):
+    """The producer skips its first copy (test hook), so the barrier the consumers wait
+    on is never completed: their 1 ms bounded waits run out, the kernel records code 1
+    and returns; the context stays usable and the next call is correct."""
+    import torch
+    from bit_weight_quantized_int4_gb300 import q4lin as q
+    c = synth.make_case(8, 256, 512, 32, scale_f16=False, bias=False, seed=77)
+    st, code = q.q4lin_check_device_status(handle, None)
+    assert (st, code) == (q.Q4LIN_OK, 0)
+    q.q4lin_set_option(handle, q.Q4LIN_OPT_WAIT_LIMIT, 1_000_000)
+    q.q4lin_set_option(handle, q.Q4LIN_OPT_TC_SKIP_FIRST_COPY, 1)
+    try:
+        run_q4lin(handle, c, TC)
+    except AssertionError:
+        pass  # the output of a timed-out call is undefined (NaN-poisoned here)
+    finally:
+        q.q4lin_set_option(handle, q.Q4LIN_OPT_TC_SKIP_FIRST_COPY, 0)
+        q.q4lin_set_option(handle, q.Q4LIN_OPT_WAIT_LIMIT, 0)
+    st, code = q.q4lin_check_device_status(handle, None)
+    assert st == q.Q4LIN_ERR_TIMEOUT and code == 1
+    st, code = q.q4lin_check_device_status(handle, None)
+    assert (st, code) == (q.Q4LIN_OK, 0)
+    torch.cuda.synchronize()
+    check_case(handle, c, TC)
+
+
+# ----------------------------------------------------- programmatic dependent launch
+@pytest.mark.parametrize("pdl", [0, 1])
+def test_dependent_chain(handle, pdl):
+    """GEMVs chained on one stream, each reading the previous output as its x, with every
+    buffer NaN-poisoned first.  With programmatic dependent launch a kernel starts
+    streaming weights early but must read x only after its predecessor completed; each
+    link is checked against the oracle applied to the input it actually received."""
+    import torch
+    from bit_weight_quantized_int4_gb300 import q4lin as q
+    dims = [2048, 4096, 1024, 2048, 8192, 2048]
+    links = []
+    for i in range(len(dims) - 1):
+        K, N = dims[i], dims[i + 1]
+        c = synth.make_case(1, N, K, 32, scale_f16=True, bias=(i % 2 == 0), seed=900 + i)
+        links.append(c)
+    bufs = [torch.from_numpy(links[0].x.ravel()).cuda()]
+    bufs += [torch.full((d,), float("nan"), device="cuda") for d in dims[1:]]
+    dev = [tuple(None if a is None else torch.from_numpy(a).cuda()
+                 for a in (c.qweight, c.scales, c.bias)) for c in links]
+    torch.cuda.synchronize()
+    q.q4lin_set_option(handle, q.Q4LIN_OPT_PDL, pdl)
+    try:
+        stream = torch.cuda.current_stream().cuda_stream
+        for i, c in enumerate(links):
+            w, s, b = dev[i]
+            st = q.q4lin_run(handle, bufs[i].data_ptr(), w.data_ptr(), s.data_ptr(),
+                             None if b is None else b.data_ptr(), bufs[i + 1].data_ptr(),
+                             1, c.N, c.K, 32, q.Q4LIN_SCALE_F16, stream)
+            assert st == q.Q4LIN_OK
+        torch.cuda.synchronize()
+    finally:
+        q.q4lin_set_option(handle, q.Q4LIN_OPT_PDL, 0)
+    host = [b.cpu().numpy() for b in bufs]
+    for i, c in enumerate(links):
+        assert not np.isnan(host[i + 1]).any(), f"link {i} output has NaN"
+        ref, mag = oracle.linear(host[i][None, :], c.qweight, c.scales, c.bias, c.K, 32)
+        assert_parity(host[i + 1][None, :], ref, mag, TOL_FP32)
