@@ -18,7 +18,7 @@
 //     32 codes of chunk j of each of its V = rb/32 rows and dots them with the x chunk
 //     (read once per tile from shared memory, where x is staged in padded 32-float chunks,
 //     and reused across the V rows), scaling each 32-value chunk by its group scale; the
-//     scales are fetched two tiles ahead.  A warp reads 512 contiguous bytes of the tile
+//     scales are fetched three tiles ahead.  A warp reads 512 contiguous bytes of the tile
 //     per load (conflict-free).  Partial sums stay in registers across the whole row; the
 //     16 chunk lanes of a row group are reduced with shuffles once per row block.
 // The CTAs are persistent and walk row blocks; the pipeline runs across block boundaries.
@@ -42,18 +42,35 @@ constexpr int kThreadsG = kCThreads + 32;  // + the producer warp
 constexpr int kSliceBytes = 256;           // packed bytes per row per tile
 constexpr int kSliceK = 512;
 constexpr int kStagesG = 4;
-constexpr int kPrefetch = 2;               // tiles of scales loaded ahead
+constexpr int kScaleRing = 4;              // tiles of scales in flight per thread
 constexpr int kXPad = 36;                  // floats per 32-float x chunk in shared memory
 constexpr int64_t kDrainNs = 4000000000LL;
 constexpr int kMaxSmemG = 227 * 1024;
+constexpr int kMaxMats = 4;
 
-struct GArgs {
-    const float* x;
+// One weight matrix of a launch.  Several matrices that share x (the q/k/v projections
+// of a layer, or gate/up) run in one launch over a virtual row space: matrix i owns the
+// row blocks [blk_begin, blk_begin + row_blocks).
+struct MatArgs {
     const void* scales;
     const float* bias;
     float* out;
-    int64_t N, K, gs;
-    int scale_f16, per_channel, svec, kslices, x_chunks;
+    int64_t N;
+    int64_t blk_begin;
+};
+struct TensorMaps {
+    CUtensorMap m[kMaxMats];
+};
+
+struct GArgs {
+    const float* x;
+    MatArgs mat[kMaxMats];
+    int nmat;
+    int64_t K, gs;
+    int scale_f16, per_channel, kslices, x_chunks;
+    int k_chunks;   // K / 32
+    int gs_chunks;  // group size / 32 (grouped scales)
+    int gs_shift;   // log2(gs_chunks) when a power of two, else -1
     int64_t row_blocks;
     int* status;
     int64_t wait_ns;
@@ -71,42 +88,37 @@ __device__ __forceinline__ float load_scale(const void* scales, int f16, int64_t
     return __ldg(reinterpret_cast<const float*>(scales) + idx);
 }
 
-// s[v] = scale[g, n0 + v] (0 past N or when !valid).
+// Raw bits of scale[g, n0 + v] (binary16 in the low half, or fp32), 0 past N or when
+// !valid.  Kept raw in the prefetch ring and converted only when used: converting at
+// load time would make the thread wait for the load right away.
 template <int V>
-__device__ __forceinline__ void load_scales(const GArgs& a, int64_t g, int64_t n0, bool valid,
-                                            float (&s)[V]) {
-    const int64_t base = g * a.N + n0;
-    if (valid && a.svec && n0 + V <= a.N) {
-        if (a.scale_f16) {
-            const __half* p = reinterpret_cast<const __half*>(a.scales) + base;
-            if constexpr (V == 4) {
-                const uint2 u = __ldg(reinterpret_cast<const uint2*>(p));
-                const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
-                const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
-                s[0] = f0.x; s[1] = f0.y; s[2] = f1.x; s[3] = f1.y;
-            } else if constexpr (V == 2) {
-                const float2 f = __half22float2(__ldg(reinterpret_cast<const __half2*>(p)));
-                s[0] = f.x; s[1] = f.y;
-            } else {
-                s[0] = __half2float(__ldg(p));
-            }
-        } else {
-            const float* p = reinterpret_cast<const float*>(a.scales) + base;
-            if constexpr (V == 4) {
-                const float4 f = __ldg(reinterpret_cast<const float4*>(p));
-                s[0] = f.x; s[1] = f.y; s[2] = f.z; s[3] = f.w;
-            } else if constexpr (V == 2) {
-                const float2 f = __ldg(reinterpret_cast<const float2*>(p));
-                s[0] = f.x; s[1] = f.y;
-            } else {
-                s[0] = __ldg(p);
-            }
-        }
-    } else {
+__device__ __forceinline__ void load_scale_bits(const MatArgs& m, int f16, int64_t g, int64_t n0,
+                                                bool valid, uint32_t (&r)[V]) {
+    const int64_t base = g * m.N + n0;
 #pragma unroll
-        for (int v = 0; v < V; ++v)
-            s[v] = (valid && n0 + v < a.N) ? load_scale(a.scales, a.scale_f16, base + v) : 0.f;
+    for (int v = 0; v < V; ++v) {
+        uint32_t bits = 0;
+        if (valid && n0 + v < m.N) {
+            if (f16)
+                bits = __ldg(reinterpret_cast<const unsigned short*>(m.scales) + base + v);
+            else
+                bits = __ldg(reinterpret_cast<const unsigned int*>(m.scales) + base + v);
+        }
+        r[v] = bits;
     }
+}
+
+// Matrix that owns global row block blk (blk_begin ascending, matrix 0 begins at 0).
+__device__ __forceinline__ int mat_of(const GArgs& a, int64_t blk) {
+    int i = 0;
+#pragma unroll
+    for (int q = 1; q < kMaxMats; ++q)
+        if (q < a.nmat && blk >= a.mat[q].blk_begin) i = q;
+    return i;
+}
+
+__device__ __forceinline__ float scale_from_bits(uint32_t bits, int f16) {
+    return f16 ? __half2float(__ushort_as_half((unsigned short)bits)) : __uint_as_float(bits);
 }
 
 // sum over the 32 values of one 16-byte chunk of x[t] * (code_t - 8).
@@ -130,7 +142,7 @@ __device__ __forceinline__ float chunk_dot(const uint4& wv, const float4 (&xv)[8
 
 template <int V, bool EH>
 __global__ void __launch_bounds__(kThreadsG, 1)
-    gemv_tma_kernel(const __grid_constant__ CUtensorMap tmap_w, const GArgs a) {
+    gemv_tma_kernel(const __grid_constant__ TensorMaps tmaps, const GArgs a) {
     constexpr int rb = 32 * V;  // rows per block: 32 row groups of V rows
     constexpr uint32_t tile_bytes = rb * kSliceBytes;
     extern __shared__ uint8_t smem_raw[];
@@ -159,12 +171,12 @@ __global__ void __launch_bounds__(kThreadsG, 1)
     if (warp == kCWarps) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
-            prefetch_tensormap(&tmap_w);
-            int64_t t = 0;
+            for (int q = 0; q < a.nmat; ++q) prefetch_tensormap(&tmaps.m[q]);
+            int t = 0;
             bool stop = false;
             for (int64_t blk = blockIdx.x; blk < a.row_blocks && !stop; blk += gridDim.x) {
                 for (int ks = 0; ks < a.kslices; ++ks) {
-                    const int s = (int)(t % kStagesG);
+                    const int s = t & (kStagesG - 1);
                     if (t >= kStagesG &&
                         !wait_bounded(empty(s), (uint32_t)((t / kStagesG) - 1) & 1, a.wait_ns,
                                       failed)) {
@@ -176,15 +188,16 @@ __global__ void __launch_bounds__(kThreadsG, 1)
                         stop = true;
                         break;
                     }
+                    const int mi = mat_of(a, blk);
                     mbar_arrive_expect_tx(full(s), tile_bytes);
-                    tma_load_2d(base + s * tile_bytes, &tmap_w, ks * kSliceBytes, (int)(blk * rb),
-                                full(s));
+                    tma_load_2d(base + s * tile_bytes, &tmaps.m[mi], ks * kSliceBytes,
+                                (int)((blk - a.mat[mi].blk_begin) * rb), full(s));
                     ++t;
                 }
             }
             // The last armed tiles may still be landing; the CTA must not exit first.
-            for (int64_t j = t > kStagesG ? t - kStagesG : 0; j < t; ++j)
-                wait_bounded(full((int)(j % kStagesG)), (uint32_t)(j / kStagesG) & 1, kDrainNs,
+            for (int j = t > kStagesG ? t - kStagesG : 0; j < t; ++j)
+                wait_bounded(full(j & (kStagesG - 1)), (uint32_t)(j / kStagesG) & 1, kDrainNs,
                              nullptr);
         }
         return;
@@ -194,23 +207,34 @@ __global__ void __launch_bounds__(kThreadsG, 1)
     const int j = threadIdx.x & 15;          // chunk lane within a 256-byte slice
     const int r0 = (threadIdx.x >> 4) * V;   // first of this thread's V rows in a block
 
-    // Scales of this thread's tiles, kPrefetch tiles ahead of use (they do not depend
-    // on the preceding kernel, so the first ones are requested before griddep_wait).
-    float sc[kPrefetch + 1][V];
+    // Scales of this thread's tiles, kScaleRing - 1 tiles ahead of use.  Tile t uses
+    // ring slot t % kScaleRing and refills it for tile t + kScaleRing right after; the
+    // tile loop is unrolled by the ring size so every slot has a fixed register (moving
+    // a register whose load is in flight would wait for the load).  The first loads go
+    // out before griddep_wait: scales do not depend on the preceding kernel.  Tile
+    // coordinates advance incrementally (no integer division in the loop).
+    const int tiles_mine =
+        (int)((a.row_blocks - blockIdx.x + gridDim.x - 1) / gridDim.x) * a.kslices;
+    int pf_ks = 0, pf_t = 0;
     int64_t pf_blk = blockIdx.x;
-    int pf_ks = 0;
-    auto fetch = [&](float (&dst)[V]) {
-        if (pf_blk < a.row_blocks && !a.per_channel) {
-            const int64_t k0 = (int64_t)pf_ks * kSliceK + j * 32;
-            load_scales<V>(a, k0 < a.K ? k0 / a.gs : 0, pf_blk * rb + r0, k0 < a.K, dst);
+    auto fetch_next = [&](uint32_t (&dst)[V]) {
+        if (pf_t < tiles_mine && !a.per_channel) {
+            const int chunk = pf_ks * 16 + j;
+            const bool kv = chunk < a.k_chunks;
+            const int g = a.gs_shift >= 0 ? (chunk >> a.gs_shift) : chunk / a.gs_chunks;
+            const int mi = mat_of(a, pf_blk);
+            load_scale_bits<V>(a.mat[mi], a.scale_f16, kv ? g : 0,
+                               (pf_blk - a.mat[mi].blk_begin) * rb + r0, kv, dst);
         }
+        ++pf_t;
         if (++pf_ks == a.kslices) {
             pf_ks = 0;
             pf_blk += gridDim.x;
         }
     };
+    uint32_t sc[kScaleRing][V];
 #pragma unroll
-    for (int p = 0; p < kPrefetch; ++p) fetch(sc[p]);
+    for (int u = 0; u < kScaleRing; ++u) fetch_next(sc[u]);
 
     // x into shared memory once: chunk c (32 floats) at xs + c * kXPad; zero past K.
     griddep_wait();
@@ -223,15 +247,17 @@ __global__ void __launch_bounds__(kThreadsG, 1)
     }
     asm volatile("bar.sync 1, %0;" ::"r"(kCThreads) : "memory");
 
-    int64_t t = 0;
-    for (int64_t blk = blockIdx.x; blk < a.row_blocks; blk += gridDim.x) {
-        const int64_t n0 = blk * rb + r0;
-        float acc[V];
+    float acc[V];
 #pragma unroll
-        for (int v = 0; v < V; ++v) acc[v] = 0.f;
-        for (int ks = 0; ks < a.kslices; ++ks, ++t) {
-            const int s = (int)(t % kStagesG);
-            fetch(sc[kPrefetch]);
+    for (int v = 0; v < V; ++v) acc[v] = 0.f;
+    int ks = 0;
+    int64_t blk = blockIdx.x;
+    for (int t0 = 0; t0 < tiles_mine; t0 += kScaleRing) {
+#pragma unroll
+        for (int u = 0; u < kScaleRing; ++u) {
+            const int t = t0 + u;
+            if (t >= tiles_mine) break;
+            const int s = t & (kStagesG - 1);
             float4 xv[8];
             const float* xc = xs + (ks * 16 + j) * kXPad;
 #pragma unroll
@@ -247,29 +273,36 @@ __global__ void __launch_bounds__(kThreadsG, 1)
             for (int v = 0; v < V; ++v) {
                 const uint4 wv = ld_shared_v4(tile + (r0 + v) * kSliceBytes + j * 16);
                 const float d = chunk_dot<EH>(wv, xv);
-                acc[v] = a.per_channel ? acc[v] + d : fmaf(d, sc[0][v], acc[v]);
+                acc[v] = a.per_channel ? acc[v] + d
+                                       : fmaf(d, scale_from_bits(sc[u][v], a.scale_f16), acc[v]);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(empty(s));
+            fetch_next(sc[u]);
+            if (++ks == a.kslices) {
+                // Row block done: reduce the 16 chunk lanes of each row and store.
+                ks = 0;
 #pragma unroll
-            for (int p = 0; p < kPrefetch; ++p)
+                for (int v = 0; v < V; ++v) {
 #pragma unroll
-                for (int v = 0; v < V; ++v) sc[p][v] = sc[p + 1][v];
-        }
+                    for (int o = 1; o < 16; o <<= 1)
+                        acc[v] += __shfl_xor_sync(0xffffffffu, acc[v], o);
+                }
+                float mine = acc[0];
 #pragma unroll
-        for (int v = 0; v < V; ++v) {
+                for (int v = 1; v < V; ++v)
+                    if (j == v) mine = acc[v];
+                const MatArgs& m = a.mat[mat_of(a, blk)];
+                const int64_t n = (blk - m.blk_begin) * rb + r0 + j;
+                if (j < V && n < m.N) {
+                    if (a.per_channel) mine *= load_scale(m.scales, a.scale_f16, n);
+                    if (m.bias) mine += __ldg(m.bias + n);
+                    m.out[n] = mine;
+                }
 #pragma unroll
-            for (int o = 1; o < 16; o <<= 1) acc[v] += __shfl_xor_sync(0xffffffffu, acc[v], o);
-        }
-        float mine = acc[0];
-#pragma unroll
-        for (int v = 1; v < V; ++v)
-            if (j == v) mine = acc[v];
-        const int64_t n = n0 + j;
-        if (j < V && n < a.N) {
-            if (a.per_channel) mine *= load_scale(a.scales, a.scale_f16, n);
-            if (a.bias) mine += __ldg(a.bias + n);
-            a.out[n] = mine;
+                for (int v = 0; v < V; ++v) acc[v] = 0.f;
+                blk += gridDim.x;
+            }
         }
     }
 }
@@ -296,7 +329,7 @@ EncodeTiledFn encode_fn() {
 }
 
 template <int V, bool EH>
-cudaError_t launch_v(const CUtensorMap& tw, const GArgs& a, unsigned grid, const LaunchCtx& c) {
+cudaError_t launch_v(const TensorMaps& tm, const GArgs& a, unsigned grid, const LaunchCtx& c) {
     static cudaError_t attr = cudaFuncSetAttribute(
         gemv_tma_kernel<V, EH>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmemG);
     if (attr != cudaSuccess) return attr;
@@ -312,7 +345,7 @@ cudaError_t launch_v(const CUtensorMap& tw, const GArgs& a, unsigned grid, const
         cfg.attrs = attrs;
         cfg.numAttrs = 1;
     }
-    return cudaLaunchKernelEx(&cfg, gemv_tma_kernel<V, EH>, tw, a);
+    return cudaLaunchKernelEx(&cfg, gemv_tma_kernel<V, EH>, tm, a);
 }
 
 }  // namespace
@@ -323,52 +356,81 @@ bool gemv_tma_eligible(const Problem& p) {
     if (reinterpret_cast<uintptr_t>(p.x) % 16 || reinterpret_cast<uintptr_t>(p.qweight) % 16)
         return false;
     if (!(p.group_size >= p.K || p.group_size % 32 == 0)) return false;
-    if (p.N > 0x7FFFFFFFLL) return false;
+    if (p.N > (1LL << 30)) return false;
     return encode_fn() != nullptr;
 }
 
-cudaError_t gemv_tma_launch(const Problem& p, const LaunchCtx& c) {
+int gemv_tma_max_group() { return kMaxMats; }
+
+bool gemv_tma_groupable(const Problem& a, const Problem& b) {
+    return a.x == b.x && a.K == b.K && a.group_size == b.group_size &&
+           a.scale_f16 == b.scale_f16 && a.even_high == b.even_high &&
+           (a.group_size >= a.K) == (b.group_size >= b.K);
+}
+
+cudaError_t gemv_tma_launch_group(const Problem* ps, int count, const LaunchCtx& c) {
     EncodeTiledFn enc = encode_fn();
-    if (!enc) return cudaErrorNotSupported;
+    if (!enc || count < 1 || count > kMaxMats) return cudaErrorNotSupported;
+    const Problem& p0 = ps[0];
+    int64_t rows = 0;
+    for (int i = 0; i < count; ++i) rows += ps[i].N;
     // Rows per block: as large as the GPU stays busy with (more rows per thread reuse
     // the x chunk more), smaller for short matrices so every SM gets a block.
     int V = 4;
-    if ((p.N + 127) / 128 < c.sm_count) V = 2;
-    if ((p.N + 63) / 64 < c.sm_count) V = 1;
+    if ((rows + 127) / 128 < c.sm_count) V = 2;
+    if ((rows + 63) / 64 < c.sm_count) V = 1;
     const int rb = 32 * V;
-    GArgs a;
-    a.x = p.x;
-    a.scales = p.scales;
-    a.bias = p.bias;
-    a.out = p.out;
-    a.N = p.N;
-    a.K = p.K;
-    a.gs = p.group_size;
-    a.scale_f16 = p.scale_f16;
-    a.per_channel = p.group_size >= p.K;
-    const int esize = p.scale_f16 ? 2 : 4;
-    a.svec = (reinterpret_cast<uintptr_t>(p.scales) % 16 == 0) && (p.N % 4 == 0) && esize > 0;
-    a.kslices = (int)((p.K + kSliceK - 1) / kSliceK);
+    GArgs a = {};
+    a.x = p0.x;
+    a.nmat = count;
+    a.K = p0.K;
+    a.gs = p0.group_size;
+    a.scale_f16 = p0.scale_f16;
+    a.per_channel = p0.group_size >= p0.K;
+    a.kslices = (int)((p0.K + kSliceK - 1) / kSliceK);
     a.x_chunks = a.kslices * 16;
-    a.row_blocks = (p.N + rb - 1) / rb;
+    a.k_chunks = (int)(p0.K / 32);
+    a.gs_chunks = a.per_channel ? 1 : (int)(p0.group_size / 32);
+    a.gs_shift = -1;
+    for (int sft = 0; sft < 31; ++sft)
+        if ((1 << sft) == a.gs_chunks) a.gs_shift = sft;
     a.status = c.status_word;
     a.wait_ns = c.wait_limit_ns;
+    TensorMaps tm;
+    int64_t blocks = 0;
+    for (int i = 0; i < count; ++i) {
+        const Problem& p = ps[i];
+        a.mat[i].scales = p.scales;
+        a.mat[i].bias = p.bias;
+        a.mat[i].out = p.out;
+        a.mat[i].N = p.N;
+        a.mat[i].blk_begin = blocks;
+        blocks += (p.N + rb - 1) / rb;
+        const int64_t Kp = p.K / 2;
+        const cuuint64_t dims[2] = {(cuuint64_t)Kp, (cuuint64_t)p.N};
+        const cuuint64_t strides[1] = {(cuuint64_t)Kp};
+        const cuuint32_t box[2] = {(cuuint32_t)kSliceBytes, (cuuint32_t)rb};
+        const cuuint32_t estr[2] = {1, 1};
+        if (enc(&tm.m[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(p.qweight), dims,
+                strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    for (int i = count; i < kMaxMats; ++i) {
+        a.mat[i] = a.mat[count - 1];
+        a.mat[i].blk_begin = blocks;  // never selected: begins past the last block
+        tm.m[i] = tm.m[count - 1];
+    }
+    a.row_blocks = blocks;
+    const unsigned grid = (unsigned)std::min<int64_t>(blocks, c.sm_count);
+    const bool eh = p0.even_high != 0;
+    if (V == 4) return eh ? launch_v<4, true>(tm, a, grid, c) : launch_v<4, false>(tm, a, grid, c);
+    if (V == 2) return eh ? launch_v<2, true>(tm, a, grid, c) : launch_v<2, false>(tm, a, grid, c);
+    return eh ? launch_v<1, true>(tm, a, grid, c) : launch_v<1, false>(tm, a, grid, c);
+}
 
-    CUtensorMap tw;
-    const int64_t Kp = p.K / 2;
-    const cuuint64_t dims[2] = {(cuuint64_t)Kp, (cuuint64_t)p.N};
-    const cuuint64_t strides[1] = {(cuuint64_t)Kp};
-    const cuuint32_t box[2] = {(cuuint32_t)kSliceBytes, (cuuint32_t)rb};
-    const cuuint32_t estr[2] = {1, 1};
-    if (enc(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(p.qweight), dims, strides,
-            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-        return cudaErrorInvalidValue;
-    const unsigned grid = (unsigned)std::min<int64_t>(a.row_blocks, c.sm_count);
-    const bool eh = p.even_high != 0;
-    if (V == 4) return eh ? launch_v<4, true>(tw, a, grid, c) : launch_v<4, false>(tw, a, grid, c);
-    if (V == 2) return eh ? launch_v<2, true>(tw, a, grid, c) : launch_v<2, false>(tw, a, grid, c);
-    return eh ? launch_v<1, true>(tw, a, grid, c) : launch_v<1, false>(tw, a, grid, c);
+cudaError_t gemv_tma_launch(const Problem& p, const LaunchCtx& c) {
+    return gemv_tma_launch_group(&p, 1, c);
 }
 
 }  // namespace q4lin

@@ -241,6 +241,81 @@ q4lin_status_t q4lin_run(q4lin_handle_t h, const float* x, const uint8_t* qweigh
     return err == cudaSuccess ? Q4LIN_OK : Q4LIN_ERR_CUDA;
 }
 
+q4lin_status_t q4lin_run_grouped(q4lin_handle_t h, const q4lin_problem_t* problems, int count,
+                                 void* stream) {
+    if (!h || count < 0 || (count > 0 && !problems)) return Q4LIN_ERR_INVALID_ARG;
+    if (count == 0) return Q4LIN_OK;
+    constexpr int kMax = 4;
+    q4lin::Problem ps[kMax];
+    const q4lin::LaunchCtx c = make_ctx(h, static_cast<cudaStream_t>(stream));
+    // Validate everything first: an error means nothing was enqueued.
+    for (int i = 0; i < count; ++i) {
+        const q4lin_problem_t& q = problems[i];
+        q4lin::Problem p;
+        bool empty = false;
+        q4lin_status_t st = validate(h, q.x, q.qweight, q.scales, q.bias, q.out, q.M, q.N, q.K,
+                                     q.group_size, q.scale_dtype, &p, &empty);
+        if (st != Q4LIN_OK) return st;
+        int path = 0;
+        if (!empty && (st = plan(h, p, c, &path)) != Q4LIN_OK) return st;
+    }
+    DeviceGuard g(h->device);
+    if (!g.ok()) return Q4LIN_ERR_CUDA;
+    const bool gemv_forced_off =
+        h->force_path == Q4LIN_PATH_FFMA || h->force_path == Q4LIN_PATH_TC;
+    int i = 0;
+    while (i < count) {
+        // Gather a run of fusable problems starting at i.
+        int n = 0;
+        bool empty = false;
+        const q4lin_problem_t* q = &problems[i];
+        validate(h, q->x, q->qweight, q->scales, q->bias, q->out, q->M, q->N, q->K,
+                 q->group_size, q->scale_dtype, &ps[0], &empty);
+        if (!empty && !gemv_forced_off && q4lin::gemv_tma_eligible(ps[0])) {
+            n = 1;
+            while (n < kMax && n < q4lin::gemv_tma_max_group() && i + n < count) {
+                const q4lin_problem_t& r = problems[i + n];
+                q4lin::Problem pr;
+                bool e2 = false;
+                validate(h, r.x, r.qweight, r.scales, r.bias, r.out, r.M, r.N, r.K, r.group_size,
+                         r.scale_dtype, &pr, &e2);
+                if (e2 || !q4lin::gemv_tma_eligible(pr) || !q4lin::gemv_tma_groupable(ps[0], pr))
+                    break;
+                // Fused problems run concurrently: no output may touch another's buffers.
+                bool clash = false;
+                for (int k = 0; k < n && !clash; ++k) {
+                    const int64_t ob_new = pr.N * 4, ob_old = ps[k].N * 4;
+                    const int64_t es = pr.scale_f16 ? 2 : 4;
+                    const int64_t G = (pr.K + pr.group_size - 1) / pr.group_size;
+                    clash = overlaps(pr.out, ob_new, ps[k].out, ob_old) ||
+                            overlaps(pr.out, ob_new, ps[k].qweight, ps[k].N * (ps[k].K / 2)) ||
+                            overlaps(pr.out, ob_new, ps[k].scales, G * ps[k].N * es) ||
+                            overlaps(pr.out, ob_new, ps[k].bias, ps[k].bias ? ob_old : 0) ||
+                            overlaps(ps[k].out, ob_old, pr.qweight, pr.N * (pr.K / 2)) ||
+                            overlaps(ps[k].out, ob_old, pr.scales, G * pr.N * es) ||
+                            overlaps(ps[k].out, ob_old, pr.bias, pr.bias ? ob_new : 0);
+                }
+                if (clash) break;
+                ps[n++] = pr;
+            }
+        }
+        cudaError_t err = cudaSuccess;
+        if (n >= 2) {
+            err = q4lin::gemv_tma_launch_group(ps, n, c);
+            i += n;
+        } else {
+            err = cudaSuccess;
+            q4lin_status_t st = q4lin_run(h, q->x, q->qweight, q->scales, q->bias, q->out, q->M,
+                                          q->N, q->K, q->group_size, q->scale_dtype, stream);
+            if (st != Q4LIN_OK) return st;
+            ++i;
+        }
+        if (err == cudaSuccess) err = cudaGetLastError();
+        if (err != cudaSuccess) return Q4LIN_ERR_CUDA;
+    }
+    return Q4LIN_OK;
+}
+
 q4lin_status_t q4lin_set_option(q4lin_handle_t h, int option, int64_t value) {
     if (!h) return Q4LIN_ERR_INVALID_ARG;
     switch (option) {

@@ -41,6 +41,11 @@ cudaError_t rowstream_launch(const Problem& p, const LaunchCtx& c);
 // qweight, and group_size % 32 == 0 or group_size >= K.
 bool gemv_tma_eligible(const Problem& p);
 cudaError_t gemv_tma_launch(const Problem& p, const LaunchCtx& c);
+// Several eligible M = 1 problems that share x, K, group size, scale dtype and nibble
+// order in one launch (at most gemv_tma_max_group()).
+int gemv_tma_max_group();
+bool gemv_tma_groupable(const Problem& a, const Problem& b);
+cudaError_t gemv_tma_launch_group(const Problem* ps, int count, const LaunchCtx& c);
 
 // Generic CUDA-core kernel: any K (odd included), any group size, any alignment.
 cudaError_t generic_launch(const Problem& p, const LaunchCtx& c);

@@ -18,30 +18,33 @@
 // tf32 keeps 10 explicit mantissa bits of each operand, so a product carries a relative
 // error below 2^-9 -- inside the 4e-3 * sum|x*w| bar of the tensor-core path.
 //
-// Roles (192 threads, one CTA per 128 x bm output tile):
+// Roles (320 threads, one CTA per 128 x bm output tile):
 //   warp 0, one lane: TMA producer; per stage (32 k) the x tile [bm x 128 B] and the
 //                     packed weight tile [128 rows x 16 B] land in a 4-stage ring.
 //   warp 1:           allocates tensor memory; one lane issues 4 tcgen05.mma (K = 8
 //                     each) per stage and commits each stage's completion to "empty".
-//   warps 2-5:        one thread per weight row: widen 32 codes, multiply by the group
-//                     scale, store the row into the swizzled A stage, arrive on
-//                     "a_ready"; at the end read their 32-lane slice of D with
-//                     tcgen05.ld, add the bias and store out (predicated m < M, n < N).
+//   warps 2-9:        two groups of 4 warps, each taking alternate stages (so one
+//                     group's proxy fence and arrive overlap the other's work); one
+//                     thread per weight row: widen 32 codes, multiply by the group
+//                     scale, store the row into the swizzled A stage, fence, arrive on
+//                     "a_ready"; at the end each warp reads its 32-lane slice of D with
+//                     tcgen05.ld (the groups split the columns), adds the bias and
+//                     stores out (predicated m < M, n < N).
 // Every mbarrier wait is bounded in time (%globaltimer).  A wait that runs out records
 // code 1 in the status word; the CTA then stops issuing work, waits for its own copies
 // and MMAs in flight, frees its tensor memory and returns.
-#include <cuda.h>
-#include <cuda_fp16.h>
-
 #include <algorithm>
 #include <mutex>
 
+#include "ptx.cuh"
 #include "q4lin_internal.h"
 
 namespace q4lin {
 namespace {
+using namespace ptx;
 
-constexpr int kThreadsTc = 192;
+constexpr int kDequantGroups = 2;     // warp groups of 4 that dequantize alternate stages
+constexpr int kThreadsTc = 64 + 128 * kDequantGroups;
 constexpr int kRows = 128;            // weight rows per tile (MMA M)
 constexpr int kStageK = 32;           // k per stage: 32 fp32 = one 128-byte swizzle row
 constexpr int kStages = 4;
@@ -62,131 +65,12 @@ struct TcArgs {
     int64_t M, N, K, gs;
     int scale_f16, per_channel, even_high;
     int bm, k_iters, tmem_cols;
+    int gs_stages;  // group size in stages of 32 k (grouped scales)
+    int gs_shift;   // log2(gs_stages) when a power of two, else -1
     int* status;
     int64_t wait_ns;
     int skip_first_copy;
 };
-
-// ---------------------------------------------------------------------- PTX wrappers
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ uint64_t global_timer() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-// Wait for the phase of `bar` with the given parity, for at most limit_ns of global time
-// (and, when `failed` is given, only while no thread of the CTA has failed).
-__device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, int64_t limit_ns,
-                                          const volatile int* failed) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = global_timer();
-    while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if (failed && *failed) return false;
-        if ((int64_t)(global_timer() - t0) > limit_ns) return false;
-    }
-}
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
-                                            uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
-        : "memory");
-}
-__device__ __forceinline__ void fence_proxy_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_before() {
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_alloc(uint32_t slot, uint32_t cols) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot),
-                 "r"(cols)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t cols) {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(cols)
-                 : "memory");
-}
-// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, 8-row atoms of
-// 1024 bytes (stride byte offset), leading byte offset unused, descriptor version 1.
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-    uint64_t d = 0;
-    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
-    d |= (uint64_t)1 << 16;
-    d |= (uint64_t)(1024 >> 4) << 32;
-    d |= (uint64_t)1 << 46;
-    d |= (uint64_t)2 << 61;
-    return d;
-}
-// Instruction descriptor of kind::tf32: D fp32, A and B tf32, both K-major, M = 128.
-__device__ __forceinline__ uint32_t tf32_idesc(int n) {
-    return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(n >> 3) << 17) |
-           ((uint32_t)(kRows >> 4) << 24);
-}
-__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                         uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-        : "memory");
-}
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-        "%14,%15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
-    uint4 v;
-    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "r"(addr));
-    return v;
-}
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, float a, float b, float c, float d) {
-    asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "f"(a), "f"(b), "f"(c),
-                 "f"(d)
-                 : "memory");
-}
-__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 __device__ __forceinline__ float load_scale(const void* scales, int f16, int64_t idx) {
     if (f16) return __half2float(__ldg(reinterpret_cast<const __half*>(scales) + idx));
@@ -207,11 +91,6 @@ __device__ __forceinline__ void codes8(uint32_t w, float (&v)[8]) {
             : "=f"(v[i]), "=f"(v[i + 4])
             : "r"(h[i]), "f"(-1032.0f));
     }
-}
-
-__device__ __forceinline__ void record_failure(int* status, volatile int* failed) {
-    atomicCAS(status, 0, 1);
-    *failed = 1;
 }
 
 __global__ void __launch_bounds__(kThreadsTc, 1)
@@ -238,7 +117,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(full(s), 1);
-            mbar_init(aready(s), 128);
+            mbar_init(aready(s), 128);  // the 128 threads of the group that owns the stage
             mbar_init(empty(s), 1);
         }
         mbar_init(accfull, 1);
@@ -279,7 +158,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     } else if (warp == 1) {
         if (lane == 0) {
             // ------------------------------------------------------------- MMA issuer
-            const uint32_t idesc = tf32_idesc(bm);
+            const uint32_t idesc = tf32_idesc(kRows, bm);
             for (int it = 0; it < a.k_iters; ++it) {
                 const int s = it % kStages;
                 const uint32_t par = (it / kStages) & 1;
@@ -288,7 +167,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                     record_failure(a.status, failed);
                     break;
                 }
-                tc_fence_after();
+                // The A stage was written through the generic proxy, fenced to the async
+                // proxy by its writers before they arrived; the B stage came by TMA.  The
+                // mbarrier waits above order both before these MMAs.
                 const uint32_t ab = a_base + s * kATile, bb = b_base + s * bm * 128;
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
@@ -301,53 +182,60 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         __syncwarp();
     } else {
         // ------------------------------------------------- dequantization, epilogue
-        const int quarter = warp & 3;  // the 32-lane slice of tensor memory this warp owns
+        const int group = (warp - 2) >> 2;  // dequantizes stages it % kDequantGroups == group
+        const int quarter = warp & 3;       // the 32-lane slice of tensor memory this warp owns
         const int row = quarter * 32 + lane;
         const int64_t n = (int64_t)blockIdx.x * kRows + row;
         const bool row_ok = n < a.N;
         const uint32_t swz = (uint32_t)(row & 7);
         bool ok = true;
-        // Group scales of this row, kScaleAhead stages ahead of use (a global load takes
-        // longer than one stage of MMAs).
+        // Group scales of this row for this group's stages, kScaleAhead of them ahead of
+        // use (a global load takes longer than a stage of MMAs).  The loop is unrolled by
+        // the ring size so each slot is a fixed register (no move of a pending load).
         float sc_ring[kScaleAhead];
         auto scale_of = [&](int it) -> float {
             if (!row_ok) return 0.f;
             if (a.per_channel || it >= a.k_iters) return 1.f;
-            return load_scale(a.scales, a.scale_f16, ((int64_t)it * kStageK / a.gs) * a.N + n);
+            const int g = a.gs_shift >= 0 ? (it >> a.gs_shift) : it / a.gs_stages;
+            return load_scale(a.scales, a.scale_f16, (int64_t)g * a.N + n);
         };
 #pragma unroll
-        for (int i = 0; i < kScaleAhead; ++i) sc_ring[i] = scale_of(i);
-        for (int it = 0; it < a.k_iters; ++it) {
-            const int s = it % kStages;
-            const float sc = sc_ring[0];
+        for (int i = 0; i < kScaleAhead; ++i) sc_ring[i] = scale_of(group + i * kDequantGroups);
+        constexpr int kStride = kScaleAhead * kDequantGroups;
+        for (int it0 = group; it0 < a.k_iters && ok; it0 += kStride) {
 #pragma unroll
-            for (int i = 0; i + 1 < kScaleAhead; ++i) sc_ring[i] = sc_ring[i + 1];
-            sc_ring[kScaleAhead - 1] = scale_of(it + kScaleAhead);
-            if (!wait_bounded(full(s), (it / kStages) & 1, a.wait_ns, failed)) {
-                record_failure(a.status, failed);
-                ok = false;
-                break;
-            }
-            uint4 wv = ld_shared_v4(w_base + s * kWTile + row * 16);
-            if (a.even_high) {
-                wv.x = ((wv.x & 0x0F0F0F0Fu) << 4) | ((wv.x >> 4) & 0x0F0F0F0Fu);
-                wv.y = ((wv.y & 0x0F0F0F0Fu) << 4) | ((wv.y >> 4) & 0x0F0F0F0Fu);
-                wv.z = ((wv.z & 0x0F0F0F0Fu) << 4) | ((wv.z >> 4) & 0x0F0F0F0Fu);
-                wv.w = ((wv.w & 0x0F0F0F0Fu) << 4) | ((wv.w >> 4) & 0x0F0F0F0Fu);
-            }
-            const uint32_t words[4] = {wv.x, wv.y, wv.z, wv.w};
-            const uint32_t arow = a_base + s * kATile + row * 128;
+            for (int u = 0; u < kScaleAhead; ++u) {
+                const int it = it0 + u * kDequantGroups;
+                if (it >= a.k_iters) break;
+                const int s = it % kStages;
+                if (!wait_bounded(full(s), (it / kStages) & 1, a.wait_ns, failed)) {
+                    record_failure(a.status, failed);
+                    ok = false;
+                    break;
+                }
+                uint4 wv = ld_shared_v4(w_base + s * kWTile + row * 16);
+                if (a.even_high) {
+                    wv.x = ((wv.x & 0x0F0F0F0Fu) << 4) | ((wv.x >> 4) & 0x0F0F0F0Fu);
+                    wv.y = ((wv.y & 0x0F0F0F0Fu) << 4) | ((wv.y >> 4) & 0x0F0F0F0Fu);
+                    wv.z = ((wv.z & 0x0F0F0F0Fu) << 4) | ((wv.z >> 4) & 0x0F0F0F0Fu);
+                    wv.w = ((wv.w & 0x0F0F0F0Fu) << 4) | ((wv.w >> 4) & 0x0F0F0F0Fu);
+                }
+                const float sc = sc_ring[u];
+                sc_ring[u] = scale_of(it + kStride);
+                const uint32_t words[4] = {wv.x, wv.y, wv.z, wv.w};
+                const uint32_t arow = a_base + s * kATile + row * 128;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                float v[8];
-                codes8(words[j], v);
+                for (int j = 0; j < 4; ++j) {
+                    float v[8];
+                    codes8(words[j], v);
 #pragma unroll
-                for (int t = 0; t < 8; ++t) v[t] *= sc;
-                st_shared_v4(arow + (((2u * j) ^ swz) << 4), v[0], v[1], v[2], v[3]);
-                st_shared_v4(arow + (((2u * j + 1) ^ swz) << 4), v[4], v[5], v[6], v[7]);
+                    for (int t = 0; t < 8; ++t) v[t] *= sc;
+                    st_shared_v4(arow + (((2u * j) ^ swz) << 4), v[0], v[1], v[2], v[3]);
+                    st_shared_v4(arow + (((2u * j + 1) ^ swz) << 4), v[4], v[5], v[6], v[7]);
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(aready(s));
             }
-            fence_proxy_async_smem();
-            mbar_arrive(aready(s));
         }
         const bool acc_ok = wait_bounded(accfull, 0, ok ? a.wait_ns : kDrainLimitNs, nullptr);
         if (!acc_ok) record_failure(a.status, failed);
@@ -358,7 +246,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             const float bs = (a.bias && row_ok) ? __ldg(a.bias + n) : 0.f;
             const int64_t m0 = (int64_t)blockIdx.y * bm;
             const uint32_t lane_base = tmem_d + ((uint32_t)(quarter * 32) << 16);
-            for (int c0 = 0; c0 < bm; c0 += 16) {
+            for (int c0 = 16 * group; c0 < bm; c0 += 16 * kDequantGroups) {
                 uint32_t r[16];
                 tmem_ld16(lane_base + (uint32_t)c0, r);
                 if (row_ok) {
@@ -428,9 +316,26 @@ cudaError_t tc_launch(const Problem& p, const LaunchCtx& c) {
     if (!enc) return cudaErrorNotSupported;
     cudaError_t e = ensure_smem_attr();
     if (e != cudaSuccess) return e;
-    const int64_t mtiles = (p.M + kMaxBm - 1) / kMaxBm;
-    const int64_t per_tile = (p.M + mtiles - 1) / mtiles;
-    const int bm = (int)std::min<int64_t>(kMaxBm, (per_tile + 15) / 16 * 16);
+    // x rows per tile (the MMA's N).  Larger tiles reuse each dequantized weight tile
+    // more; smaller ones give more CTAs.  Estimate waves x cycles per stage, where a
+    // stage costs ~2 * bm cycles of tf32 MMA but no less than the CUDA-core dequant
+    // (~160 cycles for 128 rows x 32 codes on 4 warps), and take the cheapest.
+    const int64_t ntiles = (p.N + kRows - 1) / kRows;
+    int bm = 16;
+    int64_t mtiles = 0, best = -1;
+    for (int cand = kMaxBm; cand >= 16; cand /= 2) {
+        const int64_t mt = (p.M + cand - 1) / cand;
+        if (mt > 65535) continue;
+        const int64_t per_tile = (p.M + mt - 1) / mt;
+        const int b = (int)std::min<int64_t>(cand, (per_tile + 15) / 16 * 16);
+        const int64_t waves = (ntiles * mt + c.sm_count - 1) / c.sm_count;
+        const int64_t cost = waves * std::max<int64_t>(2 * b, 160);
+        if (best < 0 || cost < best) {
+            best = cost;
+            bm = b;
+            mtiles = mt;
+        }
+    }
     int cols = 32;
     while (cols < bm) cols <<= 1;
 
@@ -451,6 +356,10 @@ cudaError_t tc_launch(const Problem& p, const LaunchCtx& c) {
     a.status = c.status_word;
     a.wait_ns = c.wait_limit_ns;
     a.skip_first_copy = c.tc_skip_first_copy;
+    a.gs_stages = a.per_channel ? 1 : (int)(p.group_size / kStageK);
+    a.gs_shift = -1;
+    for (int sft = 0; sft < 31; ++sft)
+        if ((1 << sft) == a.gs_stages) a.gs_shift = sft;
 
     CUtensorMap tx, tw;
     {

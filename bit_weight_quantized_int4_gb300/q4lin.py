@@ -52,6 +52,14 @@ _lib.q4lin_destroy.argtypes = [_vp]
 _lib.q4lin_destroy.restype = _i32
 _lib.q4lin_run.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i32, _vp]
 _lib.q4lin_run.restype = _i32
+class q4lin_problem_t(ctypes.Structure):
+    _fields_ = [("x", _vp), ("qweight", _vp), ("scales", _vp), ("bias", _vp), ("out", _vp),
+                ("M", _i64), ("N", _i64), ("K", _i64), ("group_size", _i64),
+                ("scale_dtype", _i32)]
+
+
+_lib.q4lin_run_grouped.argtypes = [_vp, ctypes.POINTER(q4lin_problem_t), _i32, _vp]
+_lib.q4lin_run_grouped.restype = _i32
 _lib.q4lin_plan.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i32,
                             ctypes.POINTER(_i32)]
 _lib.q4lin_plan.restype = _i32
@@ -96,6 +104,14 @@ def q4lin_run(handle, x, qweight, scales, bias, out, M, N, K, group_size, scale_
     """Raw call: pointers and the stream are integers (0 / None for NULL)."""
     return _lib.q4lin_run(handle, x, qweight, scales, bias, out, M, N, K, group_size,
                           scale_dtype, stream)
+
+
+def q4lin_run_grouped(handle, problems, stream) -> int:
+    """problems: a sequence of q4lin_problem_t (or of 10-tuples in its field order)."""
+    arr = (q4lin_problem_t * max(1, len(problems)))()
+    for i, p in enumerate(problems):
+        arr[i] = p if isinstance(p, q4lin_problem_t) else q4lin_problem_t(*p)
+    return _lib.q4lin_run_grouped(handle, arr, len(problems), stream)
 
 
 def q4lin_plan(handle, x, qweight, scales, bias, out, M, N, K, group_size, scale_dtype):

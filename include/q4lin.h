@@ -122,6 +122,30 @@ Q4LIN_API q4lin_status_t q4lin_run(q4lin_handle_t handle, const float* x,
                                    int64_t K, int64_t group_size, int scale_dtype,
                                    void* stream);
 
+/* One problem of q4lin_run_grouped: the arguments of one q4lin_run call. */
+typedef struct q4lin_problem {
+    const float* x;
+    const uint8_t* qweight;
+    const void* scales;
+    const float* bias; /* may be NULL */
+    float* out;
+    int64_t M, N, K, group_size;
+    int scale_dtype;
+} q4lin_problem_t;
+
+/* Run `count` problems on `stream`; the result is that of calling q4lin_run on each in
+ * order.  Consecutive M = 1 problems that read the same x with the same K, group size and
+ * scale dtype (for example the q, k and v projections of a decoder layer, or its gate
+ * and up projections) run as one launch, up to 4 per launch, when none of their outputs
+ * overlaps another problem's buffers; everything else runs one call at a time.  This is
+ * the fused decode launch that the pages' MLC fusion passes produce before the GEMV
+ * schedule ("dlight.gpu.GEMV" notice: "fusion passes -> LowBatchGemvSpecialize").
+ * Every problem is validated before anything is enqueued (same rules and status codes
+ * as q4lin_run); `problems` is read during the call only.  count == 0 is Q4LIN_OK. */
+Q4LIN_API q4lin_status_t q4lin_run_grouped(q4lin_handle_t handle,
+                                           const q4lin_problem_t* problems, int count,
+                                           void* stream);
+
 /* The path q4lin_run would take for these arguments (no launch, no device access);
  * *path_out receives a q4lin_path_t other than AUTO.  Same validation and status codes
  * as q4lin_run.  For M == 0 or N == 0, *path_out is Q4LIN_PATH_AUTO (nothing runs). */
