@@ -88,24 +88,18 @@ __device__ __forceinline__ float load_scale(const void* scales, int f16, int64_t
     return __ldg(reinterpret_cast<const float*>(scales) + idx);
 }
 
-// Raw bits of scale[g, n0 + v] (binary16 in the low half, or fp32), 0 past N or when
-// !valid.  Kept raw in the prefetch ring and converted only when used: converting at
-// load time would make the thread wait for the load right away.
-template <int V>
-__device__ __forceinline__ void load_scale_bits(const MatArgs& m, int f16, int64_t g, int64_t n0,
-                                                bool valid, uint32_t (&r)[V]) {
-    const int64_t base = g * m.N + n0;
-#pragma unroll
-    for (int v = 0; v < V; ++v) {
-        uint32_t bits = 0;
-        if (valid && n0 + v < m.N) {
-            if (f16)
-                bits = __ldg(reinterpret_cast<const unsigned short*>(m.scales) + base + v);
-            else
-                bits = __ldg(reinterpret_cast<const unsigned int*>(m.scales) + base + v);
-        }
-        r[v] = bits;
-    }
+// Raw bits of one scale (binary16 in the low half, or fp32).  Kept raw in the prefetch
+// ring and converted only when used: converting at load time would make the thread wait
+// for the load right away.
+template <bool F16>
+__device__ __forceinline__ uint32_t scale_bits(const void* scales, int64_t idx) {
+    if (F16) return __ldg(reinterpret_cast<const unsigned short*>(scales) + idx);
+    return __ldg(reinterpret_cast<const unsigned int*>(scales) + idx);
+}
+template <bool F16>
+__device__ __forceinline__ float scale_value(uint32_t bits) {
+    if (F16) return __half2float(__ushort_as_half((unsigned short)bits));
+    return __uint_as_float(bits);
 }
 
 // Matrix that owns global row block blk (blk_begin ascending, matrix 0 begins at 0).
@@ -117,30 +111,40 @@ __device__ __forceinline__ int mat_of(const GArgs& a, int64_t blk) {
     return i;
 }
 
-__device__ __forceinline__ float scale_from_bits(uint32_t bits, int f16) {
-    return f16 ? __half2float(__ushort_as_half((unsigned short)bits)) : __uint_as_float(bits);
-}
-
-// sum over the 32 values of one 16-byte chunk of x[t] * (code_t - 8).
+// Products x[t] * (code_t - 8) of one 16-byte chunk (32 codes), summed as a float2 of
+// (even-k sum, odd-k sum) where the lane fed from the HIGH nibbles carries a factor 16.
+// Byte b of a word holds k = 2b in its low nibble and k = 2b + 1 in its high nibble
+// (swapped when EH).  The low nibbles are isolated with one mask (w & 0x0F0F0F0F) and the
+// high nibbles in place with another (w & 0xF0F0F0F0, i.e. 16 * code): no shift.  A byte
+// permute builds the float 2^23 + byte (bit pattern 0x4B0000bb) and one packed add of
+// -(2^23 + 8) (low lane) / -(2^23 + 128) (high lane) gives c - 8 and 16 * (c - 8), both
+// exact.  The factor 16 is removed once per row (a power of two: exact).
 template <bool EH>
-__device__ __forceinline__ float chunk_dot(const uint4& wv, const float4 (&xv)[8]) {
+__device__ __forceinline__ float2 chunk_dot(const uint4& wv, const float4 (&xv)[8]) {
+    constexpr float kLo = -8388616.0f, kHi = -8388736.0f;
+    const float2 bias = EH ? make_float2(kHi, kLo) : make_float2(kLo, kHi);
     float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
     const uint32_t words[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
-        float2 c[4];
-        codes_word<EH>(words[w], c);
+        const uint32_t lo = words[w] & 0x0F0F0F0Fu, hi = words[w] & 0xF0F0F0F0u;
+        const uint32_t ev = EH ? hi : lo, od = EH ? lo : hi;
         const float4 p = xv[2 * w], q = xv[2 * w + 1];
+        const float2 xs[4] = {make_float2(p.x, p.y), make_float2(p.z, p.w), make_float2(q.x, q.y),
+                              make_float2(q.z, q.w)};
         float2& acc = (w & 1) ? a1 : a0;
-        acc = ffma2(c[0], make_float2(p.x, p.y), acc);
-        acc = ffma2(c[1], make_float2(p.z, p.w), acc);
-        acc = ffma2(c[2], make_float2(q.x, q.y), acc);
-        acc = ffma2(c[3], make_float2(q.z, q.w), acc);
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            const float2 c = fadd2(make_float2(__uint_as_float(prmt(ev, 0x4B000000u, 0x7440u | b)),
+                                               __uint_as_float(prmt(od, 0x4B000000u, 0x7440u | b))),
+                                   bias);
+            acc = ffma2(c, xs[b], acc);
+        }
     }
-    return (a0.x + a0.y) + (a1.x + a1.y);
+    return fadd2(a0, a1);
 }
 
-template <int V, bool EH>
+template <int V, bool EH, bool PC, bool F16>
 __global__ void __launch_bounds__(kThreadsG, 1)
     gemv_tma_kernel(const __grid_constant__ TensorMaps tmaps, const GArgs a) {
     constexpr int rb = 32 * V;  // rows per block: 32 row groups of V rows
@@ -218,13 +222,26 @@ __global__ void __launch_bounds__(kThreadsG, 1)
     int pf_ks = 0, pf_t = 0;
     int64_t pf_blk = blockIdx.x;
     auto fetch_next = [&](uint32_t (&dst)[V]) {
-        if (pf_t < tiles_mine && !a.per_channel) {
+        if (!PC && pf_t < tiles_mine) {
             const int chunk = pf_ks * 16 + j;
-            const bool kv = chunk < a.k_chunks;
-            const int g = a.gs_shift >= 0 ? (chunk >> a.gs_shift) : chunk / a.gs_chunks;
             const int mi = mat_of(a, pf_blk);
-            load_scale_bits<V>(a.mat[mi], a.scale_f16, kv ? g : 0,
-                               (pf_blk - a.mat[mi].blk_begin) * rb + r0, kv, dst);
+            const MatArgs& m = a.mat[mi];
+            const int64_t n0 = (pf_blk - m.blk_begin) * rb + r0;
+            if (chunk < a.k_chunks) {
+                const int g = a.gs_shift >= 0 ? (chunk >> a.gs_shift) : chunk / a.gs_chunks;
+                const int64_t bi = (int64_t)g * m.N + n0;
+                if (n0 + V <= m.N) {
+#pragma unroll
+                    for (int v = 0; v < V; ++v) dst[v] = scale_bits<F16>(m.scales, bi + v);
+                } else {
+#pragma unroll
+                    for (int v = 0; v < V; ++v)
+                        dst[v] = n0 + v < m.N ? scale_bits<F16>(m.scales, bi + v) : 0u;
+                }
+            } else {
+#pragma unroll
+                for (int v = 0; v < V; ++v) dst[v] = 0u;
+            }
         }
         ++pf_t;
         if (++pf_ks == a.kslices) {
@@ -247,11 +264,13 @@ __global__ void __launch_bounds__(kThreadsG, 1)
     }
     asm volatile("bar.sync 1, %0;" ::"r"(kCThreads) : "memory");
 
-    float acc[V];
+    // Per row: (even-k, odd-k) partial sums, scaled per chunk by the group scale.
+    float2 acc[V];
 #pragma unroll
-    for (int v = 0; v < V; ++v) acc[v] = 0.f;
+    for (int v = 0; v < V; ++v) acc[v] = make_float2(0.f, 0.f);
     int ks = 0;
     int64_t blk = blockIdx.x;
+    const float* xrow = xs + j * kXPad;
     for (int t0 = 0; t0 < tiles_mine; t0 += kScaleRing) {
 #pragma unroll
         for (int u = 0; u < kScaleRing; ++u) {
@@ -259,7 +278,7 @@ __global__ void __launch_bounds__(kThreadsG, 1)
             if (t >= tiles_mine) break;
             const int s = t & (kStagesG - 1);
             float4 xv[8];
-            const float* xc = xs + (ks * 16 + j) * kXPad;
+            const float* xc = xrow + ks * (16 * kXPad);
 #pragma unroll
             for (int i = 0; i < 8; ++i) xv[i] = *reinterpret_cast<const float4*>(xc + 4 * i);
             const bool got = __all_sync(
@@ -268,39 +287,45 @@ __global__ void __launch_bounds__(kThreadsG, 1)
                 if (lane == 0) record_failure(a.status, failed);
                 return;
             }
-            const uint32_t tile = base + s * tile_bytes;
+            const uint32_t wrow = base + s * tile_bytes + r0 * kSliceBytes + j * 16;
 #pragma unroll
             for (int v = 0; v < V; ++v) {
-                const uint4 wv = ld_shared_v4(tile + (r0 + v) * kSliceBytes + j * 16);
-                const float d = chunk_dot<EH>(wv, xv);
-                acc[v] = a.per_channel ? acc[v] + d
-                                       : fmaf(d, scale_from_bits(sc[u][v], a.scale_f16), acc[v]);
+                const uint4 wv = ld_shared_v4(wrow + v * kSliceBytes);
+                const float2 d = chunk_dot<EH>(wv, xv);
+                if (PC) {
+                    acc[v] = fadd2(acc[v], d);
+                } else {
+                    const float sv = scale_value<F16>(sc[u][v]);
+                    acc[v] = ffma2(d, make_float2(sv, sv), acc[v]);
+                }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(empty(s));
             fetch_next(sc[u]);
             if (++ks == a.kslices) {
-                // Row block done: reduce the 16 chunk lanes of each row and store.
+                // Row block done: undo the factor 16 of the high-nibble lane, reduce the
+                // 16 chunk lanes of each row, store.
                 ks = 0;
+                float tot[V];
 #pragma unroll
                 for (int v = 0; v < V; ++v) {
+                    tot[v] = EH ? fmaf(acc[v].x, 0.0625f, acc[v].y) : fmaf(acc[v].y, 0.0625f, acc[v].x);
 #pragma unroll
                     for (int o = 1; o < 16; o <<= 1)
-                        acc[v] += __shfl_xor_sync(0xffffffffu, acc[v], o);
+                        tot[v] += __shfl_xor_sync(0xffffffffu, tot[v], o);
+                    acc[v] = make_float2(0.f, 0.f);
                 }
-                float mine = acc[0];
+                float mine = tot[0];
 #pragma unroll
                 for (int v = 1; v < V; ++v)
-                    if (j == v) mine = acc[v];
+                    if (j == v) mine = tot[v];
                 const MatArgs& m = a.mat[mat_of(a, blk)];
                 const int64_t n = (blk - m.blk_begin) * rb + r0 + j;
                 if (j < V && n < m.N) {
-                    if (a.per_channel) mine *= load_scale(m.scales, a.scale_f16, n);
+                    if (PC) mine *= scale_value<F16>(scale_bits<F16>(m.scales, n));
                     if (m.bias) mine += __ldg(m.bias + n);
                     m.out[n] = mine;
                 }
-#pragma unroll
-                for (int v = 0; v < V; ++v) acc[v] = 0.f;
                 blk += gridDim.x;
             }
         }
@@ -328,10 +353,10 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-template <int V, bool EH>
+template <int V, bool EH, bool PC, bool F16>
 cudaError_t launch_v(const TensorMaps& tm, const GArgs& a, unsigned grid, const LaunchCtx& c) {
     static cudaError_t attr = cudaFuncSetAttribute(
-        gemv_tma_kernel<V, EH>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmemG);
+        gemv_tma_kernel<V, EH, PC, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmemG);
     if (attr != cudaSuccess) return attr;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
@@ -345,7 +370,31 @@ cudaError_t launch_v(const TensorMaps& tm, const GArgs& a, unsigned grid, const 
         cfg.attrs = attrs;
         cfg.numAttrs = 1;
     }
-    return cudaLaunchKernelEx(&cfg, gemv_tma_kernel<V, EH>, tm, a);
+    return cudaLaunchKernelEx(&cfg, gemv_tma_kernel<V, EH, PC, F16>, tm, a);
+}
+
+template <int V, bool EH, bool PC>
+cudaError_t dispatch_f16(bool f16, const TensorMaps& tm, const GArgs& a, unsigned grid,
+                         const LaunchCtx& c) {
+    return f16 ? launch_v<V, EH, PC, true>(tm, a, grid, c) : launch_v<V, EH, PC, false>(tm, a, grid, c);
+}
+template <int V, bool EH>
+cudaError_t dispatch_pc(bool pc, bool f16, const TensorMaps& tm, const GArgs& a, unsigned grid,
+                        const LaunchCtx& c) {
+    return pc ? dispatch_f16<V, EH, true>(f16, tm, a, grid, c)
+              : dispatch_f16<V, EH, false>(f16, tm, a, grid, c);
+}
+template <int V>
+cudaError_t dispatch_eh(bool eh, bool pc, bool f16, const TensorMaps& tm, const GArgs& a,
+                        unsigned grid, const LaunchCtx& c) {
+    return eh ? dispatch_pc<V, true>(pc, f16, tm, a, grid, c)
+              : dispatch_pc<V, false>(pc, f16, tm, a, grid, c);
+}
+cudaError_t dispatch_v(int V, bool eh, bool pc, bool f16, const TensorMaps& tm, const GArgs& a,
+                       unsigned grid, const LaunchCtx& c) {
+    if (V == 4) return dispatch_eh<4>(eh, pc, f16, tm, a, grid, c);
+    if (V == 2) return dispatch_eh<2>(eh, pc, f16, tm, a, grid, c);
+    return dispatch_eh<1>(eh, pc, f16, tm, a, grid, c);
 }
 
 }  // namespace
@@ -423,10 +472,7 @@ cudaError_t gemv_tma_launch_group(const Problem* ps, int count, const LaunchCtx&
     }
     a.row_blocks = blocks;
     const unsigned grid = (unsigned)std::min<int64_t>(blocks, c.sm_count);
-    const bool eh = p0.even_high != 0;
-    if (V == 4) return eh ? launch_v<4, true>(tm, a, grid, c) : launch_v<4, false>(tm, a, grid, c);
-    if (V == 2) return eh ? launch_v<2, true>(tm, a, grid, c) : launch_v<2, false>(tm, a, grid, c);
-    return eh ? launch_v<1, true>(tm, a, grid, c) : launch_v<1, false>(tm, a, grid, c);
+    return dispatch_v(V, p0.even_high != 0, a.per_channel != 0, a.scale_f16 != 0, tm, a, grid, c);
 }
 
 cudaError_t gemv_tma_launch(const Problem& p, const LaunchCtx& c) {

@@ -1,38 +1,39 @@
-// tc_gemm.cu -- tcgen05 tensor-core GEMM of the 4-bit weight-quantized linear (sm_103a).
+// tc_gemm2.cu -- tcgen05 tensor-core GEMM of the 4-bit weight-quantized linear, with the
+// activations as the MMA's A operand (sm_103a).
 //
 //   out[m, n] = bias[n] + sum_k x[m, k] * (code[n, k] - 8) * scale[k / gs, n]
 //
-// (the formula of "[ExecuTorch][WebGPU] Add linear_qcs4w op", Solution; prefill, M > 1,
-// is the regime of "Add 256-thread steel q4gsw prefill GEMM").  The page's kernel stages
-// f32 activations and dequantized weights of a BK = 16 slice in shared memory and
-// accumulates a 64x64 tile on CUDA cores; on GB300 the contraction goes to the 5th-gen
-// tensor cores instead, and what survives of the page's design is its "dequantize once
-// per packed word, read the group scale once" staging (the pwdq variant).
+// (the formula of "[ExecuTorch][WebGPU] Add linear_qcs4w op", Solution; prefill, M > 1, is
+// the regime of "Add 256-thread steel q4gsw prefill GEMM", whose 64x64 CUDA-core tile with
+// a BK = 16 shared-memory slice is replaced here by the 5th-generation tensor cores; what
+// is kept from that page is its dequantize-once staging of the "pwdq" variant: each packed
+// word is widened once per tile and its group scale read once.)
 //
-// Computed as D[n, m] = sum_k A[n, k] * B[m, k] with
-//   A = dequantized weight tile, 128 rows of W (the MMA's M), written by CUDA cores into
-//       shared memory as fp32 (read by the MMA as tf32), K-major, 128-byte swizzle;
-//   B = x tile, bm rows of x (the MMA's N, 16..256), fp32 straight from HBM by TMA
-//       (read as tf32), K-major, 128-byte swizzle;
-//   D = fp32 accumulator in tensor memory (128 lanes x bm columns).
-// tf32 keeps 10 explicit mantissa bits of each operand, so a product carries a relative
-// error below 2^-9 -- inside the 4e-3 * sum|x*w| bar of the tensor-core path.
+// D[m, n] = sum_k A[m, k] * B[n, k] with
+//   A = x tile, 128 rows of x (the MMA's M), fp32 from HBM by TMA with the 128-byte
+//       swizzle, read by the MMA as tf32 (K-major);
+//   B = dequantized weight tile, bn rows of W (the MMA's N, 64..256), written by CUDA
+//       cores into shared memory as fp32 (tf32 to the MMA), K-major, 128-byte swizzle;
+//   D = fp32 accumulator in tensor memory: 128 lanes (m) x bn columns (n).
+// Putting the weights on the MMA's N side keeps the MMAs wide (N = 256) even for a short
+// prompt, and each stage of x (16 KiB) feeds 256 weight rows.  tf32 keeps 10 explicit
+// mantissa bits of each operand: a product carries a relative error below 2^-9, inside
+// the 4e-3 * sum|x*w| bar of the tensor-core path.
 //
-// Roles (320 threads, one CTA per 128 x bm output tile):
-//   warp 0, one lane: TMA producer; per stage (32 k) the x tile [bm x 128 B] and the
-//                     packed weight tile [128 rows x 16 B] land in a 4-stage ring.
-//   warp 1:           allocates tensor memory; one lane issues 4 tcgen05.mma (K = 8
-//                     each) per stage and commits each stage's completion to "empty".
-//   warps 2-9:        two groups of 4 warps, each taking alternate stages (so one
-//                     group's proxy fence and arrive overlap the other's work); one
-//                     thread per weight row: widen 32 codes, multiply by the group
-//                     scale, store the row into the swizzled A stage, fence, arrive on
-//                     "a_ready"; at the end each warp reads its 32-lane slice of D with
-//                     tcgen05.ld (the groups split the columns), adds the bias and
-//                     stores out (predicated m < M, n < N).
-// Every mbarrier wait is bounded in time (%globaltimer).  A wait that runs out records
-// code 1 in the status word; the CTA then stops issuing work, waits for its own copies
-// and MMAs in flight, frees its tensor memory and returns.
+// Roles (320 threads, one CTA per 128 x bn output tile, a ring of 32-k stages):
+//   warp 0, one lane: TMA producer: per stage the x tile [128 x 128 B] and the packed
+//                     weight tile [bn rows x 16 B].
+//   warp 1:           allocates tensor memory; one lane issues 4 tcgen05.mma (K = 8) per
+//                     stage and commits each stage's completion to "empty".
+//   warps 2-9:        two groups of 4 warps taking alternate stages; each thread widens
+//                     the codes of bn/128 weight rows, applies the group scale, writes the
+//                     rows into the swizzled B stage, fences them to the async proxy and
+//                     arrives on "b_ready".  At the end each warp reads its 32 lanes (m)
+//                     of D with tcgen05.ld (the groups split the columns), applies the
+//                     channel scale and bias, and stores out (predicated m < M, n < N).
+// Every mbarrier wait is bounded in time; a timeout records code 1 in the status word,
+// after which the CTA stops issuing work, drains its copies and MMAs, frees its tensor
+// memory and returns.
 #include <algorithm>
 #include <mutex>
 
@@ -43,30 +44,28 @@ namespace q4lin {
 namespace {
 using namespace ptx;
 
-constexpr int kDequantGroups = 2;     // warp groups of 4 that dequantize alternate stages
-constexpr int kThreadsTc = 64 + 128 * kDequantGroups;
-constexpr int kRows = 128;            // weight rows per tile (MMA M)
-constexpr int kStageK = 32;           // k per stage: 32 fp32 = one 128-byte swizzle row
-constexpr int kStages = 4;
-constexpr int kATile = kRows * 128;   // 16 KiB
-constexpr int kWTile = kRows * 16;    // 2 KiB: 32 codes per row
-constexpr int kMaxBm = 256;
-constexpr int64_t kDrainLimitNs = 4000000000LL;
-constexpr int kScaleAhead = 6;        // stages of group scales requested ahead of use
+constexpr int kGroups = 2;                   // dequantizing warp groups (alternate stages)
+constexpr int kThreads2 = 64 + 128 * kGroups;
+constexpr int kXRows = 128;                  // x rows per tile (MMA M)
+constexpr int kStageK = 32;                  // 32 fp32 = one 128-byte swizzle row
+constexpr int kATile = kXRows * 128;         // 16 KiB
+constexpr int kMaxStages = 8;
+constexpr int kScaleAhead = 4;               // stages of scales in flight per thread
+constexpr int64_t kDrainNs = 4000000000LL;
+constexpr int kSmemLimit = 227 * 1024;
 
-constexpr int smem_bytes_for(int bm) {
-    return 1024 + kStages * (kATile + bm * 128 + kWTile) + 256;
-}
+__host__ __device__ constexpr int stage_bytes(int bn) { return kATile + bn * 128 + bn * 16; }
+inline int smem_bytes(int bn, int stages) { return 1024 + stages * stage_bytes(bn) + 256; }
 
-struct TcArgs {
+struct Tc2Args {
     const void* scales;
     const float* bias;
     float* out;
-    int64_t M, N, K, gs;
-    int scale_f16, per_channel, even_high;
-    int bm, k_iters, tmem_cols;
-    int gs_stages;  // group size in stages of 32 k (grouped scales)
-    int gs_shift;   // log2(gs_stages) when a power of two, else -1
+    int64_t M, N, K;
+    int scale_f16, per_channel;
+    int bn, stages, k_iters, tmem_cols;
+    int gs_stages, gs_shift;  // group size in stages; log2 of it or -1
+    int out_vec;              // 16-byte stores of out are aligned
     int* status;
     int64_t wait_ns;
     int skip_first_copy;
@@ -76,53 +75,45 @@ __device__ __forceinline__ float load_scale(const void* scales, int f16, int64_t
     if (f16) return __half2float(__ldg(reinterpret_cast<const __half*>(scales) + idx));
     return __ldg(reinterpret_cast<const float*>(scales) + idx);
 }
-
-// Signed codes (c - 8) of the 8 nibbles of one packed word, in k order (nibble i holds
-// k = i).  0x6400 is binary16 1024; OR-ing a 4-bit code into its mantissa gives 1024 + c,
-// and one mixed-precision add widens it and subtracts 1032, exactly.
-__device__ __forceinline__ void codes8(uint32_t w, float (&v)[8]) {
-    const uint32_t h[4] = {(w & 0x000F000Fu) | 0x64006400u, ((w >> 4) & 0x000F000Fu) | 0x64006400u,
-                           ((w >> 8) & 0x000F000Fu) | 0x64006400u,
-                           ((w >> 12) & 0x000F000Fu) | 0x64006400u};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        asm("{\n\t.reg .b16 l, u;\n\tmov.b32 {l, u}, %2;\n\t"
-            "add.rn.f32.f16 %0, l, %3;\n\tadd.rn.f32.f16 %1, u, %3;\n\t}"
-            : "=f"(v[i]), "=f"(v[i + 4])
-            : "r"(h[i]), "f"(-1032.0f));
-    }
+__device__ __forceinline__ uint32_t load_scale_bits(const void* scales, int f16, int64_t idx) {
+    if (f16) return __ldg(reinterpret_cast<const unsigned short*>(scales) + idx);
+    return __ldg(reinterpret_cast<const unsigned int*>(scales) + idx);
+}
+__device__ __forceinline__ float scale_from_bits(uint32_t bits, int f16) {
+    return f16 ? __half2float(__ushort_as_half((unsigned short)bits)) : __uint_as_float(bits);
 }
 
-__global__ void __launch_bounds__(kThreadsTc, 1)
-    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x,
-                   const __grid_constant__ CUtensorMap tmap_w, const TcArgs a) {
+template <int RPT, bool EH>
+__global__ void __launch_bounds__(kThreads2, 1)
+    tc_xa_kernel(const __grid_constant__ CUtensorMap tmap_x,
+                 const __grid_constant__ CUtensorMap tmap_w, const Tc2Args a) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* gbase = smem_raw + (base - raw);
-    const int bm = a.bm;
+    const int bn = a.bn, S = a.stages;
     const uint32_t a_base = base;
-    const uint32_t b_base = a_base + kStages * kATile;
-    const uint32_t w_base = b_base + kStages * bm * 128;
-    const uint32_t bar_base = w_base + kStages * kWTile;
-    const uint32_t accfull = bar_base + 8 * 3 * kStages;
+    const uint32_t b_base = a_base + S * kATile;
+    const uint32_t w_base = b_base + S * bn * 128;
+    const uint32_t bar_base = w_base + S * bn * 16;
+    const uint32_t accfull = bar_base + 8 * 3 * kMaxStages;
     const uint32_t tmem_slot = accfull + 8;
     uint32_t* tmem_slot_ptr = reinterpret_cast<uint32_t*>(gbase + (tmem_slot - base));
     volatile int* failed = reinterpret_cast<volatile int*>(gbase + (tmem_slot + 4 - base));
     auto full = [&](int s) { return bar_base + 8u * s; };
-    auto aready = [&](int s) { return bar_base + 8u * (kStages + s); };
-    auto empty = [&](int s) { return bar_base + 8u * (2 * kStages + s); };
+    auto bready = [&](int s) { return bar_base + 8u * (kMaxStages + s); };
+    auto empty = [&](int s) { return bar_base + 8u * (2 * kMaxStages + s); };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < S; ++s) {
             mbar_init(full(s), 1);
-            mbar_init(aready(s), 128);  // the 128 threads of the group that owns the stage
+            mbar_init(bready(s), 128);  // the 128 threads of the group that owns the stage
             mbar_init(empty(s), 1);
         }
         mbar_init(accfull, 1);
         *failed = 0;
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        mbar_init_fence();
     }
     if (warp == 1) tmem_alloc(tmem_slot, (uint32_t)a.tmem_cols);
     tc_fence_before();
@@ -134,43 +125,44 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     if (warp == 0) {
         if (lane == 0) {
             // ------------------------------------------------------------ TMA producer
-            const int m0 = (int)blockIdx.y * bm, n0 = (int)blockIdx.x * kRows;
+            prefetch_tensormap(&tmap_x);
+            prefetch_tensormap(&tmap_w);
+            const int m0 = (int)blockIdx.y * kXRows, n0 = (int)blockIdx.x * bn;
+            const uint32_t tx = (uint32_t)(kATile + bn * 16);
             int it = 0;
             for (; it < a.k_iters; ++it) {
-                const int s = it % kStages;
-                if (it >= kStages &&
-                    !wait_bounded(empty(s), ((it / kStages) - 1) & 1, a.wait_ns, failed)) {
+                const int s = it % S;
+                if (it >= S && !wait_bounded(empty(s), ((it / S) - 1) & 1, a.wait_ns, failed)) {
                     record_failure(a.status, failed);
                     break;
                 }
                 if (*failed) break;
                 if (a.skip_first_copy && it == 0) continue;
-                mbar_arrive_expect_tx(full(s), (uint32_t)(bm * 128 + kWTile));
-                tma_load_2d(b_base + s * bm * 128, &tmap_x, it * kStageK, m0, full(s));
-                tma_load_2d(w_base + s * kWTile, &tmap_w, it * (kStageK / 2), n0, full(s));
+                mbar_arrive_expect_tx(full(s), tx);
+                tma_load_2d(a_base + s * kATile, &tmap_x, it * kStageK, m0, full(s));
+                tma_load_2d(w_base + s * bn * 16, &tmap_w, it * (kStageK / 2), n0, full(s));
             }
             // Copies of the last stages may still be landing; the CTA must not exit first.
-            for (int j = it > kStages ? it - kStages : 0; j < it; ++j) {
+            for (int j = it > S ? it - S : 0; j < it; ++j) {
                 if (a.skip_first_copy && j == 0) continue;
-                wait_bounded(full(j % kStages), (j / kStages) & 1, kDrainLimitNs, nullptr);
+                wait_bounded(full(j % S), (j / S) & 1, kDrainNs, nullptr);
             }
         }
     } else if (warp == 1) {
         if (lane == 0) {
             // ------------------------------------------------------------- MMA issuer
-            const uint32_t idesc = tf32_idesc(kRows, bm);
+            const uint32_t idesc = tf32_idesc(kXRows, bn);
             for (int it = 0; it < a.k_iters; ++it) {
-                const int s = it % kStages;
-                const uint32_t par = (it / kStages) & 1;
+                const int s = it % S;
+                const uint32_t par = (it / S) & 1;
                 if (!wait_bounded(full(s), par, a.wait_ns, failed) ||
-                    !wait_bounded(aready(s), par, a.wait_ns, failed)) {
+                    !wait_bounded(bready(s), par, a.wait_ns, failed)) {
                     record_failure(a.status, failed);
                     break;
                 }
-                // The A stage was written through the generic proxy, fenced to the async
-                // proxy by its writers before they arrived; the B stage came by TMA.  The
-                // mbarrier waits above order both before these MMAs.
-                const uint32_t ab = a_base + s * kATile, bb = b_base + s * bm * 128;
+                // B was written through the generic proxy and fenced to the async proxy by
+                // its writers before they arrived; A came by TMA.  The waits order both.
+                const uint32_t ab = a_base + s * kATile, bb = b_base + s * bn * 128;
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
                     mma_tf32(tmem_d, sw128_desc(ab + kk * 32), sw128_desc(bb + kk * 32), idesc,
@@ -182,79 +174,110 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         __syncwarp();
     } else {
         // ------------------------------------------------- dequantization, epilogue
-        const int group = (warp - 2) >> 2;  // dequantizes stages it % kDequantGroups == group
-        const int quarter = warp & 3;       // the 32-lane slice of tensor memory this warp owns
-        const int row = quarter * 32 + lane;
-        const int64_t n = (int64_t)blockIdx.x * kRows + row;
-        const bool row_ok = n < a.N;
-        const uint32_t swz = (uint32_t)(row & 7);
+        const int group = (warp - 2) >> 2;
+        const int tg = ((warp - 2) & 3) * 32 + lane;  // thread within its group
+        const int64_t n0 = (int64_t)blockIdx.x * bn;
         bool ok = true;
-        // Group scales of this row for this group's stages, kScaleAhead of them ahead of
-        // use (a global load takes longer than a stage of MMAs).  The loop is unrolled by
-        // the ring size so each slot is a fixed register (no move of a pending load).
-        float sc_ring[kScaleAhead];
-        auto scale_of = [&](int it) -> float {
-            if (!row_ok) return 0.f;
-            if (a.per_channel || it >= a.k_iters) return 1.f;
-            const int g = a.gs_shift >= 0 ? (it >> a.gs_shift) : it / a.gs_stages;
-            return load_scale(a.scales, a.scale_f16, (int64_t)g * a.N + n);
+        // Rows of the weight tile this thread widens: tg + 128 * i.
+        int64_t nrow[RPT];
+        bool rvalid[RPT];
+#pragma unroll
+        for (int i = 0; i < RPT; ++i) {
+            const int r = tg + 128 * i;
+            nrow[i] = n0 + r;
+            rvalid[i] = r < bn && n0 + r < a.N;
+        }
+        // Group scales (raw bits) of this thread's rows for its group's stages,
+        // kScaleAhead stages ahead; the loop is unrolled by the ring size so every slot
+        // is a fixed register (no move of a pending load).
+        uint32_t ring[kScaleAhead][RPT];
+        auto fetch = [&](int it, uint32_t (&dst)[RPT]) {
+#pragma unroll
+            for (int i = 0; i < RPT; ++i) {
+                uint32_t bits = 0;
+                if (rvalid[i] && !a.per_channel && it < a.k_iters) {
+                    const int g = a.gs_shift >= 0 ? (it >> a.gs_shift) : it / a.gs_stages;
+                    bits = load_scale_bits(a.scales, a.scale_f16, (int64_t)g * a.N + nrow[i]);
+                }
+                dst[i] = bits;
+            }
         };
 #pragma unroll
-        for (int i = 0; i < kScaleAhead; ++i) sc_ring[i] = scale_of(group + i * kDequantGroups);
-        constexpr int kStride = kScaleAhead * kDequantGroups;
+        for (int u = 0; u < kScaleAhead; ++u) fetch(group + u * kGroups, ring[u]);
+        constexpr int kStride = kScaleAhead * kGroups;
         for (int it0 = group; it0 < a.k_iters && ok; it0 += kStride) {
 #pragma unroll
             for (int u = 0; u < kScaleAhead; ++u) {
-                const int it = it0 + u * kDequantGroups;
+                const int it = it0 + u * kGroups;
                 if (it >= a.k_iters) break;
-                const int s = it % kStages;
-                if (!wait_bounded(full(s), (it / kStages) & 1, a.wait_ns, failed)) {
+                const int s = it % S;
+                if (!wait_bounded(full(s), (it / S) & 1, a.wait_ns, failed)) {
                     record_failure(a.status, failed);
                     ok = false;
                     break;
                 }
-                uint4 wv = ld_shared_v4(w_base + s * kWTile + row * 16);
-                if (a.even_high) {
-                    wv.x = ((wv.x & 0x0F0F0F0Fu) << 4) | ((wv.x >> 4) & 0x0F0F0F0Fu);
-                    wv.y = ((wv.y & 0x0F0F0F0Fu) << 4) | ((wv.y >> 4) & 0x0F0F0F0Fu);
-                    wv.z = ((wv.z & 0x0F0F0F0Fu) << 4) | ((wv.z >> 4) & 0x0F0F0F0Fu);
-                    wv.w = ((wv.w & 0x0F0F0F0Fu) << 4) | ((wv.w >> 4) & 0x0F0F0F0Fu);
-                }
-                const float sc = sc_ring[u];
-                sc_ring[u] = scale_of(it + kStride);
-                const uint32_t words[4] = {wv.x, wv.y, wv.z, wv.w};
-                const uint32_t arow = a_base + s * kATile + row * 128;
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    float v[8];
-                    codes8(words[j], v);
+                for (int i = 0; i < RPT; ++i) {
+                    const int r = tg + 128 * i;
+                    if (r >= bn) continue;
+                    const uint4 wv = ld_shared_v4(w_base + s * bn * 16 + r * 16);
+                    float sc = 0.f;
+                    if (rvalid[i]) sc = a.per_channel ? 1.f : scale_from_bits(ring[u][i], a.scale_f16);
+                    const float2 sc2 = make_float2(sc, sc);
+                    const uint32_t words[4] = {wv.x, wv.y, wv.z, wv.w};
+                    const uint32_t brow = b_base + s * bn * 128 + r * 128;
+                    const uint32_t swz = (uint32_t)(r & 7);
 #pragma unroll
-                    for (int t = 0; t < 8; ++t) v[t] *= sc;
-                    st_shared_v4(arow + (((2u * j) ^ swz) << 4), v[0], v[1], v[2], v[3]);
-                    st_shared_v4(arow + (((2u * j + 1) ^ swz) << 4), v[4], v[5], v[6], v[7]);
+                    for (int j = 0; j < 4; ++j) {
+                        float2 c[4];
+                        codes_word<EH>(words[j], c);
+#pragma unroll
+                        for (int t = 0; t < 4; ++t) c[t] = fmul2(c[t], sc2);
+                        st_shared_v4(brow + (((2u * j) ^ swz) << 4), c[0].x, c[0].y, c[1].x, c[1].y);
+                        st_shared_v4(brow + (((2u * j + 1) ^ swz) << 4), c[2].x, c[2].y, c[3].x,
+                                     c[3].y);
+                    }
                 }
+                fetch(it + kStride, ring[u]);
                 fence_proxy_async_smem();
-                mbar_arrive(aready(s));
+                mbar_arrive(bready(s));
             }
         }
-        const bool acc_ok = wait_bounded(accfull, 0, ok ? a.wait_ns : kDrainLimitNs, nullptr);
+        const bool acc_ok = wait_bounded(accfull, 0, ok ? a.wait_ns : kDrainNs, nullptr);
         if (!acc_ok) record_failure(a.status, failed);
         tc_fence_after();
         const bool go = __all_sync(0xffffffffu, acc_ok && !*failed);
         if (go) {
-            const float pc = (a.per_channel && row_ok) ? load_scale(a.scales, a.scale_f16, n) : 1.f;
-            const float bs = (a.bias && row_ok) ? __ldg(a.bias + n) : 0.f;
-            const int64_t m0 = (int64_t)blockIdx.y * bm;
+            const int quarter = warp & 3;  // the 32-lane slice of tensor memory this warp owns
+            const int64_t m = (int64_t)blockIdx.y * kXRows + quarter * 32 + lane;
+            const bool m_ok = m < a.M;
             const uint32_t lane_base = tmem_d + ((uint32_t)(quarter * 32) << 16);
-            for (int c0 = 16 * group; c0 < bm; c0 += 16 * kDequantGroups) {
+            float* orow = a.out + (m_ok ? m : 0) * a.N;
+            for (int c0 = 16 * group; c0 < bn; c0 += 16 * kGroups) {
                 uint32_t r[16];
                 tmem_ld16(lane_base + (uint32_t)c0, r);
-                if (row_ok) {
+                const int64_t nb = n0 + c0;
+                float v[16];
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int64_t m = m0 + c0 + j;
-                        if (m < a.M) a.out[m * a.N + n] = fmaf(__uint_as_float(r[j]), pc, bs);
+                for (int j = 0; j < 16; ++j) {
+                    const int64_t n = nb + j;
+                    float val = __uint_as_float(r[j]);
+                    if (n < a.N) {
+                        if (a.per_channel) val *= load_scale(a.scales, a.scale_f16, n);
+                        if (a.bias) val += __ldg(a.bias + n);
                     }
+                    v[j] = val;
+                }
+                if (!m_ok) continue;
+                if (a.out_vec && nb + 16 <= a.N) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        *reinterpret_cast<float4*>(orow + nb + 4 * q) =
+                            make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        if (nb + j < a.N) orow[nb + j] = v[j];
                 }
             }
         }
@@ -267,7 +290,6 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     }
 }
 
-// ------------------------------------------------------------------------- host side
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                    const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -289,14 +311,25 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-cudaError_t ensure_smem_attr() {
-    static cudaError_t err = cudaErrorNotReady;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        err = cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   smem_bytes_for(kMaxBm));
-    });
-    return err;
+template <int RPT, bool EH>
+cudaError_t launch2(const CUtensorMap& tx, const CUtensorMap& tw, const Tc2Args& a, dim3 grid,
+                    const LaunchCtx& c) {
+    static cudaError_t attr = cudaFuncSetAttribute(
+        tc_xa_kernel<RPT, EH>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+    if (attr != cudaSuccess) return attr;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreads2);
+    cfg.dynamicSmemBytes = smem_bytes(a.bn, a.stages);
+    cfg.stream = c.stream;
+    cudaLaunchAttribute attrs[1];
+    if (c.pdl) {
+        attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attrs[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attrs;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, tc_xa_kernel<RPT, EH>, tx, tw, a);
 }
 
 }  // namespace
@@ -306,66 +339,67 @@ bool tc_eligible(const Problem& p, const LaunchCtx& c) {
     if (reinterpret_cast<uintptr_t>(p.x) % 16 || reinterpret_cast<uintptr_t>(p.qweight) % 16)
         return false;
     if (!(p.group_size >= p.K || p.group_size % kStageK == 0)) return false;
-    if (p.M > 65535LL * kMaxBm) return false;
-    if (c.max_smem_optin < smem_bytes_for(kMaxBm)) return false;
+    if (p.M > 65535LL * kXRows || p.N > (1LL << 31) - 1) return false;
+    if (c.max_smem_optin < smem_bytes(256, 4)) return false;
     return encode_fn() != nullptr;
 }
 
 cudaError_t tc_launch(const Problem& p, const LaunchCtx& c) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
-    cudaError_t e = ensure_smem_attr();
-    if (e != cudaSuccess) return e;
-    // x rows per tile (the MMA's N).  Larger tiles reuse each dequantized weight tile
-    // more; smaller ones give more CTAs.  Estimate waves x cycles per stage, where a
-    // stage costs ~2 * bm cycles of tf32 MMA but no less than the CUDA-core dequant
-    // (~160 cycles for 128 rows x 32 codes on 4 warps), and take the cheapest.
-    const int64_t ntiles = (p.N + kRows - 1) / kRows;
-    int bm = 16;
-    int64_t mtiles = 0, best = -1;
-    for (int cand = kMaxBm; cand >= 16; cand /= 2) {
-        const int64_t mt = (p.M + cand - 1) / cand;
-        if (mt > 65535) continue;
-        const int64_t per_tile = (p.M + mt - 1) / mt;
-        const int b = (int)std::min<int64_t>(cand, (per_tile + 15) / 16 * 16);
-        const int64_t waves = (ntiles * mt + c.sm_count - 1) / c.sm_count;
-        const int64_t cost = waves * std::max<int64_t>(2 * b, 160);
+    // Weight rows per tile (the MMA's N).  Wider tiles make wider MMAs and feed more
+    // weight rows from each 16 KiB stage of x; narrower ones give more CTAs.  Estimate
+    // waves x cycles per stage: an MMA stage costs ~2 * bn cycles, a stage of x must
+    // arrive from L2 (~340 cycles at the L2 bandwidth share of an SM when every SM
+    // streams), and the widening of bn rows needs ~bn cycles of issue.
+    const int64_t mtiles = (p.M + kXRows - 1) / kXRows;
+    int bn = 256;
+    int64_t best = -1;
+    for (int cand = 256; cand >= 64; cand /= 2) {
+        const int64_t ntiles = (p.N + cand - 1) / cand;
+        const int64_t ctas = ntiles * mtiles;
+        const int64_t waves = (ctas + c.sm_count - 1) / c.sm_count;
+        const int64_t busy = std::min<int64_t>(ctas, c.sm_count);
+        const int64_t l2 = 340 * busy / c.sm_count;
+        const int64_t cost = waves * std::max<int64_t>({2LL * cand, l2, (int64_t)cand});
         if (best < 0 || cost < best) {
             best = cost;
-            bm = b;
-            mtiles = mt;
+            bn = cand;
         }
     }
+    int stages = std::min(kMaxStages, (kSmemLimit - 1024 - 256) / stage_bytes(bn));
+    if (stages > c.max_smem_optin / stage_bytes(bn)) stages = c.max_smem_optin / stage_bytes(bn);
+    while (stages > 2 && smem_bytes(bn, stages) > c.max_smem_optin) --stages;
     int cols = 32;
-    while (cols < bm) cols <<= 1;
+    while (cols < bn) cols <<= 1;
 
-    TcArgs a;
+    Tc2Args a;
     a.scales = p.scales;
     a.bias = p.bias;
     a.out = p.out;
     a.M = p.M;
     a.N = p.N;
     a.K = p.K;
-    a.gs = p.group_size;
     a.scale_f16 = p.scale_f16;
     a.per_channel = p.group_size >= p.K;
-    a.even_high = p.even_high;
-    a.bm = bm;
+    a.bn = bn;
+    a.stages = stages;
     a.k_iters = (int)(p.K / kStageK);
     a.tmem_cols = cols;
-    a.status = c.status_word;
-    a.wait_ns = c.wait_limit_ns;
-    a.skip_first_copy = c.tc_skip_first_copy;
     a.gs_stages = a.per_channel ? 1 : (int)(p.group_size / kStageK);
     a.gs_shift = -1;
     for (int sft = 0; sft < 31; ++sft)
         if ((1 << sft) == a.gs_stages) a.gs_shift = sft;
+    a.out_vec = (reinterpret_cast<uintptr_t>(p.out) % 16 == 0) && (p.N % 4 == 0);
+    a.status = c.status_word;
+    a.wait_ns = c.wait_limit_ns;
+    a.skip_first_copy = c.tc_skip_first_copy;
 
     CUtensorMap tx, tw;
     {
         const cuuint64_t dims[2] = {(cuuint64_t)p.K, (cuuint64_t)p.M};
         const cuuint64_t strides[1] = {(cuuint64_t)p.K * 4};
-        const cuuint32_t box[2] = {(cuuint32_t)kStageK, (cuuint32_t)bm};
+        const cuuint32_t box[2] = {(cuuint32_t)kStageK, (cuuint32_t)kXRows};
         const cuuint32_t estr[2] = {1, 1};
         if (enc(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(p.x), dims, strides,
                 box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -376,27 +410,18 @@ cudaError_t tc_launch(const Problem& p, const LaunchCtx& c) {
         const int64_t Kp = p.K / 2;
         const cuuint64_t dims[2] = {(cuuint64_t)Kp, (cuuint64_t)p.N};
         const cuuint64_t strides[1] = {(cuuint64_t)Kp};
-        const cuuint32_t box[2] = {(cuuint32_t)(kStageK / 2), (cuuint32_t)kRows};
+        const cuuint32_t box[2] = {(cuuint32_t)(kStageK / 2), (cuuint32_t)bn};
         const cuuint32_t estr[2] = {1, 1};
         if (enc(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(p.qweight), dims,
                 strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
-
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((p.N + kRows - 1) / kRows), (unsigned)mtiles);
-    cfg.blockDim = dim3(kThreadsTc);
-    cfg.dynamicSmemBytes = smem_bytes_for(bm);
-    cfg.stream = c.stream;
-    cudaLaunchAttribute attr[1];
-    if (c.pdl) {
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-    }
-    return cudaLaunchKernelEx(&cfg, tc_gemm_kernel, tx, tw, a);
+    const dim3 grid((unsigned)((p.N + bn - 1) / bn), (unsigned)mtiles);
+    const bool eh = p.even_high != 0;
+    if (bn > 128)
+        return eh ? launch2<2, true>(tx, tw, a, grid, c) : launch2<2, false>(tx, tw, a, grid, c);
+    return eh ? launch2<1, true>(tx, tw, a, grid, c) : launch2<1, false>(tx, tw, a, grid, c);
 }
 
 }  // namespace q4lin
