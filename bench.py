@@ -156,49 +156,84 @@ def max_over_ranks(value, world, device=None):
 
 
 # ------------------------------------------------------------------------- our workload
-class DecodeToken:
-    """Device buffers of one model's decode token and the q4lin_run calls over them."""
+# Projections of a layer that read the same activation (fused into one launch).
+SHARED_INPUT = ({"q", "k", "v"}, {"gate", "up"})
 
-    def __init__(self, handle, model, device, seed_base=1000):
+
+def token_groups(model):
+    """Consecutive shapes of a token that read the same x: [[(name, N, K), ...], ...]."""
+    groups = []
+    for name, N, K in token_shapes(model):
+        base = name.rstrip("0123456789")
+        if groups:
+            prev = groups[-1][-1][0].rstrip("0123456789")
+            same_layer = name[len(base):] == groups[-1][-1][0][len(prev):]
+            if same_layer and any(base in g and prev in g for g in SHARED_INPUT):
+                groups[-1].append((name, N, K))
+                continue
+        groups.append([(name, N, K)])
+    return groups
+
+
+class DecodeToken:
+    """Device buffers of one model's decode token and the q4lin calls over them.
+
+    Each group of projections that read the same activation (q/k/v, gate/up) has one x
+    buffer and runs as one q4lin_run_grouped call (or as separate q4lin_run calls with
+    grouped=False).  Every projection has its own weight, scale and output buffers."""
+
+    def __init__(self, handle, model, device, seed_base=1000, grouped=True):
         import torch
         self.torch = torch
         self.h = handle
-        self.shapes = token_shapes(model)
-        self.bufs = []
+        self.grouped = grouped
+        self.groups = token_groups(model)
         gen = torch.Generator(device=device)
-        for i, (name, N, K) in enumerate(self.shapes):
-            gen.manual_seed(seed_base * 1 + i)
-            w = torch.randint(0, 256, (N, (K + 1) // 2), dtype=torch.uint8, device=device,
-                              generator=gen)
-            s = (torch.rand((-(-K // GROUP), N), device=device, generator=gen) * 0.015
-                 + 0.005).to(torch.float16)
-            self.bufs.append((N, K, w, s))
+        self.bufs = []  # per group: list of (N, K, w, s, out_offset)
+        x_sizes, oo, i = [], 0, 0
+        for grp in self.groups:
+            entries = []
+            for name, N, K in grp:
+                gen.manual_seed(seed_base + i)
+                i += 1
+                w = torch.randint(0, 256, (N, (K + 1) // 2), dtype=torch.uint8, device=device,
+                                  generator=gen)
+                s = (torch.rand((-(-K // GROUP), N), device=device, generator=gen) * 0.015
+                     + 0.005).to(torch.float16)
+                entries.append((N, K, w, s, oo))
+                oo += N
+            self.bufs.append(entries)
+            x_sizes.append(grp[0][2])
         # All activations of a token in one buffer, all outputs in another, so an
         # end-to-end step is one host->device and one device->host copy.
-        self.x_offsets, self.out_offsets = [], []
-        xo = oo = 0
-        for N, K, _, _ in self.bufs:
-            self.x_offsets.append(xo)
-            self.out_offsets.append(oo)
-            xo += K
-            oo += N
-        self.x_all = torch.randn(xo, device=device, generator=gen)
+        self.x_offsets = [sum(x_sizes[:g]) for g in range(len(x_sizes))]
+        self.x_all = torch.randn(sum(x_sizes), device=device, generator=gen)
         self.out_all = torch.empty(oo, device=device)
-        self.bytes = sum(gemv_bytes(N, K) for N, K, _, _ in self.bufs)
-        self.launches = len(self.bufs)
+        self.bytes = sum(
+            sum(N * ((K + 1) // 2) + (-(-K // GROUP)) * N * 2 + 4 * N for N, K, _, _, _ in entries)
+            + 4 * entries[0][1] for entries in self.bufs)
+        self.gemvs = sum(len(e) for e in self.bufs)
+        self.launches = len(self.bufs) if grouped else self.gemvs
 
     def run(self, stream_ptr):
         from bit_weight_quantized_int4_gb300 import q4lin as q
         xb, ob = self.x_all.data_ptr(), self.out_all.data_ptr()
-        for (N, K, w, s), xo, oo in zip(self.bufs, self.x_offsets, self.out_offsets):
-            st = q.q4lin_run(self.h, xb + 4 * xo, w.data_ptr(), s.data_ptr(), None,
-                             ob + 4 * oo, 1, N, K, GROUP, q.Q4LIN_SCALE_F16, stream_ptr)
+        for entries, xo in zip(self.bufs, self.x_offsets):
+            probs = [(xb + 4 * xo, w.data_ptr(), s.data_ptr(), None, ob + 4 * oo, 1, N, K, GROUP,
+                      q.Q4LIN_SCALE_F16) for N, K, w, s, oo in entries]
+            if self.grouped and len(probs) > 1:
+                st = q.q4lin_run_grouped(self.h, probs, stream_ptr)
+            else:
+                for pr in probs:
+                    st = q.q4lin_run(self.h, *pr, stream_ptr)
+                    if st != q.Q4LIN_OK:
+                        break
             if st != q.Q4LIN_OK:
                 raise q.Q4LinError(st, "q4lin_run")
 
     def head_output(self):
-        N = self.bufs[-1][0]
-        return self.out_all[self.out_offsets[-1]:self.out_offsets[-1] + N]
+        N, _, _, _, oo = self.bufs[-1][-1]
+        return self.out_all[oo:oo + N]
 
     def capture(self):
         torch = self.torch
@@ -264,7 +299,8 @@ def measure_e2e(torch, token, graph, steps, warmup):
 
 def shape_bandwidth(torch, handle, N, K, reps=30, l2_bytes=129 << 20):
     """GB/s of one GEMV shape in isolation: enough weight copies rotated that each launch
-    streams from HBM; CUDA events around `reps` launches."""
+    streams from HBM; `reps` launches captured in a CUDA graph (device time, without host
+    launch overhead), CUDA events around the replay."""
     from bit_weight_quantized_int4_gb300 import q4lin as q
     b = gemv_bytes(N, K)
     copies = max(2, -(-3 * l2_bytes // b))
@@ -272,28 +308,34 @@ def shape_bandwidth(torch, handle, N, K, reps=30, l2_bytes=129 << 20):
     ss = [(torch.rand((K // GROUP, N), device="cuda") * 0.015 + 0.005).half() for _ in range(copies)]
     x = torch.randn(K, device="cuda")
     out = torch.empty(N, device="cuda")
-    stream = torch.cuda.Stream()
-    sp = stream.cuda_stream
 
-    def launch(i):
+    def launch(i, sp):
         st = q.q4lin_run(handle, x.data_ptr(), ws[i % copies].data_ptr(),
                          ss[i % copies].data_ptr(), None, out.data_ptr(), 1, N, K, GROUP,
                          q.Q4LIN_SCALE_F16, sp)
         assert st == q.Q4LIN_OK
 
+    side = torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        for i in range(copies):
+            launch(i, side.cuda_stream)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(reps):
+            launch(i, torch.cuda.current_stream().cuda_stream)
+    stream = torch.cuda.Stream()
     with torch.cuda.stream(stream):
-        for i in range(5):
-            launch(i)
+        g.replay()
     torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         start.record(stream)
-        for i in range(reps):
-            launch(i)
+        g.replay()
         end.record(stream)
     end.synchronize()
     us = start.elapsed_time(end) * 1000 / reps
-    del ws, ss
+    del ws, ss, g
     return {"N": N, "K": K, "us": round(us, 3), "GB_s": round(b / us / 1e3, 1)}
 
 
@@ -382,12 +424,23 @@ def run_reference(args, world, rank):
     return 0
 
 
+def token_bytes(model):
+    """Algorithmic bytes of one decode token: every packed weight, scale and output once,
+    and each activation once per group of projections that share it."""
+    total = 0
+    for grp in token_groups(model):
+        total += 4 * grp[0][2]
+        for _, N, K in grp:
+            total += N * ((K + 1) // 2) + (-(-K // GROUP)) * N * 2 + 4 * N
+    return total
+
+
 def workload_config(model):
     shapes = token_shapes(model)
-    b = sum(gemv_bytes(N, K) for _, N, K in shapes)
+    b = token_bytes(model)
     return {"workload": f"{MODELS[model]['desc']}: {len(shapes)} q4 GEMVs (M=1, group 32, "
                         f"fp16 scales, distinct buffers per layer), {b / 1e6:.1f} MB per token",
-            "bytes_per_step": b, "launches_per_step": len(shapes),
+            "bytes_per_step": b, "gemvs_per_step": len(shapes),
             "l2": "inputs larger than L2 (129 MB): every token streams from HBM; no flush",
             "parallelism": "replicas"}
 
@@ -398,6 +451,56 @@ def load_peaks():
         p = json.load(open(path))
         return p["hbm_gbs"], p.get("bf16_tflops"), "measured"
     return 6800.0, 1900.0, "fallback"
+
+
+CROSSOVER_M = (1, 2, 3, 4, 5, 7, 8, 12, 16, 24, 32, 33, 48, 64, 96, 128, 256, 512)
+CROSSOVER_NK = ((2048, 2048), (8192, 2048), (2048, 8192), (128256, 2048), (1000, 2048))
+
+
+def crossover():
+    """Device time (CUDA graph replay) of each forced path over M for several (N, K)."""
+    import torch
+    from bit_weight_quantized_int4_gb300 import q4lin as q
+    h = q.q4lin_create(0)
+    table = []
+    for N, K in CROSSOVER_NK:
+        w = torch.randint(0, 256, (N, K // 2), dtype=torch.uint8, device="cuda")
+        s = (torch.rand((K // GROUP, N), device="cuda") * 0.015 + 0.005).half()
+        for M in CROSSOVER_M:
+            x = torch.randn(M, K, device="cuda")
+            out = torch.empty(M, N, device="cuda")
+            row = {"N": N, "K": K, "M": M}
+            for name, path in (("gemv", q.Q4LIN_PATH_GEMV), ("tc", q.Q4LIN_PATH_TC)):
+                q.q4lin_set_option(h, q.Q4LIN_OPT_FORCE_PATH, path)
+                args = (x.data_ptr(), w.data_ptr(), s.data_ptr(), None, out.data_ptr(), M, N, K,
+                        GROUP, q.Q4LIN_SCALE_F16)
+                st, _ = q.q4lin_plan(h, *args)
+                if st != q.Q4LIN_OK:
+                    row[name + "_us"] = None
+                    continue
+                side = torch.cuda.Stream()
+                with torch.cuda.stream(side):
+                    q.q4lin_run(h, *args, side.cuda_stream)
+                torch.cuda.synchronize()
+                g = torch.cuda.CUDAGraph()
+                reps = 10
+                with torch.cuda.graph(g):
+                    for _ in range(reps):
+                        q.q4lin_run(h, *args, torch.cuda.current_stream().cuda_stream)
+                g.replay()
+                torch.cuda.synchronize()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                g.replay()
+                e1.record()
+                e1.synchronize()
+                row[name + "_us"] = round(e0.elapsed_time(e1) * 1000 / reps, 2)
+                del g
+            q.q4lin_set_option(h, q.Q4LIN_OPT_FORCE_PATH, q.Q4LIN_PATH_AUTO)
+            table.append(row)
+            print(json.dumps(row), flush=True)
+    q.q4lin_destroy(h)
+    return 0
 
 
 def profile(spec):
@@ -431,15 +534,23 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true")
+    ap.add_argument("--no-group", action="store_true",
+                    help="run every projection as its own q4lin_run call (113 launches per "
+                         "1B token) instead of fusing those that share an input")
     ap.add_argument("--pdl", type=int, default=1, choices=[0, 1],
                     help="launch with programmatic dependent launch (kernels start "
                          "streaming weights while the previous one drains)")
+    ap.add_argument("--crossover", action="store_true",
+                    help="time the CUDA-core and tensor-core paths over M and print the "
+                         "measured table (JSON) instead of the benchmark line")
     ap.add_argument("--profile", default=None,
                     help="run a few launches of one op and exit (for ncu): gemv:N:K, "
                          "prefill:M:N:K or token:1b|8b")
     args = ap.parse_args()
     if args.profile:
         return profile(args.profile)
+    if args.crossover:
+        return crossover()
     world, rank, local = dist_setup(args)
     if args.impl == "reference":
         return run_reference(args, world, rank)
@@ -450,7 +561,7 @@ def main():
     h = q.q4lin_create(local)
     q.q4lin_set_option(h, q.Q4LIN_OPT_PDL, args.pdl)
 
-    token = DecodeToken(h, "1b", "cuda")
+    token = DecodeToken(h, "1b", "cuda", grouped=not args.no_group)
     graph = token.capture()
     with ClockSampler(local) as clk:
         ms = time_graph(torch, graph, args.steps, args.warmup, world)
@@ -466,12 +577,13 @@ def main():
 
     extra = {}
     if not args.no_extra and rank == 0:
-        tok8 = DecodeToken(h, "8b", "cuda", seed_base=2000)
+        tok8 = DecodeToken(h, "8b", "cuda", seed_base=2000, grouped=not args.no_group)
         g8 = tok8.capture()
         ms8 = time_graph(torch, g8, max(5, args.steps // 4), 3, 1)
         extra["decode_8b"] = {"ms_per_token": round(ms8, 4),
                               "GB_s": round(tok8.bytes / (ms8 * 1e-3) / 1e9, 1),
-                              "bytes_per_token": tok8.bytes, "launches": tok8.launches}
+                              "bytes_per_token": tok8.bytes, "launches": tok8.launches,
+                              "gemvs": tok8.gemvs}
         del g8, tok8
         torch.cuda.empty_cache()
         seen, shapes = set(), []
@@ -488,17 +600,19 @@ def main():
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max, 4),
         "ms_per_token": round(ms_max, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": dict(workload_config("1b"), pdl=bool(args.pdl)),
+        "config": dict(workload_config("1b"), pdl=bool(args.pdl), grouped=not args.no_group,
+                       launches_per_step=token.launches),
         "roofline": {"bound": "hbm", "achieved": round(per_gpu_gbs, 1), "peak": hbm_peak,
                      "unit": "GB/s", "frac": round(per_gpu_gbs / hbm_peak, 4),
                      "traffic": None,
-                     "kernel": "gemv_kernel (all 113 launches of a token; launch gaps "
-                               "included)", "peak_source": peak_src},
+                     "kernel": f"gemv_tma_kernel (all {token.launches} launches of a token; "
+                               "launch gaps included)", "peak_source": peak_src},
         "e2e": {"value": round(token.bytes * world / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "clocks": clocks,
         "gpu_launches": token.launches * args.steps,
+        "gemvs_per_step": token.gemvs,
     }
     if extra:
         line["extra"] = extra

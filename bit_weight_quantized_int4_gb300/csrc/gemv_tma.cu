@@ -41,7 +41,7 @@ constexpr int kCThreads = 32 * kCWarps;
 constexpr int kThreadsG = kCThreads + 32;  // + the producer warp
 constexpr int kSliceBytes = 256;           // packed bytes per row per tile
 constexpr int kSliceK = 512;
-constexpr int kStagesG = 4;
+constexpr int kRingBytes = 128 * 1024;      // weight tiles in flight per SM
 constexpr int kScaleRing = 4;              // tiles of scales in flight per thread
 constexpr int kXPad = 36;                  // floats per 32-float x chunk in shared memory
 constexpr int64_t kDrainNs = 4000000000LL;
@@ -72,13 +72,51 @@ struct GArgs {
     int gs_chunks;  // group size / 32 (grouped scales)
     int gs_shift;   // log2(gs_chunks) when a power of two, else -1
     int64_t row_blocks;
+    // Split K: each row block's k-slices are cut into `parts` runs of `tpp` slices; a work
+    // item is (row block, part).  With parts > 1 the items write partial row sums to
+    // ws[part * ws_rows + row] and the last item of a row block (ticket count) adds them
+    // in part order, so the result does not depend on which CTA finishes last.
+    int parts, tpp;
+    int items;
+    float* ws;       // [parts, ws_rows] partial sums (parts > 1)
+    int* tickets;    // [row_blocks], zero between launches (the last item resets its own)
+    int64_t ws_rows; // row_blocks * rows per block
     int* status;
     int64_t wait_ns;
 };
 
+// A CTA's walk over its work items: item = blockIdx.x + i * gridDim.x, item -> (row block
+// blk = item / parts, part), covering k-slices [part * tpp, min((part + 1) * tpp, kslices)).
+// One division per item, none per tile.
+struct Cursor {
+    int item, blk, part, ks, ks_end;
+    __device__ __forceinline__ void set(const GArgs& a) {
+        blk = item / a.parts;
+        part = item - blk * a.parts;
+        ks = part * a.tpp;
+        ks_end = min(ks + a.tpp, a.kslices);
+    }
+    __device__ __forceinline__ void start(const GArgs& a) {
+        item = (int)blockIdx.x;
+        if (item < a.items) set(a);
+    }
+    __device__ __forceinline__ bool valid(const GArgs& a) const { return item < a.items; }
+    // Move to the next tile; true when that finished the current item.
+    __device__ __forceinline__ bool advance(const GArgs& a) {
+        if (++ks < ks_end) return false;
+        item += gridDim.x;
+        if (item < a.items) set(a);
+        return true;
+    }
+};
+
+// Ring depth for row blocks of rb rows: always kRingBytes of tiles (4, 8 or 16 stages).
+__host__ __device__ constexpr int stages_for(int rb) { return kRingBytes / (rb * kSliceBytes); }
 // Shared memory: the stage ring, the barriers, then x (padded chunks of 32 floats).
-__host__ __device__ constexpr int ring_bytes(int rb) { return kStagesG * rb * kSliceBytes; }
-__host__ __device__ constexpr int x_offset(int rb) { return ring_bytes(rb) + 16 * kStagesG + 16; }
+__host__ __device__ constexpr int ring_bytes(int rb) { return stages_for(rb) * rb * kSliceBytes; }
+__host__ __device__ constexpr int x_offset(int rb) {
+    return ring_bytes(rb) + 16 * stages_for(rb) + 16;
+}
 inline int smem_bytes_g(int rb, int64_t K) {
     return 128 + x_offset(rb) + (int)((K + kSliceK - 1) / kSliceK * 16) * kXPad * 4;
 }
@@ -149,6 +187,8 @@ __global__ void __launch_bounds__(kThreadsG, 1)
     gemv_tma_kernel(const __grid_constant__ TensorMaps tmaps, const GArgs a) {
     constexpr int rb = 32 * V;  // rows per block: 32 row groups of V rows
     constexpr uint32_t tile_bytes = rb * kSliceBytes;
+    constexpr int kStagesG = stages_for(rb);
+    static_assert((kStagesG & (kStagesG - 1)) == 0, "ring depth must be a power of two");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 127u) & ~127u;
@@ -156,6 +196,7 @@ __global__ void __launch_bounds__(kThreadsG, 1)
     const uint32_t bar_base = base + ring_bytes(rb);
     volatile int* failed =
         reinterpret_cast<volatile int*>(gbase + (bar_base + 16 * kStagesG - base));
+    volatile int* s_ticket = failed + 1;  // last-item decision, broadcast to the consumers
     float* xs = reinterpret_cast<float*>(gbase + x_offset(rb));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     auto full = [&](int s) { return bar_base + 8u * s; };
@@ -177,31 +218,26 @@ __global__ void __launch_bounds__(kThreadsG, 1)
         if (lane == 0) {
             for (int q = 0; q < a.nmat; ++q) prefetch_tensormap(&tmaps.m[q]);
             int t = 0;
-            bool stop = false;
-            for (int64_t blk = blockIdx.x; blk < a.row_blocks && !stop; blk += gridDim.x) {
-                for (int ks = 0; ks < a.kslices; ++ks) {
-                    const int s = t & (kStagesG - 1);
-                    if (t >= kStagesG &&
-                        !wait_bounded(empty(s), (uint32_t)((t / kStagesG) - 1) & 1, a.wait_ns,
-                                      failed)) {
-                        record_failure(a.status, failed);
-                        stop = true;
-                        break;
-                    }
-                    if (*failed) {
-                        stop = true;
-                        break;
-                    }
-                    const int mi = mat_of(a, blk);
-                    mbar_arrive_expect_tx(full(s), tile_bytes);
-                    tma_load_2d(base + s * tile_bytes, &tmaps.m[mi], ks * kSliceBytes,
-                                (int)((blk - a.mat[mi].blk_begin) * rb), full(s));
-                    ++t;
+            Cursor cur;
+            cur.start(a);
+            while (cur.valid(a)) {
+                const int s = t & (kStagesG - 1);
+                if (t >= kStagesG &&
+                    !wait_bounded(empty(s), (uint32_t)((t / kStagesG) - 1) & 1, a.wait_ns, failed)) {
+                    record_failure(a.status, failed);
+                    break;
                 }
+                if (*failed) break;
+                const int mi = mat_of(a, cur.blk);
+                mbar_arrive_expect_tx(full(s), tile_bytes);
+                tma_load_2d(base + s * tile_bytes, &tmaps.m[mi], cur.ks * kSliceBytes,
+                            (int)((cur.blk - a.mat[mi].blk_begin) * rb), full(s));
+                ++t;
+                cur.advance(a);
             }
             // The last armed tiles may still be landing; the CTA must not exit first.
-            for (int j = t > kStagesG ? t - kStagesG : 0; j < t; ++j)
-                wait_bounded(full(j & (kStagesG - 1)), (uint32_t)(j / kStagesG) & 1, kDrainNs,
+            for (int q = t > kStagesG ? t - kStagesG : 0; q < t; ++q)
+                wait_bounded(full(q & (kStagesG - 1)), (uint32_t)(q / kStagesG) & 1, kDrainNs,
                              nullptr);
         }
         return;
@@ -217,16 +253,19 @@ __global__ void __launch_bounds__(kThreadsG, 1)
     // a register whose load is in flight would wait for the load).  The first loads go
     // out before griddep_wait: scales do not depend on the preceding kernel.  Tile
     // coordinates advance incrementally (no integer division in the loop).
-    const int tiles_mine =
-        (int)((a.row_blocks - blockIdx.x + gridDim.x - 1) / gridDim.x) * a.kslices;
-    int pf_ks = 0, pf_t = 0;
-    int64_t pf_blk = blockIdx.x;
+    int tiles_mine = 0;
+    for (int it = blockIdx.x; it < a.items; it += gridDim.x) {
+        const int part = it % a.parts;
+        tiles_mine += min(a.tpp, a.kslices - part * a.tpp);
+    }
+    Cursor pf;
+    pf.start(a);
     auto fetch_next = [&](uint32_t (&dst)[V]) {
-        if (!PC && pf_t < tiles_mine) {
-            const int chunk = pf_ks * 16 + j;
-            const int mi = mat_of(a, pf_blk);
+        if (!PC && pf.valid(a)) {
+            const int chunk = pf.ks * 16 + j;
+            const int mi = mat_of(a, pf.blk);
             const MatArgs& m = a.mat[mi];
-            const int64_t n0 = (pf_blk - m.blk_begin) * rb + r0;
+            const int64_t n0 = (pf.blk - m.blk_begin) * rb + r0;
             if (chunk < a.k_chunks) {
                 const int g = a.gs_shift >= 0 ? (chunk >> a.gs_shift) : chunk / a.gs_chunks;
                 const int64_t bi = (int64_t)g * m.N + n0;
@@ -243,11 +282,7 @@ __global__ void __launch_bounds__(kThreadsG, 1)
                 for (int v = 0; v < V; ++v) dst[v] = 0u;
             }
         }
-        ++pf_t;
-        if (++pf_ks == a.kslices) {
-            pf_ks = 0;
-            pf_blk += gridDim.x;
-        }
+        if (pf.valid(a)) pf.advance(a);
     };
     uint32_t sc[kScaleRing][V];
 #pragma unroll
@@ -268,24 +303,26 @@ __global__ void __launch_bounds__(kThreadsG, 1)
     float2 acc[V];
 #pragma unroll
     for (int v = 0; v < V; ++v) acc[v] = make_float2(0.f, 0.f);
-    int ks = 0;
-    int64_t blk = blockIdx.x;
+    Cursor cur;
+    cur.start(a);
     const float* xrow = xs + j * kXPad;
-    for (int t0 = 0; t0 < tiles_mine; t0 += kScaleRing) {
+    bool dead = false;
+    for (int t0 = 0; t0 < tiles_mine && !dead; t0 += kScaleRing) {
 #pragma unroll
         for (int u = 0; u < kScaleRing; ++u) {
             const int t = t0 + u;
             if (t >= tiles_mine) break;
             const int s = t & (kStagesG - 1);
             float4 xv[8];
-            const float* xc = xrow + ks * (16 * kXPad);
+            const float* xc = xrow + cur.ks * (16 * kXPad);
 #pragma unroll
             for (int i = 0; i < 8; ++i) xv[i] = *reinterpret_cast<const float4*>(xc + 4 * i);
             const bool got = __all_sync(
                 0xffffffffu, wait_bounded(full(s), (uint32_t)(t / kStagesG) & 1, a.wait_ns, failed));
             if (!got) {
                 if (lane == 0) record_failure(a.status, failed);
-                return;
+                dead = true;
+                break;
             }
             const uint32_t wrow = base + s * tile_bytes + r0 * kSliceBytes + j * 16;
 #pragma unroll
@@ -302,10 +339,11 @@ __global__ void __launch_bounds__(kThreadsG, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(empty(s));
             fetch_next(sc[u]);
-            if (++ks == a.kslices) {
-                // Row block done: undo the factor 16 of the high-nibble lane, reduce the
-                // 16 chunk lanes of each row, store.
-                ks = 0;
+            const int blk = cur.blk;
+            const int part = cur.part;
+            if (cur.advance(a)) {
+                // Item done: undo the factor 16 of the high-nibble lane, reduce the 16
+                // chunk lanes of each row; store (or hand the partial to the last item).
                 float tot[V];
 #pragma unroll
                 for (int v = 0; v < V; ++v) {
@@ -321,12 +359,30 @@ __global__ void __launch_bounds__(kThreadsG, 1)
                     if (j == v) mine = tot[v];
                 const MatArgs& m = a.mat[mat_of(a, blk)];
                 const int64_t n = (blk - m.blk_begin) * rb + r0 + j;
-                if (j < V && n < m.N) {
+                const int64_t vrow = (int64_t)blk * rb + r0 + j;  // row in the virtual row space
+                bool finish = true;
+                if (a.parts > 1) {
+                    if (j < V) a.ws[(int64_t)part * a.ws_rows + vrow] = mine;
+                    __threadfence();
+                    asm volatile("bar.sync 1, %0;" ::"r"(kCThreads) : "memory");
+                    if (threadIdx.x == 0) *s_ticket = atomicAdd(a.tickets + blk, 1);
+                    asm volatile("bar.sync 1, %0;" ::"r"(kCThreads) : "memory");
+                    finish = *s_ticket == a.parts - 1;
+                    if (finish) {
+                        __threadfence();
+                        if (j < V) {
+                            mine = 0.f;
+                            for (int q = 0; q < a.parts; ++q)
+                                mine += __ldcg(a.ws + (int64_t)q * a.ws_rows + vrow);
+                        }
+                        if (threadIdx.x == 0) a.tickets[blk] = 0;
+                    }
+                }
+                if (finish && j < V && n < m.N) {
                     if (PC) mine *= scale_value<F16>(scale_bits<F16>(m.scales, n));
                     if (m.bias) mine += __ldg(m.bias + n);
                     m.out[n] = mine;
                 }
-                blk += gridDim.x;
             }
         }
     }
@@ -471,7 +527,24 @@ cudaError_t gemv_tma_launch_group(const Problem* ps, int count, const LaunchCtx&
         tm.m[i] = tm.m[count - 1];
     }
     a.row_blocks = blocks;
-    const unsigned grid = (unsigned)std::min<int64_t>(blocks, c.sm_count);
+    // Split K when the row blocks alone would leave SMs idle (the widening is ALU work,
+    // so every SM should get a share), if the handle's workspace can hold the partials.
+    // The partial-sum handoff costs a dependent round trip through L2, so a part keeps at
+    // least 8 k-slices (4096 k): only long rows are split.
+    a.parts = 1;
+    if (blocks < c.sm_count && c.ws && c.tickets) {
+        int parts = (int)std::min<int64_t>(c.sm_count / blocks, a.kslices / 8);
+        while (parts > 1 && ((int64_t)parts * blocks * rb > c.ws_floats || blocks > c.ticket_count))
+            --parts;
+        a.parts = std::max(parts, 1);
+    }
+    a.tpp = (a.kslices + a.parts - 1) / a.parts;
+    a.parts = (a.kslices + a.tpp - 1) / a.tpp;  // no empty part
+    a.items = (int)(blocks * a.parts);
+    a.ws = c.ws;
+    a.tickets = c.tickets;
+    a.ws_rows = blocks * rb;
+    const unsigned grid = (unsigned)std::min<int64_t>(a.items, c.sm_count);
     return dispatch_v(V, p0.even_high != 0, a.per_channel != 0, a.scale_f16 != 0, tm, a, grid, c);
 }
 

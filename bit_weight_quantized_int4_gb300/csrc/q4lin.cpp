@@ -27,11 +27,16 @@ struct q4lin_handle {
     int64_t wait_limit = 0;  // ns; 0: default
     int tc_skip_first_copy = 0;
     int* d_status = nullptr;
+    float* d_ws = nullptr;     // split-K partial sums
+    int* d_tickets = nullptr;  // split-K row-block counters (zero between launches)
 };
 
 namespace {
 
 constexpr int64_t kDefaultWaitLimit = 2000000000LL;  // 2 s of GPU global time
+// Scratch of a handle: partial sums of split-K launches and their row-block counters.
+constexpr int64_t kWsFloats = 1 << 19;   // 2 MiB
+constexpr int64_t kTickets = 1 << 14;    // 64 KiB
 
 // Crossover: at and above this M the tensor-core GEMM replaces the row-streaming
 // CUDA-core kernel (when both are eligible).  Measured on GB300; see plan().
@@ -116,6 +121,10 @@ q4lin::LaunchCtx make_ctx(q4lin_handle_t h, cudaStream_t stream) {
     c.status_word = h->d_status;
     c.wait_limit_ns = h->wait_limit > 0 ? h->wait_limit : kDefaultWaitLimit;
     c.tc_skip_first_copy = h->tc_skip_first_copy;
+    c.ws = h->d_ws;
+    c.ws_floats = kWsFloats;
+    c.tickets = h->d_tickets;
+    c.ticket_count = kTickets;
     return c;
 }
 
@@ -176,8 +185,14 @@ q4lin_status_t q4lin_create(q4lin_handle_t* handle, int device) {
     {
         DeviceGuard g(device);
         if (!g.ok() || cudaMalloc(&h->d_status, sizeof(int)) != cudaSuccess ||
-            cudaMemset(h->d_status, 0, sizeof(int)) != cudaSuccess) {
+            cudaMemset(h->d_status, 0, sizeof(int)) != cudaSuccess ||
+            cudaMalloc(&h->d_ws, kWsFloats * sizeof(float)) != cudaSuccess ||
+            cudaMalloc(&h->d_tickets, kTickets * sizeof(int)) != cudaSuccess ||
+            cudaMemset(h->d_tickets, 0, kTickets * sizeof(int)) != cudaSuccess ||
+            cudaDeviceSynchronize() != cudaSuccess) {
             if (h->d_status) cudaFree(h->d_status);
+            if (h->d_ws) cudaFree(h->d_ws);
+            if (h->d_tickets) cudaFree(h->d_tickets);
             delete h;
             return Q4LIN_ERR_CUDA;
         }
@@ -191,6 +206,8 @@ q4lin_status_t q4lin_destroy(q4lin_handle_t h) {
     {
         DeviceGuard g(h->device);
         if (h->d_status) cudaFree(h->d_status);
+        if (h->d_ws) cudaFree(h->d_ws);
+        if (h->d_tickets) cudaFree(h->d_tickets);
     }
     delete h;
     return Q4LIN_OK;

@@ -28,6 +28,10 @@ struct LaunchCtx {
     int* status_word;        // device int, first nonzero code a kernel records
     int64_t wait_limit_ns;   // time limit of bounded device-side waits
     int tc_skip_first_copy;  // test hook: the TC producer skips stage 0
+    float* ws;               // scratch for split-K partial sums (may be null)
+    int64_t ws_floats;
+    int* tickets;            // per-row-block counters, zero between launches (may be null)
+    int64_t ticket_count;
 };
 
 // Row-streaming CUDA-core kernel (decode GEMV, and small M with weight reuse across a

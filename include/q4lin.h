@@ -20,12 +20,16 @@
  * Conventions for every entry point:
  *   - Every buffer is owned by the caller.  q4lin_run allocates nothing, never
  *     synchronizes the device and only enqueues kernels on the given stream.  A handle
- *     owns its options and one small device status word, nothing else.
+ *     owns its options, a 4-byte device status word and about 2 MiB of device scratch
+ *     (partial sums of decode launches that split K across CTAs, and their counters),
+ *     all allocated by q4lin_create.
  *   - Status codes, never exceptions, aborts or prints.  Arguments are validated before
  *     any launch: a non-OK status from validation means nothing was enqueued.
  *   - All device pointers must be device-accessible memory of the handle's device.
- *   - Reentrant for distinct streams; q4lin_set_option must not race with q4lin_run on
- *     the same handle.
+ *   - The handle's scratch is shared by its calls: calls on one handle must be ordered on
+ *     the GPU (one stream, or streams ordered by events).  Use one handle per stream for
+ *     calls that run concurrently.  q4lin_set_option must not race with q4lin_run on the
+ *     same handle.
  */
 #ifndef Q4LIN_H
 #define Q4LIN_H
@@ -90,12 +94,12 @@ typedef enum {
 } q4lin_option_t;
 
 /* Create a handle for CUDA device `device`.  Queries the SM count and shared-memory
- * limit and allocates the 4-byte device status word.  Q4LIN_ERR_NO_DEVICE if the
+ * limit and allocates the 4-byte device status word and the handle's scratch.  Q4LIN_ERR_NO_DEVICE if the
  * ordinal does not exist, Q4LIN_ERR_UNSUPPORTED if it is not compute capability 10.3.
  * The caller's current device is left unchanged. */
 Q4LIN_API q4lin_status_t q4lin_create(q4lin_handle_t* handle, int device);
 
-/* Release the handle and its status word.  NULL is accepted (no-op). */
+/* Release the handle, its status word and its scratch.  NULL is accepted (no-op). */
 Q4LIN_API q4lin_status_t q4lin_destroy(q4lin_handle_t handle);
 
 /* out = x @ dequant(W)^T (+ bias), enqueued on `stream` (a cudaStream_t; NULL = the

@@ -369,3 +369,18 @@ def test_dependent_chain(handle, pdl):
         assert not np.isnan(host[i + 1]).any(), f"link {i} output has NaN"
         ref, mag = oracle.linear(host[i][None, :], c.qweight, c.scales, c.bias, c.K, 32)
         assert_parity(host[i + 1][None, :], ref, mag, TOL_FP32)
+
+
+# ------------------------------------------------------------- split K (decode GEMV)
+@pytest.mark.parametrize("N,K,gs", [(512, 8192, 32), (64, 4096, 64), (2048, 2048, 32),
+                                    (1000, 8192, 8192), (2047, 14336, 128)])
+def test_split_k_parity_and_determinism(handle, N, K, gs):
+    """Short matrices split K across CTAs (partial sums in the handle's scratch, summed
+    in a fixed order by the last CTA of each row block): parity, and bit-identical
+    results over repeated calls (the counters reset themselves)."""
+    c = synth.make_case(1, N, K, gs, scale_f16=(gs != K), bias=True, seed=N + K)
+    outs = [run_q4lin(handle, c, AUTO)[0] for _ in range(3)]
+    ref, mag = oracle.linear(c.x, c.qweight, c.scales, c.bias, K, gs)
+    assert_parity(outs[0], ref, mag, TOL_FP32)
+    np.testing.assert_array_equal(outs[0], outs[1])
+    np.testing.assert_array_equal(outs[0], outs[2])
