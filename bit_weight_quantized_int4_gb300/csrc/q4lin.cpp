@@ -397,6 +397,7 @@ const char* q4lin_status_string(q4lin_status_t s) {
         case Q4LIN_ERR_CUDA: return "CUDA error";
         case Q4LIN_ERR_TIMEOUT: return "device-side bounded wait ran out";
         case Q4LIN_ERR_NO_DEVICE: return "no such CUDA device";
+        case Q4LIN_ERR_TOO_LARGE: return "problem exceeds a fixed capacity";
         default: return "unknown status";
     }
 }

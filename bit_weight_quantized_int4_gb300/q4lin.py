@@ -28,6 +28,7 @@ Q4LIN_ERR_UNSUPPORTED = 2
 Q4LIN_ERR_CUDA = 3
 Q4LIN_ERR_TIMEOUT = 4
 Q4LIN_ERR_NO_DEVICE = 5
+Q4LIN_ERR_TOO_LARGE = 6
 
 Q4LIN_SCALE_F32 = 0
 Q4LIN_SCALE_F16 = 1
@@ -60,6 +61,8 @@ class q4lin_problem_t(ctypes.Structure):
 
 _lib.q4lin_run_grouped.argtypes = [_vp, ctypes.POINTER(q4lin_problem_t), _i32, _vp]
 _lib.q4lin_run_grouped.restype = _i32
+_lib.q4lin_run_static_scratch.argtypes = [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp]
+_lib.q4lin_run_static_scratch.restype = _i32
 _lib.q4lin_plan.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i32,
                             ctypes.POINTER(_i32)]
 _lib.q4lin_plan.restype = _i32
@@ -112,6 +115,13 @@ def q4lin_run_grouped(handle, problems, stream) -> int:
     for i, p in enumerate(problems):
         arr[i] = p if isinstance(p, q4lin_problem_t) else q4lin_problem_t(*p)
     return _lib.q4lin_run_grouped(handle, arr, len(problems), stream)
+
+
+def q4lin_run_static_scratch(x, qweight, scales, bias, out, N, K, group_size, scale_dtype,
+                             stream) -> int:
+    """Raw call of the allocation-free decode GEMV (pointers and stream as integers)."""
+    return _lib.q4lin_run_static_scratch(x, qweight, scales, bias, out, N, K, group_size,
+                                         scale_dtype, stream)
 
 
 def q4lin_plan(handle, x, qweight, scales, bias, out, M, N, K, group_size, scale_dtype):

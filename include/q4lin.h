@@ -54,7 +54,8 @@ typedef enum {
     Q4LIN_ERR_UNSUPPORTED = 2, /* device is not sm_103, or a forced path cannot run   */
     Q4LIN_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed                 */
     Q4LIN_ERR_TIMEOUT = 4,     /* a bounded device-side wait gave up (see status word) */
-    Q4LIN_ERR_NO_DEVICE = 5    /* no CUDA device with that ordinal                     */
+    Q4LIN_ERR_NO_DEVICE = 5,   /* no CUDA device with that ordinal                     */
+    Q4LIN_ERR_TOO_LARGE = 6    /* exceeds a fixed capacity (q4lin_run_static_scratch)  */
 } q4lin_status_t;
 
 /* Element type of the scales array. */
@@ -149,6 +150,37 @@ typedef struct q4lin_problem {
 Q4LIN_API q4lin_status_t q4lin_run_grouped(q4lin_handle_t handle,
                                            const q4lin_problem_t* problems, int count,
                                            void* stream);
+
+/* Decode GEMV (M = 1) for callers that cannot allocate device memory.
+ *
+ * No counterpart on the pages: this entry point exists for callers that may not call
+ * cudaMalloc -- code that runs while a stream is being captured into a CUDA graph in a
+ * mode that forbids allocation, code inside a custom allocator or memory pool (where
+ * allocating would recurse), and real-time paths where an allocation's latency or
+ * failure is not allowed.  Such callers cannot create a handle (q4lin_create allocates),
+ * so this call needs none: it runs the same decode GEMV as q4lin_run with M = 1, whose
+ * split-K partial sums and counters live in a fixed array of about 537 KB that the
+ * library reserves in the device code image; every GPU that loads the library holds it
+ * until the process exits.  Nothing is allocated: no cudaMalloc, cudaFree or allocating
+ * library routine.
+ *
+ *   Arguments as q4lin_run with M = 1 (x is [K], out is [N]); default nibble order, no
+ *   PDL.  N must be at most 16384: larger N returns Q4LIN_ERR_TOO_LARGE and runs nothing.
+ *   Shapes the TMA-fed GEMV cannot take (K % 32 != 0, K < 512, N < 32, x or qweight not
+ *   16-byte aligned, group_size neither a multiple of 32 nor >= K) return
+ *   Q4LIN_ERR_UNSUPPORTED.
+ *   The first call on a device looks up the array's device address (once per device, on
+ *   the current device); make that first call before any stream capture.
+ *   Every call shares the array and it keeps the last call's contents: each call clears
+ *   the counters it needs (an asynchronous memset on `stream`) before its kernel.  Calls
+ *   that overlap on the GPU race on the array: order them (one stream, or events).
+ *   A bounded device-side wait that runs out is not reported by this entry point (the
+ *   output is then undefined); the kernel still returns. */
+Q4LIN_API q4lin_status_t q4lin_run_static_scratch(const float* x, const uint8_t* qweight,
+                                                  const void* scales, const float* bias,
+                                                  float* out, int64_t N, int64_t K,
+                                                  int64_t group_size, int scale_dtype,
+                                                  void* stream);
 
 /* The path q4lin_run would take for these arguments (no launch, no device access);
  * *path_out receives a q4lin_path_t other than AUTO.  Same validation and status codes

@@ -54,7 +54,7 @@ def test_python_constants_match_header():
 
 def test_status_strings(lib):
     from bit_weight_quantized_int4_gb300 import q4lin
-    for code in range(6):
+    for code in range(7):
         s = q4lin.q4lin_status_string(code)
         assert s and s != "unknown status"
     assert q4lin.q4lin_status_string(99) == "unknown status"
