@@ -33,6 +33,29 @@ sys.path.insert(0, ROOT)
 
 METRIC = "decode GEMV HBM GB/s & ms/token; prefill TFLOP/s; % roofline on 1 GB300"
 GROUP = 32
+L2_BYTES = 129 << 20
+
+# DRAM bytes (read + write) of the 65 launches of one 1B decode token, summed from one ncu
+# launch list (dram__bytes_read.sum + dram__bytes_write.sum per launch; the summary is
+# profiles/gemv_tma_token_1b_launches.md).  Valid only for the kernel source it was taken
+# with: the sha256 prefix of gemv_tma.cu + ptx.cuh; any other source reports null.
+TOKEN_TRAFFIC = {"bytes": 700564480, "launches": 65, "source_sha256": "923f41173426ba4d"}
+
+
+def gemv_source_sha():
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("gemv_tma.cu", "ptx.cuh"):
+        with open(os.path.join(ROOT, "bit_weight_quantized_int4_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def token_traffic_per_launch(launches):
+    t = TOKEN_TRAFFIC
+    if launches != t["launches"] or gemv_source_sha() != t["source_sha256"]:
+        return None
+    return round(t["bytes"] / t["launches"])
 
 # (name, N, K) per decoder layer, in layer order; lm_head last.
 LAYER_1B = [("q", 2048, 2048), ("k", 512, 2048), ("v", 512, 2048), ("o", 2048, 2048),
@@ -297,32 +320,17 @@ def measure_e2e(torch, token, graph, steps, warmup):
     return ms, x_host.numel() * 4, out_host.numel() * 4
 
 
-def shape_bandwidth(torch, handle, N, K, reps=30, l2_bytes=129 << 20):
-    """GB/s of one GEMV shape in isolation: enough weight copies rotated that each launch
-    streams from HBM; `reps` launches captured in a CUDA graph (device time, without host
-    launch overhead), CUDA events around the replay."""
-    from bit_weight_quantized_int4_gb300 import q4lin as q
-    b = gemv_bytes(N, K)
-    copies = max(2, -(-3 * l2_bytes // b))
-    ws = [torch.randint(0, 256, (N, K // 2), dtype=torch.uint8, device="cuda") for _ in range(copies)]
-    ss = [(torch.rand((K // GROUP, N), device="cuda") * 0.015 + 0.005).half() for _ in range(copies)]
-    x = torch.randn(K, device="cuda")
-    out = torch.empty(N, device="cuda")
-
-    def launch(i, sp):
-        st = q.q4lin_run(handle, x.data_ptr(), ws[i % copies].data_ptr(),
-                         ss[i % copies].data_ptr(), None, out.data_ptr(), 1, N, K, GROUP,
-                         q.Q4LIN_SCALE_F16, sp)
-        assert st == q.Q4LIN_OK
-
+def graph_time_us(torch, launch, count, reps=1):
+    """Device time per launch: `count` launches (launch(i, stream_ptr)) captured in one CUDA
+    graph, replayed once untimed and `reps` times timed with CUDA events on the replay
+    stream (no host launch overhead inside the timed region)."""
     side = torch.cuda.Stream()
     with torch.cuda.stream(side):
-        for i in range(copies):
-            launch(i, side.cuda_stream)
+        launch(0, side.cuda_stream)              # loads the kernels before capture
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
-        for i in range(reps):
+        for i in range(count):
             launch(i, torch.cuda.current_stream().cuda_stream)
     stream = torch.cuda.Stream()
     with torch.cuda.stream(stream):
@@ -331,11 +339,40 @@ def shape_bandwidth(torch, handle, N, K, reps=30, l2_bytes=129 << 20):
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         start.record(stream)
-        g.replay()
+        for _ in range(reps):
+            g.replay()
         end.record(stream)
     end.synchronize()
-    us = start.elapsed_time(end) * 1000 / reps
-    del ws, ss, g
+    del g
+    return start.elapsed_time(end) * 1000 / (count * reps)
+
+
+def weight_copies(torch, N, K, bytes_each, l2_bytes=L2_BYTES, cap=1024):
+    """Enough distinct (weight, scale) copies that cycling through them streams at least
+    three L2 capacities, so every launch reads its weights from HBM."""
+    copies = int(min(cap, max(2, -(-3 * l2_bytes // bytes_each))))
+    ws = [torch.randint(0, 256, (N, K // 2), dtype=torch.uint8, device="cuda") for _ in range(copies)]
+    ss = [(torch.rand((K // GROUP, N), device="cuda") * 0.015 + 0.005).half() for _ in range(copies)]
+    return ws, ss
+
+
+def shape_bandwidth(torch, handle, N, K):
+    """GB/s of one GEMV shape in isolation, every launch on its own weight copy (HBM-cold
+    weights; x stays L2-resident as it would in a model)."""
+    from bit_weight_quantized_int4_gb300 import q4lin as q
+    b = gemv_bytes(N, K)
+    ws, ss = weight_copies(torch, N, K, b)
+    x = torch.randn(K, device="cuda")
+    out = torch.empty(N, device="cuda")
+
+    def launch(i, sp):
+        st = q.q4lin_run(handle, x.data_ptr(), ws[i % len(ws)].data_ptr(),
+                         ss[i % len(ws)].data_ptr(), None, out.data_ptr(), 1, N, K, GROUP,
+                         q.Q4LIN_SCALE_F16, sp)
+        assert st == q.Q4LIN_OK
+
+    us = graph_time_us(torch, launch, len(ws))
+    del ws, ss
     return {"N": N, "K": K, "us": round(us, 3), "GB_s": round(b / us / 1e3, 1)}
 
 
@@ -458,47 +495,41 @@ CROSSOVER_NK = ((2048, 2048), (8192, 2048), (2048, 8192), (128256, 2048), (1000,
 
 
 def crossover():
-    """Device time (CUDA graph replay) of each forced path over M for several (N, K)."""
+    """Device time per launch of each forced path (CUDA-core row streaming, the generic
+    FFMA kernel, the tensor-core GEMM) over M for several (N, K): one JSON row per (N, K, M).
+    Every launch in a graph reads its own weight copy, so weights come from HBM."""
     import torch
     from bit_weight_quantized_int4_gb300 import q4lin as q
     h = q.q4lin_create(0)
-    table = []
+    paths = (("gemv", q.Q4LIN_PATH_GEMV), ("ffma", q.Q4LIN_PATH_FFMA), ("tc", q.Q4LIN_PATH_TC))
     for N, K in CROSSOVER_NK:
-        w = torch.randint(0, 256, (N, K // 2), dtype=torch.uint8, device="cuda")
-        s = (torch.rand((K // GROUP, N), device="cuda") * 0.015 + 0.005).half()
+        ws, ss = weight_copies(torch, N, K, gemv_bytes(N, K), cap=64)
         for M in CROSSOVER_M:
             x = torch.randn(M, K, device="cuda")
             out = torch.empty(M, N, device="cuda")
-            row = {"N": N, "K": K, "M": M}
-            for name, path in (("gemv", q.Q4LIN_PATH_GEMV), ("tc", q.Q4LIN_PATH_TC)):
+            row = {"N": N, "K": K, "M": M, "copies": len(ws)}
+            for name, path in paths:
                 q.q4lin_set_option(h, q.Q4LIN_OPT_FORCE_PATH, path)
-                args = (x.data_ptr(), w.data_ptr(), s.data_ptr(), None, out.data_ptr(), M, N, K,
-                        GROUP, q.Q4LIN_SCALE_F16)
-                st, _ = q.q4lin_plan(h, *args)
-                if st != q.Q4LIN_OK:
+                st, _ = q.q4lin_plan(h, x.data_ptr(), ws[0].data_ptr(), ss[0].data_ptr(), None,
+                                     out.data_ptr(), M, N, K, GROUP, q.Q4LIN_SCALE_F16)
+                if st != q.Q4LIN_OK or (name == "ffma" and M * N * K > (1 << 34)):
                     row[name + "_us"] = None
                     continue
-                side = torch.cuda.Stream()
-                with torch.cuda.stream(side):
-                    q.q4lin_run(h, *args, side.cuda_stream)
-                torch.cuda.synchronize()
-                g = torch.cuda.CUDAGraph()
-                reps = 10
-                with torch.cuda.graph(g):
-                    for _ in range(reps):
-                        q.q4lin_run(h, *args, torch.cuda.current_stream().cuda_stream)
-                g.replay()
-                torch.cuda.synchronize()
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record()
-                g.replay()
-                e1.record()
-                e1.synchronize()
-                row[name + "_us"] = round(e0.elapsed_time(e1) * 1000 / reps, 2)
-                del g
+
+                def launch(i, sp):
+                    r = q.q4lin_run(h, x.data_ptr(), ws[i % len(ws)].data_ptr(),
+                                    ss[i % len(ws)].data_ptr(), None, out.data_ptr(), M, N, K,
+                                    GROUP, q.Q4LIN_SCALE_F16, sp)
+                    assert r == q.Q4LIN_OK
+
+                row[name + "_us"] = round(graph_time_us(torch, launch, len(ws)), 2)
             q.q4lin_set_option(h, q.Q4LIN_OPT_FORCE_PATH, q.Q4LIN_PATH_AUTO)
-            table.append(row)
+            st, auto = q.q4lin_plan(h, x.data_ptr(), ws[0].data_ptr(), ss[0].data_ptr(), None,
+                                    out.data_ptr(), M, N, K, GROUP, q.Q4LIN_SCALE_F16)
+            row["auto"] = q.PATH_NAMES[auto]
             print(json.dumps(row), flush=True)
+        del ws, ss
+        torch.cuda.empty_cache()
     q.q4lin_destroy(h)
     return 0
 
@@ -515,7 +546,7 @@ def profile(spec):
             token.run(torch.cuda.current_stream().cuda_stream)
     elif kind == "gemv":
         N, K = int(dims[0]), int(dims[1])
-        shape_bandwidth(torch, h, N, K, reps=3)
+        shape_bandwidth(torch, h, N, K)
     elif kind == "prefill":
         M, N, K = (int(d) for d in dims)
         prefill_tflops(torch, h, M, N, K, reps=3)
@@ -604,7 +635,9 @@ def main():
                        launches_per_step=token.launches),
         "roofline": {"bound": "hbm", "achieved": round(per_gpu_gbs, 1), "peak": hbm_peak,
                      "unit": "GB/s", "frac": round(per_gpu_gbs / hbm_peak, 4),
-                     "traffic": None,
+                     "traffic": token_traffic_per_launch(token.launches),
+                     "traffic_unit": "bytes per launch (mean over the token)",
+                     "algorithmic_bytes_per_launch": round(token.bytes / token.launches),
                      "kernel": f"gemv_tma_kernel (all {token.launches} launches of a token; "
                                "launch gaps included)", "peak_source": peak_src},
         "e2e": {"value": round(token.bytes * world / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
