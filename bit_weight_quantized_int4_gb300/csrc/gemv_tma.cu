@@ -7,25 +7,29 @@
 // workgroup, a short reduction per row, and a predicated final store for a ragged vocab
 // such as 128257 -- is kept here.)
 //
-// HBM-bound: every packed byte is read exactly once.  The design decouples the memory
-// stream from the arithmetic:
-//   producer warp (one lane): 2D TMA copies of weight tiles [rb rows x 256 bytes]
-//     (= 512 k per row) into a 4-stage shared-memory ring, one mbarrier per stage.  The
-//     copies are long contiguous row segments, so DRAM sees streaming reads; the ring
-//     keeps up to 4 tiles (up to 128 KiB) in flight per SM without spending registers.
-//   16 consumer warps (512 threads, 4 per SM sub-partition, enough to keep the issue
-//     slots busy): thread = (chunk lane j in 0..15, row group r0); per tile it widens the
-//     32 codes of chunk j of each of its V = rb/32 rows and dots them with the x chunk
-//     (read once per tile from shared memory, where x is staged in padded 32-float chunks,
-//     and reused across the V rows), scaling each 32-value chunk by its group scale; the
-//     scales are fetched three tiles ahead.  A warp reads 512 contiguous bytes of the tile
-//     per load (conflict-free).  Partial sums stay in registers across the whole row; the
-//     16 chunk lanes of a row group are reduced with shuffles once per row block.
-// The CTAs are persistent and walk row blocks; the pipeline runs across block boundaries.
-// With programmatic dependent launch the producer starts streaming weights before the
-// preceding kernel on the stream has finished; x, bias and out are touched only after
-// griddepcontrol.wait.  Waits are bounded in time; a timeout records code 1 in the
-// status word and the CTA drains its copies and returns.
+// HBM-bound: every packed byte and every scale is read exactly once.  The memory stream
+// is decoupled from the arithmetic:
+//   producer warp (one lane): per stage, 2D TMA copies of the weight tile [rb rows x 512
+//     bytes] (= 1024 k per row, as two 256-byte boxes) and of the matching block of group
+//     scales [1024 / group size groups x rb rows], all on one mbarrier, into a ring of
+//     2..8 stages.  Weight rows are long contiguous segments, so DRAM sees streaming reads.
+//   8 consumer warps (256 threads): thread = (chunk lane j in 0..15, row group of V rows);
+//     per stage it widens chunks j and j + 16 (32 codes each) of each of its V rows and
+//     dots them with the x chunks (read from shared memory, where x is staged in padded
+//     32-float chunks, and reused across the V rows), scaling each chunk by its group
+//     scale.  A quarter-warp reads 128 contiguous bytes of a weight row (conflict-free).
+//     Partial sums stay in registers across the whole row; the 16 chunk lanes of a row
+//     group are reduced with shuffles once per row block.
+// A CTA is small enough (288 threads, at most 113 KiB of shared memory) that two fit on
+// one SM: the CTAs of the next kernel on the stream can become resident while this one
+// runs.  With programmatic dependent launch their producers then stream weights and
+// scales (which do not depend on the preceding kernel) before griddepcontrol.wait; x,
+// bias, out and the split-K workspace are touched only after it.
+// Row blocks of long-K, short-N matrices are split along K across CTAs; the partial row
+// sums go to a workspace and the last CTA of a row block adds them in part order (the
+// result does not depend on which CTA finishes last).
+// Waits are bounded in time; a timeout records code 1 in the status word and the CTA
+// drains its copies and returns.
 #include <algorithm>
 #include <mutex>
 
@@ -36,21 +40,22 @@ namespace q4lin {
 namespace {
 using namespace ptx;
 
-constexpr int kCWarps = 16;                // consumer warps: 4 per SM sub-partition
+constexpr int kCWarps = 8;                 // consumer warps: 2 per SM sub-partition
 constexpr int kCThreads = 32 * kCWarps;
 constexpr int kThreadsG = kCThreads + 32;  // + the producer warp
-constexpr int kSliceBytes = 256;           // packed bytes per row per tile
-constexpr int kSliceK = 512;
-constexpr int kRingBytes = 128 * 1024;      // weight tiles in flight per SM
-constexpr int kScaleRing = 4;              // tiles of scales in flight per thread
+constexpr int kRowGroups = kCThreads / 16; // 16 chunk lanes per row group
+constexpr int kBoxBytes = 256;             // packed bytes per row of one TMA box (maximum)
+constexpr int kStageRowBytes = 2 * kBoxBytes;  // 512 packed bytes = 1024 k per row
+constexpr int kStageChunks = 32;           // 32-k chunks per row per stage
 constexpr int kXPad = 36;                  // floats per 32-float x chunk in shared memory
+constexpr int kMaxStages = 8;
+constexpr int kCtaSmem = 113 * 1024;       // two CTAs per SM
 constexpr int64_t kDrainNs = 4000000000LL;
-constexpr int kMaxSmemG = 227 * 1024;
 constexpr int kMaxMats = 4;
 
 // One weight matrix of a launch.  Several matrices that share x (the q/k/v projections
 // of a layer, or gate/up) run in one launch over a virtual row space: matrix i owns the
-// row blocks [blk_begin, blk_begin + row_blocks).
+// row blocks [blk_begin, blk_begin + ceil(N / rb)).
 struct MatArgs {
     const void* scales;
     const float* bias;
@@ -59,23 +64,25 @@ struct MatArgs {
     int64_t blk_begin;
 };
 struct TensorMaps {
-    CUtensorMap m[kMaxMats];
+    CUtensorMap w[kMaxMats];  // packed weights [N, K/2] bytes, box [rb rows x 256 bytes]
+    CUtensorMap s[kMaxMats];  // group scales [G, N], box [groups per stage x rb rows]
 };
 
 struct GArgs {
     const float* x;
     MatArgs mat[kMaxMats];
     int nmat;
-    int64_t K, gs;
-    int scale_f16, per_channel, kslices, x_chunks;
-    int k_chunks;   // K / 32
-    int gs_chunks;  // group size / 32 (grouped scales)
-    int gs_shift;   // log2(gs_chunks) when a power of two, else -1
+    int64_t K;
+    int kstages;     // ceil(K / 1024)
+    int x_chunks;    // kstages * 32
+    int gs_shift;    // log2(group size / 32) (grouped scales)
+    int stages;      // ring depth
+    uint32_t stage_bytes, scale_off, stage_tx;
     int64_t row_blocks;
-    // Split K: each row block's k-slices are cut into `parts` runs of `tpp` slices; a work
+    // Split K: each row block's stages are cut into `parts` runs of `tpp` stages; a work
     // item is (row block, part).  With parts > 1 the items write partial row sums to
     // ws[part * ws_rows + row] and the last item of a row block (ticket count) adds them
-    // in part order, so the result does not depend on which CTA finishes last.
+    // in part order.
     int parts, tpp;
     int items;
     float* ws;       // [parts, ws_rows] partial sums (parts > 1)
@@ -86,22 +93,22 @@ struct GArgs {
 };
 
 // A CTA's walk over its work items: item = blockIdx.x + i * gridDim.x, item -> (row block
-// blk = item / parts, part), covering k-slices [part * tpp, min((part + 1) * tpp, kslices)).
-// One division per item, none per tile.
+// blk = item / parts, part), covering stages [part * tpp, min((part + 1) * tpp, kstages)).
+// One division per item, none per stage.
 struct Cursor {
     int item, blk, part, ks, ks_end;
     __device__ __forceinline__ void set(const GArgs& a) {
         blk = item / a.parts;
         part = item - blk * a.parts;
         ks = part * a.tpp;
-        ks_end = min(ks + a.tpp, a.kslices);
+        ks_end = min(ks + a.tpp, a.kstages);
     }
     __device__ __forceinline__ void start(const GArgs& a) {
         item = (int)blockIdx.x;
         if (item < a.items) set(a);
     }
     __device__ __forceinline__ bool valid(const GArgs& a) const { return item < a.items; }
-    // Move to the next tile; true when that finished the current item.
+    // Move to the next stage; true when that finished the current item.
     __device__ __forceinline__ bool advance(const GArgs& a) {
         if (++ks < ks_end) return false;
         item += gridDim.x;
@@ -110,15 +117,10 @@ struct Cursor {
     }
 };
 
-// Ring depth for row blocks of rb rows: always kRingBytes of tiles (4, 8 or 16 stages).
-__host__ __device__ constexpr int stages_for(int rb) { return kRingBytes / (rb * kSliceBytes); }
-// Shared memory: the stage ring, the barriers, then x (padded chunks of 32 floats).
-__host__ __device__ constexpr int ring_bytes(int rb) { return stages_for(rb) * rb * kSliceBytes; }
-__host__ __device__ constexpr int x_offset(int rb) {
-    return ring_bytes(rb) + 16 * stages_for(rb) + 16;
-}
-inline int smem_bytes_g(int rb, int64_t K) {
-    return 128 + x_offset(rb) + (int)((K + kSliceK - 1) / kSliceK * 16) * kXPad * 4;
+__host__ __device__ constexpr int x_bytes(int x_chunks) { return x_chunks * kXPad * 4; }
+// Shared memory: the stage ring, then the barriers and flags (256 bytes), then x.
+inline int smem_bytes_g(int stages, uint32_t stage_bytes, int x_chunks) {
+    return 128 + stages * (int)stage_bytes + 256 + x_bytes(x_chunks);
 }
 
 __device__ __forceinline__ float load_scale(const void* scales, int f16, int64_t idx) {
@@ -126,18 +128,43 @@ __device__ __forceinline__ float load_scale(const void* scales, int f16, int64_t
     return __ldg(reinterpret_cast<const float*>(scales) + idx);
 }
 
-// Raw bits of one scale (binary16 in the low half, or fp32).  Kept raw in the prefetch
-// ring and converted only when used: converting at load time would make the thread wait
-// for the load right away.
-template <bool F16>
-__device__ __forceinline__ uint32_t scale_bits(const void* scales, int64_t idx) {
-    if (F16) return __ldg(reinterpret_cast<const unsigned short*>(scales) + idx);
-    return __ldg(reinterpret_cast<const unsigned int*>(scales) + idx);
-}
-template <bool F16>
-__device__ __forceinline__ float scale_value(uint32_t bits) {
-    if (F16) return __half2float(__ushort_as_half((unsigned short)bits));
-    return __uint_as_float(bits);
+// V consecutive group scales of one group row, from the staged scale block.
+template <int V, bool F16>
+__device__ __forceinline__ void stage_scales(uint32_t addr, float (&s)[V]) {
+    if (F16) {
+        if (V == 4) {
+            uint32_t a, b;
+            asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(a), "=r"(b) : "r"(addr));
+            const float2 p = __half22float2(*reinterpret_cast<__half2*>(&a));
+            const float2 q = __half22float2(*reinterpret_cast<__half2*>(&b));
+            s[0] = p.x, s[1 % V] = p.y, s[2 % V] = q.x, s[3 % V] = q.y;
+        } else if (V == 2) {
+            uint32_t a;
+            asm volatile("ld.shared.u32 %0, [%1];" : "=r"(a) : "r"(addr));
+            const float2 p = __half22float2(*reinterpret_cast<__half2*>(&a));
+            s[0] = p.x, s[1 % V] = p.y;
+        } else {
+            unsigned short h;
+            asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h) : "r"(addr));
+            s[0] = __half2float(__ushort_as_half(h));
+        }
+    } else {
+        if (V == 4) {
+            float a, b, c, d;
+            asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];"
+                         : "=f"(a), "=f"(b), "=f"(c), "=f"(d)
+                         : "r"(addr));
+            s[0] = a, s[1 % V] = b, s[2 % V] = c, s[3 % V] = d;
+        } else if (V == 2) {
+            float a, b;
+            asm volatile("ld.shared.v2.f32 {%0,%1}, [%2];" : "=f"(a), "=f"(b) : "r"(addr));
+            s[0] = a, s[1 % V] = b;
+        } else {
+            float a;
+            asm volatile("ld.shared.f32 %0, [%1];" : "=f"(a) : "r"(addr));
+            s[0] = a;
+        }
+    }
 }
 
 // Matrix that owns global row block blk (blk_begin ascending, matrix 0 begins at 0).
@@ -183,27 +210,25 @@ __device__ __forceinline__ float2 chunk_dot(const uint4& wv, const float4 (&xv)[
 }
 
 template <int V, bool EH, bool PC, bool F16>
-__global__ void __launch_bounds__(kThreadsG, 1)
+__global__ void __launch_bounds__(kThreadsG, 2)
     gemv_tma_kernel(const __grid_constant__ TensorMaps tmaps, const GArgs a) {
-    constexpr int rb = 32 * V;  // rows per block: 32 row groups of V rows
-    constexpr uint32_t tile_bytes = rb * kSliceBytes;
-    constexpr int kStagesG = stages_for(rb);
-    static_assert((kStagesG & (kStagesG - 1)) == 0, "ring depth must be a power of two");
+    constexpr int rb = kRowGroups * V;  // rows per block: 16 row groups of V rows
+    constexpr uint32_t esz = F16 ? 2 : 4;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 127u) & ~127u;
     uint8_t* gbase = smem_raw + (base - raw);
-    const uint32_t bar_base = base + ring_bytes(rb);
-    volatile int* failed =
-        reinterpret_cast<volatile int*>(gbase + (bar_base + 16 * kStagesG - base));
+    const int S = a.stages;
+    const uint32_t bar_base = base + (uint32_t)S * a.stage_bytes;
+    volatile int* failed = reinterpret_cast<volatile int*>(gbase + (bar_base + 16 * kMaxStages - base));
     volatile int* s_ticket = failed + 1;  // last-item decision, broadcast to the consumers
-    float* xs = reinterpret_cast<float*>(gbase + x_offset(rb));
+    float* xs = reinterpret_cast<float*>(gbase + (bar_base + 256 - base));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     auto full = [&](int s) { return bar_base + 8u * s; };
-    auto empty = [&](int s) { return bar_base + 8u * (kStagesG + s); };
+    auto empty = [&](int s) { return bar_base + 8u * (kMaxStages + s); };
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStagesG; ++s) {
+        for (int s = 0; s < S; ++s) {
             mbar_init(full(s), 1);
             mbar_init(empty(s), kCWarps);
         }
@@ -216,77 +241,44 @@ __global__ void __launch_bounds__(kThreadsG, 1)
     if (warp == kCWarps) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
-            for (int q = 0; q < a.nmat; ++q) prefetch_tensormap(&tmaps.m[q]);
-            int t = 0;
+            for (int q = 0; q < a.nmat; ++q) {
+                prefetch_tensormap(&tmaps.w[q]);
+                if (!PC) prefetch_tensormap(&tmaps.s[q]);
+            }
+            int t = 0, s = 0;
+            uint32_t ph = 0;
             Cursor cur;
             cur.start(a);
             while (cur.valid(a)) {
-                const int s = t & (kStagesG - 1);
-                if (t >= kStagesG &&
-                    !wait_bounded(empty(s), (uint32_t)((t / kStagesG) - 1) & 1, a.wait_ns, failed)) {
+                if (t >= S && !wait_bounded(empty(s), ph ^ 1u, a.wait_ns, failed)) {
                     record_failure(a.status, failed);
                     break;
                 }
                 if (*failed) break;
                 const int mi = mat_of(a, cur.blk);
-                mbar_arrive_expect_tx(full(s), tile_bytes);
-                tma_load_2d(base + s * tile_bytes, &tmaps.m[mi], cur.ks * kSliceBytes,
-                            (int)((cur.blk - a.mat[mi].blk_begin) * rb), full(s));
+                const int row0 = (int)((cur.blk - a.mat[mi].blk_begin) * rb);
+                const uint32_t sb = base + (uint32_t)s * a.stage_bytes;
+                mbar_arrive_expect_tx(full(s), a.stage_tx);
+                tma_load_2d(sb, &tmaps.w[mi], cur.ks * kStageRowBytes, row0, full(s));
+                tma_load_2d(sb + rb * kBoxBytes, &tmaps.w[mi], cur.ks * kStageRowBytes + kBoxBytes,
+                            row0, full(s));
+                if (!PC)
+                    tma_load_2d(sb + a.scale_off, &tmaps.s[mi], row0,
+                                (cur.ks * kStageChunks) >> a.gs_shift, full(s));
                 ++t;
+                if (++s == S) s = 0, ph ^= 1u;
                 cur.advance(a);
             }
-            // The last armed tiles may still be landing; the CTA must not exit first.
-            for (int q = t > kStagesG ? t - kStagesG : 0; q < t; ++q)
-                wait_bounded(full(q & (kStagesG - 1)), (uint32_t)(q / kStagesG) & 1, kDrainNs,
-                             nullptr);
+            // The last armed stages may still be landing; the CTA must not exit first.
+            for (int q = t > S ? t - S : 0; q < t; ++q)
+                wait_bounded(full(q % S), (uint32_t)(q / S) & 1u, kDrainNs, nullptr);
         }
         return;
     }
 
     // ------------------------------------------------------------------ consumers
-    const int j = threadIdx.x & 15;          // chunk lane within a 256-byte slice
+    const int j = threadIdx.x & 15;          // chunk lane within a 256-byte box row
     const int r0 = (threadIdx.x >> 4) * V;   // first of this thread's V rows in a block
-
-    // Scales of this thread's tiles, kScaleRing - 1 tiles ahead of use.  Tile t uses
-    // ring slot t % kScaleRing and refills it for tile t + kScaleRing right after; the
-    // tile loop is unrolled by the ring size so every slot has a fixed register (moving
-    // a register whose load is in flight would wait for the load).  The first loads go
-    // out before griddep_wait: scales do not depend on the preceding kernel.  Tile
-    // coordinates advance incrementally (no integer division in the loop).
-    int tiles_mine = 0;
-    for (int it = blockIdx.x; it < a.items; it += gridDim.x) {
-        const int part = it % a.parts;
-        tiles_mine += min(a.tpp, a.kslices - part * a.tpp);
-    }
-    Cursor pf;
-    pf.start(a);
-    auto fetch_next = [&](uint32_t (&dst)[V]) {
-        if (!PC && pf.valid(a)) {
-            const int chunk = pf.ks * 16 + j;
-            const int mi = mat_of(a, pf.blk);
-            const MatArgs& m = a.mat[mi];
-            const int64_t n0 = (pf.blk - m.blk_begin) * rb + r0;
-            if (chunk < a.k_chunks) {
-                const int g = a.gs_shift >= 0 ? (chunk >> a.gs_shift) : chunk / a.gs_chunks;
-                const int64_t bi = (int64_t)g * m.N + n0;
-                if (n0 + V <= m.N) {
-#pragma unroll
-                    for (int v = 0; v < V; ++v) dst[v] = scale_bits<F16>(m.scales, bi + v);
-                } else {
-#pragma unroll
-                    for (int v = 0; v < V; ++v)
-                        dst[v] = n0 + v < m.N ? scale_bits<F16>(m.scales, bi + v) : 0u;
-                }
-            } else {
-#pragma unroll
-                for (int v = 0; v < V; ++v) dst[v] = 0u;
-            }
-        }
-        if (pf.valid(a)) pf.advance(a);
-    };
-    uint32_t sc[kScaleRing][V];
-#pragma unroll
-    for (int u = 0; u < kScaleRing; ++u) fetch_next(sc[u]);
 
     // x into shared memory once: chunk c (32 floats) at xs + c * kXPad; zero past K.
     griddep_wait();
@@ -305,84 +297,91 @@ __global__ void __launch_bounds__(kThreadsG, 1)
     for (int v = 0; v < V; ++v) acc[v] = make_float2(0.f, 0.f);
     Cursor cur;
     cur.start(a);
-    const float* xrow = xs + j * kXPad;
+    int s = 0;
+    uint32_t ph = 0;
+    const uint32_t xrow = smem_u32(xs) + (uint32_t)j * (kXPad * 4);
+    // After a timed-out wait (`dead`) the warp still walks every item, without waiting or
+    // computing, so that all consumer warps reach the same named barriers and every split-K
+    // ticket is still counted and reset; nothing is stored.
     bool dead = false;
-    for (int t0 = 0; t0 < tiles_mine && !dead; t0 += kScaleRing) {
+    while (cur.valid(a)) {
+        const bool got =
+            !dead && __all_sync(0xffffffffu, wait_bounded(full(s), ph, a.wait_ns, failed));
+        if (!got && !dead) {
+            if (lane == 0) record_failure(a.status, failed);
+            dead = true;
+        }
+        const uint32_t sb = base + (uint32_t)s * a.stage_bytes;
 #pragma unroll
-        for (int u = 0; u < kScaleRing; ++u) {
-            const int t = t0 + u;
-            if (t >= tiles_mine) break;
-            const int s = t & (kStagesG - 1);
+        for (int h = 0; h < 2 && got; ++h) {
+            const int cl = h * 16 + j;  // chunk within the stage
             float4 xv[8];
-            const float* xc = xrow + cur.ks * (16 * kXPad);
+            const uint32_t xa = xrow + (uint32_t)(cur.ks * kStageChunks + h * 16) * (kXPad * 4);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) xv[i] = *reinterpret_cast<const float4*>(xc + 4 * i);
-            const bool got = __all_sync(
-                0xffffffffu, wait_bounded(full(s), (uint32_t)(t / kStagesG) & 1, a.wait_ns, failed));
-            if (!got) {
-                if (lane == 0) record_failure(a.status, failed);
-                dead = true;
-                break;
+            for (int i = 0; i < 8; ++i) {
+                const uint4 u = ld_shared_v4(xa + 16 * i);
+                xv[i] = make_float4(__uint_as_float(u.x), __uint_as_float(u.y),
+                                    __uint_as_float(u.z), __uint_as_float(u.w));
             }
-            const uint32_t wrow = base + s * tile_bytes + r0 * kSliceBytes + j * 16;
+            float sc[V];
+            if (!PC)
+                stage_scales<V, F16>(sb + a.scale_off +
+                                         (uint32_t)(((cl >> a.gs_shift) * rb + r0) * (int)esz),
+                                     sc);
+            const uint32_t wrow = sb + (uint32_t)(h * rb * kBoxBytes + r0 * kBoxBytes + j * 16);
 #pragma unroll
             for (int v = 0; v < V; ++v) {
-                const uint4 wv = ld_shared_v4(wrow + v * kSliceBytes);
+                const uint4 wv = ld_shared_v4(wrow + v * kBoxBytes);
                 const float2 d = chunk_dot<EH>(wv, xv);
-                if (PC) {
-                    acc[v] = fadd2(acc[v], d);
-                } else {
-                    const float sv = scale_value<F16>(sc[u][v]);
-                    acc[v] = ffma2(d, make_float2(sv, sv), acc[v]);
+                acc[v] = PC ? fadd2(acc[v], d) : ffma2(d, make_float2(sc[v], sc[v]), acc[v]);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty(s));
+        if (++s == S) s = 0, ph ^= 1u;
+        const int blk = cur.blk;
+        const int part = cur.part;
+        if (cur.advance(a)) {
+            // Item done: undo the factor 16 of the high-nibble lane, reduce the 16 chunk
+            // lanes of each row; store (or hand the partial to the last item).
+            float tot[V];
+#pragma unroll
+            for (int v = 0; v < V; ++v) {
+                tot[v] = EH ? fmaf(acc[v].x, 0.0625f, acc[v].y) : fmaf(acc[v].y, 0.0625f, acc[v].x);
+#pragma unroll
+                for (int o = 1; o < 16; o <<= 1)
+                    tot[v] += __shfl_xor_sync(0xffffffffu, tot[v], o);
+                acc[v] = make_float2(0.f, 0.f);
+            }
+            float mine = tot[0];
+#pragma unroll
+            for (int v = 1; v < V; ++v)
+                if (j == v) mine = tot[v];
+            const MatArgs& m = a.mat[mat_of(a, blk)];
+            const int64_t n = (blk - m.blk_begin) * rb + r0 + j;
+            const int64_t vrow = (int64_t)blk * rb + r0 + j;  // row in the virtual row space
+            bool finish = true;
+            if (a.parts > 1) {
+                if (j < V) a.ws[(int64_t)part * a.ws_rows + vrow] = mine;
+                __threadfence();
+                asm volatile("bar.sync 1, %0;" ::"r"(kCThreads) : "memory");
+                if (threadIdx.x == 0) *s_ticket = atomicAdd(a.tickets + blk, 1);
+                asm volatile("bar.sync 1, %0;" ::"r"(kCThreads) : "memory");
+                finish = *s_ticket == a.parts - 1;
+                if (finish) {
+                    __threadfence();
+                    if (j < V) {
+                        mine = 0.f;
+                        for (int q = 0; q < a.parts; ++q)
+                            mine += __ldcg(a.ws + (int64_t)q * a.ws_rows + vrow);
+                    }
+                    if (threadIdx.x == 0) a.tickets[blk] = 0;
                 }
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(empty(s));
-            fetch_next(sc[u]);
-            const int blk = cur.blk;
-            const int part = cur.part;
-            if (cur.advance(a)) {
-                // Item done: undo the factor 16 of the high-nibble lane, reduce the 16
-                // chunk lanes of each row; store (or hand the partial to the last item).
-                float tot[V];
-#pragma unroll
-                for (int v = 0; v < V; ++v) {
-                    tot[v] = EH ? fmaf(acc[v].x, 0.0625f, acc[v].y) : fmaf(acc[v].y, 0.0625f, acc[v].x);
-#pragma unroll
-                    for (int o = 1; o < 16; o <<= 1)
-                        tot[v] += __shfl_xor_sync(0xffffffffu, tot[v], o);
-                    acc[v] = make_float2(0.f, 0.f);
-                }
-                float mine = tot[0];
-#pragma unroll
-                for (int v = 1; v < V; ++v)
-                    if (j == v) mine = tot[v];
-                const MatArgs& m = a.mat[mat_of(a, blk)];
-                const int64_t n = (blk - m.blk_begin) * rb + r0 + j;
-                const int64_t vrow = (int64_t)blk * rb + r0 + j;  // row in the virtual row space
-                bool finish = true;
-                if (a.parts > 1) {
-                    if (j < V) a.ws[(int64_t)part * a.ws_rows + vrow] = mine;
-                    __threadfence();
-                    asm volatile("bar.sync 1, %0;" ::"r"(kCThreads) : "memory");
-                    if (threadIdx.x == 0) *s_ticket = atomicAdd(a.tickets + blk, 1);
-                    asm volatile("bar.sync 1, %0;" ::"r"(kCThreads) : "memory");
-                    finish = *s_ticket == a.parts - 1;
-                    if (finish) {
-                        __threadfence();
-                        if (j < V) {
-                            mine = 0.f;
-                            for (int q = 0; q < a.parts; ++q)
-                                mine += __ldcg(a.ws + (int64_t)q * a.ws_rows + vrow);
-                        }
-                        if (threadIdx.x == 0) a.tickets[blk] = 0;
-                    }
-                }
-                if (finish && j < V && n < m.N) {
-                    if (PC) mine *= scale_value<F16>(scale_bits<F16>(m.scales, n));
-                    if (m.bias) mine += __ldg(m.bias + n);
-                    m.out[n] = mine;
-                }
+            if (finish && j < V && n < m.N && !*failed) {
+                if (PC) mine *= load_scale(m.scales, F16, n);
+                if (m.bias) mine += __ldg(m.bias + n);
+                m.out[n] = mine;
             }
         }
     }
@@ -411,13 +410,19 @@ EncodeTiledFn encode_fn() {
 
 template <int V, bool EH, bool PC, bool F16>
 cudaError_t launch_v(const TensorMaps& tm, const GArgs& a, unsigned grid, const LaunchCtx& c) {
-    static cudaError_t attr = cudaFuncSetAttribute(
-        gemv_tma_kernel<V, EH, PC, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmemG);
+    static cudaError_t attr = [] {
+        cudaError_t e = cudaFuncSetAttribute(gemv_tma_kernel<V, EH, PC, F16>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kCtaSmem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(gemv_tma_kernel<V, EH, PC, F16>,
+                                     cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+        return e;
+    }();
     if (attr != cudaSuccess) return attr;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kThreadsG);
-    cfg.dynamicSmemBytes = smem_bytes_g(32 * V, a.K);
+    cfg.dynamicSmemBytes = smem_bytes_g(a.stages, a.stage_bytes, a.x_chunks);
     cfg.stream = c.stream;
     cudaLaunchAttribute attrs[1];
     if (c.pdl) {
@@ -453,15 +458,45 @@ cudaError_t dispatch_v(int V, bool eh, bool pc, bool f16, const TensorMaps& tm, 
     return dispatch_eh<1>(eh, pc, f16, tm, a, grid, c);
 }
 
+int log2_exact(int64_t v) {
+    for (int s = 0; s < 62; ++s)
+        if (((int64_t)1 << s) == v) return s;
+    return -1;
+}
+
+// Bytes of one stage (weights, then the scale block rounded up to 128 bytes).
+uint32_t stage_bytes_for(int V, bool pc, int esz, int gs_shift, uint32_t* scale_off,
+                         uint32_t* tx) {
+    const int rb = kRowGroups * V;
+    const uint32_t wbytes = (uint32_t)(rb * kStageRowBytes);
+    const int gps = pc ? 0 : (gs_shift >= 5 ? 1 : kStageChunks >> gs_shift);
+    const uint32_t sbytes = (uint32_t)(gps * rb * esz);
+    *scale_off = wbytes;
+    *tx = wbytes + sbytes;
+    return wbytes + ((sbytes + 127u) & ~127u);
+}
+
 }  // namespace
 
 bool gemv_tma_eligible(const Problem& p) {
-    if (p.M != 1 || p.K % 32 != 0 || p.K < 2 * kSliceBytes || p.N < 32) return false;
-    if (smem_bytes_g(128, p.K) > kMaxSmemG) return false;
+    if (p.M != 1 || p.K % 32 != 0 || p.K < 512 || p.N < 16) return false;
+    if (p.N > (1LL << 30) || p.K > (1LL << 24)) return false;
     if (reinterpret_cast<uintptr_t>(p.x) % 16 || reinterpret_cast<uintptr_t>(p.qweight) % 16)
         return false;
-    if (!(p.group_size >= p.K || p.group_size % 32 == 0)) return false;
-    if (p.N > (1LL << 30)) return false;
+    const bool pc = p.group_size >= p.K;
+    if (!pc) {
+        // Group scales arrive by TMA: 16-byte aligned base and row stride, group size a
+        // power-of-two multiple of 32.
+        const int esz = p.scale_f16 ? 2 : 4;
+        if (p.group_size % 32 != 0 || log2_exact(p.group_size / 32) < 0) return false;
+        if (reinterpret_cast<uintptr_t>(p.scales) % 16 || (p.N * esz) % 16 != 0) return false;
+    }
+    // x staged whole, plus at least two stages of the smallest tile.
+    const int x_chunks = (int)((p.K + 1023) / 1024) * kStageChunks;
+    uint32_t so, tx;
+    const uint32_t sb1 = stage_bytes_for(1, pc, p.scale_f16 ? 2 : 4,
+                                         pc ? 0 : log2_exact(p.group_size / 32), &so, &tx);
+    if (smem_bytes_g(2, sb1, x_chunks) > kCtaSmem) return false;
     return encode_fn() != nullptr;
 }
 
@@ -477,28 +512,42 @@ cudaError_t gemv_tma_launch_group(const Problem* ps, int count, const LaunchCtx&
     EncodeTiledFn enc = encode_fn();
     if (!enc || count < 1 || count > kMaxMats) return cudaErrorNotSupported;
     const Problem& p0 = ps[0];
-    int64_t rows = 0;
-    for (int i = 0; i < count; ++i) rows += ps[i].N;
-    // Rows per block: as large as the GPU stays busy with (more rows per thread reuse
-    // the x chunk more), smaller for short matrices so every SM gets a block.
-    int V = 4;
-    if ((rows + 127) / 128 < c.sm_count) V = 2;
-    if ((rows + 63) / 64 < c.sm_count) V = 1;
-    const int rb = 32 * V;
+    const bool pc = p0.group_size >= p0.K;
+    const int esz = p0.scale_f16 ? 2 : 4;
+    const int gs_shift = pc ? 0 : log2_exact(p0.group_size / 32);
+    const int kstages = (int)((p0.K + 1023) / 1024);
+    const int x_chunks = kstages * kStageChunks;
+    const int slots = 2 * c.sm_count;
+    auto blocks_for = [&](int V) {
+        int64_t b = 0;
+        for (int i = 0; i < count; ++i) b += (ps[i].N + kRowGroups * V - 1) / (kRowGroups * V);
+        return b;
+    };
+    auto stages_for = [&](int V) {
+        uint32_t so, tx;
+        const uint32_t sb = stage_bytes_for(V, pc, esz, gs_shift, &so, &tx);
+        const int room = kCtaSmem - smem_bytes_g(0, sb, x_chunks);
+        return std::min<int>(kMaxStages, room / (int)sb);
+    };
+    // Rows per block: four per thread when the row blocks alone fill both CTA slots of
+    // every SM (more rows per thread reuse each x chunk more), two when they fill one
+    // slot, else one (short matrices: every SM gets a block).
+    int V = 1;
+    if (blocks_for(4) >= slots && stages_for(4) >= 2)
+        V = 4;
+    else if (blocks_for(2) >= c.sm_count && stages_for(2) >= 2)
+        V = 2;
+    const int rb = kRowGroups * V;
     GArgs a = {};
     a.x = p0.x;
     a.nmat = count;
     a.K = p0.K;
-    a.gs = p0.group_size;
-    a.scale_f16 = p0.scale_f16;
-    a.per_channel = p0.group_size >= p0.K;
-    a.kslices = (int)((p0.K + kSliceK - 1) / kSliceK);
-    a.x_chunks = a.kslices * 16;
-    a.k_chunks = (int)(p0.K / 32);
-    a.gs_chunks = a.per_channel ? 1 : (int)(p0.group_size / 32);
-    a.gs_shift = -1;
-    for (int sft = 0; sft < 31; ++sft)
-        if ((1 << sft) == a.gs_chunks) a.gs_shift = sft;
+    a.kstages = kstages;
+    a.x_chunks = x_chunks;
+    a.gs_shift = gs_shift;
+    a.stage_bytes = stage_bytes_for(V, pc, esz, gs_shift, &a.scale_off, &a.stage_tx);
+    a.stages = stages_for(V);
+    if (a.stages < 2) return cudaErrorNotSupported;
     a.status = c.status_word;
     a.wait_ns = c.wait_limit_ns;
     TensorMaps tm;
@@ -511,41 +560,58 @@ cudaError_t gemv_tma_launch_group(const Problem* ps, int count, const LaunchCtx&
         a.mat[i].N = p.N;
         a.mat[i].blk_begin = blocks;
         blocks += (p.N + rb - 1) / rb;
-        const int64_t Kp = p.K / 2;
-        const cuuint64_t dims[2] = {(cuuint64_t)Kp, (cuuint64_t)p.N};
-        const cuuint64_t strides[1] = {(cuuint64_t)Kp};
-        const cuuint32_t box[2] = {(cuuint32_t)kSliceBytes, (cuuint32_t)rb};
-        const cuuint32_t estr[2] = {1, 1};
-        if (enc(&tm.m[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(p.qweight), dims,
-                strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return cudaErrorInvalidValue;
+        {
+            const cuuint64_t dims[2] = {(cuuint64_t)(p.K / 2), (cuuint64_t)p.N};
+            const cuuint64_t strides[1] = {(cuuint64_t)(p.K / 2)};
+            const cuuint32_t box[2] = {(cuuint32_t)kBoxBytes, (cuuint32_t)rb};
+            const cuuint32_t estr[2] = {1, 1};
+            if (enc(&tm.w[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(p.qweight),
+                    dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+                return cudaErrorInvalidValue;
+        }
+        if (!pc) {
+            const int64_t G = (p.K + p.group_size - 1) / p.group_size;
+            const int gps = gs_shift >= 5 ? 1 : kStageChunks >> gs_shift;
+            const cuuint64_t dims[2] = {(cuuint64_t)p.N, (cuuint64_t)G};
+            const cuuint64_t strides[1] = {(cuuint64_t)(p.N * esz)};
+            const cuuint32_t box[2] = {(cuuint32_t)rb, (cuuint32_t)gps};
+            const cuuint32_t estr[2] = {1, 1};
+            if (enc(&tm.s[i], p.scale_f16 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT32,
+                    2, const_cast<void*>(p.scales), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+                return cudaErrorInvalidValue;
+        } else {
+            tm.s[i] = tm.w[i];  // unused
+        }
     }
     for (int i = count; i < kMaxMats; ++i) {
         a.mat[i] = a.mat[count - 1];
         a.mat[i].blk_begin = blocks;  // never selected: begins past the last block
-        tm.m[i] = tm.m[count - 1];
+        tm.w[i] = tm.w[count - 1];
+        tm.s[i] = tm.s[count - 1];
     }
     a.row_blocks = blocks;
-    // Split K when the row blocks alone would leave SMs idle (the widening is ALU work,
-    // so every SM should get a share), if the handle's workspace can hold the partials.
-    // The partial-sum handoff costs a dependent round trip through L2, so a part keeps at
-    // least 8 k-slices (4096 k): only long rows are split.
+    // Split K when the row blocks alone would leave SMs idle, if the handle's workspace
+    // can hold the partials.  The partial-sum handoff costs a dependent round trip
+    // through L2, so a part keeps at least two stages (2048 k): only long rows are split.
     a.parts = 1;
     if (blocks < c.sm_count && c.ws && c.tickets) {
-        int parts = (int)std::min<int64_t>(c.sm_count / blocks, a.kslices / 8);
+        int parts = (int)std::min<int64_t>((c.sm_count + blocks - 1) / blocks, kstages / 2);
         while (parts > 1 && ((int64_t)parts * blocks * rb > c.ws_floats || blocks > c.ticket_count))
             --parts;
         a.parts = std::max(parts, 1);
     }
-    a.tpp = (a.kslices + a.parts - 1) / a.parts;
-    a.parts = (a.kslices + a.tpp - 1) / a.tpp;  // no empty part
+    a.tpp = (kstages + a.parts - 1) / a.parts;
+    a.parts = (kstages + a.tpp - 1) / a.tpp;  // no empty part
     a.items = (int)(blocks * a.parts);
     a.ws = c.ws;
     a.tickets = c.tickets;
     a.ws_rows = blocks * rb;
-    const unsigned grid = (unsigned)std::min<int64_t>(a.items, c.sm_count);
-    return dispatch_v(V, p0.even_high != 0, a.per_channel != 0, a.scale_f16 != 0, tm, a, grid, c);
+    const unsigned grid = (unsigned)std::min<int64_t>(a.items, slots);
+    return dispatch_v(V, p0.even_high != 0, pc, p0.scale_f16 != 0, tm, a, grid, c);
 }
 
 cudaError_t gemv_tma_launch(const Problem& p, const LaunchCtx& c) {
