@@ -377,6 +377,8 @@ def shape_bandwidth(torch, handle, N, K):
 
 
 def prefill_tflops(torch, handle, M, N, K, reps=10):
+    """TFLOP/s (2*M*N*K per launch) of one prefill shape: `reps` launches captured in a CUDA
+    graph, device time from CUDA events around a replay."""
     from bit_weight_quantized_int4_gb300 import q4lin as q
     w = torch.randint(0, 256, (N, K // 2), dtype=torch.uint8, device="cuda")
     s = torch.rand((K // GROUP, N), device="cuda") * 0.015 + 0.005
@@ -385,27 +387,15 @@ def prefill_tflops(torch, handle, M, N, K, reps=10):
     out = torch.empty(M, N, device="cuda")
     st, path = q.q4lin_plan(handle, x.data_ptr(), w.data_ptr(), s.data_ptr(), bias.data_ptr(),
                             out.data_ptr(), M, N, K, GROUP, q.Q4LIN_SCALE_F32)
-    stream = torch.cuda.Stream()
 
-    def launch():
+    def launch(i, sp):
         r = q.q4lin_run(handle, x.data_ptr(), w.data_ptr(), s.data_ptr(), bias.data_ptr(),
-                        out.data_ptr(), M, N, K, GROUP, q.Q4LIN_SCALE_F32, stream.cuda_stream)
+                        out.data_ptr(), M, N, K, GROUP, q.Q4LIN_SCALE_F32, sp)
         assert r == q.Q4LIN_OK
 
-    with torch.cuda.stream(stream):
-        for _ in range(3):
-            launch()
-    torch.cuda.synchronize()
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        start.record(stream)
-        for _ in range(reps):
-            launch()
-        end.record(stream)
-    end.synchronize()
-    ms = start.elapsed_time(end) / reps
-    return {"M": M, "N": N, "K": K, "path": q.PATH_NAMES[path], "us": round(ms * 1000, 2),
-            "TFLOP_s": round(2.0 * M * N * K / (ms * 1e-3) / 1e12, 2)}
+    us = graph_time_us(torch, launch, reps)
+    return {"M": M, "N": N, "K": K, "path": q.PATH_NAMES[path], "us": round(us, 2),
+            "TFLOP_s": round(2.0 * M * N * K / (us * 1e-6) / 1e12, 2)}
 
 
 # ------------------------------------------------------------------------- CPU baseline

@@ -10,7 +10,8 @@
 // HBM-bound: every packed byte and every scale is read exactly once.  The memory stream
 // is decoupled from the arithmetic:
 //   producer warp (one lane): per stage, 2D TMA copies of the weight tile [rb rows x 512
-//     bytes] (= 1024 k per row, as two 256-byte boxes) and of the matching block of group
+//     bytes] (= 1024 k per row; the packed matrix viewed as 16-bit elements, so one box
+//     spans the 512 bytes) and of the matching block of group
 //     scales [1024 / group size groups x rb rows], all on one mbarrier, into a ring of
 //     2..8 stages.  Weight rows are long contiguous segments, so DRAM sees streaming reads.
 //   8 consumer warps (256 threads): thread = (chunk lane j in 0..15, row group of V rows);
@@ -44,9 +45,13 @@ constexpr int kCWarps = 8;                 // consumer warps: 2 per SM sub-parti
 constexpr int kCThreads = 32 * kCWarps;
 constexpr int kThreadsG = kCThreads + 32;  // + the producer warp
 constexpr int kRowGroups = kCThreads / 16; // 16 chunk lanes per row group
-constexpr int kBoxBytes = 256;             // packed bytes per row of one TMA box (maximum)
-constexpr int kStageRowBytes = 2 * kBoxBytes;  // 512 packed bytes = 1024 k per row
-constexpr int kStageChunks = 32;           // 32-k chunks per row per stage
+// Stage width: H chunk columns of 16 bytes per thread, i.e. 256 * H packed bytes (512 * H
+// k) per row per stage.  H = 2 for every tile height (measured: halving the stage of the
+// V = 4 tiles to fit a deeper ring made them slower, the per-stage overhead outweighs the
+// extra depth).
+__host__ __device__ constexpr int chunk_cols(int) { return 2; }
+__host__ __device__ constexpr int stage_row_bytes(int V) { return 256 * chunk_cols(V); }
+__host__ __device__ constexpr int stage_chunks(int V) { return 16 * chunk_cols(V); }
 constexpr int kXPad = 36;                  // floats per 32-float x chunk in shared memory
 constexpr int kMaxStages = 8;
 constexpr int kCtaSmem = 113 * 1024;       // two CTAs per SM
@@ -64,7 +69,7 @@ struct MatArgs {
     int64_t blk_begin;
 };
 struct TensorMaps {
-    CUtensorMap w[kMaxMats];  // packed weights [N, K/2] bytes, box [rb rows x 256 bytes]
+    CUtensorMap w[kMaxMats];  // packed weights [N, K/4] 16-bit, box [rb rows x 512 bytes]
     CUtensorMap s[kMaxMats];  // group scales [G, N], box [groups per stage x rb rows]
 };
 
@@ -73,8 +78,8 @@ struct GArgs {
     MatArgs mat[kMaxMats];
     int nmat;
     int64_t K;
-    int kstages;     // ceil(K / 1024)
-    int x_chunks;    // kstages * 32
+    int kstages;     // ceil(K / stage k)
+    int x_chunks;    // kstages * chunks per stage
     int gs_shift;    // log2(group size / 32) (grouped scales)
     int stages;      // ring depth
     uint32_t stage_bytes, scale_off, stage_tx;
@@ -128,7 +133,8 @@ __device__ __forceinline__ float load_scale(const void* scales, int f16, int64_t
     return __ldg(reinterpret_cast<const float*>(scales) + idx);
 }
 
-// V consecutive group scales of one group row, from the staged scale block.
+// V consecutive group scales of one group row, from the staged scale block (shared
+// memory; 2V or 4V bytes, aligned to their size).
 template <int V, bool F16>
 __device__ __forceinline__ void stage_scales(uint32_t addr, float (&s)[V]) {
     if (F16) {
@@ -213,6 +219,7 @@ template <int V, bool EH, bool PC, bool F16>
 __global__ void __launch_bounds__(kThreadsG, 2)
     gemv_tma_kernel(const __grid_constant__ TensorMaps tmaps, const GArgs a) {
     constexpr int rb = kRowGroups * V;  // rows per block: 16 row groups of V rows
+    constexpr int H = chunk_cols(V), kSRB = stage_row_bytes(V), kSC = stage_chunks(V);
     constexpr uint32_t esz = F16 ? 2 : 4;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -245,6 +252,13 @@ __global__ void __launch_bounds__(kThreadsG, 2)
                 prefetch_tensormap(&tmaps.w[q]);
                 if (!PC) prefetch_tensormap(&tmaps.s[q]);
             }
+            // Pull x toward L2 now, so that the read after griddepcontrol.wait is short.
+            // L2 is where global memory is kept coherent: if the preceding kernel writes x
+            // after this prefetch, the L2 line is updated and the later read sees it; no
+            // copy of x enters this SM's L1 before the wait.
+            const int64_t xb = a.K * 4;
+            for (int64_t off = 0; off < xb; off += 32768)
+                l2_prefetch_bulk(a.x + off / 4, (uint32_t)(xb - off < 32768 ? xb - off : 32768));
             int t = 0, s = 0;
             uint32_t ph = 0;
             Cursor cur;
@@ -259,12 +273,10 @@ __global__ void __launch_bounds__(kThreadsG, 2)
                 const int row0 = (int)((cur.blk - a.mat[mi].blk_begin) * rb);
                 const uint32_t sb = base + (uint32_t)s * a.stage_bytes;
                 mbar_arrive_expect_tx(full(s), a.stage_tx);
-                tma_load_2d(sb, &tmaps.w[mi], cur.ks * kStageRowBytes, row0, full(s));
-                tma_load_2d(sb + rb * kBoxBytes, &tmaps.w[mi], cur.ks * kStageRowBytes + kBoxBytes,
-                            row0, full(s));
+                tma_load_2d(sb, &tmaps.w[mi], cur.ks * (kSRB / 2), row0, full(s));
                 if (!PC)
                     tma_load_2d(sb + a.scale_off, &tmaps.s[mi], row0,
-                                (cur.ks * kStageChunks) >> a.gs_shift, full(s));
+                                (cur.ks * kSC) >> a.gs_shift, full(s));
                 ++t;
                 if (++s == S) s = 0, ph ^= 1u;
                 cur.advance(a);
@@ -281,13 +293,23 @@ __global__ void __launch_bounds__(kThreadsG, 2)
     const int r0 = (threadIdx.x >> 4) * V;   // first of this thread's V rows in a block
 
     // x into shared memory once: chunk c (32 floats) at xs + c * kXPad; zero past K.
+    // (Four loads in flight per thread before the shared-memory stores.)
     griddep_wait();
-    for (int i = threadIdx.x; i < a.x_chunks * 8; i += kCThreads) {
-        const int c = i >> 3, q = i & 7;
-        const int64_t k = (int64_t)c * 32 + q * 4;
-        const float4 v = k < a.K ? __ldg(reinterpret_cast<const float4*>(a.x + k))
-                                 : make_float4(0.f, 0.f, 0.f, 0.f);
-        *reinterpret_cast<float4*>(xs + c * kXPad + q * 4) = v;
+    for (int i0 = threadIdx.x; i0 < a.x_chunks * 8; i0 += 4 * kCThreads) {
+        float4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int i = i0 + u * kCThreads;
+            const int64_t k = (int64_t)(i >> 3) * 32 + (i & 7) * 4;
+            v[u] = (i < a.x_chunks * 8 && k < a.K) ? __ldg(reinterpret_cast<const float4*>(a.x + k))
+                                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int i = i0 + u * kCThreads;
+            if (i < a.x_chunks * 8)
+                *reinterpret_cast<float4*>(xs + (i >> 3) * kXPad + (i & 7) * 4) = v[u];
+        }
     }
     asm volatile("bar.sync 1, %0;" ::"r"(kCThreads) : "memory");
 
@@ -297,9 +319,30 @@ __global__ void __launch_bounds__(kThreadsG, 2)
     for (int v = 0; v < V; ++v) acc[v] = make_float2(0.f, 0.f);
     Cursor cur;
     cur.start(a);
+    // Where this thread's row of the current item goes, with its bias and (per channel)
+    // scale, loaded when the item starts so that the loads overlap the item's stages.
+    float* st_out = nullptr;
+    float st_bias = 0.f, st_scale = 1.f;
+    bool st_ok = false;
+    auto prepare = [&](int blk) {
+        const MatArgs& m = a.mat[mat_of(a, blk)];
+        const int64_t n = (blk - m.blk_begin) * rb + r0 + j;
+        st_ok = j < V && n < m.N;
+        st_out = m.out + (st_ok ? n : 0);
+        st_bias = (st_ok && m.bias) ? __ldg(m.bias + n) : 0.f;
+        st_scale = (PC && st_ok) ? load_scale(m.scales, F16, n) : 1.f;
+    };
+    if (cur.valid(a)) prepare(cur.blk);
     int s = 0;
     uint32_t ph = 0;
-    const uint32_t xrow = smem_u32(xs) + (uint32_t)j * (kXPad * 4);
+    // Per-thread offsets: chunk lane j of the x chunks, the thread's rows of a weight
+    // stage (row r at r * kSRB bytes, chunk column c at c * 16), its group-scale rows.
+    const uint32_t xthr = smem_u32(xs) + (uint32_t)j * (kXPad * 4);
+    const uint32_t w_off = (uint32_t)(r0 * kSRB + j * 16);
+    uint32_t s_off[H];
+#pragma unroll
+    for (int h = 0; h < H; ++h)
+        s_off[h] = a.scale_off + (uint32_t)((((h * 16 + j) >> a.gs_shift) * rb + r0) * (int)esz);
     // After a timed-out wait (`dead`) the warp still walks every item, without waiting or
     // computing, so that all consumer warps reach the same named barriers and every split-K
     // ticket is still counted and reset; nothing is stored.
@@ -311,29 +354,27 @@ __global__ void __launch_bounds__(kThreadsG, 2)
             if (lane == 0) record_failure(a.status, failed);
             dead = true;
         }
-        const uint32_t sb = base + (uint32_t)s * a.stage_bytes;
+        if (got) {
+            const uint32_t sb = base + (uint32_t)s * a.stage_bytes;
+            const uint32_t xc = xthr + (uint32_t)(cur.ks * kSC) * (kXPad * 4);
 #pragma unroll
-        for (int h = 0; h < 2 && got; ++h) {
-            const int cl = h * 16 + j;  // chunk within the stage
-            float4 xv[8];
-            const uint32_t xa = xrow + (uint32_t)(cur.ks * kStageChunks + h * 16) * (kXPad * 4);
+            for (int h = 0; h < H; ++h) {
+                float4 xv[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const uint4 u = ld_shared_v4(xa + 16 * i);
-                xv[i] = make_float4(__uint_as_float(u.x), __uint_as_float(u.y),
-                                    __uint_as_float(u.z), __uint_as_float(u.w));
-            }
-            float sc[V];
-            if (!PC)
-                stage_scales<V, F16>(sb + a.scale_off +
-                                         (uint32_t)(((cl >> a.gs_shift) * rb + r0) * (int)esz),
-                                     sc);
-            const uint32_t wrow = sb + (uint32_t)(h * rb * kBoxBytes + r0 * kBoxBytes + j * 16);
+                for (int i = 0; i < 8; ++i) {
+                    const uint4 u = ld_shared_v4(xc + h * 16 * kXPad * 4 + 16 * i);
+                    xv[i] = make_float4(__uint_as_float(u.x), __uint_as_float(u.y),
+                                        __uint_as_float(u.z), __uint_as_float(u.w));
+                }
+                float sc[V];
+                if (!PC) stage_scales<V, F16>(sb + s_off[h], sc);
+                const uint32_t wrow = sb + w_off + h * 256;
 #pragma unroll
-            for (int v = 0; v < V; ++v) {
-                const uint4 wv = ld_shared_v4(wrow + v * kBoxBytes);
-                const float2 d = chunk_dot<EH>(wv, xv);
-                acc[v] = PC ? fadd2(acc[v], d) : ffma2(d, make_float2(sc[v], sc[v]), acc[v]);
+                for (int v = 0; v < V; ++v) {
+                    const uint4 wv = ld_shared_v4(wrow + v * kSRB);
+                    const float2 d = chunk_dot<EH>(wv, xv);
+                    acc[v] = PC ? fadd2(acc[v], d) : ffma2(d, make_float2(sc[v], sc[v]), acc[v]);
+                }
             }
         }
         __syncwarp();
@@ -357,8 +398,6 @@ __global__ void __launch_bounds__(kThreadsG, 2)
 #pragma unroll
             for (int v = 1; v < V; ++v)
                 if (j == v) mine = tot[v];
-            const MatArgs& m = a.mat[mat_of(a, blk)];
-            const int64_t n = (blk - m.blk_begin) * rb + r0 + j;
             const int64_t vrow = (int64_t)blk * rb + r0 + j;  // row in the virtual row space
             bool finish = true;
             if (a.parts > 1) {
@@ -378,11 +417,11 @@ __global__ void __launch_bounds__(kThreadsG, 2)
                     if (threadIdx.x == 0) a.tickets[blk] = 0;
                 }
             }
-            if (finish && j < V && n < m.N && !*failed) {
-                if (PC) mine *= load_scale(m.scales, F16, n);
-                if (m.bias) mine += __ldg(m.bias + n);
-                m.out[n] = mine;
+            if (finish && st_ok && !*failed) {
+                if (PC) mine *= st_scale;
+                *st_out = mine + st_bias;
             }
+            if (cur.valid(a)) prepare(cur.blk);
         }
     }
 }
@@ -468,8 +507,9 @@ int log2_exact(int64_t v) {
 uint32_t stage_bytes_for(int V, bool pc, int esz, int gs_shift, uint32_t* scale_off,
                          uint32_t* tx) {
     const int rb = kRowGroups * V;
-    const uint32_t wbytes = (uint32_t)(rb * kStageRowBytes);
-    const int gps = pc ? 0 : (gs_shift >= 5 ? 1 : kStageChunks >> gs_shift);
+    const uint32_t wbytes = (uint32_t)(rb * stage_row_bytes(V));
+    const int sc_log = chunk_cols(V) == 1 ? 4 : 5;  // log2(chunks per stage)
+    const int gps = pc ? 0 : (gs_shift >= sc_log ? 1 : stage_chunks(V) >> gs_shift);
     const uint32_t sbytes = (uint32_t)(gps * rb * esz);
     *scale_off = wbytes;
     *tx = wbytes + sbytes;
@@ -492,7 +532,7 @@ bool gemv_tma_eligible(const Problem& p) {
         if (reinterpret_cast<uintptr_t>(p.scales) % 16 || (p.N * esz) % 16 != 0) return false;
     }
     // x staged whole, plus at least two stages of the smallest tile.
-    const int x_chunks = (int)((p.K + 1023) / 1024) * kStageChunks;
+    const int x_chunks = (int)((p.K + 1023) / 1024) * stage_chunks(1);
     uint32_t so, tx;
     const uint32_t sb1 = stage_bytes_for(1, pc, p.scale_f16 ? 2 : 4,
                                          pc ? 0 : log2_exact(p.group_size / 32), &so, &tx);
@@ -515,8 +555,11 @@ cudaError_t gemv_tma_launch_group(const Problem* ps, int count, const LaunchCtx&
     const bool pc = p0.group_size >= p0.K;
     const int esz = p0.scale_f16 ? 2 : 4;
     const int gs_shift = pc ? 0 : log2_exact(p0.group_size / 32);
-    const int kstages = (int)((p0.K + 1023) / 1024);
-    const int x_chunks = kstages * kStageChunks;
+    auto kstages_for = [&](int V) {
+        const int sk = 512 * chunk_cols(V);
+        return (int)((p0.K + sk - 1) / sk);
+    };
+    auto x_chunks_for = [&](int V) { return kstages_for(V) * stage_chunks(V); };
     const int slots = 2 * c.sm_count;
     auto blocks_for = [&](int V) {
         int64_t b = 0;
@@ -526,24 +569,43 @@ cudaError_t gemv_tma_launch_group(const Problem* ps, int count, const LaunchCtx&
     auto stages_for = [&](int V) {
         uint32_t so, tx;
         const uint32_t sb = stage_bytes_for(V, pc, esz, gs_shift, &so, &tx);
-        const int room = kCtaSmem - smem_bytes_g(0, sb, x_chunks);
+        const int room = kCtaSmem - smem_bytes_g(0, sb, x_chunks_for(V));
         return std::min<int>(kMaxStages, room / (int)sb);
     };
-    // Rows per block: four per thread when the row blocks alone fill both CTA slots of
-    // every SM (more rows per thread reuse each x chunk more), two when they fill one
-    // slot, else one (short matrices: every SM gets a block).
-    int V = 1;
-    if (blocks_for(4) >= slots && stages_for(4) >= 2)
-        V = 4;
-    else if (blocks_for(2) >= c.sm_count && stages_for(2) >= 2)
-        V = 2;
+    // Tile shape (V rows per thread) and split-K parts from a cost model of the critical
+    // CTA, fitted to measured launch times on GB300 (isolated GEMVs, 1B/8B decode shapes):
+    //   cost = waves * (0.06 us per KiB of the CTA's weight bytes * eff(V)
+    //                   + 2.1 us for the split-K handoff when parts > 1)
+    // with waves = ceil(items / CTA slots).  eff(V) is the relative cost of a weight byte
+    // (1.4, 1.1, 1.0 for V = 1, 2, 4: more rows per thread reuse each x chunk more).
+    int V = 1, best_parts = 1;
+    double best = 1e30;
+    for (int v : {1, 2, 4}) {
+        if (stages_for(v) < 2) continue;
+        const int64_t blocks_v = blocks_for(v);
+        const double eff = v == 1 ? 1.4 : (v == 2 ? 1.1 : 1.0);
+        for (int parts = 1; parts <= 8; parts *= 2) {
+            const int kstages = kstages_for(v);
+            if (parts > 1 && (kstages * 512 * chunk_cols(v) / parts < 2048 || !c.ws || !c.tickets ||
+                              (int64_t)parts * blocks_v * kRowGroups * v > c.ws_floats ||
+                              blocks_v > c.ticket_count))
+                break;
+            const int tpp = (kstages + parts - 1) / parts;
+            const int64_t items = blocks_v * ((kstages + tpp - 1) / tpp);
+            const double waves = (double)((items + slots - 1) / slots);
+            const double kib = (double)kRowGroups * v * tpp * stage_row_bytes(v) / 1024.0;
+            const double cost = waves * (0.06 * kib * eff + (parts > 1 ? 2.1 : 0.0));
+            if (cost < best * 0.999) best = cost, V = v, best_parts = parts;
+        }
+    }
     const int rb = kRowGroups * V;
     GArgs a = {};
     a.x = p0.x;
     a.nmat = count;
     a.K = p0.K;
+    const int kstages = kstages_for(V);
     a.kstages = kstages;
-    a.x_chunks = x_chunks;
+    a.x_chunks = x_chunks_for(V);
     a.gs_shift = gs_shift;
     a.stage_bytes = stage_bytes_for(V, pc, esz, gs_shift, &a.scale_off, &a.stage_tx);
     a.stages = stages_for(V);
@@ -561,11 +623,11 @@ cudaError_t gemv_tma_launch_group(const Problem* ps, int count, const LaunchCtx&
         a.mat[i].blk_begin = blocks;
         blocks += (p.N + rb - 1) / rb;
         {
-            const cuuint64_t dims[2] = {(cuuint64_t)(p.K / 2), (cuuint64_t)p.N};
+            const cuuint64_t dims[2] = {(cuuint64_t)(p.K / 4), (cuuint64_t)p.N};
             const cuuint64_t strides[1] = {(cuuint64_t)(p.K / 2)};
-            const cuuint32_t box[2] = {(cuuint32_t)kBoxBytes, (cuuint32_t)rb};
+            const cuuint32_t box[2] = {(cuuint32_t)(stage_row_bytes(V) / 2), (cuuint32_t)rb};
             const cuuint32_t estr[2] = {1, 1};
-            if (enc(&tm.w[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(p.qweight),
+            if (enc(&tm.w[i], CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<uint8_t*>(p.qweight),
                     dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                     CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
@@ -573,7 +635,8 @@ cudaError_t gemv_tma_launch_group(const Problem* ps, int count, const LaunchCtx&
         }
         if (!pc) {
             const int64_t G = (p.K + p.group_size - 1) / p.group_size;
-            const int gps = gs_shift >= 5 ? 1 : kStageChunks >> gs_shift;
+            const int sc_log = chunk_cols(V) == 1 ? 4 : 5;
+            const int gps = gs_shift >= sc_log ? 1 : stage_chunks(V) >> gs_shift;
             const cuuint64_t dims[2] = {(cuuint64_t)p.N, (cuuint64_t)G};
             const cuuint64_t strides[1] = {(cuuint64_t)(p.N * esz)};
             const cuuint32_t box[2] = {(cuuint32_t)rb, (cuuint32_t)gps};
@@ -594,16 +657,7 @@ cudaError_t gemv_tma_launch_group(const Problem* ps, int count, const LaunchCtx&
         tm.s[i] = tm.s[count - 1];
     }
     a.row_blocks = blocks;
-    // Split K when the row blocks alone would leave SMs idle, if the handle's workspace
-    // can hold the partials.  The partial-sum handoff costs a dependent round trip
-    // through L2, so a part keeps at least two stages (2048 k): only long rows are split.
-    a.parts = 1;
-    if (blocks < c.sm_count && c.ws && c.tickets) {
-        int parts = (int)std::min<int64_t>((c.sm_count + blocks - 1) / blocks, kstages / 2);
-        while (parts > 1 && ((int64_t)parts * blocks * rb > c.ws_floats || blocks > c.ticket_count))
-            --parts;
-        a.parts = std::max(parts, 1);
-    }
+    a.parts = best_parts;
     a.tpp = (kstages + a.parts - 1) / a.parts;
     a.parts = (kstages + a.tpp - 1) / a.tpp;  // no empty part
     a.items = (int)(blocks * a.parts);

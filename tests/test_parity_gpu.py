@@ -285,6 +285,23 @@ def test_tc_parity(handle, M, N, K, gs, f16, bias):
     assert used == TC
 
 
+@pytest.mark.parametrize("M,N,K,gs,f16,bias", [
+    (128, 2048, 2048, 32, False, True),   # 16 tiles of 128 rows: K split over 8-CTA clusters
+    (64, 256, 8192, 128, True, False),    # one 256-row tile: 8-way split of long K
+    (200, 520, 1024, 1024, False, True),  # per-channel scales applied after the exchange
+    (9, 96, 512, 32, True, True),         # 16 stages over 4 CTAs, ragged N inside the slices
+])
+def test_tc_split_k_parity_and_determinism(handle, M, N, K, gs, f16, bias):
+    """Few output tiles: the K range is split over the CTAs of a cluster, whose partial
+    tiles are added in rank order in distributed shared memory.  Parity with the oracle,
+    and bitwise-identical results on a second call."""
+    c = synth.make_case(M, N, K, gs, scale_f16=f16, bias=bias, seed=N + K)
+    out1, used = check_case(handle, c, TC, rows=sample_rows(M))
+    assert used == TC
+    out2, _ = run_q4lin(handle, c, TC)
+    np.testing.assert_array_equal(out1, out2)
+
+
 @pytest.mark.parametrize("M", [1, 5, 48, 300])
 def test_tc_dyadic_bit_exact(handle, M):
     c = synth.make_dyadic_case(M, 260, 1024, 32, scale_f16=(M % 2 == 1), bias=True, seed=M)
