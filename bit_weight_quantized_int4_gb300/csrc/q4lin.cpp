@@ -38,9 +38,18 @@ constexpr int64_t kDefaultWaitLimit = 2000000000LL;  // 2 s of GPU global time
 constexpr int64_t kWsFloats = 1 << 19;   // 2 MiB
 constexpr int64_t kTickets = 1 << 14;    // 64 KiB
 
-// Crossover: at and above this M the tensor-core GEMM replaces the row-streaming
-// CUDA-core kernel (when both are eligible).  Measured on GB300; see plan().
-constexpr int64_t kTcMinM = 4;
+// M-dispatch between the row-streaming CUDA-core kernel (which re-reads the weights for
+// every 4 activation rows, so its time grows with M) and the tensor-core GEMM (flat in M
+// up to 128 rows).  Crossover table from a device-time sweep on GB300 (M = 1..512;
+// N x K = 1000 x 2048, 2048 x 2048, 8192 x 2048, 2048 x 8192, 128256 x 2048; every launch
+// on HBM-cold weights): the largest M for which row streaming is still faster, by the
+// weight count N * K (and long K, where the tensor-core main loop is longest).
+int64_t rowstream_max_m(const q4lin::Problem& p) {
+    const double nk = (double)p.N * (double)p.K;
+    if (nk < 8.0e6) return 16;
+    if (nk < 64.0e6) return p.K >= 8192 ? 12 : 8;
+    return 4;
+}
 
 class DeviceGuard {
    public:
@@ -147,7 +156,7 @@ q4lin_status_t plan(q4lin_handle_t h, const q4lin::Problem& p, const q4lin::Laun
         default:
             break;
     }
-    if (p.M >= kTcMinM && q4lin::tc_eligible(p, c)) {
+    if (p.M > 1 && q4lin::tc_eligible(p, c) && (!row_ok || p.M > rowstream_max_m(p))) {
         *path = Q4LIN_PATH_TC;
     } else if (row_ok) {
         *path = Q4LIN_PATH_GEMV;

@@ -53,6 +53,7 @@ constexpr int kStageK = 32;                  // 32 fp32 = one 128-byte swizzle r
 constexpr int kATile = kXRows * 128;         // 16 KiB
 constexpr int kMaxStages = 8;
 constexpr int kScaleAhead = 4;               // stages of scales in flight per thread
+constexpr int kWPrefetch = 8;                // stages per L2 prefetch block of packed weights
 constexpr int64_t kDrainNs = 4000000000LL;
 constexpr int kSmemLimit = 227 * 1024;
 
@@ -79,6 +80,8 @@ struct Tc2Args {
     // distributed shared memory, where rank q adds the columns [q * sw, (q + 1) * sw) of
     // all partials in rank order (row stride rs floats in the exchange buffer).
     int splitk, kpp, sw, rs;
+    int w_prefetch;  // pull 128-byte weight row segments into L2 ahead (few M tiles: the
+                     // weights stream from DRAM once; with many M tiles they sit in L2)
 };
 
 __device__ __forceinline__ float load_scale(const void* scales, int f16, int64_t idx) {
@@ -97,7 +100,8 @@ template <int RPT, bool EH>
 __global__ void __launch_bounds__(kThreads2, 1)
     tc_xa_kernel(const __grid_constant__ CUtensorMap tmap_x,
                  const __grid_constant__ CUtensorMap tmap_w,
-                 const __grid_constant__ CUtensorMap tmap_o, const Tc2Args a) {
+                 const __grid_constant__ CUtensorMap tmap_o,
+                 const __grid_constant__ CUtensorMap tmap_wp, const Tc2Args a) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -108,7 +112,6 @@ __global__ void __launch_bounds__(kThreads2, 1)
     const uint32_t w_base = b_base + S * bn * 128;
     const uint32_t bar_base = w_base + S * bn * 16;
     const uint32_t accfull = bar_base + 8 * 3 * kMaxStages;
-    const uint32_t cl_recv = accfull + 8;   // split K: partial tiles received (bytes)
     const uint32_t tmem_slot = accfull + 24;
     const int P = a.splitk;
     const int rank = P > 1 ? (int)cluster_ctarank() : 0;
@@ -131,7 +134,6 @@ __global__ void __launch_bounds__(kThreads2, 1)
             mbar_init(empty(s), 1);
         }
         mbar_init(accfull, 1);
-        if (P > 1) mbar_init(cl_recv, 1);
         *failed = 0;
         mbar_init_fence();
     }
@@ -150,6 +152,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
             // ------------------------------------------------------------ TMA producer
             prefetch_tensormap(&tmap_x);
             prefetch_tensormap(&tmap_w);
+            prefetch_tensormap(&tmap_wp);
             const int m0 = (int)blockIdx.y * kXRows, n0 = ntile * bn;
             const uint32_t tx = (uint32_t)(kATile + bn * 16);
             int li = 0;
@@ -160,6 +163,15 @@ __global__ void __launch_bounds__(kThreads2, 1)
                     break;
                 }
                 if (*failed) break;
+                // The packed-weight tile of a stage is only 16 bytes per row; with few M
+                // tiles, whole 128-byte row segments (eight stages) are pulled into L2 a
+                // block ahead, so that DRAM streams long segments and the per-stage copies
+                // hit L2.
+                if (a.w_prefetch && (li & (kWPrefetch - 1)) == 0) {
+                    const int first = li == 0 ? 0 : li + kWPrefetch;
+                    for (int pb = first; pb <= li + kWPrefetch && pb < n_iters; pb += kWPrefetch)
+                        tma_prefetch_l2_2d(&tmap_wp, (it_begin + pb) * (kStageK / 2), n0);
+                }
                 if (a.skip_first_copy && li == 0) continue;
                 const int it = it_begin + li;
                 mbar_arrive_expect_tx(full(s), tx);
@@ -349,7 +361,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
                     tma_store_2d(&tmap_o, (int)(n0 + 32 * b), (int)blockIdx.y * kXRows,
                                  a_base + (uint32_t)b * (kXRows * 128));
                 bulk_commit();
-                bulk_wait_all();
+                bulk_wait_read();
             }
         }
     }
@@ -357,13 +369,12 @@ __global__ void __launch_bounds__(kThreads2, 1)
         // ------------------------------------------- split K: reduce over the cluster
         // Shared memory (the free stage ring): send blocks [P][128][rs] (block q: columns
         // [q * sw, (q + 1) * sw) of this CTA's partial tile, rows padded to rs floats so a
-        // quarter-warp writes 8 distinct bank groups), receive blocks [P][128][rs] (block r:
-        // rank r's partial of this CTA's slice), then the reduced slice [128][sw].  Every
-        // thread reaches both cluster barriers: all earlier waits are bounded in time.
+        // quarter-warp writes 8 distinct bank groups), then this CTA's reduced slice
+        // [128][sw].  Every thread reaches both cluster barriers: all earlier waits in this
+        // kernel are bounded in time.
         const uint32_t blk_bytes = (uint32_t)(kXRows * a.rs * 4);
-        const uint32_t send_base = a_base, recv_base = a_base + (uint32_t)P * blk_bytes;
-        const uint32_t slice_base = recv_base + (uint32_t)P * blk_bytes;
-        if (threadIdx.x == 0) mbar_arrive_expect_tx(cl_recv, (uint32_t)P * blk_bytes);
+        const uint32_t send_base = a_base;
+        const uint32_t slice_base = send_base + (uint32_t)P * blk_bytes;
         if (warp >= 2 && epi_go) {
             const int group = (warp - 2) >> 2;
             const int quarter = warp & 3;
@@ -381,46 +392,46 @@ __global__ void __launch_bounds__(kThreads2, 1)
                                  __uint_as_float(r[4 * v4 + 1]), __uint_as_float(r[4 * v4 + 2]),
                                  __uint_as_float(r[4 * v4 + 3]));
             }
-            fence_proxy_async_smem();
         }
-        // 1. Every CTA of the cluster has completed its MMAs, drained its copies and staged
-        //    its send blocks: receive blocks may now be written.
+        // 1. Every CTA of the cluster has staged its send blocks.
         cluster_sync_all();
-        if (threadIdx.x == 0) {
-            for (int q = 0; q < P; ++q)
-                bulk_copy_to_cluster(
-                    map_shared_rank(recv_base + (uint32_t)rank * blk_bytes, (uint32_t)q),
-                    send_base + (uint32_t)q * blk_bytes, blk_bytes,
-                    map_shared_rank(cl_recv, (uint32_t)q));
-        }
-        // 2. This CTA's column slice: wait for the P partials, add them in rank order, then
-        //    the channel scale and bias, into the slice tile; one TMA store writes it out.
+        // 2. This CTA's column slice: read block `rank` of every CTA's send blocks (remote
+        //    shared-memory loads, four columns at a time), add them in rank order, then the
+        //    channel scale and bias, into the slice tile; one TMA store writes it out.
         if (warp >= 2) {
-            const bool got = wait_cluster_bounded(cl_recv, 0, a.wait_ns);
-            if (!got && lane == 0) record_failure(a.status, failed);
-            if (__all_sync(0xffffffffu, got)) {
-                const float* recv = reinterpret_cast<const float*>(gbase + (recv_base - base));
+            const bool ok2 = __all_sync(0xffffffffu, epi_go);
+            if (ok2) {
                 float* slice = reinterpret_cast<float*>(gbase + (slice_base - base));
                 const int cbase = rank * a.sw;
-                const int sw_shift = 31 - __clz(a.sw);  // sw is a power of two
-                for (int idx = threadIdx.x - 64; idx < kXRows * a.sw; idx += 128 * kGroups) {
-                    const int m = idx >> sw_shift, c = idx & (a.sw - 1);
-                    float v = 0.f;
-                    for (int r = 0; r < P; ++r) v += recv[(r * kXRows + m) * a.rs + c];
-                    if (a.per_channel) v *= s_cscale[cbase + c];
-                    slice[idx] = v + s_bias[cbase + c];
+                const int q_shift = 31 - __clz(a.sw / 4);  // sw / 4 is a power of two
+                const uint32_t my_blk = send_base + (uint32_t)rank * blk_bytes;
+                for (int idx = threadIdx.x - 64; idx < kXRows * (a.sw / 4); idx += 128 * kGroups) {
+                    const int m = idx >> q_shift, c = (idx & (a.sw / 4 - 1)) * 4;
+                    const uint32_t off = my_blk + (uint32_t)((m * a.rs + c) * 4);
+                    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                    for (int r = 0; r < P; ++r) {
+                        const float4 t = ld_cluster_v4(map_shared_rank(off, (uint32_t)r));
+                        v.x += t.x, v.y += t.y, v.z += t.z, v.w += t.w;
+                    }
+                    if (a.per_channel) {
+                        v.x *= s_cscale[cbase + c], v.y *= s_cscale[cbase + c + 1];
+                        v.z *= s_cscale[cbase + c + 2], v.w *= s_cscale[cbase + c + 3];
+                    }
+                    v.x += s_bias[cbase + c], v.y += s_bias[cbase + c + 1];
+                    v.z += s_bias[cbase + c + 2], v.w += s_bias[cbase + c + 3];
+                    *reinterpret_cast<float4*>(slice + m * a.sw + c) = v;
                 }
                 fence_proxy_async_smem();
             }
             asm volatile("bar.sync 2, %0;" ::"r"(128 * kGroups) : "memory");
             const int64_t ncol = (int64_t)ntile * bn + (int64_t)rank * a.sw;
-            if (threadIdx.x == 64 && got && !*failed && ncol < a.N) {
+            if (threadIdx.x == 64 && ok2 && !*failed && ncol < a.N) {
                 tma_store_2d(&tmap_o, (int)ncol, (int)blockIdx.y * kXRows, slice_base);
                 bulk_commit();
-                bulk_wait_all();
+                bulk_wait_read();
             }
         }
-        // 3. No CTA leaves while blocks it sent may still be in flight.
+        // 3. No CTA leaves while another may still read its send blocks.
         cluster_sync_all();
     }
     if (warp >= 2) tc_fence_before();
@@ -506,7 +517,7 @@ int max_active_clusters(int bn, int P, const LaunchCtx& c) {
 
 template <int RPT, bool EH>
 cudaError_t launch2(const CUtensorMap& tx, const CUtensorMap& tw, const CUtensorMap& to,
-                    const Tc2Args& a, dim3 grid, const LaunchCtx& c) {
+                    const CUtensorMap& twp, const Tc2Args& a, dim3 grid, const LaunchCtx& c) {
     const cudaError_t attr = kernel_attr<RPT, EH>();
     if (attr != cudaSuccess) return attr;
     cudaLaunchConfig_t cfg = {};
@@ -530,7 +541,7 @@ cudaError_t launch2(const CUtensorMap& tx, const CUtensorMap& tw, const CUtensor
     }
     cfg.attrs = na ? attrs : nullptr;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, tc_xa_kernel<RPT, EH>, tx, tw, to, a);
+    return cudaLaunchKernelEx(&cfg, tc_xa_kernel<RPT, EH>, tx, tw, to, twp, a);
 }
 
 }  // namespace
@@ -598,11 +609,11 @@ cudaError_t tc_launch(const Problem& p, const LaunchCtx& c) {
     a.bn = bn;
     a.stages = stages;
     a.k_iters = k_iters;
-    // The split-K exchange (send and receive blocks [P][128][sw + 4] floats, the slice
-    // [128][sw]) must fit in the stage ring, and its result goes out by TMA stores.
+    // The split-K exchange (send blocks [P][128][sw + 4] floats, the slice [128][sw]) must
+    // fit in the stage ring, and its result goes out by TMA stores.
     if (!((reinterpret_cast<uintptr_t>(p.out) % 16 == 0) && (p.N % 4 == 0))) splitk = 1;
     while (splitk > 1 &&
-           (2LL * splitk * kXRows * (bn / splitk + 4) + (int64_t)kXRows * (bn / splitk)) * 4 >
+           ((int64_t)splitk * kXRows * (bn / splitk + 4) + (int64_t)kXRows * (bn / splitk)) * 4 >
                (int64_t)stages * stage_bytes(bn))
         splitk /= 2;
     a.splitk = splitk;
@@ -616,6 +627,7 @@ cudaError_t tc_launch(const Problem& p, const LaunchCtx& c) {
         if ((1 << sft) == a.gs_stages) a.gs_shift = sft;
     a.out_vec = (reinterpret_cast<uintptr_t>(p.out) % 16 == 0) && (p.N % 4 == 0);
     a.tma_out = a.out_vec;
+    a.w_prefetch = mtiles <= 2;
     a.status = c.status_word;
     a.wait_ns = c.wait_limit_ns;
     a.skip_first_copy = c.tc_skip_first_copy;
@@ -642,6 +654,18 @@ cudaError_t tc_launch(const Problem& p, const LaunchCtx& c) {
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
+    CUtensorMap twp;  // the packed weights in blocks of kWPrefetch stages (L2 prefetch)
+    {
+        const int64_t Kp = p.K / 2;
+        const cuuint64_t dims[2] = {(cuuint64_t)Kp, (cuuint64_t)p.N};
+        const cuuint64_t strides[1] = {(cuuint64_t)Kp};
+        const cuuint32_t box[2] = {(cuuint32_t)(kWPrefetch * kStageK / 2), (cuuint32_t)bn};
+        const cuuint32_t estr[2] = {1, 1};
+        if (enc(&twp, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(p.qweight), dims,
+                strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
     CUtensorMap to = tx;  // unused unless a.tma_out
     if (a.tma_out) {
         // Non-split tiles: 32-column blocks in the 128-byte swizzle; split-K slices: sw
@@ -659,9 +683,10 @@ cudaError_t tc_launch(const Problem& p, const LaunchCtx& c) {
     const dim3 grid((unsigned)((p.N + bn - 1) / bn * splitk), (unsigned)mtiles);
     const bool eh = p.even_high != 0;
     if (bn > 128)
-        return eh ? launch2<2, true>(tx, tw, to, a, grid, c)
-                  : launch2<2, false>(tx, tw, to, a, grid, c);
-    return eh ? launch2<1, true>(tx, tw, to, a, grid, c) : launch2<1, false>(tx, tw, to, a, grid, c);
+        return eh ? launch2<2, true>(tx, tw, to, twp, a, grid, c)
+                  : launch2<2, false>(tx, tw, to, twp, a, grid, c);
+    return eh ? launch2<1, true>(tx, tw, to, twp, a, grid, c)
+              : launch2<1, false>(tx, tw, to, twp, a, grid, c);
 }
 
 }  // namespace q4lin
