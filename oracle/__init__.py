@@ -50,6 +50,10 @@ def _load():
         lib.q4o_linear_at.restype = i32
         lib.q4o_linear_qcs4w.argtypes = [vp, vp, vp, i32, vp, i64, i64, i64, dp, dp]
         lib.q4o_linear_qcs4w.restype = i32
+        lib.q4o_backward_dx.argtypes = [vp, vp, vp, i32, i64, i64, i64, i64, i32, dp, dp]
+        lib.q4o_backward_dx.restype = i32
+        lib.q4o_requant.argtypes = [vp, vp, i32, i64, i64, i64, i32, vp]
+        lib.q4o_requant.restype = i32
         _lib = lib
     return _lib
 
@@ -143,3 +147,45 @@ def linear_qcs4w(x, qweight, scales_n, bias, K: int) -> Tuple[np.ndarray, np.nda
     if rc != 0:
         raise ValueError("oracle rejected its arguments")
     return out, mag
+
+
+def backward_dx(d_out, qweight, scales, K: int, group_size: int,
+                even_high: bool = False) -> Tuple[np.ndarray, np.ndarray]:
+    """fp64 d_x[M,K] = d_out[M,N] @ dequant(W)[N,K] and mag[M,K] = sum_n |d_out * w|.
+
+    d_out: float32 [M,N]; qweight: uint8 [N, ceil(K/2)]; scales: float32 or float16
+    [ceil(K/group_size), N].
+    """
+    qweight = np.ascontiguousarray(qweight, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales)
+    N = qweight.shape[0]
+    d_out = np.ascontiguousarray(d_out, dtype=np.float32).reshape(-1, N)
+    M = d_out.shape[0]
+    if qweight.shape[1] != (K + 1) // 2:
+        raise ValueError("qweight must be [N, ceil(K/2)]")
+    if scales.size != -(-K // group_size) * N:
+        raise ValueError("scales must be [ceil(K/group_size), N]")
+    d_x = np.empty((M, K), np.float64)
+    mag = np.empty((M, K), np.float64)
+    rc = _load().q4o_backward_dx(_ptr(d_out), _ptr(qweight), _ptr(scales),
+                                 _scales_kind(scales), M, N, K, group_size, int(even_high),
+                                 _ptr(d_x), _ptr(mag))
+    if rc != 0:
+        raise ValueError("oracle rejected its arguments")
+    return d_x, mag
+
+
+def requant(latent, scales, group_size: int, even_high: bool = False) -> np.ndarray:
+    """Packed codes uint8 [N, ceil(K/2)] of fp32 latents [N,K] with frozen scales
+    [ceil(K/group_size), N]: clamp(round(latent / scale), -8, 7) + 8, zero scale -> 8."""
+    latent = np.ascontiguousarray(latent, dtype=np.float32)
+    scales = np.ascontiguousarray(scales)
+    N, K = latent.shape
+    if scales.size != -(-K // group_size) * N:
+        raise ValueError("scales must be [ceil(K/group_size), N]")
+    out = np.empty((N, (K + 1) // 2), np.uint8)
+    rc = _load().q4o_requant(_ptr(latent), _ptr(scales), _scales_kind(scales), N, K,
+                             group_size, int(even_high), _ptr(out))
+    if rc != 0:
+        raise ValueError("oracle rejected its arguments")
+    return out

@@ -184,3 +184,83 @@ int q4o_linear_qcs4w(const float* x, const uint8_t* qweight, const void* scales_
     }
     return Q4O_OK;
 }
+
+/* ------------------------------------------------------------ training-path ops
+ *
+ * Input gradient of the linear (the frozen 4-bit base during adapter training):
+ *
+ *   d_x[m,k] = sum_n d_out[m,n] * (nib(W)[n,k] - 8) * scale[k / group_size, n]
+ *
+ * "[ExecuTorch][WebGPU] Add fp32 matmul ops ... (linear_q4gsw_backward)", #20943:
+ * d_x[M,K] = d_out[M,N] @ dequant(W)[N,K], contracting over N, dequant(W[n,k]) =
+ * (code - 8) * scale with [num_groups, N] scales, on the same packed weight and scale
+ * layout as the forward.  n ascending, IEEE double; mag = sum_n |d_out * w| (the
+ * tolerance denominator).  OpenMP over the independent (m, k) elements. */
+int q4o_backward_dx(const float* d_out, const uint8_t* qweight, const void* scales,
+                    int scale_is_f16, int64_t M, int64_t N, int64_t K, int64_t group_size,
+                    int even_high, double* d_x, double* mag) {
+    if (M < 0 || N < 0 || K < 1 || group_size < 1) return Q4O_BAD_ARG;
+    if ((M > 0 && N > 0 && !d_out) || (N > 0 && (!qweight || !scales))) return Q4O_BAD_ARG;
+    int64_t row_bytes = (K + 1) / 2;
+    int64_t total = M * K;
+#pragma omp parallel for schedule(dynamic, 16)
+    for (int64_t i = 0; i < total; ++i) {
+        int64_t m = i / K, k = i % K;
+        double acc = 0.0, mg = 0.0;
+        for (int64_t n = 0; n < N; ++n) {
+            int q = nibble_at(qweight, row_bytes, n, k, even_high);
+            double w = (double)(q - 8) * scale_at(scales, scale_is_f16, N, k / group_size, n);
+            double p = (double)d_out[m * N + n] * w;
+            acc += p;
+            mg += fabs(p);
+        }
+        d_x[i] = acc;
+        mag[i] = mg;
+    }
+    return Q4O_OK;
+}
+
+/* Straight-through re-quantisation of fp32 latent weights [N, K] to the 4-bit codes with
+ * frozen scales, packed in the forward's layout [N, ceil(K/2)]:
+ *
+ *   code[n,k] = clamp(round(latent[n,k] / scale[k / group_size, n]), -8, 7) + 8,
+ *   a zero scale gives code 8.
+ *
+ * "[ExecuTorch][WebGPU] Add fp32 matmul ops ... (q4gsw_requant)", #20945 (the rule and
+ * the zero-scale case) and #20946 (its golden: round / clamp, zero scale -> code 8).
+ * Readings where the page is silent (also in the design notes):
+ *   - the quotient is an fp32 quotient (latents and scales are fp32 on the page, and the
+ *     integer decision is taken at that precision): it is computed in double and rounded
+ *     once to float, which for a division equals the IEEE fp32 quotient (53 >= 2*24 + 2);
+ *   - round() rounds half to even (the page's tests avoid ties);
+ *   - a NaN quotient gives code 8, like a zero scale;
+ *   - for odd K the padding nibble of the last byte is 8, the bias-zero code the page
+ *     writes for positions outside the matrix. */
+int q4o_requant(const float* latent, const void* scales, int scale_is_f16, int64_t N,
+                int64_t K, int64_t group_size, int even_high, uint8_t* qweight) {
+    if (N < 0 || K < 1 || group_size < 1) return Q4O_BAD_ARG;
+    if (N > 0 && (!latent || !scales || !qweight)) return Q4O_BAD_ARG;
+    int64_t row_bytes = (K + 1) / 2;
+#pragma omp parallel for schedule(static)
+    for (int64_t n = 0; n < N; ++n) {
+        for (int64_t b = 0; b < row_bytes; ++b) {
+            int codes[2] = {8, 8}; /* [even k, odd k] */
+            for (int j = 0; j < 2; ++j) {
+                int64_t k = 2 * b + j;
+                if (k >= K) break;
+                double s = scale_at(scales, scale_is_f16, N, k / group_size, n);
+                if (s == 0.0) continue;
+                float quotient = (float)((double)latent[n * K + k] / s);
+                if (isnan(quotient)) continue;
+                double r = rint((double)quotient);
+                if (r < -8.0) r = -8.0;
+                if (r > 7.0) r = 7.0;
+                codes[j] = (int)r + 8;
+            }
+            int low = even_high ? codes[1] : codes[0];
+            int high = even_high ? codes[0] : codes[1];
+            qweight[n * row_bytes + b] = (uint8_t)(low | (high << 4));
+        }
+    }
+    return Q4O_OK;
+}

@@ -201,8 +201,8 @@ MUTANTS = {
                              "int take_low = even_high ? k_is_even : !k_is_even;"),
     "offset 7 instead of 8": ("double w = (double)(q - 8) * s;",
                               "double w = (double)(q - 7) * s;"),
-    "group index k % gs": ("scale_at(scales, scale_is_f16, N, k / group_size, n)",
-                           "scale_at(scales, scale_is_f16, N, k % group_size, n)"),
+    "group index k % gs": ("double s = scale_at(scales, scale_is_f16, N, k / group_size, n);\n        double w",
+                           "double s = scale_at(scales, scale_is_f16, N, k % group_size, n);\n        double w"),
     # the worked example has G = 2 fp32 groups, so [n * 2 + g] reads scales as [N, G]
     "scale matrix transposed": ("((const float*)scales)[g * N + n]",
                                 "((const float*)scales)[n * 2 + g]"),
