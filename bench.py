@@ -398,6 +398,47 @@ def prefill_tflops(torch, handle, M, N, K, reps=10):
             "TFLOP_s": round(2.0 * M * N * K / (us * 1e-6) / 1e12, 2)}
 
 
+def backward_bandwidth(torch, handle, M, N, K):
+    """Input gradient d_x[M,K] = d_out[M,N] @ dequant(W): device time per launch (CUDA graph,
+    every launch on its own HBM-cold weight copy) and GB/s of the algorithmic bytes (packed
+    codes + fp16 scales read once per 8 rows of d_out, d_out, d_x)."""
+    from bit_weight_quantized_int4_gb300 import q4lin as q
+    wbytes = gemv_bytes(N, K) - 4 * K - 4 * N
+    ws, ss = weight_copies(torch, N, K, wbytes)
+    d_out = torch.randn(M, N, device="cuda")
+    d_x = torch.empty(M, K, device="cuda")
+
+    def launch(i, sp):
+        st = q.q4lin_run_backward_dx(handle, d_out.data_ptr(), ws[i % len(ws)].data_ptr(),
+                                     ss[i % len(ws)].data_ptr(), d_x.data_ptr(), M, N, K,
+                                     GROUP, q.Q4LIN_SCALE_F16, sp)
+        assert st == q.Q4LIN_OK
+
+    us = graph_time_us(torch, launch, len(ws))
+    byts = wbytes * (-(-M // 8)) + 4 * M * N + 4 * M * K
+    del ws, ss
+    return {"op": "backward_dx", "M": M, "N": N, "K": K, "us": round(us, 3),
+            "GB_s": round(byts / us / 1e3, 1)}
+
+
+def requant_bandwidth(torch, handle, N, K):
+    """Re-quantisation of fp32 latents [N,K]: device time and GB/s of latent + scales read
+    and packed codes written."""
+    from bit_weight_quantized_int4_gb300 import q4lin as q
+    latent = torch.randn(N, K, device="cuda") * 0.05
+    scales = (torch.rand((K // GROUP, N), device="cuda") * 0.015 + 0.005).half()
+    codes = torch.empty(N, K // 2, dtype=torch.uint8, device="cuda")
+
+    def launch(i, sp):
+        st = q.q4lin_run_requant(handle, latent.data_ptr(), scales.data_ptr(), codes.data_ptr(),
+                                 N, K, GROUP, q.Q4LIN_SCALE_F16, sp)
+        assert st == q.Q4LIN_OK
+
+    us = graph_time_us(torch, launch, 10)
+    byts = 4 * N * K + 2 * (K // GROUP) * N + N * K // 2
+    return {"op": "requant", "N": N, "K": K, "us": round(us, 3), "GB_s": round(byts / us / 1e3, 1)}
+
+
 # ------------------------------------------------------------------------- CPU baseline
 def cpu_baseline(min_seconds=10.0, row_fraction=8):
     """The fp64 oracle, as it stands, on the host cores: every matrix of a 1B decode
@@ -615,6 +656,10 @@ def main():
         extra["gemv_shapes"] = shapes
         extra["prefill"] = [prefill_tflops(torch, h, M, N, K)
                             for M in (128, 512, 2048) for N, K in PREFILL_NK]
+        extra["training"] = ([backward_bandwidth(torch, h, M, N, K)
+                              for M in (1, 8) for N, K in ((2048, 2048), (8192, 2048), (2048, 8192))]
+                             + [requant_bandwidth(torch, h, N, K)
+                                for N, K in ((2048, 2048), (8192, 2048), (2048, 8192))])
 
     line = {
         "metric": METRIC, "value": round(gbs, 1), "unit": "GB/s", "n_gpus": world,

@@ -342,6 +342,91 @@ q4lin_status_t q4lin_run_grouped(q4lin_handle_t h, const q4lin_problem_t* proble
     return Q4LIN_OK;
 }
 
+q4lin_status_t q4lin_run_backward_dx(q4lin_handle_t h, const float* d_out,
+                                     const uint8_t* qweight, const void* scales, float* d_x,
+                                     int64_t M, int64_t N, int64_t K, int64_t group_size,
+                                     int scale_dtype, void* stream) {
+    if (!h) return Q4LIN_ERR_INVALID_ARG;
+    if (M < 0 || N < 0 || K < 1 || group_size < 1) return Q4LIN_ERR_INVALID_ARG;
+    if (scale_dtype != Q4LIN_SCALE_F32 && scale_dtype != Q4LIN_SCALE_F16)
+        return Q4LIN_ERR_INVALID_ARG;
+    if (M == 0) return Q4LIN_OK;
+    if (!d_x || (N > 0 && (!d_out || !qweight || !scales))) return Q4LIN_ERR_INVALID_ARG;
+    const int64_t esize = scale_dtype == Q4LIN_SCALE_F16 ? 2 : 4;
+    const int64_t Kp = (K + 1) / 2;
+    const int64_t G = (K + group_size - 1) / group_size;
+    int64_t db, wb, sb, xb, t;
+    if (!mul_ok(M, N, &t) || !mul_ok(t, 4, &db)) return Q4LIN_ERR_INVALID_ARG;
+    if (!mul_ok(N, Kp, &wb)) return Q4LIN_ERR_INVALID_ARG;
+    if (!mul_ok(G, N, &t) || !mul_ok(t, esize, &sb)) return Q4LIN_ERR_INVALID_ARG;
+    if (!mul_ok(M, K, &t) || !mul_ok(t, 4, &xb)) return Q4LIN_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(d_x) % 4 || (d_out && reinterpret_cast<uintptr_t>(d_out) % 4) ||
+        (scales && reinterpret_cast<uintptr_t>(scales) % esize))
+        return Q4LIN_ERR_INVALID_ARG;
+    if (overlaps(d_x, xb, d_out, db) || overlaps(d_x, xb, qweight, wb) ||
+        overlaps(d_x, xb, scales, sb))
+        return Q4LIN_ERR_INVALID_ARG;
+    const q4lin::LaunchCtx c = make_ctx(h, static_cast<cudaStream_t>(stream));
+    DeviceGuard g(h->device);
+    if (!g.ok()) return Q4LIN_ERR_CUDA;
+    cudaError_t err;
+    if (N == 0) {
+        err = cudaMemsetAsync(d_x, 0, (size_t)xb, c.stream);
+    } else {
+        q4lin::TrainProblem p;
+        p.d_out = d_out;
+        p.qweight = qweight;
+        p.scales = scales;
+        p.d_x = d_x;
+        p.M = M;
+        p.N = N;
+        p.K = K;
+        p.group_size = group_size;
+        p.scale_f16 = scale_dtype == Q4LIN_SCALE_F16;
+        p.even_high = h->even_high;
+        err = q4lin::backward_dx_launch(p, c);
+    }
+    if (err == cudaSuccess) err = cudaGetLastError();
+    return err == cudaSuccess ? Q4LIN_OK : Q4LIN_ERR_CUDA;
+}
+
+q4lin_status_t q4lin_run_requant(q4lin_handle_t h, const float* latent, const void* scales,
+                                 uint8_t* qweight, int64_t N, int64_t K, int64_t group_size,
+                                 int scale_dtype, void* stream) {
+    if (!h) return Q4LIN_ERR_INVALID_ARG;
+    if (N < 0 || K < 1 || group_size < 1) return Q4LIN_ERR_INVALID_ARG;
+    if (scale_dtype != Q4LIN_SCALE_F32 && scale_dtype != Q4LIN_SCALE_F16)
+        return Q4LIN_ERR_INVALID_ARG;
+    if (N == 0) return Q4LIN_OK;
+    if (!latent || !scales || !qweight) return Q4LIN_ERR_INVALID_ARG;
+    const int64_t esize = scale_dtype == Q4LIN_SCALE_F16 ? 2 : 4;
+    const int64_t Kp = (K + 1) / 2;
+    const int64_t G = (K + group_size - 1) / group_size;
+    int64_t lb, wb, sb, t;
+    if (!mul_ok(N, K, &t) || !mul_ok(t, 4, &lb)) return Q4LIN_ERR_INVALID_ARG;
+    if (!mul_ok(N, Kp, &wb)) return Q4LIN_ERR_INVALID_ARG;
+    if (!mul_ok(G, N, &t) || !mul_ok(t, esize, &sb)) return Q4LIN_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(latent) % 4 || reinterpret_cast<uintptr_t>(scales) % esize)
+        return Q4LIN_ERR_INVALID_ARG;
+    if (overlaps(qweight, wb, latent, lb) || overlaps(qweight, wb, scales, sb))
+        return Q4LIN_ERR_INVALID_ARG;
+    const q4lin::LaunchCtx c = make_ctx(h, static_cast<cudaStream_t>(stream));
+    DeviceGuard g(h->device);
+    if (!g.ok()) return Q4LIN_ERR_CUDA;
+    q4lin::RequantProblem p;
+    p.latent = latent;
+    p.scales = scales;
+    p.qweight = qweight;
+    p.N = N;
+    p.K = K;
+    p.group_size = group_size;
+    p.scale_f16 = scale_dtype == Q4LIN_SCALE_F16;
+    p.even_high = h->even_high;
+    cudaError_t err = q4lin::requant_launch(p, c);
+    if (err == cudaSuccess) err = cudaGetLastError();
+    return err == cudaSuccess ? Q4LIN_OK : Q4LIN_ERR_CUDA;
+}
+
 q4lin_status_t q4lin_set_option(q4lin_handle_t h, int option, int64_t value) {
     if (!h) return Q4LIN_ERR_INVALID_ARG;
     switch (option) {

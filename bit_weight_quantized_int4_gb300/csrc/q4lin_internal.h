@@ -54,6 +54,25 @@ cudaError_t gemv_tma_launch_group(const Problem* ps, int count, const LaunchCtx&
 // Generic CUDA-core kernel: any K (odd included), any group size, any alignment.
 cudaError_t generic_launch(const Problem& p, const LaunchCtx& c);
 
+// Training-path problems on the same packed weights, validated by the host layer.
+struct TrainProblem {  // d_x[M,K] = d_out[M,N] @ dequant(W)[N,K]
+    const float* d_out;      // [M, N] fp32
+    const uint8_t* qweight;  // [N, ceil(K/2)]
+    const void* scales;      // [ceil(K/gs), N]
+    float* d_x;              // [M, K] fp32
+    int64_t M, N, K, group_size;
+    int scale_f16, even_high;
+};
+struct RequantProblem {  // qweight[N, ceil(K/2)] = pack(clamp(round(latent / scale), -8, 7) + 8)
+    const float* latent;  // [N, K] fp32
+    const void* scales;   // [ceil(K/gs), N]
+    uint8_t* qweight;     // [N, ceil(K/2)]
+    int64_t N, K, group_size;
+    int scale_f16, even_high;
+};
+cudaError_t backward_dx_launch(const TrainProblem& p, const LaunchCtx& c);
+cudaError_t requant_launch(const RequantProblem& p, const LaunchCtx& c);
+
 // tcgen05 tensor-core GEMM.  Eligibility and launch live in tc_gemm.cu.
 bool tc_eligible(const Problem& p, const LaunchCtx& c);
 cudaError_t tc_launch(const Problem& p, const LaunchCtx& c);

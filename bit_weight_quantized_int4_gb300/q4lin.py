@@ -63,6 +63,11 @@ _lib.q4lin_run_grouped.argtypes = [_vp, ctypes.POINTER(q4lin_problem_t), _i32, _
 _lib.q4lin_run_grouped.restype = _i32
 _lib.q4lin_run_static_scratch.argtypes = [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp]
 _lib.q4lin_run_static_scratch.restype = _i32
+_lib.q4lin_run_backward_dx.argtypes = [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i32,
+                                       _vp]
+_lib.q4lin_run_backward_dx.restype = _i32
+_lib.q4lin_run_requant.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp]
+_lib.q4lin_run_requant.restype = _i32
 _lib.q4lin_plan.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i32,
                             ctypes.POINTER(_i32)]
 _lib.q4lin_plan.restype = _i32
@@ -122,6 +127,20 @@ def q4lin_run_static_scratch(x, qweight, scales, bias, out, N, K, group_size, sc
     """Raw call of the allocation-free decode GEMV (pointers and stream as integers)."""
     return _lib.q4lin_run_static_scratch(x, qweight, scales, bias, out, N, K, group_size,
                                          scale_dtype, stream)
+
+
+def q4lin_run_backward_dx(handle, d_out, qweight, scales, d_x, M, N, K, group_size,
+                          scale_dtype, stream) -> int:
+    """Raw call: d_x[M,K] = d_out[M,N] @ dequant(W)[N,K] (pointers and stream as integers)."""
+    return _lib.q4lin_run_backward_dx(handle, d_out, qweight, scales, d_x, M, N, K,
+                                      group_size, scale_dtype, stream)
+
+
+def q4lin_run_requant(handle, latent, scales, qweight, N, K, group_size, scale_dtype,
+                      stream) -> int:
+    """Raw call: packed codes of fp32 latents [N,K] with frozen scales (integers as pointers)."""
+    return _lib.q4lin_run_requant(handle, latent, scales, qweight, N, K, group_size,
+                                  scale_dtype, stream)
 
 
 def q4lin_plan(handle, x, qweight, scales, bias, out, M, N, K, group_size, scale_dtype):

@@ -182,6 +182,49 @@ Q4LIN_API q4lin_status_t q4lin_run_static_scratch(const float* x, const uint8_t*
                                                   int64_t group_size, int scale_dtype,
                                                   void* stream);
 
+/* Input gradient of the linear on the same packed weights (the frozen 4-bit base of
+ * adapter training):
+ *
+ *   d_x[m,k] = sum_n d_out[m,n] * (nib(W)[n,k] - 8) * scale[k / group_size, n]
+ *
+ * "[ExecuTorch][WebGPU] Add fp32 matmul ops ... (linear_q4gsw_backward)", #20943:
+ * d_x[M,K] = d_out[M,N] @ dequant(W)[N,K], contracting over N, with the forward's weight
+ * and scale layout.
+ *   d_out   device fp32 [M, N] row-major (4-byte aligned)
+ *   qweight, scales, K, group_size, scale_dtype: exactly as q4lin_run (the handle's
+ *           Q4LIN_OPT_NIBBLE_EVEN_HIGH applies)
+ *   d_x     device fp32 [M, K] row-major (4-byte aligned); must not overlap any input
+ * Summation order over n is not specified (fp32 accumulation; results within
+ * 1e-5 * sum_n |d_out * w| + 1e-7 of the fp64 definition), but it is fixed for a given
+ * shape: repeated calls give identical bits.  M == 0 is Q4LIN_OK (nothing runs); N == 0
+ * writes zeros to d_x.  Uses the handle's workspace when the rows are split over CTAs
+ * (calls on one handle must be ordered on the GPU).  Validated before anything is
+ * enqueued; same status codes as q4lin_run. */
+Q4LIN_API q4lin_status_t q4lin_run_backward_dx(q4lin_handle_t handle, const float* d_out,
+                                               const uint8_t* qweight, const void* scales,
+                                               float* d_x, int64_t M, int64_t N, int64_t K,
+                                               int64_t group_size, int scale_dtype,
+                                               void* stream);
+
+/* Straight-through re-quantisation of fp32 latent weights to packed 4-bit codes with
+ * frozen scales, in the layout q4lin_run reads:
+ *
+ *   code[n,k] = clamp(round(latent[n,k] / scale[k / group_size, n]), -8, 7) + 8
+ *
+ * "[ExecuTorch][WebGPU] Add fp32 matmul ops ... (q4gsw_requant)", #20945: a zero scale
+ * gives code 8.  The quotient is the IEEE fp32 quotient, round() rounds half to even,
+ * a NaN quotient gives code 8, and for odd K the padding nibble of each row's last byte
+ * is 8.  Bit-exact (integer output).
+ *   latent  device fp32 [N, K] row-major (4-byte aligned)
+ *   scales  device fp32 or fp16 [ceil(K/group_size), N], as q4lin_run
+ *   qweight device uint8 [N, ceil(K/2)] output (low nibble = even k, or swapped when the
+ *           handle's Q4LIN_OPT_NIBBLE_EVEN_HIGH is set); must not overlap any input
+ * N == 0 is Q4LIN_OK (nothing runs).  Validated before anything is enqueued. */
+Q4LIN_API q4lin_status_t q4lin_run_requant(q4lin_handle_t handle, const float* latent,
+                                           const void* scales, uint8_t* qweight, int64_t N,
+                                           int64_t K, int64_t group_size, int scale_dtype,
+                                           void* stream);
+
 /* The path q4lin_run would take for these arguments (no launch, no device access);
  * *path_out receives a q4lin_path_t other than AUTO.  Same validation and status codes
  * as q4lin_run.  For M == 0 or N == 0, *path_out is Q4LIN_PATH_AUTO (nothing runs). */

@@ -68,6 +68,9 @@ def test_validation_rejects_before_device_work():
     assert st == q.Q4LIN_ERR_INVALID_ARG
     assert q.q4lin_set_option(None, q.Q4LIN_OPT_PDL, 1) == q.Q4LIN_ERR_INVALID_ARG
     assert q.q4lin_destroy(None) == q.Q4LIN_OK
+    assert (q.q4lin_run_backward_dx(None, 16, 16, 16, 4096, 1, 1, 32, 32, 0, None)
+            == q.Q4LIN_ERR_INVALID_ARG)
+    assert q.q4lin_run_requant(None, 16, 16, 4096, 1, 32, 32, 0, None) == q.Q4LIN_ERR_INVALID_ARG
 
 
 def test_create_without_gpu_reports_no_device():
