@@ -410,9 +410,15 @@ __global__ void __launch_bounds__(kThreadsG, 2)
                 if (finish) {
                     __threadfence();
                     if (j < V) {
-                        mine = 0.f;
-                        for (int q = 0; q < a.parts; ++q)
-                            mine += __ldcg(a.ws + (int64_t)q * a.ws_rows + vrow);
+                        // All parts' loads in flight together (parts <= 8); added in order.
+                        float t[8];
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            t[q] = q < a.parts ? __ldcg(a.ws + (int64_t)q * a.ws_rows + vrow) : 0.f;
+                        mine = t[0];
+#pragma unroll
+                        for (int q = 1; q < 8; ++q)
+                            if (q < a.parts) mine += t[q];
                     }
                     if (threadIdx.x == 0) a.tickets[blk] = 0;
                 }
