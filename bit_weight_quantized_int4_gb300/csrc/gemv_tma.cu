@@ -125,7 +125,7 @@ struct Cursor {
 __host__ __device__ constexpr int x_bytes(int x_chunks) { return x_chunks * kXPad * 4; }
 // Shared memory: the stage ring, then the barriers and flags (256 bytes), then x.
 inline int smem_bytes_g(int stages, uint32_t stage_bytes, int x_chunks) {
-    return 128 + stages * (int)stage_bytes + 256 + x_bytes(x_chunks);
+    return 1024 + stages * (int)stage_bytes + 256 + x_bytes(x_chunks);
 }
 
 __device__ __forceinline__ float load_scale(const void* scales, int f16, int64_t idx) {
@@ -171,6 +171,18 @@ __device__ __forceinline__ void stage_scales(uint32_t addr, float (&s)[V]) {
             s[0] = a;
         }
     }
+}
+
+// Byte offset of `off` within group row g of the staged scale block, whose rows are
+// IB = rows-per-block x scale-size bytes.  The block is staged with the TMA swizzle of its
+// row width (32, 64 or 128 bytes; none for 256): 16-byte unit u of row g sits at unit
+// u ^ f(g), so the 8 lanes of a quarter-warp, which read 8 different group rows at the
+// same offset, hit 8 different bank groups.
+template <int IB>
+__device__ __forceinline__ uint32_t scale_slot(int g, int off) {
+    if (IB > 128) return (uint32_t)(g * IB + off);
+    const int f = IB == 128 ? (g & 7) : IB == 64 ? ((g >> 1) & 3) : ((g >> 2) & 1);
+    return (uint32_t)(g * IB + ((((off >> 4) ^ f) << 4) | (off & 15)));
 }
 
 // Matrix that owns global row block blk (blk_begin ascending, matrix 0 begins at 0).
@@ -223,7 +235,7 @@ __global__ void __launch_bounds__(kThreadsG, 2)
     constexpr uint32_t esz = F16 ? 2 : 4;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
-    const uint32_t base = (raw + 127u) & ~127u;
+    const uint32_t base = (raw + 1023u) & ~1023u;  // stages are 1024-byte aligned
     uint8_t* gbase = smem_raw + (base - raw);
     const int S = a.stages;
     const uint32_t bar_base = base + (uint32_t)S * a.stage_bytes;
@@ -342,7 +354,7 @@ __global__ void __launch_bounds__(kThreadsG, 2)
     uint32_t s_off[H];
 #pragma unroll
     for (int h = 0; h < H; ++h)
-        s_off[h] = a.scale_off + (uint32_t)((((h * 16 + j) >> a.gs_shift) * rb + r0) * (int)esz);
+        s_off[h] = a.scale_off + scale_slot<rb * esz>((h * 16 + j) >> a.gs_shift, r0 * esz);
     // After a timed-out wait (`dead`) the warp still walks every item, without waiting or
     // computing, so that all consumer warps reach the same named barriers and every split-K
     // ticket is still counted and reset; nothing is stored.
@@ -519,7 +531,7 @@ uint32_t stage_bytes_for(int V, bool pc, int esz, int gs_shift, uint32_t* scale_
     const uint32_t sbytes = (uint32_t)(gps * rb * esz);
     *scale_off = wbytes;
     *tx = wbytes + sbytes;
-    return wbytes + ((sbytes + 127u) & ~127u);
+    return wbytes + ((sbytes + 1023u) & ~1023u);  // keeps every stage 1024-byte aligned
 }
 
 }  // namespace
@@ -647,9 +659,14 @@ cudaError_t gemv_tma_launch_group(const Problem* ps, int count, const LaunchCtx&
             const cuuint64_t strides[1] = {(cuuint64_t)(p.N * esz)};
             const cuuint32_t box[2] = {(cuuint32_t)rb, (cuuint32_t)gps};
             const cuuint32_t estr[2] = {1, 1};
+            const int ib = rb * esz;
+            const CUtensorMapSwizzle swz = ib == 32    ? CU_TENSOR_MAP_SWIZZLE_32B
+                                           : ib == 64  ? CU_TENSOR_MAP_SWIZZLE_64B
+                                           : ib == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                                       : CU_TENSOR_MAP_SWIZZLE_NONE;
             if (enc(&tm.s[i], p.scale_f16 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT32,
                     2, const_cast<void*>(p.scales), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                     CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
                 return cudaErrorInvalidValue;
         } else {
