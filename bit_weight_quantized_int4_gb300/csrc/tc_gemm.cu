@@ -39,7 +39,9 @@
 //   warps 4-19:       four groups of 4 warps (as many as there are stages in the ring, so
 //                     that a group always takes the same slot and waits on its barrier
 //                     phase by phase) taking stages in turn; thread = weight row
-//                     (its warp's lane quarter of tensor memory): it reads the row's 64
+//                     (its warp's lane quarter of tensor memory): once the MMAs that read
+//                     the stage's A slot last have completed (not waiting for the stage's
+//                     x, whose copy overlaps), it reads the row's 64
 //                     codes of the stage (two 16-byte chunks of the swizzled block row),
 //                     applies the group scales, stores the 64 values into the stage's A
 //                     columns, and arrives on "a_ready".  At the end each warp reads its 32
@@ -255,20 +257,29 @@ __global__ void __launch_bounds__(kThreads2, 1)
             for (int it = 0; it < n_iters; ++it) {  // it: stage of this CTA's range
                 const int s = it % S;
                 const uint32_t par = (it / S) & 1;
-                if (!wait_bounded(full(s), par, a.wait_ns, failed) ||
-                    !wait_bounded(aready(s), par, a.wait_ns, failed)) {
+                if (!wait_bounded(aready(s), par, a.wait_ns, failed) ||
+                    !wait_bounded(full(s), par, a.wait_ns, failed)) {
                     record_failure(a.status, failed);
                     break;
                 }
                 // A was written with tcgen05.st and fenced by its writers before they
                 // arrived; B (x) came by TMA.  The waits order both.
                 tc_fence_after();
+                // Descriptors: +2 in the address field per 32 bytes (K = 8 tf32) along the
+                // swizzle row, +xbox / 16 for the second box.
                 const uint32_t acol = tmem_d + (uint32_t)(kACol0 + kStageK * s);
-                const int nk = (int64_t)(it_begin + it) * kStageK + kHalfK < a.K ? 8 : 4;
-                for (int kk = 0; kk < nk; ++kk)
-                    mma_tf32_ts(tmem_d, acol + 8 * kk,
-                                sw128_desc(xslot(s) + (uint32_t)(kk >> 2) * xbox + (kk & 3) * 32),
-                                idesc, (it | kk) != 0);
+                const uint64_t d0 = sw128_desc(xslot(s));
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_tf32_ts(tmem_d, acol + 8 * kk, d0 + (uint64_t)(2 * kk), idesc,
+                                (it | kk) != 0);
+                if ((int64_t)(it_begin + it) * kStageK + kHalfK < a.K) {
+                    const uint64_t d1 = d0 + (uint64_t)(xbox >> 4);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_tf32_ts(tmem_d, acol + kHalfK + 8 * kk, d1 + (uint64_t)(2 * kk), idesc,
+                                    1u);
+                }
                 mma_commit(empty(s));
             }
             mma_commit(accfull);  // arrives once every MMA issued above has completed
@@ -316,14 +327,16 @@ __global__ void __launch_bounds__(kThreads2, 1)
                 if (it >= n_iters) break;
                 const int s = it % S;
                 const int bi = it / kWBlkStages, b = bi % kWSlots;
-                // full(s): the A slot's previous MMAs have completed (the producers waited
-                // for them); wfull(b): the packed weights have landed.
-                if (!wait_bounded(full(s), (it / S) & 1, a.wait_ns, failed) ||
+                // empty(s): the MMAs that read this A slot last have completed (the x copy
+                // of the stage may still be landing: dequantization overlaps it);
+                // wfull(b): the packed weights have landed.
+                if ((it >= S && !wait_bounded(empty(s), ((it / S) - 1) & 1, a.wait_ns, failed)) ||
                     !wait_bounded(wfull(b), (bi / kWSlots) & 1, a.wait_ns, failed)) {
                     record_failure(a.status, failed);
                     ok = false;
                     break;
                 }
+                tc_fence_after();
                 // Chunk c of the block row sits at chunk c ^ (r % 8) (128-byte swizzle).
                 const int c0 = 2 * (it % kWBlkStages);
                 const uint32_t rowp = wslot(b) + (uint32_t)r * 128;
