@@ -78,6 +78,7 @@ constexpr int kWRows = 128;                  // weight rows per tile (MMA M = TM
 constexpr int kStageK = 64;                  // k per stage: two 128-byte swizzle rows of x
 constexpr int kHalfK = 32;
 constexpr int kMaxStages = 4;                // A ring: 4 x 64 tensor-memory columns
+static_assert(kMaxStages <= kGroups, "one dequantizing group per ring slot");
 constexpr int kWBlkStages = 4;               // stages per packed-weight block (128 B a row)
 constexpr int kWBlkBytes = kWRows * 128;     // 16 KiB
 constexpr int kWSlots = 2;
@@ -207,10 +208,11 @@ __global__ void __launch_bounds__(kThreads2, 1)
             // ------------------------------------------------------ TMA producers of x
             const int j = warp >> 1;  // which 32-k half of every stage
             prefetch_tensormap(&tmap_x);
-            int li = 0;
-            for (; li < n_iters; ++li) {
-                const int s = li % S;
-                if (li >= S && !wait_bounded(empty(s), ((li / S) - 1) & 1, a.wait_ns, failed)) {
+            // Slot and phase kept incrementally (no divisions on this serial path).
+            int li = 0, s = 0;
+            uint32_t ph = 0;  // parity of the slot's current use
+            for (; li < n_iters; ++li, s = (s + 1 == S) ? 0 : s + 1, ph ^= (s == 0)) {
+                if (li >= S && !wait_bounded(empty(s), ph ^ 1u, a.wait_ns, failed)) {
                     record_failure(a.status, failed);
                     break;
                 }
@@ -254,9 +256,11 @@ __global__ void __launch_bounds__(kThreads2, 1)
         if (lane == 0) {
             // ------------------------------------------------------------- MMA issuer
             const uint32_t idesc = tf32_idesc(kWRows, bt);
-            for (int it = 0; it < n_iters; ++it) {  // it: stage of this CTA's range
-                const int s = it % S;
-                const uint32_t par = (it / S) & 1;
+            const int64_t k_two = a.K - kHalfK - (int64_t)it_begin * kStageK;
+            int s = 0;
+            uint32_t par = 0;
+            for (int it = 0; it < n_iters;  // it: stage of this CTA's range
+                 ++it, s = (s + 1 == S) ? 0 : s + 1, par ^= (s == 0)) {
                 if (!wait_bounded(aready(s), par, a.wait_ns, failed) ||
                     !wait_bounded(full(s), par, a.wait_ns, failed)) {
                     record_failure(a.status, failed);
@@ -273,7 +277,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
                 for (int kk = 0; kk < 4; ++kk)
                     mma_tf32_ts(tmem_d, acol + 8 * kk, d0 + (uint64_t)(2 * kk), idesc,
                                 (it | kk) != 0);
-                if ((int64_t)(it_begin + it) * kStageK + kHalfK < a.K) {
+                if ((int64_t)it * kStageK < k_two) {
                     const uint64_t d1 = d0 + (uint64_t)(xbox >> 4);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
@@ -288,7 +292,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
     } else {
         // ------------------------------------------------- dequantization, epilogue
         const int group = (warp - kCtlWarps) >> 2;
-        const int G = min(S, kGroups);  // dequantizing groups: group g takes slot g
+        const int G = S;  // dequantizing groups (S <= kGroups): group g always takes slot g
         const int quarter = warp & 3;  // the 32-lane slice of tensor memory this warp owns
         const int r = quarter * 32 + lane;  // this thread's weight row in the tile
         const int64_t n = n0 + r;
@@ -320,17 +324,18 @@ __global__ void __launch_bounds__(kThreads2, 1)
             ring[u][1] = fetch(group + u * G, 1);
         }
         const int stride = kScaleAhead * G;
+        const int s = group;
+        uint32_t ph = 0;  // parity of the slot's current use (this group's stage count)
         for (int it0 = group; group < G && it0 < n_iters && ok; it0 += stride) {
 #pragma unroll
-            for (int u = 0; u < kScaleAhead; ++u) {
+            for (int u = 0; u < kScaleAhead; ++u, ph ^= 1u) {
                 const int it = it0 + u * G;
                 if (it >= n_iters) break;
-                const int s = it % S;
                 const int bi = it / kWBlkStages, b = bi % kWSlots;
                 // empty(s): the MMAs that read this A slot last have completed (the x copy
                 // of the stage may still be landing: dequantization overlaps it);
                 // wfull(b): the packed weights have landed.
-                if ((it >= S && !wait_bounded(empty(s), ((it / S) - 1) & 1, a.wait_ns, failed)) ||
+                if ((it >= S && !wait_bounded(empty(s), ph ^ 1u, a.wait_ns, failed)) ||
                     !wait_bounded(wfull(b), (bi / kWSlots) & 1, a.wait_ns, failed)) {
                     record_failure(a.status, failed);
                     ok = false;
