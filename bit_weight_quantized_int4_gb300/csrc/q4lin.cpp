@@ -35,7 +35,7 @@ namespace {
 
 constexpr int64_t kDefaultWaitLimit = 2000000000LL;  // 2 s of GPU global time
 // Scratch of a handle: partial sums of split-K launches and their row-block counters.
-constexpr int64_t kWsFloats = 1 << 19;   // 2 MiB
+constexpr int64_t kWsFloats = 1 << 23;   // 32 MiB (split-K partials: GEMV, backward, TC)
 constexpr int64_t kTickets = 1 << 14;    // 64 KiB
 
 // M-dispatch between the row-streaming CUDA-core kernel (which re-reads the weights for

@@ -52,9 +52,9 @@
 //   When K % 64 == 32 the last stage has one half: its second box is not loaded, its
 //   second half of A not written and its last 4 MMAs not issued.
 //   Split K (few tiles): the CTAs of a cluster take disjoint K ranges of one tile; each
-//                     stages its partial tile in shared memory as one padded block per
-//                     destination rank; rank q reads its column slice of every block with
-//                     ld.shared::cluster, adds them in rank order (deterministic) and
+//                     writes the other ranks' columns of its partial tile to the workspace,
+//                     and after a cluster barrier rank q adds the P partials of its column
+//                     slice in rank order (deterministic; its own from tensor memory) and
 //                     stores the slice.
 // Every mbarrier wait is bounded in time; a timeout records code 1 in the status word,
 // after which the CTA stops issuing work, drains its copies and MMAs, frees its tensor
@@ -112,8 +112,9 @@ struct Tc2Args {
     int skip_first_copy;
     // Split K over a cluster of `splitk` CTAs (1: no split): CTA rank r of the cluster
     // covers stages [r * kpp, (r + 1) * kpp) of the tile; rank q finishes the activation
-    // rows [q * sw, (q + 1) * sw) of the tile (exchange block row stride rs floats).
-    int splitk, kpp, sw, rs;
+    // rows [q * sw, (q + 1) * sw) of the tile.
+    int splitk, kpp, sw;
+    float* ws;  // split K: [tiles][P][P - 1][sw][128] partial columns exchanged through L2
 };
 
 __device__ __forceinline__ float load_scale(const void* scales, int f16, int64_t idx) {
@@ -197,17 +198,22 @@ __global__ void __launch_bounds__(kThreads2, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_d = *tmem_slot_ptr;
-    if (P > 1) cluster_sync_all();  // peers read this CTA's shared memory only later
-    griddep_wait();
+    // Programmatic dependent launch: the next grid may start launching now (its CTAs
+    // become resident as this grid's leave).  Packed weights and scales do not depend on
+    // the preceding grid and stream at once; x is loaded, and bias, out and the workspace
+    // are touched, only after griddepcontrol.wait (x producers, epilogue threads).
+    griddep_launch_dependents();
 
     const int64_t n0 = (int64_t)wtile * kWRows;
     const int64_t m0 = (int64_t)blockIdx.y * bt;
     bool epi_go = false;  // dequantization warps: the accumulator is complete and valid
+    float row_cs = 1.f, row_b = 0.f;  // dequantization warps: channel scale, bias of row r
     if (warp == 0 || warp == 2) {
         if (lane == 0) {
             // ------------------------------------------------------ TMA producers of x
             const int j = warp >> 1;  // which 32-k half of every stage
             prefetch_tensormap(&tmap_x);
+            griddep_wait();
             // Slot and phase kept incrementally (no divisions on this serial path).
             int li = 0, s = 0;
             uint32_t ph = 0;  // parity of the slot's current use
@@ -298,10 +304,11 @@ __global__ void __launch_bounds__(kThreads2, 1)
         const int64_t n = n0 + r;
         const bool rvalid = n < a.N;
         const uint32_t lane_base = tmem_d + ((uint32_t)(quarter * 32) << 16);
-        // The row's channel scale and bias, loaded now (their latency overlaps the loop).
+        // The row's channel scale, loaded now (its latency overlaps the loop); the bias
+        // after the dependency wait below.
         const float cscale =
             (rvalid && a.per_channel) ? load_scale(a.scales, a.scale_f16, n) : 1.f;
-        const float rbias = (rvalid && a.bias) ? __ldg(a.bias + n) : 0.f;
+        row_cs = cscale;
         bool ok = true;
         // Group scales (raw bits) of this row for its group's stages (both halves),
         // kScaleAhead stages ahead; the loop is unrolled by the ring size so every slot is
@@ -371,79 +378,95 @@ __global__ void __launch_bounds__(kThreads2, 1)
         }
         const bool acc_ok = wait_bounded(accfull, 0, ok ? a.wait_ns : kDrainNs, nullptr);
         if (!acc_ok) record_failure(a.status, failed);
+        griddep_wait();  // (long complete by now: the x copies waited for it)
+        const float rbias = (rvalid && a.bias) ? __ldg(a.bias + n) : 0.f;
+        row_b = rbias;
         tc_fence_after();
         const bool go = __all_sync(0xffffffffu, acc_ok && !*failed);
         epi_go = go;
         if (go && P == 1) {
-            // For one activation row the 32 lanes store 32 consecutive n (whole lines).
-            for (int c0 = 16 * group; c0 < bt; c0 += 16 * kGroups) {
-                uint32_t v[16];
-                tmem_ld16(lane_base + (uint32_t)c0, v);
+            // Columns in chunks of 32 (one load and one wait each), the groups in turn; for
+            // one activation row the 32 lanes store 32 consecutive n (whole lines).
+            for (int c0 = 32 * group; c0 < bt; c0 += 32 * kGroups) {
+                uint32_t v[32];
+                tmem_ld32(lane_base + (uint32_t)c0, v);
                 if (!rvalid) continue;
+                float* dst = a.out + (m0 + c0) * a.N + n;
+                const int64_t rows = a.M - (m0 + c0);
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int64_t m = m0 + c0 + j;
-                    if (m < a.M) a.out[m * a.N + n] = __uint_as_float(v[j]) * cscale + rbias;
-                }
+                for (int j = 0; j < 32; ++j)
+                    if (j < rows) dst[(int64_t)j * a.N] = __uint_as_float(v[j]) * cscale + rbias;
             }
         }
     }
     if (P > 1) {
         // ------------------------------------------- split K: reduce over the cluster
-        // Shared memory (the free x ring): send blocks [P][128][rs] (block q: the
-        // activation columns [q * sw, (q + 1) * sw) of this CTA's partial tile, rows padded
-        // to rs floats).  Every thread reaches both cluster barriers: all earlier waits in
-        // this kernel are bounded in time.
-        const uint32_t blk_bytes = (uint32_t)(kWRows * a.rs * 4);
+        // Rank q owns the activation columns [q * sw, (q + 1) * sw) of the tile.  Every
+        // CTA writes the other ranks' columns of its partial tile from tensor memory to
+        // the workspace (slot j of a destination holds the partial of its j-th other rank,
+        // in rank order; column-major, so the 32 lanes of a warp write 128 contiguous
+        // bytes), the cluster barrier orders those writes before the reads, and each rank
+        // adds the P partials of its columns in rank order (its own from tensor memory),
+        // reading the peers' through L2, and stores.  (Distributed shared memory moved
+        // these bytes several times slower than L2 on this part.)
+        const int64_t tile_id = (int64_t)blockIdx.y * (gridDim.x / P) + wtile;
+        float* wst = a.ws + tile_id * (int64_t)(P - 1) * kWRows * bt;
         if (warp >= kCtlWarps && epi_go) {
             const int group = (warp - kCtlWarps) >> 2;
             const int quarter = warp & 3;
             const int r = quarter * 32 + lane;
             const uint32_t lane_base = tmem_d + ((uint32_t)(quarter * 32) << 16);
             for (int c0 = 16 * group; c0 < bt; c0 += 16 * kGroups) {
+                const int q = c0 / a.sw;
+                if (q == rank) continue;
                 uint32_t v[16];
                 tmem_ld16(lane_base + (uint32_t)c0, v);
-                const int q = c0 / a.sw, cl = c0 - q * a.sw;
-                const uint32_t dst =
-                    base + (uint32_t)q * blk_bytes + (uint32_t)((r * a.rs + cl) * 4);
+                const int j = rank < q ? rank : rank - 1;  // this CTA's slot at rank q
+                float* dst = wst + ((int64_t)(q * (P - 1) + j) * a.sw + (c0 - q * a.sw)) * kWRows + r;
 #pragma unroll
-                for (int v4 = 0; v4 < 4; ++v4)
-                    st_shared_v4(dst + 16 * v4, __uint_as_float(v[4 * v4]),
-                                 __uint_as_float(v[4 * v4 + 1]), __uint_as_float(v[4 * v4 + 2]),
-                                 __uint_as_float(v[4 * v4 + 3]));
+                for (int t = 0; t < 16; ++t) dst[t * kWRows] = __uint_as_float(v[t]);
             }
         }
-        // 1. Every CTA of the cluster has staged its send blocks.
+        // Every thread reaches this barrier (all earlier waits are bounded in time); its
+        // release / acquire at cluster scope orders the workspace writes before the reads.
         cluster_sync_all();
-        // 2. This CTA's activation-column slice: read block `rank` of every CTA (remote
-        //    shared-memory loads, 4 columns at a time), add them in rank order, apply the
-        //    channel scale and bias; consecutive threads store consecutive n.
-        if (warp >= kCtlWarps && __all_sync(0xffffffffu, epi_go)) {
-            const int cbase = rank * a.sw;
-            const uint32_t my_blk = base + (uint32_t)rank * blk_bytes;
-            const int cells = kWRows * (a.sw / 4);
-            for (int idx = threadIdx.x - 32 * kCtlWarps; idx < cells; idx += 128 * kGroups) {
-                const int r = idx & (kWRows - 1), c = (idx >> 7) * 4;
-                const int64_t n = n0 + r;
-                const uint32_t off = my_blk + (uint32_t)((r * a.rs + c) * 4);
-                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (warp >= kCtlWarps && __all_sync(0xffffffffu, epi_go && !*failed)) {
+            const int group = (warp - kCtlWarps) >> 2;
+            const int quarter = warp & 3;
+            const int r = quarter * 32 + lane;
+            const int64_t n = n0 + r;
+            const uint32_t lane_base = tmem_d + ((uint32_t)(quarter * 32) << 16);
+            for (int c0 = 16 * group; c0 < a.sw; c0 += 16 * kGroups) {
+                uint32_t own[16];
+                tmem_ld16(lane_base + (uint32_t)(rank * a.sw + c0), own);
+                float acc[16];
+#pragma unroll
+                for (int t = 0; t < 16; ++t) acc[t] = 0.f;
                 for (int q = 0; q < P; ++q) {
-                    const float4 t = ld_cluster_v4(map_shared_rank(off, (uint32_t)q));
-                    v.x += t.x, v.y += t.y, v.z += t.z, v.w += t.w;
-                }
-                if (n >= a.N || *failed) continue;
-                const float cs = a.per_channel ? load_scale(a.scales, a.scale_f16, n) : 1.f;
-                const float b = a.bias ? __ldg(a.bias + n) : 0.f;
-                const float vals[4] = {v.x, v.y, v.z, v.w};
+                    if (q == rank) {
 #pragma unroll
-                for (int t = 0; t < 4; ++t) {
-                    const int64_t m = m0 + cbase + c + t;
-                    if (m < a.M) a.out[m * a.N + n] = vals[t] * cs + b;
+                        for (int t = 0; t < 16; ++t) acc[t] += __uint_as_float(own[t]);
+                    } else {
+                        const int j = q < rank ? q : q - 1;
+                        const float* src =
+                            wst + ((int64_t)(rank * (P - 1) + j) * a.sw + c0) * kWRows + r;
+                        float in[16];
+#pragma unroll
+                        for (int t = 0; t < 16; ++t) in[t] = __ldcg(src + t * kWRows);
+#pragma unroll
+                        for (int t = 0; t < 16; ++t) acc[t] += in[t];
+                    }
+                }
+                // For one activation row the 32 lanes store 32 consecutive n; the row's
+                // channel scale and bias (row_cs, row_b) were loaded before the main loop.
+                if (n < a.N) {
+                    const int64_t mb = m0 + rank * a.sw + c0;
+#pragma unroll
+                    for (int t = 0; t < 16; ++t)
+                        if (mb + t < a.M) a.out[(mb + t) * a.N + n] = acc[t] * row_cs + row_b;
                 }
             }
         }
-        // 3. No CTA leaves while another may still read its send blocks.
-        cluster_sync_all();
     }
     if (warp >= kCtlWarps) tc_fence_before();
     __syncthreads();
@@ -601,11 +624,11 @@ cudaError_t tc_launch(const Problem& p, const LaunchCtx& c) {
         }
     }
     const int stages = stages_for_bt(bt, c);
-    // The split-K exchange (send blocks [P][128][sw + 4] floats) must fit in the ring.
-    while (splitk > 1 &&
-           (int64_t)splitk * kWRows * (bt / splitk + 4) * 4 > (int64_t)stages * stage_bytes(bt))
-        splitk /= 2;
     const int64_t mtiles = (p.M + bt - 1) / bt;
+    // The split-K exchange ([tiles][P - 1][128][bt] floats) must fit in the workspace.
+    while (splitk > 1 &&
+           (!c.ws || wtiles * mtiles * (splitk - 1) * kWRows * bt > c.ws_floats))
+        splitk /= 2;
 
     Tc2Args a;
     a.scales = p.scales;
@@ -622,7 +645,7 @@ cudaError_t tc_launch(const Problem& p, const LaunchCtx& c) {
     a.splitk = splitk;
     a.kpp = k_iters / splitk;
     a.sw = bt / splitk;
-    a.rs = a.sw + 4;
+    a.ws = c.ws;
     a.gs_halves = a.per_channel ? 1 : (int)(p.group_size / kHalfK);
     a.gs_shift = -1;
     for (int sft = 0; sft < 31; ++sft)

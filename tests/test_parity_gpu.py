@@ -388,6 +388,50 @@ def test_dependent_chain(handle, pdl):
         assert_parity(host[i + 1][None, :], ref, mag, TOL_FP32)
 
 
+@pytest.mark.parametrize("pdl", [0, 1])
+@pytest.mark.parametrize("M", [96, 300])
+def test_tc_dependent_chain(handle, pdl, M):
+    """Tensor-core GEMMs chained on one stream, each reading the previous output as its x,
+    every buffer NaN-poisoned first.  With programmatic dependent launch the kernel
+    streams packed weights before the dependency wait but loads x, reads the bias and
+    writes out only after it; each link is checked against the oracle applied to the
+    input it actually received.  M = 300 takes several activation tiles, M = 96 few
+    tiles with K split over clusters (workspace exchange)."""
+    import torch
+    from bit_weight_quantized_int4_gb300 import q4lin as q
+    dims = [512, 1024, 256, 768, 2048]
+    links = []
+    for i in range(len(dims) - 1):
+        K, N = dims[i], dims[i + 1]
+        links.append(synth.make_case(M, N, K, 32, scale_f16=(i % 2 == 1), bias=(i % 2 == 0),
+                                     seed=700 + i + M))
+    bufs = [torch.from_numpy(np.ascontiguousarray(links[0].x)).cuda()]
+    bufs += [torch.full((M, d), float("nan"), device="cuda") for d in dims[1:]]
+    dev = [tuple(None if a is None else torch.from_numpy(a).cuda()
+                 for a in (c.qweight, c.scales, c.bias)) for c in links]
+    torch.cuda.synchronize()
+    q.q4lin_set_option(handle, q.Q4LIN_OPT_PDL, pdl)
+    q.q4lin_set_option(handle, q.Q4LIN_OPT_FORCE_PATH, TC)
+    try:
+        stream = torch.cuda.current_stream().cuda_stream
+        for i, c in enumerate(links):
+            w, s, b = dev[i]
+            sd = q.Q4LIN_SCALE_F16 if c.scales.dtype == np.float16 else q.Q4LIN_SCALE_F32
+            st = q.q4lin_run(handle, bufs[i].data_ptr(), w.data_ptr(), s.data_ptr(),
+                             None if b is None else b.data_ptr(), bufs[i + 1].data_ptr(),
+                             M, c.N, c.K, 32, sd, stream)
+            assert st == q.Q4LIN_OK
+        torch.cuda.synchronize()
+    finally:
+        q.q4lin_set_option(handle, q.Q4LIN_OPT_PDL, 0)
+        q.q4lin_set_option(handle, q.Q4LIN_OPT_FORCE_PATH, AUTO)
+    host = [b.cpu().numpy() for b in bufs]
+    for i, c in enumerate(links):
+        assert not np.isnan(host[i + 1]).any(), f"link {i} output has NaN"
+        ref, mag = oracle.linear(host[i], c.qweight, c.scales, c.bias, c.K, 32)
+        assert_parity(host[i + 1], ref, mag, TOL_TC)
+
+
 # ------------------------------------------------------------- split K (decode GEMV)
 @pytest.mark.parametrize("N,K,gs", [(512, 8192, 32), (64, 4096, 64), (2048, 2048, 32),
                                     (1000, 8192, 8192), (2047, 14336, 128)])
