@@ -444,27 +444,6 @@ __global__ void __launch_bounds__(kThreadsG, 2)
     }
 }
 
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                             &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
-        else
-            cudaGetLastError();
-    });
-    return fn;
-}
-
 template <int V, bool EH, bool PC, bool F16>
 cudaError_t launch_v(const TensorMaps& tm, const GArgs& a, unsigned grid, const LaunchCtx& c) {
     static cudaError_t attr = [] {
@@ -536,6 +515,22 @@ uint32_t stage_bytes_for(int V, bool pc, int esz, int gs_shift, uint32_t* scale_
 
 }  // namespace
 
+EncodeTiledFn tensor_map_encoder() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
 bool gemv_tma_eligible(const Problem& p) {
     if (p.M != 1 || p.K % 32 != 0 || p.K < 512 || p.N < 16) return false;
     if (p.N > (1LL << 30) || p.K > (1LL << 24)) return false;
@@ -555,7 +550,7 @@ bool gemv_tma_eligible(const Problem& p) {
     const uint32_t sb1 = stage_bytes_for(1, pc, p.scale_f16 ? 2 : 4,
                                          pc ? 0 : log2_exact(p.group_size / 32), &so, &tx);
     if (smem_bytes_g(2, sb1, x_chunks) > kCtaSmem) return false;
-    return encode_fn() != nullptr;
+    return tensor_map_encoder() != nullptr;
 }
 
 int gemv_tma_max_group() { return kMaxMats; }
@@ -567,7 +562,7 @@ bool gemv_tma_groupable(const Problem& a, const Problem& b) {
 }
 
 cudaError_t gemv_tma_launch_group(const Problem* ps, int count, const LaunchCtx& c) {
-    EncodeTiledFn enc = encode_fn();
+    EncodeTiledFn enc = tensor_map_encoder();
     if (!enc || count < 1 || count > kMaxMats) return cudaErrorNotSupported;
     const Problem& p0 = ps[0];
     const bool pc = p0.group_size >= p0.K;

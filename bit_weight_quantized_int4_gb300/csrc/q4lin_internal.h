@@ -2,10 +2,19 @@
 // Not installed; the public interface is include/q4lin.h.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 namespace q4lin {
+
+// cuTensorMapEncodeTiled of the driver, resolved once through the runtime (null when the
+// driver does not provide it); used by every TMA-fed kernel to build its tensor maps.
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn tensor_map_encoder();
 
 // One linear problem, already validated by the host layer.
 struct Problem {

@@ -476,27 +476,6 @@ __global__ void __launch_bounds__(kThreads2, 1)
     }
 }
 
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                             &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
-        else
-            cudaGetLastError();
-    });
-    return fn;
-}
-
 template <bool EH>
 cudaError_t kernel_attr() {
     static cudaError_t attr = cudaFuncSetAttribute(
@@ -586,11 +565,11 @@ bool tc_eligible(const Problem& p, const LaunchCtx& c) {
     if (!(p.group_size >= p.K || p.group_size % kHalfK == 0)) return false;
     if (p.M > 65535LL * 64 || p.N > (1LL << 31) - 1) return false;
     if (c.max_smem_optin < smem_bytes(256, 2)) return false;
-    return encode_fn() != nullptr;
+    return tensor_map_encoder() != nullptr;
 }
 
 cudaError_t tc_launch(const Problem& p, const LaunchCtx& c) {
-    EncodeTiledFn enc = encode_fn();
+    EncodeTiledFn enc = tensor_map_encoder();
     if (!enc) return cudaErrorNotSupported;
     // Activation rows per tile (the MMA's N) and the split of K over a cluster.  Wider
     // tiles make wider MMAs; narrower ones give more CTAs.  When the tiles alone leave SMs

@@ -19,6 +19,12 @@
 //     over several CTAs (few k tiles), each writes its partial [MT, 256] tile to the
 //     handle's workspace and the last CTA of the k tile (an atomic ticket) adds the parts
 //     in split order: the result does not depend on which CTA finishes last.
+//   backward_tma_kernel (the fast path when the tensors suit TMA): the same CTA tile of
+//     256 k, fed by a producer warp that streams per stage the weight tile [64 rows x
+//     128 B], the group scales of those rows [groups of the tile x 64] and d_out
+//     [MT x 64] into a shared-memory ring with one TMA copy each; 8 consumer warps take
+//     every 8th row of a stage (lane = 32-bit word of codes, 8 k).  The rows are split
+//     over CTAs (multiples of 64 rows each); partials are added like above.
 //   backward_dx_generic_kernel: one thread per (m, k), n ascending; any K, any group size,
 //     any alignment.
 //
@@ -203,6 +209,216 @@ __global__ void backward_dx_generic_kernel(const BwArgs a) {
     }
 }
 
+// ------------------------------------------------------- TMA-fed input gradient
+constexpr int kBtCWarps = 8;                       // consumer warps
+constexpr int kBtThreads = 32 * kBtCWarps + 32;    // + the producer warp
+constexpr int kBtKT = 256;                         // k per CTA tile: 128 bytes of a row
+constexpr int kBtRB = 64;                          // weight rows per stage
+constexpr int kBtMaxStages = 8;
+constexpr int64_t kDrainNs = 4000000000LL;
+constexpr uint32_t kBtScOff = kBtRB * kBtKT / 2;   // 8 KiB of codes, then the scales
+constexpr uint32_t kBtDoOff = kBtScOff + 2048;     // then d_out [MT x 64]
+
+struct BtMaps {
+    CUtensorMap w;   // uint8 [N, Kp], box {128, 64}
+    CUtensorMap s;   // scales [G, N] (fp16 / fp32), box {64, GT}
+    CUtensorMap d;   // d_out fp32 [M, N], box {64, MT}
+};
+
+struct BtArgs {
+    float* d_x;
+    float* ws;     // [m tiles x k tiles][splits][MT][256] partials (splits > 1)
+    int* tickets;  // [m tiles x k tiles], zero between launches
+    int* status;
+    int64_t M, N, K;
+    int gs_in_tile;       // group size when a k tile holds whole groups (gs <= 256), else 0
+    int gs_shift256;      // then: group row of k tile kt = kt << gs_shift256
+    int tiles_per_group;  // else: group row = kt / tiles_per_group
+    int scale_f16, even_high;
+    int splits, stages;
+    int64_t rows_per_split;  // multiple of 64
+    uint32_t stage_bytes, tx;
+    int64_t wait_ns;
+};
+
+// grid: x = k tile, y = split of the rows, z = tile of MT rows of d_out.
+template <int MT>
+__global__ void __launch_bounds__(kBtThreads, 2)
+    backward_tma_kernel(const __grid_constant__ BtMaps maps, const BtArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* gbase = smem_raw + (base - raw);
+    const int S = a.stages;
+    // The partial-tile reduction reuses the ring: max(ring, [8 warps][MT][256] floats).
+    const uint32_t ring = (uint32_t)S * a.stage_bytes;
+    const uint32_t red_bytes = (uint32_t)kBtCWarps * MT * kBtKT * 4;
+    const uint32_t bar_base = base + (ring > red_bytes ? ring : red_bytes);
+    volatile int* failed = reinterpret_cast<volatile int*>(gbase + (bar_base + 16 * kBtMaxStages - base));
+    volatile int* s_last = failed + 1;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    auto full = [&](int s) { return bar_base + 8u * s; };
+    auto empty = [&](int s) { return bar_base + 8u * (kBtMaxStages + s); };
+
+    const int kt = (int)blockIdx.x;
+    const int64_t m0 = (int64_t)blockIdx.z * MT;
+    const int64_t n_begin = (int64_t)blockIdx.y * a.rows_per_split;
+    const int64_t n_end = n_begin + a.rows_per_split < a.N ? n_begin + a.rows_per_split : a.N;
+    const int nst = n_end > n_begin ? (int)((n_end - n_begin + kBtRB - 1) / kBtRB) : 0;
+    const int g_row = a.gs_in_tile ? kt << a.gs_shift256 : kt / a.tiles_per_group;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full(s), 1);
+            mbar_init(empty(s), kBtCWarps);
+        }
+        *failed = 0;
+        mbar_init_fence();
+    }
+    __syncthreads();
+    griddep_launch_dependents();
+
+    if (warp == kBtCWarps) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            prefetch_tensormap(&maps.w);
+            prefetch_tensormap(&maps.s);
+            prefetch_tensormap(&maps.d);
+            griddep_wait();  // d_out comes from the preceding grid
+            int li = 0, s = 0;
+            uint32_t ph = 0;
+            for (; li < nst; ++li) {
+                if (li >= S && !wait_bounded(empty(s), ph ^ 1u, a.wait_ns, failed)) {
+                    record_failure(a.status, failed);
+                    break;
+                }
+                if (*failed) break;
+                const int n = (int)(n_begin + (int64_t)li * kBtRB);
+                const uint32_t sb = base + (uint32_t)s * a.stage_bytes;
+                mbar_arrive_expect_tx(full(s), a.tx);
+                tma_load_2d(sb, &maps.w, kt * (kBtKT / 2), n, full(s));
+                tma_load_2d(sb + kBtScOff, &maps.s, n, g_row, full(s));
+                tma_load_2d(sb + kBtDoOff, &maps.d, n, (int)m0, full(s));
+                if (++s == S) s = 0, ph ^= 1u;
+            }
+            for (int q = li > S ? li - S : 0; q < li; ++q)
+                wait_bounded(full(q % S), (uint32_t)(q / S) & 1u, kDrainNs, nullptr);
+        }
+        return;
+    }
+
+    // ------------------------------------------------------------------ consumers
+    // Lane = 32-bit word of codes (k = 256 kt + 8 lane + j), warp = rows warp, warp + 8, ...
+    // of every stage; gl = the lane's group inside the tile.
+    const int gl = a.gs_in_tile ? (lane * 8) / a.gs_in_tile : 0;
+    float acc[MT][8];
+#pragma unroll
+    for (int m = 0; m < MT; ++m)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[m][j] = 0.f;
+    constexpr float kMagic = 8388616.0f;  // 2^23 + 8
+    int s = 0;
+    uint32_t ph = 0;
+    // After a timed-out wait (`dead`) the warp still walks every stage, without waiting or
+    // computing, so that the consumer barriers and the split ticket are still reached.
+    bool dead = false;
+    for (int li = 0; li < nst; ++li) {
+        const bool got =
+            !dead && __all_sync(0xffffffffu, wait_bounded(full(s), ph, a.wait_ns, failed));
+        if (!got && !dead) {
+            if (lane == 0) record_failure(a.status, failed);
+            dead = true;
+        }
+        if (got) {
+            const uint8_t* stage = gbase + (uint32_t)s * a.stage_bytes;
+            const uint32_t* wrow = reinterpret_cast<const uint32_t*>(stage) + lane;
+            const __half* sc16 = reinterpret_cast<const __half*>(stage + kBtScOff) + gl * kBtRB;
+            const float* sc32 = reinterpret_cast<const float*>(stage + kBtScOff) + gl * kBtRB;
+            const float* dop = reinterpret_cast<const float*>(stage + kBtDoOff);
+#pragma unroll 4
+            for (int rr = 0; rr < kBtRB / kBtCWarps; ++rr) {
+                const int r = warp + rr * kBtCWarps;
+                const uint32_t word = wrow[r * (kBtKT / 8)];
+                const float sc = a.scale_f16 ? __half2float(sc16[r]) : sc32[r];
+                float ds[MT];
+#pragma unroll
+                for (int m = 0; m < MT; ++m) ds[m] = dop[m * kBtRB + r] * sc;
+                const uint32_t lo = word & 0x0F0F0F0Fu, hi = (word >> 4) & 0x0F0F0F0Fu;
+                const uint32_t ev = a.even_high ? hi : lo, od = a.even_high ? lo : hi;
+#pragma unroll
+                for (int b = 0; b < 4; ++b) {
+                    const float ce = __uint_as_float(prmt(ev, 0x4B000000u, 0x7440u | b)) - kMagic;
+                    const float co = __uint_as_float(prmt(od, 0x4B000000u, 0x7440u | b)) - kMagic;
+#pragma unroll
+                    for (int m = 0; m < MT; ++m) {
+                        acc[m][2 * b] = fmaf(ds[m], ce, acc[m][2 * b]);
+                        acc[m][2 * b + 1] = fmaf(ds[m], co, acc[m][2 * b + 1]);
+                    }
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty(s));
+        if (++s == S) s = 0, ph ^= 1u;
+    }
+    // The CTA's partial tile: the 8 warps added in warp order through shared memory (the
+    // ring is free once every consumer warp has passed its last stage).
+    asm volatile("bar.sync 1, %0;" ::"r"(kBtCWarps * 32) : "memory");
+    float* red = reinterpret_cast<float*>(gbase);  // [8][MT][256]
+#pragma unroll
+    for (int m = 0; m < MT; ++m)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) red[(warp * MT + m) * kBtKT + lane * 8 + j] = acc[m][j];
+    asm volatile("bar.sync 1, %0;" ::"r"(kBtCWarps * 32) : "memory");
+    const int mt = a.M - m0 < MT ? (int)(a.M - m0) : MT;
+    const int c = threadIdx.x;  // consumer thread = column of the tile
+    const int64_t k = (int64_t)kt * kBtKT + c;
+    float part[MT];
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+        float v = 0.f;
+#pragma unroll
+        for (int w = 0; w < kBtCWarps; ++w) v += red[(w * MT + m) * kBtKT + c];
+        part[m] = v;
+    }
+    griddep_wait();  // (long complete: the d_out copies waited for it) before any store
+    const bool store = !dead && !*failed;
+    if (a.splits == 1) {
+        if (store && k < a.K)
+            for (int m = 0; m < mt; ++m) a.d_x[(m0 + m) * a.K + k] = part[m];
+        return;
+    }
+    // Split rows: partials to the workspace; the last CTA of this (m tile, k tile) adds
+    // them in split order.
+    const int64_t item = (int64_t)blockIdx.z * gridDim.x + blockIdx.x;
+    float* wsi = a.ws + item * (int64_t)a.splits * MT * kBtKT;
+#pragma unroll
+    for (int m = 0; m < MT; ++m) wsi[((int64_t)blockIdx.y * MT + m) * kBtKT + c] = part[m];
+    __threadfence();
+    asm volatile("bar.sync 1, %0;" ::"r"(kBtCWarps * 32) : "memory");
+    if (threadIdx.x == 0) *s_last = atomicAdd(a.tickets + item, 1) == a.splits - 1;
+    asm volatile("bar.sync 1, %0;" ::"r"(kBtCWarps * 32) : "memory");
+    if (!*s_last) return;
+    __threadfence();
+    for (int m = 0; m < mt; ++m) {
+        // Loads of 8 parts in flight at a time; still added in split order.
+        const float* src = wsi + (int64_t)m * kBtKT + c;
+        const int64_t stride = (int64_t)MT * kBtKT;
+        float v = 0.f;
+        int sp = 0;
+        for (; sp + 8 <= a.splits; sp += 8) {
+            float t[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) t[u] = __ldcg(src + (int64_t)(sp + u) * stride);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v += t[u];
+        }
+        for (; sp < a.splits; ++sp) v += __ldcg(src + (int64_t)sp * stride);
+        if (store && !*failed && k < a.K) a.d_x[(m0 + m) * a.K + k] = v;
+    }
+    if (threadIdx.x == 0) a.tickets[item] = 0;
+}
+
 struct RqArgs {
     const float* latent;
     const void* scales;
@@ -284,6 +500,136 @@ cudaError_t launch(Kern k, const Args& a, dim3 grid, unsigned block, const Launc
     return cudaLaunchKernelEx(&cfg, k, a);
 }
 
+constexpr int kBtSmemLimit = 113 * 1024;  // two CTAs per SM
+
+template <int MT>
+cudaError_t launch_bt(const BtMaps& maps, const BtArgs& a, dim3 grid, int smem,
+                      const LaunchCtx& c) {
+    static const cudaError_t attr = cudaFuncSetAttribute(
+        backward_tma_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, kBtSmemLimit);
+    if (attr != cudaSuccess) return attr;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kBtThreads);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = c.stream;
+    cudaLaunchAttribute attrs[1];
+    if (c.pdl) {
+        attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attrs[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attrs;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, backward_tma_kernel<MT>, maps, a);
+}
+
+// TMA needs 16-byte aligned bases and row strides (K % 32, N % 8) and a k tile of 256
+// that holds whole groups or lies inside one.
+bool bt_eligible(const TrainProblem& p) {
+    auto al16 = [](const void* q) { return reinterpret_cast<uintptr_t>(q) % 16 == 0; };
+    if (p.K % 32 != 0 || p.N % 8 != 0) return false;
+    if (!al16(p.qweight) || !al16(p.scales) || !al16(p.d_out)) return false;
+    const int64_t gs = p.group_size;
+    if (gs < p.K && !(gs % 32 == 0 && ((gs <= kBtKT && kBtKT % gs == 0) || gs % kBtKT == 0)))
+        return false;
+    return tensor_map_encoder() != nullptr;
+}
+
+cudaError_t backward_tma_launch(const TrainProblem& p, const LaunchCtx& c) {
+    EncodeTiledFn enc = tensor_map_encoder();
+    const int MT = p.M <= 1 ? 1 : p.M <= 2 ? 2 : p.M <= 4 ? 4 : kMT;
+    const int64_t k_tiles = (p.K + kBtKT - 1) / kBtKT;
+    const int64_t m_tiles = (p.M + MT - 1) / MT;
+    const int64_t tiles = k_tiles * m_tiles;
+    const bool one_group = p.group_size >= p.K;
+    const int64_t G = one_group ? 1 : (p.K + p.group_size - 1) / p.group_size;
+    const int gt = one_group || p.group_size >= kBtKT ? 1 : (int)(kBtKT / p.group_size);
+    const uint32_t esz = p.scale_f16 ? 2 : 4;
+
+    BtArgs a;
+    a.d_x = p.d_x;
+    a.ws = c.ws;
+    a.tickets = c.tickets;
+    a.status = c.status_word;
+    a.M = p.M;
+    a.N = p.N;
+    a.K = p.K;
+    // Group row of k tile kt: kt * 256 / gs when a tile holds whole groups (gs in {32, 64,
+    // 128, 256}: a shift by log2(256 / gs)), kt / (gs / 256) when a group spans tiles, 0
+    // when one group covers K.
+    a.gs_in_tile = 0;
+    a.gs_shift256 = 0;
+    a.tiles_per_group = 1;
+    if (one_group) {
+        a.tiles_per_group = (int)k_tiles;
+    } else if (p.group_size <= kBtKT) {
+        a.gs_in_tile = (int)p.group_size;
+        while ((kBtKT >> a.gs_shift256) > p.group_size) ++a.gs_shift256;
+    } else {
+        a.tiles_per_group = (int)(p.group_size / kBtKT);
+    }
+    a.scale_f16 = p.scale_f16;
+    a.even_high = p.even_high;
+    a.wait_ns = c.wait_limit_ns;
+    // Rows split so that one wave keeps about two CTAs on every SM, in multiples of 64 rows,
+    // within the workspace and ticket capacity.
+    int64_t splits = std::max<int64_t>(1, 2LL * c.sm_count / tiles);
+    if (!c.ws || !c.tickets || tiles > c.ticket_count) splits = 1;
+    while (splits > 1 && tiles * splits * MT * kBtKT > c.ws_floats) --splits;
+    int64_t rows = (p.N + splits - 1) / splits;
+    rows = (rows + kBtRB - 1) / kBtRB * kBtRB;
+    splits = (p.N + rows - 1) / rows;
+    if (splits > 65535 || m_tiles > 65535 || k_tiles > 0x7fffffff) return cudaErrorInvalidValue;
+    a.splits = (int)splits;
+    a.rows_per_split = rows;
+    a.stage_bytes = (uint32_t)((kBtDoOff + MT * kBtRB * 4 + 1023) / 1024 * 1024);
+    a.stages = (int)std::min<int64_t>(kBtMaxStages, rows / kBtRB);
+    a.tx = (uint32_t)(kBtRB * kBtKT / 2) + (uint32_t)gt * kBtRB * esz + (uint32_t)MT * kBtRB * 4;
+    const int red = kBtCWarps * MT * kBtKT * 4;
+    const int ring = a.stages * (int)a.stage_bytes;
+    const int smem = 1024 + (ring > red ? ring : red) + 256;
+    if (smem > kBtSmemLimit) return cudaErrorInvalidValue;
+
+    BtMaps maps;
+    const cuuint32_t estr[2] = {1, 1};
+    {
+        const int64_t Kp = p.K / 2;
+        const cuuint64_t dims[2] = {(cuuint64_t)Kp, (cuuint64_t)p.N};
+        const cuuint64_t strides[1] = {(cuuint64_t)Kp};
+        const cuuint32_t box[2] = {(cuuint32_t)(kBtKT / 2), (cuuint32_t)kBtRB};
+        if (enc(&maps.w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(p.qweight), dims,
+                strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    {
+        const cuuint64_t dims[2] = {(cuuint64_t)p.N, (cuuint64_t)G};
+        const cuuint64_t strides[1] = {(cuuint64_t)p.N * esz};
+        const cuuint32_t box[2] = {(cuuint32_t)kBtRB, (cuuint32_t)gt};
+        if (enc(&maps.s, p.scale_f16 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT32, 2,
+                const_cast<void*>(p.scales), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    {
+        const cuuint64_t dims[2] = {(cuuint64_t)p.N, (cuuint64_t)p.M};
+        const cuuint64_t strides[1] = {(cuuint64_t)p.N * 4};
+        const cuuint32_t box[2] = {(cuuint32_t)kBtRB, (cuuint32_t)MT};
+        if (enc(&maps.d, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(p.d_out), dims,
+                strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    const dim3 grid((unsigned)k_tiles, (unsigned)splits, (unsigned)m_tiles);
+    switch (MT) {
+        case 1: return launch_bt<1>(maps, a, grid, smem, c);
+        case 2: return launch_bt<2>(maps, a, grid, smem, c);
+        case 4: return launch_bt<4>(maps, a, grid, smem, c);
+        default: return launch_bt<kMT>(maps, a, grid, smem, c);
+    }
+}
+
 }  // namespace
 
 cudaError_t backward_dx_launch(const TrainProblem& p, const LaunchCtx& c) {
@@ -301,6 +647,7 @@ cudaError_t backward_dx_launch(const TrainProblem& p, const LaunchCtx& c) {
     a.even_high = p.even_high;
     a.ws = c.ws;
     a.tickets = c.tickets;
+    if (bt_eligible(p)) return backward_tma_launch(p, c);
     const bool fast = p.K % 8 == 0 && p.group_size % 8 == 0 &&
                       reinterpret_cast<uintptr_t>(p.qweight) % 4 == 0;
     if (!fast) {

@@ -83,6 +83,37 @@ def test_backward_parity(handle, M, N, K, gs, f16):
     assert_parity(out, ref, mag, TOL_FP32)
 
 
+# Shapes taking the TMA-fed kernel (K % 32 == 0, N % 8 == 0, 16-byte aligned tensors, a
+# group size that tiles 256 k or spans whole tiles): ragged k tiles and 64-row stages,
+# partial d_out tiles, groups of 32..512 and per channel, both scale dtypes.
+BACKWARD_TMA_SHAPES = [
+    # M, N, K, gs, f16
+    (3, 520, 1056, 32, False),     # K % 256 != 0, N % 64 != 0, MT = 4 with 3 rows
+    (5, 1000, 2048, 128, True),    # MT = 8 with 5 rows
+    (2, 4096, 4096, 512, True),    # a group spans two k tiles
+    (9, 264, 768, 768, False),     # per channel, two d_out tiles
+    (1, 8, 256, 256, False),       # one stage of 8 rows
+    (4, 2048, 8192, 256, True),    # one group per k tile, rows split over CTAs
+    (1, 8192, 2048, 64, False),    # deep row split, fp32 scales
+]
+
+
+@pytest.mark.parametrize("M,N,K,gs,f16", BACKWARD_TMA_SHAPES)
+def test_backward_tma_parity(handle, M, N, K, gs, f16):
+    c = synth.make_backward_case(M, N, K, gs, scale_f16=f16, seed=M * 13 + N + K)
+    out = run_backward(handle, c)
+    ref, mag = oracle.backward_dx(c.d_out, c.qweight, c.scales, K, gs)
+    assert_parity(out, ref, mag, TOL_FP32)
+
+
+def test_backward_tma_nibble_even_high_and_repeat(handle):
+    c = synth.make_backward_case(3, 256, 1024, 64, scale_f16=True, seed=6)
+    ref, mag = oracle.backward_dx(c.d_out, c.qweight, c.scales, 1024, 64, even_high=True)
+    out = run_backward(handle, c, even_high=True)
+    assert_parity(out, ref, mag, TOL_FP32)
+    np.testing.assert_array_equal(out, run_backward(handle, c, even_high=True))
+
+
 @pytest.mark.parametrize("M,N,K,gs", [(4, 300, 512, 32), (9, 1000, 2048, 128), (1, 77, 40, 8)])
 def test_backward_dyadic_bit_exact(handle, M, N, K, gs):
     c = synth.make_backward_case(M, N, K, gs, seed=N, dyadic=True)
