@@ -36,8 +36,9 @@
 // ("[ExecuTorch][WebGPU] Add fp32 matmul ops ... (q4gsw_requant)", #20945.)  The quotient
 // is the IEEE fp32 quotient (__fdiv_rn), rounded half to even (rintf); a NaN quotient gives
 // code 8, like a zero scale; for odd K the padding nibble is 8.
-//   requant_kernel: one thread per 4 k of a row (one float4 of latents, two output bytes);
-//     consecutive threads walk a row (coalesced loads and stores).
+//   requant16_kernel: one thread per 16 k of a row (four float4 loads of latents in flight,
+//     one 8-byte store); consecutive threads walk a row (coalesced loads and stores).
+//   requant_kernel: the same with 4 k per thread (K % 4 == 0).
 //   requant_generic_kernel: one thread per output byte (any K, any alignment).
 #include <cuda_fp16.h>
 
@@ -465,6 +466,50 @@ __global__ void requant_kernel(const RqArgs a) {
     }
 }
 
+// One thread per 16 consecutive k of a row: four float4 loads of latents in flight, one
+// 8-byte store of codes; K % 16 == 0, 16-byte aligned latents, 8-byte aligned codes.
+__global__ void requant16_kernel(const RqArgs a) {
+    griddep_wait();
+    const int64_t chunks = a.K / 16;
+    const int64_t total = a.N * chunks;
+    const int gs = (int)(a.gs < a.K ? a.gs : a.K);  // gs >= K: one group
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t n = i / chunks;
+        const int k0 = (int)(i - n * chunks) * 16;
+        const float4* src = reinterpret_cast<const float4*>(a.latent + n * a.K + k0);
+        float l[16];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float4 u = __ldg(src + q);
+            l[4 * q] = u.x, l[4 * q + 1] = u.y, l[4 * q + 2] = u.z, l[4 * q + 3] = u.w;
+        }
+        int code[16];
+        if (gs % 16 == 0) {  // the 16 k share one group
+            const float sc = scale_value(a.scales, a.scale_f16, (int64_t)(k0 / gs) * a.N + n);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) code[j] = requant_code(l[j], sc);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                code[j] = requant_code(l[j], scale_value(a.scales, a.scale_f16,
+                                                         (int64_t)((k0 + j) / gs) * a.N + n));
+        }
+        uint32_t word[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            uint32_t w = 0;
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+                const int e = code[8 * h + 2 * b], o = code[8 * h + 2 * b + 1];
+                w |= (uint32_t)(a.even_high ? (o | (e << 4)) : (e | (o << 4))) << (8 * b);
+            }
+            word[h] = w;
+        }
+        *reinterpret_cast<uint2*>(a.w + n * a.Kp + k0 / 2) = make_uint2(word[0], word[1]);
+    }
+}
+
 __global__ void requant_generic_kernel(const RqArgs a) {
     griddep_wait();
     const int64_t total = a.N * a.Kp;
@@ -692,11 +737,12 @@ cudaError_t requant_launch(const RequantProblem& p, const LaunchCtx& c) {
     a.gs = p.group_size;
     a.scale_f16 = p.scale_f16;
     a.even_high = p.even_high;
-    const bool fast = p.K % 4 == 0 && p.K < (1LL << 31) &&
-                      reinterpret_cast<uintptr_t>(p.latent) % 16 == 0 &&
-                      reinterpret_cast<uintptr_t>(p.qweight) % 2 == 0;
-    const int64_t units = fast ? p.N * (p.K / 4) : p.N * a.Kp;
+    const bool lat16 = reinterpret_cast<uintptr_t>(p.latent) % 16 == 0 && p.K < (1LL << 31);
+    const bool wide = lat16 && p.K % 16 == 0 && reinterpret_cast<uintptr_t>(p.qweight) % 8 == 0;
+    const bool fast = lat16 && p.K % 4 == 0 && reinterpret_cast<uintptr_t>(p.qweight) % 2 == 0;
+    const int64_t units = wide ? p.N * (p.K / 16) : fast ? p.N * (p.K / 4) : p.N * a.Kp;
     const int64_t blocks = std::max<int64_t>(1, std::min<int64_t>((units + 255) / 256, 32LL * c.sm_count));
+    if (wide) return launch(requant16_kernel, a, dim3((unsigned)blocks), 256, c);
     return fast ? launch(requant_kernel, a, dim3((unsigned)blocks), 256, c)
                 : launch(requant_generic_kernel, a, dim3((unsigned)blocks), 256, c);
 }

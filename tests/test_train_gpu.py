@@ -181,6 +181,30 @@ def test_requant_bit_exact(handle, N, K, gs, f16, specials):
     np.testing.assert_array_equal(run_requant(handle, c), oracle.requant(c.latent, c.scales, gs))
 
 
+@pytest.mark.parametrize("f16", [False, True])
+def test_requant_near_half_integers(handle, f16):
+    """Latents whose fp32 quotients fall on, or within a few ulps of, half-integers (and
+    of the clamp edges -8.5 / 7.5) under non-power-of-two scales: the rounding decision
+    near a tie must be the one of the exact fp32 quotient."""
+    rng = np.random.default_rng(17)
+    N, K, gs = 64, 1024, 32
+    s = rng.uniform(0.003, 0.05, size=(K // gs, N)).astype(np.float32)
+    scales = s.astype(np.float16) if f16 else s
+    s_used = np.repeat(scales.astype(np.float64), gs, axis=0).T  # [N, K]
+    h = rng.integers(-9, 9, size=(N, K)) + 0.5
+    ulps = rng.integers(-4, 5, size=(N, K))
+    target = (h * s_used).astype(np.float32)
+    latent = np.nextafter(target, np.where(ulps >= 0, np.inf, -np.inf).astype(np.float32))
+    for _ in range(3):  # a few ulps either side, some exact
+        step = np.abs(ulps) > 1
+        latent = np.where(step, np.nextafter(latent, np.where(ulps >= 0, np.inf, -np.inf)
+                                             .astype(np.float32)), latent)
+        ulps = np.where(step, ulps - np.sign(ulps), ulps)
+    latent = np.where(rng.random((N, K)) < 0.2, target, latent).astype(np.float32)
+    c = synth.RequantCase(N, K, gs, latent, scales)
+    np.testing.assert_array_equal(run_requant(handle, c), oracle.requant(latent, scales, gs))
+
+
 def test_requant_hand_example(handle):
     r = load_requant_example()
     c = synth.RequantCase(2, 8, r["group_size"], r["latent"], r["scales"])
