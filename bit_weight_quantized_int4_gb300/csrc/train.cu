@@ -312,12 +312,12 @@ __global__ void __launch_bounds__(kBtThreads, 2)
     // Lane = 32-bit word of codes (k = 256 kt + 8 lane + j), warp = rows warp, warp + 8, ...
     // of every stage; gl = the lane's group inside the tile.
     const int gl = a.gs_in_tile ? (lane * 8) / a.gs_in_tile : 0;
-    float acc[MT][8];
+    // acc[m][b] = (k = 2b, k = 2b + 1) of the lane's 8 k: packed fp32x2 FMAs.
+    float2 acc[MT][4];
 #pragma unroll
     for (int m = 0; m < MT; ++m)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[m][j] = 0.f;
-    constexpr float kMagic = 8388616.0f;  // 2^23 + 8
+        for (int b = 0; b < 4; ++b) acc[m][b] = make_float2(0.f, 0.f);
     int s = 0;
     uint32_t ph = 0;
     // After a timed-out wait (`dead`) the warp still walks every stage, without waiting or
@@ -341,20 +341,17 @@ __global__ void __launch_bounds__(kBtThreads, 2)
                 const int r = warp + rr * kBtCWarps;
                 const uint32_t word = wrow[r * (kBtKT / 8)];
                 const float sc = a.scale_f16 ? __half2float(sc16[r]) : sc32[r];
-                float ds[MT];
+                float2 cv[4];  // (c - 8) of k = 2b, 2b + 1, exact
+                if (a.even_high)
+                    codes_word<true>(word, cv);
+                else
+                    codes_word<false>(word, cv);
 #pragma unroll
-                for (int m = 0; m < MT; ++m) ds[m] = dop[m * kBtRB + r] * sc;
-                const uint32_t lo = word & 0x0F0F0F0Fu, hi = (word >> 4) & 0x0F0F0F0Fu;
-                const uint32_t ev = a.even_high ? hi : lo, od = a.even_high ? lo : hi;
+                for (int m = 0; m < MT; ++m) {
+                    const float d = dop[m * kBtRB + r] * sc;
+                    const float2 d2 = make_float2(d, d);
 #pragma unroll
-                for (int b = 0; b < 4; ++b) {
-                    const float ce = __uint_as_float(prmt(ev, 0x4B000000u, 0x7440u | b)) - kMagic;
-                    const float co = __uint_as_float(prmt(od, 0x4B000000u, 0x7440u | b)) - kMagic;
-#pragma unroll
-                    for (int m = 0; m < MT; ++m) {
-                        acc[m][2 * b] = fmaf(ds[m], ce, acc[m][2 * b]);
-                        acc[m][2 * b + 1] = fmaf(ds[m], co, acc[m][2 * b + 1]);
-                    }
+                    for (int b = 0; b < 4; ++b) acc[m][b] = ffma2(d2, cv[b], acc[m][b]);
                 }
             }
         }
@@ -369,7 +366,10 @@ __global__ void __launch_bounds__(kBtThreads, 2)
 #pragma unroll
     for (int m = 0; m < MT; ++m)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) red[(warp * MT + m) * kBtKT + lane * 8 + j] = acc[m][j];
+        for (int b = 0; b < 4; ++b) {
+            red[(warp * MT + m) * kBtKT + lane * 8 + 2 * b] = acc[m][b].x;
+            red[(warp * MT + m) * kBtKT + lane * 8 + 2 * b + 1] = acc[m][b].y;
+        }
     asm volatile("bar.sync 1, %0;" ::"r"(kBtCWarps * 32) : "memory");
     const int mt = a.M - m0 < MT ? (int)(a.M - m0) : MT;
     const int c = threadIdx.x;  // consumer thread = column of the tile
@@ -401,22 +401,32 @@ __global__ void __launch_bounds__(kBtThreads, 2)
     asm volatile("bar.sync 1, %0;" ::"r"(kBtCWarps * 32) : "memory");
     if (!*s_last) return;
     __threadfence();
-    for (int m = 0; m < mt; ++m) {
-        // Loads of 8 parts in flight at a time; still added in split order.
-        const float* src = wsi + (int64_t)m * kBtKT + c;
-        const int64_t stride = (int64_t)MT * kBtKT;
-        float v = 0.f;
-        int sp = 0;
-        for (; sp + 8 <= a.splits; sp += 8) {
-            float t[8];
+    // The MT rows of the column together, the loads of PB parts of all of them in flight
+    // at a time (MT * PB <= 32); every row still added in split order.
+    constexpr int PB = MT >= 8 ? 4 : 32 / MT > 8 ? 8 : 32 / MT;
+    const float* src = wsi + c;
+    const int64_t stride = (int64_t)MT * kBtKT;
+    float v[MT];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) t[u] = __ldcg(src + (int64_t)(sp + u) * stride);
+    for (int m = 0; m < MT; ++m) v[m] = 0.f;
+    for (int sp = 0; sp < a.splits; sp += PB) {
+        float t[PB][MT];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) v += t[u];
-        }
-        for (; sp < a.splits; ++sp) v += __ldcg(src + (int64_t)sp * stride);
-        if (store && !*failed && k < a.K) a.d_x[(m0 + m) * a.K + k] = v;
+        for (int u = 0; u < PB; ++u)
+#pragma unroll
+            for (int m = 0; m < MT; ++m)
+                t[u][m] = sp + u < a.splits ? __ldcg(src + (int64_t)(sp + u) * stride + m * kBtKT)
+                                            : 0.f;
+#pragma unroll
+        for (int u = 0; u < PB; ++u)
+#pragma unroll
+            for (int m = 0; m < MT; ++m)
+                if (sp + u < a.splits) v[m] += t[u][m];
     }
+    if (store && !*failed && k < a.K)
+#pragma unroll
+        for (int m = 0; m < MT; ++m)
+            if (m < mt) a.d_x[(m0 + m) * a.K + k] = v[m];
     if (threadIdx.x == 0) a.tickets[item] = 0;
 }
 
