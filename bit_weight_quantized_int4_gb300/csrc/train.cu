@@ -218,7 +218,11 @@ constexpr int kBtRB = 64;                          // weight rows per stage
 constexpr int kBtMaxStages = 8;
 constexpr int64_t kDrainNs = 4000000000LL;
 constexpr uint32_t kBtScOff = kBtRB * kBtKT / 2;   // 8 KiB of codes, then the scales
-constexpr uint32_t kBtDoOff = kBtScOff + 2048;     // then d_out [MT x 64]
+// Scales are copied for 72 rows (fp16: 144-byte box rows) or 68 rows (fp32: 272 bytes): the
+// lanes of a warp read up to 8 groups of one row, and the padded row stride puts them in
+// different banks (a box row must be a multiple of 16 bytes).
+constexpr int kBtScRows16 = kBtRB + 8, kBtScRows32 = kBtRB + 4;
+constexpr uint32_t kBtDoOff = kBtScOff + 2304;  // then d_out [MT x 64]
 
 struct BtMaps {
     CUtensorMap w;   // uint8 [N, Kp], box {128, 64}
@@ -236,6 +240,7 @@ struct BtArgs {
     int gs_shift256;      // then: group row of k tile kt = kt << gs_shift256
     int tiles_per_group;  // else: group row = kt / tiles_per_group
     int scale_f16, even_high;
+    int sc_rows;  // staged scale rows per group (72 / 68)
     int splits, stages;
     int64_t rows_per_split;  // multiple of 64
     uint32_t stage_bytes, tx;
@@ -333,8 +338,8 @@ __global__ void __launch_bounds__(kBtThreads, 2)
         if (got) {
             const uint8_t* stage = gbase + (uint32_t)s * a.stage_bytes;
             const uint32_t* wrow = reinterpret_cast<const uint32_t*>(stage) + lane;
-            const __half* sc16 = reinterpret_cast<const __half*>(stage + kBtScOff) + gl * kBtRB;
-            const float* sc32 = reinterpret_cast<const float*>(stage + kBtScOff) + gl * kBtRB;
+            const __half* sc16 = reinterpret_cast<const __half*>(stage + kBtScOff) + gl * a.sc_rows;
+            const float* sc32 = reinterpret_cast<const float*>(stage + kBtScOff) + gl * a.sc_rows;
             const float* dop = reinterpret_cast<const float*>(stage + kBtDoOff);
 #pragma unroll 4
             for (int rr = 0; rr < kBtRB / kBtCWarps; ++rr) {
@@ -364,12 +369,11 @@ __global__ void __launch_bounds__(kBtThreads, 2)
     asm volatile("bar.sync 1, %0;" ::"r"(kBtCWarps * 32) : "memory");
     float* red = reinterpret_cast<float*>(gbase);  // [8][MT][256]
 #pragma unroll
-    for (int m = 0; m < MT; ++m)
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-            red[(warp * MT + m) * kBtKT + lane * 8 + 2 * b] = acc[m][b].x;
-            red[(warp * MT + m) * kBtKT + lane * 8 + 2 * b + 1] = acc[m][b].y;
-        }
+    for (int m = 0; m < MT; ++m) {
+        float4* dst = reinterpret_cast<float4*>(red + (warp * MT + m) * kBtKT + lane * 8);
+        dst[0] = make_float4(acc[m][0].x, acc[m][0].y, acc[m][1].x, acc[m][1].y);
+        dst[1] = make_float4(acc[m][2].x, acc[m][2].y, acc[m][3].x, acc[m][3].y);
+    }
     asm volatile("bar.sync 1, %0;" ::"r"(kBtCWarps * 32) : "memory");
     const int mt = a.M - m0 < MT ? (int)(a.M - m0) : MT;
     const int c = threadIdx.x;  // consumer thread = column of the tile
@@ -639,7 +643,8 @@ cudaError_t backward_tma_launch(const TrainProblem& p, const LaunchCtx& c) {
     a.rows_per_split = rows;
     a.stage_bytes = (uint32_t)((kBtDoOff + MT * kBtRB * 4 + 1023) / 1024 * 1024);
     a.stages = (int)std::min<int64_t>(kBtMaxStages, rows / kBtRB);
-    a.tx = (uint32_t)(kBtRB * kBtKT / 2) + (uint32_t)gt * kBtRB * esz + (uint32_t)MT * kBtRB * 4;
+    a.sc_rows = p.scale_f16 ? kBtScRows16 : kBtScRows32;
+    a.tx = (uint32_t)(kBtRB * kBtKT / 2) + (uint32_t)gt * a.sc_rows * esz + (uint32_t)MT * kBtRB * 4;
     const int red = kBtCWarps * MT * kBtKT * 4;
     const int ring = a.stages * (int)a.stage_bytes;
     const int smem = 1024 + (ring > red ? ring : red) + 256;
@@ -660,7 +665,7 @@ cudaError_t backward_tma_launch(const TrainProblem& p, const LaunchCtx& c) {
     {
         const cuuint64_t dims[2] = {(cuuint64_t)p.N, (cuuint64_t)G};
         const cuuint64_t strides[1] = {(cuuint64_t)p.N * esz};
-        const cuuint32_t box[2] = {(cuuint32_t)kBtRB, (cuuint32_t)gt};
+        const cuuint32_t box[2] = {(cuuint32_t)a.sc_rows, (cuuint32_t)gt};
         if (enc(&maps.s, p.scale_f16 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT32, 2,
                 const_cast<void*>(p.scales), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                 CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
