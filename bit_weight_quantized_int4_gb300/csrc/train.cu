@@ -442,12 +442,12 @@ struct RqArgs {
     int scale_f16, even_high;
 };
 
+// The code of one latent: the fp32 quotient (correctly rounded division), converted to an
+// integer rounding half to even (cvt.rni, which saturates and maps NaN to 0, i.e. code 8),
+// clamped to [-8, 7] and offset by 8; a zero scale gives code 8.
 __device__ __forceinline__ int requant_code(float l, float s) {
-    if (s == 0.f) return 8;
-    const float q = __fdiv_rn(l, s);
-    if (isnan(q)) return 8;
-    const float r = fminf(fmaxf(rintf(q), -8.f), 7.f);
-    return (int)r + 8;
+    const int c = s == 0.f ? 0 : __float2int_rn(__fdiv_rn(l, s));
+    return min(max(c, -8), 7) + 8;
 }
 
 // One thread per 4 consecutive k (one float4 of latents, two output bytes); K % 4 == 0,
