@@ -46,9 +46,9 @@ constexpr int64_t kTickets = 1 << 14;    // 64 KiB
 // weight count N * K (and long K, where the tensor-core main loop is longest).
 int64_t rowstream_max_m(const q4lin::Problem& p) {
     const double nk = (double)p.N * (double)p.K;
-    if (nk < 3.0e6) return 24;
-    if (nk < 8.0e6) return 12;
-    return p.K >= 8192 ? 8 : 4;
+    if (nk < 3.0e6) return 16;
+    if (nk < 8.0e6 || p.K >= 8192) return 8;
+    return 4;
 }
 
 class DeviceGuard {
