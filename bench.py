@@ -581,6 +581,12 @@ def profile(spec):
     elif kind == "prefill":
         M, N, K = (int(d) for d in dims)
         prefill_tflops(torch, h, M, N, K, reps=3)
+    elif kind == "backward":
+        M, N, K = (int(d) for d in dims)
+        backward_bandwidth(torch, h, M, N, K)
+    elif kind == "requant":
+        N, K = (int(d) for d in dims)
+        requant_bandwidth(torch, h, N, K)
     else:
         raise SystemExit(f"unknown profile spec {spec}")
     torch.cuda.synchronize()
@@ -607,7 +613,7 @@ def main():
                          "measured table (JSON) instead of the benchmark line")
     ap.add_argument("--profile", default=None,
                     help="run a few launches of one op and exit (for ncu): gemv:N:K, "
-                         "prefill:M:N:K or token:1b|8b")
+                         "prefill:M:N:K, backward:M:N:K, requant:N:K or token:1b|8b")
     args = ap.parse_args()
     if args.profile:
         return profile(args.profile)

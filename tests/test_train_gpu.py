@@ -95,6 +95,8 @@ BACKWARD_TMA_SHAPES = [
     (1, 8, 256, 256, False),       # one stage of 8 rows
     (4, 2048, 8192, 256, True),    # one group per k tile, rows split over CTAs
     (1, 8192, 2048, 64, False),    # deep row split, fp32 scales
+    (8, 2048, 8192, 32, True),     # the benchmark's M = 8 shape
+    (1, 8192, 2048, 32, True),     # the benchmark's M = 1 shape
 ]
 
 
@@ -166,6 +168,7 @@ def test_backward_rejects_overlap(handle):
 # --------------------------------------------------------------------------- requant
 REQUANT_SHAPES = [
     # N, K, gs, f16
+    (8192, 2048, 32, True),    # the benchmark's shape (16-k kernel)
     (64, 2048, 32, False),     # fast kernel
     (33, 4096, 4096, True),    # per channel, fp16 scales
     (100, 512, 64, False),
