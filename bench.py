@@ -39,7 +39,7 @@ L2_BYTES = 129 << 20
 # launch list (dram__bytes_read.sum + dram__bytes_write.sum per launch; the summary is
 # profiles/gemv_tma_token_1b_launches.md).  Valid only for the kernel source it was taken
 # with: the sha256 prefix of gemv_tma.cu + ptx.cuh; any other source reports null.
-TOKEN_TRAFFIC = {"bytes": 698315008, "launches": 65, "source_sha256": "44a2ce91bfa89908"}
+TOKEN_TRAFFIC = {"bytes": 698170880, "launches": 65, "source_sha256": "487c08129dbd7bed"}
 
 
 def gemv_source_sha():
