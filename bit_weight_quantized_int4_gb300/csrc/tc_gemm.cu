@@ -27,16 +27,22 @@
 // commit ~500.  So the stage is wide, its two x boxes come from two producer threads in
 // different warps, and the packed weights arrive in blocks of four stages.
 //
-// Roles (640 threads, one CTA per [128 weight rows x bt activation rows] tile; tensor
-// memory: D in columns [0, bt), the A ring in columns [256, 256 + 64 * S)):
-//   warps 0 and 2, one lane each: TMA producers of x: per stage, box j (j = 0, 1) is the
-//                     tile [bt rows x 32 k] at k = 64 * stage + 32 * j (128-byte rows).
+// Roles (640 threads, 672 with the second issuer; one CTA per [128 weight rows x bt
+// activation rows] tile; tensor memory: D in columns [0, bt) (and D1 in [bt, 2 bt)), the A
+// ring in [256, 256 + 64 * S)):
+//   warps 0 and 2, one lane each: TMA producers of x: box j (j = 0, 1) of a stage is the
+//                     tile [bt rows x 32 k] at k = 64 * stage + 32 * j (128-byte rows);
+//                     with an even ring depth the producers take alternate stages (both
+//                     boxes), else one box of every stage each.
 //   warp 3, one lane: TMA producer of the packed weights: blocks [128 rows x 128 B]
 //                     (256 k, four stages) with the 128-byte swizzle, a ring of two.
-//   warp 1:           allocates tensor memory; one lane issues 8 tcgen05.mma (K = 8, A
-//                     from tensor memory) per stage and commits each stage's completion to
-//                     "empty" (freeing the x slot and the A slot).
-//   warps 4-19:       four groups of 4 warps (as many as there are stages in the ring, so
+//   warps 1 (and 4):  warp 1 allocates tensor memory; one lane of each issues 8
+//                     tcgen05.mma (K = 8, A from tensor memory) per stage and commits each
+//                     stage's completion to "empty" (freeing the x slot and the A slot):
+//                     for tiles of up to 128 activation rows (and an even ring depth) the
+//                     two take alternate stages into two accumulators summed at the end,
+//                     else warp 1 takes every stage.
+//   then 16 warps:    four groups of 4 warps (as many as there are stages in the ring, so
 //                     that a group always takes the same slot and waits on its barrier
 //                     phase by phase) taking stages in turn; thread = weight row
 //                     (its warp's lane quarter of tensor memory): once the MMAs that read
@@ -71,9 +77,13 @@ namespace q4lin {
 namespace {
 using namespace ptx;
 
-constexpr int kCtlWarps = 4;                 // two x producers, the MMA issuer, the W producer
+// Control warps: two x producers, the MMA issuer(s), the W producer; DUAL kernels (tiles of
+// up to 128 activation rows) have a second MMA issuer.
+__host__ __device__ constexpr int ctl_warps(bool dual) { return dual ? 5 : 4; }
 constexpr int kGroups = 4;                   // dequantizing warp groups (stages in turn)
-constexpr int kThreads2 = 32 * kCtlWarps + 128 * kGroups;
+__host__ __device__ constexpr int kernel_threads(bool dual) {
+    return 32 * ctl_warps(dual) + 128 * kGroups;
+}
 constexpr int kWRows = 128;                  // weight rows per tile (MMA M = TMEM lanes)
 constexpr int kStageK = 64;                  // k per stage: two 128-byte swizzle rows of x
 constexpr int kHalfK = 32;
@@ -147,10 +157,11 @@ __device__ __forceinline__ void dequant_chunk(const uint4 wv, float sc, uint32_t
     }
 }
 
-template <bool EH>
-__global__ void __launch_bounds__(kThreads2, 1)
+template <bool EH, bool DUAL>
+__global__ void __launch_bounds__(kernel_threads(DUAL), 1)
     tc_wa_kernel(const __grid_constant__ CUtensorMap tmap_x,
                  const __grid_constant__ CUtensorMap tmap_w, const Tc2Args a) {
+    constexpr int kCtl = ctl_warps(DUAL);
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -168,6 +179,14 @@ __global__ void __launch_bounds__(kThreads2, 1)
     const int it_begin = rank * a.kpp;
     const int n_iters = min(a.kpp, a.k_iters - it_begin);
     const int n_blk = (n_iters + kWBlkStages - 1) / kWBlkStages;
+    // With an even ring depth the two x producers take alternate stages (both boxes each)
+    // and, for tiles up to 128 activation rows, two MMA issuers take alternate stages into
+    // two accumulators (D0 in columns [0, bt), D1 in [bt, 2 bt)), summed in the epilogue:
+    // each slot then belongs to one producer and one issuer, which see its barrier phases
+    // one by one.  A single thread's issue of 8 MMAs and its barrier work bound a stage at
+    // narrow tiles.
+    const bool alt = S % 2 == 0;
+    const bool dual = DUAL && alt && bt <= 128 && n_iters >= 2;
     uint32_t* tmem_slot_ptr = reinterpret_cast<uint32_t*>(gbase + (tmem_slot - base));
     volatile int* failed = reinterpret_cast<volatile int*>(gbase + (tmem_slot + 4 - base));
     auto xslot = [&](int s) { return base + (uint32_t)s * sbytes; };
@@ -181,7 +200,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(full(s), 2);      // the two x producers
+            mbar_init(full(s), alt ? 1 : 2);  // one producer a stage, or one a box
             mbar_init(aready(s), 128);  // the 128 threads of the group that owns the stage
             mbar_init(empty(s), 1);
         }
@@ -189,7 +208,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
             mbar_init(wfull(b), 1);
             mbar_init(wempty(b), 128 * kWBlkStages);  // every thread of every stage's group
         }
-        mbar_init(accfull, 1);
+        mbar_init(accfull, DUAL ? 2 : 1);  // every MMA issuer commits it
         *failed = 0;
         mbar_init_fence();
     }
@@ -211,29 +230,47 @@ __global__ void __launch_bounds__(kThreads2, 1)
     if (warp == 0 || warp == 2) {
         if (lane == 0) {
             // ------------------------------------------------------ TMA producers of x
-            const int j = warp >> 1;  // which 32-k half of every stage
+            const int pr = warp >> 1;  // producer 0 or 1
             prefetch_tensormap(&tmap_x);
             griddep_wait();
-            // Slot and phase kept incrementally (no divisions on this serial path).
-            int li = 0, s = 0;
+            // Stages of this producer: every stage (box pr) or, with alt, stages pr,
+            // pr + 2, ... (both boxes).  Slot and phase kept incrementally.
+            const int first = alt ? pr : 0, stride = alt ? 2 : 1;
+            int s = 0;
             uint32_t ph = 0;  // parity of the slot's current use
-            for (; li < n_iters; ++li, s = (s + 1 == S) ? 0 : s + 1, ph ^= (s == 0)) {
+            auto step = [&]() {
+                if (++s == S) s = 0, ph ^= 1u;
+            };
+            for (int q = 0; q < first; ++q) step();
+            int li = first;
+            for (; li < n_iters; li += stride) {
                 if (li >= S && !wait_bounded(empty(s), ph ^ 1u, a.wait_ns, failed)) {
                     record_failure(a.status, failed);
                     break;
                 }
                 if (*failed) break;
-                if (a.skip_first_copy && li == 0) continue;
-                const int64_t k = (int64_t)(it_begin + li) * kStageK + kHalfK * j;
-                if (k < a.K) {
-                    mbar_arrive_expect_tx(full(s), xbox);
-                    tma_load_2d(xslot(s) + (uint32_t)j * xbox, &tmap_x, (int)k, (int)m0, full(s));
-                } else {
-                    mbar_arrive(full(s));  // the missing half of a last stage
+                if (!(a.skip_first_copy && li == 0)) {
+                    const int64_t k = (int64_t)(it_begin + li) * kStageK;
+                    const bool two = k + kHalfK < a.K;  // else the last stage has one half
+                    if (alt) {
+                        mbar_arrive_expect_tx(full(s), two ? 2 * xbox : xbox);
+                        tma_load_2d(xslot(s), &tmap_x, (int)k, (int)m0, full(s));
+                        if (two)
+                            tma_load_2d(xslot(s) + xbox, &tmap_x, (int)(k + kHalfK), (int)m0,
+                                        full(s));
+                    } else if (pr == 0 || two) {
+                        mbar_arrive_expect_tx(full(s), xbox);
+                        tma_load_2d(xslot(s) + (uint32_t)pr * xbox, &tmap_x,
+                                    (int)(k + kHalfK * pr), (int)m0, full(s));
+                    } else {
+                        mbar_arrive(full(s));  // the missing half of a last stage
+                    }
                 }
+                for (int q = 0; q < stride; ++q) step();
             }
-            // Copies of the last stages may still be landing; the CTA must not exit first.
-            for (int q = li > S ? li - S : 0; q < li; ++q) {
+            // Copies of this producer's last stages may still be landing; the CTA must not
+            // exit first.  (Its stages among the last S are the latest uses of their slots.)
+            for (int q = li - stride; q >= first && q >= li - S; q -= stride) {
                 if (a.skip_first_copy && q == 0) continue;
                 wait_bounded(full(q % S), (q / S) & 1, kDrainNs, nullptr);
             }
@@ -258,15 +295,22 @@ __global__ void __launch_bounds__(kThreads2, 1)
             for (int q = bi > kWSlots ? bi - kWSlots : 0; q < bi; ++q)
                 wait_bounded(wfull(q % kWSlots), (q / kWSlots) & 1, kDrainNs, nullptr);
         }
-    } else if (warp == 1) {
+    } else if (warp == 1 || (DUAL && warp == 4)) {
         if (lane == 0) {
-            // ------------------------------------------------------------- MMA issuer
+            // ------------------------------------------------------------ MMA issuers
+            const int is = warp == 1 ? 0 : 1;
             const uint32_t idesc = tf32_idesc(kWRows, bt);
             const int64_t k_two = a.K - kHalfK - (int64_t)it_begin * kStageK;
+            const uint32_t dacc = tmem_d + (dual ? (uint32_t)(is * bt) : 0u);
+            // Stages of this issuer: all (issuer 0, single), or is, is + 2, ... (dual).
+            const int first = dual ? is : (is == 0 ? 0 : n_iters), stride = dual ? 2 : 1;
             int s = 0;
             uint32_t par = 0;
-            for (int it = 0; it < n_iters;  // it: stage of this CTA's range
-                 ++it, s = (s + 1 == S) ? 0 : s + 1, par ^= (s == 0)) {
+            auto step = [&]() {
+                if (++s == S) s = 0, par ^= 1u;
+            };
+            for (int q = 0; q < first && q < S * 2; ++q) step();
+            for (int it = first; it < n_iters; it += stride) {  // it: stage of this CTA's range
                 if (!wait_bounded(aready(s), par, a.wait_ns, failed) ||
                     !wait_bounded(full(s), par, a.wait_ns, failed)) {
                     record_failure(a.status, failed);
@@ -281,23 +325,24 @@ __global__ void __launch_bounds__(kThreads2, 1)
                 const uint64_t d0 = sw128_desc(xslot(s));
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_tf32_ts(tmem_d, acol + 8 * kk, d0 + (uint64_t)(2 * kk), idesc,
-                                (it | kk) != 0);
+                    mma_tf32_ts(dacc, acol + 8 * kk, d0 + (uint64_t)(2 * kk), idesc,
+                                (it != first) || kk != 0);
                 if ((int64_t)it * kStageK < k_two) {
                     const uint64_t d1 = d0 + (uint64_t)(xbox >> 4);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        mma_tf32_ts(tmem_d, acol + kHalfK + 8 * kk, d1 + (uint64_t)(2 * kk), idesc,
+                        mma_tf32_ts(dacc, acol + kHalfK + 8 * kk, d1 + (uint64_t)(2 * kk), idesc,
                                     1u);
                 }
                 mma_commit(empty(s));
+                for (int q = 0; q < stride; ++q) step();
             }
             mma_commit(accfull);  // arrives once every MMA issued above has completed
         }
         __syncwarp();
     } else {
         // ------------------------------------------------- dequantization, epilogue
-        const int group = (warp - kCtlWarps) >> 2;
+        const int group = (warp - kCtl) >> 2;
         const int G = S;  // dequantizing groups (S <= kGroups): group g always takes slot g
         const int quarter = warp & 3;  // the 32-lane slice of tensor memory this warp owns
         const int r = quarter * 32 + lane;  // this thread's weight row in the tile
@@ -390,6 +435,13 @@ __global__ void __launch_bounds__(kThreads2, 1)
             for (int c0 = 32 * group; c0 < bt; c0 += 32 * kGroups) {
                 uint32_t v[32];
                 tmem_ld32(lane_base + (uint32_t)c0, v);
+                if (dual) {  // D0 + D1
+                    uint32_t v1[32];
+                    tmem_ld32(lane_base + (uint32_t)(bt + c0), v1);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        v[j] = __float_as_uint(__uint_as_float(v[j]) + __uint_as_float(v1[j]));
+                }
                 if (!rvalid) continue;
                 float* dst = a.out + (m0 + c0) * a.N + n;
                 const int64_t rows = a.M - (m0 + c0);
@@ -411,8 +463,8 @@ __global__ void __launch_bounds__(kThreads2, 1)
         // these bytes several times slower than L2 on this part.)
         const int64_t tile_id = (int64_t)blockIdx.y * (gridDim.x / P) + wtile;
         float* wst = a.ws + tile_id * (int64_t)(P - 1) * kWRows * bt;
-        if (warp >= kCtlWarps && epi_go) {
-            const int group = (warp - kCtlWarps) >> 2;
+        if (warp >= kCtl && epi_go) {
+            const int group = (warp - kCtl) >> 2;
             const int quarter = warp & 3;
             const int r = quarter * 32 + lane;
             const uint32_t lane_base = tmem_d + ((uint32_t)(quarter * 32) << 16);
@@ -421,6 +473,13 @@ __global__ void __launch_bounds__(kThreads2, 1)
                 if (q == rank) continue;
                 uint32_t v[16];
                 tmem_ld16(lane_base + (uint32_t)c0, v);
+                if (dual) {  // D0 + D1
+                    uint32_t v1[16];
+                    tmem_ld16(lane_base + (uint32_t)(bt + c0), v1);
+#pragma unroll
+                    for (int t = 0; t < 16; ++t)
+                        v[t] = __float_as_uint(__uint_as_float(v[t]) + __uint_as_float(v1[t]));
+                }
                 const int j = rank < q ? rank : rank - 1;  // this CTA's slot at rank q
                 float* dst = wst + ((int64_t)(q * (P - 1) + j) * a.sw + (c0 - q * a.sw)) * kWRows + r;
 #pragma unroll
@@ -430,8 +489,8 @@ __global__ void __launch_bounds__(kThreads2, 1)
         // Every thread reaches this barrier (all earlier waits are bounded in time); its
         // release / acquire at cluster scope orders the workspace writes before the reads.
         cluster_sync_all();
-        if (warp >= kCtlWarps && __all_sync(0xffffffffu, epi_go && !*failed)) {
-            const int group = (warp - kCtlWarps) >> 2;
+        if (warp >= kCtl && __all_sync(0xffffffffu, epi_go && !*failed)) {
+            const int group = (warp - kCtl) >> 2;
             const int quarter = warp & 3;
             const int r = quarter * 32 + lane;
             const int64_t n = n0 + r;
@@ -439,6 +498,13 @@ __global__ void __launch_bounds__(kThreads2, 1)
             for (int c0 = 16 * group; c0 < a.sw; c0 += 16 * kGroups) {
                 uint32_t own[16];
                 tmem_ld16(lane_base + (uint32_t)(rank * a.sw + c0), own);
+                if (dual) {  // D0 + D1
+                    uint32_t own1[16];
+                    tmem_ld16(lane_base + (uint32_t)(bt + rank * a.sw + c0), own1);
+#pragma unroll
+                    for (int t = 0; t < 16; ++t)
+                        own[t] = __float_as_uint(__uint_as_float(own[t]) + __uint_as_float(own1[t]));
+                }
                 float acc[16];
 #pragma unroll
                 for (int t = 0; t < 16; ++t) acc[t] = 0.f;
@@ -468,7 +534,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
             }
         }
     }
-    if (warp >= kCtlWarps) tc_fence_before();
+    if (warp >= kCtl) tc_fence_before();
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
@@ -476,10 +542,10 @@ __global__ void __launch_bounds__(kThreads2, 1)
     }
 }
 
-template <bool EH>
+template <bool EH, bool DUAL>
 cudaError_t kernel_attr() {
     static cudaError_t attr = cudaFuncSetAttribute(
-        tc_wa_kernel<EH>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+        tc_wa_kernel<EH, DUAL>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
     return attr;
 }
 
@@ -506,7 +572,8 @@ int max_active_clusters(int bt, int P, const LaunchCtx& c) {
     if (it != cache.end()) return it->second;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(P * 64));
-    cfg.blockDim = dim3(kThreads2);
+    const bool dual = bt <= 128;
+    cfg.blockDim = dim3(kernel_threads(dual));
     cfg.dynamicSmemBytes = smem_bytes(bt, stages_for_bt(bt, c));
     cudaLaunchAttribute at;
     at.id = cudaLaunchAttributeClusterDimension;
@@ -516,9 +583,11 @@ int max_active_clusters(int bt, int P, const LaunchCtx& c) {
     cfg.attrs = &at;
     cfg.numAttrs = 1;
     int n = 0;
-    const cudaError_t e = kernel_attr<false>() == cudaSuccess
-                              ? cudaOccupancyMaxActiveClusters(&n, tc_wa_kernel<false>, &cfg)
-                              : cudaErrorUnknown;
+    cudaError_t e = cudaErrorUnknown;
+    if (dual && kernel_attr<false, true>() == cudaSuccess)
+        e = cudaOccupancyMaxActiveClusters(&n, tc_wa_kernel<false, true>, &cfg);
+    else if (!dual && kernel_attr<false, false>() == cudaSuccess)
+        e = cudaOccupancyMaxActiveClusters(&n, tc_wa_kernel<false, false>, &cfg);
     if (e != cudaSuccess) {
         cudaGetLastError();
         n = 0;
@@ -527,14 +596,14 @@ int max_active_clusters(int bt, int P, const LaunchCtx& c) {
     return n;
 }
 
-template <bool EH>
+template <bool EH, bool DUAL>
 cudaError_t launch2(const CUtensorMap& tx, const CUtensorMap& tw,
                     const Tc2Args& a, dim3 grid, const LaunchCtx& c) {
-    const cudaError_t attr = kernel_attr<EH>();
+    const cudaError_t attr = kernel_attr<EH, DUAL>();
     if (attr != cudaSuccess) return attr;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
-    cfg.blockDim = dim3(kThreads2);
+    cfg.blockDim = dim3(kernel_threads(DUAL));
     cfg.dynamicSmemBytes = smem_bytes(a.bt, a.stages);
     cfg.stream = c.stream;
     cudaLaunchAttribute attrs[2];
@@ -553,7 +622,7 @@ cudaError_t launch2(const CUtensorMap& tx, const CUtensorMap& tw,
     }
     cfg.attrs = na ? attrs : nullptr;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, tc_wa_kernel<EH>, tx, tw, a);
+    return cudaLaunchKernelEx(&cfg, tc_wa_kernel<EH, DUAL>, tx, tw, a);
 }
 
 }  // namespace
@@ -657,7 +726,11 @@ cudaError_t tc_launch(const Problem& p, const LaunchCtx& c) {
             return cudaErrorInvalidValue;
     }
     const dim3 grid((unsigned)(wtiles * splitk), (unsigned)mtiles);
-    return p.even_high ? launch2<true>(tx, tw, a, grid, c) : launch2<false>(tx, tw, a, grid, c);
+    if (bt <= 128)
+        return p.even_high ? launch2<true, true>(tx, tw, a, grid, c)
+                           : launch2<false, true>(tx, tw, a, grid, c);
+    return p.even_high ? launch2<true, false>(tx, tw, a, grid, c)
+                       : launch2<false, false>(tx, tw, a, grid, c);
 }
 
 }  // namespace q4lin
