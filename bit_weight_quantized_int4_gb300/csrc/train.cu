@@ -36,7 +36,7 @@
 // ("[ExecuTorch][WebGPU] Add fp32 matmul ops ... (q4gsw_requant)", #20945.)  The quotient
 // is the IEEE fp32 quotient (__fdiv_rn), rounded half to even (rintf); a NaN quotient gives
 // code 8, like a zero scale; for odd K the padding nibble is 8.
-//   requant16_kernel: one thread per 16 k of a row (four float4 loads of latents in flight,
+//   requant_wide_kernel: one thread per 16 k of a row (four float4 loads of latents in flight,
 //     one 8-byte store); consecutive threads walk a row (coalesced loads and stores).
 //   requant_kernel: the same with 4 k per thread (K % 4 == 0).
 //   requant_generic_kernel: one thread per output byte (any K, any alignment).
@@ -480,47 +480,59 @@ __global__ void requant_kernel(const RqArgs a) {
     }
 }
 
-// One thread per 16 consecutive k of a row: four float4 loads of latents in flight, one
-// 8-byte store of codes; K % 16 == 0, 16-byte aligned latents, 8-byte aligned codes.
-__global__ void requant16_kernel(const RqArgs a) {
+// One thread per 4 * Q consecutive k of a row (Q = 4 or 8): Q float4 loads of latents in
+// flight, one store of 2 * Q code bytes; K % (4 * Q) == 0, 16-byte aligned latents,
+// (2 * Q)-byte aligned codes.  The nibble order is a template parameter.
+template <int Q, bool EH>
+__global__ void requant_wide_kernel(const RqArgs a) {
+    constexpr int KC = 4 * Q;  // k per thread
     griddep_wait();
-    const int64_t chunks = a.K / 16;
+    const int64_t chunks = a.K / KC;
     const int64_t total = a.N * chunks;
     const int gs = (int)(a.gs < a.K ? a.gs : a.K);  // gs >= K: one group
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
          i += (int64_t)gridDim.x * blockDim.x) {
         const int64_t n = i / chunks;
-        const int k0 = (int)(i - n * chunks) * 16;
+        const int k0 = (int)(i - n * chunks) * KC;
         const float4* src = reinterpret_cast<const float4*>(a.latent + n * a.K + k0);
-        float l[16];
+        float l[KC];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < Q; ++q) {
             const float4 u = __ldg(src + q);
             l[4 * q] = u.x, l[4 * q + 1] = u.y, l[4 * q + 2] = u.z, l[4 * q + 3] = u.w;
         }
-        int code[16];
-        if (gs % 16 == 0) {  // the 16 k share one group
-            const float sc = scale_value(a.scales, a.scale_f16, (int64_t)(k0 / gs) * a.N + n);
+        int code[KC];
+        if (gs % 16 == 0) {  // every 16 k share one group
 #pragma unroll
-            for (int j = 0; j < 16; ++j) code[j] = requant_code(l[j], sc);
+            for (int h = 0; h < KC / 16; ++h) {
+                const float sc =
+                    scale_value(a.scales, a.scale_f16, (int64_t)((k0 + 16 * h) / gs) * a.N + n);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) code[16 * h + j] = requant_code(l[16 * h + j], sc);
+            }
         } else {
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
+            for (int j = 0; j < KC; ++j)
                 code[j] = requant_code(l[j], scale_value(a.scales, a.scale_f16,
                                                          (int64_t)((k0 + j) / gs) * a.N + n));
         }
-        uint32_t word[2];
+        uint32_t word[KC / 8];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
+        for (int h = 0; h < KC / 8; ++h) {
             uint32_t w = 0;
 #pragma unroll
             for (int b = 0; b < 4; ++b) {
                 const int e = code[8 * h + 2 * b], o = code[8 * h + 2 * b + 1];
-                w |= (uint32_t)(a.even_high ? (o | (e << 4)) : (e | (o << 4))) << (8 * b);
+                w |= (uint32_t)(EH ? (o | (e << 4)) : (e | (o << 4))) << (8 * b);
             }
             word[h] = w;
         }
-        *reinterpret_cast<uint2*>(a.w + n * a.Kp + k0 / 2) = make_uint2(word[0], word[1]);
+        uint8_t* dst = a.w + n * a.Kp + k0 / 2;
+        if (Q == 8)
+            *reinterpret_cast<uint4*>(dst) = make_uint4(word[0], word[1 % (KC / 8)],
+                                                        word[2 % (KC / 8)], word[3 % (KC / 8)]);
+        else
+            *reinterpret_cast<uint2*>(dst) = make_uint2(word[0], word[1 % (KC / 8)]);
     }
 }
 
@@ -752,12 +764,17 @@ cudaError_t requant_launch(const RequantProblem& p, const LaunchCtx& c) {
     a.gs = p.group_size;
     a.scale_f16 = p.scale_f16;
     a.even_high = p.even_high;
+    const uintptr_t wq = reinterpret_cast<uintptr_t>(p.qweight);
     const bool lat16 = reinterpret_cast<uintptr_t>(p.latent) % 16 == 0 && p.K < (1LL << 31);
-    const bool wide = lat16 && p.K % 16 == 0 && reinterpret_cast<uintptr_t>(p.qweight) % 8 == 0;
-    const bool fast = lat16 && p.K % 4 == 0 && reinterpret_cast<uintptr_t>(p.qweight) % 2 == 0;
-    const int64_t units = wide ? p.N * (p.K / 16) : fast ? p.N * (p.K / 4) : p.N * a.Kp;
+    // (Eight float4 loads a thread, 32 k, measured slower than four on 8192 x 2048.)
+    const bool w16 = lat16 && p.K % 16 == 0 && wq % 8 == 0;
+    const bool fast = lat16 && p.K % 4 == 0 && wq % 2 == 0;
+    const int64_t units = w16 ? p.N * (p.K / 16) : fast ? p.N * (p.K / 4) : p.N * a.Kp;
     const int64_t blocks = std::max<int64_t>(1, std::min<int64_t>((units + 255) / 256, 32LL * c.sm_count));
-    if (wide) return launch(requant16_kernel, a, dim3((unsigned)blocks), 256, c);
+    const dim3 grid((unsigned)blocks);
+    if (w16)
+        return p.even_high ? launch(requant_wide_kernel<4, true>, a, grid, 256, c)
+                           : launch(requant_wide_kernel<4, false>, a, grid, 256, c);
     return fast ? launch(requant_kernel, a, dim3((unsigned)blocks), 256, c)
                 : launch(requant_generic_kernel, a, dim3((unsigned)blocks), 256, c);
 }

@@ -169,6 +169,7 @@ def test_backward_rejects_overlap(handle):
 REQUANT_SHAPES = [
     # N, K, gs, f16
     (8192, 2048, 32, True),    # the benchmark's shape (16-k kernel)
+    (40, 1040, 16, False),     # 16-k kernel, K % 32 == 16, groups of 16
     (64, 2048, 32, False),     # fast kernel
     (33, 4096, 4096, True),    # per channel, fp16 scales
     (100, 512, 64, False),
