@@ -644,10 +644,11 @@ cudaError_t tc_launch(const Problem& p, const LaunchCtx& c) {
     // tiles make wider MMAs; narrower ones give more CTAs.  When the tiles alone leave SMs
     // idle, K is split over a cluster of P CTAs (a power of two up to 8, at least 4 stages
     // each, 16-column slices, only if all the clusters stay resident at once).  Estimate:
-    // waves x stages per CTA x cycles per stage, plus ~2000 cycles for the exchange; a
-    // 64-k stage costs the larger of the tf32 MMAs (~4.2 * bt cycles) and the serial
-    // chains of the producer and issuer threads (~700 cycles); ties go to the narrower
-    // tile.
+    // waves x stages per CTA x cycles per stage, plus the split-K exchange (~30 cycles per
+    // exchanged column of the 128-row partial tile: bt * (P - 1) / P of them); a 64-k
+    // stage costs the larger of the tf32 MMAs (~4.2 * bt cycles) and the serial chains of
+    // the producer and issuer threads (~700 cycles); ties go to the narrower tile.  (Fitted
+    // to a sweep of forced tile heights over M = 64..2048.)
     const int64_t wtiles = (p.N + kWRows - 1) / kWRows;
     const int k_iters = (int)((p.K + kStageK - 1) / kStageK);
     int bt = 256, splitk = 1;
@@ -664,7 +665,8 @@ cudaError_t tc_launch(const Problem& p, const LaunchCtx& c) {
         const int64_t ctas = tiles * P;
         const int64_t waves = (ctas + c.sm_count - 1) / c.sm_count;
         const int64_t per_stage = std::max<int64_t>(700, (int64_t)(4.2 * cand));
-        const int64_t cost = waves * (k_iters / P) * per_stage + (P > 1 ? 2000 : 0);
+        const int64_t cost =
+            waves * (k_iters / P) * per_stage + (P > 1 ? 30LL * cand * (P - 1) / P : 0);
         if (best < 0 || cost <= best) {
             best = cost;
             bt = cand;
