@@ -20,9 +20,9 @@
  * Conventions for every entry point:
  *   - Every buffer is owned by the caller.  q4lin_run allocates nothing, never
  *     synchronizes the device and only enqueues kernels on the given stream.  A handle
- *     owns its options, a 4-byte device status word and about 2 MiB of device scratch
- *     (partial sums of decode launches that split K across CTAs, and their counters),
- *     all allocated by q4lin_create.
+ *     owns its options, a 4-byte device status word and 32 MiB of device scratch plus
+ *     64 KiB of counters (partial sums of launches that split K or the rows across CTAs:
+ *     decode GEMV, tensor-core GEMM, input gradient), all allocated by q4lin_create.
  *   - Status codes, never exceptions, aborts or prints.  Arguments are validated before
  *     any launch: a non-OK status from validation means nothing was enqueued.
  *   - All device pointers must be device-accessible memory of the handle's device.
