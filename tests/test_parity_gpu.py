@@ -275,6 +275,9 @@ TC_SHAPES = [
     (600, 1000, 768, 32, True, True),     # three M tiles, ragged everything
     (33, 1000, 4096, 4096, False, False), # per-channel
     (64, 128257, 4096, 4096, False, False),
+    (40, 200, 320, 32, True, True),       # 5 stages: two MMA issuers with unequal shares
+    (100, 520, 1120, 32, False, True),    # 17.5 stages (odd, last one half), two issuers
+    (300, 1000, 736, 32, True, False),    # 11.5 stages on 128-row tiles
 ]
 
 
@@ -290,6 +293,7 @@ def test_tc_parity(handle, M, N, K, gs, f16, bias):
     (64, 256, 8192, 128, True, False),    # one 256-row tile: 8-way split of long K
     (200, 520, 1024, 1024, False, True),  # per-channel scales applied after the exchange
     (9, 96, 512, 32, True, True),         # 16 stages over 4 CTAs, ragged N inside the slices
+    (64, 1024, 4096, 128, True, True),    # 64-row tiles, two issuers, K split over 4 CTAs
 ])
 def test_tc_split_k_parity_and_determinism(handle, M, N, K, gs, f16, bias):
     """Few output tiles: the K range is split over the CTAs of a cluster, whose partial
