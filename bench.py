@@ -356,24 +356,27 @@ def weight_copies(torch, N, K, bytes_each, l2_bytes=L2_BYTES, cap=1024):
     return ws, ss
 
 
-def shape_bandwidth(torch, handle, N, K):
-    """GB/s of one GEMV shape in isolation, every launch on its own weight copy (HBM-cold
-    weights; x stays L2-resident as it would in a model)."""
+def shape_bandwidth(torch, handle, N, K, M=1):
+    """GB/s of one GEMV shape (M activation rows) in isolation, every launch on its own
+    weight copy (HBM-cold weights; x stays L2-resident as it would in a model)."""
     from bit_weight_quantized_int4_gb300 import q4lin as q
-    b = gemv_bytes(N, K)
+    b = gemv_bytes(N, K) + 4 * (M - 1) * (K + N)
     ws, ss = weight_copies(torch, N, K, b)
-    x = torch.randn(K, device="cuda")
-    out = torch.empty(N, device="cuda")
+    x = torch.randn(M, K, device="cuda")
+    out = torch.empty(M, N, device="cuda")
 
     def launch(i, sp):
         st = q.q4lin_run(handle, x.data_ptr(), ws[i % len(ws)].data_ptr(),
-                         ss[i % len(ws)].data_ptr(), None, out.data_ptr(), 1, N, K, GROUP,
+                         ss[i % len(ws)].data_ptr(), None, out.data_ptr(), M, N, K, GROUP,
                          q.Q4LIN_SCALE_F16, sp)
         assert st == q.Q4LIN_OK
 
     us = graph_time_us(torch, launch, len(ws))
     del ws, ss
-    return {"N": N, "K": K, "us": round(us, 3), "GB_s": round(b / us / 1e3, 1)}
+    row = {"N": N, "K": K, "us": round(us, 3), "GB_s": round(b / us / 1e3, 1)}
+    if M > 1:
+        row["M"] = M
+    return row
 
 
 def prefill_tflops(torch, handle, M, N, K, reps=10):
@@ -522,7 +525,8 @@ def load_peaks():
 
 
 CROSSOVER_M = (1, 2, 3, 4, 5, 7, 8, 12, 16, 24, 32, 33, 48, 64, 96, 128, 256, 512)
-CROSSOVER_NK = ((2048, 2048), (8192, 2048), (2048, 8192), (128256, 2048), (1000, 2048))
+CROSSOVER_NK = ((2048, 2048), (8192, 2048), (2048, 8192), (128256, 2048), (1000, 2048),
+                (4096, 14336), (14336, 4096))
 
 
 def crossover():
@@ -577,7 +581,7 @@ def profile(spec):
             token.run(torch.cuda.current_stream().cuda_stream)
     elif kind == "gemv":
         N, K = int(dims[0]), int(dims[1])
-        shape_bandwidth(torch, h, N, K)
+        shape_bandwidth(torch, h, N, K, int(dims[2]) if len(dims) > 2 else 1)
     elif kind == "prefill":
         M, N, K = (int(d) for d in dims)
         prefill_tflops(torch, h, M, N, K, reps=3)
@@ -612,7 +616,7 @@ def main():
                     help="time the CUDA-core and tensor-core paths over M and print the "
                          "measured table (JSON) instead of the benchmark line")
     ap.add_argument("--profile", default=None,
-                    help="run a few launches of one op and exit (for ncu): gemv:N:K, "
+                    help="run a few launches of one op and exit (for ncu): gemv:N:K[:M], "
                          "prefill:M:N:K, backward:M:N:K, requant:N:K or token:1b|8b")
     args = ap.parse_args()
     if args.profile:

@@ -38,17 +38,25 @@ constexpr int64_t kDefaultWaitLimit = 2000000000LL;  // 2 s of GPU global time
 constexpr int64_t kWsFloats = 1 << 23;   // 32 MiB (split-K partials: GEMV, backward, TC)
 constexpr int64_t kTickets = 1 << 14;    // 64 KiB
 
-// M-dispatch between the row-streaming CUDA-core kernel (which re-reads the weights for
-// every 4 activation rows, so its time grows with M) and the tensor-core GEMM (flat in M
-// up to 128 rows).  Crossover table from a device-time sweep on GB300 (M = 1..512;
-// N x K = 1000 x 2048, 2048 x 2048, 8192 x 2048, 2048 x 8192, 128256 x 2048; every launch
-// on HBM-cold weights): the largest M for which row streaming is still faster, by the
-// weight count N * K (and long K, where the tensor-core main loop is longest).
+// M-dispatch between the CUDA-core kernels (the row-streaming kernel, which re-reads the
+// weights for every 4 activation rows, so its time grows with M, and the TMA-fed multi-row
+// GEMV for 2..4 rows) and the tensor-core GEMM (flat in M up to 64 rows).  Crossover table
+// from a device-time sweep on GB300 (M = 1..512; N x K = 1000 x 2048, 2048 x 2048,
+// 8192 x 2048, 2048 x 8192, 128256 x 2048, 4096 x 14336, 14336 x 4096; every launch on
+// HBM-cold weights): the largest M for which the CUDA-core path is still faster, by the
+// weight count N * K.
 int64_t rowstream_max_m(const q4lin::Problem& p) {
     const double nk = (double)p.N * (double)p.K;
     if (nk < 3.0e6) return 16;
-    if (nk < 8.0e6 || p.K >= 8192) return 8;
+    if (nk < 8.0e6) return 8;
     return 4;
+}
+
+// For 2..4 rows the multi-row GEMV beats row streaming from about 8 M weights on (1.2x at
+// 8192 x 2048, 1.7x at 128256 x 2048 and 4 rows); below that its fixed pipeline latency
+// loses to row streaming (2048 x 2048: 6.2 against 4.3 us at 2 rows).
+bool multirow_preferred(const q4lin::Problem& p) {
+    return (double)p.N * (double)p.K >= 8.0e6 && q4lin::gemv_mr_eligible(p);
 }
 
 class DeviceGuard {
@@ -259,7 +267,8 @@ q4lin_status_t q4lin_run(q4lin_handle_t h, const float* x, const uint8_t* qweigh
         case Q4LIN_PATH_TC: err = q4lin::tc_launch(p, c); break;
         case Q4LIN_PATH_GEMV:
             err = q4lin::gemv_tma_eligible(p) ? q4lin::gemv_tma_launch(p, c)
-                                              : q4lin::rowstream_launch(p, c);
+                  : multirow_preferred(p)       ? q4lin::gemv_mr_launch(p, c)
+                                                : q4lin::rowstream_launch(p, c);
             break;
         default: err = q4lin::generic_launch(p, c); break;
     }

@@ -60,6 +60,14 @@ int gemv_tma_max_group();
 bool gemv_tma_groupable(const Problem& a, const Problem& b);
 cudaError_t gemv_tma_launch_group(const Problem* ps, int count, const LaunchCtx& c);
 
+// TMA-fed GEMV for 2 <= M <= 4 activation rows: a producer warp streams the weight
+// tile, its group scales and the x tile of each 512-k stage into a shared-memory ring;
+// each widened code is used for all M rows.  Needs K % 32 == 0, K >= 512, N >= 16, a
+// scale row of whole 16-byte units, 16-byte aligned x, qweight and scales, and a
+// power-of-two group size that is a multiple of 32, or group_size >= K.
+bool gemv_mr_eligible(const Problem& p);
+cudaError_t gemv_mr_launch(const Problem& p, const LaunchCtx& c);
+
 // Generic CUDA-core kernel: any K (odd included), any group size, any alignment.
 cudaError_t generic_launch(const Problem& p, const LaunchCtx& c);
 

@@ -124,6 +124,10 @@ struct Tc2Args {
     // covers stages [r * kpp, (r + 1) * kpp) of the tile; rank q finishes the activation
     // rows [q * sw, (q + 1) * sw) of the tile.
     int splitk, kpp, sw;
+    // Rows of the x box of the last activation tile: the rows it still holds, rounded up
+    // to 8 (its own tensor map).  Rows of a box past the end of x cost the copy engine
+    // nearly as much as real ones; the slot rows past them are never stored.
+    int xrows_last;
     float* ws;  // split K: [tiles][P][P - 1][sw][128] partial columns exchanged through L2
 };
 
@@ -160,6 +164,7 @@ __device__ __forceinline__ void dequant_chunk(const uint4 wv, float sc, uint32_t
 template <bool EH, bool DUAL>
 __global__ void __launch_bounds__(kernel_threads(DUAL), 1)
     tc_wa_kernel(const __grid_constant__ CUtensorMap tmap_x,
+                 const __grid_constant__ CUtensorMap tmap_xl,
                  const __grid_constant__ CUtensorMap tmap_w, const Tc2Args a) {
     constexpr int kCtl = ctl_warps(DUAL);
     extern __shared__ uint8_t smem_raw[];
@@ -231,7 +236,10 @@ __global__ void __launch_bounds__(kernel_threads(DUAL), 1)
         if (lane == 0) {
             // ------------------------------------------------------ TMA producers of x
             const int pr = warp >> 1;  // producer 0 or 1
-            prefetch_tensormap(&tmap_x);
+            const bool last_tile = blockIdx.y == gridDim.y - 1;
+            const CUtensorMap* xmap = last_tile ? &tmap_xl : &tmap_x;
+            const uint32_t xtx = (uint32_t)(last_tile ? a.xrows_last : bt) * 128;
+            prefetch_tensormap(xmap);
             griddep_wait();
             // Stages of this producer: every stage (box pr) or, with alt, stages pr,
             // pr + 2, ... (both boxes).  Slot and phase kept incrementally.
@@ -253,14 +261,14 @@ __global__ void __launch_bounds__(kernel_threads(DUAL), 1)
                     const int64_t k = (int64_t)(it_begin + li) * kStageK;
                     const bool two = k + kHalfK < a.K;  // else the last stage has one half
                     if (alt) {
-                        mbar_arrive_expect_tx(full(s), two ? 2 * xbox : xbox);
-                        tma_load_2d(xslot(s), &tmap_x, (int)k, (int)m0, full(s));
+                        mbar_arrive_expect_tx(full(s), two ? 2 * xtx : xtx);
+                        tma_load_2d(xslot(s), xmap, (int)k, (int)m0, full(s));
                         if (two)
-                            tma_load_2d(xslot(s) + xbox, &tmap_x, (int)(k + kHalfK), (int)m0,
+                            tma_load_2d(xslot(s) + xbox, xmap, (int)(k + kHalfK), (int)m0,
                                         full(s));
                     } else if (pr == 0 || two) {
-                        mbar_arrive_expect_tx(full(s), xbox);
-                        tma_load_2d(xslot(s) + (uint32_t)pr * xbox, &tmap_x,
+                        mbar_arrive_expect_tx(full(s), xtx);
+                        tma_load_2d(xslot(s) + (uint32_t)pr * xbox, xmap,
                                     (int)(k + kHalfK * pr), (int)m0, full(s));
                     } else {
                         mbar_arrive(full(s));  // the missing half of a last stage
@@ -597,7 +605,7 @@ int max_active_clusters(int bt, int P, const LaunchCtx& c) {
 }
 
 template <bool EH, bool DUAL>
-cudaError_t launch2(const CUtensorMap& tx, const CUtensorMap& tw,
+cudaError_t launch2(const CUtensorMap& tx, const CUtensorMap& txl, const CUtensorMap& tw,
                     const Tc2Args& a, dim3 grid, const LaunchCtx& c) {
     const cudaError_t attr = kernel_attr<EH, DUAL>();
     if (attr != cudaSuccess) return attr;
@@ -622,7 +630,7 @@ cudaError_t launch2(const CUtensorMap& tx, const CUtensorMap& tw,
     }
     cfg.attrs = na ? attrs : nullptr;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, tc_wa_kernel<EH, DUAL>, tx, tw, a);
+    return cudaLaunchKernelEx(&cfg, tc_wa_kernel<EH, DUAL>, tx, txl, tw, a);
 }
 
 }  // namespace
@@ -704,14 +712,16 @@ cudaError_t tc_launch(const Problem& p, const LaunchCtx& c) {
     a.wait_ns = c.wait_limit_ns;
     a.skip_first_copy = c.tc_skip_first_copy;
 
-    CUtensorMap tx, tw;
-    {
+    a.xrows_last = (int)std::min<int64_t>(bt, (p.M - (mtiles - 1) * bt + 7) / 8 * 8);
+
+    CUtensorMap tx, txl, tw;
+    for (int last = 0; last < 2; ++last) {
         const cuuint64_t dims[2] = {(cuuint64_t)p.K, (cuuint64_t)p.M};
         const cuuint64_t strides[1] = {(cuuint64_t)p.K * 4};
-        const cuuint32_t box[2] = {(cuuint32_t)kHalfK, (cuuint32_t)bt};
+        const cuuint32_t box[2] = {(cuuint32_t)kHalfK, (cuuint32_t)(last ? a.xrows_last : bt)};
         const cuuint32_t estr[2] = {1, 1};
-        if (enc(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(p.x), dims, strides,
-                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+        if (enc(last ? &txl : &tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(p.x),
+                dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
@@ -729,10 +739,10 @@ cudaError_t tc_launch(const Problem& p, const LaunchCtx& c) {
     }
     const dim3 grid((unsigned)(wtiles * splitk), (unsigned)mtiles);
     if (bt <= 128)
-        return p.even_high ? launch2<true, true>(tx, tw, a, grid, c)
-                           : launch2<false, true>(tx, tw, a, grid, c);
-    return p.even_high ? launch2<true, false>(tx, tw, a, grid, c)
-                       : launch2<false, false>(tx, tw, a, grid, c);
+        return p.even_high ? launch2<true, true>(tx, txl, tw, a, grid, c)
+                           : launch2<false, true>(tx, txl, tw, a, grid, c);
+    return p.even_high ? launch2<true, false>(tx, txl, tw, a, grid, c)
+                       : launch2<false, false>(tx, txl, tw, a, grid, c);
 }
 
 }  // namespace q4lin

@@ -449,3 +449,104 @@ def test_split_k_parity_and_determinism(handle, N, K, gs):
     assert_parity(outs[0], ref, mag, TOL_FP32)
     np.testing.assert_array_equal(outs[0], outs[1])
     np.testing.assert_array_equal(outs[0], outs[2])
+
+
+# ------------------------------------------------------- TMA-fed GEMV, 2 <= M <= 4 rows
+# Shapes that take the multi-row TMA GEMV: at least 8 M weights, K % 32 == 0, K >= 512,
+# N >= 16, a scale row of whole 16-byte units (N % 8 for fp16 scales, N % 4 for fp32), a
+# power-of-two group size (or one group per row).  Covered: ragged N (not a multiple of the
+# 64-row block), a K tail shorter than a 512-k stage, groups wider than a stage, per-channel
+# scales, the smallest N with a K long enough for the 8-part split, fp32 and fp16 scales.
+MR_SHAPES = [
+    # N, K, gs, f16, bias
+    (8192, 2048, 32, True, True),
+    (8200, 1056, 32, False, True),
+    (2048, 8192, 128, True, True),
+    (4104, 4096, 1024, False, False),
+    (136, 65536, 65536, True, True),
+    (16, 524288, 524288, True, False),
+    (2080, 4096, 64, False, True),
+]
+
+
+@pytest.mark.parametrize("M", [2, 3, 4])
+@pytest.mark.parametrize("N,K,gs,f16,bias", MR_SHAPES)
+def test_multirow_gemv_parity(handle, M, N, K, gs, f16, bias):
+    c = synth.make_case(M, N, K, gs, scale_f16=f16, bias=bias, seed=7 * N + K + M)
+    _, used = check_case(handle, c, AUTO)
+    assert used == GEMV
+
+
+@pytest.mark.parametrize("M", [2, 4])
+def test_multirow_gemv_lm_head(handle, M):
+    c = synth.make_case(M, 128256, 2048, 32, scale_f16=True, bias=False, seed=50 + M)
+    check_case(handle, c, GEMV)
+
+
+@pytest.mark.parametrize("M", [2, 3, 4])
+def test_multirow_gemv_even_high(handle, M):
+    c = synth.make_case(M, 2056, 4096, 64, scale_f16=True, bias=True, seed=60 + M)
+    check_case(handle, c, GEMV, even_high=True)
+
+
+@pytest.mark.parametrize("M", [2, 3, 4])
+@pytest.mark.parametrize("f16", [False, True])
+def test_multirow_gemv_dyadic_bit_exact(handle, M, f16):
+    c = synth.make_dyadic_case(M, 2048, 4096, 32, scale_f16=f16, bias=True, seed=70 + M)
+    out, _ = run_q4lin(handle, c, GEMV)
+    ref, _ = oracle.linear(c.x, c.qweight, c.scales, c.bias, c.K, c.group_size)
+    np.testing.assert_array_equal(out.astype(np.float64), ref)
+
+
+def test_multirow_gemv_all_codes_eight(handle):
+    c = synth.make_case(4, 4096, 2048, 32, scale_f16=True, bias=True, seed=80)
+    c.qweight = synth.fill_codes(4096, 2048, 8)
+    out, _ = run_q4lin(handle, c, GEMV)
+    np.testing.assert_array_equal(out, np.broadcast_to(c.bias, out.shape))
+
+
+@pytest.mark.parametrize("M", [2, 4])
+def test_multirow_gemv_split_k_deterministic(handle, M):
+    """Few row blocks, long K: the K range is cut into parts whose partial sums are added
+    in part order; repeated calls give identical bits."""
+    c = synth.make_case(M, 512, 16384, 32, scale_f16=True, bias=True, seed=90 + M)
+    outs = [run_q4lin(handle, c, AUTO)[0] for _ in range(3)]
+    ref, mag = oracle.linear(c.x, c.qweight, c.scales, c.bias, c.K, 32)
+    assert_parity(outs[0], ref, mag, TOL_FP32)
+    np.testing.assert_array_equal(outs[0], outs[1])
+    np.testing.assert_array_equal(outs[0], outs[2])
+
+
+@pytest.mark.parametrize("pdl", [0, 1])
+@pytest.mark.parametrize("M", [2, 4])
+def test_multirow_dependent_chain(handle, pdl, M):
+    """Multi-row GEMVs chained on one stream, each reading the previous output as its x
+    (NaN-poisoned first): with programmatic dependent launch the weights of the first
+    stages are requested early, x only after the predecessor completed."""
+    import torch
+    from bit_weight_quantized_int4_gb300 import q4lin as q
+    dims = [2048, 4096, 1024, 2048, 8192, 2048]
+    links = [synth.make_case(M, dims[i + 1], dims[i], 32, scale_f16=True, bias=(i % 2 == 0),
+                             seed=950 + i) for i in range(len(dims) - 1)]
+    bufs = [torch.from_numpy(links[0].x).cuda()]
+    bufs += [torch.full((M, d), float("nan"), device="cuda") for d in dims[1:]]
+    dev = [tuple(None if a is None else torch.from_numpy(a).cuda()
+                 for a in (c.qweight, c.scales, c.bias)) for c in links]
+    torch.cuda.synchronize()
+    q.q4lin_set_option(handle, q.Q4LIN_OPT_PDL, pdl)
+    try:
+        stream = torch.cuda.current_stream().cuda_stream
+        for i, c in enumerate(links):
+            w, s, b = dev[i]
+            st = q.q4lin_run(handle, bufs[i].data_ptr(), w.data_ptr(), s.data_ptr(),
+                             None if b is None else b.data_ptr(), bufs[i + 1].data_ptr(),
+                             M, c.N, c.K, 32, q.Q4LIN_SCALE_F16, stream)
+            assert st == q.Q4LIN_OK
+        torch.cuda.synchronize()
+    finally:
+        q.q4lin_set_option(handle, q.Q4LIN_OPT_PDL, 0)
+    host = [b.cpu().numpy() for b in bufs]
+    for i, c in enumerate(links):
+        assert not np.isnan(host[i + 1]).any(), f"link {i} output has NaN"
+        ref, mag = oracle.linear(host[i], c.qweight, c.scales, c.bias, c.K, 32)
+        assert_parity(host[i + 1], ref, mag, TOL_FP32)
