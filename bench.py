@@ -664,6 +664,9 @@ def main():
                 seen.add((N, K))
                 shapes.append(shape_bandwidth(torch, h, N, K))
         extra["gemv_shapes"] = shapes
+        # A few activation rows (speculative decoding, small batches): the multi-row GEMV.
+        extra["small_m"] = [shape_bandwidth(torch, h, N, K, M) for M in (2, 4)
+                            for N, K in ((8192, 2048), (2048, 8192), (128256, 2048))]
         extra["prefill"] = [prefill_tflops(torch, h, M, N, K)
                             for M in (128, 512, 2048) for N, K in PREFILL_NK]
         extra["training"] = ([backward_bandwidth(torch, h, M, N, K)
