@@ -39,7 +39,7 @@ L2_BYTES = 129 << 20
 # launch list (dram__bytes_read.sum + dram__bytes_write.sum per launch; the summary is
 # profiles/gemv_tma_token_1b_launches.md).  Valid only for the kernel source it was taken
 # with: the sha256 prefix of gemv_tma.cu + ptx.cuh; any other source reports null.
-TOKEN_TRAFFIC = {"bytes": 698170880, "launches": 65, "source_sha256": "487c08129dbd7bed"}
+TOKEN_TRAFFIC = {"bytes": 698272000, "launches": 65, "source_sha256": "6accd3e6b8e2c593"}
 
 
 def gemv_source_sha():

@@ -347,8 +347,7 @@ __global__ void __launch_bounds__(kMrThreads, 2)
 template <int MR, bool EH, bool F16>
 cudaError_t launch_mr(const MrMaps& maps, const MrArgs& a, unsigned grid, int smem,
                       const LaunchCtx& c) {
-    static const cudaError_t attr = cudaFuncSetAttribute(
-        gemv_mr_kernel<MR, EH, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMrSmem);
+    const cudaError_t attr = kernel_smem_once<gemv_mr_kernel<MR, EH, F16>>(kMrSmem);
     if (attr != cudaSuccess) return attr;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);

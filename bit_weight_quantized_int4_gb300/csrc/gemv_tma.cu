@@ -446,14 +446,7 @@ __global__ void __launch_bounds__(kThreadsG, 2)
 
 template <int V, bool EH, bool PC, bool F16>
 cudaError_t launch_v(const TensorMaps& tm, const GArgs& a, unsigned grid, const LaunchCtx& c) {
-    static cudaError_t attr = [] {
-        cudaError_t e = cudaFuncSetAttribute(gemv_tma_kernel<V, EH, PC, F16>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kCtaSmem);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(gemv_tma_kernel<V, EH, PC, F16>,
-                                     cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-        return e;
-    }();
+    const cudaError_t attr = kernel_smem_once<gemv_tma_kernel<V, EH, PC, F16>>(kCtaSmem, 100);
     if (attr != cudaSuccess) return attr;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);

@@ -6,7 +6,28 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace q4lin {
+
+// Function attributes belong to the function's instance in one device's context: a kernel
+// that needs more than 48 KiB of dynamic shared memory (or a carveout) gets them set once
+// per device, on the first launch there (the caller has made the handle's device current).
+// Thread-safe; concurrent first launches may both set them, which is harmless.
+template <auto Kernel>
+cudaError_t kernel_smem_once(int bytes, int carveout = -1) {
+    static std::atomic<uint64_t> done{0};  // one bit per device ordinal < 64
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = dev >= 0 && dev < 64 ? (1ULL << dev) : 0;
+    if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+    e = cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && carveout >= 0)
+        e = cudaFuncSetAttribute(Kernel, cudaFuncAttributePreferredSharedMemoryCarveout, carveout);
+    if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_release);
+    return e;
+}
 
 // cuTensorMapEncodeTiled of the driver, resolved once through the runtime (null when the
 // driver does not provide it); used by every TMA-fed kernel to build its tensor maps.

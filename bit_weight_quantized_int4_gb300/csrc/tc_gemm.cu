@@ -552,9 +552,7 @@ __global__ void __launch_bounds__(kernel_threads(DUAL), 1)
 
 template <bool EH, bool DUAL>
 cudaError_t kernel_attr() {
-    static cudaError_t attr = cudaFuncSetAttribute(
-        tc_wa_kernel<EH, DUAL>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
-    return attr;
+    return kernel_smem_once<tc_wa_kernel<EH, DUAL>>(kSmemLimit);
 }
 
 int stages_for_bt(int bt, const LaunchCtx& c) {

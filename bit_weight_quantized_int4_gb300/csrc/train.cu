@@ -576,8 +576,7 @@ constexpr int kBtSmemLimit = 113 * 1024;  // two CTAs per SM
 template <int MT>
 cudaError_t launch_bt(const BtMaps& maps, const BtArgs& a, dim3 grid, int smem,
                       const LaunchCtx& c) {
-    static const cudaError_t attr = cudaFuncSetAttribute(
-        backward_tma_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, kBtSmemLimit);
+    const cudaError_t attr = kernel_smem_once<backward_tma_kernel<MT>>(kBtSmemLimit);
     if (attr != cudaSuccess) return attr;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
