@@ -52,11 +52,12 @@ int64_t rowstream_max_m(const q4lin::Problem& p) {
     return 4;
 }
 
-// For 2..4 rows the multi-row GEMV beats row streaming from about 8 M weights on (1.2x at
+// For 2..4 rows the multi-row GEMV beats row streaming from about 10 M weights on (1.2x at
 // 8192 x 2048, 1.7x at 128256 x 2048 and 4 rows); below that its fixed pipeline latency
-// loses to row streaming (2048 x 2048: 6.2 against 4.3 us at 2 rows).
+// (~5 us) loses to row streaming (2048 x 2048: 6.2 against 4.3 us at 2 rows; 4096 x 2048:
+// 6.5 against 6.0).
 bool multirow_preferred(const q4lin::Problem& p) {
-    return (double)p.N * (double)p.K >= 8.0e6 && q4lin::gemv_mr_eligible(p);
+    return (double)p.N * (double)p.K >= 1.0e7 && q4lin::gemv_mr_eligible(p);
 }
 
 class DeviceGuard {

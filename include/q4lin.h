@@ -65,7 +65,7 @@ typedef enum { Q4LIN_SCALE_F32 = 0, Q4LIN_SCALE_F16 = 1 } q4lin_scale_dtype_t;
 typedef enum {
     Q4LIN_PATH_AUTO = 0,
     Q4LIN_PATH_GEMV = 1,    /* CUDA-core GEMV family: TMA-fed decode GEMV (M = 1),
-                               TMA-fed multi-row GEMV (2 <= M <= 4, >= 8 M weights),
+                               TMA-fed multi-row GEMV (2 <= M <= 4, >= 10 M weights),
                                else the row-streaming kernel (small M)                */
     Q4LIN_PATH_FFMA = 2,    /* generic CUDA-core kernel: any K, group size, alignment  */
     Q4LIN_PATH_TC = 3       /* tcgen05 tensor-core GEMM (TMEM accumulators)            */

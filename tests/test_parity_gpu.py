@@ -452,7 +452,7 @@ def test_split_k_parity_and_determinism(handle, N, K, gs):
 
 
 # ------------------------------------------------------- TMA-fed GEMV, 2 <= M <= 4 rows
-# Shapes that take the multi-row TMA GEMV: at least 8 M weights, K % 32 == 0, K >= 512,
+# Shapes that take the multi-row TMA GEMV: at least 10 M weights, K % 32 == 0, K >= 512,
 # N >= 16, a scale row of whole 16-byte units (N % 8 for fp16 scales, N % 4 for fp32), a
 # power-of-two group size (or one group per row).  Covered: ragged N (not a multiple of the
 # 64-row block), a K tail shorter than a 512-k stage, groups wider than a stage, per-channel
@@ -460,12 +460,12 @@ def test_split_k_parity_and_determinism(handle, N, K, gs):
 MR_SHAPES = [
     # N, K, gs, f16, bias
     (8192, 2048, 32, True, True),
-    (8200, 1056, 32, False, True),
+    (10056, 1056, 32, False, True),
     (2048, 8192, 128, True, True),
     (4104, 4096, 1024, False, False),
-    (136, 65536, 65536, True, True),
-    (16, 524288, 524288, True, False),
-    (2080, 4096, 64, False, True),
+    (168, 65536, 65536, True, True),
+    (24, 524288, 524288, True, False),
+    (2600, 4096, 64, False, True),
 ]
 
 
@@ -485,22 +485,22 @@ def test_multirow_gemv_lm_head(handle, M):
 
 @pytest.mark.parametrize("M", [2, 3, 4])
 def test_multirow_gemv_even_high(handle, M):
-    c = synth.make_case(M, 2056, 4096, 64, scale_f16=True, bias=True, seed=60 + M)
+    c = synth.make_case(M, 2568, 4096, 64, scale_f16=True, bias=True, seed=60 + M)
     check_case(handle, c, GEMV, even_high=True)
 
 
 @pytest.mark.parametrize("M", [2, 3, 4])
 @pytest.mark.parametrize("f16", [False, True])
 def test_multirow_gemv_dyadic_bit_exact(handle, M, f16):
-    c = synth.make_dyadic_case(M, 2048, 4096, 32, scale_f16=f16, bias=True, seed=70 + M)
+    c = synth.make_dyadic_case(M, 2560, 4096, 32, scale_f16=f16, bias=True, seed=70 + M)
     out, _ = run_q4lin(handle, c, GEMV)
     ref, _ = oracle.linear(c.x, c.qweight, c.scales, c.bias, c.K, c.group_size)
     np.testing.assert_array_equal(out.astype(np.float64), ref)
 
 
 def test_multirow_gemv_all_codes_eight(handle):
-    c = synth.make_case(4, 4096, 2048, 32, scale_f16=True, bias=True, seed=80)
-    c.qweight = synth.fill_codes(4096, 2048, 8)
+    c = synth.make_case(4, 5120, 2048, 32, scale_f16=True, bias=True, seed=80)
+    c.qweight = synth.fill_codes(5120, 2048, 8)
     out, _ = run_q4lin(handle, c, GEMV)
     np.testing.assert_array_equal(out, np.broadcast_to(c.bias, out.shape))
 
@@ -509,7 +509,7 @@ def test_multirow_gemv_all_codes_eight(handle):
 def test_multirow_gemv_split_k_deterministic(handle, M):
     """Few row blocks, long K: the K range is cut into parts whose partial sums are added
     in part order; repeated calls give identical bits."""
-    c = synth.make_case(M, 512, 16384, 32, scale_f16=True, bias=True, seed=90 + M)
+    c = synth.make_case(M, 640, 16384, 32, scale_f16=True, bias=True, seed=90 + M)
     outs = [run_q4lin(handle, c, AUTO)[0] for _ in range(3)]
     ref, mag = oracle.linear(c.x, c.qweight, c.scales, c.bias, c.K, 32)
     assert_parity(outs[0], ref, mag, TOL_FP32)
