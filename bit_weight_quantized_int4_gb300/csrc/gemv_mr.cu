@@ -12,13 +12,17 @@
 // padded row stride spreads the 16 chunk lanes' group rows over the banks] and the x tile
 // [MR rows x 512 k] (a 3D box of 128-byte chunk rows with the 128-byte swizzle, so that
 // the 16 chunk lanes reading the same offset of 16 chunks hit different banks) into a
-// ring, all on one mbarrier.  Consumer thread = (chunk lane j of 16, row group of 4 rows):
-// per stage it takes chunk j (32 k) of its 4 rows, word by word (8 k): it loads the x
-// values of the MR rows once, widens each row's word once (byte permute + packed add, as
-// in the M = 1 GEMV), applies the row's group scale, and accumulates MR packed FMAs.  So
-// x is read from shared memory once per 4 rows and each code is widened once for all MR
-// rows.  The 16 chunk lanes of a row group are added with shuffles; lane j then holds all
-// (m, row) sums and stores sum (j / 4, j % 4).  When the row blocks alone leave SMs idle,
+// ring, all on one mbarrier; the weight and scale copies of the first stages go out before
+// the grid-dependency wait, their x copies after it.  Consumer thread = (chunk lane j of
+// 16, row group of 4 rows): per stage it takes chunk j (32 k, one group) of its 4 rows,
+// word by word (8 k, in a lane-rotated order that keeps the warp's code reads on 32
+// banks): it loads the x values of the MR rows once, widens each row's word once (byte
+// permute + packed add, as in the M = 1 GEMV) and issues MR packed FMAs per pair of
+// codes; the group scale multiplies each widened pair (MR = 4) or the stage's unscaled
+// sums (MR = 2, which has the registers for them).  So x is read from shared memory once
+// per 4 rows and each code is widened once for all MR rows.  The 16 chunk lanes of a row
+// group are added with shuffles; lane j then holds all (m, row) sums and stores sum
+// (j / 4, j % 4).  When the row blocks alone leave SMs idle,
 // K is cut into parts; the parts write partial sums to the handle's workspace and the
 // last item of a row block (an atomic ticket) adds them in part order (deterministic).
 // Every wait is bounded in time; after a timeout the warps walk their remaining items
@@ -65,7 +69,7 @@ struct MrArgs {
     int gs_in_stage;       // group size when a stage holds whole groups (gs <= 512), else 0
     int gshift;            // then: group row of stage ks = ks << gshift
     int stages_per_group;  // else: group row = ks / stages_per_group
-    int sc_rows, scale_f16;
+    int sc_rows;
     int parts, tpp, items;
     int64_t wait_ns;
 };
@@ -404,7 +408,6 @@ cudaError_t gemv_mr_launch(const Problem& p, const LaunchCtx& c) {
     a.ws_rows = blocks * kMrRows;
     a.kstages = kstages;
     a.sc_rows = p.scale_f16 ? kMrScRows16 : kMrScRows32;
-    a.scale_f16 = p.scale_f16;
     a.wait_ns = c.wait_limit_ns;
     // Group row of stage ks: ks * 512 / gs (gs <= 512: a shift), ks / (gs / 512), or 0.
     int gps = 1;
