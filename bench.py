@@ -88,15 +88,21 @@ def token_shapes(model):
 
 # ------------------------------------------------------------------------------ clocks
 class ClockSampler:
-    """nvidia-smi clocks/throttle reasons every 200 ms while the timed region runs."""
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi clocks and throttle reasons every 20 ms around the timed region.
+
+    mark_start() / mark_end() bracket the timed region on the host clock; the summary keeps
+    the samples whose nvidia-smi timestamp falls inside it (widened by one sampling period
+    on each side), and says how many there were."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    PERIOD_MS = 20
 
     def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.proc = None
         self.path = None
+        self.t0 = self.t1 = None
 
     def __enter__(self):
         fd, self.path = tempfile.mkstemp(prefix="q4clk_", suffix=".csv")
@@ -104,20 +110,37 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.PERIOD_MS)],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except (FileNotFoundError, OSError):
             self.proc = None
         time.sleep(0.3)
         return self
 
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
     def __exit__(self, *exc):
         if self.proc is not None:
+            time.sleep(2 * self.PERIOD_MS / 1000)
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
+
+    @staticmethod
+    def _stamp(text):
+        import datetime
+        for fmt in ("%Y/%m/%d %H:%M:%S.%f", "%Y/%m/%d %H:%M:%S"):
+            try:
+                return datetime.datetime.strptime(text, fmt).timestamp()
+            except ValueError:
+                pass
+        return None
 
     def summary(self):
         if self.proc is None or not self.path:
@@ -125,27 +148,33 @@ class ClockSampler:
         rows = []
         for line in open(self.path):
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
             try:
-                rows.append(dict(sm=float(parts[1]), smax=float(parts[2]),
-                                 power=float(parts[3]) if parts[3] not in ("[N/A]", "") else None,
-                                 hw=parts[5], hwt=parts[6], swt=parts[7], swp=parts[8]))
+                rows.append(dict(t=self._stamp(parts[0]), sm=float(parts[2]),
+                                 smax=float(parts[3]),
+                                 power=float(parts[4]) if parts[4] not in ("[N/A]", "") else None,
+                                 hw=parts[6], hwt=parts[7], swt=parts[8], swp=parts[9]))
             except ValueError:
                 continue
         os.unlink(self.path)
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        loaded = [r for r in rows if r["power"] is None or r["power"] > 0] or rows
+        slack = self.PERIOD_MS / 1000
+        inside = [r for r in rows if r["t"] is not None and self.t0 is not None and
+                  self.t1 is not None and self.t0 - slack <= r["t"] <= self.t1 + slack]
+        use = inside or rows
         reasons = set()
-        for r in loaded:
+        for r in use:
             for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
                               ("swt", "sw_thermal_slowdown"), ("swp", "sw_power_cap")):
                 if r[key].lower().startswith("active"):
                     reasons.add(name)
-        return {"sm_mhz": statistics.median(r["sm"] for r in loaded),
-                "sm_max_mhz": max(r["smax"] for r in loaded),
-                "samples": len(loaded), "reasons": sorted(reasons)}
+        return {"sm_mhz": statistics.median(r["sm"] for r in use),
+                "sm_max_mhz": max(r["smax"] for r in use),
+                "samples": len(use), "samples_in_timed_region": len(inside),
+                "timed_region_s": round(self.t1 - self.t0, 4) if self.t0 and self.t1 else None,
+                "reasons": sorted(reasons)}
 
 
 # -------------------------------------------------------------------------- distributed
@@ -272,8 +301,9 @@ class DecodeToken:
         return g
 
 
-def time_graph(torch, graph, steps, warmup, world):
-    """ms per replay, CUDA events on the replay stream, barrier + sync on both sides."""
+def time_graph(torch, graph, steps, warmup, world, clk=None):
+    """ms per replay, CUDA events on the replay stream, barrier + sync on both sides (the
+    clock sampler, if given, is told when the timed region starts and ends)."""
     stream = torch.cuda.Stream()
     with torch.cuda.stream(stream):
         for _ in range(warmup):
@@ -282,12 +312,16 @@ def time_graph(torch, graph, steps, warmup, world):
     barrier(world)
     torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if clk is not None:
+        clk.mark_start()
     with torch.cuda.stream(stream):
         start.record(stream)
         for _ in range(steps):
             graph.replay()
         end.record(stream)
     torch.cuda.synchronize()
+    if clk is not None:
+        clk.mark_end()
     barrier(world)
     return start.elapsed_time(end) / steps
 
@@ -480,7 +514,10 @@ def run_reference(args, world, rank):
         return 0
     for _ in range(args.warmup):
         cpu_baseline(min_seconds=0.0)
-    vals = [cpu_baseline(min_seconds=1.0) for _ in range(args.steps)]
+    # Each step repeats the bounded sample for at least 1 s, or less when there are many
+    # steps, so that the whole arm takes about a minute of host time.
+    per_step = min(1.0, 60.0 / max(1, args.steps))
+    vals = [cpu_baseline(min_seconds=per_step) for _ in range(args.steps)]
     gbs = statistics.median(v["value"] for v in vals)
     line = {"impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
@@ -601,7 +638,7 @@ def profile(spec):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -636,7 +673,7 @@ def main():
     token = DecodeToken(h, "1b", "cuda", grouped=not args.no_group)
     graph = token.capture()
     with ClockSampler(local) as clk:
-        ms = time_graph(torch, graph, args.steps, args.warmup, world)
+        ms = time_graph(torch, graph, args.steps, args.warmup, world, clk)
     clocks = clk.summary()
     ms_max = max_over_ranks(ms, world, device="cuda")
     total_bytes = token.bytes * world
