@@ -72,6 +72,7 @@ struct MrArgs {
     int sc_rows;
     int parts, tpp, items;
     int64_t wait_ns;
+    int skip_copies;  // test hook: the producer issues nothing, so the consumers' waits run out
 };
 
 // A CTA's walk over its work items (row block, part of K), as in the M = 1 GEMV.
@@ -134,7 +135,7 @@ __global__ void __launch_bounds__(kMrThreads, 2)
 
     if (warp == kMrCWarps) {
         // ---------------------------------------------------------------- TMA producer
-        if (lane == 0) {
+        if (lane == 0 && !a.skip_copies) {
             prefetch_tensormap(&maps.w);
             prefetch_tensormap(&maps.s);
             prefetch_tensormap(&maps.x);
@@ -409,6 +410,7 @@ cudaError_t gemv_mr_launch(const Problem& p, const LaunchCtx& c) {
     a.kstages = kstages;
     a.sc_rows = p.scale_f16 ? kMrScRows16 : kMrScRows32;
     a.wait_ns = c.wait_limit_ns;
+    a.skip_copies = c.tc_skip_first_copy;
     // Group row of stage ks: ks * 512 / gs (gs <= 512: a shift), ks / (gs / 512), or 0.
     int gps = 1;
     a.gs_in_stage = 0;

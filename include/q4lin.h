@@ -81,18 +81,20 @@ typedef enum {
      * order, "Add linear_qcs4w op", Constraints (2)). */
     Q4LIN_OPT_NIBBLE_EVEN_HIGH = 2,
     /* Time limit, in nanoseconds of the GPU's global timer, of every bounded
-     * device-side wait (mbarrier polls) of the tensor-core kernel; <= 0 restores the
-     * default (2 s).  When a wait runs out the kernel records code 1 in the handle's
-     * status word, stops issuing work, lets its own copies and MMAs in flight finish,
-     * frees its tensor memory and returns; its output is then undefined. */
+     * device-side wait (mbarrier polls) of the TMA-fed kernels (decode and multi-row
+     * GEMV, tensor-core GEMM, input gradient); <= 0 restores the default (2 s).  When a
+     * wait runs out the kernel records code 1 in the handle's status word, stops issuing
+     * work, lets its own copies (and MMAs) in flight finish, frees its tensor memory and
+     * returns; its output is then undefined. */
     Q4LIN_OPT_WAIT_LIMIT = 3,
     /* 1: launch with programmatic dependent launch, so a kernel may start streaming
      * its weights while the previous kernel on the stream drains (default 0).  The
      * preceding kernel must not write this call's qweight or scales. */
     Q4LIN_OPT_PDL = 4,
     /* Test hook, default 0.  1: the tensor-core kernel's copy engine skips the first
-     * pipeline stage, so the barrier its consumers wait on is never completed and their
-     * bounded waits run out (exercises the timeout path without faulting the GPU). */
+     * pipeline stage, and the multi-row GEMV's copy engine issues nothing, so the barrier
+     * their consumers wait on is never completed and their bounded waits run out
+     * (exercises the timeout path without faulting the GPU). */
     Q4LIN_OPT_TC_SKIP_FIRST_COPY = 5
 } q4lin_option_t;
 
