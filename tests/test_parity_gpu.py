@@ -455,8 +455,9 @@ def test_split_k_parity_and_determinism(handle, N, K, gs):
 # Shapes that take the multi-row TMA GEMV: at least 10 M weights, K % 32 == 0, K >= 512,
 # N >= 16, a scale row of whole 16-byte units (N % 8 for fp16 scales, N % 4 for fp32), a
 # power-of-two group size (or one group per row).  Covered: ragged N (not a multiple of the
-# 64-row block), a K tail shorter than a 512-k stage, groups wider than a stage, per-channel
-# scales, the smallest N with a K long enough for the 8-part split, fp32 and fp16 scales.
+# 64-row block), a K tail shorter than a 512-k stage, groups of 32..512 k inside a stage
+# and wider than a stage, per-channel scales (fp16 and fp32), the smallest N with a K long
+# enough for the 8-part split, fp32 and fp16 scales.
 MR_SHAPES = [
     # N, K, gs, f16, bias
     (8192, 2048, 32, True, True),
@@ -466,6 +467,9 @@ MR_SHAPES = [
     (168, 65536, 65536, True, True),
     (24, 524288, 524288, True, False),
     (2600, 4096, 64, False, True),
+    (5120, 2048, 256, True, False),
+    (5120, 2048, 512, False, False),
+    (10000, 1024, 1024, False, True),
 ]
 
 
