@@ -11,7 +11,8 @@ a CUDA graph and replayed; steps are timed with CUDA events on the replay stream
 Printed: one JSON line with the aggregate GB/s, ms/token, the roofline of the GEMV kernel,
 an end-to-end figure through the public C API with host copies, clocks sampled during the
 timed region, the oracle timed on the host cores (rank 0, N = 1), and extra measurements
-(8B decode token, per-shape GEMV bandwidth, prefill TFLOP/s).
+(8B decode token, per-shape GEMV bandwidth, 2- and 4-row GEMVs, prefill TFLOP/s, the
+training-path kernels).
 
 N > 1 (torchrun): replicas only -- each rank runs the same token on its own GPU with no
 collective on the data path; a barrier brackets the timed region and the slowest rank's
