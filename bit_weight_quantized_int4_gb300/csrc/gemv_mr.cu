@@ -18,8 +18,8 @@
 // word by word (8 k, in a lane-rotated order that keeps the warp's code reads on 32
 // banks): it loads the x values of the MR rows once, widens each row's word once (byte
 // permute + packed add, as in the M = 1 GEMV) and issues MR packed FMAs per pair of
-// codes; the group scale multiplies each widened pair (MR = 4) or the stage's unscaled
-// sums (MR = 2, which has the registers for them).  So x is read from shared memory once
+// codes (MR = M, 2..4); the group scale multiplies each widened pair (MR = 4) or the
+// stage's unscaled sums (MR = 2, 3, which have the registers for them).  So x is read from shared memory once
 // per 4 rows and each code is widened once for all MR rows.  The 16 chunk lanes of a row
 // group are added with shuffles; lane j then holds all (m, row) sums and stores sum
 // (j / 4, j % 4).  When the row blocks alone leave SMs idle,
@@ -202,10 +202,11 @@ __global__ void __launch_bounds__(kMrThreads, 2)
     const uint32_t x_off = (uint32_t)j * 128;
     const uint32_t w_off = kXBytes + (uint32_t)(rg * kMrV) * 256 + (uint32_t)j * 16;
     const uint32_t s_off = kXBytes + kMrCodeBytes + ((uint32_t)gl * a.sc_rows + rg * kMrV) * esz;
-    // With 2 rows of x, the products of a stage are summed unscaled and the group scale is
-    // applied once per stage (acc.x); with 4 rows that would not fit the registers, and
-    // each widened pair is scaled before its 4 FMAs (acc = even-k and odd-k sums).
-    constexpr bool kDefer = MR <= 2;
+    // With 2 or 3 rows of x, the products of a stage are summed unscaled and the group
+    // scale is applied once per stage (acc.x); with 4 rows that would not fit the
+    // registers, and each widened pair is scaled before its 4 FMAs (acc = even-k and odd-k
+    // sums).
+    constexpr bool kDefer = MR <= 3;
     float2 acc[MR][kMrV];
 #pragma unroll
     for (int m = 0; m < MR; ++m)
@@ -392,7 +393,7 @@ bool gemv_mr_eligible(const Problem& p) {
 
 cudaError_t gemv_mr_launch(const Problem& p, const LaunchCtx& c) {
     EncodeTiledFn enc = tensor_map_encoder();
-    const int MR = p.M <= 2 ? 2 : 4;
+    const int MR = (int)p.M;  // 2, 3 or 4 rows of x per stage
     const bool one_group = p.group_size >= p.K;
     const uint32_t esz = p.scale_f16 ? 2 : 4;
     const int kstages = (int)((p.K + kMrStageK - 1) / kMrStageK);
@@ -481,6 +482,12 @@ cudaError_t gemv_mr_launch(const Problem& p, const LaunchCtx& c) {
                            : launch_mr<2, true, false>(maps, a, grid, smem, c);
         return f16 ? launch_mr<2, false, true>(maps, a, grid, smem, c)
                    : launch_mr<2, false, false>(maps, a, grid, smem, c);
+    }
+    if (MR == 3) {
+        if (eh) return f16 ? launch_mr<3, true, true>(maps, a, grid, smem, c)
+                           : launch_mr<3, true, false>(maps, a, grid, smem, c);
+        return f16 ? launch_mr<3, false, true>(maps, a, grid, smem, c)
+                   : launch_mr<3, false, false>(maps, a, grid, smem, c);
     }
     if (eh) return f16 ? launch_mr<4, true, true>(maps, a, grid, smem, c)
                        : launch_mr<4, true, false>(maps, a, grid, smem, c);
