@@ -18,8 +18,7 @@
 // word by word (8 k, in a lane-rotated order that keeps the warp's code reads on 32
 // banks): it loads the x values of the MR rows once, widens each row's word once (byte
 // permute + packed add, as in the M = 1 GEMV) and issues MR packed FMAs per pair of
-// codes (MR = M, 2..4); the group scale multiplies each widened pair (MR = 4) or the
-// stage's unscaled sums (MR = 2, 3, which have the registers for them).  So x is read from shared memory once
+// codes (MR = M, 2..4); the group scale multiplies the stage's unscaled sums once.  So x is read from shared memory once
 // per 4 rows and each code is widened once for all MR rows.  The 16 chunk lanes of a row
 // group are added with shuffles; lane j then holds all (m, row) sums and stores sum
 // (j / 4, j % 4).  When the row blocks alone leave SMs idle,
@@ -202,11 +201,8 @@ __global__ void __launch_bounds__(kMrThreads, 2)
     const uint32_t x_off = (uint32_t)j * 128;
     const uint32_t w_off = kXBytes + (uint32_t)(rg * kMrV) * 256 + (uint32_t)j * 16;
     const uint32_t s_off = kXBytes + kMrCodeBytes + ((uint32_t)gl * a.sc_rows + rg * kMrV) * esz;
-    // With 2 or 3 rows of x, the products of a stage are summed unscaled and the group
-    // scale is applied once per stage (acc.x); with 4 rows that would not fit the
-    // registers, and each widened pair is scaled before its 4 FMAs (acc = even-k and odd-k
-    // sums).
-    constexpr bool kDefer = MR <= 3;
+    // The products of a stage are summed unscaled over the thread's 32 k (one group: part,
+    // even-k and odd-k sums) and the group scale is applied once per stage (acc.x).
     float2 acc[MR][kMrV];
 #pragma unroll
     for (int m = 0; m < MR; ++m)
@@ -240,13 +236,11 @@ __global__ void __launch_bounds__(kMrThreads, 2)
                 const float4 f = *reinterpret_cast<const float4*>(st + s_off);
                 sc[0] = f.x, sc[1] = f.y, sc[2] = f.z, sc[3] = f.w;
             }
-            float2 part[kDefer ? MR : 1][kDefer ? kMrV : 1];
-            if (kDefer) {
+            float2 part[MR][kMrV];
 #pragma unroll
-                for (int m = 0; m < MR; ++m)
+            for (int m = 0; m < MR; ++m)
 #pragma unroll
-                    for (int v = 0; v < kMrV; ++v) part[kDefer ? m : 0][kDefer ? v : 0] = make_float2(0.f, 0.f);
-            }
+                for (int v = 0; v < kMrV; ++v) part[m][v] = make_float2(0.f, 0.f);
 #pragma unroll
             for (int w = 0; w < 4; ++w) {
                 // Word we of each of the 4 rows: k = 32 j + 8 we + (0..7).
@@ -280,27 +274,19 @@ __global__ void __launch_bounds__(kMrThreads, 2)
                             c[b] = fadd2(make_float2(__uint_as_float(prmt(lo[v], 0x4B000000u, sel)),
                                                      __uint_as_float(prmt(hi[v], 0x4B000000u, sel))),
                                          make_float2(-8388616.0f, -8388616.0f));
-                            if (!kDefer) c[b] = fmul2(c[b], make_float2(sc[v], sc[v]));
                         }
 #pragma unroll
                         for (int m = 0; m < MR; ++m)
 #pragma unroll
-                            for (int b = 0; b < 2; ++b) {
-                                float2& dst = kDefer ? part[kDefer ? m : 0][kDefer ? v : 0] : acc[m][v];
-                                dst = ffma2(c[b], xv[m][b], dst);
-                            }
+                            for (int b = 0; b < 2; ++b) part[m][v] = ffma2(c[b], xv[m][b], part[m][v]);
                     }
                 }
             }
-            if (kDefer) {
 #pragma unroll
-                for (int m = 0; m < MR; ++m)
+            for (int m = 0; m < MR; ++m)
 #pragma unroll
-                    for (int v = 0; v < kMrV; ++v) {
-                        const float2 pv = part[kDefer ? m : 0][kDefer ? v : 0];
-                        acc[m][v].x = fmaf(sc[v], pv.x + pv.y, acc[m][v].x);
-                    }
-            }
+                for (int v = 0; v < kMrV; ++v)
+                    acc[m][v].x = fmaf(sc[v], part[m][v].x + part[m][v].y, acc[m][v].x);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(empty(s));
