@@ -11,7 +11,7 @@ a CUDA graph and replayed; steps are timed with CUDA events on the replay stream
 Printed: one JSON line with the aggregate GB/s, ms/token, the roofline of the GEMV kernel,
 an end-to-end figure through the public C API with host copies, clocks sampled during the
 timed region, the oracle timed on the host cores (rank 0, N = 1), and extra measurements
-(8B decode token, per-shape GEMV bandwidth, 2- and 4-row GEMVs, prefill TFLOP/s, the
+(8B decode token, per-shape GEMV bandwidth, 2- to 4-row GEMVs, prefill TFLOP/s, the
 training-path kernels).
 
 N > 1 (torchrun): replicas only -- each rank runs the same token on its own GPU with no
@@ -703,7 +703,7 @@ def main():
                 shapes.append(shape_bandwidth(torch, h, N, K))
         extra["gemv_shapes"] = shapes
         # A few activation rows (speculative decoding, small batches): the multi-row GEMV.
-        extra["small_m"] = [shape_bandwidth(torch, h, N, K, M) for M in (2, 4)
+        extra["small_m"] = [shape_bandwidth(torch, h, N, K, M) for M in (2, 3, 4)
                             for N, K in ((8192, 2048), (2048, 8192), (128256, 2048))]
         extra["prefill"] = [prefill_tflops(torch, h, M, N, K)
                             for M in (128, 512, 2048) for N, K in PREFILL_NK]
