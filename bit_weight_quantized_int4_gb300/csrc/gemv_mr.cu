@@ -40,11 +40,14 @@ using namespace ptx;
 constexpr int kMrCWarps = 8;                          // consumer warps
 constexpr int kMrCThreads = 32 * kMrCWarps;
 constexpr int kMrThreads = kMrCThreads + 32;          // + the producer warp
-constexpr int kMrV = 4;                               // weight rows per consumer thread
-constexpr int kMrRows = 16 * kMrV;                    // rows per block: 16 row groups
+// V weight rows per consumer thread (4, or 2 when that saves a split of K): a block is
+// 16 row groups of V rows.
+__host__ __device__ constexpr int mr_rows(int V) { return 16 * V; }
 constexpr int kMrStageK = 512;                        // k per stage: 16 chunks of 32
-constexpr uint32_t kMrCodeBytes = kMrRows * kMrStageK / 2;  // 16 KiB
-constexpr int kMrScRows16 = kMrRows + 8, kMrScRows32 = kMrRows + 4;
+__host__ __device__ constexpr uint32_t mr_code_bytes(int V) { return mr_rows(V) * kMrStageK / 2; }
+// Staged scale rows per group: the block's rows plus padding that spreads the 16 chunk
+// lanes' group rows over the banks (a whole number of 16-byte units).
+__host__ __device__ constexpr int mr_sc_rows(int V, bool f16) { return mr_rows(V) + (f16 ? 8 : 4); }
 constexpr uint32_t kMrScBytes = 4608;                 // >= 16 groups x 68 rows x 4 B
 constexpr int kMrMaxStages = 8;
 constexpr int kMrSmem = 113 * 1024;                   // two CTAs per SM
@@ -105,7 +108,7 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
-template <int MR, bool EH, bool F16>
+template <int MR, int V, bool EH, bool F16>
 __global__ void __launch_bounds__(kMrThreads, 2)
     gemv_mr_kernel(const __grid_constant__ MrMaps maps, const MrArgs a) {
     extern __shared__ uint8_t smem_raw[];
@@ -120,6 +123,8 @@ __global__ void __launch_bounds__(kMrThreads, 2)
     auto full = [&](int s) { return bar_base + 8u * s; };
     auto empty = [&](int s) { return bar_base + 8u * (kMrMaxStages + s); };
     constexpr uint32_t kXBytes = (uint32_t)MR * 2048;  // x tile, then codes, then scales
+    constexpr int kRows = mr_rows(V);
+    constexpr uint32_t kCodeBytes = mr_code_bytes(V);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -148,11 +153,11 @@ __global__ void __launch_bounds__(kMrThreads, 2)
             int pre_ks[kMrMaxStages];
             while (cur.valid(a) && t < S) {
                 const uint32_t sb = base + (uint32_t)t * a.stage_bytes;
-                const int row0 = cur.blk * kMrRows;
+                const int row0 = cur.blk * kRows;
                 const int grow = a.gs_in_stage ? (cur.ks << a.gshift) : cur.ks / a.stages_per_group;
                 mbar_arrive_expect_tx(full(t), a.tx);
                 tma_load_2d(sb + kXBytes, &maps.w, cur.ks * (kMrStageK / 2), row0, full(t));
-                tma_load_2d(sb + kXBytes + kMrCodeBytes, &maps.s, row0, grow, full(t));
+                tma_load_2d(sb + kXBytes + kCodeBytes, &maps.s, row0, grow, full(t));
                 pre_ks[t] = cur.ks;
                 ++t;
                 cur.advance(a);
@@ -170,11 +175,11 @@ __global__ void __launch_bounds__(kMrThreads, 2)
                 }
                 if (*failed) break;
                 const uint32_t sb = base + (uint32_t)s * a.stage_bytes;
-                const int row0 = cur.blk * kMrRows;
+                const int row0 = cur.blk * kRows;
                 const int grow = a.gs_in_stage ? (cur.ks << a.gshift) : cur.ks / a.stages_per_group;
                 mbar_arrive_expect_tx(full(s), a.tx);
                 tma_load_2d(sb + kXBytes, &maps.w, cur.ks * (kMrStageK / 2), row0, full(s));
-                tma_load_2d(sb + kXBytes + kMrCodeBytes, &maps.s, row0, grow, full(s));
+                tma_load_2d(sb + kXBytes + kCodeBytes, &maps.s, row0, grow, full(s));
                 tma_load_3d(sb, &maps.x, 0, cur.ks * (kMrStageK / 32), 0, full(s));
                 ++t;
                 if (++s == S) s = 0, ph ^= 1u;
@@ -199,15 +204,15 @@ __global__ void __launch_bounds__(kMrThreads, 2)
     // m * 2048 + j * 128 + ((u ^ (j & 7)) << 4); the thread's code chunk of row v at
     // v * 256; its 4 consecutive scales of group row gl.
     const uint32_t x_off = (uint32_t)j * 128;
-    const uint32_t w_off = kXBytes + (uint32_t)(rg * kMrV) * 256 + (uint32_t)j * 16;
-    const uint32_t s_off = kXBytes + kMrCodeBytes + ((uint32_t)gl * a.sc_rows + rg * kMrV) * esz;
+    const uint32_t w_off = kXBytes + (uint32_t)(rg * V) * 256 + (uint32_t)j * 16;
+    const uint32_t s_off = kXBytes + kCodeBytes + ((uint32_t)gl * a.sc_rows + rg * V) * esz;
     // The products of a stage are summed unscaled over the thread's 32 k (one group: part,
     // even-k and odd-k sums) and the group scale is applied once per stage (acc.x).
-    float2 acc[MR][kMrV];
+    float2 acc[MR][V];
 #pragma unroll
     for (int m = 0; m < MR; ++m)
 #pragma unroll
-        for (int v = 0; v < kMrV; ++v) acc[m][v] = make_float2(0.f, 0.f);
+        for (int v = 0; v < V; ++v) acc[m][v] = make_float2(0.f, 0.f);
     int s = 0;
     uint32_t ph = 0;
     bool dead = false;
@@ -226,28 +231,35 @@ __global__ void __launch_bounds__(kMrThreads, 2)
             const uint8_t* st = gbase + (size_t)s * a.stage_bytes;
             const uint8_t* xs = st + x_off;
             const uint8_t* cs = st + w_off;
-            float sc[kMrV];
-            if (F16) {
-                const uint2 hv = *reinterpret_cast<const uint2*>(st + s_off);
-                const float2 p = __half22float2(*reinterpret_cast<const __half2*>(&hv.x));
-                const float2 q = __half22float2(*reinterpret_cast<const __half2*>(&hv.y));
-                sc[0] = p.x, sc[1] = p.y, sc[2] = q.x, sc[3] = q.y;
+            float sc[V];  // the V rows' scales of the thread's group row
+            if constexpr (V == 4) {
+                if (F16) {
+                    const uint2 hv = *reinterpret_cast<const uint2*>(st + s_off);
+                    const float2 p = __half22float2(*reinterpret_cast<const __half2*>(&hv.x));
+                    const float2 q = __half22float2(*reinterpret_cast<const __half2*>(&hv.y));
+                    sc[0] = p.x, sc[1] = p.y, sc[2] = q.x, sc[3] = q.y;
+                } else {
+                    const float4 f = *reinterpret_cast<const float4*>(st + s_off);
+                    sc[0] = f.x, sc[1] = f.y, sc[2] = f.z, sc[3] = f.w;
+                }
             } else {
-                const float4 f = *reinterpret_cast<const float4*>(st + s_off);
-                sc[0] = f.x, sc[1] = f.y, sc[2] = f.z, sc[3] = f.w;
+                static_assert(V == 2, "4 or 2 rows per thread");
+                const float2 f = F16 ? __half22float2(*reinterpret_cast<const __half2*>(st + s_off))
+                                     : *reinterpret_cast<const float2*>(st + s_off);
+                sc[0] = f.x, sc[1] = f.y;
             }
-            float2 part[MR][kMrV];
+            float2 part[MR][V];
 #pragma unroll
             for (int m = 0; m < MR; ++m)
 #pragma unroll
-                for (int v = 0; v < kMrV; ++v) part[m][v] = make_float2(0.f, 0.f);
+                for (int v = 0; v < V; ++v) part[m][v] = make_float2(0.f, 0.f);
 #pragma unroll
             for (int w = 0; w < 4; ++w) {
                 // Word we of each of the 4 rows: k = 32 j + 8 we + (0..7).
                 const int we = (w + rot) & 3;
-                uint32_t lo[kMrV], hi[kMrV];
+                uint32_t lo[V], hi[V];
 #pragma unroll
-                for (int v = 0; v < kMrV; ++v) {
+                for (int v = 0; v < V; ++v) {
                     const uint32_t word = *reinterpret_cast<const uint32_t*>(cs + v * 256 + we * 4);
                     const uint32_t m4 = word & 0x0F0F0F0Fu, s4 = (word >> 4) & 0x0F0F0F0Fu;
                     lo[v] = EH ? s4 : m4;
@@ -265,7 +277,7 @@ __global__ void __launch_bounds__(kMrThreads, 2)
                         xv[m][1] = make_float2(p.z, p.w);
                     }
 #pragma unroll
-                    for (int v = 0; v < kMrV; ++v) {
+                    for (int v = 0; v < V; ++v) {
                         // Pairs (k even, k odd) of bytes 2h and 2h + 1 as exact c - 8.
                         float2 c[2];
 #pragma unroll
@@ -285,7 +297,7 @@ __global__ void __launch_bounds__(kMrThreads, 2)
 #pragma unroll
             for (int m = 0; m < MR; ++m)
 #pragma unroll
-                for (int v = 0; v < kMrV; ++v)
+                for (int v = 0; v < V; ++v)
                     acc[m][v].x = fmaf(sc[v], part[m][v].x + part[m][v].y, acc[m][v].x);
         }
         __syncwarp();
@@ -299,15 +311,15 @@ __global__ void __launch_bounds__(kMrThreads, 2)
 #pragma unroll
             for (int m = 0; m < MR; ++m)
 #pragma unroll
-                for (int v = 0; v < kMrV; ++v) {
+                for (int v = 0; v < V; ++v) {
                     float t = acc[m][v].x + acc[m][v].y;
 #pragma unroll
                     for (int o = 1; o < 16; o <<= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-                    if (j == m * kMrV + v) mine = t;
+                    if (j == m * V + v) mine = t;
                     acc[m][v] = make_float2(0.f, 0.f);
                 }
-            const int mj = j / kMrV, vj = j % kMrV;
-            const int64_t nrow = (int64_t)blk * kMrRows + rg * kMrV + vj;  // row of the matrix
+            const int mj = j / V, vj = j % V;
+            const int64_t nrow = (int64_t)blk * kRows + rg * V + vj;  // row of the matrix
             const bool mine_ok = mj < MR;
             griddep_wait();  // (long complete: the x copies waited for it) before any store
             bool finish = true;
@@ -336,10 +348,10 @@ __global__ void __launch_bounds__(kMrThreads, 2)
     }
 }
 
-template <int MR, bool EH, bool F16>
+template <int MR, int V, bool EH, bool F16>
 cudaError_t launch_mr(const MrMaps& maps, const MrArgs& a, unsigned grid, int smem,
                       const LaunchCtx& c) {
-    const cudaError_t attr = kernel_smem_once<gemv_mr_kernel<MR, EH, F16>>(kMrSmem);
+    const cudaError_t attr = kernel_smem_once<gemv_mr_kernel<MR, V, EH, F16>>(kMrSmem);
     if (attr != cudaSuccess) return attr;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
@@ -353,7 +365,28 @@ cudaError_t launch_mr(const MrMaps& maps, const MrArgs& a, unsigned grid, int sm
         cfg.attrs = attrs;
         cfg.numAttrs = 1;
     }
-    return cudaLaunchKernelEx(&cfg, gemv_mr_kernel<MR, EH, F16>, maps, a);
+    return cudaLaunchKernelEx(&cfg, gemv_mr_kernel<MR, V, EH, F16>, maps, a);
+}
+
+template <int MR, int V>
+cudaError_t launch_mr_v(bool eh, bool f16, const MrMaps& maps, const MrArgs& a, unsigned grid,
+                        int smem, const LaunchCtx& c) {
+    if (eh) return f16 ? launch_mr<MR, V, true, true>(maps, a, grid, smem, c)
+                       : launch_mr<MR, V, true, false>(maps, a, grid, smem, c);
+    return f16 ? launch_mr<MR, V, false, true>(maps, a, grid, smem, c)
+               : launch_mr<MR, V, false, false>(maps, a, grid, smem, c);
+}
+
+// Parts of K per row block: split while the row blocks alone fill less than one wave of
+// two CTAs per SM (at least two stages a part, within the workspace and ticket capacity).
+int mr_parts(int64_t blocks, int kstages, int MR, int64_t ws_rows, const LaunchCtx& c) {
+    const int64_t slots = 2LL * c.sm_count;
+    int parts = 1;
+    while (parts < 8 && blocks * parts * 2 <= slots && kstages / (parts * 2) >= 2 && c.ws &&
+           c.tickets && blocks <= c.ticket_count &&
+           (int64_t)(parts * 2) * MR * ws_rows <= c.ws_floats)
+        parts *= 2;
+    return parts;
 }
 
 int log2_exact_mr(int64_t v) {
@@ -370,7 +403,7 @@ bool gemv_mr_eligible(const Problem& p) {
     if (p.M < 2 || p.M > 4 || p.K % 32 != 0 || p.K < kMrStageK || p.N < 16 ||
         (p.N * (p.scale_f16 ? 2 : 4)) % 16 != 0)
         return false;
-    if (p.N > (1LL << 31) - kMrRows || p.K > (1LL << 30)) return false;
+    if (p.N > (1LL << 31) - mr_rows(4) || p.K > (1LL << 30)) return false;
     if (!al16(p.x) || !al16(p.qweight) || !al16(p.scales)) return false;
     const int64_t gs = p.group_size;
     if (gs < p.K && !(gs % 32 == 0 && log2_exact_mr(gs) >= 0)) return false;
@@ -383,7 +416,18 @@ cudaError_t gemv_mr_launch(const Problem& p, const LaunchCtx& c) {
     const bool one_group = p.group_size >= p.K;
     const uint32_t esz = p.scale_f16 ? 2 : 4;
     const int kstages = (int)((p.K + kMrStageK - 1) / kMrStageK);
-    const int64_t blocks = (p.N + kMrRows - 1) / kMrRows;
+    // 4 rows per thread, or 2 when that gives enough row blocks to need no split of K
+    // while 4 would (measured: 8192 x 2048 at M = 2 / 4, 8.8 / 11.4 -> 7.2 / 9.8 us; where
+    // both split, or neither, 4 is as fast or faster).
+    int V = 4;
+    {
+        const int64_t b4 = (p.N + mr_rows(4) - 1) / mr_rows(4);
+        const int64_t b2 = (p.N + mr_rows(2) - 1) / mr_rows(2);
+        if (mr_parts(b4, kstages, MR, b4 * mr_rows(4), c) > 1 &&
+            mr_parts(b2, kstages, MR, b2 * mr_rows(2), c) == 1)
+            V = 2;
+    }
+    const int64_t blocks = (p.N + mr_rows(V) - 1) / mr_rows(V);
 
     MrArgs a = {};
     a.bias = p.bias;
@@ -393,9 +437,9 @@ cudaError_t gemv_mr_launch(const Problem& p, const LaunchCtx& c) {
     a.status = c.status_word;
     a.M = p.M;
     a.N = p.N;
-    a.ws_rows = blocks * kMrRows;
+    a.ws_rows = blocks * mr_rows(V);
     a.kstages = kstages;
-    a.sc_rows = p.scale_f16 ? kMrScRows16 : kMrScRows32;
+    a.sc_rows = mr_sc_rows(V, p.scale_f16 != 0);
     a.wait_ns = c.wait_limit_ns;
     a.skip_copies = c.tc_skip_first_copy;
     // Group row of stage ks: ks * 512 / gs (gs <= 512: a shift), ks / (gs / 512), or 0.
@@ -411,18 +455,12 @@ cudaError_t gemv_mr_launch(const Problem& p, const LaunchCtx& c) {
         a.stages_per_group = (int)(p.group_size / kMrStageK);
     }
     const int64_t G = one_group ? 1 : (p.K + p.group_size - 1) / p.group_size;
-    a.stage_bytes = (uint32_t)((MR * 2048 + kMrCodeBytes + kMrScBytes + 1023) / 1024 * 1024);
+    a.stage_bytes = (uint32_t)((MR * 2048 + mr_code_bytes(V) + kMrScBytes + 1023) / 1024 * 1024);
     a.stages = std::min<int>(kMrMaxStages, (kMrSmem - 1024 - 256) / (int)a.stage_bytes);
     if (a.stages < 2) return cudaErrorNotSupported;
-    a.tx = (uint32_t)MR * 2048 + kMrCodeBytes + (uint32_t)gps * a.sc_rows * esz;
-    // Split K when the row blocks alone fill less than one wave of two CTAs per SM (at
-    // least two stages a part, within the workspace and ticket capacity).
+    a.tx = (uint32_t)MR * 2048 + mr_code_bytes(V) + (uint32_t)gps * a.sc_rows * esz;
     const int64_t slots = 2LL * c.sm_count;
-    int parts = 1;
-    while (parts < 8 && blocks * parts * 2 <= slots && kstages / (parts * 2) >= 2 && c.ws &&
-           c.tickets && blocks <= c.ticket_count &&
-           (int64_t)(parts * 2) * MR * a.ws_rows <= c.ws_floats)
-        parts *= 2;
+    const int parts = mr_parts(blocks, kstages, MR, a.ws_rows, c);
     a.tpp = (kstages + parts - 1) / parts;
     a.parts = (kstages + a.tpp - 1) / a.tpp;
     if (blocks * a.parts > 0x7fffffff) return cudaErrorInvalidValue;
@@ -435,7 +473,7 @@ cudaError_t gemv_mr_launch(const Problem& p, const LaunchCtx& c) {
         const int64_t Kp = p.K / 2;
         const cuuint64_t dims[2] = {(cuuint64_t)Kp, (cuuint64_t)p.N};
         const cuuint64_t strides[1] = {(cuuint64_t)Kp};
-        const cuuint32_t box[2] = {(cuuint32_t)(kMrStageK / 2), (cuuint32_t)kMrRows};
+        const cuuint32_t box[2] = {(cuuint32_t)(kMrStageK / 2), (cuuint32_t)mr_rows(V)};
         if (enc(&maps.w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(p.qweight), dims,
                 strides, box, estr2, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
@@ -463,22 +501,12 @@ cudaError_t gemv_mr_launch(const Problem& p, const LaunchCtx& c) {
     }
     const unsigned grid = (unsigned)std::min<int64_t>(a.items, slots);
     const bool eh = p.even_high != 0, f16 = p.scale_f16 != 0;
-    if (MR == 2) {
-        if (eh) return f16 ? launch_mr<2, true, true>(maps, a, grid, smem, c)
-                           : launch_mr<2, true, false>(maps, a, grid, smem, c);
-        return f16 ? launch_mr<2, false, true>(maps, a, grid, smem, c)
-                   : launch_mr<2, false, false>(maps, a, grid, smem, c);
-    }
-    if (MR == 3) {
-        if (eh) return f16 ? launch_mr<3, true, true>(maps, a, grid, smem, c)
-                           : launch_mr<3, true, false>(maps, a, grid, smem, c);
-        return f16 ? launch_mr<3, false, true>(maps, a, grid, smem, c)
-                   : launch_mr<3, false, false>(maps, a, grid, smem, c);
-    }
-    if (eh) return f16 ? launch_mr<4, true, true>(maps, a, grid, smem, c)
-                       : launch_mr<4, true, false>(maps, a, grid, smem, c);
-    return f16 ? launch_mr<4, false, true>(maps, a, grid, smem, c)
-               : launch_mr<4, false, false>(maps, a, grid, smem, c);
+    if (MR == 2) return V == 2 ? launch_mr_v<2, 2>(eh, f16, maps, a, grid, smem, c)
+                               : launch_mr_v<2, 4>(eh, f16, maps, a, grid, smem, c);
+    if (MR == 3) return V == 2 ? launch_mr_v<3, 2>(eh, f16, maps, a, grid, smem, c)
+                               : launch_mr_v<3, 4>(eh, f16, maps, a, grid, smem, c);
+    return V == 2 ? launch_mr_v<4, 2>(eh, f16, maps, a, grid, smem, c)
+                  : launch_mr_v<4, 4>(eh, f16, maps, a, grid, smem, c);
 }
 
 }  // namespace q4lin

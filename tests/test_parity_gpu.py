@@ -452,7 +452,8 @@ def test_split_k_parity_and_determinism(handle, N, K, gs):
 
 
 # ------------------------------------------------------- TMA-fed GEMV, 2 <= M <= 4 rows
-# Shapes that take the multi-row TMA GEMV: at least 10 M weights, K % 32 == 0, K >= 512,
+# Shapes that take the multi-row TMA GEMV (4 weight rows per thread, or 2 when that avoids
+# splitting K: 8192 x 2048 and 5120 x 2048 here): at least 10 M weights, K % 32 == 0, K >= 512,
 # N >= 16, a scale row of whole 16-byte units (N % 8 for fp16 scales, N % 4 for fp32), a
 # power-of-two group size (or one group per row).  Covered: ragged N (not a multiple of the
 # 64-row block), a K tail shorter than a 512-k stage, groups of 32..512 k inside a stage
@@ -488,8 +489,11 @@ def test_multirow_gemv_lm_head(handle, M):
 
 
 @pytest.mark.parametrize("M", [2, 3, 4])
-def test_multirow_gemv_even_high(handle, M):
-    c = synth.make_case(M, 2568, 4096, 64, scale_f16=True, bias=True, seed=60 + M)
+@pytest.mark.parametrize("N,K", [(2568, 4096), (6144, 2048)])
+def test_multirow_gemv_even_high(handle, M, N, K):
+    """Even k in the high nibble, with 4 weight rows per thread and K split (2568 x 4096)
+    and with 2 rows per thread and no split (6144 x 2048)."""
+    c = synth.make_case(M, N, K, 64, scale_f16=True, bias=True, seed=60 + M + N)
     check_case(handle, c, GEMV, even_high=True)
 
 
