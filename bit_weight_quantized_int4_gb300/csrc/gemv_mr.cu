@@ -325,13 +325,20 @@ __global__ void __launch_bounds__(kMrThreads, 2)
             bool finish = true;
             if (a.parts > 1) {
                 if (mine_ok) a.ws[((int64_t)part * MR + mj) * a.ws_rows + nrow] = mine;
-                __threadfence();
+                // The consumers' partial sums are ordered before the ticket by the CTA
+                // barrier and one device-scope fence of the thread that takes the ticket
+                // (cumulative); the last item's reads are ordered after it by that thread's
+                // second fence and the barrier that follows.
                 asm volatile("bar.sync 1, %0;" ::"r"(kMrCThreads) : "memory");
-                if (threadIdx.x == 0) *s_ticket = atomicAdd(a.tickets + blk, 1);
+                if (threadIdx.x == 0) {
+                    __threadfence();
+                    const int t = atomicAdd(a.tickets + blk, 1);
+                    __threadfence();
+                    *s_ticket = t;
+                }
                 asm volatile("bar.sync 1, %0;" ::"r"(kMrCThreads) : "memory");
                 finish = *s_ticket == a.parts - 1;
                 if (finish) {
-                    __threadfence();
                     if (mine_ok) {
                         // Parts added in part order: the sum does not depend on which
                         // item finished last.
