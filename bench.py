@@ -40,7 +40,7 @@ L2_BYTES = 129 << 20
 # launch list (dram__bytes_read.sum + dram__bytes_write.sum per launch; the summary is
 # profiles/gemv_tma_token_1b_launches.md).  Valid only for the kernel source it was taken
 # with: the sha256 prefix of gemv_tma.cu + ptx.cuh; any other source reports null.
-TOKEN_TRAFFIC = {"bytes": 698272000, "launches": 65, "source_sha256": "6accd3e6b8e2c593"}
+TOKEN_TRAFFIC = {"bytes": 698246656, "launches": 65, "source_sha256": "0702c7c64ddbcf43"}
 
 
 def gemv_source_sha():

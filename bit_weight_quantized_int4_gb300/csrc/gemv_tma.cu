@@ -414,13 +414,19 @@ __global__ void __launch_bounds__(kThreadsG, 2)
             bool finish = true;
             if (a.parts > 1) {
                 if (j < V) a.ws[(int64_t)part * a.ws_rows + vrow] = mine;
-                __threadfence();
+                // The partial sums are ordered before the ticket by the CTA barrier and one
+                // device-scope fence of the thread that takes it (cumulative); the last
+                // item's reads after it by that thread's second fence and the next barrier.
                 asm volatile("bar.sync 1, %0;" ::"r"(kCThreads) : "memory");
-                if (threadIdx.x == 0) *s_ticket = atomicAdd(a.tickets + blk, 1);
+                if (threadIdx.x == 0) {
+                    __threadfence();
+                    const int t = atomicAdd(a.tickets + blk, 1);
+                    __threadfence();
+                    *s_ticket = t;
+                }
                 asm volatile("bar.sync 1, %0;" ::"r"(kCThreads) : "memory");
                 finish = *s_ticket == a.parts - 1;
                 if (finish) {
-                    __threadfence();
                     if (j < V) {
                         // All parts' loads in flight together (parts <= 8); added in order.
                         float t[8];

@@ -164,13 +164,17 @@ __global__ void __launch_bounds__(kBwThreads, 2) backward_dx_kernel(const BwArgs
     if (k < a.K)
         for (int m = 0; m < mt; ++m)
             a.ws[((int64_t)blockIdx.y * a.M + m0 + m) * a.K + k] = part[m];
-    __threadfence();
+    // Partials before the ticket: the CTA barrier and one device-scope fence of the thread
+    // that takes it; the last CTA's reads after it: that thread's second fence and barrier.
     __syncthreads();
     const int item = (int)(blockIdx.z * gridDim.x + blockIdx.x);
-    if (threadIdx.x == 0) s_last = atomicAdd(a.tickets + item, 1) == a.splits - 1;
+    if (threadIdx.x == 0) {
+        __threadfence();
+        s_last = atomicAdd(a.tickets + item, 1) == a.splits - 1;
+        __threadfence();
+    }
     __syncthreads();
     if (!s_last) return;
-    __threadfence();
     if (k < a.K)
         for (int m = 0; m < mt; ++m) {
             // Loads of 8 parts in flight at a time; still added in split order.
@@ -399,12 +403,16 @@ __global__ void __launch_bounds__(kBtThreads, 2)
     float* wsi = a.ws + item * (int64_t)a.splits * MT * kBtKT;
 #pragma unroll
     for (int m = 0; m < MT; ++m) wsi[((int64_t)blockIdx.y * MT + m) * kBtKT + c] = part[m];
-    __threadfence();
+    // Partials before the ticket: the barrier and one device-scope fence of the thread that
+    // takes it; the last CTA's reads after it: that thread's second fence and barrier.
     asm volatile("bar.sync 1, %0;" ::"r"(kBtCWarps * 32) : "memory");
-    if (threadIdx.x == 0) *s_last = atomicAdd(a.tickets + item, 1) == a.splits - 1;
+    if (threadIdx.x == 0) {
+        __threadfence();
+        *s_last = atomicAdd(a.tickets + item, 1) == a.splits - 1;
+        __threadfence();
+    }
     asm volatile("bar.sync 1, %0;" ::"r"(kBtCWarps * 32) : "memory");
     if (!*s_last) return;
-    __threadfence();
     // The MT rows of the column together, the loads of PB parts of all of them in flight
     // at a time (MT * PB <= 32); every row still added in split order.
     constexpr int PB = MT >= 8 ? 4 : 32 / MT > 8 ? 8 : 32 / MT;
