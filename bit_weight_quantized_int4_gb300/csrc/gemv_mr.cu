@@ -7,25 +7,27 @@
 // regime below the tensor-core crossover, where each dequantized weight is reused across
 // the M activation rows.)
 //
-// A producer warp streams per stage (512 k) the packed weights of a block of 64 rows
-// [64 x 256 B], their group scales [groups of the stage x 72 (fp16) / 68 (fp32) rows: the
-// padded row stride spreads the 16 chunk lanes' group rows over the banks] and the x tile
-// [MR rows x 512 k] (a 3D box of 128-byte chunk rows with the 128-byte swizzle, so that
-// the 16 chunk lanes reading the same offset of 16 chunks hit different banks) into a
-// ring, all on one mbarrier; the weight and scale copies of the first stages go out before
-// the grid-dependency wait, their x copies after it.  Consumer thread = (chunk lane j of
-// 16, row group of 4 rows): per stage it takes chunk j (32 k, one group) of its 4 rows,
-// word by word (8 k, in a lane-rotated order that keeps the warp's code reads on 32
-// banks): it loads the x values of the MR rows once, widens each row's word once (byte
-// permute + packed add, as in the M = 1 GEMV) and issues MR packed FMAs per pair of
-// codes (MR = M, 2..4); the group scale multiplies the stage's unscaled sums once.  So x is read from shared memory once
-// per 4 rows and each code is widened once for all MR rows.  The 16 chunk lanes of a row
-// group are added with shuffles; lane j then holds all (m, row) sums and stores sum
-// (j / 4, j % 4).  When the row blocks alone leave SMs idle,
-// K is cut into parts; the parts write partial sums to the handle's workspace and the
-// last item of a row block (an atomic ticket) adds them in part order (deterministic).
-// Every wait is bounded in time; after a timeout the warps walk their remaining items
-// without waiting or computing, so the barriers and tickets are still reached.
+// A producer warp streams per stage (512 k) the packed weights of a block of 16 V rows
+// [16 V x 256 B] (V = 4, or 2 when 32-row blocks avoid a split of K that 64-row blocks
+// need), their group scales [groups of the stage x (16 V + 8) fp16 / (16 V + 4) fp32 rows:
+// the padded row stride spreads the 16 chunk lanes' group rows over the banks] and the x
+// tile [MR rows x 512 k] (MR = M; a 3D box of 128-byte chunk rows with the 128-byte
+// swizzle, so that the 16 chunk lanes reading the same offset of 16 chunks hit different
+// banks) into a ring, all on one mbarrier; the weight and scale copies of the first
+// stages go out before the grid-dependency wait, their x copies after it.
+// Consumer thread = (chunk lane j of 16, row group of V rows): per stage it takes chunk j
+// (32 k, one group) of its V rows, word by word (8 k, in a lane-rotated order that keeps
+// the warp's code reads on 32 banks): it loads the x values of the MR rows once, widens
+// each row's word once (byte permute + packed add, as in the M = 1 GEMV) and issues MR
+// packed FMAs per pair of codes; the group scale multiplies the stage's unscaled sums
+// once.  So x is read from shared memory once per V rows and each code is widened once
+// for all MR rows.  The 16 chunk lanes of a row group are added with shuffles; lane j
+// then holds all (m, row) sums and stores sum (j / V, j % V).  When the row blocks alone
+// leave SMs idle, K is cut into parts; the parts write partial sums to the handle's
+// workspace and the last item of a row block (an atomic ticket) adds them in part order
+// (deterministic).  Every wait is bounded in time; after a timeout the warps walk their
+// remaining items without waiting or computing, so the barriers and tickets are still
+// reached.
 #include <cuda_fp16.h>
 
 #include <algorithm>
@@ -48,14 +50,14 @@ __host__ __device__ constexpr uint32_t mr_code_bytes(int V) { return mr_rows(V) 
 // Staged scale rows per group: the block's rows plus padding that spreads the 16 chunk
 // lanes' group rows over the banks (a whole number of 16-byte units).
 __host__ __device__ constexpr int mr_sc_rows(int V, bool f16) { return mr_rows(V) + (f16 ? 8 : 4); }
-constexpr uint32_t kMrScBytes = 4608;                 // >= 16 groups x 68 rows x 4 B
+constexpr uint32_t kMrScBytes = 4608;                 // >= 16 groups x 68 fp32 rows (V = 4)
 constexpr int kMrMaxStages = 8;
 constexpr int kMrSmem = 113 * 1024;                   // two CTAs per SM
 constexpr int64_t kMrDrainNs = 4000000000LL;
 
 struct MrMaps {
-    CUtensorMap w;  // uint8 [N, K/2], box {256, 64}
-    CUtensorMap s;  // scales [G, N], box {72 / 68, groups per stage}
+    CUtensorMap w;  // uint8 [N, K/2], box {256, 16 V}
+    CUtensorMap s;  // scales [G, N], box {16 V + 8 (fp16) / + 4 (fp32), groups per stage}
     CUtensorMap x;  // fp32 [M][K/32][32], box {32, 16, MR}, 128-byte swizzle
 };
 
