@@ -195,16 +195,16 @@ __global__ void __launch_bounds__(kMrThreads, 2)
 
     // ------------------------------------------------------------------ consumers
     const int j = threadIdx.x & 15;          // chunk lane: chunk j (32 k) of every stage
-    const int rg = threadIdx.x >> 4;         // row group: rows 4 rg .. 4 rg + 3 of a block
+    const int rg = threadIdx.x >> 4;         // row group: rows V rg .. V rg + V - 1 of a block
     const int gl = a.gs_in_stage ? (j * 32) / a.gs_in_stage : 0;  // group row in the stage
     // A thread takes the 4 words of its chunk in a rotated order, so that the 32 lanes of a
-    // warp (chunks j and j + 8 are 128 bytes apart, the two row groups 1 KiB apart) read
-    // 32 different banks.
+    // warp (chunks j and j + 8 are 128 bytes apart, the two row groups V x 256 bytes apart)
+    // read 32 different banks.
     const int rot = (j >> 3) + 2 * (rg & 1);
     constexpr uint32_t esz = F16 ? 2 : 4;
     // Per-thread offsets inside a stage: x chunk j of row m, 16-byte unit u at
     // m * 2048 + j * 128 + ((u ^ (j & 7)) << 4); the thread's code chunk of row v at
-    // v * 256; its 4 consecutive scales of group row gl.
+    // v * 256; its V consecutive scales of group row gl.
     const uint32_t x_off = (uint32_t)j * 128;
     const uint32_t w_off = kXBytes + (uint32_t)(rg * V) * 256 + (uint32_t)j * 16;
     const uint32_t s_off = kXBytes + kCodeBytes + ((uint32_t)gl * a.sc_rows + rg * V) * esz;
