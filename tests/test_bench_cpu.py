@@ -55,3 +55,39 @@ def test_clock_summary_without_nvidia_smi():
     import bench
     c = bench.ClockSampler(0)
     assert c.summary()["reasons"] == ["nvidia-smi unavailable"]
+
+
+def test_token_bytes_are_the_algorithmic_bytes():
+    """Bytes of one decode token, the numerator of the bench's GB/s and roofline: every
+    packed weight (N * K/2), fp16 group scale (K/32 * N * 2) and output (4N) once, and each
+    activation (4K) once per group of projections that read it (q/k/v, o, gate/up, down,
+    lm_head)."""
+    import bench
+
+    def matrix(N, K):
+        return N * (K // 2) + (K // 32) * N * 2 + 4 * N
+
+    for model, want in (("1b", 698053632), ("8b", 4230812672)):
+        m = bench.MODELS[model]
+        per_layer = sum(matrix(N, K) for _, N, K in m["layer"])
+        per_layer += sum(4 * K for name, _, K in m["layer"] if name in ("q", "o", "gate", "down"))
+        _, hN, hK = m["head"]
+        total = m["layers"] * per_layer + matrix(hN, hK) + 4 * hK
+        assert bench.token_bytes(model) == total == want
+
+
+def test_token_groups_share_x():
+    import bench
+    groups = bench.token_groups("1b")
+    assert len(groups) == 16 * 4 + 1
+    assert [n.rstrip("0123456789") for n, _, _ in groups[0]] == ["q", "k", "v"]
+    assert [n.rstrip("0123456789") for n, _, _ in groups[2]] == ["gate", "up"]
+    assert groups[-1] == [("lm_head", 128256, 2048)]
+
+
+def test_token_traffic_only_for_the_captured_launch_count():
+    import bench
+    t = bench.TOKEN_TRAFFIC
+    assert bench.token_traffic_per_launch(t["launches"] + 1) is None
+    if bench.gemv_source_sha() == t["source_sha256"]:
+        assert bench.token_traffic_per_launch(t["launches"]) == round(t["bytes"] / t["launches"])
