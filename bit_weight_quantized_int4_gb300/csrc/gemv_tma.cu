@@ -45,6 +45,8 @@ constexpr int kCWarps = 8;                 // consumer warps: 2 per SM sub-parti
 constexpr int kCThreads = 32 * kCWarps;
 constexpr int kThreadsG = kCThreads + 32;  // + the producer warp
 constexpr int kRowGroups = kCThreads / 16; // 16 chunk lanes per row group
+static_assert(kRowGroups == kGemvMinRowBlock && 4 * kRowGroups == kGemvMaxRowBlock,
+              "row blocks of 16 row groups x V rows, V in {1, 2, 4}");
 // Stage width: H chunk columns of 16 bytes per thread, i.e. 256 * H packed bytes (512 * H
 // k) per row per stage.  H = 2 for every tile height (measured: halving the stage of the
 // V = 4 tiles to fit a deeper ring made them slower, the per-stage overhead outweighs the
@@ -596,7 +598,7 @@ cudaError_t gemv_tma_launch_group(const Problem* ps, int count, const LaunchCtx&
         if (stages_for(v) < 2) continue;
         const int64_t blocks_v = blocks_for(v);
         const double eff = v == 1 ? 1.4 : (v == 2 ? 1.1 : 1.0);
-        for (int parts = 1; parts <= 8; parts *= 2) {
+        for (int parts = 1; parts <= kGemvMaxParts; parts *= 2) {
             const int kstages = kstages_for(v);
             if (parts > 1 && (kstages * 512 * chunk_cols(v) / parts < 2048 || !c.ws || !c.tickets ||
                               (int64_t)parts * blocks_v * kRowGroups * v > c.ws_floats ||

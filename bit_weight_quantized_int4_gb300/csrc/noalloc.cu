@@ -5,6 +5,7 @@
 // TMA-fed decode GEMV (M = 1), and its split-K scratch -- partial sums, per-row-block
 // counters and a status word -- lives in the file-scope array below, which every GPU
 // that loads the library holds until the process exits.
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -15,36 +16,84 @@
 
 namespace {
 
-// Largest N accepted: 16384 output rows, split into at most 8 parts along K.
+// Largest N accepted: 16384 output rows.  The GEMV's smallest row block is 16 rows, so at
+// most 1024 row blocks (one counter each); K is split into at most 8 parts, each holding
+// one partial sum per row of the row blocks (the last block may extend up to 63 rows past
+// N, for 64-row blocks).
 constexpr int64_t kMaxRows = 16384;
-constexpr int64_t kMaxParts = 8;
-constexpr int64_t kRowPad = 128;  // the last row block may extend past N
-constexpr int64_t kPartialFloats = kMaxParts * (kMaxRows + kRowPad);
-constexpr int64_t kTicketWords = 1024;  // >= row blocks of kMaxRows rows (32 rows each)
+constexpr int64_t kRowPad = 128;
+constexpr int64_t kPartialFloats = q4lin::kGemvMaxParts * (kMaxRows + kRowPad);
+constexpr int64_t kTicketWords = 1024;
 constexpr int64_t kStatusWords = 64;
 constexpr int64_t kScratchWords = kPartialFloats + kTicketWords + kStatusWords;  // ~537 KB
+static_assert(kTicketWords * q4lin::kGemvMinRowBlock >= kMaxRows,
+              "one counter per row block of the smallest height");
+static_assert(kRowPad >= q4lin::kGemvMaxRowBlock - 1,
+              "partial sums cover the rows of the last, partly filled row block");
 
 // The scratch.  In host code this name is a host-side stand-in, not a device address:
-// the address comes from cudaGetSymbolAddress once per device.
+// the address comes from cudaGetSymbolAddress (scratch_address below).
 static __device__ __align__(256) float g_scratch[kScratchWords];
 
 constexpr int kMaxDevices = 64;
-void* g_scratch_addr[kMaxDevices] = {};
+// Per device: the device address of g_scratch and the unique id of the CUDA context it
+// was looked up in.  A device reset destroys the context (and the module holding the
+// array); the next call sees a new context id and looks the address up again.
+struct ScratchSlot {
+    void* addr = nullptr;
+    unsigned long long ctx_id = 0;
+    bool have_id = false;
+};
+ScratchSlot g_slots[kMaxDevices];
 std::mutex g_setup_mutex;
 
-// Device address of g_scratch on the current device (looked up on first use).
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// Unique id of the calling thread's current context (false if there is none or the driver
+// does not provide the query).
+bool current_context_id(unsigned long long* id) {
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<CtxGetIdFn>(p);
+        cudaGetLastError();
+    });
+    CUcontext ctx = nullptr;
+    return get_current && get_id && get_current(&ctx) == CUDA_SUCCESS && ctx &&
+           get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// Device address of g_scratch on the current device `device`: looked up on the first call
+// there, and again whenever the device's context has changed since.
 q4lin_status_t scratch_address(int device, void** addr) {
     if (device < 0 || device >= kMaxDevices) return Q4LIN_ERR_NO_DEVICE;
     std::lock_guard<std::mutex> lock(g_setup_mutex);
-    if (!g_scratch_addr[device]) {
+    ScratchSlot& s = g_slots[device];
+    unsigned long long id = 0;
+    const bool have_id = current_context_id(&id);
+    if (!s.addr || !have_id || !s.have_id || s.ctx_id != id) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || !p) {
             cudaGetLastError();
+            s.addr = nullptr;
             return Q4LIN_ERR_CUDA;
         }
-        g_scratch_addr[device] = p;
+        s.addr = p;
+        s.have_id = current_context_id(&s.ctx_id);  // the lookup made the context current
     }
-    *addr = g_scratch_addr[device];
+    *addr = s.addr;
     return Q4LIN_OK;
 }
 

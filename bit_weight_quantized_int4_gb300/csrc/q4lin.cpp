@@ -175,6 +175,18 @@ q4lin_status_t plan(q4lin_handle_t h, const q4lin::Problem& p, const q4lin::Laun
     return Q4LIN_OK;
 }
 
+// The kernel behind a path for an M >= 1, N >= 1 problem (the dispatch of q4lin_run).
+int kernel_of(const q4lin::Problem& p, int path) {
+    switch (path) {
+        case Q4LIN_PATH_TC: return Q4LIN_KERNEL_TC;
+        case Q4LIN_PATH_GEMV:
+            return q4lin::gemv_tma_eligible(p) ? Q4LIN_KERNEL_GEMV_TMA
+                   : multirow_preferred(p)     ? Q4LIN_KERNEL_MULTIROW
+                                               : Q4LIN_KERNEL_ROWSTREAM;
+        default: return Q4LIN_KERNEL_GENERIC;
+    }
+}
+
 }  // namespace
 
 extern "C" {
@@ -248,6 +260,27 @@ q4lin_status_t q4lin_plan(q4lin_handle_t h, const float* x, const uint8_t* qweig
     return plan(h, p, make_ctx(h, nullptr), path_out);
 }
 
+q4lin_status_t q4lin_plan_kernel(q4lin_handle_t h, const float* x, const uint8_t* qweight,
+                                 const void* scales, const float* bias, const float* out,
+                                 int64_t M, int64_t N, int64_t K, int64_t group_size,
+                                 int scale_dtype, int* kernel_out) {
+    if (!kernel_out) return Q4LIN_ERR_INVALID_ARG;
+    q4lin::Problem p;
+    bool empty = false;
+    q4lin_status_t st = validate(h, x, qweight, scales, bias, out, M, N, K, group_size,
+                                 scale_dtype, &p, &empty);
+    if (st != Q4LIN_OK) return st;
+    if (empty) {
+        *kernel_out = Q4LIN_KERNEL_NONE;
+        return Q4LIN_OK;
+    }
+    int path = 0;
+    st = plan(h, p, make_ctx(h, nullptr), &path);
+    if (st != Q4LIN_OK) return st;
+    *kernel_out = kernel_of(p, path);
+    return Q4LIN_OK;
+}
+
 q4lin_status_t q4lin_run(q4lin_handle_t h, const float* x, const uint8_t* qweight,
                          const void* scales, const float* bias, float* out, int64_t M,
                          int64_t N, int64_t K, int64_t group_size, int scale_dtype,
@@ -264,13 +297,11 @@ q4lin_status_t q4lin_run(q4lin_handle_t h, const float* x, const uint8_t* qweigh
     DeviceGuard g(h->device);
     if (!g.ok()) return Q4LIN_ERR_CUDA;
     cudaError_t err;
-    switch (path) {
-        case Q4LIN_PATH_TC: err = q4lin::tc_launch(p, c); break;
-        case Q4LIN_PATH_GEMV:
-            err = q4lin::gemv_tma_eligible(p) ? q4lin::gemv_tma_launch(p, c)
-                  : multirow_preferred(p)       ? q4lin::gemv_mr_launch(p, c)
-                                                : q4lin::rowstream_launch(p, c);
-            break;
+    switch (kernel_of(p, path)) {
+        case Q4LIN_KERNEL_TC: err = q4lin::tc_launch(p, c); break;
+        case Q4LIN_KERNEL_GEMV_TMA: err = q4lin::gemv_tma_launch(p, c); break;
+        case Q4LIN_KERNEL_MULTIROW: err = q4lin::gemv_mr_launch(p, c); break;
+        case Q4LIN_KERNEL_ROWSTREAM: err = q4lin::rowstream_launch(p, c); break;
         default: err = q4lin::generic_launch(p, c); break;
     }
     if (err == cudaSuccess) err = cudaGetLastError();

@@ -70,6 +70,14 @@ struct LaunchCtx {
 bool rowstream_eligible(const Problem& p);
 cudaError_t rowstream_launch(const Problem& p, const LaunchCtx& c);
 
+// Tiling of the TMA-fed decode GEMV that bounds its split-K scratch: row blocks of 16, 32
+// or 64 rows, K split into at most 8 parts.  A launch that splits K uses parts x (row
+// blocks x rows per block) partial sums and one counter per row block; a launch whose
+// scratch does not fit the context's capacity does not split.
+constexpr int kGemvMinRowBlock = 16;
+constexpr int kGemvMaxRowBlock = 64;
+constexpr int kGemvMaxParts = 8;
+
 // TMA-fed decode GEMV (M = 1): persistent CTAs, a producer warp streams weight tiles
 // into a shared-memory ring.  Needs K % 32 == 0, K >= 512, N >= 16, 16-byte aligned x and
 // qweight, and group_size % 32 == 0 or group_size >= K.

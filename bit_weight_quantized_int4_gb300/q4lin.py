@@ -39,6 +39,15 @@ Q4LIN_PATH_FFMA = 2
 Q4LIN_PATH_TC = 3
 PATH_NAMES = {0: "auto", 1: "gemv", 2: "ffma", 3: "tc"}
 
+Q4LIN_KERNEL_NONE = 0
+Q4LIN_KERNEL_GEMV_TMA = 1
+Q4LIN_KERNEL_MULTIROW = 2
+Q4LIN_KERNEL_ROWSTREAM = 3
+Q4LIN_KERNEL_GENERIC = 4
+Q4LIN_KERNEL_TC = 5
+KERNEL_NAMES = {0: "none", 1: "gemv_tma", 2: "multirow", 3: "rowstream", 4: "generic",
+                5: "tc"}
+
 Q4LIN_OPT_FORCE_PATH = 1
 Q4LIN_OPT_NIBBLE_EVEN_HIGH = 2
 Q4LIN_OPT_WAIT_LIMIT = 3
@@ -71,6 +80,9 @@ _lib.q4lin_run_requant.restype = _i32
 _lib.q4lin_plan.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i32,
                             ctypes.POINTER(_i32)]
 _lib.q4lin_plan.restype = _i32
+_lib.q4lin_plan_kernel.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i32,
+                                   ctypes.POINTER(_i32)]
+_lib.q4lin_plan_kernel.restype = _i32
 _lib.q4lin_set_option.argtypes = [_vp, _i32, _i64]
 _lib.q4lin_set_option.restype = _i32
 _lib.q4lin_get_option.argtypes = [_vp, _i32, ctypes.POINTER(_i64)]
@@ -149,6 +161,15 @@ def q4lin_plan(handle, x, qweight, scales, bias, out, M, N, K, group_size, scale
     st = _lib.q4lin_plan(handle, x, qweight, scales, bias, out, M, N, K, group_size,
                          scale_dtype, ctypes.byref(path))
     return st, path.value
+
+
+def q4lin_plan_kernel(handle, x, qweight, scales, bias, out, M, N, K, group_size,
+                      scale_dtype):
+    """Returns (status, kernel)."""
+    kernel = _i32(0)
+    st = _lib.q4lin_plan_kernel(handle, x, qweight, scales, bias, out, M, N, K, group_size,
+                                scale_dtype, ctypes.byref(kernel))
+    return st, kernel.value
 
 
 def q4lin_set_option(handle, option: int, value: int) -> int:
@@ -242,3 +263,13 @@ def plan(handle: Handle, x, qweight, scales, bias, group_size: int, out) -> str:
     if st != Q4LIN_OK:
         raise Q4LinError(st, "q4lin_plan")
     return PATH_NAMES[path]
+
+
+def plan_kernel(handle: Handle, x, qweight, scales, bias, group_size: int, out) -> str:
+    """Name of the kernel q4lin_run would launch for these tensors."""
+    M, N, K, sd = _check_args(x, qweight, scales, bias, group_size)
+    st, kernel = q4lin_plan_kernel(handle.ptr, _ptr(x), _ptr(qweight), _ptr(scales),
+                                   _ptr(bias), _ptr(out), M, N, K, group_size, sd)
+    if st != Q4LIN_OK:
+        raise Q4LinError(st, "q4lin_plan_kernel")
+    return KERNEL_NAMES[kernel]

@@ -174,7 +174,10 @@ Q4LIN_API q4lin_status_t q4lin_run_grouped(q4lin_handle_t handle,
  *   16-byte aligned, group_size neither a multiple of 32 nor >= K) return
  *   Q4LIN_ERR_UNSUPPORTED.
  *   The first call on a device looks up the array's device address (once per device, on
- *   the current device); make that first call before any stream capture.
+ *   the current device); make that first call before any stream capture.  A device reset
+ *   (cudaDeviceReset) destroys the array with the context: the next call on that device
+ *   sees the new context and looks the address up again, so after a reset, too, make the
+ *   first call before any capture.
  *   Every call shares the array and it keeps the last call's contents: each call clears
  *   the counters it needs (an asynchronous memset on `stream`) before its kernel.  Calls
  *   that overlap on the GPU race on the array: order them (one stream, or events).
@@ -237,6 +240,25 @@ Q4LIN_API q4lin_status_t q4lin_plan(q4lin_handle_t handle, const float* x,
                                     const float* bias, const float* out, int64_t M,
                                     int64_t N, int64_t K, int64_t group_size,
                                     int scale_dtype, int* path_out);
+
+/* Kernels behind the paths (what q4lin_plan_kernel reports). */
+typedef enum {
+    Q4LIN_KERNEL_NONE = 0,      /* M == 0 or N == 0: nothing runs                          */
+    Q4LIN_KERNEL_GEMV_TMA = 1,  /* TMA-fed decode GEMV (M = 1)                             */
+    Q4LIN_KERNEL_MULTIROW = 2,  /* TMA-fed multi-row GEMV (2 <= M <= 4)                    */
+    Q4LIN_KERNEL_ROWSTREAM = 3, /* row-streaming CUDA-core kernel (small M)                */
+    Q4LIN_KERNEL_GENERIC = 4,   /* generic CUDA-core kernel (any K, group size, alignment) */
+    Q4LIN_KERNEL_TC = 5         /* tcgen05 tensor-core GEMM                                */
+} q4lin_kernel_t;
+
+/* The kernel q4lin_run would launch for these arguments (no launch, no device access);
+ * *kernel_out receives a q4lin_kernel_t.  Same arguments, validation and status codes as
+ * q4lin_plan; for M == 0 or N == 0, *kernel_out is Q4LIN_KERNEL_NONE. */
+Q4LIN_API q4lin_status_t q4lin_plan_kernel(q4lin_handle_t handle, const float* x,
+                                           const uint8_t* qweight, const void* scales,
+                                           const float* bias, const float* out, int64_t M,
+                                           int64_t N, int64_t K, int64_t group_size,
+                                           int scale_dtype, int* kernel_out);
 
 /* Set / read one q4lin_option_t.  Q4LIN_ERR_INVALID_ARG for an unknown option or an
  * out-of-range value. */

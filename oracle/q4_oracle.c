@@ -27,7 +27,7 @@
  * bits and a scale at most 24, so w = (q - 8) * s is exact in double; x has 24 bits, so
  * x * w (<= 52 bits) is exact too.  The only roundings are those of the running sums.
  *
- * Readings of points the pages leave open (each is listed in the design notes too):
+ * Readings of points the pages leave open (the pages are silent on each):
  *   - Packed row stride is ceil(K/2) bytes; for odd K the last byte's high nibble is
  *     padding and is never read ("K_packed == ceil(K/2)" guard of the qcs4w page).
  *   - num_groups = ceil(K / group_size); a last partial group is indexed floor(k / gs).
@@ -228,7 +228,7 @@ int q4o_backward_dx(const float* d_out, const uint8_t* qweight, const void* scal
  *
  * "[ExecuTorch][WebGPU] Add fp32 matmul ops ... (q4gsw_requant)", #20945 (the rule and
  * the zero-scale case) and #20946 (its golden: round / clamp, zero scale -> code 8).
- * Readings where the page is silent (also in the design notes):
+ * Readings where the page is silent:
  *   - the quotient is an fp32 quotient (latents and scales are fp32 on the page, and the
  *     integer decision is taken at that precision): it is computed in double and rounded
  *     once to float, which for a division equals the IEEE fp32 quotient (53 >= 2*24 + 2);

@@ -32,20 +32,13 @@ def tol_for(path):
     return TOL_TC if path == TC else TOL_FP32
 
 
-def sample_rows(M, max_rows=24):
-    if M <= max_rows:
-        return np.arange(M)
-    step = -(-M // 16)
-    return np.unique(np.concatenate([[0, M - 1], np.arange(0, M, step)]))
-
-
-def check_case(handle, case, path=AUTO, even_high=False, rows=None):
+def check_case(handle, case, path=AUTO, even_high=False):
+    """Every element of out[M,N] against the oracle (full rows and columns: the oracle
+    finishes the largest configs, 2048 x 8192 x 2048, in seconds on the host cores)."""
     out, used = run_q4lin(handle, case, path, even_high)
-    if rows is None:
-        rows = np.arange(case.M)
-    ref, mag = oracle.linear(case.x[rows], case.qweight, case.scales, case.bias, case.K,
+    ref, mag = oracle.linear(case.x, case.qweight, case.scales, case.bias, case.K,
                              case.group_size, even_high=even_high)
-    assert_parity(out[rows], ref, mag, tol_for(used))
+    assert_parity(out, ref, mag, tol_for(used))
     return out, used
 
 
@@ -84,7 +77,7 @@ def test_decode_gemv_shapes(handle, N, K):
 @pytest.mark.parametrize("M", [1, 7, 64])
 def test_qcs4w_vocab_ragged(handle, M):
     c = synth.make_case(M, 128257, 4096, 4096, scale_f16=False, bias=False, seed=4)
-    check_case(handle, c, AUTO, rows=sample_rows(M, 8))
+    check_case(handle, c, AUTO)
 
 
 @pytest.mark.parametrize("M", [1, 33])
@@ -251,7 +244,8 @@ PREFILL_NK = [(2048, 2048), (512, 2048), (8192, 2048), (2048, 8192)]
 @pytest.mark.parametrize("N,K", PREFILL_NK)
 def test_prefill_shapes(handle, M, N, K):
     c = synth.make_case(M, N, K, 32, scale_f16=False, bias=(N != 512), seed=3)
-    check_case(handle, c, AUTO, rows=sample_rows(M))
+    _, used = check_case(handle, c, AUTO)
+    assert used == TC
 
 
 @pytest.mark.parametrize("M,K,N,gs", [(96, 2048, 256, 32), (70, 1024, 136, 32),
@@ -259,7 +253,7 @@ def test_prefill_shapes(handle, M, N, K):
                                       (128, 8192, 2048, 32)])
 def test_extra_page_shapes(handle, M, K, N, gs):
     c = synth.make_case(M, N, K, gs, scale_f16=False, bias=True, seed=12)
-    check_case(handle, c, AUTO, rows=sample_rows(M))
+    check_case(handle, c, AUTO)
 
 
 # ------------------------------------------------------------------- tensor-core path
@@ -284,7 +278,7 @@ TC_SHAPES = [
 @pytest.mark.parametrize("M,N,K,gs,f16,bias", TC_SHAPES)
 def test_tc_parity(handle, M, N, K, gs, f16, bias):
     c = synth.make_case(M, N, K, gs, scale_f16=f16, bias=bias, seed=M + N)
-    _, used = check_case(handle, c, TC, rows=sample_rows(M))
+    _, used = check_case(handle, c, TC)
     assert used == TC
 
 
@@ -300,7 +294,7 @@ def test_tc_split_k_parity_and_determinism(handle, M, N, K, gs, f16, bias):
     tiles are added in rank order in distributed shared memory.  Parity with the oracle,
     and bitwise-identical results on a second call."""
     c = synth.make_case(M, N, K, gs, scale_f16=f16, bias=bias, seed=N + K)
-    out1, used = check_case(handle, c, TC, rows=sample_rows(M))
+    out1, used = check_case(handle, c, TC)
     assert used == TC
     out2, _ = run_q4lin(handle, c, TC)
     np.testing.assert_array_equal(out1, out2)
