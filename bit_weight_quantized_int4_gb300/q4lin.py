@@ -134,6 +134,11 @@ def q4lin_run_grouped(handle, problems, stream) -> int:
     return _lib.q4lin_run_grouped(handle, arr, len(problems), stream)
 
 
+def q4lin_run_grouped_array(handle, array, count, stream) -> int:
+    """Raw call with a prebuilt ctypes array of q4lin_problem_t (no per-call marshalling)."""
+    return _lib.q4lin_run_grouped(handle, array, int(count), stream)
+
+
 def q4lin_run_static_scratch(x, qweight, scales, bias, out, N, K, group_size, scale_dtype,
                              stream) -> int:
     """Raw call of the allocation-free decode GEMV (pointers and stream as integers)."""

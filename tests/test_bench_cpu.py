@@ -85,9 +85,43 @@ def test_token_groups_share_x():
     assert groups[-1] == [("lm_head", 128256, 2048)]
 
 
-def test_token_traffic_only_for_the_captured_launch_count():
+def test_launch_kinds_of_a_token():
     import bench
-    t = bench.TOKEN_TRAFFIC
-    assert bench.token_traffic_per_launch(t["launches"] + 1) is None
-    if bench.gemv_source_sha() == t["source_sha256"]:
-        assert bench.token_traffic_per_launch(t["launches"]) == round(t["bytes"] / t["launches"])
+    kinds = [bench.launch_kind(g) for g in bench.token_groups("8b")]
+    assert kinds[:4] == ["qkv", "o", "gateup", "down"] and kinds[-1] == "lm_head"
+    assert len(kinds) == 32 * 4 + 1
+
+
+def test_token_traffic_needs_every_launch_shape_and_the_source():
+    """Traffic per launch = captured bytes of each launch shape summed over the token's
+    launches / launches; null unless the capture's source hash is the current one and
+    every launch shape was captured."""
+    import bench
+    table = {"source_sha256": "abc", "bytes": {"8b:qkv": 1000, "8b:o": 200, "8b:gateup": 3000,
+                                               "8b:down": 400, "8b:lm_head": 50000}}
+    want = round((32 * (1000 + 200 + 3000 + 400) + 50000) / 129)
+    assert bench.token_traffic_per_launch("8b", "abc", table) == want
+    assert bench.token_traffic_per_launch("8b", "def", table) is None
+    assert bench.token_traffic_per_launch("1b", "abc", table) is None
+    assert bench.token_traffic_per_launch("8b", "abc", {"source_sha256": None, "bytes": {}}) is None
+
+
+def test_cpu_baseline_summary_scales_shapes_to_tokens_and_prefill():
+    """Per-token oracle time = sum over the token's GEMVs of the per-shape time; 16-layer
+    prefill = 16 x sum over the layer's classes (count x per-4-row time x M / 4)."""
+    import bench
+
+    def worker(threads, ms):
+        return {"threads": threads,
+                "shapes": [{"label": l, "N": N, "K": K, "M": M, "rows_timed": 16,
+                            "ms_full": ms(N, K, M)} for l, N, K, _, M in bench._cpu_shapes()]}
+    one = worker(1, lambda N, K, M: N * K * M * 1e-6)
+    allc = worker(16, lambda N, K, M: N * K * M * 1e-7)
+    per_shape, tokens, prefill = bench.cpu_baseline_summary(one, allc)
+    assert len(per_shape) == len(bench._cpu_shapes())
+    t8 = sum(N * K * 1e-7 for _, N, K in bench.token_shapes("8b"))
+    assert abs(tokens["8b"]["ms_all"] - round(t8, 1)) < 1e-9
+    assert abs(tokens["8b"]["GB_s_all"] - round(bench.token_bytes("8b") / (t8 * 1e-3) / 1e9, 4)) < 1e-9
+    p = {r["M"]: r for r in prefill}
+    t = 16 * sum(c * N * K * 4 * 1e-6 * 2048 / 4 for (N, K), c in bench.PREFILL_LAYER_COUNTS.items())
+    assert abs(p[2048]["ms_16_layers_1_thread"] - round(t, 1)) < 1e-9
