@@ -503,11 +503,13 @@ def shape_bandwidth(torch, handle, N, K, M=1):
     return row
 
 
-def prefill_time(torch, handle, M, N, K, bias=True, min_reps=100):
+def prefill_time(torch, handle, M, N, K, bias=True, min_reps=100, f16=False):
     """One prefill shape (fp32 scales, group 32, fp32 bias): median device time per launch
     over >= min_reps launches, each on its own HBM-cold weight copy, and TFLOP/s of
-    2*M*N*K."""
+    2*M*N*K.  f16: with the tensor-core path's fp16 operands (Q4LIN_OPT_TC_F16; the time
+    includes the conversion of x)."""
     from bit_weight_quantized_int4_gb300 import q4lin as q
+    q.q4lin_set_option(handle, q.Q4LIN_OPT_TC_F16, int(f16))
     wbytes = N * K // 2 + (K // GROUP) * N * 4
     ws, ss = weight_copies(torch, N, K, wbytes, scale_dtype=torch.float32, cap=256)
     bvec = torch.randn(N, device="cuda") * 0.1
@@ -525,6 +527,7 @@ def prefill_time(torch, handle, M, N, K, bias=True, min_reps=100):
         assert r == q.Q4LIN_OK
 
     us, reps = median_launch_us(torch, launch, len(ws), min_reps=min_reps)
+    q.q4lin_set_option(handle, q.Q4LIN_OPT_TC_F16, 0)
     del ws, ss
     return {"M": M, "N": N, "K": K, "kernel": q.KERNEL_NAMES[kernel], "us": round(us, 2),
             "TFLOP_s": round(2.0 * M * N * K / (us * 1e-6) / 1e12, 2), "reps": reps}
@@ -620,6 +623,28 @@ def prefill_roofline(torch, handle, bf16_peak):
         layer16.append({"M": M, "ms": round(16 * t / 1000, 4),
                         "TFLOP_s": round(fl / (t * 1e-6) / 1e12, 2)})
     top = layer16[-1]
+    # The same shapes with fp16 operands (kind::f16, twice the tf32 MMA rate), against the
+    # dense 16-bit peak of the peaks file.
+    shapes16 = []
+    for M in PREFILL_M:
+        for N, K in PREFILL_NK:
+            r = prefill_time(torch, handle, M, N, K, bias=(N != 512), f16=True)
+            r["frac_of_bf16"] = round(r["TFLOP_s"] / bf16_peak, 4) if bf16_peak else None
+            shapes16.append(r)
+    layer16_f16 = []
+    for M in PREFILL_M:
+        t = sum(PREFILL_LAYER_COUNTS[(s["N"], s["K"])] * s["us"] for s in shapes16 if s["M"] == M)
+        fl = sum(PREFILL_LAYER_COUNTS[(s["N"], s["K"])] * 2.0 * M * s["N"] * s["K"]
+                 for s in shapes16 if s["M"] == M)
+        layer16_f16.append({"M": M, "ms": round(16 * t / 1000, 4),
+                            "TFLOP_s": round(fl / (t * 1e-6) / 1e12, 2)})
+    top16 = layer16_f16[-1]
+    f16_block = {"kernel": "tc_wa_kernel with fp16 operands (Q4LIN_OPT_TC_F16: x converted by "
+                           "x_to_f16_kernel, tcgen05.mma kind::f16)",
+                 "achieved": top16["TFLOP_s"], "peak": bf16_peak, "unit": "TFLOP/s",
+                 "frac": round(top16["TFLOP_s"] / bf16_peak, 4) if bf16_peak else None,
+                 "peak_source": "bf16_tflops of the peaks file (dense 16-bit; fp16 = bf16 rate)",
+                 "shapes": shapes16, "layer16": layer16_f16}
     return {"bound": "tensor", "kernel": "tc_wa_kernel (tcgen05.mma kind::tf32, TMEM accumulators)",
             "workload": "16-layer Llama-3.2-1B-shaped prefill GEMMs at M=2048 (fp32 scales, group 32)",
             "achieved": top["TFLOP_s"], "peak": tf32_cublas, "unit": "TFLOP/s",
@@ -631,7 +656,7 @@ def prefill_roofline(torch, handle, bf16_peak):
             "bf16_peak": bf16_peak,
             "frac_of_bf16": round(top["TFLOP_s"] / bf16_peak, 4) if bf16_peak else None,
             "timing": "median of >= 100 launches after >= 20 warm-up, weight copies rotated (HBM-cold)",
-            "shapes": shapes, "layer16": layer16}
+            "shapes": shapes, "layer16": layer16, "f16": f16_block}
 
 
 # ------------------------------------------------------------------------- CPU baseline

@@ -11,16 +11,31 @@
 // is decoupled from the arithmetic:
 //   producer warp (one lane): per stage, 2D TMA copies of the weight tile [rb rows x 512
 //     bytes] (= 1024 k per row; the packed matrix viewed as 16-bit elements, so one box
-//     spans the 512 bytes) and of the matching block of group
-//     scales [1024 / group size groups x rb rows], all on one mbarrier, into a ring of
-//     2..8 stages.  Weight rows are long contiguous segments, so DRAM sees streaming reads.
+//     spans the 512 bytes) and of the matching block of group scales [1024 / group size
+//     groups x rb rows], all on one mbarrier, into a ring of 2..8 stages.  Weight rows
+//     are long contiguous segments, so DRAM sees streaming reads.
 //   8 consumer warps (256 threads): thread = (chunk lane j in 0..15, row group of V rows);
-//     per stage it widens chunks j and j + 16 (32 codes each) of each of its V rows and
-//     dots them with the x chunks (read from shared memory, where x is staged in padded
-//     32-float chunks, and reused across the V rows), scaling each chunk by its group
-//     scale.  A quarter-warp reads 128 contiguous bytes of a weight row (conflict-free).
-//     Partial sums stay in registers across the whole row; the 16 chunk lanes of a row
-//     group are reduced with shuffles once per row block.
+//     per stage it takes chunks j and j + 16 (32 codes each) of each of its V rows.
+//     x is staged whole in shared memory once per CTA after the dependency wait (every
+//     consumer thread loads 16-byte units, eight in flight at a time), unit u of 32-k
+//     chunk c at unit u ^ (c % 8) of the chunk's 128-byte row.  A quarter-warp then reads
+//     128 contiguous bytes of a weight row and 8 different 16-byte units of x, both
+//     conflict-free.  Partial sums stay in registers for
+//     the whole row; the 16 chunk lanes of a row group are reduced with shuffles once per
+//     row block.
+// Arithmetic (X8 instances): the first time a CTA uses a 1024-k stage, its consumers
+// convert the staged x of that stage in place into 32-bit fixed point per 32-k chunk: with F the largest
+// exponent field of the chunk, q = round(x * 2^(157 - F)) (|q| < 2^31; exact for every
+// element within a factor 128 of the chunk's largest), stored as 4 byte slices.  A chunk's
+// dot product sum_k (c_k - 8) * q_k is then exact integer arithmetic: 8 dp4a per 8 codes
+// (codes as unsigned bytes, one nibble mask each), with the -8 offset folded into the
+// accumulators' starting values (-8 * sum_k q_k, split into two 16-bit halves); it is
+// rounded once to fp32, scaled by 2^(F - 157) (exact) and accumulated with the group scale
+// in fp32.  A stage holding Inf or NaN (IEEE propagation is unchanged) or a chunk with a
+// nonzero element more than 2^13 below the chunk's largest keeps its fp32 values and takes
+// the fp32 path, so every converted element has a relative error <= 2^-18.  fp32 instances
+// (and such stages): the codes widened to exact floats by a byte permute
+// (0x4B0000cc = 2^23 + c) and one packed add, fp32 FMA.
 // A CTA is small enough (288 threads, at most 113 KiB of shared memory) that two fit on
 // one SM: the CTAs of the next kernel on the stream can become resident while this one
 // runs.  With programmatic dependent launch their producers then stream weights and
@@ -28,7 +43,9 @@
 // bias, out and the split-K workspace are touched only after it.
 // Row blocks of long-K, short-N matrices are split along K across CTAs; the partial row
 // sums go to a workspace and the last CTA of a row block adds them in part order (the
-// result does not depend on which CTA finishes last).
+// result does not depend on which CTA finishes last).  (A stream-K cut of the (row block,
+// stage) units into equal runs per CTA was measured too: its split hand-offs cost more
+// than its balance gained on the decode shapes.)
 // Waits are bounded in time; a timeout records code 1 in the status word and the CTA
 // drains its copies and returns.
 #include <algorithm>
@@ -47,15 +64,12 @@ constexpr int kThreadsG = kCThreads + 32;  // + the producer warp
 constexpr int kRowGroups = kCThreads / 16; // 16 chunk lanes per row group
 static_assert(kRowGroups == kGemvMinRowBlock && 4 * kRowGroups == kGemvMaxRowBlock,
               "row blocks of 16 row groups x V rows, V in {1, 2, 4}");
-// Stage width: H chunk columns of 16 bytes per thread, i.e. 256 * H packed bytes (512 * H
-// k) per row per stage.  H = 2 for every tile height (measured: halving the stage of the
-// V = 4 tiles to fit a deeper ring made them slower, the per-stage overhead outweighs the
-// extra depth).
-__host__ __device__ constexpr int chunk_cols(int) { return 2; }
-__host__ __device__ constexpr int stage_row_bytes(int V) { return 256 * chunk_cols(V); }
-__host__ __device__ constexpr int stage_chunks(int V) { return 16 * chunk_cols(V); }
-constexpr int kXPad = 36;                  // floats per 32-float x chunk in shared memory
+constexpr int kSRB = 512;                  // packed bytes of a row per stage (1024 k)
+constexpr int kSC = 32;                    // 32-k chunks per stage
+constexpr int kXStageBytes = 4096;         // x of one stage: 32 chunk rows x 128 bytes
+constexpr int kMetaBytes = 16;             // per chunk: factor, two offsets (one word unused)
 constexpr int kMaxStages = 8;
+constexpr int kMaxXStages = 32;            // K <= 32768 (x staged whole in shared memory)
 constexpr int kCtaSmem = 113 * 1024;       // two CTAs per SM
 constexpr int64_t kDrainNs = 4000000000LL;
 constexpr int kMaxMats = 4;
@@ -80,11 +94,11 @@ struct GArgs {
     MatArgs mat[kMaxMats];
     int nmat;
     int64_t K;
-    int kstages;     // ceil(K / stage k)
-    int x_chunks;    // kstages * chunks per stage
+    int kstages;     // ceil(K / 1024)
     int gs_shift;    // log2(group size / 32) (grouped scales)
     int stages;      // ring depth
     uint32_t stage_bytes, scale_off, stage_tx;
+    uint32_t x_off, meta_off, bar_off;  // shared-memory layout, from the 1024-aligned base
     int64_t row_blocks;
     // Split K: each row block's stages are cut into `parts` runs of `tpp` stages; a work
     // item is (row block, part).  With parts > 1 the items write partial row sums to
@@ -124,10 +138,18 @@ struct Cursor {
     }
 };
 
-__host__ __device__ constexpr int x_bytes(int x_chunks) { return x_chunks * kXPad * 4; }
-// Shared memory: the stage ring, then the barriers and flags (256 bytes), then x.
-inline int smem_bytes_g(int stages, uint32_t stage_bytes, int x_chunks) {
-    return 1024 + stages * (int)stage_bytes + 256 + x_bytes(x_chunks);
+// Shared memory: the stage ring, x (kstages x 4 KiB), the chunk metadata, then barriers
+// and flags (512 bytes).
+struct SmemLayout {
+    uint32_t x_off, meta_off, bar_off, total;
+};
+inline SmemLayout smem_layout(int stages, uint32_t stage_bytes, int kstages) {
+    SmemLayout l;
+    l.x_off = (uint32_t)stages * stage_bytes;  // stage bytes are multiples of 1024
+    l.meta_off = l.x_off + (uint32_t)kstages * kXStageBytes;
+    l.bar_off = l.meta_off + (uint32_t)kstages * kSC * kMetaBytes;
+    l.total = 1024 + l.bar_off + 512;
+    return l;
 }
 
 __device__ __forceinline__ float load_scale(const void* scales, int f16, int64_t idx) {
@@ -187,6 +209,13 @@ __device__ __forceinline__ uint32_t scale_slot(int g, int off) {
     return (uint32_t)(g * IB + ((((off >> 4) ^ f) << 4) | (off & 15)));
 }
 
+// Address of 16-byte unit u (4 consecutive k) of 32-k chunk c in the staged x: chunk row
+// c at c * 128 bytes, unit u at u ^ (c % 8), so that the 8 chunk lanes of a quarter-warp
+// (8 consecutive chunks, same unit) hit 8 different bank groups.
+__device__ __forceinline__ uint32_t x_unit(uint32_t xa, int c, int u) {
+    return xa + (uint32_t)c * 128u + ((uint32_t)(u ^ (c & 7)) << 4);
+}
+
 // Matrix that owns global row block blk (blk_begin ascending, matrix 0 begins at 0).
 __device__ __forceinline__ int mat_of(const GArgs& a, int64_t blk) {
     int i = 0;
@@ -196,14 +225,14 @@ __device__ __forceinline__ int mat_of(const GArgs& a, int64_t blk) {
     return i;
 }
 
-// Products x[t] * (code_t - 8) of one 16-byte chunk (32 codes), summed as a float2 of
-// (even-k sum, odd-k sum) where the lane fed from the HIGH nibbles carries a factor 16.
-// Byte b of a word holds k = 2b in its low nibble and k = 2b + 1 in its high nibble
-// (swapped when EH).  The low nibbles are isolated with one mask (w & 0x0F0F0F0F) and the
-// high nibbles in place with another (w & 0xF0F0F0F0, i.e. 16 * code): no shift.  A byte
-// permute builds the float 2^23 + byte (bit pattern 0x4B0000bb) and one packed add of
-// -(2^23 + 8) (low lane) / -(2^23 + 128) (high lane) gives c - 8 and 16 * (c - 8), both
-// exact.  The factor 16 is removed once per row (a power of two: exact).
+// fp32 chunk dot: products x[t] * (code_t - 8) of one 16-byte chunk (32 codes), summed as
+// a float2 of (even-k sum, odd-k sum) where the lane fed from the HIGH nibbles carries a
+// factor 16.  Byte b of a word holds k = 2b in its low nibble and k = 2b + 1 in its high
+// nibble (swapped when EH).  The low nibbles are isolated with one mask (w & 0x0F0F0F0F)
+// and the high nibbles in place with another (w & 0xF0F0F0F0, i.e. 16 * code): no shift.
+// A byte permute builds the float 2^23 + byte (bit pattern 0x4B0000bb) and one packed add
+// of -(2^23 + 8) (low lane) / -(2^23 + 128) (high lane) gives c - 8 and 16 * (c - 8), both
+// exact.
 template <bool EH>
 __device__ __forceinline__ float2 chunk_dot(const uint4& wv, const float4 (&xv)[8]) {
     constexpr float kLo = -8388616.0f, kHi = -8388736.0f;
@@ -228,22 +257,135 @@ __device__ __forceinline__ float2 chunk_dot(const uint4& wv, const float4 (&xv)[
     }
     return fadd2(a0, a1);
 }
+template <bool EH>
+__device__ __forceinline__ float chunk_dot_f32(const uint4& wv, const uint4 (&xu)[8]) {
+    float4 xv[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        xv[i] = make_float4(__uint_as_float(xu[i].x), __uint_as_float(xu[i].y),
+                            __uint_as_float(xu[i].z), __uint_as_float(xu[i].w));
+    const float2 d = chunk_dot<EH>(wv, xv);
+    return EH ? fmaf(d.x, 0.0625f, d.y) : fmaf(d.y, 0.0625f, d.x);
+}
 
-template <int V, bool EH, bool PC, bool F16>
+// OR of `v` over the 256 consumer threads (named barrier 1; the producer warp does not take
+// part).
+__device__ __forceinline__ bool consumers_any(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, 1, %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v), "r"(kCThreads)
+        : "memory");
+    return r != 0;
+}
+
+// Fixed-point chunk dot: sum_k (c_k - 8) * q_k of one chunk, exact, rounded once to fp32.
+// xu[2w] = (s0e, s1e, s0o, s1o) and xu[2w+1] = (s2e, s3e, s2o, s3o) for word w: slice s
+// (byte 3 - s of q, slice 0 signed) of the even / odd k of the word, one byte per k.
+// init = (-8 * sum_k (q_k >> 16), -8 * sum_k (q_k & 0xFFFF)).
+template <bool EH>
+__device__ __forceinline__ float chunk_dot_x8(const uint4& wv, const uint4 (&xu)[8], int init_hi,
+                                              int init_lo) {
+    int a0 = 0, a1 = init_hi, a2 = 0, a3 = init_lo;
+    const uint32_t words[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        const uint32_t lo = words[w] & 0x0F0F0F0Fu, hi = (words[w] >> 4) & 0x0F0F0F0Fu;
+        const uint32_t ev = EH ? hi : lo, od = EH ? lo : hi;  // codes of even / odd k
+        const uint4 A = xu[2 * w], B = xu[2 * w + 1];
+        a0 = dp4a_us(ev, A.x, a0);
+        a0 = dp4a_us(od, A.z, a0);
+        a1 = dp4a_uu(ev, A.y, a1);
+        a1 = dp4a_uu(od, A.w, a1);
+        a2 = dp4a_uu(ev, B.x, a2);
+        a2 = dp4a_uu(od, B.z, a2);
+        a3 = dp4a_uu(ev, B.y, a3);
+        a3 = dp4a_uu(od, B.w, a3);
+    }
+    // |hi| < 2^23 and |lo| < 2^24: both convert exactly; one rounding in the fma.
+    const int hi_v = a0 * 256 + a1, lo_v = a2 * 256 + a3;
+    return fmaf((float)hi_v, 65536.f, (float)lo_v);
+}
+
+// Converts stage ks of the staged x in place, unless one of its chunks holds an Inf or NaN
+// (largest exponent field 255) or a nonzero element more than 2^13 below the chunk's
+// largest: then the whole stage stays fp32 and false is returned (the same on every
+// consumer thread).  Converted elements keep at least 18 significant bits (relative error
+// <= 2^-18; exact within a factor 128 of the chunk's largest), for any input.  Consumer
+// thread t takes unit t % 8 (4 consecutive k) of chunk row t / 8 of the stage (the 8
+// threads of a chunk are consecutive lanes of one warp) and lane 0 of each chunk writes
+// its metadata (factor 2^(F - 157), the two offsets).  Ends with the consumers' barrier.
+__device__ __forceinline__ bool convert_x_stage(uint32_t xa, uint32_t meta, int ks, int t) {
+    const int c = ks * kSC + (t >> 3), u = t & 7;
+    const uint32_t addr = x_unit(xa, c, u);
+    const uint4 raw = ld_shared_v4(addr);
+    const uint32_t b[4] = {raw.x, raw.y, raw.z, raw.w};
+    uint32_t F = 0, E = 255;  // largest exponent field; smallest of the nonzero elements
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t f = (b[i] >> 23) & 0xFFu;
+        F = max(F, f);
+        E = min(E, (b[i] & 0x7FFFFFFFu) ? max(f, 1u) : 255u);
+    }
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) {
+        F = max(F, __shfl_xor_sync(0xffffffffu, F, o));
+        E = min(E, __shfl_xor_sync(0xffffffffu, E, o));
+    }
+    const bool keep_f32 = consumers_any(F == 255u || E + 13u < F);
+    const uint32_t Fm = max(F, 31u);  // 2^(157 - Fm) and 2^(Fm - 157) stay normal floats
+    const float mul = __uint_as_float((284u - min(Fm, 254u)) << 23);
+    int q[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) q[i] = __float2int_rn(__uint_as_float(b[i]) * mul);
+    // Lane pair (2w, 2w + 1) holds word w (8 k); this lane's half h holds k % 8 = 4h .. 4h+3.
+    // Bytes of slices 0/1 (e01) and 2/3 (e23) of the even k, and likewise of the odd k;
+    // half 0 keeps slices 0/1 and sends 2/3, half 1 the other way round.
+    const int h = u & 1;
+    const uint32_t sel_keep = h ? 0x4051u : 0x6273u, sel_send = h ? 0x6273u : 0x4051u;
+    const uint32_t e_keep = prmt((uint32_t)q[0], (uint32_t)q[2], sel_keep);
+    const uint32_t o_keep = prmt((uint32_t)q[1], (uint32_t)q[3], sel_keep);
+    const uint32_t e_recv =
+        __shfl_xor_sync(0xffffffffu, prmt((uint32_t)q[0], (uint32_t)q[2], sel_send), 1);
+    const uint32_t o_recv =
+        __shfl_xor_sync(0xffffffffu, prmt((uint32_t)q[1], (uint32_t)q[3], sel_send), 1);
+    // Half 0's bytes (k % 8 = 0, 2 or 1, 3) go first in each register.
+    const uint32_t s_lo = h ? 0x1054u : 0x5410u, s_hi = h ? 0x3276u : 0x7632u;
+    int qh = 0, ql = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) qh += q[i] >> 16, ql += q[i] & 0xFFFF;
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) {
+        qh += __shfl_xor_sync(0xffffffffu, qh, o);
+        ql += __shfl_xor_sync(0xffffffffu, ql, o);
+    }
+    if (!keep_f32) {
+        st_shared_v4(addr, prmt(e_keep, e_recv, s_lo), prmt(e_keep, e_recv, s_hi),
+                     prmt(o_keep, o_recv, s_lo), prmt(o_keep, o_recv, s_hi));
+        if (u == 0)
+            st_shared_v4(meta + (uint32_t)c * kMetaBytes, (Fm - 30u) << 23, (uint32_t)(-8 * qh),
+                         (uint32_t)(-8 * ql), 0u);
+    }
+    asm volatile("bar.sync 1, %0;" ::"r"(kCThreads) : "memory");
+    return !keep_f32;
+}
+
+template <int V, bool EH, bool PC, bool F16, bool X8>
 __global__ void __launch_bounds__(kThreadsG, 2)
     gemv_tma_kernel(const __grid_constant__ TensorMaps tmaps, const GArgs a) {
     constexpr int rb = kRowGroups * V;  // rows per block: 16 row groups of V rows
-    constexpr int H = chunk_cols(V), kSRB = stage_row_bytes(V), kSC = stage_chunks(V);
     constexpr uint32_t esz = F16 ? 2 : 4;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;  // stages are 1024-byte aligned
     uint8_t* gbase = smem_raw + (base - raw);
     const int S = a.stages;
-    const uint32_t bar_base = base + (uint32_t)S * a.stage_bytes;
-    volatile int* failed = reinterpret_cast<volatile int*>(gbase + (bar_base + 16 * kMaxStages - base));
+    const uint32_t bar_base = base + a.bar_off;
+    const uint32_t xa = base + a.x_off, meta = base + a.meta_off;
+    volatile int* failed = reinterpret_cast<volatile int*>(gbase + a.bar_off + 16 * kMaxStages);
     volatile int* s_ticket = failed + 1;  // last-item decision, broadcast to the consumers
-    float* xs = reinterpret_cast<float*>(gbase + (bar_base + 256 - base));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     auto full = [&](int s) { return bar_base + 8u * s; };
     auto empty = [&](int s) { return bar_base + 8u * (kMaxStages + s); };
@@ -266,10 +408,10 @@ __global__ void __launch_bounds__(kThreadsG, 2)
                 prefetch_tensormap(&tmaps.w[q]);
                 if (!PC) prefetch_tensormap(&tmaps.s[q]);
             }
-            // Pull x toward L2 now, so that the read after griddepcontrol.wait is short.
-            // L2 is where global memory is kept coherent: if the preceding kernel writes x
-            // after this prefetch, the L2 line is updated and the later read sees it; no
-            // copy of x enters this SM's L1 before the wait.
+            // Pull x toward L2 now, so that the consumers' reads after griddepcontrol.wait
+            // are short.  L2 is where global memory is kept coherent: if the preceding
+            // kernel writes x after this prefetch, the L2 line is updated and the later read
+            // sees it; no copy of x enters this SM before the wait.
             const int64_t xb = a.K * 4;
             for (int64_t off = 0; off < xb; off += 32768)
                 l2_prefetch_bulk(a.x + off / 4, (uint32_t)(xb - off < 32768 ? xb - off : 32768));
@@ -289,13 +431,13 @@ __global__ void __launch_bounds__(kThreadsG, 2)
                 mbar_arrive_expect_tx(full(s), a.stage_tx);
                 tma_load_2d(sb, &tmaps.w[mi], cur.ks * (kSRB / 2), row0, full(s));
                 if (!PC)
-                    tma_load_2d(sb + a.scale_off, &tmaps.s[mi], row0,
-                                (cur.ks * kSC) >> a.gs_shift, full(s));
+                    tma_load_2d(sb + a.scale_off, &tmaps.s[mi], row0, (cur.ks * kSC) >> a.gs_shift,
+                                full(s));
                 ++t;
                 if (++s == S) s = 0, ph ^= 1u;
                 cur.advance(a);
             }
-            // The last armed stages may still be landing; the CTA must not exit first.
+            // The last armed copies may still be landing; the CTA must not exit first.
             for (int q = t > S ? t - S : 0; q < t; ++q)
                 wait_bounded(full(q % S), (uint32_t)(q / S) & 1u, kDrainNs, nullptr);
         }
@@ -305,32 +447,36 @@ __global__ void __launch_bounds__(kThreadsG, 2)
     // ------------------------------------------------------------------ consumers
     const int j = threadIdx.x & 15;          // chunk lane within a 256-byte box row
     const int r0 = (threadIdx.x >> 4) * V;   // first of this thread's V rows in a block
-
-    // x into shared memory once: chunk c (32 floats) at xs + c * kXPad; zero past K.
-    // (Four loads in flight per thread before the shared-memory stores.)
-    griddep_wait();
-    for (int i0 = threadIdx.x; i0 < a.x_chunks * 8; i0 += 4 * kCThreads) {
-        float4 v[4];
+    griddep_wait();  // x, bias, out and the workspace belong to the dependency chain
+    // x into shared memory once: 16-byte unit i (k = 4 i .. 4 i + 3) of chunk i / 8 at its
+    // swizzled place, zero past K; eight loads in flight per thread before the stores.
+    {
+        const int units = a.kstages * kSC * 8;
+        for (int i0 = threadIdx.x; i0 < units; i0 += 8 * kCThreads) {
+            float4 v[8];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int i = i0 + u * kCThreads;
-            const int64_t k = (int64_t)(i >> 3) * 32 + (i & 7) * 4;
-            v[u] = (i < a.x_chunks * 8 && k < a.K) ? __ldg(reinterpret_cast<const float4*>(a.x + k))
-                                                    : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
+            for (int q = 0; q < 8; ++q) {
+                const int i = i0 + q * kCThreads;
+                v[q] = (i < units && 4 * (int64_t)i < a.K)
+                           ? __ldg(reinterpret_cast<const float4*>(a.x) + i)
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int i = i0 + u * kCThreads;
-            if (i < a.x_chunks * 8)
-                *reinterpret_cast<float4*>(xs + (i >> 3) * kXPad + (i & 7) * 4) = v[u];
+            for (int q = 0; q < 8; ++q) {
+                const int i = i0 + q * kCThreads;
+                if (i < units)
+                    st_shared_v4(x_unit(xa, i >> 3, i & 7), __float_as_uint(v[q].x),
+                                 __float_as_uint(v[q].y), __float_as_uint(v[q].z),
+                                 __float_as_uint(v[q].w));
+            }
         }
+        asm volatile("bar.sync 1, %0;" ::"r"(kCThreads) : "memory");
     }
-    asm volatile("bar.sync 1, %0;" ::"r"(kCThreads) : "memory");
 
-    // Per row: (even-k, odd-k) partial sums, scaled per chunk by the group scale.
-    float2 acc[V];
+    // Per row: fp32 partial sum, scaled per chunk by the group scale.
+    float acc[V];
 #pragma unroll
-    for (int v = 0; v < V; ++v) acc[v] = make_float2(0.f, 0.f);
+    for (int v = 0; v < V; ++v) acc[v] = 0.f;
     Cursor cur;
     cur.start(a);
     // Where this thread's row of the current item goes, with its bias and (per channel)
@@ -349,19 +495,27 @@ __global__ void __launch_bounds__(kThreadsG, 2)
     if (cur.valid(a)) prepare(cur.blk);
     int s = 0;
     uint32_t ph = 0;
-    // Per-thread offsets: chunk lane j of the x chunks, the thread's rows of a weight
-    // stage (row r at r * kSRB bytes, chunk column c at c * 16), its group-scale rows.
-    const uint32_t xthr = smem_u32(xs) + (uint32_t)j * (kXPad * 4);
+    // Per-thread offsets: the thread's rows of a weight stage (row r at r * kSRB bytes,
+    // chunk column c at c * 16), its group-scale rows.
     const uint32_t w_off = (uint32_t)(r0 * kSRB + j * 16);
-    uint32_t s_off[H];
+    uint32_t s_off[2];
 #pragma unroll
-    for (int h = 0; h < H; ++h)
+    for (int h = 0; h < 2; ++h)
         s_off[h] = a.scale_off + scale_slot<rb * esz>((h * 16 + j) >> a.gs_shift, r0 * esz);
+    uint32_t x_ready = X8 ? 0u : ~0u;  // stages of x this CTA has looked at
+    uint32_t x_fixed = 0u;             // ... and converted to fixed point
     // After a timed-out wait (`dead`) the warp still walks every item, without waiting or
     // computing, so that all consumer warps reach the same named barriers and every split-K
     // ticket is still counted and reset; nothing is stored.
     bool dead = false;
     while (cur.valid(a)) {
+        const int ks = cur.ks;
+        if (X8 && !((x_ready >> ks) & 1u)) {
+            // First use of this stage of x by the CTA: convert it (its barriers are reached
+            // by every consumer thread whatever its state).
+            if (convert_x_stage(xa, meta, ks, threadIdx.x)) x_fixed |= 1u << ks;
+            x_ready |= 1u << ks;
+        }
         const bool got =
             !dead && __all_sync(0xffffffffu, wait_bounded(full(s), ph, a.wait_ns, failed));
         if (!got && !dead) {
@@ -370,24 +524,41 @@ __global__ void __launch_bounds__(kThreadsG, 2)
         }
         if (got) {
             const uint32_t sb = base + (uint32_t)s * a.stage_bytes;
-            const uint32_t xc = xthr + (uint32_t)(cur.ks * kSC) * (kXPad * 4);
+            if (X8 && ((x_fixed >> ks) & 1u)) {
 #pragma unroll
-            for (int h = 0; h < H; ++h) {
-                float4 xv[8];
+                for (int h = 0; h < 2; ++h) {
+                    const int c = ks * kSC + h * 16 + j;
+                    uint4 xu[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const uint4 u = ld_shared_v4(xc + h * 16 * kXPad * 4 + 16 * i);
-                    xv[i] = make_float4(__uint_as_float(u.x), __uint_as_float(u.y),
-                                        __uint_as_float(u.z), __uint_as_float(u.w));
+                    for (int i = 0; i < 8; ++i) xu[i] = ld_shared_v4(x_unit(xa, c, i));
+                    const uint4 md = ld_shared_v4(meta + (uint32_t)c * kMetaBytes);
+                    float sc[V];
+                    if (!PC) stage_scales<V, F16>(sb + s_off[h], sc);
+                    const uint32_t wrow = sb + w_off + h * 256;
+#pragma unroll
+                    for (int v = 0; v < V; ++v) {
+                        const uint4 wv = ld_shared_v4(wrow + v * kSRB);
+                        const float tf = chunk_dot_x8<EH>(wv, xu, (int)md.y, (int)md.z) *
+                                         __uint_as_float(md.x);
+                        acc[v] = PC ? acc[v] + tf : fmaf(tf, sc[v], acc[v]);
+                    }
                 }
-                float sc[V];
-                if (!PC) stage_scales<V, F16>(sb + s_off[h], sc);
-                const uint32_t wrow = sb + w_off + h * 256;
+            } else {
 #pragma unroll
-                for (int v = 0; v < V; ++v) {
-                    const uint4 wv = ld_shared_v4(wrow + v * kSRB);
-                    const float2 d = chunk_dot<EH>(wv, xv);
-                    acc[v] = PC ? fadd2(acc[v], d) : ffma2(d, make_float2(sc[v], sc[v]), acc[v]);
+                for (int h = 0; h < 2; ++h) {
+                    const int c = ks * kSC + h * 16 + j;
+                    uint4 xu[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) xu[i] = ld_shared_v4(x_unit(xa, c, i));
+                    float sc[V];
+                    if (!PC) stage_scales<V, F16>(sb + s_off[h], sc);
+                    const uint32_t wrow = sb + w_off + h * 256;
+#pragma unroll
+                    for (int v = 0; v < V; ++v) {
+                        const uint4 wv = ld_shared_v4(wrow + v * kSRB);
+                        const float t = chunk_dot_f32<EH>(wv, xu);
+                        acc[v] = PC ? acc[v] + t : fmaf(t, sc[v], acc[v]);
+                    }
                 }
             }
         }
@@ -397,16 +568,16 @@ __global__ void __launch_bounds__(kThreadsG, 2)
         const int blk = cur.blk;
         const int part = cur.part;
         if (cur.advance(a)) {
-            // Item done: undo the factor 16 of the high-nibble lane, reduce the 16 chunk
-            // lanes of each row; store (or hand the partial to the last item).
+            // Item done: reduce the 16 chunk lanes of each row; store (or hand the partial
+            // to the last item).
             float tot[V];
 #pragma unroll
             for (int v = 0; v < V; ++v) {
-                tot[v] = EH ? fmaf(acc[v].x, 0.0625f, acc[v].y) : fmaf(acc[v].y, 0.0625f, acc[v].x);
+                tot[v] = acc[v];
 #pragma unroll
                 for (int o = 1; o < 16; o <<= 1)
                     tot[v] += __shfl_xor_sync(0xffffffffu, tot[v], o);
-                acc[v] = make_float2(0.f, 0.f);
+                acc[v] = 0.f;
             }
             float mine = tot[0];
 #pragma unroll
@@ -431,13 +602,13 @@ __global__ void __launch_bounds__(kThreadsG, 2)
                 if (finish) {
                     if (j < V) {
                         // All parts' loads in flight together (parts <= 8); added in order.
-                        float t[8];
+                        float t[kGemvMaxParts];
 #pragma unroll
-                        for (int q = 0; q < 8; ++q)
+                        for (int q = 0; q < kGemvMaxParts; ++q)
                             t[q] = q < a.parts ? __ldcg(a.ws + (int64_t)q * a.ws_rows + vrow) : 0.f;
                         mine = t[0];
 #pragma unroll
-                        for (int q = 1; q < 8; ++q)
+                        for (int q = 1; q < kGemvMaxParts; ++q)
                             if (q < a.parts) mine += t[q];
                     }
                     if (threadIdx.x == 0) a.tickets[blk] = 0;
@@ -452,14 +623,15 @@ __global__ void __launch_bounds__(kThreadsG, 2)
     }
 }
 
-template <int V, bool EH, bool PC, bool F16>
-cudaError_t launch_v(const TensorMaps& tm, const GArgs& a, unsigned grid, const LaunchCtx& c) {
-    const cudaError_t attr = kernel_smem_once<gemv_tma_kernel<V, EH, PC, F16>>(kCtaSmem, 100);
+template <int V, bool EH, bool PC, bool F16, bool X8>
+cudaError_t launch_v(const TensorMaps& tm, const GArgs& a, unsigned grid, uint32_t smem,
+                     const LaunchCtx& c) {
+    const cudaError_t attr = kernel_smem_once<gemv_tma_kernel<V, EH, PC, F16, X8>>(kCtaSmem, 100);
     if (attr != cudaSuccess) return attr;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kThreadsG);
-    cfg.dynamicSmemBytes = smem_bytes_g(a.stages, a.stage_bytes, a.x_chunks);
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = c.stream;
     cudaLaunchAttribute attrs[1];
     if (c.pdl) {
@@ -468,31 +640,38 @@ cudaError_t launch_v(const TensorMaps& tm, const GArgs& a, unsigned grid, const 
         cfg.attrs = attrs;
         cfg.numAttrs = 1;
     }
-    return cudaLaunchKernelEx(&cfg, gemv_tma_kernel<V, EH, PC, F16>, tm, a);
+    return cudaLaunchKernelEx(&cfg, gemv_tma_kernel<V, EH, PC, F16, X8>, tm, a);
 }
 
+template <int V, bool EH, bool PC, bool F16>
+cudaError_t dispatch_x8(bool x8, const TensorMaps& tm, const GArgs& a, unsigned grid,
+                        uint32_t smem, const LaunchCtx& c) {
+    return x8 ? launch_v<V, EH, PC, F16, true>(tm, a, grid, smem, c)
+              : launch_v<V, EH, PC, F16, false>(tm, a, grid, smem, c);
+}
 template <int V, bool EH, bool PC>
-cudaError_t dispatch_f16(bool f16, const TensorMaps& tm, const GArgs& a, unsigned grid,
-                         const LaunchCtx& c) {
-    return f16 ? launch_v<V, EH, PC, true>(tm, a, grid, c) : launch_v<V, EH, PC, false>(tm, a, grid, c);
+cudaError_t dispatch_f16(bool f16, bool x8, const TensorMaps& tm, const GArgs& a, unsigned grid,
+                         uint32_t smem, const LaunchCtx& c) {
+    return f16 ? dispatch_x8<V, EH, PC, true>(x8, tm, a, grid, smem, c)
+               : dispatch_x8<V, EH, PC, false>(x8, tm, a, grid, smem, c);
 }
 template <int V, bool EH>
-cudaError_t dispatch_pc(bool pc, bool f16, const TensorMaps& tm, const GArgs& a, unsigned grid,
-                        const LaunchCtx& c) {
-    return pc ? dispatch_f16<V, EH, true>(f16, tm, a, grid, c)
-              : dispatch_f16<V, EH, false>(f16, tm, a, grid, c);
+cudaError_t dispatch_pc(bool pc, bool f16, bool x8, const TensorMaps& tm, const GArgs& a,
+                        unsigned grid, uint32_t smem, const LaunchCtx& c) {
+    return pc ? dispatch_f16<V, EH, true>(f16, x8, tm, a, grid, smem, c)
+              : dispatch_f16<V, EH, false>(f16, x8, tm, a, grid, smem, c);
 }
 template <int V>
-cudaError_t dispatch_eh(bool eh, bool pc, bool f16, const TensorMaps& tm, const GArgs& a,
-                        unsigned grid, const LaunchCtx& c) {
-    return eh ? dispatch_pc<V, true>(pc, f16, tm, a, grid, c)
-              : dispatch_pc<V, false>(pc, f16, tm, a, grid, c);
+cudaError_t dispatch_eh(bool eh, bool pc, bool f16, bool x8, const TensorMaps& tm,
+                        const GArgs& a, unsigned grid, uint32_t smem, const LaunchCtx& c) {
+    return eh ? dispatch_pc<V, true>(pc, f16, x8, tm, a, grid, smem, c)
+              : dispatch_pc<V, false>(pc, f16, x8, tm, a, grid, smem, c);
 }
-cudaError_t dispatch_v(int V, bool eh, bool pc, bool f16, const TensorMaps& tm, const GArgs& a,
-                       unsigned grid, const LaunchCtx& c) {
-    if (V == 4) return dispatch_eh<4>(eh, pc, f16, tm, a, grid, c);
-    if (V == 2) return dispatch_eh<2>(eh, pc, f16, tm, a, grid, c);
-    return dispatch_eh<1>(eh, pc, f16, tm, a, grid, c);
+cudaError_t dispatch_v(int V, bool eh, bool pc, bool f16, bool x8, const TensorMaps& tm,
+                       const GArgs& a, unsigned grid, uint32_t smem, const LaunchCtx& c) {
+    if (V == 4) return dispatch_eh<4>(eh, pc, f16, x8, tm, a, grid, smem, c);
+    if (V == 2) return dispatch_eh<2>(eh, pc, f16, x8, tm, a, grid, smem, c);
+    return dispatch_eh<1>(eh, pc, f16, x8, tm, a, grid, smem, c);
 }
 
 int log2_exact(int64_t v) {
@@ -505,9 +684,8 @@ int log2_exact(int64_t v) {
 uint32_t stage_bytes_for(int V, bool pc, int esz, int gs_shift, uint32_t* scale_off,
                          uint32_t* tx) {
     const int rb = kRowGroups * V;
-    const uint32_t wbytes = (uint32_t)(rb * stage_row_bytes(V));
-    const int sc_log = chunk_cols(V) == 1 ? 4 : 5;  // log2(chunks per stage)
-    const int gps = pc ? 0 : (gs_shift >= sc_log ? 1 : stage_chunks(V) >> gs_shift);
+    const uint32_t wbytes = (uint32_t)(rb * kSRB);
+    const int gps = pc ? 0 : (gs_shift >= 5 ? 1 : kSC >> gs_shift);
     const uint32_t sbytes = (uint32_t)(gps * rb * esz);
     *scale_off = wbytes;
     *tx = wbytes + sbytes;
@@ -534,7 +712,7 @@ EncodeTiledFn tensor_map_encoder() {
 
 bool gemv_tma_eligible(const Problem& p) {
     if (p.M != 1 || p.K % 32 != 0 || p.K < 512 || p.N < 16) return false;
-    if (p.N > (1LL << 30) || p.K > (1LL << 24)) return false;
+    if (p.N > (1LL << 30) || p.K > (int64_t)kMaxXStages * 1024) return false;
     if (reinterpret_cast<uintptr_t>(p.x) % 16 || reinterpret_cast<uintptr_t>(p.qweight) % 16)
         return false;
     const bool pc = p.group_size >= p.K;
@@ -546,11 +724,11 @@ bool gemv_tma_eligible(const Problem& p) {
         if (reinterpret_cast<uintptr_t>(p.scales) % 16 || (p.N * esz) % 16 != 0) return false;
     }
     // x staged whole, plus at least two stages of the smallest tile.
-    const int x_chunks = (int)((p.K + 1023) / 1024) * stage_chunks(1);
+    const int kstages = (int)((p.K + 1023) / 1024);
     uint32_t so, tx;
     const uint32_t sb1 = stage_bytes_for(1, pc, p.scale_f16 ? 2 : 4,
                                          pc ? 0 : log2_exact(p.group_size / 32), &so, &tx);
-    if (smem_bytes_g(2, sb1, x_chunks) > kCtaSmem) return false;
+    if (smem_layout(2, sb1, kstages).total > (uint32_t)kCtaSmem) return false;
     return tensor_map_encoder() != nullptr;
 }
 
@@ -569,11 +747,7 @@ cudaError_t gemv_tma_launch_group(const Problem* ps, int count, const LaunchCtx&
     const bool pc = p0.group_size >= p0.K;
     const int esz = p0.scale_f16 ? 2 : 4;
     const int gs_shift = pc ? 0 : log2_exact(p0.group_size / 32);
-    auto kstages_for = [&](int V) {
-        const int sk = 512 * chunk_cols(V);
-        return (int)((p0.K + sk - 1) / sk);
-    };
-    auto x_chunks_for = [&](int V) { return kstages_for(V) * stage_chunks(V); };
+    const int kstages = (int)((p0.K + 1023) / 1024);
     const int slots = 2 * c.sm_count;
     auto blocks_for = [&](int V) {
         int64_t b = 0;
@@ -583,7 +757,7 @@ cudaError_t gemv_tma_launch_group(const Problem* ps, int count, const LaunchCtx&
     auto stages_for = [&](int V) {
         uint32_t so, tx;
         const uint32_t sb = stage_bytes_for(V, pc, esz, gs_shift, &so, &tx);
-        const int room = kCtaSmem - smem_bytes_g(0, sb, x_chunks_for(V));
+        const int room = kCtaSmem - (int)smem_layout(0, sb, kstages).total;
         return std::min<int>(kMaxStages, room / (int)sb);
     };
     // Tile shape (V rows per thread) and split-K parts from a cost model of the critical
@@ -599,15 +773,14 @@ cudaError_t gemv_tma_launch_group(const Problem* ps, int count, const LaunchCtx&
         const int64_t blocks_v = blocks_for(v);
         const double eff = v == 1 ? 1.4 : (v == 2 ? 1.1 : 1.0);
         for (int parts = 1; parts <= kGemvMaxParts; parts *= 2) {
-            const int kstages = kstages_for(v);
-            if (parts > 1 && (kstages * 512 * chunk_cols(v) / parts < 2048 || !c.ws || !c.tickets ||
+            if (parts > 1 && (kstages * 1024 / parts < 2048 || !c.ws || !c.tickets ||
                               (int64_t)parts * blocks_v * kRowGroups * v > c.ws_floats ||
                               blocks_v > c.ticket_count))
                 break;
             const int tpp = (kstages + parts - 1) / parts;
             const int64_t items = blocks_v * ((kstages + tpp - 1) / tpp);
             const double waves = (double)((items + slots - 1) / slots);
-            const double kib = (double)kRowGroups * v * tpp * stage_row_bytes(v) / 1024.0;
+            const double kib = (double)kRowGroups * v * tpp * kSRB / 1024.0;
             const double cost = waves * (0.06 * kib * eff + (parts > 1 ? 2.1 : 0.0));
             if (cost < best * 0.999) best = cost, V = v, best_parts = parts;
         }
@@ -617,13 +790,15 @@ cudaError_t gemv_tma_launch_group(const Problem* ps, int count, const LaunchCtx&
     a.x = p0.x;
     a.nmat = count;
     a.K = p0.K;
-    const int kstages = kstages_for(V);
     a.kstages = kstages;
-    a.x_chunks = x_chunks_for(V);
     a.gs_shift = gs_shift;
     a.stage_bytes = stage_bytes_for(V, pc, esz, gs_shift, &a.scale_off, &a.stage_tx);
     a.stages = stages_for(V);
     if (a.stages < 2) return cudaErrorNotSupported;
+    const SmemLayout lay = smem_layout(a.stages, a.stage_bytes, kstages);
+    a.x_off = lay.x_off;
+    a.meta_off = lay.meta_off;
+    a.bar_off = lay.bar_off;
     a.status = c.status_word;
     a.wait_ns = c.wait_limit_ns;
     TensorMaps tm;
@@ -639,7 +814,7 @@ cudaError_t gemv_tma_launch_group(const Problem* ps, int count, const LaunchCtx&
         {
             const cuuint64_t dims[2] = {(cuuint64_t)(p.K / 4), (cuuint64_t)p.N};
             const cuuint64_t strides[1] = {(cuuint64_t)(p.K / 2)};
-            const cuuint32_t box[2] = {(cuuint32_t)(stage_row_bytes(V) / 2), (cuuint32_t)rb};
+            const cuuint32_t box[2] = {(cuuint32_t)(kSRB / 2), (cuuint32_t)rb};
             const cuuint32_t estr[2] = {1, 1};
             if (enc(&tm.w[i], CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<uint8_t*>(p.qweight),
                     dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -649,8 +824,7 @@ cudaError_t gemv_tma_launch_group(const Problem* ps, int count, const LaunchCtx&
         }
         if (!pc) {
             const int64_t G = (p.K + p.group_size - 1) / p.group_size;
-            const int sc_log = chunk_cols(V) == 1 ? 4 : 5;
-            const int gps = gs_shift >= sc_log ? 1 : stage_chunks(V) >> gs_shift;
+            const int gps = gs_shift >= 5 ? 1 : kSC >> gs_shift;
             const cuuint64_t dims[2] = {(cuuint64_t)p.N, (cuuint64_t)G};
             const cuuint64_t strides[1] = {(cuuint64_t)(p.N * esz)};
             const cuuint32_t box[2] = {(cuuint32_t)rb, (cuuint32_t)gps};
@@ -684,7 +858,12 @@ cudaError_t gemv_tma_launch_group(const Problem* ps, int count, const LaunchCtx&
     a.tickets = c.tickets;
     a.ws_rows = blocks * rb;
     const unsigned grid = (unsigned)std::min<int64_t>(a.items, slots);
-    return dispatch_v(V, p0.even_high != 0, pc, p0.scale_f16 != 0, tm, a, grid, c);
+    // Fixed-point dp4a arithmetic where its per-CTA conversion of x pays off: each CTA
+    // converts the x stages it uses once, which the cheaper inner loop repays only over
+    // about four row blocks per CTA (measured on the decode tokens: vocabulary-sized
+    // heads gain 5-10 %; gate/up with three blocks per CTA is 2-4 % slower).
+    const bool x8 = a.items >= 4 * (int64_t)grid;
+    return dispatch_v(V, p0.even_high != 0, pc, p0.scale_f16 != 0, x8, tm, a, grid, lay.total, c);
 }
 
 cudaError_t gemv_tma_launch(const Problem& p, const LaunchCtx& c) {

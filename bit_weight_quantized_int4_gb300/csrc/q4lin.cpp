@@ -26,6 +26,7 @@ struct q4lin_handle {
     int pdl = 0;
     int64_t wait_limit = 0;  // ns; 0: default
     int tc_skip_first_copy = 0;
+    int tc_f16 = 0;
     int* d_status = nullptr;
     float* d_ws = nullptr;     // split-K partial sums
     int* d_tickets = nullptr;  // split-K row-block counters (zero between launches)
@@ -35,7 +36,7 @@ namespace {
 
 constexpr int64_t kDefaultWaitLimit = 2000000000LL;  // 2 s of GPU global time
 // Scratch of a handle: partial sums of split-K launches and their row-block counters.
-constexpr int64_t kWsFloats = 1 << 23;   // 32 MiB (split-K partials: GEMV, backward, TC)
+constexpr int64_t kWsFloats = 1 << 24;   // 64 MiB (split-K partials; the fp16 copy of x)
 constexpr int64_t kTickets = 1 << 14;    // 64 KiB
 
 // M-dispatch between the CUDA-core kernels (the row-streaming kernel, which re-reads the
@@ -139,6 +140,7 @@ q4lin::LaunchCtx make_ctx(q4lin_handle_t h, cudaStream_t stream) {
     c.status_word = h->d_status;
     c.wait_limit_ns = h->wait_limit > 0 ? h->wait_limit : kDefaultWaitLimit;
     c.tc_skip_first_copy = h->tc_skip_first_copy;
+    c.tc_f16 = h->tc_f16;
     c.ws = h->d_ws;
     c.ws_floats = kWsFloats;
     c.tickets = h->d_tickets;
@@ -176,9 +178,9 @@ q4lin_status_t plan(q4lin_handle_t h, const q4lin::Problem& p, const q4lin::Laun
 }
 
 // The kernel behind a path for an M >= 1, N >= 1 problem (the dispatch of q4lin_run).
-int kernel_of(const q4lin::Problem& p, int path) {
+int kernel_of(const q4lin::Problem& p, const q4lin::LaunchCtx& c, int path) {
     switch (path) {
-        case Q4LIN_PATH_TC: return Q4LIN_KERNEL_TC;
+        case Q4LIN_PATH_TC: return q4lin::tc_uses_f16(p, c) ? Q4LIN_KERNEL_TC_F16 : Q4LIN_KERNEL_TC;
         case Q4LIN_PATH_GEMV:
             return q4lin::gemv_tma_eligible(p) ? Q4LIN_KERNEL_GEMV_TMA
                    : multirow_preferred(p)     ? Q4LIN_KERNEL_MULTIROW
@@ -275,9 +277,10 @@ q4lin_status_t q4lin_plan_kernel(q4lin_handle_t h, const float* x, const uint8_t
         return Q4LIN_OK;
     }
     int path = 0;
-    st = plan(h, p, make_ctx(h, nullptr), &path);
+    const q4lin::LaunchCtx c = make_ctx(h, nullptr);
+    st = plan(h, p, c, &path);
     if (st != Q4LIN_OK) return st;
-    *kernel_out = kernel_of(p, path);
+    *kernel_out = kernel_of(p, c, path);
     return Q4LIN_OK;
 }
 
@@ -297,8 +300,9 @@ q4lin_status_t q4lin_run(q4lin_handle_t h, const float* x, const uint8_t* qweigh
     DeviceGuard g(h->device);
     if (!g.ok()) return Q4LIN_ERR_CUDA;
     cudaError_t err;
-    switch (kernel_of(p, path)) {
-        case Q4LIN_KERNEL_TC: err = q4lin::tc_launch(p, c); break;
+    switch (kernel_of(p, c, path)) {
+        case Q4LIN_KERNEL_TC:
+        case Q4LIN_KERNEL_TC_F16: err = q4lin::tc_launch(p, c); break;
         case Q4LIN_KERNEL_GEMV_TMA: err = q4lin::gemv_tma_launch(p, c); break;
         case Q4LIN_KERNEL_MULTIROW: err = q4lin::gemv_mr_launch(p, c); break;
         case Q4LIN_KERNEL_ROWSTREAM: err = q4lin::rowstream_launch(p, c); break;
@@ -490,6 +494,10 @@ q4lin_status_t q4lin_set_option(q4lin_handle_t h, int option, int64_t value) {
             if (value != 0 && value != 1) return Q4LIN_ERR_INVALID_ARG;
             h->tc_skip_first_copy = (int)value;
             return Q4LIN_OK;
+        case Q4LIN_OPT_TC_F16:
+            if (value != 0 && value != 1) return Q4LIN_ERR_INVALID_ARG;
+            h->tc_f16 = (int)value;
+            return Q4LIN_OK;
         default:
             return Q4LIN_ERR_INVALID_ARG;
     }
@@ -505,6 +513,7 @@ q4lin_status_t q4lin_get_option(q4lin_handle_t h, int option, int64_t* value) {
             return Q4LIN_OK;
         case Q4LIN_OPT_PDL: *value = h->pdl; return Q4LIN_OK;
         case Q4LIN_OPT_TC_SKIP_FIRST_COPY: *value = h->tc_skip_first_copy; return Q4LIN_OK;
+        case Q4LIN_OPT_TC_F16: *value = h->tc_f16; return Q4LIN_OK;
         default: return Q4LIN_ERR_INVALID_ARG;
     }
 }

@@ -58,6 +58,7 @@ struct LaunchCtx {
     int* status_word;        // device int, first nonzero code a kernel records
     int64_t wait_limit_ns;   // time limit of bounded device-side waits
     int tc_skip_first_copy;  // test hook: the TC producer skips stage 0
+    int tc_f16;              // tensor-core GEMM with fp16 operands
     float* ws;               // scratch for split-K partial sums (may be null)
     int64_t ws_floats;
     int* tickets;            // per-row-block counters, zero between launches (may be null)
@@ -121,6 +122,9 @@ cudaError_t requant_launch(const RequantProblem& p, const LaunchCtx& c);
 
 // tcgen05 tensor-core GEMM.  Eligibility and launch live in tc_gemm.cu.
 bool tc_eligible(const Problem& p, const LaunchCtx& c);
+// Whether tc_launch multiplies fp16 operands for this problem (the option is set and the
+// fp16 copy of x fits the scratch).
+bool tc_uses_f16(const Problem& p, const LaunchCtx& c);
 cudaError_t tc_launch(const Problem& p, const LaunchCtx& c);
 
 }  // namespace q4lin

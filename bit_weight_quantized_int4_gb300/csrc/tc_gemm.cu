@@ -98,15 +98,16 @@ constexpr uint32_t kTmemCols = 512;
 constexpr int64_t kDrainNs = 4000000000LL;
 constexpr int kSmemLimit = 227 * 1024;
 
-// A stage of x: two boxes [bt rows x 128 B] (1024-byte aligned for the swizzle).
-__host__ __device__ constexpr int stage_bytes(int bt) { return bt * 256; }
+// A stage of x: two boxes [bt rows x 128 B] of fp32 (1024-byte aligned for the swizzle),
+// or one box [bt rows x 128 B] of fp16 for the fp16-operand kernel.
+__host__ __device__ constexpr int stage_bytes(int bt, bool h16) { return h16 ? bt * 128 : bt * 256; }
 // Shared memory: alignment slack, the x ring, the weight ring, barriers (256 bytes); never
 // less than 116 KiB, so that one CTA of this kernel holds an SM (it allocates all 512
 // tensor-memory columns: a second one on the SM would block in tcgen05.alloc, and with
 // clusters two such CTAs could wait on each other's peers).
 constexpr int kOneCtaSmem = 116 * 1024;
-inline int smem_bytes(int bt, int stages) {
-    return std::max(1024 + stages * stage_bytes(bt) + kWSlots * kWBlkBytes + 256, kOneCtaSmem);
+inline int smem_bytes(int bt, int stages, bool h16) {
+    return std::max(1024 + stages * stage_bytes(bt, h16) + kWSlots * kWBlkBytes + 256, kOneCtaSmem);
 }
 
 struct Tc2Args {
@@ -161,7 +162,40 @@ __device__ __forceinline__ void dequant_chunk(const uint4 wv, float sc, uint32_t
     }
 }
 
-template <bool EH, bool DUAL>
+// fp16 pairs (even k in the low half) of the 32 values of dequant_chunk.
+template <bool EH>
+__device__ __forceinline__ void dequant_chunk_h16(const uint4 wv, float sc, uint32_t* pairs) {
+    uint32_t vals[32];
+    dequant_chunk<EH>(wv, sc, vals);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const __half2 h = __floats2half2_rn(__uint_as_float(vals[2 * i]), __uint_as_float(vals[2 * i + 1]));
+        pairs[i] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+}
+
+// x fp32 -> fp16 (round to nearest even) for the fp16-operand GEMM, into the handle's
+// scratch; code 2 in the status word when a finite value is outside the fp16 range
+// (|x| >= 65520 rounds to infinity).  Under programmatic dependent launch the GEMM may
+// start streaming its weights at once; it reads this kernel's output only after its own
+// dependency wait (this grid's completion).
+__global__ void __launch_bounds__(256) x_to_f16_kernel(const float4* __restrict__ x,
+                                                       uint2* __restrict__ y, int64_t n4,
+                                                       int* status) {
+    griddep_launch_dependents();
+    griddep_wait();
+    bool bad = false;
+    for (int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x; i < n4; i += (int64_t)gridDim.x * 256) {
+        const float4 v = __ldg(x + i);
+        bad |= (fabsf(v.x) >= 65520.f && isfinite(v.x)) || (fabsf(v.y) >= 65520.f && isfinite(v.y)) ||
+               (fabsf(v.z) >= 65520.f && isfinite(v.z)) || (fabsf(v.w) >= 65520.f && isfinite(v.w));
+        const __half2 a = __floats2half2_rn(v.x, v.y), b = __floats2half2_rn(v.z, v.w);
+        y[i] = make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
+    }
+    if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) atomicCAS(status, 0, 2);
+}
+
+template <bool EH, bool DUAL, bool H16>
 __global__ void __launch_bounds__(kernel_threads(DUAL), 1)
     tc_wa_kernel(const __grid_constant__ CUtensorMap tmap_x,
                  const __grid_constant__ CUtensorMap tmap_xl,
@@ -173,7 +207,7 @@ __global__ void __launch_bounds__(kernel_threads(DUAL), 1)
     uint8_t* gbase = smem_raw + (base - raw);
     const int bt = a.bt, S = a.stages;
     const uint32_t xbox = (uint32_t)bt * 128;
-    const uint32_t sbytes = (uint32_t)stage_bytes(bt);
+    const uint32_t sbytes = (uint32_t)stage_bytes(bt, H16);
     const uint32_t wring = base + (uint32_t)S * sbytes;
     const uint32_t bar_base = wring + (uint32_t)(kWSlots * kWBlkBytes);
     const uint32_t accfull = bar_base + 8 * (3 * kMaxStages + 2 * kWSlots);
@@ -205,7 +239,7 @@ __global__ void __launch_bounds__(kernel_threads(DUAL), 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(full(s), alt ? 1 : 2);  // one producer a stage, or one a box
+            mbar_init(full(s), (alt || H16) ? 1 : 2);  // one producer a stage, or one a box
             mbar_init(aready(s), 128);  // the 128 threads of the group that owns the stage
             mbar_init(empty(s), 1);
         }
@@ -243,6 +277,7 @@ __global__ void __launch_bounds__(kernel_threads(DUAL), 1)
             griddep_wait();
             // Stages of this producer: every stage (box pr) or, with alt, stages pr,
             // pr + 2, ... (both boxes).  Slot and phase kept incrementally.
+            // (fp16 operands: a stage is one box; without alt producer 0 takes them all.)
             const int first = alt ? pr : 0, stride = alt ? 2 : 1;
             int s = 0;
             uint32_t ph = 0;  // parity of the slot's current use
@@ -251,7 +286,8 @@ __global__ void __launch_bounds__(kernel_threads(DUAL), 1)
             };
             for (int q = 0; q < first; ++q) step();
             int li = first;
-            for (; li < n_iters; li += stride) {
+            const int li_end = (H16 && !alt && pr == 1) ? 0 : n_iters;
+            for (; li < li_end; li += stride) {
                 if (li >= S && !wait_bounded(empty(s), ph ^ 1u, a.wait_ns, failed)) {
                     record_failure(a.status, failed);
                     break;
@@ -260,7 +296,11 @@ __global__ void __launch_bounds__(kernel_threads(DUAL), 1)
                 if (!(a.skip_first_copy && li == 0)) {
                     const int64_t k = (int64_t)(it_begin + li) * kStageK;
                     const bool two = k + kHalfK < a.K;  // else the last stage has one half
-                    if (alt) {
+                    if (H16) {
+                        // [rows x 64 k] of fp16; k past K reads as zeros.
+                        mbar_arrive_expect_tx(full(s), xtx);
+                        tma_load_2d(xslot(s), xmap, (int)k, (int)m0, full(s));
+                    } else if (alt) {
                         mbar_arrive_expect_tx(full(s), two ? 2 * xtx : xtx);
                         tma_load_2d(xslot(s), xmap, (int)k, (int)m0, full(s));
                         if (two)
@@ -278,7 +318,7 @@ __global__ void __launch_bounds__(kernel_threads(DUAL), 1)
             }
             // Copies of this producer's last stages may still be landing; the CTA must not
             // exit first.  (Its stages among the last S are the latest uses of their slots.)
-            for (int q = li - stride; q >= first && q >= li - S; q -= stride) {
+            for (int q = li - stride; li_end > 0 && q >= first && q >= li - S; q -= stride) {
                 if (a.skip_first_copy && q == 0) continue;
                 wait_bounded(full(q % S), (q / S) & 1, kDrainNs, nullptr);
             }
@@ -307,7 +347,7 @@ __global__ void __launch_bounds__(kernel_threads(DUAL), 1)
         if (lane == 0) {
             // ------------------------------------------------------------ MMA issuers
             const int is = warp == 1 ? 0 : 1;
-            const uint32_t idesc = tf32_idesc(kWRows, bt);
+            const uint32_t idesc = H16 ? f16_idesc(kWRows, bt) : tf32_idesc(kWRows, bt);
             const int64_t k_two = a.K - kHalfK - (int64_t)it_begin * kStageK;
             const uint32_t dacc = tmem_d + (dual ? (uint32_t)(is * bt) : 0u);
             // Stages of this issuer: all (issuer 0, single), or is, is + 2, ... (dual).
@@ -331,11 +371,20 @@ __global__ void __launch_bounds__(kernel_threads(DUAL), 1)
                 // swizzle row, +xbox / 16 for the second box.
                 const uint32_t acol = tmem_d + (uint32_t)(kACol0 + kStageK * s);
                 const uint64_t d0 = sw128_desc(xslot(s));
+                if (H16) {
+                    // 4 MMAs of K = 16 (8 tensor-memory columns of fp16 pairs, 32 bytes along
+                    // the swizzle row each).  A missing second half is zeros in both operands.
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_tf32_ts(dacc, acol + 8 * kk, d0 + (uint64_t)(2 * kk), idesc,
-                                (it != first) || kk != 0);
-                if ((int64_t)it * kStageK < k_two) {
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_f16_ts(dacc, acol + 8 * kk, d0 + (uint64_t)(2 * kk), idesc,
+                                   (it != first) || kk != 0);
+                } else {
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_tf32_ts(dacc, acol + 8 * kk, d0 + (uint64_t)(2 * kk), idesc,
+                                    (it != first) || kk != 0);
+                }
+                if (!H16 && (int64_t)it * kStageK < k_two) {
                     const uint64_t d1 = d0 + (uint64_t)(xbox >> 4);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
@@ -416,11 +465,25 @@ __global__ void __launch_bounds__(kernel_threads(DUAL), 1)
                 }
                 const uint32_t acol = lane_base + (uint32_t)(kACol0 + kStageK * s);
                 uint32_t vals[32];
-                dequant_chunk<EH>(w0, sc0, vals);
-                tmem_st32_async(acol, vals);
-                if (second) {
-                    dequant_chunk<EH>(w1, sc1, vals);
-                    tmem_st32_async(acol + kHalfK, vals);
+                if (H16) {
+                    // 64 values as 32 fp16 pairs (zeros for a missing second half); a scale
+                    // that would take (code - 8) * scale past the fp16 range is reported.
+                    if (fabsf(sc0) > 8188.f || fabsf(sc1) > 8188.f) atomicCAS(a.status, 0, 2);
+                    dequant_chunk_h16<EH>(w0, sc0, vals);
+                    if (second) {
+                        dequant_chunk_h16<EH>(w1, sc1, vals + 16);
+                    } else {
+#pragma unroll
+                        for (int i = 16; i < 32; ++i) vals[i] = 0u;
+                    }
+                    tmem_st32_async(acol, vals);
+                } else {
+                    dequant_chunk<EH>(w0, sc0, vals);
+                    tmem_st32_async(acol, vals);
+                    if (second) {
+                        dequant_chunk<EH>(w1, sc1, vals);
+                        tmem_st32_async(acol + kHalfK, vals);
+                    }
                 }
                 ring[u][0] = fetch(it + stride, 0);
                 ring[u][1] = fetch(it + stride, 1);
@@ -550,15 +613,15 @@ __global__ void __launch_bounds__(kernel_threads(DUAL), 1)
     }
 }
 
-template <bool EH, bool DUAL>
+template <bool EH, bool DUAL, bool H16>
 cudaError_t kernel_attr() {
-    return kernel_smem_once<tc_wa_kernel<EH, DUAL>>(kSmemLimit);
+    return kernel_smem_once<tc_wa_kernel<EH, DUAL, H16>>(kSmemLimit);
 }
 
-int stages_for_bt(int bt, const LaunchCtx& c) {
-    int stages =
-        std::min(kMaxStages, (kSmemLimit - 1024 - 256 - kWSlots * kWBlkBytes) / stage_bytes(bt));
-    while (stages > 2 && smem_bytes(bt, stages) > c.max_smem_optin) --stages;
+int stages_for_bt(int bt, bool h16, const LaunchCtx& c) {
+    int stages = std::min(kMaxStages,
+                          (kSmemLimit - 1024 - 256 - kWSlots * kWBlkBytes) / stage_bytes(bt, h16));
+    while (stages > 2 && smem_bytes(bt, stages, h16) > c.max_smem_optin) --stages;
     return stages;
 }
 
@@ -580,7 +643,7 @@ int max_active_clusters(int bt, int P, const LaunchCtx& c) {
     cfg.gridDim = dim3((unsigned)(P * 64));
     const bool dual = bt <= 128;
     cfg.blockDim = dim3(kernel_threads(dual));
-    cfg.dynamicSmemBytes = smem_bytes(bt, stages_for_bt(bt, c));
+    cfg.dynamicSmemBytes = smem_bytes(bt, stages_for_bt(bt, false, c), false);
     cudaLaunchAttribute at;
     at.id = cudaLaunchAttributeClusterDimension;
     at.val.clusterDim.x = (unsigned)P;
@@ -590,10 +653,10 @@ int max_active_clusters(int bt, int P, const LaunchCtx& c) {
     cfg.numAttrs = 1;
     int n = 0;
     cudaError_t e = cudaErrorUnknown;
-    if (dual && kernel_attr<false, true>() == cudaSuccess)
-        e = cudaOccupancyMaxActiveClusters(&n, tc_wa_kernel<false, true>, &cfg);
-    else if (!dual && kernel_attr<false, false>() == cudaSuccess)
-        e = cudaOccupancyMaxActiveClusters(&n, tc_wa_kernel<false, false>, &cfg);
+    if (dual && kernel_attr<false, true, false>() == cudaSuccess)
+        e = cudaOccupancyMaxActiveClusters(&n, tc_wa_kernel<false, true, false>, &cfg);
+    else if (!dual && kernel_attr<false, false, false>() == cudaSuccess)
+        e = cudaOccupancyMaxActiveClusters(&n, tc_wa_kernel<false, false, false>, &cfg);
     if (e != cudaSuccess) {
         cudaGetLastError();
         n = 0;
@@ -602,15 +665,15 @@ int max_active_clusters(int bt, int P, const LaunchCtx& c) {
     return n;
 }
 
-template <bool EH, bool DUAL>
+template <bool EH, bool DUAL, bool H16>
 cudaError_t launch2(const CUtensorMap& tx, const CUtensorMap& txl, const CUtensorMap& tw,
                     const Tc2Args& a, dim3 grid, const LaunchCtx& c) {
-    const cudaError_t attr = kernel_attr<EH, DUAL>();
+    const cudaError_t attr = kernel_attr<EH, DUAL, H16>();
     if (attr != cudaSuccess) return attr;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(kernel_threads(DUAL));
-    cfg.dynamicSmemBytes = smem_bytes(a.bt, a.stages);
+    cfg.dynamicSmemBytes = smem_bytes(a.bt, a.stages, H16);
     cfg.stream = c.stream;
     cudaLaunchAttribute attrs[2];
     int na = 0;
@@ -628,8 +691,29 @@ cudaError_t launch2(const CUtensorMap& tx, const CUtensorMap& txl, const CUtenso
     }
     cfg.attrs = na ? attrs : nullptr;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, tc_wa_kernel<EH, DUAL>, tx, txl, tw, a);
+    return cudaLaunchKernelEx(&cfg, tc_wa_kernel<EH, DUAL, H16>, tx, txl, tw, a);
 }
+
+// The fp16 copy of x [M, K] in the handle's scratch, before the GEMM on the same stream.
+cudaError_t launch_x_to_f16(const Problem& p, uint2* y, const LaunchCtx& c) {
+    const int64_t n4 = p.M * p.K / 4;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)std::min<int64_t>((n4 + 255) / 256, 8LL * c.sm_count));
+    cfg.blockDim = dim3(256);
+    cfg.stream = c.stream;
+    cudaLaunchAttribute at[1];
+    if (c.pdl) {
+        at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        at[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = at;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, x_to_f16_kernel, reinterpret_cast<const float4*>(p.x), y, n4,
+                              c.status_word);
+}
+
+// Floats of the scratch the fp16 copy of x takes (rounded up to 256 bytes).
+int64_t x16_floats(const Problem& p) { return ((p.M * p.K * 2 + 255) / 256) * 64; }
 
 }  // namespace
 
@@ -639,13 +723,22 @@ bool tc_eligible(const Problem& p, const LaunchCtx& c) {
         return false;
     if (!(p.group_size >= p.K || p.group_size % kHalfK == 0)) return false;
     if (p.M > 65535LL * 64 || p.N > (1LL << 31) - 1) return false;
-    if (c.max_smem_optin < smem_bytes(256, 2)) return false;
+    if (c.max_smem_optin < smem_bytes(256, 2, false)) return false;
     return tensor_map_encoder() != nullptr;
+}
+
+bool tc_uses_f16(const Problem& p, const LaunchCtx& c) {
+    // The fp16 copy of x may take at most half of the scratch (the rest is left to the
+    // split-K exchange).
+    return c.tc_f16 && c.ws && x16_floats(p) <= c.ws_floats / 2;
 }
 
 cudaError_t tc_launch(const Problem& p, const LaunchCtx& c) {
     EncodeTiledFn enc = tensor_map_encoder();
     if (!enc) return cudaErrorNotSupported;
+    const bool h16 = tc_uses_f16(p, c);
+    float* const ws_split = h16 ? c.ws + x16_floats(p) : c.ws;
+    const int64_t ws_split_floats = h16 ? c.ws_floats - x16_floats(p) : c.ws_floats;
     // Activation rows per tile (the MMA's N) and the split of K over a cluster.  Wider
     // tiles make wider MMAs; narrower ones give more CTAs.  When the tiles alone leave SMs
     // idle, K is split over a cluster of P CTAs (a power of two up to 8, at least 4 stages
@@ -679,11 +772,11 @@ cudaError_t tc_launch(const Problem& p, const LaunchCtx& c) {
             splitk = P;
         }
     }
-    const int stages = stages_for_bt(bt, c);
+    const int stages = stages_for_bt(bt, h16, c);
     const int64_t mtiles = (p.M + bt - 1) / bt;
     // The split-K exchange ([tiles][P - 1][128][bt] floats) must fit in the workspace.
     while (splitk > 1 &&
-           (!c.ws || wtiles * mtiles * (splitk - 1) * kWRows * bt > c.ws_floats))
+           (!c.ws || wtiles * mtiles * (splitk - 1) * kWRows * bt > ws_split_floats))
         splitk /= 2;
 
     Tc2Args a;
@@ -701,7 +794,7 @@ cudaError_t tc_launch(const Problem& p, const LaunchCtx& c) {
     a.splitk = splitk;
     a.kpp = k_iters / splitk;
     a.sw = bt / splitk;
-    a.ws = c.ws;
+    a.ws = ws_split;
     a.gs_halves = a.per_channel ? 1 : (int)(p.group_size / kHalfK);
     a.gs_shift = -1;
     for (int sft = 0; sft < 31; ++sft)
@@ -714,11 +807,16 @@ cudaError_t tc_launch(const Problem& p, const LaunchCtx& c) {
 
     CUtensorMap tx, txl, tw;
     for (int last = 0; last < 2; ++last) {
+        // x [M, K]: fp32 boxes [rows x 32 k], or fp16 boxes [rows x 64 k] of the copy in the
+        // scratch; 128-byte rows either way.
         const cuuint64_t dims[2] = {(cuuint64_t)p.K, (cuuint64_t)p.M};
-        const cuuint64_t strides[1] = {(cuuint64_t)p.K * 4};
-        const cuuint32_t box[2] = {(cuuint32_t)kHalfK, (cuuint32_t)(last ? a.xrows_last : bt)};
+        const cuuint64_t strides[1] = {(cuuint64_t)p.K * (h16 ? 2 : 4)};
+        const cuuint32_t box[2] = {(cuuint32_t)(h16 ? kStageK : kHalfK),
+                                   (cuuint32_t)(last ? a.xrows_last : bt)};
         const cuuint32_t estr[2] = {1, 1};
-        if (enc(last ? &txl : &tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(p.x),
+        void* src = h16 ? static_cast<void*>(c.ws) : const_cast<float*>(p.x);
+        if (enc(last ? &txl : &tx,
+                h16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, src,
                 dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
@@ -736,11 +834,20 @@ cudaError_t tc_launch(const Problem& p, const LaunchCtx& c) {
             return cudaErrorInvalidValue;
     }
     const dim3 grid((unsigned)(wtiles * splitk), (unsigned)mtiles);
+    if (h16) {
+        const cudaError_t e = launch_x_to_f16(p, reinterpret_cast<uint2*>(c.ws), c);
+        if (e != cudaSuccess) return e;
+        if (bt <= 128)
+            return p.even_high ? launch2<true, true, true>(tx, txl, tw, a, grid, c)
+                               : launch2<false, true, true>(tx, txl, tw, a, grid, c);
+        return p.even_high ? launch2<true, false, true>(tx, txl, tw, a, grid, c)
+                           : launch2<false, false, true>(tx, txl, tw, a, grid, c);
+    }
     if (bt <= 128)
-        return p.even_high ? launch2<true, true>(tx, txl, tw, a, grid, c)
-                           : launch2<false, true>(tx, txl, tw, a, grid, c);
-    return p.even_high ? launch2<true, false>(tx, txl, tw, a, grid, c)
-                       : launch2<false, false>(tx, txl, tw, a, grid, c);
+        return p.even_high ? launch2<true, true, false>(tx, txl, tw, a, grid, c)
+                           : launch2<false, true, false>(tx, txl, tw, a, grid, c);
+    return p.even_high ? launch2<true, false, false>(tx, txl, tw, a, grid, c)
+                       : launch2<false, false, false>(tx, txl, tw, a, grid, c);
 }
 
 }  // namespace q4lin

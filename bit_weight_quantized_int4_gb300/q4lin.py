@@ -45,14 +45,16 @@ Q4LIN_KERNEL_MULTIROW = 2
 Q4LIN_KERNEL_ROWSTREAM = 3
 Q4LIN_KERNEL_GENERIC = 4
 Q4LIN_KERNEL_TC = 5
+Q4LIN_KERNEL_TC_F16 = 6
 KERNEL_NAMES = {0: "none", 1: "gemv_tma", 2: "multirow", 3: "rowstream", 4: "generic",
-                5: "tc"}
+                5: "tc", 6: "tc_f16"}
 
 Q4LIN_OPT_FORCE_PATH = 1
 Q4LIN_OPT_NIBBLE_EVEN_HIGH = 2
 Q4LIN_OPT_WAIT_LIMIT = 3
 Q4LIN_OPT_PDL = 4
 Q4LIN_OPT_TC_SKIP_FIRST_COPY = 5
+Q4LIN_OPT_TC_F16 = 6
 
 _vp, _i64, _i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
 

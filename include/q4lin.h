@@ -20,9 +20,10 @@
  * Conventions for every entry point:
  *   - Every buffer is owned by the caller.  q4lin_run allocates nothing, never
  *     synchronizes the device and only enqueues kernels on the given stream.  A handle
- *     owns its options, a 4-byte device status word and 32 MiB of device scratch plus
+ *     owns its options, a 4-byte device status word and 64 MiB of device scratch plus
  *     64 KiB of counters (partial sums of launches that split K or the rows across CTAs:
- *     decode GEMV, tensor-core GEMM, input gradient), all allocated by q4lin_create.
+ *     decode GEMV, tensor-core GEMM, input gradient; the fp16 copy of x of the fp16
+ *     tensor-core path), all allocated by q4lin_create.
  *   - Status codes, never exceptions, aborts or prints.  Arguments are validated before
  *     any launch: a non-OK status from validation means nothing was enqueued.
  *   - All device pointers must be device-accessible memory of the handle's device.
@@ -95,7 +96,16 @@ typedef enum {
      * pipeline stage, and the multi-row GEMV's copy engine issues nothing, so the barrier
      * their consumers wait on is never completed and their bounded waits run out
      * (exercises the timeout path without faulting the GPU). */
-    Q4LIN_OPT_TC_SKIP_FIRST_COPY = 5
+    Q4LIN_OPT_TC_SKIP_FIRST_COPY = 5,
+    /* 1: the tensor-core GEMM multiplies fp16 operands (x and the dequantized weights
+     * (code - 8) * scale rounded to IEEE binary16, fp32 accumulation: tcgen05.mma
+     * kind::f16, twice the tf32 rate) instead of tf32 (default 0).  Each product carries a
+     * relative error below 2^-10, inside the tensor-core path's 4e-3 * sum|x*w| bar.
+     * Values outside the fp16 range (|x| >= 65520, or a scale with |scale| > 8188) make
+     * the call record code 2 in the status word; its output is then undefined.  x is
+     * first converted into the handle's scratch (M * K * 2 bytes); a problem whose copy
+     * does not fit there runs in tf32. */
+    Q4LIN_OPT_TC_F16 = 6
 } q4lin_option_t;
 
 /* Create a handle for CUDA device `device`.  Queries the SM count and shared-memory
@@ -248,7 +258,8 @@ typedef enum {
     Q4LIN_KERNEL_MULTIROW = 2,  /* TMA-fed multi-row GEMV (2 <= M <= 4)                    */
     Q4LIN_KERNEL_ROWSTREAM = 3, /* row-streaming CUDA-core kernel (small M)                */
     Q4LIN_KERNEL_GENERIC = 4,   /* generic CUDA-core kernel (any K, group size, alignment) */
-    Q4LIN_KERNEL_TC = 5         /* tcgen05 tensor-core GEMM                                */
+    Q4LIN_KERNEL_TC = 5,        /* tcgen05 tensor-core GEMM, tf32 operands                 */
+    Q4LIN_KERNEL_TC_F16 = 6     /* the same with fp16 operands (Q4LIN_OPT_TC_F16)          */
 } q4lin_kernel_t;
 
 /* The kernel q4lin_run would launch for these arguments (no launch, no device access);
@@ -269,7 +280,8 @@ Q4LIN_API q4lin_status_t q4lin_get_option(q4lin_handle_t handle, int option,
 
 /* Read and clear the handle's device status word after synchronizing `stream`.
  * *code_out = 0 if no kernel recorded a problem since the last call; otherwise the
- * first recorded code (1 = a bounded wait of the tensor-core kernel ran out).
+ * first recorded code (1 = a bounded device-side wait ran out; 2 = a value outside the
+ * fp16 range on the fp16 tensor-core path).
  * The word is shared by every call on the handle.
  * Returns Q4LIN_ERR_TIMEOUT when the code is non-zero, Q4LIN_OK otherwise. */
 Q4LIN_API q4lin_status_t q4lin_check_device_status(q4lin_handle_t handle, void* stream,

@@ -432,10 +432,12 @@ def test_tc_dependent_chain(handle, pdl, M):
 
 # ------------------------------------------------------------- split K (decode GEMV)
 @pytest.mark.parametrize("N,K,gs", [(512, 8192, 32), (64, 4096, 64), (2048, 2048, 32),
-                                    (1000, 8192, 8192), (2047, 14336, 128)])
+                                    (1000, 8192, 8192), (2047, 14336, 128), (4096, 14336, 32),
+                                    (28672, 4096, 32), (2048, 8192, 32)])
 def test_split_k_parity_and_determinism(handle, N, K, gs):
-    """Short matrices split K across CTAs (partial sums in the handle's scratch, summed
-    in a fixed order by the last CTA of each row block): parity, and bit-identical
+    """The decode GEMV cuts its (row block, 1024-k stage) units evenly over the CTAs, so
+    row blocks are split across CTAs at uneven K boundaries (partial sums in the handle's
+    scratch, summed in K order by the last CTA of each block): parity, and bit-identical
     results over repeated calls (the counters reset themselves)."""
     c = synth.make_case(1, N, K, gs, scale_f16=(gs != K), bias=True, seed=N + K)
     outs = [run_q4lin(handle, c, AUTO)[0] for _ in range(3)]
@@ -581,3 +583,217 @@ def test_multirow_bounded_wait_times_out_cleanly(handle):
     a, _ = check_case(handle, c, GEMV)
     b, _ = run_q4lin(handle, c, GEMV)
     np.testing.assert_array_equal(a, b)
+
+
+# ------------------------------------------- decode GEMV: fixed-point (dp4a) arithmetic
+# Shapes with at least two 16-row blocks per CTA (here 8192 x 2048 and 14336 x 4096, 32-row
+# blocks) take the decode GEMV's fixed-point path: x converted per 32-k chunk to 32-bit
+# fixed point, exact integer dot products of the codes (dp4a), one rounding per chunk.
+# Chunks with Inf / NaN, or with a nonzero element more than 2^13 below the chunk's
+# largest, stay on the fp32 path.
+X8_SHAPES = [(8192, 2048), (14336, 4096)]
+
+
+@pytest.mark.parametrize("N,K", X8_SHAPES)
+@pytest.mark.parametrize("gs,f16", [(32, True), (32, False), (128, True), (None, False)])
+def test_gemv_fixed_point_dyadic_bit_exact(handle, N, K, gs, f16):
+    gs = gs or K
+    c = synth.make_dyadic_case(1, N, K, gs, scale_f16=f16, bias=True, seed=N + gs)
+    out, used = run_q4lin(handle, c, AUTO)
+    assert used == GEMV
+    ref, _ = oracle.linear(c.x, c.qweight, c.scales, c.bias, c.K, c.group_size)
+    np.testing.assert_array_equal(out.astype(np.float64), ref)
+
+
+def test_gemv_fixed_point_all_codes_eight_gives_bias(handle):
+    c = synth.make_case(1, 8192, 2048, 32, scale_f16=True, bias=True, seed=19)
+    c.qweight = synth.fill_codes(8192, 2048, 8)
+    out, _ = run_q4lin(handle, c, AUTO)
+    np.testing.assert_array_equal(out, np.broadcast_to(c.bias, out.shape))
+
+
+@pytest.mark.parametrize("N,K", X8_SHAPES)
+def test_gemv_fixed_point_even_high(handle, N, K):
+    c = synth.make_case(1, N, K, 32, scale_f16=True, bias=True, seed=23)
+    check_case(handle, c, AUTO, even_high=True)
+
+
+def _assert_ieee_match(out, ref, mag):
+    """NaN and +/-Inf positions equal to the oracle's, finite elements within the bar."""
+    o = out.astype(np.float64)
+    assert np.array_equal(np.isnan(o), np.isnan(ref)), "NaN positions differ"
+    inf = np.isinf(ref)
+    assert np.array_equal(np.isinf(o), inf), "Inf positions differ"
+    assert np.array_equal(o[inf], ref[inf]), "Inf signs differ"
+    fin = np.isfinite(ref)
+    if fin.any():
+        assert_parity(out[fin][None, :], ref[fin][None, :], mag[fin][None, :], TOL_FP32)
+
+
+@pytest.mark.parametrize("case", ["pos_inf", "neg_and_pos_inf", "nan"])
+def test_gemv_fixed_point_non_finite_x(handle, case):
+    """Inf and NaN in x propagate as in IEEE arithmetic (Inf * 0 = NaN, Inf - Inf = NaN),
+    element by element as the fp64 oracle computes them; the other chunks of the same
+    launch stay on the fixed-point path."""
+    c = synth.make_case(1, 8192, 2048, 32, scale_f16=True, bias=True, seed=29)
+    x = c.x.copy()
+    if case == "pos_inf":
+        x[0, 5] = np.inf
+    elif case == "neg_and_pos_inf":
+        x[0, 5] = np.inf
+        x[0, 1500] = -np.inf
+    else:
+        x[0, 700] = np.nan
+    c.x = x
+    out, _ = run_q4lin(handle, c, AUTO)
+    with np.errstate(invalid="ignore"):
+        ref, mag = oracle.linear(c.x, c.qweight, c.scales, c.bias, c.K, 32)
+    _assert_ieee_match(out, ref, mag)
+    if case == "pos_inf":
+        assert np.isnan(out).any() and np.isinf(out).any()
+
+
+@pytest.mark.parametrize("ratio", [1e3, 1e4, 1e5, 1e7])
+def test_gemv_fixed_point_dynamic_range(handle, ratio):
+    """Every 32-k chunk holds one element `ratio` times larger than the rest, and for half
+    of the rows that element's code is 8 (weight 0), so the tolerance comes only from the
+    small elements: chunks within 2^13 of their largest are converted to fixed point
+    (relative error <= 2^-18 per element), wider ones stay fp32; both stay in the bar."""
+    N, K = 8192, 2048
+    c = synth.make_case(1, N, K, 32, scale_f16=True, bias=True, seed=int(ratio) % 1000)
+    x = c.x.copy()
+    x[0, 7::32] *= ratio
+    c.x = x
+    w = c.qweight.copy()
+    rows = np.arange(0, N, 2)
+    byte = 7 // 2  # k = 7 + 32 j sits in byte 16 j + 3, high nibble
+    for j in range(K // 32):
+        b = w[rows, 16 * j + byte]
+        w[rows, 16 * j + byte] = (b & 0x0F) | 0x80
+    c.qweight = w
+    check_case(handle, c, AUTO)
+
+
+def test_gemv_fixed_point_zero_and_subnormal_chunks(handle):
+    """All-zero chunks, subnormal x and a chunk of equal values convert without error."""
+    N, K = 8192, 2048
+    c = synth.make_case(1, N, K, 32, scale_f16=False, bias=True, seed=37)
+    x = c.x.copy()
+    x[0, :64] = 0.0
+    x[0, 64:96] = np.float32(1e-40)
+    x[0, 96:128] = np.float32(-3.0)
+    x[0, 128:160] = np.float32(2.0 ** -120)
+    c.x = x
+    check_case(handle, c, AUTO)
+
+
+# ------------------------------------------------ tensor-core GEMM with fp16 operands
+# Q4LIN_OPT_TC_F16: x and the dequantized weights rounded to fp16 (x by a conversion
+# kernel into the handle's scratch), tcgen05.mma kind::f16 with fp32 accumulation.
+@pytest.fixture()
+def f16_handle(handle):
+    from bit_weight_quantized_int4_gb300 import q4lin as q
+    assert q.q4lin_set_option(handle, q.Q4LIN_OPT_TC_F16, 1) == q.Q4LIN_OK
+    yield handle
+    q.q4lin_set_option(handle, q.Q4LIN_OPT_TC_F16, 0)
+
+
+def _kernel_of(handle, c, path=AUTO):
+    import torch
+    from bit_weight_quantized_int4_gb300 import q4lin as q
+    from tests._gpu import device_case
+    x, w, s, b = device_case(c)
+    out = torch.empty(c.M, c.N, device="cuda")
+    sd = q.Q4LIN_SCALE_F16 if c.scale_f16 else q.Q4LIN_SCALE_F32
+    q.q4lin_set_option(handle, q.Q4LIN_OPT_FORCE_PATH, path)
+    try:
+        st, k = q.q4lin_plan_kernel(handle, x.data_ptr(), w.data_ptr(), s.data_ptr(),
+                                    None if b is None else b.data_ptr(), out.data_ptr(), c.M,
+                                    c.N, c.K, c.group_size, sd)
+    finally:
+        q.q4lin_set_option(handle, q.Q4LIN_OPT_FORCE_PATH, AUTO)
+    assert st == q.Q4LIN_OK
+    return q.KERNEL_NAMES[k]
+
+
+@pytest.mark.parametrize("M,N,K,gs,f16,bias", TC_SHAPES)
+def test_tc_f16_parity(f16_handle, M, N, K, gs, f16, bias):
+    c = synth.make_case(M, N, K, gs, scale_f16=f16, bias=bias, seed=M + N + 1)
+    assert _kernel_of(f16_handle, c, TC) == "tc_f16"
+    _, used = check_case(f16_handle, c, TC)
+    assert used == TC
+
+
+@pytest.mark.parametrize("M,N,K", [(2048, 2048, 2048), (512, 8192, 2048), (128, 2048, 8192),
+                                   (2048, 512, 2048)])
+def test_tc_f16_prefill_shapes(f16_handle, M, N, K):
+    c = synth.make_case(M, N, K, 32, scale_f16=False, bias=True, seed=M + K)
+    assert _kernel_of(f16_handle, c) == "tc_f16"
+    check_case(f16_handle, c, AUTO)
+
+
+@pytest.mark.parametrize("M", [5, 48, 300])
+def test_tc_f16_dyadic_bit_exact(f16_handle, M):
+    c = synth.make_dyadic_case(M, 260, 1056, 32, scale_f16=(M % 2 == 1), bias=True, seed=M)
+    out, used = run_q4lin(f16_handle, c, TC)
+    assert used == TC
+    ref, _ = oracle.linear(c.x, c.qweight, c.scales, c.bias, c.K, c.group_size)
+    np.testing.assert_array_equal(out.astype(np.float64), ref)
+
+
+@pytest.mark.parametrize("what", ["x", "scale"])
+def test_tc_f16_out_of_range_is_reported(f16_handle, what):
+    """A value that fp16 cannot hold (x >= 65520, or a scale above 8188 so that a weight
+    passes 65504) records code 2 in the status word; the next in-range call is correct."""
+    from bit_weight_quantized_int4_gb300 import q4lin as q
+    c = synth.make_case(64, 256, 512, 32, scale_f16=False, bias=False, seed=5)
+    bad = synth.make_case(64, 256, 512, 32, scale_f16=False, bias=False, seed=5)
+    if what == "x":
+        bad.x = bad.x.copy()
+        bad.x[3, 17] = 1.0e5
+    else:
+        bad.scales = bad.scales.copy()
+        bad.scales[2, 9] = 1.0e4
+    assert q.q4lin_check_device_status(f16_handle, None) == (q.Q4LIN_OK, 0)
+    run_q4lin(f16_handle, bad, TC)
+    st, code = q.q4lin_check_device_status(f16_handle, None)
+    assert st == q.Q4LIN_ERR_TIMEOUT and code == 2
+    check_case(f16_handle, c, TC)
+    assert q.q4lin_check_device_status(f16_handle, None) == (q.Q4LIN_OK, 0)
+
+
+@pytest.mark.parametrize("pdl", [0, 1])
+def test_tc_f16_dependent_chain(f16_handle, pdl):
+    """fp16 GEMMs chained on one stream (each reads the previous output as x): the
+    conversion of x runs after the preceding GEMM completed, the GEMM after the
+    conversion; each link checked against the oracle on the input it received."""
+    import torch
+    from bit_weight_quantized_int4_gb300 import q4lin as q
+    M, dims = 200, [512, 1024, 256, 768]
+    links = [synth.make_case(M, dims[i + 1], dims[i], 32, scale_f16=(i % 2 == 1),
+                             bias=(i % 2 == 0), seed=800 + i) for i in range(len(dims) - 1)]
+    bufs = [torch.from_numpy(np.ascontiguousarray(links[0].x)).cuda()]
+    bufs += [torch.full((M, d), float("nan"), device="cuda") for d in dims[1:]]
+    dev = [tuple(None if a is None else torch.from_numpy(a).cuda()
+                 for a in (c.qweight, c.scales, c.bias)) for c in links]
+    torch.cuda.synchronize()
+    q.q4lin_set_option(f16_handle, q.Q4LIN_OPT_PDL, pdl)
+    q.q4lin_set_option(f16_handle, q.Q4LIN_OPT_FORCE_PATH, TC)
+    try:
+        stream = torch.cuda.current_stream().cuda_stream
+        for i, c in enumerate(links):
+            w, s, b = dev[i]
+            sd = q.Q4LIN_SCALE_F16 if c.scales.dtype == np.float16 else q.Q4LIN_SCALE_F32
+            st = q.q4lin_run(f16_handle, bufs[i].data_ptr(), w.data_ptr(), s.data_ptr(),
+                             None if b is None else b.data_ptr(), bufs[i + 1].data_ptr(),
+                             M, c.N, c.K, 32, sd, stream)
+            assert st == q.Q4LIN_OK
+        torch.cuda.synchronize()
+    finally:
+        q.q4lin_set_option(f16_handle, q.Q4LIN_OPT_PDL, 0)
+        q.q4lin_set_option(f16_handle, q.Q4LIN_OPT_FORCE_PATH, AUTO)
+    host = [b.cpu().numpy() for b in bufs]
+    for i, c in enumerate(links):
+        assert not np.isnan(host[i + 1]).any(), f"link {i} output has NaN"
+        ref, mag = oracle.linear(host[i], c.qweight, c.scales, c.bias, c.K, 32)
+        assert_parity(host[i + 1], ref, mag, TOL_TC)
