@@ -48,7 +48,10 @@ HEADLINE = "8b"
 # --profile launch:<model>:<kind>, each launch on its own cold weights).  Valid only for
 # the kernel source they were taken with (sha256 prefix of gemv_tma.cu + ptx.cuh); any
 # other source reports null.
-LAUNCH_TRAFFIC = {"source_sha256": None, "bytes": {}}
+LAUNCH_TRAFFIC = {"source_sha256": "f2503f5fb5542fd3", "bytes": {
+    "8b:qkv": 14203136, "8b:o": 9481472, "8b:gateup": 66248448, "8b:down": 33115392,
+    "8b:lm_head": 298889216, "1b:qkv": 3574784, "1b:o": 2394880, "1b:gateup": 18919936,
+    "1b:down": 9501184, "1b:lm_head": 150976768}}
 
 
 def gemv_source_sha():
@@ -695,7 +698,15 @@ def cpu_baseline_worker(target_s=0.4):
             if dt >= target_s or n >= N:
                 break
             n = min(N, max(2 * n, int(n * target_s / max(dt, 1e-4) * 1.2)))
-        res.append({"label": label, "N": N, "K": K, "M": M, "rows_timed": n,
+        # Small shapes (all rows in less than target_s): repeat until target_s, keep the
+        # fastest pass.
+        reps, t_start = 1, time.perf_counter()
+        while time.perf_counter() - t_start < target_s:
+            t0 = time.perf_counter()
+            oracle.linear(x, w, s, None, K, GROUP)
+            dt = min(dt, time.perf_counter() - t0)
+            reps += 1
+        res.append({"label": label, "N": N, "K": K, "M": M, "rows_timed": n, "passes": reps,
                     "ms_full": dt * 1000 * N / n})
     return {"threads": oracle.num_threads(), "shapes": res}
 
@@ -935,9 +946,9 @@ def profile(spec):
     elif kind == "gemv":
         N, K = int(dims[0]), int(dims[1])
         shape_bandwidth(torch, h, N, K, int(dims[2]) if len(dims) > 2 else 1)
-    elif kind == "prefill":
+    elif kind in ("prefill", "prefill16"):
         M, N, K = (int(d) for d in dims)
-        prefill_time(torch, h, M, N, K, min_reps=3)
+        prefill_time(torch, h, M, N, K, min_reps=3, f16=kind == "prefill16")
     elif kind == "backward":
         M, N, K = (int(d) for d in dims)
         backward_bandwidth(torch, h, M, N, K)
@@ -970,7 +981,8 @@ def main():
                          "measured table (JSON) instead of the benchmark line")
     ap.add_argument("--profile", default=None,
                     help="run a few launches of one op and exit (for ncu): gemv:N:K[:M], "
-                         "prefill:M:N:K, backward:M:N:K, requant:N:K, token:1b|8b or "
+                         "prefill:M:N:K, prefill16:M:N:K, backward:M:N:K, requant:N:K, "
+                         "token:1b|8b or "
                          "launch:1b|8b:qkv|o|gateup|down|lm_head")
     ap.add_argument("--cpu-worker", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args()

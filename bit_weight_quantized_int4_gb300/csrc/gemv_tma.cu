@@ -859,10 +859,11 @@ cudaError_t gemv_tma_launch_group(const Problem* ps, int count, const LaunchCtx&
     a.ws_rows = blocks * rb;
     const unsigned grid = (unsigned)std::min<int64_t>(a.items, slots);
     // Fixed-point dp4a arithmetic where its per-CTA conversion of x pays off: each CTA
-    // converts the x stages it uses once, which the cheaper inner loop repays only over
-    // about four row blocks per CTA (measured on the decode tokens: vocabulary-sized
-    // heads gain 5-10 %; gate/up with three blocks per CTA is 2-4 % slower).
-    const bool x8 = a.items >= 4 * (int64_t)grid;
+    // converts the x stages it uses once, which the cheaper inner loop repays from about
+    // two row blocks per CTA on (measured on the decode tokens: vocabulary-sized heads
+    // 15 %, 8B gate/up 5 % faster; one block per CTA, as in q/k/v, o and down, 5-50 %
+    // slower).
+    const bool x8 = a.items >= 2 * (int64_t)grid;
     return dispatch_v(V, p0.even_high != 0, pc, p0.scale_f16 != 0, x8, tm, a, grid, lay.total, c);
 }
 
