@@ -274,8 +274,9 @@ class DecodeToken:
     """Device buffers of one model's decode token and the q4lin calls over them.
 
     Each group of projections that read the same activation (q/k/v, gate/up) has one x
-    buffer and runs as one q4lin_run_grouped call (or as separate q4lin_run calls with
-    grouped=False).  Every projection has its own weight, scale and output buffers."""
+    buffer.  grouped=True runs the whole token as one q4lin_run_grouped call (which fuses
+    each group into one launch); grouped=False as one q4lin_run call per projection.
+    Every projection has its own weight, scale and output buffers."""
 
     def __init__(self, handle, model, device, seed_base=1000, grouped=True):
         import torch
@@ -320,16 +321,19 @@ class DecodeToken:
 
     def run(self, stream_ptr):
         from bit_weight_quantized_int4_gb300 import q4lin as q
-        for probs in self.problem_tuples():
-            if self.grouped and len(probs) > 1:
-                st = q.q4lin_run_grouped(self.h, probs, stream_ptr)
-            else:
-                for pr in probs:
-                    st = q.q4lin_run(self.h, *pr, stream_ptr)
-                    if st != q.Q4LIN_OK:
-                        break
+        if self.grouped:
+            # One call over the whole token, as a serving loop makes it: the library fuses
+            # the projections that share an input.
+            st = q.q4lin_run_grouped(self.h, [p for grp in self.problem_tuples() for p in grp],
+                                     stream_ptr)
             if st != q.Q4LIN_OK:
-                raise q.Q4LinError(st, "q4lin_run")
+                raise q.Q4LinError(st, "q4lin_run_grouped")
+            return
+        for probs in self.problem_tuples():
+            for pr in probs:
+                st = q.q4lin_run(self.h, *pr, stream_ptr)
+                if st != q.Q4LIN_OK:
+                    raise q.Q4LinError(st, "q4lin_run")
 
     def head_output(self):
         N, _, _, _, oo = self.bufs[-1][-1]

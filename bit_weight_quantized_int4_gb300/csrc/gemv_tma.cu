@@ -14,15 +14,16 @@
 //     spans the 512 bytes) and of the matching block of group scales [1024 / group size
 //     groups x rb rows], all on one mbarrier, into a ring of 2..8 stages.  Weight rows
 //     are long contiguous segments, so DRAM sees streaming reads.
-//   8 consumer warps (256 threads): thread = (chunk lane j in 0..15, row group of V rows);
-//     per stage it takes chunks j and j + 16 (32 codes each) of each of its V rows.
+//   8 consumer warps (256 threads): thread = (chunk lane j of CL, row group of V rows),
+//     with (V, CL) = (2, 32) or (4, 32) for blocks of 16 or 32 rows and (4, 16) for 64;
+//     per stage it takes chunks j, j + CL, ... (32 codes each) of each of its V rows, and
+//     each x chunk it loads serves all V rows.
 //     x is staged whole in shared memory once per CTA after the dependency wait (every
 //     consumer thread loads 16-byte units, eight in flight at a time), unit u of 32-k
 //     chunk c at unit u ^ (c % 8) of the chunk's 128-byte row.  A quarter-warp then reads
 //     128 contiguous bytes of a weight row and 8 different 16-byte units of x, both
-//     conflict-free.  Partial sums stay in registers for
-//     the whole row; the 16 chunk lanes of a row group are reduced with shuffles once per
-//     row block.
+//     conflict-free.  Partial sums stay in registers for the whole row; the CL chunk lanes
+//     of a row group are reduced with shuffles once per row block.
 // Arithmetic (X8 instances): the first time a CTA uses a 1024-k stage, its consumers
 // convert the staged x of that stage in place into 32-bit fixed point per 32-k chunk: with F the largest
 // exponent field of the chunk, q = round(x * 2^(157 - F)) (|q| < 2^31; exact for every
@@ -61,9 +62,11 @@ using namespace ptx;
 constexpr int kCWarps = 8;                 // consumer warps: 2 per SM sub-partition
 constexpr int kCThreads = 32 * kCWarps;
 constexpr int kThreadsG = kCThreads + 32;  // + the producer warp
-constexpr int kRowGroups = kCThreads / 16; // 16 chunk lanes per row group
-static_assert(kRowGroups == kGemvMinRowBlock && 4 * kRowGroups == kGemvMaxRowBlock,
-              "row blocks of 16 row groups x V rows, V in {1, 2, 4}");
+// A consumer thread is (row group, chunk lane): CL chunk lanes (16 or 32) per row group,
+// kCThreads / CL row groups of V rows each, so a row block has kCThreads / CL * V rows.
+__host__ __device__ constexpr int rows_per_block(int V, int CL) { return kCThreads / CL * V; }
+static_assert(rows_per_block(2, 32) == kGemvMinRowBlock && rows_per_block(4, 16) == kGemvMaxRowBlock,
+              "row blocks of 16 to 64 rows");
 constexpr int kSRB = 512;                  // packed bytes of a row per stage (1024 k)
 constexpr int kSC = 32;                    // 32-k chunks per stage
 constexpr int kXStageBytes = 4096;         // x of one stage: 32 chunk rows x 128 bytes
@@ -372,10 +375,31 @@ __device__ __forceinline__ bool convert_x_stage(uint32_t xa, uint32_t meta, int 
     return !keep_f32;
 }
 
-template <int V, bool EH, bool PC, bool F16, bool X8>
+// One chunk of a stage for a thread's V rows: x chunk c from the staged x, the V rows'
+// 16-byte code units at wrow + v * 512, their group scales at saddr; fixed-point (FX, with
+// the chunk's metadata md: factor, two offsets) or fp32 arithmetic, accumulated into acc.
+template <int V, bool EH, bool PC, bool F16, bool FX>
+__device__ __forceinline__ void stage_chunk(uint32_t xa, int c, const uint4& md, uint32_t saddr,
+                                            uint32_t wrow, float (&acc)[V]) {
+    uint4 xu[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) xu[i] = ld_shared_v4(x_unit(xa, c, i));
+    float sc[V];
+    if (!PC) stage_scales<V, F16>(saddr, sc);
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+        const uint4 wv = ld_shared_v4(wrow + v * kSRB);
+        const float t = FX ? chunk_dot_x8<EH>(wv, xu, (int)md.y, (int)md.z) * __uint_as_float(md.x)
+                           : chunk_dot_f32<EH>(wv, xu);
+        acc[v] = PC ? acc[v] + t : fmaf(t, sc[v], acc[v]);
+    }
+}
+
+template <int V, int CL, bool EH, bool PC, bool F16, bool X8>
 __global__ void __launch_bounds__(kThreadsG, 2)
     gemv_tma_kernel(const __grid_constant__ TensorMaps tmaps, const GArgs a) {
-    constexpr int rb = kRowGroups * V;  // rows per block: 16 row groups of V rows
+    constexpr int rb = rows_per_block(V, CL);  // row groups of V rows
+    constexpr int H = kSC / CL;                // chunks of a stage per chunk lane
     constexpr uint32_t esz = F16 ? 2 : 4;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -445,8 +469,8 @@ __global__ void __launch_bounds__(kThreadsG, 2)
     }
 
     // ------------------------------------------------------------------ consumers
-    const int j = threadIdx.x & 15;          // chunk lane within a 256-byte box row
-    const int r0 = (threadIdx.x >> 4) * V;   // first of this thread's V rows in a block
+    const int j = threadIdx.x & (CL - 1);    // chunk lane: chunks j, j + CL, ... of a stage
+    const int r0 = (threadIdx.x / CL) * V;   // first of this thread's V rows in a block
     griddep_wait();  // x, bias, out and the workspace belong to the dependency chain
     // x into shared memory once: 16-byte unit i (k = 4 i .. 4 i + 3) of chunk i / 8 at its
     // swizzled place, zero past K; eight loads in flight per thread before the stores.
@@ -498,10 +522,10 @@ __global__ void __launch_bounds__(kThreadsG, 2)
     // Per-thread offsets: the thread's rows of a weight stage (row r at r * kSRB bytes,
     // chunk column c at c * 16), its group-scale rows.
     const uint32_t w_off = (uint32_t)(r0 * kSRB + j * 16);
-    uint32_t s_off[2];
+    uint32_t s_off[H];
 #pragma unroll
-    for (int h = 0; h < 2; ++h)
-        s_off[h] = a.scale_off + scale_slot<rb * esz>((h * 16 + j) >> a.gs_shift, r0 * esz);
+    for (int h = 0; h < H; ++h)
+        s_off[h] = a.scale_off + scale_slot<rb * esz>((h * CL + j) >> a.gs_shift, r0 * esz);
     uint32_t x_ready = X8 ? 0u : ~0u;  // stages of x this CTA has looked at
     uint32_t x_fixed = 0u;             // ... and converted to fixed point
     // After a timed-out wait (`dead`) the warp still walks every item, without waiting or
@@ -526,40 +550,16 @@ __global__ void __launch_bounds__(kThreadsG, 2)
             const uint32_t sb = base + (uint32_t)s * a.stage_bytes;
             if (X8 && ((x_fixed >> ks) & 1u)) {
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int c = ks * kSC + h * 16 + j;
-                    uint4 xu[8];
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) xu[i] = ld_shared_v4(x_unit(xa, c, i));
-                    const uint4 md = ld_shared_v4(meta + (uint32_t)c * kMetaBytes);
-                    float sc[V];
-                    if (!PC) stage_scales<V, F16>(sb + s_off[h], sc);
-                    const uint32_t wrow = sb + w_off + h * 256;
-#pragma unroll
-                    for (int v = 0; v < V; ++v) {
-                        const uint4 wv = ld_shared_v4(wrow + v * kSRB);
-                        const float tf = chunk_dot_x8<EH>(wv, xu, (int)md.y, (int)md.z) *
-                                         __uint_as_float(md.x);
-                        acc[v] = PC ? acc[v] + tf : fmaf(tf, sc[v], acc[v]);
-                    }
+                for (int h = 0; h < H; ++h) {
+                    const int c = ks * kSC + h * CL + j;
+                    stage_chunk<V, EH, PC, F16, true>(xa, c, ld_shared_v4(meta + (uint32_t)c * kMetaBytes),
+                                                      sb + s_off[h], sb + w_off + h * CL * 16, acc);
                 }
             } else {
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int c = ks * kSC + h * 16 + j;
-                    uint4 xu[8];
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) xu[i] = ld_shared_v4(x_unit(xa, c, i));
-                    float sc[V];
-                    if (!PC) stage_scales<V, F16>(sb + s_off[h], sc);
-                    const uint32_t wrow = sb + w_off + h * 256;
-#pragma unroll
-                    for (int v = 0; v < V; ++v) {
-                        const uint4 wv = ld_shared_v4(wrow + v * kSRB);
-                        const float t = chunk_dot_f32<EH>(wv, xu);
-                        acc[v] = PC ? acc[v] + t : fmaf(t, sc[v], acc[v]);
-                    }
-                }
+                for (int h = 0; h < H; ++h)
+                    stage_chunk<V, EH, PC, F16, false>(xa, ks * kSC + h * CL + j, make_uint4(0u, 0u, 0u, 0u),
+                                                       sb + s_off[h], sb + w_off + h * CL * 16, acc);
             }
         }
         __syncwarp();
@@ -568,14 +568,14 @@ __global__ void __launch_bounds__(kThreadsG, 2)
         const int blk = cur.blk;
         const int part = cur.part;
         if (cur.advance(a)) {
-            // Item done: reduce the 16 chunk lanes of each row; store (or hand the partial
+            // Item done: reduce the CL chunk lanes of each row; store (or hand the partial
             // to the last item).
             float tot[V];
 #pragma unroll
             for (int v = 0; v < V; ++v) {
                 tot[v] = acc[v];
 #pragma unroll
-                for (int o = 1; o < 16; o <<= 1)
+                for (int o = 1; o < CL; o <<= 1)
                     tot[v] += __shfl_xor_sync(0xffffffffu, tot[v], o);
                 acc[v] = 0.f;
             }
@@ -623,10 +623,11 @@ __global__ void __launch_bounds__(kThreadsG, 2)
     }
 }
 
-template <int V, bool EH, bool PC, bool F16, bool X8>
+template <int V, int CL, bool EH, bool PC, bool F16, bool X8>
 cudaError_t launch_v(const TensorMaps& tm, const GArgs& a, unsigned grid, uint32_t smem,
                      const LaunchCtx& c) {
-    const cudaError_t attr = kernel_smem_once<gemv_tma_kernel<V, EH, PC, F16, X8>>(kCtaSmem, 100);
+    constexpr auto kernel = gemv_tma_kernel<V, CL, EH, PC, F16, X8>;
+    const cudaError_t attr = kernel_smem_once<kernel>(kCtaSmem, 100);
     if (attr != cudaSuccess) return attr;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
@@ -640,38 +641,53 @@ cudaError_t launch_v(const TensorMaps& tm, const GArgs& a, unsigned grid, uint32
         cfg.attrs = attrs;
         cfg.numAttrs = 1;
     }
-    return cudaLaunchKernelEx(&cfg, gemv_tma_kernel<V, EH, PC, F16, X8>, tm, a);
+    return cudaLaunchKernelEx(&cfg, kernel, tm, a);
 }
 
-template <int V, bool EH, bool PC, bool F16>
+template <int V, int CL, bool EH, bool PC, bool F16>
 cudaError_t dispatch_x8(bool x8, const TensorMaps& tm, const GArgs& a, unsigned grid,
                         uint32_t smem, const LaunchCtx& c) {
-    return x8 ? launch_v<V, EH, PC, F16, true>(tm, a, grid, smem, c)
-              : launch_v<V, EH, PC, F16, false>(tm, a, grid, smem, c);
+    return x8 ? launch_v<V, CL, EH, PC, F16, true>(tm, a, grid, smem, c)
+              : launch_v<V, CL, EH, PC, F16, false>(tm, a, grid, smem, c);
 }
-template <int V, bool EH, bool PC>
+template <int V, int CL, bool EH, bool PC>
 cudaError_t dispatch_f16(bool f16, bool x8, const TensorMaps& tm, const GArgs& a, unsigned grid,
                          uint32_t smem, const LaunchCtx& c) {
-    return f16 ? dispatch_x8<V, EH, PC, true>(x8, tm, a, grid, smem, c)
-               : dispatch_x8<V, EH, PC, false>(x8, tm, a, grid, smem, c);
+    return f16 ? dispatch_x8<V, CL, EH, PC, true>(x8, tm, a, grid, smem, c)
+               : dispatch_x8<V, CL, EH, PC, false>(x8, tm, a, grid, smem, c);
 }
-template <int V, bool EH>
+template <int V, int CL, bool EH>
 cudaError_t dispatch_pc(bool pc, bool f16, bool x8, const TensorMaps& tm, const GArgs& a,
                         unsigned grid, uint32_t smem, const LaunchCtx& c) {
-    return pc ? dispatch_f16<V, EH, true>(f16, x8, tm, a, grid, smem, c)
-              : dispatch_f16<V, EH, false>(f16, x8, tm, a, grid, smem, c);
+    return pc ? dispatch_f16<V, CL, EH, true>(f16, x8, tm, a, grid, smem, c)
+              : dispatch_f16<V, CL, EH, false>(f16, x8, tm, a, grid, smem, c);
 }
-template <int V>
+template <int V, int CL>
 cudaError_t dispatch_eh(bool eh, bool pc, bool f16, bool x8, const TensorMaps& tm,
                         const GArgs& a, unsigned grid, uint32_t smem, const LaunchCtx& c) {
-    return eh ? dispatch_pc<V, true>(pc, f16, x8, tm, a, grid, smem, c)
-              : dispatch_pc<V, false>(pc, f16, x8, tm, a, grid, smem, c);
+    return eh ? dispatch_pc<V, CL, true>(pc, f16, x8, tm, a, grid, smem, c)
+              : dispatch_pc<V, CL, false>(pc, f16, x8, tm, a, grid, smem, c);
 }
-cudaError_t dispatch_v(int V, bool eh, bool pc, bool f16, bool x8, const TensorMaps& tm,
-                       const GArgs& a, unsigned grid, uint32_t smem, const LaunchCtx& c) {
-    if (V == 4) return dispatch_eh<4>(eh, pc, f16, x8, tm, a, grid, smem, c);
-    if (V == 2) return dispatch_eh<2>(eh, pc, f16, x8, tm, a, grid, smem, c);
-    return dispatch_eh<1>(eh, pc, f16, x8, tm, a, grid, smem, c);
+
+// Tiles of the decode GEMV: V rows per thread and CL chunk lanes per row group, so
+// kCThreads / CL * V rows per block.  Rows 16 and 32 use 32 chunk lanes: each thread takes
+// one chunk of a stage for its 2 or 4 rows, and a staged x chunk is read once per 2 or 4
+// rows (with 16 chunk lanes the same heights would be 1 or 2 rows per thread, and x, read
+// once per row or two, would bound the launch by shared-memory bandwidth).  Rows 64 keep
+// 16 chunk lanes (4 rows per thread: 32 would need 8).  Listed so that at equal cost the
+// taller block wins: it does twice the work per stage and per row-block reduction
+// (measured: 128256 x 4096 55.3 us with 64-row blocks, 62.4 with 32).
+struct Tile {
+    int V, CL;
+    int rows() const { return kCThreads / CL * V; }
+};
+constexpr Tile kTiles[] = {{4, 16}, {4, 32}, {2, 32}};
+
+cudaError_t dispatch_tile(Tile t, bool eh, bool pc, bool f16, bool x8, const TensorMaps& tm,
+                          const GArgs& a, unsigned grid, uint32_t smem, const LaunchCtx& c) {
+    if (t.CL == 16) return dispatch_eh<4, 16>(eh, pc, f16, x8, tm, a, grid, smem, c);
+    if (t.V == 4) return dispatch_eh<4, 32>(eh, pc, f16, x8, tm, a, grid, smem, c);
+    return dispatch_eh<2, 32>(eh, pc, f16, x8, tm, a, grid, smem, c);
 }
 
 int log2_exact(int64_t v) {
@@ -680,10 +696,9 @@ int log2_exact(int64_t v) {
     return -1;
 }
 
-// Bytes of one stage (weights, then the scale block rounded up to 128 bytes).
-uint32_t stage_bytes_for(int V, bool pc, int esz, int gs_shift, uint32_t* scale_off,
+// Bytes of one stage of rb rows (weights, then the scale block, rounded up to 1 KiB).
+uint32_t stage_bytes_for(int rb, bool pc, int esz, int gs_shift, uint32_t* scale_off,
                          uint32_t* tx) {
-    const int rb = kRowGroups * V;
     const uint32_t wbytes = (uint32_t)(rb * kSRB);
     const int gps = pc ? 0 : (gs_shift >= 5 ? 1 : kSC >> gs_shift);
     const uint32_t sbytes = (uint32_t)(gps * rb * esz);
@@ -726,7 +741,7 @@ bool gemv_tma_eligible(const Problem& p) {
     // x staged whole, plus at least two stages of the smallest tile.
     const int kstages = (int)((p.K + 1023) / 1024);
     uint32_t so, tx;
-    const uint32_t sb1 = stage_bytes_for(1, pc, p.scale_f16 ? 2 : 4,
+    const uint32_t sb1 = stage_bytes_for(kGemvMinRowBlock, pc, p.scale_f16 ? 2 : 4,
                                          pc ? 0 : log2_exact(p.group_size / 32), &so, &tx);
     if (smem_layout(2, sb1, kstages).total > (uint32_t)kCtaSmem) return false;
     return tensor_map_encoder() != nullptr;
@@ -749,51 +764,53 @@ cudaError_t gemv_tma_launch_group(const Problem* ps, int count, const LaunchCtx&
     const int gs_shift = pc ? 0 : log2_exact(p0.group_size / 32);
     const int kstages = (int)((p0.K + 1023) / 1024);
     const int slots = 2 * c.sm_count;
-    auto blocks_for = [&](int V) {
+    auto blocks_for = [&](int rb) {
         int64_t b = 0;
-        for (int i = 0; i < count; ++i) b += (ps[i].N + kRowGroups * V - 1) / (kRowGroups * V);
+        for (int i = 0; i < count; ++i) b += (ps[i].N + rb - 1) / rb;
         return b;
     };
-    auto stages_for = [&](int V) {
+    auto stages_for = [&](int rb) {
         uint32_t so, tx;
-        const uint32_t sb = stage_bytes_for(V, pc, esz, gs_shift, &so, &tx);
+        const uint32_t sb = stage_bytes_for(rb, pc, esz, gs_shift, &so, &tx);
         const int room = kCtaSmem - (int)smem_layout(0, sb, kstages).total;
         return std::min<int>(kMaxStages, room / (int)sb);
     };
-    // Tile shape (V rows per thread) and split-K parts from a cost model of the critical
-    // CTA, fitted to measured launch times on GB300 (isolated GEMVs, 1B/8B decode shapes):
-    //   cost = waves * (0.06 us per KiB of the CTA's weight bytes * eff(V)
+    // Tile and split-K parts from a cost model of the critical CTA, fitted to measured
+    // launch times on GB300 (isolated GEMVs, 1B/8B decode shapes):
+    //   cost = waves * (0.06 us per KiB of the CTA's weight bytes * eff(tile)
     //                   + 2.1 us for the split-K handoff when parts > 1)
-    // with waves = ceil(items / CTA slots).  eff(V) is the relative cost of a weight byte
-    // (1.4, 1.1, 1.0 for V = 1, 2, 4: more rows per thread reuse each x chunk more).
-    int V = 1, best_parts = 1;
+    // with waves = ceil(items / CTA slots).  eff is the relative cost of a weight byte,
+    // set by how many rows share each staged x chunk (V): 1.4, 1.1, 1.0 for V = 1, 2, 4.
+    Tile tile = kTiles[0];
+    int best_parts = 1;
     double best = 1e30;
-    for (int v : {1, 2, 4}) {
-        if (stages_for(v) < 2) continue;
-        const int64_t blocks_v = blocks_for(v);
-        const double eff = v == 1 ? 1.4 : (v == 2 ? 1.1 : 1.0);
+    for (const Tile t : kTiles) {
+        const int rbt = t.rows();
+        if (stages_for(rbt) < 2) continue;
+        const int64_t blocks_t = blocks_for(rbt);
+        const double eff = t.V == 1 ? 1.4 : (t.V == 2 ? 1.1 : 1.0);
         for (int parts = 1; parts <= kGemvMaxParts; parts *= 2) {
             if (parts > 1 && (kstages * 1024 / parts < 2048 || !c.ws || !c.tickets ||
-                              (int64_t)parts * blocks_v * kRowGroups * v > c.ws_floats ||
-                              blocks_v > c.ticket_count))
+                              (int64_t)parts * blocks_t * rbt > c.ws_floats ||
+                              blocks_t > c.ticket_count))
                 break;
             const int tpp = (kstages + parts - 1) / parts;
-            const int64_t items = blocks_v * ((kstages + tpp - 1) / tpp);
+            const int64_t items = blocks_t * ((kstages + tpp - 1) / tpp);
             const double waves = (double)((items + slots - 1) / slots);
-            const double kib = (double)kRowGroups * v * tpp * kSRB / 1024.0;
+            const double kib = (double)rbt * tpp * kSRB / 1024.0;
             const double cost = waves * (0.06 * kib * eff + (parts > 1 ? 2.1 : 0.0));
-            if (cost < best * 0.999) best = cost, V = v, best_parts = parts;
+            if (cost < best * 0.999) best = cost, tile = t, best_parts = parts;
         }
     }
-    const int rb = kRowGroups * V;
+    const int rb = tile.rows();
     GArgs a = {};
     a.x = p0.x;
     a.nmat = count;
     a.K = p0.K;
     a.kstages = kstages;
     a.gs_shift = gs_shift;
-    a.stage_bytes = stage_bytes_for(V, pc, esz, gs_shift, &a.scale_off, &a.stage_tx);
-    a.stages = stages_for(V);
+    a.stage_bytes = stage_bytes_for(rb, pc, esz, gs_shift, &a.scale_off, &a.stage_tx);
+    a.stages = stages_for(rb);
     if (a.stages < 2) return cudaErrorNotSupported;
     const SmemLayout lay = smem_layout(a.stages, a.stage_bytes, kstages);
     a.x_off = lay.x_off;
@@ -864,7 +881,8 @@ cudaError_t gemv_tma_launch_group(const Problem* ps, int count, const LaunchCtx&
     // 15 %, 8B gate/up 5 % faster; one block per CTA, as in q/k/v, o and down, 5-50 %
     // slower).
     const bool x8 = a.items >= 2 * (int64_t)grid;
-    return dispatch_v(V, p0.even_high != 0, pc, p0.scale_f16 != 0, x8, tm, a, grid, lay.total, c);
+    return dispatch_tile(tile, p0.even_high != 0, pc, p0.scale_f16 != 0, x8, tm, a, grid, lay.total,
+                         c);
 }
 
 cudaError_t gemv_tma_launch(const Problem& p, const LaunchCtx& c) {
