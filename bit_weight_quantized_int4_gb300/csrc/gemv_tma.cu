@@ -19,7 +19,7 @@
 //     per stage it takes chunks j, j + CL, ... (32 codes each) of each of its V rows, and
 //     each x chunk it loads serves all V rows.
 //     x is staged whole in shared memory once per CTA after the dependency wait (every
-//     consumer thread loads 16-byte units, eight in flight at a time), unit u of 32-k
+//     consumer thread copies 16-byte units, all in flight at once), unit u of 32-k
 //     chunk c at unit u ^ (c % 8) of the chunk's 128-byte row.  A quarter-warp then reads
 //     128 contiguous bytes of a weight row and 8 different 16-byte units of x, both
 //     conflict-free.  Partial sums stay in registers for the whole row; the CL chunk lanes
@@ -100,6 +100,7 @@ struct GArgs {
     int kstages;     // ceil(K / 1024)
     int gs_shift;    // log2(group size / 32) (grouped scales)
     int stages;      // ring depth
+    int burst;       // stages armed before the first one has landed (0: the whole ring)
     uint32_t stage_bytes, scale_off, stage_tx;
     uint32_t x_off, meta_off, bar_off;  // shared-memory layout, from the 1024-aligned base
     int64_t row_blocks;
@@ -444,6 +445,14 @@ __global__ void __launch_bounds__(kThreadsG, 2)
             Cursor cur;
             cur.start(a);
             while (cur.valid(a)) {
+                // Arm `burst` stages, then wait for the first to land before arming the rest
+                // of the ring: every CTA's first stage is then ahead of the grid's later
+                // stages in the memory queues, and the consumers start sooner.
+                if (t == a.burst && a.burst > 0 && a.burst < S &&
+                    !wait_bounded(full(0), 0u, a.wait_ns, failed)) {
+                    record_failure(a.status, failed);
+                    break;
+                }
                 if (t >= S && !wait_bounded(empty(s), ph ^ 1u, a.wait_ns, failed)) {
                     record_failure(a.status, failed);
                     break;
@@ -473,27 +482,17 @@ __global__ void __launch_bounds__(kThreadsG, 2)
     const int r0 = (threadIdx.x / CL) * V;   // first of this thread's V rows in a block
     griddep_wait();  // x, bias, out and the workspace belong to the dependency chain
     // x into shared memory once: 16-byte unit i (k = 4 i .. 4 i + 3) of chunk i / 8 at its
-    // swizzled place, zero past K; eight loads in flight per thread before the stores.
+    // swizzled place, zero past K.  Asynchronous copies: all of a thread's units are in
+    // flight at once, whatever K.
     {
         const int units = a.kstages * kSC * 8;
-        for (int i0 = threadIdx.x; i0 < units; i0 += 8 * kCThreads) {
-            float4 v[8];
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const int i = i0 + q * kCThreads;
-                v[q] = (i < units && 4 * (int64_t)i < a.K)
-                           ? __ldg(reinterpret_cast<const float4*>(a.x) + i)
-                           : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const int i = i0 + q * kCThreads;
-                if (i < units)
-                    st_shared_v4(x_unit(xa, i >> 3, i & 7), __float_as_uint(v[q].x),
-                                 __float_as_uint(v[q].y), __float_as_uint(v[q].z),
-                                 __float_as_uint(v[q].w));
-            }
+        for (int i = threadIdx.x; i < units; i += kCThreads) {
+            const bool in = 4 * (int64_t)i < a.K;
+            cp_async_16(x_unit(xa, i >> 3, i & 7),
+                        in ? static_cast<const void*>(reinterpret_cast<const float4*>(a.x) + i) : a.x,
+                        in ? 16u : 0u);
         }
+        cp_async_wait_all();
         asm volatile("bar.sync 1, %0;" ::"r"(kCThreads) : "memory");
     }
 
@@ -811,6 +810,7 @@ cudaError_t gemv_tma_launch_group(const Problem* ps, int count, const LaunchCtx&
     a.gs_shift = gs_shift;
     a.stage_bytes = stage_bytes_for(rb, pc, esz, gs_shift, &a.scale_off, &a.stage_tx);
     a.stages = stages_for(rb);
+    a.burst = 1;
     if (a.stages < 2) return cudaErrorNotSupported;
     const SmemLayout lay = smem_layout(a.stages, a.stage_bytes, kstages);
     a.x_off = lay.x_off;
