@@ -48,10 +48,10 @@ HEADLINE = "8b"
 # --profile launch:<model>:<kind>, each launch on its own cold weights).  Valid only for
 # the kernel source they were taken with (sha256 prefix of gemv_tma.cu + ptx.cuh); any
 # other source reports null.
-LAUNCH_TRAFFIC = {"source_sha256": "f2503f5fb5542fd3", "bytes": {
-    "8b:qkv": 14203136, "8b:o": 9481472, "8b:gateup": 66248448, "8b:down": 33115392,
-    "8b:lm_head": 298889216, "1b:qkv": 3574784, "1b:o": 2394880, "1b:gateup": 18919936,
-    "1b:down": 9501184, "1b:lm_head": 150976768}}
+LAUNCH_TRAFFIC = {"source_sha256": "a7de575055abd084", "bytes": {
+    "8b:qkv": 14204928, "8b:o": 9482240, "8b:gateup": 66211840, "8b:down": 33116416,
+    "8b:lm_head": 298932480, "1b:qkv": 3575552, "1b:o": 2395904, "1b:gateup": 18919936,
+    "1b:down": 9503488, "1b:lm_head": 150932736}}
 
 
 def gemv_source_sha():
