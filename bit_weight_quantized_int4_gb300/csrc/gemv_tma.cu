@@ -777,9 +777,12 @@ cudaError_t gemv_tma_launch_group(const Problem* ps, int count, const LaunchCtx&
     // Tile and split-K parts from a cost model of the critical CTA, fitted to measured
     // launch times on GB300 (isolated GEMVs, 1B/8B decode shapes):
     //   cost = waves * (0.06 us per KiB of the CTA's weight bytes * eff(tile)
-    //                   + 2.1 us for the split-K handoff when parts > 1)
+    //                   + 0.8 us per item + 2.1 us for the split-K handoff when parts > 1)
     // with waves = ceil(items / CTA slots).  eff is the relative cost of a weight byte,
     // set by how many rows share each staged x chunk (V): 1.4, 1.1, 1.0 for V = 1, 2, 4.
+    // The per-item term is each row block's reduction, store and pipeline turn: without it
+    // the model chose 16-row blocks for a lone 14336 x 4096 (12.4 us; 64-row blocks 10.7)
+    // and 22016 x 4096 (17.1 us; 32-row blocks 14.8).
     Tile tile = kTiles[0];
     int best_parts = 1;
     double best = 1e30;
@@ -797,7 +800,7 @@ cudaError_t gemv_tma_launch_group(const Problem* ps, int count, const LaunchCtx&
             const int64_t items = blocks_t * ((kstages + tpp - 1) / tpp);
             const double waves = (double)((items + slots - 1) / slots);
             const double kib = (double)rbt * tpp * kSRB / 1024.0;
-            const double cost = waves * (0.06 * kib * eff + (parts > 1 ? 2.1 : 0.0));
+            const double cost = waves * (0.06 * kib * eff + 0.8 + (parts > 1 ? 2.1 : 0.0));
             if (cost < best * 0.999) best = cost, tile = t, best_parts = parts;
         }
     }
