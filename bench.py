@@ -48,10 +48,10 @@ HEADLINE = "8b"
 # --profile launch:<model>:<kind>, each launch on its own cold weights).  Valid only for
 # the kernel source they were taken with (sha256 prefix of gemv_tma.cu + ptx.cuh); any
 # other source reports null.
-LAUNCH_TRAFFIC = {"source_sha256": "a7de575055abd084", "bytes": {
-    "8b:qkv": 14204928, "8b:o": 9482240, "8b:gateup": 66211840, "8b:down": 33116416,
-    "8b:lm_head": 298932480, "1b:qkv": 3575552, "1b:o": 2395904, "1b:gateup": 18919936,
-    "1b:down": 9503488, "1b:lm_head": 150932736}}
+LAUNCH_TRAFFIC = {"source_sha256": "bf2bb3ca751c649a", "bytes": {
+    "8b:qkv": 14204928, "8b:o": 9482496, "8b:gateup": 66245376, "8b:down": 33116416,
+    "8b:lm_head": 299284224, "1b:qkv": 3575552, "1b:o": 2395904, "1b:gateup": 18920192,
+    "1b:down": 9503488, "1b:lm_head": 150921216}}
 
 
 def gemv_source_sha():
