@@ -24,13 +24,14 @@
 //     128 contiguous bytes of a weight row and 8 different 16-byte units of x, both
 //     conflict-free.  Partial sums stay in registers for the whole row; the CL chunk lanes
 //     of a row group are reduced with shuffles once per row block.
-// Arithmetic (X8 instances): the first time a CTA uses a 1024-k stage, its consumers
-// convert the staged x of that stage in place into 32-bit fixed point per 32-k chunk: with F the largest
-// exponent field of the chunk, q = round(x * 2^(157 - F)) (|q| < 2^31; exact for every
-// element within a factor 128 of the chunk's largest), stored as 4 byte slices.  A chunk's
-// dot product sum_k (c_k - 8) * q_k is then exact integer arithmetic: 8 dp4a per 8 codes
-// (codes as unsigned bytes, one nibble mask each), with the -8 offset folded into the
-// accumulators' starting values (-8 * sum_k q_k, split into two 16-bit halves); it is
+// Arithmetic (X8 instances): a tenth warp converts the staged x, stage by stage, in place
+// into 32-bit fixed point per 32-k chunk (one chunk per lane, all in registers): with F
+// the largest exponent field of the chunk, q = round(x * 2^(157 - F)) (|q| < 2^31; exact
+// for every element within a factor 128 of the chunk's largest), stored as 4 byte slices;
+// the consumers wait for a stage's conversion (its own mbarrier) at its first use.  A
+// chunk's dot product sum_k (c_k - 8) * q_k is then exact integer arithmetic: 8 dp4a per 8
+// codes (codes as unsigned bytes, one nibble mask each), with the -8 offset folded into
+// the accumulators' starting values (-8 * sum_k q_k, split into two 16-bit halves); it is
 // rounded once to fp32, scaled by 2^(F - 157) (exact) and accumulated with the group scale
 // in fp32.  A stage holding Inf or NaN (IEEE propagation is unchanged) or a chunk with a
 // nonzero element more than 2^13 below the chunk's largest keeps its fp32 values and takes
@@ -62,6 +63,7 @@ using namespace ptx;
 constexpr int kCWarps = 8;                 // consumer warps: 2 per SM sub-partition
 constexpr int kCThreads = 32 * kCWarps;
 constexpr int kThreadsG = kCThreads + 32;  // + the producer warp
+constexpr int kThreadsX8 = kThreadsG + 32; // + the x conversion warp (fixed-point instances)
 // A consumer thread is (row group, chunk lane): CL chunk lanes (16 or 32) per row group,
 // kCThreads / CL row groups of V rows each, so a row block has kCThreads / CL * V rows.
 __host__ __device__ constexpr int rows_per_block(int V, int CL) { return kCThreads / CL * V; }
@@ -272,19 +274,6 @@ __device__ __forceinline__ float chunk_dot_f32(const uint4& wv, const uint4 (&xu
     return EH ? fmaf(d.x, 0.0625f, d.y) : fmaf(d.y, 0.0625f, d.x);
 }
 
-// OR of `v` over the 256 consumer threads (named barrier 1; the producer warp does not take
-// part).
-__device__ __forceinline__ bool consumers_any(bool v) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.or.pred q, 1, %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
-        : "=r"(r)
-        : "r"((uint32_t)v), "r"(kCThreads)
-        : "memory");
-    return r != 0;
-}
-
 // Fixed-point chunk dot: sum_k (c_k - 8) * q_k of one chunk, exact, rounded once to fp32.
 // xu[2w] = (s0e, s1e, s0o, s1o) and xu[2w+1] = (s2e, s3e, s2o, s3o) for word w: slice s
 // (byte 3 - s of q, slice 0 signed) of the even / odd k of the word, one byte per k.
@@ -313,67 +302,69 @@ __device__ __forceinline__ float chunk_dot_x8(const uint4& wv, const uint4 (&xu)
     return fmaf((float)hi_v, 65536.f, (float)lo_v);
 }
 
-// Converts stage ks of the staged x in place, unless one of its chunks holds an Inf or NaN
-// (largest exponent field 255) or a nonzero element more than 2^13 below the chunk's
-// largest: then the whole stage stays fp32 and false is returned (the same on every
-// consumer thread).  Converted elements keep at least 18 significant bits (relative error
-// <= 2^-18; exact within a factor 128 of the chunk's largest), for any input.  Consumer
-// thread t takes unit t % 8 (4 consecutive k) of chunk row t / 8 of the stage (the 8
-// threads of a chunk are consecutive lanes of one warp) and lane 0 of each chunk writes
-// its metadata (factor 2^(F - 157), the two offsets).  Ends with the consumers' barrier.
-__device__ __forceinline__ bool convert_x_stage(uint32_t xa, uint32_t meta, int ks, int t) {
-    const int c = ks * kSC + (t >> 3), u = t & 7;
-    const uint32_t addr = x_unit(xa, c, u);
-    const uint4 raw = ld_shared_v4(addr);
-    const uint32_t b[4] = {raw.x, raw.y, raw.z, raw.w};
-    uint32_t F = 0, E = 255;  // largest exponent field; smallest of the nonzero elements
+// 4 x 4 byte transpose: out[s] holds byte 3 - s of a, b, c, d (in that byte order), so
+// out[0] is the top (signed) byte slice of the four values and out[3] the lowest.
+__device__ __forceinline__ void byte_slices(uint32_t a, uint32_t b, uint32_t c, uint32_t d,
+                                            uint32_t (&out)[4]) {
+    const uint32_t t0 = prmt(a, b, 0x5140u), t1 = prmt(a, b, 0x7362u);
+    const uint32_t t2 = prmt(c, d, 0x5140u), t3 = prmt(c, d, 0x7362u);
+    out[3] = prmt(t0, t2, 0x5410u);
+    out[2] = prmt(t0, t2, 0x7632u);
+    out[1] = prmt(t1, t3, 0x5410u);
+    out[0] = prmt(t1, t3, 0x7632u);
+}
+
+// The conversion warp's share of stage ks: lane j converts 32-k chunk c = 32 ks + j of
+// the staged x in place, on its own (the whole chunk in registers: no shuffles, no CTA
+// barrier), into the fixed-point layout that chunk_dot_x8 reads: with F the chunk's largest exponent field,
+// q = round(x * 2^(157 - max(F, 31))), unit 2w = (s0e, s1e, s0o, s1o) and unit 2w + 1 =
+// (s2e, s3e, s2o, s3o) for word w, where sXe / sXo is slice X (byte 3 - X of q) of the even
+// / odd k of the word, one byte per k in k order; metadata (factor, -8 sum(q >> 16),
+// -8 sum(q & 0xFFFF), 1).  If any chunk of the stage holds an Inf or NaN or a nonzero
+// element more than 2^13 below its chunk's largest, the whole stage stays fp32 and every
+// chunk's metadata word 3 is 0.  Returns whether the stage was converted.
+__device__ __forceinline__ bool convert_x_chunk_lane(uint32_t xa, uint32_t meta, int ks, int lane) {
+    const int c = ks * kSC + lane;
+    uint32_t b[32];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+    for (int u = 0; u < 8; ++u) {
+        const uint4 r = ld_shared_v4(x_unit(xa, c, u));
+        b[4 * u] = r.x, b[4 * u + 1] = r.y, b[4 * u + 2] = r.z, b[4 * u + 3] = r.w;
+    }
+    uint32_t F = 0, E = 255;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
         const uint32_t f = (b[i] >> 23) & 0xFFu;
         F = max(F, f);
         E = min(E, (b[i] & 0x7FFFFFFFu) ? max(f, 1u) : 255u);
     }
-#pragma unroll
-    for (int o = 1; o < 8; o <<= 1) {
-        F = max(F, __shfl_xor_sync(0xffffffffu, F, o));
-        E = min(E, __shfl_xor_sync(0xffffffffu, E, o));
+    const bool keep = __any_sync(0xffffffffu, F == 255u || E + 13u < F);
+    if (keep) {
+        st_shared_v4(meta + (uint32_t)c * kMetaBytes, 0u, 0u, 0u, 0u);
+        return false;
     }
-    const bool keep_f32 = consumers_any(F == 255u || E + 13u < F);
-    const uint32_t Fm = max(F, 31u);  // 2^(157 - Fm) and 2^(Fm - 157) stay normal floats
+    const uint32_t Fm = max(F, 31u);
     const float mul = __uint_as_float((284u - min(Fm, 254u)) << 23);
-    int q[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) q[i] = __float2int_rn(__uint_as_float(b[i]) * mul);
-    // Lane pair (2w, 2w + 1) holds word w (8 k); this lane's half h holds k % 8 = 4h .. 4h+3.
-    // Bytes of slices 0/1 (e01) and 2/3 (e23) of the even k, and likewise of the odd k;
-    // half 0 keeps slices 0/1 and sends 2/3, half 1 the other way round.
-    const int h = u & 1;
-    const uint32_t sel_keep = h ? 0x4051u : 0x6273u, sel_send = h ? 0x6273u : 0x4051u;
-    const uint32_t e_keep = prmt((uint32_t)q[0], (uint32_t)q[2], sel_keep);
-    const uint32_t o_keep = prmt((uint32_t)q[1], (uint32_t)q[3], sel_keep);
-    const uint32_t e_recv =
-        __shfl_xor_sync(0xffffffffu, prmt((uint32_t)q[0], (uint32_t)q[2], sel_send), 1);
-    const uint32_t o_recv =
-        __shfl_xor_sync(0xffffffffu, prmt((uint32_t)q[1], (uint32_t)q[3], sel_send), 1);
-    // Half 0's bytes (k % 8 = 0, 2 or 1, 3) go first in each register.
-    const uint32_t s_lo = h ? 0x1054u : 0x5410u, s_hi = h ? 0x3276u : 0x7632u;
     int qh = 0, ql = 0;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) qh += q[i] >> 16, ql += q[i] & 0xFFFF;
+    for (int w = 0; w < 4; ++w) {
+        uint32_t q[8];
 #pragma unroll
-    for (int o = 1; o < 8; o <<= 1) {
-        qh += __shfl_xor_sync(0xffffffffu, qh, o);
-        ql += __shfl_xor_sync(0xffffffffu, ql, o);
+        for (int i = 0; i < 8; ++i) {
+            const int v = __float2int_rn(__uint_as_float(b[8 * w + i]) * mul);
+            q[i] = (uint32_t)v;
+            qh += v >> 16;
+            ql += v & 0xFFFF;
+        }
+        uint32_t e[4], o[4];
+        byte_slices(q[0], q[2], q[4], q[6], e);
+        byte_slices(q[1], q[3], q[5], q[7], o);
+        st_shared_v4(x_unit(xa, c, 2 * w), e[0], e[1], o[0], o[1]);
+        st_shared_v4(x_unit(xa, c, 2 * w + 1), e[2], e[3], o[2], o[3]);
     }
-    if (!keep_f32) {
-        st_shared_v4(addr, prmt(e_keep, e_recv, s_lo), prmt(e_keep, e_recv, s_hi),
-                     prmt(o_keep, o_recv, s_lo), prmt(o_keep, o_recv, s_hi));
-        if (u == 0)
-            st_shared_v4(meta + (uint32_t)c * kMetaBytes, (Fm - 30u) << 23, (uint32_t)(-8 * qh),
-                         (uint32_t)(-8 * ql), 0u);
-    }
-    asm volatile("bar.sync 1, %0;" ::"r"(kCThreads) : "memory");
-    return !keep_f32;
+    st_shared_v4(meta + (uint32_t)c * kMetaBytes, (Fm - 30u) << 23, (uint32_t)(-8 * qh),
+                 (uint32_t)(-8 * ql), 1u);
+    return true;
 }
 
 // One chunk of a stage for a thread's V rows: x chunk c from the staged x, the V rows'
@@ -397,7 +388,7 @@ __device__ __forceinline__ void stage_chunk(uint32_t xa, int c, const uint4& md,
 }
 
 template <int V, int CL, bool EH, bool PC, bool F16, bool X8>
-__global__ void __launch_bounds__(kThreadsG, 2)
+__global__ void __launch_bounds__(X8 ? kThreadsX8 : kThreadsG, 2)
     gemv_tma_kernel(const __grid_constant__ TensorMaps tmaps, const GArgs a) {
     constexpr int rb = rows_per_block(V, CL);  // row groups of V rows
     constexpr int H = kSC / CL;                // chunks of a stage per chunk lane
@@ -414,12 +405,16 @@ __global__ void __launch_bounds__(kThreadsG, 2)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     auto full = [&](int s) { return bar_base + 8u * s; };
     auto empty = [&](int s) { return bar_base + 8u * (kMaxStages + s); };
+    // X8: stage ks of x converted by the conversion warp (its 32 lanes arrive).
+    auto xconv = [&](int ks) { return bar_base + 256u + 8u * ks; };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(full(s), 1);
             mbar_init(empty(s), kCWarps);
         }
+        if (X8)
+            for (int ks = 0; ks < a.kstages; ++ks) mbar_init(xconv(ks), 32);
         *failed = 0;
         mbar_init_fence();
     }
@@ -476,6 +471,18 @@ __global__ void __launch_bounds__(kThreadsG, 2)
         }
         return;
     }
+    if (X8 && warp == kCWarps + 1) {
+        // ------------------------------------------------ x conversion (X8 instances)
+        // Once the consumers have staged x, convert it stage by stage, in the order the
+        // consumers first use the stages, off their critical path; stage ks is released
+        // to them by its barrier (every lane arrives after its stores).
+        asm volatile("bar.sync 2, %0;" ::"r"(kCThreads + 32) : "memory");
+        for (int ks = 0; ks < a.kstages; ++ks) {
+            convert_x_chunk_lane(xa, meta, ks, lane);
+            mbar_arrive(xconv(ks));
+        }
+        return;
+    }
 
     // ------------------------------------------------------------------ consumers
     const int j = threadIdx.x & (CL - 1);    // chunk lane: chunks j, j + CL, ... of a stage
@@ -493,7 +500,11 @@ __global__ void __launch_bounds__(kThreadsG, 2)
                         in ? 16u : 0u);
         }
         cp_async_wait_all();
-        asm volatile("bar.sync 1, %0;" ::"r"(kCThreads) : "memory");
+        // X8: the conversion warp takes part (it starts on x once every unit is here).
+        if (X8)
+            asm volatile("bar.sync 2, %0;" ::"r"(kCThreads + 32) : "memory");
+        else
+            asm volatile("bar.sync 1, %0;" ::"r"(kCThreads) : "memory");
     }
 
     // Per row: fp32 partial sum, scaled per chunk by the group scale.
@@ -534,9 +545,15 @@ __global__ void __launch_bounds__(kThreadsG, 2)
     while (cur.valid(a)) {
         const int ks = cur.ks;
         if (X8 && !((x_ready >> ks) & 1u)) {
-            // First use of this stage of x by the CTA: convert it (its barriers are reached
-            // by every consumer thread whatever its state).
-            if (convert_x_stage(xa, meta, ks, threadIdx.x)) x_fixed |= 1u << ks;
+            // First use of this stage of x by the CTA: wait for the conversion warp; the
+            // metadata of the stage's first chunk says whether it was converted.
+            if (!dead &&
+                !__all_sync(0xffffffffu, wait_bounded(xconv(ks), 0u, a.wait_ns, failed))) {
+                if (lane == 0) record_failure(a.status, failed);
+                dead = true;
+            }
+            if (!dead && ld_shared_v4(meta + (uint32_t)(ks * kSC) * kMetaBytes).w != 0u)
+                x_fixed |= 1u << ks;
             x_ready |= 1u << ks;
         }
         const bool got =
@@ -630,7 +647,7 @@ cudaError_t launch_v(const TensorMaps& tm, const GArgs& a, unsigned grid, uint32
     if (attr != cudaSuccess) return attr;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kThreadsG);
+    cfg.blockDim = dim3(X8 ? kThreadsX8 : kThreadsG);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = c.stream;
     cudaLaunchAttribute attrs[1];
