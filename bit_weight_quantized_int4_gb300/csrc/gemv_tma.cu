@@ -331,13 +331,18 @@ __device__ __forceinline__ bool convert_x_chunk_lane(uint32_t xa, uint32_t meta,
         const uint4 r = ld_shared_v4(x_unit(xa, c, u));
         b[4 * u] = r.x, b[4 * u + 1] = r.y, b[4 * u + 2] = r.z, b[4 * u + 3] = r.w;
     }
-    uint32_t F = 0, E = 255;
+    // Largest exponent field F, and that of the smallest nonzero |x| (E; 255 when all are
+    // zero): unsigned order of |x|'s bit pattern is exponent order.  (|x| - 1 wraps a zero
+    // to the top, so the minimum skips zeros.)
+    uint32_t amax = 0, amin1 = 0xFFFFFFFFu;
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
-        const uint32_t f = (b[i] >> 23) & 0xFFu;
-        F = max(F, f);
-        E = min(E, (b[i] & 0x7FFFFFFFu) ? max(f, 1u) : 255u);
+        const uint32_t ab = b[i] & 0x7FFFFFFFu;
+        amax = max(amax, ab);
+        amin1 = min(amin1, ab - 1u);
     }
+    const uint32_t F = amax >> 23;
+    const uint32_t E = amin1 == 0xFFFFFFFFu ? 255u : max((amin1 + 1u) >> 23, 1u);
     const bool keep = __any_sync(0xffffffffu, F == 255u || E + 13u < F);
     if (keep) {
         st_shared_v4(meta + (uint32_t)c * kMetaBytes, 0u, 0u, 0u, 0u);
@@ -345,23 +350,26 @@ __device__ __forceinline__ bool convert_x_chunk_lane(uint32_t xa, uint32_t meta,
     }
     const uint32_t Fm = max(F, 31u);
     const float mul = __uint_as_float((284u - min(Fm, 254u)) << 23);
-    int qh = 0, ql = 0;
+    // Sums of the byte slices over the chunk (slice 0 signed): q >> 16 = 256 s0 + s1 and
+    // q & 0xFFFF = 256 s2 + s3, so the offsets come from 8 dp4a per word.
+    constexpr uint32_t kOnes = 0x01010101u;
+    int s0 = 0, s1 = 0, s2 = 0, s3 = 0;
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
         uint32_t q[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int v = __float2int_rn(__uint_as_float(b[8 * w + i]) * mul);
-            q[i] = (uint32_t)v;
-            qh += v >> 16;
-            ql += v & 0xFFFF;
-        }
+        for (int i = 0; i < 8; ++i) q[i] = (uint32_t)__float2int_rn(__uint_as_float(b[8 * w + i]) * mul);
         uint32_t e[4], o[4];
         byte_slices(q[0], q[2], q[4], q[6], e);
         byte_slices(q[1], q[3], q[5], q[7], o);
         st_shared_v4(x_unit(xa, c, 2 * w), e[0], e[1], o[0], o[1]);
         st_shared_v4(x_unit(xa, c, 2 * w + 1), e[2], e[3], o[2], o[3]);
+        s0 = dp4a_us(kOnes, e[0], dp4a_us(kOnes, o[0], s0));
+        s1 = dp4a_uu(kOnes, e[1], dp4a_uu(kOnes, o[1], s1));
+        s2 = dp4a_uu(kOnes, e[2], dp4a_uu(kOnes, o[2], s2));
+        s3 = dp4a_uu(kOnes, e[3], dp4a_uu(kOnes, o[3], s3));
     }
+    const int qh = s0 * 256 + s1, ql = s2 * 256 + s3;
     st_shared_v4(meta + (uint32_t)c * kMetaBytes, (Fm - 30u) << 23, (uint32_t)(-8 * qh),
                  (uint32_t)(-8 * ql), 1u);
     return true;
