@@ -48,10 +48,10 @@ HEADLINE = "8b"
 # --profile launch:<model>:<kind>, each launch on its own cold weights).  Valid only for
 # the kernel source they were taken with (sha256 prefix of gemv_tma.cu + ptx.cuh); any
 # other source reports null.
-LAUNCH_TRAFFIC = {"source_sha256": "bf2bb3ca751c649a", "bytes": {
-    "8b:qkv": 14204928, "8b:o": 9482496, "8b:gateup": 66245376, "8b:down": 33116416,
-    "8b:lm_head": 299284224, "1b:qkv": 3575552, "1b:o": 2395904, "1b:gateup": 18920192,
-    "1b:down": 9503488, "1b:lm_head": 150921216}}
+LAUNCH_TRAFFIC = {"source_sha256": "6a8131984faaeecc", "bytes": {
+    "8b:qkv": 14204928, "8b:o": 9482240, "8b:gateup": 66249216, "8b:down": 33116672,
+    "8b:lm_head": 298914560, "1b:qkv": 3575808, "1b:o": 2395904, "1b:gateup": 18920192,
+    "1b:down": 9503232, "1b:lm_head": 150925824}}
 
 
 def gemv_source_sha():
@@ -609,6 +609,13 @@ def cublas_tf32_tflops(torch, n=8192, reps=10):
         torch.backends.cuda.matmul.allow_tf32 = prev
 
 
+# The highest tf32 tensor rate seen on this part: a bare loop of tcgen05.mma kind::tf32
+# (128 x 256 x 8 MMAs, A in tensor memory, zero operands, no loads), measured once on a
+# GB300 at 2.07 GHz during development.  Reported beside the live cuBLAS figure, as the
+# tighter denominator.
+TF32_MMA_LOOP_TFLOPS = 1216.0
+
+
 def prefill_roofline(torch, handle, bf16_peak):
     """Per-shape prefill TFLOP/s (Llama-3.2-1B layer shapes at M = 128 / 512 / 2048,
     bias on all but k/v) against the tensor-core peaks, and the 16-layer prefill time."""
@@ -620,6 +627,7 @@ def prefill_roofline(torch, handle, bf16_peak):
             r = prefill_time(torch, handle, M, N, K, bias=(N != 512))
             r["frac_of_tf32_derived"] = round(r["TFLOP_s"] / tf32_derived, 4) if tf32_derived else None
             r["frac_of_tf32_cublas"] = round(r["TFLOP_s"] / tf32_cublas, 4)
+            r["frac_of_tf32_mma_loop"] = round(r["TFLOP_s"] / TF32_MMA_LOOP_TFLOPS, 4)
             r["frac_of_bf16"] = round(r["TFLOP_s"] / bf16_peak, 4) if bf16_peak else None
             shapes.append(r)
     layer16 = []
@@ -660,6 +668,10 @@ def prefill_roofline(torch, handle, bf16_peak):
             "tf32_derived_peak": tf32_derived,
             "tf32_derived_source": "bf16_tflops of the peaks file x 1.1/2.25 (nominal tf32 : bf16)",
             "frac_of_tf32_derived": round(top["TFLOP_s"] / tf32_derived, 4) if tf32_derived else None,
+            "tf32_mma_loop_peak": TF32_MMA_LOOP_TFLOPS,
+            "tf32_mma_loop_source": "bare tcgen05.mma kind::tf32 loop (128x256x8, A in TMEM), "
+                                    "measured once on this part at 2.07 GHz",
+            "frac_of_tf32_mma_loop": round(top["TFLOP_s"] / TF32_MMA_LOOP_TFLOPS, 4),
             "bf16_peak": bf16_peak,
             "frac_of_bf16": round(top["TFLOP_s"] / bf16_peak, 4) if bf16_peak else None,
             "timing": "median of >= 100 launches after >= 20 warm-up, weight copies rotated (HBM-cold)",
