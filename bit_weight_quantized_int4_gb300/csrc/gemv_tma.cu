@@ -779,7 +779,12 @@ bool gemv_tma_groupable(const Problem& a, const Problem& b) {
            (a.group_size >= a.K) == (b.group_size >= b.K);
 }
 
-cudaError_t gemv_tma_launch_group(const Problem* ps, int count, const LaunchCtx& c) {
+namespace {
+
+// Plans the launch of ps[0..count) (tile, split of K, grid, arithmetic) and, when `launch`,
+// enqueues it; *x8_out (if given) receives whether the fixed-point instances are chosen.
+cudaError_t gemv_group(const Problem* ps, int count, const LaunchCtx& c, bool launch,
+                       bool* x8_out) {
     EncodeTiledFn enc = tensor_map_encoder();
     if (!enc || count < 1 || count > kMaxMats) return cudaErrorNotSupported;
     const Problem& p0 = ps[0];
@@ -909,12 +914,25 @@ cudaError_t gemv_tma_launch_group(const Problem* ps, int count, const LaunchCtx&
     // 15 %, 8B gate/up 5 % faster; one block per CTA, as in q/k/v, o and down, 5-50 %
     // slower).
     const bool x8 = a.items >= 2 * (int64_t)grid;
+    if (x8_out) *x8_out = x8;
+    if (!launch) return cudaSuccess;
     return dispatch_tile(tile, p0.even_high != 0, pc, p0.scale_f16 != 0, x8, tm, a, grid, lay.total,
                          c);
 }
 
+}  // namespace
+
+cudaError_t gemv_tma_launch_group(const Problem* ps, int count, const LaunchCtx& c) {
+    return gemv_group(ps, count, c, true, nullptr);
+}
+
 cudaError_t gemv_tma_launch(const Problem& p, const LaunchCtx& c) {
-    return gemv_tma_launch_group(&p, 1, c);
+    return gemv_group(&p, 1, c, true, nullptr);
+}
+
+bool gemv_tma_fixed_point(const Problem& p, const LaunchCtx& c) {
+    bool x8 = false;
+    return gemv_group(&p, 1, c, false, &x8) == cudaSuccess && x8;
 }
 
 }  // namespace q4lin

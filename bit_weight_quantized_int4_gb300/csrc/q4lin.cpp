@@ -182,9 +182,10 @@ int kernel_of(const q4lin::Problem& p, const q4lin::LaunchCtx& c, int path) {
     switch (path) {
         case Q4LIN_PATH_TC: return q4lin::tc_uses_f16(p, c) ? Q4LIN_KERNEL_TC_F16 : Q4LIN_KERNEL_TC;
         case Q4LIN_PATH_GEMV:
-            return q4lin::gemv_tma_eligible(p) ? Q4LIN_KERNEL_GEMV_TMA
-                   : multirow_preferred(p)     ? Q4LIN_KERNEL_MULTIROW
-                                               : Q4LIN_KERNEL_ROWSTREAM;
+            if (q4lin::gemv_tma_eligible(p))
+                return q4lin::gemv_tma_fixed_point(p, c) ? Q4LIN_KERNEL_GEMV_TMA_FIXED
+                                                         : Q4LIN_KERNEL_GEMV_TMA;
+            return multirow_preferred(p) ? Q4LIN_KERNEL_MULTIROW : Q4LIN_KERNEL_ROWSTREAM;
         default: return Q4LIN_KERNEL_GENERIC;
     }
 }
@@ -303,7 +304,8 @@ q4lin_status_t q4lin_run(q4lin_handle_t h, const float* x, const uint8_t* qweigh
     switch (kernel_of(p, c, path)) {
         case Q4LIN_KERNEL_TC:
         case Q4LIN_KERNEL_TC_F16: err = q4lin::tc_launch(p, c); break;
-        case Q4LIN_KERNEL_GEMV_TMA: err = q4lin::gemv_tma_launch(p, c); break;
+        case Q4LIN_KERNEL_GEMV_TMA:
+        case Q4LIN_KERNEL_GEMV_TMA_FIXED: err = q4lin::gemv_tma_launch(p, c); break;
         case Q4LIN_KERNEL_MULTIROW: err = q4lin::gemv_mr_launch(p, c); break;
         case Q4LIN_KERNEL_ROWSTREAM: err = q4lin::rowstream_launch(p, c); break;
         default: err = q4lin::generic_launch(p, c); break;

@@ -84,6 +84,10 @@ constexpr int kGemvMaxParts = 8;
 // qweight, and group_size % 32 == 0 or group_size >= K.
 bool gemv_tma_eligible(const Problem& p);
 cudaError_t gemv_tma_launch(const Problem& p, const LaunchCtx& c);
+// Whether gemv_tma_launch would run the problem with the exact fixed-point arithmetic (x
+// as 32-bit fixed point per 32-k chunk, dp4a): when its CTAs process at least two row
+// blocks each.
+bool gemv_tma_fixed_point(const Problem& p, const LaunchCtx& c);
 // Several eligible M = 1 problems that share x, K, group size, scale dtype and nibble
 // order in one launch (at most gemv_tma_max_group()).
 int gemv_tma_max_group();

@@ -46,8 +46,9 @@ Q4LIN_KERNEL_ROWSTREAM = 3
 Q4LIN_KERNEL_GENERIC = 4
 Q4LIN_KERNEL_TC = 5
 Q4LIN_KERNEL_TC_F16 = 6
+Q4LIN_KERNEL_GEMV_TMA_FIXED = 7
 KERNEL_NAMES = {0: "none", 1: "gemv_tma", 2: "multirow", 3: "rowstream", 4: "generic",
-                5: "tc", 6: "tc_f16"}
+                5: "tc", 6: "tc_f16", 7: "gemv_tma_fixed"}
 
 Q4LIN_OPT_FORCE_PATH = 1
 Q4LIN_OPT_NIBBLE_EVEN_HIGH = 2

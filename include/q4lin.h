@@ -259,7 +259,10 @@ typedef enum {
     Q4LIN_KERNEL_ROWSTREAM = 3, /* row-streaming CUDA-core kernel (small M)                */
     Q4LIN_KERNEL_GENERIC = 4,   /* generic CUDA-core kernel (any K, group size, alignment) */
     Q4LIN_KERNEL_TC = 5,        /* tcgen05 tensor-core GEMM, tf32 operands                 */
-    Q4LIN_KERNEL_TC_F16 = 6     /* the same with fp16 operands (Q4LIN_OPT_TC_F16)          */
+    Q4LIN_KERNEL_TC_F16 = 6,    /* the same with fp16 operands (Q4LIN_OPT_TC_F16)          */
+    Q4LIN_KERNEL_GEMV_TMA_FIXED = 7 /* the decode GEMV with exact fixed-point arithmetic: x as
+                                     * 32-bit fixed point per 32-k chunk, codes times x by
+                                     * dp4a; chosen when its CTAs take >= 2 row blocks each */
 } q4lin_kernel_t;
 
 /* The kernel q4lin_run would launch for these arguments (no launch, no device access);

@@ -586,12 +586,24 @@ def test_multirow_bounded_wait_times_out_cleanly(handle):
 
 
 # ------------------------------------------- decode GEMV: fixed-point (dp4a) arithmetic
-# Shapes with at least two 16-row blocks per CTA (here 8192 x 2048 and 14336 x 4096, 32-row
-# blocks) take the decode GEMV's fixed-point path: x converted per 32-k chunk to 32-bit
-# fixed point, exact integer dot products of the codes (dp4a), one rounding per chunk.
-# Chunks with Inf / NaN, or with a nonzero element more than 2^13 below the chunk's
-# largest, stay on the fp32 path.
-X8_SHAPES = [(8192, 2048), (14336, 4096)]
+# Shapes whose CTAs take at least two row blocks each (here 49152 x 2048, 64-row blocks,
+# and 28672 x 4096, 32-row blocks) run the decode GEMV's fixed-point arithmetic: x converted
+# per 32-k chunk to 32-bit fixed point, exact integer dot products of the codes (dp4a), one
+# rounding per chunk.  A stage with Inf / NaN, or with a nonzero element more than 2^13
+# below its chunk's largest, stays on the fp32 path.  Every test checks that the planner
+# chose the fixed-point kernel.
+X8_SHAPES = [(49152, 2048), (28672, 4096)]
+X8_N, X8_K = X8_SHAPES[0]
+
+
+def _assert_fixed_point(handle, c):
+    assert _kernel_of(handle, c) == "gemv_tma_fixed", "the shape no longer takes the fixed-point path"
+
+
+def test_gemv_small_launch_stays_fp32(handle):
+    """One row block per CTA: the conversion of x would not pay, the fp32 loop runs."""
+    c = synth.make_case(1, 8192, 2048, 32, scale_f16=True, bias=True, seed=17)
+    assert _kernel_of(handle, c) == "gemv_tma"
 
 
 @pytest.mark.parametrize("N,K", X8_SHAPES)
@@ -599,6 +611,7 @@ X8_SHAPES = [(8192, 2048), (14336, 4096)]
 def test_gemv_fixed_point_dyadic_bit_exact(handle, N, K, gs, f16):
     gs = gs or K
     c = synth.make_dyadic_case(1, N, K, gs, scale_f16=f16, bias=True, seed=N + gs)
+    _assert_fixed_point(handle, c)
     out, used = run_q4lin(handle, c, AUTO)
     assert used == GEMV
     ref, _ = oracle.linear(c.x, c.qweight, c.scales, c.bias, c.K, c.group_size)
@@ -606,8 +619,9 @@ def test_gemv_fixed_point_dyadic_bit_exact(handle, N, K, gs, f16):
 
 
 def test_gemv_fixed_point_all_codes_eight_gives_bias(handle):
-    c = synth.make_case(1, 8192, 2048, 32, scale_f16=True, bias=True, seed=19)
-    c.qweight = synth.fill_codes(8192, 2048, 8)
+    c = synth.make_case(1, X8_N, X8_K, 32, scale_f16=True, bias=True, seed=19)
+    c.qweight = synth.fill_codes(X8_N, X8_K, 8)
+    _assert_fixed_point(handle, c)
     out, _ = run_q4lin(handle, c, AUTO)
     np.testing.assert_array_equal(out, np.broadcast_to(c.bias, out.shape))
 
@@ -615,6 +629,7 @@ def test_gemv_fixed_point_all_codes_eight_gives_bias(handle):
 @pytest.mark.parametrize("N,K", X8_SHAPES)
 def test_gemv_fixed_point_even_high(handle, N, K):
     c = synth.make_case(1, N, K, 32, scale_f16=True, bias=True, seed=23)
+    _assert_fixed_point(handle, c)
     check_case(handle, c, AUTO, even_high=True)
 
 
@@ -635,7 +650,8 @@ def test_gemv_fixed_point_non_finite_x(handle, case):
     """Inf and NaN in x propagate as in IEEE arithmetic (Inf * 0 = NaN, Inf - Inf = NaN),
     element by element as the fp64 oracle computes them; the other chunks of the same
     launch stay on the fixed-point path."""
-    c = synth.make_case(1, 8192, 2048, 32, scale_f16=True, bias=True, seed=29)
+    c = synth.make_case(1, X8_N, X8_K, 32, scale_f16=True, bias=True, seed=29)
+    _assert_fixed_point(handle, c)
     x = c.x.copy()
     if case == "pos_inf":
         x[0, 5] = np.inf
@@ -659,8 +675,9 @@ def test_gemv_fixed_point_dynamic_range(handle, ratio):
     of the rows that element's code is 8 (weight 0), so the tolerance comes only from the
     small elements: chunks within 2^13 of their largest are converted to fixed point
     (relative error <= 2^-18 per element), wider ones stay fp32; both stay in the bar."""
-    N, K = 8192, 2048
+    N, K = X8_N, X8_K
     c = synth.make_case(1, N, K, 32, scale_f16=True, bias=True, seed=int(ratio) % 1000)
+    _assert_fixed_point(handle, c)
     x = c.x.copy()
     x[0, 7::32] *= ratio
     c.x = x
@@ -676,8 +693,9 @@ def test_gemv_fixed_point_dynamic_range(handle, ratio):
 
 def test_gemv_fixed_point_zero_and_subnormal_chunks(handle):
     """All-zero chunks, subnormal x and a chunk of equal values convert without error."""
-    N, K = 8192, 2048
+    N, K = X8_N, X8_K
     c = synth.make_case(1, N, K, 32, scale_f16=False, bias=True, seed=37)
+    _assert_fixed_point(handle, c)
     x = c.x.copy()
     x[0, :64] = 0.0
     x[0, 64:96] = np.float32(1e-40)
