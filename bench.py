@@ -48,10 +48,10 @@ HEADLINE = "8b"
 # --profile launch:<model>:<kind>, each launch on its own cold weights).  Valid only for
 # the kernel source they were taken with (sha256 prefix of gemv_tma.cu + ptx.cuh); any
 # other source reports null.
-LAUNCH_TRAFFIC = {"source_sha256": "b45d2d82f8031b16", "bytes": {
-    "8b:qkv": 14205184, "8b:o": 9482496, "8b:gateup": 66251776, "8b:down": 33116416,
-    "8b:lm_head": 298860288, "1b:qkv": 3575808, "1b:o": 2396160, "1b:gateup": 18919936,
-    "1b:down": 9503232, "1b:lm_head": 150581760}}
+LAUNCH_TRAFFIC = {"source_sha256": "4c930f7237251a48", "bytes": {
+    "8b:qkv": 14205184, "8b:o": 9482496, "8b:gateup": 66215168, "8b:down": 33116416,
+    "8b:lm_head": 298932736, "1b:qkv": 3575552, "1b:o": 2396160, "1b:gateup": 18919936,
+    "1b:down": 9503232, "1b:lm_head": 150863872}}
 
 
 def gemv_source_sha():
