@@ -12,7 +12,9 @@
 //   producer warp (one lane): per stage, 2D TMA copies of the weight tile [rb rows x 512
 //     bytes] (= 1024 k per row; the packed matrix viewed as 16-bit elements, so one box
 //     spans the 512 bytes) and of the matching block of group scales [1024 / group size
-//     groups x rb rows], all on one mbarrier, into a ring of 2..8 stages.  Weight rows
+//     groups x rb rows], all on one mbarrier, into a ring of 2..8 stages (the first
+//     stage alone, then the rest of the ring once it has landed, so that every CTA's
+//     first stage is ahead of the grid's later ones in the memory queues).  Weight rows
 //     are long contiguous segments, so DRAM sees streaming reads.
 //   8 consumer warps (256 threads): thread = (chunk lane j of CL, row group of V rows),
 //     with (V, CL) = (2, 32) or (4, 32) for blocks of 16 or 32 rows and (4, 16) for 64;
@@ -38,8 +40,8 @@
 // the fp32 path, so every converted element has a relative error <= 2^-18.  fp32 instances
 // (and such stages): the codes widened to exact floats by a byte permute
 // (0x4B0000cc = 2^23 + c) and one packed add, fp32 FMA.
-// A CTA is small enough (288 threads, at most 113 KiB of shared memory) that two fit on
-// one SM: the CTAs of the next kernel on the stream can become resident while this one
+// A CTA is small enough (288 threads, 320 with the conversion warp, at most 113 KiB of
+// shared memory) that two fit on one SM: the CTAs of the next kernel on the stream can become resident while this one
 // runs.  With programmatic dependent launch their producers then stream weights and
 // scales (which do not depend on the preceding kernel) before griddepcontrol.wait; x,
 // bias, out and the split-K workspace are touched only after it.

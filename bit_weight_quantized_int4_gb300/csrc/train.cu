@@ -23,8 +23,12 @@
 //     256 k, fed by a producer warp that streams per stage the weight tile [64 rows x
 //     128 B], the group scales of those rows [groups of the tile x 64] and d_out
 //     [MT x 64] into a shared-memory ring with one TMA copy each; 8 consumer warps take
-//     every 8th row of a stage (lane = 32-bit word of codes, 8 k).  The rows are split
-//     over CTAs (multiples of 64 rows each); partials are added like above.
+//     every 8th row of a stage (lane = 32-bit word of codes, 8 k).  The weight and scale
+//     copies of the first ring of stages go out before the grid-dependency wait, their
+//     d_out copies after it.  The rows are split over CTAs (multiples of 64 rows each);
+//     when each CTA has at most 4 stages, the splits of a k tile are one thread-block
+//     cluster that adds its partial tiles through distributed shared memory (in rank
+//     order), else the partials are added through the workspace like above.
 //   backward_dx_generic_kernel: one thread per (m, k), n ascending; any K, any group size,
 //     any alignment.
 //
