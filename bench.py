@@ -46,20 +46,22 @@ HEADLINE = "8b"
 # DRAM bytes (read + written) of one launch of each launch shape of a decode token, from
 # one-launch ncu captures (dram__bytes_read.sum + dram__bytes_write.sum; bench.py
 # --profile launch:<model>:<kind>, each launch on its own cold weights).  Valid only for
-# the kernel source they were taken with (sha256 prefix of gemv_tma.cu + ptx.cuh); any
-# other source reports null.
-LAUNCH_TRAFFIC = {"source_sha256": "4c930f7237251a48", "bytes": {
+# the kernel code they were taken with (gemv_source_sha); any other code reports null.
+LAUNCH_TRAFFIC = {"source_sha256": "0c479fce6af1e274", "bytes": {
     "8b:qkv": 14205184, "8b:o": 9482496, "8b:gateup": 66215168, "8b:down": 33116416,
     "8b:lm_head": 298932736, "1b:qkv": 3575552, "1b:o": 2396160, "1b:gateup": 18919936,
     "1b:down": 9503232, "1b:lm_head": 150863872}}
 
 
 def gemv_source_sha():
+    """sha256 prefix of the decode GEMV's code (gemv_tma.cu + ptx.cuh with // comments and
+    blank lines removed: a comment edit does not invalidate the traffic captures)."""
     import hashlib
     h = hashlib.sha256()
     for f in ("gemv_tma.cu", "ptx.cuh"):
-        with open(os.path.join(ROOT, "bit_weight_quantized_int4_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "bit_weight_quantized_int4_gb300", "csrc", f)) as fh:
+            code = [ln.split("//", 1)[0].rstrip() for ln in fh.read().splitlines()]
+        h.update(("\n".join(ln for ln in code if ln) + "\n").encode())
     return h.hexdigest()[:16]
 
 
