@@ -47,10 +47,10 @@ HEADLINE = "8b"
 # one-launch ncu captures (dram__bytes_read.sum + dram__bytes_write.sum; bench.py
 # --profile launch:<model>:<kind>, each launch on its own cold weights).  Valid only for
 # the kernel code they were taken with (gemv_source_sha); any other code reports null.
-LAUNCH_TRAFFIC = {"source_sha256": "0c479fce6af1e274", "bytes": {
-    "8b:qkv": 14205184, "8b:o": 9482496, "8b:gateup": 66215168, "8b:down": 33116416,
-    "8b:lm_head": 298932736, "1b:qkv": 3575552, "1b:o": 2396160, "1b:gateup": 18919936,
-    "1b:down": 9503232, "1b:lm_head": 150863872}}
+LAUNCH_TRAFFIC = {"source_sha256": "05abcd38b1feb287", "bytes": {
+    "8b:qkv": 14204928, "8b:o": 9482240, "8b:gateup": 66233600, "8b:down": 33116672,
+    "8b:lm_head": 299207424, "1b:qkv": 3575808, "1b:o": 2396160, "1b:gateup": 18921984,
+    "1b:down": 9507584, "1b:lm_head": 150888448}}
 
 
 def gemv_source_sha():

@@ -815,25 +815,41 @@ cudaError_t gemv_group(const Problem* ps, int count, const LaunchCtx& c, bool la
     // The per-item term is each row block's reduction, store and pipeline turn: without it
     // the model chose 16-row blocks for a lone 14336 x 4096 (12.4 us; 64-row blocks 10.7)
     // and 22016 x 4096 (17.1 us; 32-row blocks 14.8).
+    // Parts of at least 2048 k are weighed first.  Only when that picks a split are the finer
+    // counts, down to one 1024-k stage per part, weighed too, and they win a tie: once K is
+    // split, finer parts measured faster (2048 x 8192: 64-row blocks in 8 parts 5.86 us,
+    // 32-row blocks in 4 parts 6.07; 512 x 8192 4.43 against 4.87), while turning an unsplit
+    // plan into a split did not (1000 x 7168 in 4 parts 5.05 us, unsplit 4.76).
     Tile tile = kTiles[0];
     int best_parts = 1;
     double best = 1e30;
-    for (const Tile t : kTiles) {
-        const int rbt = t.rows();
-        if (stages_for(rbt) < 2) continue;
-        const int64_t blocks_t = blocks_for(rbt);
-        const double eff = t.V == 1 ? 1.4 : (t.V == 2 ? 1.1 : 1.0);
-        for (int parts = 1; parts <= kGemvMaxParts; parts *= 2) {
-            if (parts > 1 && (kstages * 1024 / parts < 2048 || !c.ws || !c.tickets ||
-                              (int64_t)parts * blocks_t * rbt > c.ws_floats ||
-                              blocks_t > c.ticket_count))
-                break;
-            const int tpp = (kstages + parts - 1) / parts;
-            const int64_t items = blocks_t * ((kstages + tpp - 1) / tpp);
-            const double waves = (double)((items + slots - 1) / slots);
-            const double kib = (double)rbt * tpp * kSRB / 1024.0;
-            const double cost = waves * (0.06 * kib * eff + 0.8 + (parts > 1 ? 2.1 : 0.0));
-            if (cost < best * 0.999) best = cost, tile = t, best_parts = parts;
+    bool fine_taken = false;
+    for (int pass = 0; pass < 2 && (pass == 0 || best_parts > 1); ++pass) {
+        for (const Tile t : kTiles) {
+            const int rbt = t.rows();
+            if (stages_for(rbt) < 2) continue;
+            const int64_t blocks_t = blocks_for(rbt);
+            const double eff = t.V == 1 ? 1.4 : (t.V == 2 ? 1.1 : 1.0);
+            for (int parts = 1; parts <= kGemvMaxParts; parts *= 2) {
+                if (parts > 1 && (parts > kstages || !c.ws || !c.tickets ||
+                                  (int64_t)parts * blocks_t * rbt > c.ws_floats ||
+                                  blocks_t > c.ticket_count))
+                    break;
+                const bool fine = parts > 1 && kstages * 1024 / parts < 2048;
+                if (fine != (pass == 1)) {
+                    if (fine) break;
+                    continue;
+                }
+                const int tpp = (kstages + parts - 1) / parts;
+                const int64_t items = blocks_t * ((kstages + tpp - 1) / tpp);
+                const double waves = (double)((items + slots - 1) / slots);
+                const double kib = (double)rbt * tpp * kSRB / 1024.0;
+                const double cost = waves * (0.06 * kib * eff + 0.8 + (parts > 1 ? 2.1 : 0.0));
+                if (pass == 1 && !fine_taken ? cost <= best : cost < best * 0.999) {
+                    best = cost, tile = t, best_parts = parts;
+                    fine_taken = pass == 1;
+                }
+            }
         }
     }
     const int rb = tile.rows();
