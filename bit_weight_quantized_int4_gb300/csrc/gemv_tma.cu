@@ -21,8 +21,9 @@
 //     per stage it takes chunks j, j + CL, ... (32 codes each) of each of its V rows, and
 //     each x chunk it loads serves all V rows.
 //     x is staged whole in shared memory once per CTA after the dependency wait (every
-//     consumer thread copies 16-byte units, all in flight at once), unit u of 32-k
-//     chunk c at unit u ^ (c % 8) of the chunk's 128-byte row.  A quarter-warp then reads
+//     consumer thread copies 16-byte units, all in flight at once; the CTA's first stage
+//     is a copy group of its own, so computing starts once it has landed), unit u of
+//     32-k chunk c at unit u ^ (c % 8) of the chunk's 128-byte row.  A quarter-warp then reads
 //     128 contiguous bytes of a weight row and 8 different 16-byte units of x, both
 //     conflict-free.  Partial sums stay in registers for the whole row; the CL chunk lanes
 //     of a row group are reduced with shuffles once per row block.
@@ -430,6 +431,9 @@ __global__ void __launch_bounds__(X8 ? kThreadsX8 : kThreadsG, 2)
     }
     __syncthreads();
     griddep_launch_dependents();
+    // The stage of x this CTA uses first (its first item's first stage): it is copied
+    // (and converted) ahead of the rest of x.
+    const int ks_first = (int)blockIdx.x < a.items ? ((int)blockIdx.x % a.parts) * a.tpp : 0;
 
     if (warp == kCWarps) {
         // ------------------------------------------------------------ TMA producer
@@ -483,11 +487,16 @@ __global__ void __launch_bounds__(X8 ? kThreadsX8 : kThreadsG, 2)
     }
     if (X8 && warp == kCWarps + 1) {
         // ------------------------------------------------ x conversion (X8 instances)
-        // Once the consumers have staged x, convert it stage by stage, in the order the
-        // consumers first use the stages, off their critical path; stage ks is released
-        // to them by its barrier (every lane arrives after its stores).
+        // The first stage of x once the consumers have staged it (named barrier 2), then
+        // the rest once that has landed too (barrier 3), in the order the consumers first
+        // use the stages, off their critical path; stage ks is released to them by its
+        // mbarrier (every lane arrives after its stores).
         asm volatile("bar.sync 2, %0;" ::"r"(kCThreads + 32) : "memory");
-        for (int ks = 0; ks < a.kstages; ++ks) {
+        convert_x_chunk_lane(xa, meta, ks_first, lane);
+        mbar_arrive(xconv(ks_first));
+        asm volatile("bar.sync 3, %0;" ::"r"(kCThreads + 32) : "memory");
+        for (int q = 1, ks = ks_first; q < a.kstages; ++q) {
+            if (++ks == a.kstages) ks = 0;
             convert_x_chunk_lane(xa, meta, ks, lane);
             mbar_arrive(xconv(ks));
         }
@@ -499,23 +508,39 @@ __global__ void __launch_bounds__(X8 ? kThreadsX8 : kThreadsG, 2)
     const int r0 = (threadIdx.x / CL) * V;   // first of this thread's V rows in a block
     griddep_wait();  // x, bias, out and the workspace belong to the dependency chain
     // x into shared memory once: 16-byte unit i (k = 4 i .. 4 i + 3) of chunk i / 8 at its
-    // swizzled place, zero past K.  Asynchronous copies: all of a thread's units are in
-    // flight at once, whatever K.
-    {
-        const int units = a.kstages * kSC * 8;
-        for (int i = threadIdx.x; i < units; i += kCThreads) {
-            const bool in = 4 * (int64_t)i < a.K;
-            cp_async_16(x_unit(xa, i >> 3, i & 7),
-                        in ? static_cast<const void*>(reinterpret_cast<const float4*>(a.x) + i) : a.x,
-                        in ? 16u : 0u);
-        }
+    // swizzled place, zero past K.  Asynchronous copies, all in flight at once, one unit
+    // per thread and stage: the CTA's first stage as one group, the rest as a second, so
+    // that the consumers start on the first stage once it has landed.
+    auto copy_x_stage = [&](int ks) {
+        const int i = ks * kCThreads + threadIdx.x;
+        const bool in = 4 * (int64_t)i < a.K;
+        cp_async_16(x_unit(xa, i >> 3, i & 7),
+                    in ? static_cast<const void*>(reinterpret_cast<const float4*>(a.x) + i) : a.x,
+                    in ? 16u : 0u);
+    };
+    static_assert(kSC * 8 == kCThreads, "one 16-byte unit of x per consumer thread and stage");
+    copy_x_stage(ks_first);
+    cp_async_commit();
+    for (int ks = 0; ks < a.kstages; ++ks)
+        if (ks != ks_first) copy_x_stage(ks);
+    cp_async_commit();
+    cp_async_wait_group<1>();
+    // X8: the conversion warp takes part (it converts the first stage next).
+    if (X8)
+        asm volatile("bar.sync 2, %0;" ::"r"(kCThreads + 32) : "memory");
+    else
+        asm volatile("bar.sync 1, %0;" ::"r"(kCThreads) : "memory");
+    // The rest of x (possibly no copy): waited for at the first use of another stage, or
+    // before leaving; either way once, with the conversion warp's second barrier.
+    bool x_rest = false;
+    auto wait_x_rest = [&]() {
         cp_async_wait_all();
-        // X8: the conversion warp takes part (it starts on x once every unit is here).
         if (X8)
-            asm volatile("bar.sync 2, %0;" ::"r"(kCThreads + 32) : "memory");
+            asm volatile("bar.sync 3, %0;" ::"r"(kCThreads + 32) : "memory");
         else
             asm volatile("bar.sync 1, %0;" ::"r"(kCThreads) : "memory");
-    }
+        x_rest = true;
+    };
 
     // Per row: fp32 partial sum, scaled per chunk by the group scale.
     float acc[V];
@@ -554,6 +579,8 @@ __global__ void __launch_bounds__(X8 ? kThreadsX8 : kThreadsG, 2)
     bool dead = false;
     while (cur.valid(a)) {
         const int ks = cur.ks;
+        // Every consumer warp walks the same items, so all of them reach this together.
+        if (!x_rest && ks != ks_first) wait_x_rest();
         if (X8 && !((x_ready >> ks) & 1u)) {
             // First use of this stage of x by the CTA: wait for the conversion warp; the
             // metadata of the stage's first chunk says whether it was converted.
@@ -647,6 +674,9 @@ __global__ void __launch_bounds__(X8 ? kThreadsX8 : kThreadsG, 2)
             if (cur.valid(a)) prepare(cur.blk);
         }
     }
+    // A CTA that used only its first stage still meets the conversion warp's barrier and
+    // must not exit while copies of x are landing.
+    if (!x_rest) wait_x_rest();
 }
 
 template <int V, int CL, bool EH, bool PC, bool F16, bool X8>

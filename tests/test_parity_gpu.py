@@ -586,13 +586,14 @@ def test_multirow_bounded_wait_times_out_cleanly(handle):
 
 
 # ------------------------------------------- decode GEMV: fixed-point (dp4a) arithmetic
-# Shapes whose CTAs take at least two row blocks each (here 49152 x 2048, 64-row blocks,
-# and 28672 x 4096, 32-row blocks) run the decode GEMV's fixed-point arithmetic: x converted
-# per 32-k chunk to 32-bit fixed point, exact integer dot products of the codes (dp4a), one
-# rounding per chunk.  A stage with Inf / NaN, or with a nonzero element more than 2^13
-# below its chunk's largest, stays on the fp32 path.  Every test checks that the planner
-# chose the fixed-point kernel.
-X8_SHAPES = [(49152, 2048), (28672, 4096)]
+# Shapes whose CTAs take at least two row blocks each (here 49152 x 2048 and 65536 x 1024,
+# 64-row blocks, and 28672 x 4096, 32-row blocks) run the decode GEMV's fixed-point
+# arithmetic: x converted per 32-k chunk to 32-bit fixed point, exact integer dot products
+# of the codes (dp4a), one rounding per chunk.  A stage with Inf / NaN, or with a nonzero
+# element more than 2^13 below its chunk's largest, stays on the fp32 path.  Every test
+# checks that the planner chose the fixed-point kernel.  65536 x 1024 is a single 1024-k
+# stage of x (no second copy group to wait for).
+X8_SHAPES = [(49152, 2048), (28672, 4096), (65536, 1024)]
 X8_N, X8_K = X8_SHAPES[0]
 
 
