@@ -886,14 +886,16 @@ CROSSOVER_NK = ((2048, 2048), (8192, 2048), (2048, 8192), (128256, 2048), (1000,
 
 def crossover():
     """Device time per launch of each forced path (CUDA-core GEMV family, the generic FFMA
-    kernel, the tensor-core GEMM) over M for several (N, K): one JSON row per (N, K, M),
+    kernel, the tensor-core GEMM, the small-M tensor-core GEMM) over M for several (N, K):
+    one JSON row per (N, K, M),
     with the kernel each path runs and the one AUTO picks.  Every launch reads its own
     weight copy (HBM-cold); median over >= 20 launches."""
     import torch
     from bit_weight_quantized_int4_gb300 import q4lin as q
     h = q.q4lin_create(0)
     q.q4lin_set_option(h, q.Q4LIN_OPT_PDL, 1)
-    paths = (("gemv", q.Q4LIN_PATH_GEMV), ("ffma", q.Q4LIN_PATH_FFMA), ("tc", q.Q4LIN_PATH_TC))
+    paths = (("gemv", q.Q4LIN_PATH_GEMV), ("ffma", q.Q4LIN_PATH_FFMA), ("tc", q.Q4LIN_PATH_TC),
+             ("tc_small", q.Q4LIN_PATH_TC_SMALL))
     for N, K in CROSSOVER_NK:
         ws, ss = weight_copies(torch, N, K, gemv_bytes(N, K), cap=64)
         for M in CROSSOVER_M:

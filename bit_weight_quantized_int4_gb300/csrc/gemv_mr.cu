@@ -101,15 +101,6 @@ struct MrCursor {
     }
 };
 
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
-                                            int c2, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
-        : "memory");
-}
-
 template <int MR, int V, bool EH, bool F16>
 __global__ void __launch_bounds__(kMrThreads, 2)
     gemv_mr_kernel(const __grid_constant__ MrMaps maps, const MrArgs a) {

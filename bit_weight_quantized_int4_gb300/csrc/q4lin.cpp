@@ -61,6 +61,23 @@ bool multirow_preferred(const q4lin::Problem& p) {
     return (double)p.N * (double)p.K >= 1.0e7 && q4lin::gemv_mr_eligible(p);
 }
 
+// 3..16 activation rows: the small-M tensor-core GEMM (one CTA per SM over 128-row weight
+// blocks, each weight read once for all rows) where its blocks fill the SMs.  Its time is
+// close to waves x stages of 256 k x ~1.05 us (device time per launch on GB300, HBM-cold
+// weights: 128256 x 2048 57 us, 28672 x 4096 33 us, 14336 x 4096 19 us, 8192 x 2048 9.1 us,
+// flat in M), against, at 3..4 rows, the multi-row GEMV (128256 x 2048: 66 / 79 us at 3 /
+// 4 rows; it stays ahead where a last wave of a few blocks doubles the small-M GEMM's time:
+// 22016 x 4096 at 3 rows 27 against 33 us) and, from 5 rows, the tile GEMM (128256 x 2048
+// 111 us, 8192 x 2048 11.1 us; it stays ahead on few long blocks: 4096 x 4096 12 against
+// 17 us).  Two rows stay with the multi-row GEMV (50.5 against 57 us on 128256 x 2048).
+bool tc_small_preferred(const q4lin::Problem& p, const q4lin::LaunchCtx& c) {
+    if (p.M < 3 || p.M > 16 || !q4lin::tc_small_eligible(p, c)) return false;
+    const int64_t blocks = (p.N + 127) / 128, sms = c.sm_count;
+    const int64_t stages = (p.K + 255) / 256, tail = blocks % sms;
+    if (p.M <= 4) return blocks >= 100 && (tail == 0 || 4 * tail > sms);
+    return blocks >= 100 || (stages <= 8 && blocks >= 40);
+}
+
 class DeviceGuard {
    public:
     explicit DeviceGuard(int device) {
@@ -164,10 +181,16 @@ q4lin_status_t plan(q4lin_handle_t h, const q4lin::Problem& p, const q4lin::Laun
             if (!q4lin::tc_eligible(p, c)) return Q4LIN_ERR_UNSUPPORTED;
             *path = Q4LIN_PATH_TC;
             return Q4LIN_OK;
+        case Q4LIN_PATH_TC_SMALL:
+            if (!q4lin::tc_small_eligible(p, c)) return Q4LIN_ERR_UNSUPPORTED;
+            *path = Q4LIN_PATH_TC_SMALL;
+            return Q4LIN_OK;
         default:
             break;
     }
-    if (p.M > 1 && q4lin::tc_eligible(p, c) && (!row_ok || p.M > rowstream_max_m(p))) {
+    if (tc_small_preferred(p, c)) {
+        *path = Q4LIN_PATH_TC_SMALL;
+    } else if (p.M > 1 && q4lin::tc_eligible(p, c) && (!row_ok || p.M > rowstream_max_m(p))) {
         *path = Q4LIN_PATH_TC;
     } else if (row_ok) {
         *path = Q4LIN_PATH_GEMV;
@@ -181,6 +204,7 @@ q4lin_status_t plan(q4lin_handle_t h, const q4lin::Problem& p, const q4lin::Laun
 int kernel_of(const q4lin::Problem& p, const q4lin::LaunchCtx& c, int path) {
     switch (path) {
         case Q4LIN_PATH_TC: return q4lin::tc_uses_f16(p, c) ? Q4LIN_KERNEL_TC_F16 : Q4LIN_KERNEL_TC;
+        case Q4LIN_PATH_TC_SMALL: return Q4LIN_KERNEL_TC_SMALL;
         case Q4LIN_PATH_GEMV:
             if (q4lin::gemv_tma_eligible(p))
                 return q4lin::gemv_tma_fixed_point(p, c) ? Q4LIN_KERNEL_GEMV_TMA_FIXED
@@ -304,6 +328,7 @@ q4lin_status_t q4lin_run(q4lin_handle_t h, const float* x, const uint8_t* qweigh
     switch (kernel_of(p, c, path)) {
         case Q4LIN_KERNEL_TC:
         case Q4LIN_KERNEL_TC_F16: err = q4lin::tc_launch(p, c); break;
+        case Q4LIN_KERNEL_TC_SMALL: err = q4lin::tc_small_launch(p, c); break;
         case Q4LIN_KERNEL_GEMV_TMA:
         case Q4LIN_KERNEL_GEMV_TMA_FIXED: err = q4lin::gemv_tma_launch(p, c); break;
         case Q4LIN_KERNEL_MULTIROW: err = q4lin::gemv_mr_launch(p, c); break;
@@ -334,8 +359,9 @@ q4lin_status_t q4lin_run_grouped(q4lin_handle_t h, const q4lin_problem_t* proble
     }
     DeviceGuard g(h->device);
     if (!g.ok()) return Q4LIN_ERR_CUDA;
-    const bool gemv_forced_off =
-        h->force_path == Q4LIN_PATH_FFMA || h->force_path == Q4LIN_PATH_TC;
+    const bool gemv_forced_off = h->force_path == Q4LIN_PATH_FFMA ||
+                                 h->force_path == Q4LIN_PATH_TC ||
+                                 h->force_path == Q4LIN_PATH_TC_SMALL;
     int i = 0;
     while (i < count) {
         // Gather a run of fusable problems starting at i.
@@ -478,7 +504,7 @@ q4lin_status_t q4lin_set_option(q4lin_handle_t h, int option, int64_t value) {
     if (!h) return Q4LIN_ERR_INVALID_ARG;
     switch (option) {
         case Q4LIN_OPT_FORCE_PATH:
-            if (value < Q4LIN_PATH_AUTO || value > Q4LIN_PATH_TC) return Q4LIN_ERR_INVALID_ARG;
+            if (value < Q4LIN_PATH_AUTO || value > Q4LIN_PATH_TC_SMALL) return Q4LIN_ERR_INVALID_ARG;
             h->force_path = (int)value;
             return Q4LIN_OK;
         case Q4LIN_OPT_NIBBLE_EVEN_HIGH:

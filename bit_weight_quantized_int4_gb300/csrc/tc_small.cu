@@ -1,0 +1,555 @@
+// tc_small.cu -- tcgen05 tensor-core GEMM of the 4-bit weight-quantized linear for a few
+// activation rows (2 <= M <= 16: batched or speculative decode), streaming the weights once.
+//
+//   out[m, n] = bias[n] + sum_k x[m, k] * (code[n, k] - 8) * scale[k / gs, n]
+//
+// (the formula of "[ExecuTorch][WebGPU] Add linear_qcs4w op", Solution.)
+//
+// D[n, m] = sum_k A[n, k] * B[m, k] per block of 128 weight rows, with
+//   A = the block's dequantized weights (c - 8) * scale as fp32, written by CUDA cores into
+//       tensor memory (lane = weight row, one column per k) and read by the MMA as tf32;
+//   B = x, fp32 chunks of 32 k with the 128-byte swizzle, 8 rows a chunk when M <= 8 and
+//       16 otherwise (rows past M are zeros from the copy's out-of-bounds fill; with 8-row
+//       chunks the MMA's rows 8-15 read the next chunk, which only D columns m >= M see),
+//       read as tf32;
+//   D = fp32 accumulators in tensor memory (128 lanes x 16 columns).
+// tf32 keeps 10 explicit mantissa bits of each operand: a product carries a relative error
+// below 2^-9, inside the 4e-3 * sum|x*w| bar of the tensor-core path.
+//
+// At 16 columns an MMA is cheap for the tensor core but not for the thread that issues it:
+// on GB300 one thread issues a tcgen05.mma of 128 x 16 x 8 about every 50-70 cycles
+// whatever its width, and issuers in different warps add up.  So four issuer threads take
+// the 64-k slots of A in turn (8 MMAs each), each into its own accumulator (summed in a
+// fixed order at the end of the block), and four teams of four warps dequantize into a ring
+// of six slots of tensor memory ahead of the MMAs.  (Measured on 128256 x 2048: 32-k slots
+// in a ring of twelve 74 us, three teams 64.8 us, this layout 57 us; the loops advance their
+// ring indices without divisions, and the roles off the issuers' path sleep between polls
+// of their barriers, which together took 93.7 to 85 us.)
+//
+// Roles (800 threads, one CTA per SM, persistent over the row blocks blockIdx.x + k grid):
+//   warp 0, one lane:  TMA producer of the weights.  Per 256-k stage of a block: the codes
+//                      [128 rows x 128 B] (128-byte swizzle) and the block's group scales
+//                      [groups of the stage x 128 rows], into a ring of up to seven stages
+//                      (what shared memory leaves next to x).  A stage is released once the
+//                      dequantizing warps have read it.  The weights do not depend on the
+//                      preceding kernel: no dependency wait.
+//   warp 24, one lane: after griddepcontrol.wait, TMA copies of the whole x (resident for
+//                      all the CTA's blocks: K <= 5120 as 8-row chunks when M <= 8, K <= 2560
+//                      as 16-row chunks), one 3D box of 8 chunks [rows x 32 k] per 256-k
+//                      group on its own barrier; then the fourth MMA issuer.
+//   warps 1-3, lane 0: MMA issuers; slot i of the CTA's sequence goes to issuer i % 4:
+//                      eight tcgen05.mma.kind::tf32 of K = 8 (A from tensor memory), then a
+//                      commit that frees the A slot; after its last slot of a block, a commit
+//                      to the block's "D full".  Warp 1 also allocates and frees the 512
+//                      tensor-memory columns.
+//   warps 4-7:         epilogue; warp w owns tensor-memory lanes 32 (w % 4) ...: adds the
+//                      four accumulators of its rows, applies the channel scale and bias and
+//                      stores out[m, n] for m < M, n < N (32 consecutive n per row m).
+//   warps 8-23:        four dequantizing teams of four warps (one per lane quarter); team
+//                      i % 4 writes slot i: each thread (one weight row) reads the row's two
+//                      16-byte chunks of 32 codes and their group scales, and stores 64 fp32
+//                      values with two tcgen05.st.  Per code: a byte permute puts it into the
+//                      mantissa of a float v (v = 0.5 + c/256 for a low nibble, 1 + c/2048
+//                      for a high one), and one packed FMA per pair gives the exactly
+//                      rounded (c - 8) * s (256 s v - 136 s, 2048 s v - 2056 s; exact
+//                      constants for fp16 and dyadic scales, within 2^-12 s otherwise, far
+//                      below the tf32 rounding).  Per-channel scales are applied in the
+//                      epilogue instead (A = c - 8 exactly).
+//   Each CTA walks K from its own starting stage (blockIdx.x % stages, wrapping).
+// Tensor memory: accumulators [0, 128) (two blocks in flight x four issuers x 16 columns),
+// the A ring [128, 512) (six slots of 64 columns).  Every wait is bounded in time; a
+// timeout records code 1 in the status word, each role stops, the issuers drain their
+// MMAs, and the CTA frees its tensor memory and returns without storing.
+#include <algorithm>
+
+#include "ptx.cuh"
+#include "q4lin_internal.h"
+
+namespace q4lin {
+namespace {
+using namespace ptx;
+
+constexpr int kRows = 128;                        // weight rows per block (MMA M)
+constexpr int kBt = 16;                           // activation rows per MMA (N); M <= kBt
+constexpr int kStageK = 256;                      // k per stage (weights and x alike)
+constexpr int kChunk = 32;                        // k per 16-byte chunk of a code row
+constexpr int kChunksPerStage = kStageK / kChunk; // 8
+constexpr int kSlotK = 64;                        // k per A slot: two chunks, 8 MMAs
+constexpr int kSlotsPerStage = kStageK / kSlotK;  // 4
+constexpr int kIssuers = 4;                       // warps 1-3 and the x producer's warp
+constexpr int kTeams = 4;
+constexpr int kASlots = 6;                        // A ring: 6 x 64 tensor-memory columns
+static_assert(kASlots >= kIssuers && kASlots >= kTeams && kSlotsPerStage >= kIssuers,
+              "ring positions advance by less than a lap; every issuer has a slot per stage");
+static_assert(2 * kIssuers * kBt <= 128, "two blocks' accumulators fit below the A ring");
+constexpr int kACol0 = 128;
+constexpr int kWBox = kRows * 128;                // codes of a stage: [128 rows x 128 B]
+constexpr int kSMax = 8 * kRows * 4;              // scales: up to 8 groups x 128 rows
+constexpr int kWStageBytes = kWBox + kSMax;       // 20 KiB
+constexpr int kMaxWStages = 7;                    // weight ring: up to 140 KiB in flight
+constexpr int kMinWStages = 3;
+constexpr int kMaxXGroups = 20;                   // x resident: K <= 5120 (20 x 256 k)
+constexpr int kWarps = 8 + 4 * kTeams + 1;
+constexpr int kThreads = 32 * kWarps;
+constexpr int kDeqWarp0 = 8;
+constexpr int kXWarp = 8 + 4 * kTeams;             // the x producer, then an MMA issuer
+constexpr int kBarBytes = 1024;
+constexpr int kSmemCap = 227 * 1024;              // opt-in shared memory of a CTA
+constexpr int64_t kDrainNs = 4000000000LL;
+
+struct TsArgs {
+    const void* scales;   // per channel: [N], read by the epilogue
+    const float* bias;
+    float* out;
+    int M, N;
+    int nst;              // stages per block: ceil(K / 256)
+    int blocks;           // row blocks: ceil(N / 128)
+    int gs_shift;         // log2(group_size / 32) (grouped scales)
+    uint32_t w_tx;        // bytes of one stage's codes and scales
+    int wst;              // stages of the weight ring
+    int xrows;            // rows of x per chunk in shared memory: 8 (M <= 8) or 16
+    uint32_t x_bytes;     // x region: 8 chunks x xrows x 128 B per 256-k group, + 1 KiB
+    int skip_first_copy;  // test hook: stage 0's codes are not requested
+    int* status;
+    int64_t wait_ns;
+};
+
+// A bounded wait for the roles that are not on the MMA issuers' path (dequantizing warps,
+// which run ahead, the epilogue, the producers): between polls the warp sleeps, so that
+// the schedulers' issue slots go to the issuer threads instead of to polling.
+static __device__ __noinline__ bool wait_backoff(uint32_t bar, uint32_t parity, int64_t limit_ns,
+                                          const volatile int* failed, unsigned sleep_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer();
+    while (true) {
+        __nanosleep(sleep_ns);
+        if (mbar_try_wait(bar, parity)) return true;
+        if (failed && *failed) return false;
+        if ((int64_t)(global_timer() - t0) > limit_ns) return false;
+    }
+}
+
+__device__ __forceinline__ float ld_scale(const void* scales, bool f16, int64_t i) {
+    if (f16) return __half2float(__ldg(reinterpret_cast<const __half*>(scales) + i));
+    return __ldg(reinterpret_cast<const float*>(scales) + i);
+}
+
+// 32 fp32 values (c - 8) * s of one row's 16-byte chunk (k order) as raw bits.  Byte b of
+// word q holds k = 8q + 2b in its low nibble and 8q + 2b + 1 in its high nibble (swapped
+// when EH).  The permutes build v = 0.5 + c/256 (low nibble into byte 2 under 0x3F..) and
+// v = 1 + c/2048 (high nibble, already << 4, into byte 1 under 0x3F80..); the FMA with the
+// exact products 256 s, 2048 s and the offsets -136 s, -2056 s rounds (c - 8) s once.
+template <bool EH>
+__device__ __forceinline__ void dequant_chunk(const uint4 w4, float s, uint32_t (&v)[32]) {
+    const float2 mul = EH ? make_float2(2048.f * s, 256.f * s) : make_float2(256.f * s, 2048.f * s);
+    const float2 add = EH ? make_float2(-2056.f * s, -136.f * s) : make_float2(-136.f * s, -2056.f * s);
+    const uint32_t words[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const uint32_t lo = words[q] & 0x0F0F0F0Fu, hi = words[q] & 0xF0F0F0F0u;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            const float vl = __uint_as_float(prmt(lo, 0x3F800000u, 0x7054u | (b << 8)));
+            const float vh = __uint_as_float(prmt(hi, 0x3F800000u, 0x7604u | (b << 4)));
+            const float2 r = ffma2(EH ? make_float2(vh, vl) : make_float2(vl, vh), mul, add);
+            v[8 * q + 2 * b] = __float_as_uint(r.x);
+            v[8 * q + 2 * b + 1] = __float_as_uint(r.y);
+        }
+    }
+}
+
+template <bool EH, bool PC, bool F16>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_small_kernel(const __grid_constant__ CUtensorMap tmw, const __grid_constant__ CUtensorMap tms,
+                    const __grid_constant__ CUtensorMap tmx, const TsArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* gbase = smem_raw + (base - raw);
+    // [x, resident: 256-k groups of 8 chunks [xrows x 128 B], + 1 KiB][weight ring][barriers]
+    const uint32_t xbase = base;
+    const uint32_t wbase = base + a.x_bytes;
+    const uint32_t bar0 = wbase + (uint32_t)(a.wst * kWStageBytes);
+    auto wstage = [&](int b) { return wbase + (uint32_t)(b * kWStageBytes); };
+    constexpr int kB0 = 0, kB1 = kB0 + 2 * kMaxWStages, kB2 = kB1 + kMaxXGroups,
+                  kB3 = kB2 + 2 * kASlots, kB4 = kB3 + 4;
+    auto wfull = [&](int b) { return bar0 + 8u * (kB0 + b); };
+    auto wempty = [&](int b) { return bar0 + 8u * (kB0 + kMaxWStages + b); };
+    auto xfull = [&](int grp) { return bar0 + 8u * (kB1 + grp); };
+    auto afull = [&](int p) { return bar0 + 8u * (kB2 + p); };
+    auto aempty = [&](int p) { return bar0 + 8u * (kB2 + kASlots + p); };
+    auto dfull = [&](int q) { return bar0 + 8u * (kB3 + q); };
+    auto dempty = [&](int q) { return bar0 + 8u * (kB3 + 2 + q); };
+    auto drain = [&](int u) { return bar0 + 8u * (kB4 + u); };
+    static_assert(8 * (kB4 + kIssuers) <= 960, "barriers fit below the flags");
+    volatile int* failed = reinterpret_cast<volatile int*>(gbase + (bar0 - base) + 960);
+    const uint32_t tslot = bar0 + 968;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int b = 0; b < a.wst; ++b) {
+            mbar_init(wfull(b), 1);
+            mbar_init(wempty(b), kSlotsPerStage * 4);  // the 4 dequantizing warps of each slot
+        }
+        for (int grp = 0; grp < a.nst; ++grp) mbar_init(xfull(grp), 1);
+        for (int p = 0; p < kASlots; ++p) {
+            mbar_init(afull(p), 4);
+            mbar_init(aempty(p), 1);
+        }
+        for (int q = 0; q < 2; ++q) {
+            mbar_init(dfull(q), kIssuers);
+            mbar_init(dempty(q), 4);
+        }
+        for (int u = 0; u < kIssuers; ++u) mbar_init(drain(u), 1);
+        *failed = 0;
+        mbar_init_fence();
+    }
+    if (warp == 1) tmem_alloc(tslot, 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    uint32_t tmem;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(tmem) : "r"(tslot) : "memory");
+    griddep_launch_dependents();
+
+    // This CTA's blocks: blockIdx.x, + gridDim.x, ...; its stages and 32-k slots in order.
+    const int my_blocks = ((int)a.blocks - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
+    const int n_stages = my_blocks * a.nst;
+    const int n_slots = n_stages * kSlotsPerStage;
+    const int slots_per_block = a.nst * kSlotsPerStage;
+    // Each CTA walks K from its own starting stage (blockIdx.x % stages, wrapping), so
+    // that the CTAs' concurrent weight requests spread over the column offsets of the
+    // rows instead of all asking for the same 128 bytes of every row at once.
+    const int rot = (int)(blockIdx.x % (unsigned)a.nst);
+    auto kstage = [&](int t) { return t + rot < a.nst ? t + rot : t + rot - a.nst; };
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------- TMA producer of codes and scales
+            // (independent of the preceding kernel: no dependency wait)
+            prefetch_tensormap(&tmw);
+            if (!PC) prefetch_tensormap(&tms);
+            int g = 0;
+            for (; g < n_stages; ++g) {
+                const int b = g % a.wst, t = kstage(g % a.nst);
+                const int row0 = ((int)blockIdx.x + (g / a.nst) * (int)gridDim.x) * kRows;
+                if (g >= a.wst &&
+                    !wait_backoff(wempty(b), ((g / a.wst) - 1) & 1, a.wait_ns, failed, 64)) {
+                    record_failure(a.status, failed);
+                    break;
+                }
+                if (*failed) break;
+                mbar_arrive_expect_tx(wfull(b), a.w_tx);
+                if (a.skip_first_copy && g == 0) continue;
+                tma_load_2d(wstage(b), &tmw, t * (kStageK / 2), row0, wfull(b));
+                if (!PC)
+                    tma_load_2d(wstage(b) + kWBox, &tms, row0, (t * kStageK) >> (a.gs_shift + 5),
+                                wfull(b));
+            }
+            // The last requested stages may still be landing; the CTA must not exit first.
+            for (int q = g > a.wst ? g - a.wst : 0; q < g; ++q) {
+                if (a.skip_first_copy && q == 0) continue;
+                wait_bounded(wfull(q % a.wst), (q / a.wst) & 1, kDrainNs, nullptr);
+            }
+        }
+    } else if (warp <= 3 || warp == kXWarp) {
+        if (lane == 0) {
+            const int u = warp == kXWarp ? 3 : warp - 1;
+            if (warp == kXWarp) {
+                // --------------------------------------------------- TMA producer of x
+                // x stays resident for all the CTA's blocks: it is read from L2 once per
+                // CTA (every CTA reads the same lines; re-reading them per block made those
+                // L2 lines the bottleneck), in 256-k groups, each on its own barrier.  Then
+                // this thread is the fourth MMA issuer.
+                prefetch_tensormap(&tmx);
+                griddep_wait();  // x belongs to the dependency chain
+                const uint32_t gbytes = (uint32_t)(kChunksPerStage * a.xrows * 128);
+                for (int q = 0; q < a.nst; ++q) {
+                    const int grp = kstage(q);  // in the order of first use
+                    mbar_arrive_expect_tx(xfull(grp), gbytes);
+                    tma_load_3d(xbase + (uint32_t)grp * gbytes, &tmx, 0, 0,
+                                grp * kChunksPerStage, xfull(grp));
+                }
+            }
+            // ------------------------------------------------------------- MMA issuers
+            const uint32_t idesc = tf32_idesc(kRows, kBt);
+            // Slots u, u + kIssuers, ...: the block j, the slot's place in the block, its A ring
+            // slot p and the parity of its barrier advance without divisions.
+            int j = 0, in_blk = u, p = u;
+            uint32_t pph = 0;
+            for (int i = u; i < n_slots; i += kIssuers) {
+                while (in_blk >= slots_per_block) in_blk -= slots_per_block, ++j;
+                const int par = j & 1;
+                const int t = in_blk / kSlotsPerStage, sl = in_blk % kSlotsPerStage;
+                const bool first = in_blk < kIssuers;
+                const bool last = in_blk + kIssuers >= slots_per_block;
+                if ((first && j >= 2 &&
+                     !wait_bounded(dempty(par), ((j >> 1) - 1) & 1, a.wait_ns, failed)) ||
+                    !wait_bounded(afull(p), pph, a.wait_ns, failed) ||
+                    (j == 0 && sl < kIssuers &&
+                     !wait_bounded(xfull(kstage(t)), 0, a.wait_ns, failed))) {
+                    record_failure(a.status, failed);
+                    break;
+                }
+                // A was written by tcgen05.st and fenced by its writers before they arrived;
+                // x came by TMA.  The waits order both.
+                tc_fence_after();
+                const uint32_t d = tmem + (uint32_t)((par * kIssuers + u) * kBt);
+                const uint32_t acol = tmem + (uint32_t)(kACol0 + p * kSlotK);
+                // The slot's two x chunks in the resident copy (with 8 rows a chunk, rows 8-15
+                // of the MMA's B read the next chunk: only D columns m >= 8 >= M see them); +2
+                // in the descriptor's address field per 32 bytes (K = 8 tf32) along a row.
+                const int chunk = kstage(t) * kChunksPerStage + sl * (kSlotK / kChunk);
+#pragma unroll
+                for (int h = 0; h < kSlotK / kChunk; ++h) {
+                    const uint64_t bd =
+                        sw128_desc(xbase + (uint32_t)((chunk + h) * a.xrows * 128));
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_tf32_ts(d, acol + kChunk * h + 8 * kk, bd + (uint64_t)(2 * kk), idesc,
+                                    (first && h == 0 && kk == 0) ? 0u : 1u);
+                }
+                mma_commit(aempty(p));
+                if (last) mma_commit(dfull(par));
+                in_blk += kIssuers;
+                if ((p += kIssuers) >= kASlots) p -= kASlots, pph ^= 1u;
+            }
+            // Every MMA this thread issued completes before the CTA frees tensor memory (and
+            // the copies of x have landed).
+            mma_commit(drain(u));
+            wait_bounded(drain(u), 0, kDrainNs, nullptr);
+            if (warp == kXWarp)
+                for (int grp = 0; grp < a.nst; ++grp) wait_bounded(xfull(grp), 0, kDrainNs, nullptr);
+        }
+    } else if (warp < kDeqWarp0) {
+        // ----------------------------------------------------------------- epilogue
+        const int q = warp & 3;
+        const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
+        griddep_wait();  // bias, out belong to the dependency chain
+        for (int j = 0; j < my_blocks; ++j) {
+            const int par = j & 1;
+            if (!wait_backoff(dfull(par), (j >> 1) & 1, a.wait_ns, failed, 256)) {
+                if (lane == 0) record_failure(a.status, failed);
+                break;
+            }
+            tc_fence_after();
+            float acc[kBt];
+#pragma unroll
+            for (int u = 0; u < kIssuers; ++u) {
+                uint32_t r[kBt];
+                tmem_ld16(lane_base + (uint32_t)((par * kIssuers + u) * kBt), r);
+#pragma unroll
+                for (int m = 0; m < kBt; ++m)
+                    acc[m] = u == 0 ? __uint_as_float(r[m]) : acc[m] + __uint_as_float(r[m]);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(dempty(par));
+            const int64_t n = ((int64_t)blockIdx.x + (int64_t)j * gridDim.x) * kRows + q * 32 + lane;
+            if (n < a.N && !*failed) {
+                const float cs = PC ? ld_scale(a.scales, F16, n) : 1.f;
+                const float bv = a.bias ? __ldg(a.bias + n) : 0.f;
+#pragma unroll
+                for (int m = 0; m < kBt; ++m)
+                    if (m < a.M) a.out[(int64_t)m * a.N + n] = fmaf(acc[m], cs, bv);
+            }
+        }
+    } else {
+        // ---------------------------------------------------------- dequantization
+        const int team = (warp - kDeqWarp0) >> 2;
+        const int q = warp & 3;
+        const int r = q * 32 + lane;  // this thread's weight row in the block
+        const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
+        // Slots team, team + kTeams, ...: stage (ring slot b, parity wph), slot sl in it, A
+        // ring slot p (parity pph), advanced without divisions.
+        int sl = team, b = 0, p = team;
+        uint32_t wph = 0, pph = 0;
+        for (int i = team; i < n_slots; i += kTeams) {
+            while (sl >= kSlotsPerStage) {
+                sl -= kSlotsPerStage;
+                if (++b == a.wst) b = 0, wph ^= 1u;
+            }
+            if ((i >= kASlots && !wait_backoff(aempty(p), pph ^ 1u, a.wait_ns, failed, 32)) ||
+                !wait_backoff(wfull(b), wph, a.wait_ns, failed, 32)) {
+                if (lane == 0) record_failure(a.status, failed);
+                break;
+            }
+            // The MMAs that read this slot last have completed (their commit): order the
+            // overwrite after them.
+            tc_fence_after();
+            // The slot's chunks c of the block row; chunk c sits at chunk c ^ (r % 8)
+            // (128-byte swizzle).  Their group scales are in the stage's scale block.
+            constexpr int kCps = kSlotK / kChunk;
+            uint4 w[kCps];
+            float sc[kCps];
+#pragma unroll
+            for (int h = 0; h < kCps; ++h) {
+                const int c = kCps * sl + h;
+                w[h] = ld_shared_v4(wstage(b) + (uint32_t)(r * 128) + ((uint32_t)(c ^ (r & 7)) << 4));
+                sc[h] = 1.f;
+                if (!PC) {
+                    const int gl = (c * kChunk) >> (a.gs_shift + 5);
+                    const uint8_t* sp = gbase + (wstage(b) - base) + kWBox;
+                    sc[h] = F16 ? __half2float(reinterpret_cast<const __half*>(sp)[gl * kRows + r])
+                                : reinterpret_cast<const float*>(sp)[gl * kRows + r];
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(wempty(b));  // the warp's reads of the stage are done
+#pragma unroll
+            for (int h = 0; h < kCps; ++h) {
+                uint32_t v[32];
+                dequant_chunk<EH>(w[h], sc[h], v);
+                tmem_st32_async(lane_base + (uint32_t)(kACol0 + p * kSlotK + kChunk * h), v);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(afull(p));
+            sl += kTeams;
+            if ((p += kTeams) >= kASlots) p -= kASlots, pph ^= 1u;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+template <bool EH, bool PC, bool F16>
+cudaError_t launch_ts(const CUtensorMap& tw, const CUtensorMap& ts, const CUtensorMap& tx,
+                      const TsArgs& a, unsigned grid, int smem, const LaunchCtx& c) {
+    constexpr auto kernel = tc_small_kernel<EH, PC, F16>;
+    const cudaError_t attr = kernel_smem_once<kernel>(kSmemCap);
+    if (attr != cudaSuccess) return attr;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = c.stream;
+    cudaLaunchAttribute at[1];
+    if (c.pdl) {
+        at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        at[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = at;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, kernel, tw, ts, tx, a);
+}
+
+int log2_pow2(int64_t v) {
+    for (int s = 0; s < 62; ++s)
+        if ((int64_t(1) << s) == v) return s;
+    return -1;
+}
+
+// Shared memory: resident x (8 chunks x rows x 128 B per 256-k group, + 1 KiB that the
+// 8-row layout's MMAs read past the last chunk), then as many weight stages as fit (at
+// most kMaxWStages).  Returns the weight stages (0 if fewer than kMinWStages fit).
+int ts_layout(const Problem& p, int smem_cap, uint32_t* x_bytes, int* xrows, int* smem) {
+    const int64_t nst = (p.K + kStageK - 1) / kStageK;
+    if (nst > kMaxXGroups) return 0;
+    *xrows = p.M <= 8 ? 8 : 16;
+    *x_bytes = (uint32_t)(nst * kChunksPerStage * *xrows * 128 + 1024);
+    const int64_t room = (int64_t)std::min(smem_cap, kSmemCap) - 1024 - *x_bytes - kBarBytes;
+    const int wst = (int)std::min<int64_t>(kMaxWStages, room / kWStageBytes);
+    if (wst < kMinWStages) return 0;
+    *smem = 1024 + (int)*x_bytes + wst * kWStageBytes + kBarBytes;
+    return wst;
+}
+
+}  // namespace
+
+bool tc_small_eligible(const Problem& p, const LaunchCtx& c) {
+    if (p.M < 2 || p.M > kBt || p.N < 1 || p.N > (1LL << 31) - kRows) return false;
+    if (p.K % kChunk != 0 || p.K > (1LL << 30)) return false;
+    if (reinterpret_cast<uintptr_t>(p.x) % 16 || reinterpret_cast<uintptr_t>(p.qweight) % 16)
+        return false;
+    if (p.group_size < p.K) {
+        // Group scales arrive by TMA: 16-byte aligned base and row, and a group size that
+        // is a power-of-two multiple of 32.
+        const int esz = p.scale_f16 ? 2 : 4;
+        if (p.group_size % kChunk != 0 || log2_pow2(p.group_size / kChunk) < 0) return false;
+        if (reinterpret_cast<uintptr_t>(p.scales) % 16 || (p.N * esz) % 16 != 0) return false;
+    }
+    uint32_t xb;
+    int xr, smem;
+    if (ts_layout(p, c.max_smem_optin, &xb, &xr, &smem) == 0) return false;
+    return tensor_map_encoder() != nullptr;
+}
+
+cudaError_t tc_small_launch(const Problem& p, const LaunchCtx& c) {
+    EncodeTiledFn enc = tensor_map_encoder();
+    if (!enc || !tc_small_eligible(p, c)) return cudaErrorNotSupported;
+    const bool pc = p.group_size >= p.K;
+    const int esz = p.scale_f16 ? 2 : 4;
+    TsArgs a = {};
+    a.scales = p.scales;
+    a.bias = p.bias;
+    a.out = p.out;
+    a.M = (int)p.M;
+    a.N = (int)p.N;
+    a.nst = (int)((p.K + kStageK - 1) / kStageK);
+    a.blocks = (int)((p.N + kRows - 1) / kRows);
+    a.gs_shift = pc ? 0 : log2_pow2(p.group_size / kChunk);
+    const int gps = pc ? 0 : std::max(1, kStageK >> (a.gs_shift + 5));
+    a.w_tx = (uint32_t)(kWBox + gps * kRows * esz);
+    int smem = 0;
+    a.wst = ts_layout(p, c.max_smem_optin, &a.x_bytes, &a.xrows, &smem);
+    a.skip_first_copy = c.tc_skip_first_copy;
+    a.status = c.status_word;
+    a.wait_ns = c.wait_limit_ns;
+
+    CUtensorMap tw, ts, tx;
+    const cuuint32_t e2[2] = {1, 1}, e3[3] = {1, 1, 1};
+    {
+        // Packed codes [N rows x K/2 bytes]: boxes [128 rows x 128 B], 128-byte swizzle.
+        const cuuint64_t dims[2] = {(cuuint64_t)(p.K / 2), (cuuint64_t)p.N};
+        const cuuint64_t strides[1] = {(cuuint64_t)(p.K / 2)};
+        const cuuint32_t box[2] = {128, (cuuint32_t)kRows};
+        if (enc(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(p.qweight), dims,
+                strides, box, e2, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    if (!pc) {
+        // Group scales [G groups x N]: boxes [gps groups x 128 rows] (gps = 256 / gs, or 1).
+        const int64_t G = (p.K + p.group_size - 1) / p.group_size;
+        const cuuint64_t dims[2] = {(cuuint64_t)p.N, (cuuint64_t)G};
+        const cuuint64_t strides[1] = {(cuuint64_t)(p.N * esz)};
+        const cuuint32_t box[2] = {(cuuint32_t)kRows, (cuuint32_t)gps};
+        if (enc(&ts, p.scale_f16 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT32,
+                2, const_cast<void*>(p.scales), dims, strides, box, e2, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    } else {
+        ts = tw;  // unused
+    }
+    {
+        // x [M rows x K] as (32 k, row, 32-k chunk): one box = 8 chunks of [16 rows x 128 B],
+        // 128-byte swizzle; rows past M and chunks past K read as zeros.
+        const cuuint64_t dims[3] = {32, (cuuint64_t)p.M, (cuuint64_t)(p.K / 32)};
+        const cuuint64_t strides[2] = {(cuuint64_t)(p.K * 4), 128};
+        const cuuint32_t box[3] = {32, (cuuint32_t)a.xrows, (cuuint32_t)kChunksPerStage};
+        if (enc(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(p.x), dims, strides,
+                box, e3, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    const unsigned grid = (unsigned)std::min<int64_t>(a.blocks, c.sm_count);
+    const bool eh = p.even_high != 0, f16 = p.scale_f16 != 0;
+    if (pc) {
+        if (eh) return f16 ? launch_ts<true, true, true>(tw, ts, tx, a, grid, smem, c)
+                           : launch_ts<true, true, false>(tw, ts, tx, a, grid, smem, c);
+        return f16 ? launch_ts<false, true, true>(tw, ts, tx, a, grid, smem, c)
+                   : launch_ts<false, true, false>(tw, ts, tx, a, grid, smem, c);
+    }
+    if (eh) return f16 ? launch_ts<true, false, true>(tw, ts, tx, a, grid, smem, c)
+                       : launch_ts<true, false, false>(tw, ts, tx, a, grid, smem, c);
+    return f16 ? launch_ts<false, false, true>(tw, ts, tx, a, grid, smem, c)
+               : launch_ts<false, false, false>(tw, ts, tx, a, grid, smem, c);
+}
+
+}  // namespace q4lin

@@ -37,7 +37,8 @@ Q4LIN_PATH_AUTO = 0
 Q4LIN_PATH_GEMV = 1
 Q4LIN_PATH_FFMA = 2
 Q4LIN_PATH_TC = 3
-PATH_NAMES = {0: "auto", 1: "gemv", 2: "ffma", 3: "tc"}
+Q4LIN_PATH_TC_SMALL = 4
+PATH_NAMES = {0: "auto", 1: "gemv", 2: "ffma", 3: "tc", 4: "tc_small"}
 
 Q4LIN_KERNEL_NONE = 0
 Q4LIN_KERNEL_GEMV_TMA = 1
@@ -47,8 +48,9 @@ Q4LIN_KERNEL_GENERIC = 4
 Q4LIN_KERNEL_TC = 5
 Q4LIN_KERNEL_TC_F16 = 6
 Q4LIN_KERNEL_GEMV_TMA_FIXED = 7
+Q4LIN_KERNEL_TC_SMALL = 8
 KERNEL_NAMES = {0: "none", 1: "gemv_tma", 2: "multirow", 3: "rowstream", 4: "generic",
-                5: "tc", 6: "tc_f16", 7: "gemv_tma_fixed"}
+                5: "tc", 6: "tc_f16", 7: "gemv_tma_fixed", 8: "tc_small"}
 
 Q4LIN_OPT_FORCE_PATH = 1
 Q4LIN_OPT_NIBBLE_EVEN_HIGH = 2

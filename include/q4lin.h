@@ -69,7 +69,15 @@ typedef enum {
                                TMA-fed multi-row GEMV (2 <= M <= 4, >= 10 M weights),
                                else the row-streaming kernel (small M)                */
     Q4LIN_PATH_FFMA = 2,    /* generic CUDA-core kernel: any K, group size, alignment  */
-    Q4LIN_PATH_TC = 3       /* tcgen05 tensor-core GEMM (TMEM accumulators)            */
+    Q4LIN_PATH_TC = 3,      /* tcgen05 tensor-core GEMM (TMEM accumulators)            */
+    Q4LIN_PATH_TC_SMALL = 4 /* tcgen05 GEMM for 2 <= M <= 16 activation rows: persistent
+                               CTAs over 128-row weight blocks, each weight read once,
+                               x resident in shared memory (K % 32 == 0, K <= 5120 up to
+                               8 rows and K <= 2560 above, 16-byte aligned x and qweight;
+                               grouped scales: a power-of-two multiple of 32 as group
+                               size and a scale row of whole 16-byte units); tensor-core
+                               tolerance.  AUTO takes it for 3..16 rows when the
+                               128-row blocks fill the SMs (measured crossover) */
 } q4lin_path_t;
 
 /* Options for q4lin_set_option / q4lin_get_option. */
@@ -260,9 +268,10 @@ typedef enum {
     Q4LIN_KERNEL_GENERIC = 4,   /* generic CUDA-core kernel (any K, group size, alignment) */
     Q4LIN_KERNEL_TC = 5,        /* tcgen05 tensor-core GEMM, tf32 operands                 */
     Q4LIN_KERNEL_TC_F16 = 6,    /* the same with fp16 operands (Q4LIN_OPT_TC_F16)          */
-    Q4LIN_KERNEL_GEMV_TMA_FIXED = 7 /* the decode GEMV with exact fixed-point arithmetic: x as
-                                     * 32-bit fixed point per 32-k chunk, codes times x by
-                                     * dp4a; chosen when its CTAs take >= 2 row blocks each */
+    Q4LIN_KERNEL_GEMV_TMA_FIXED = 7, /* the decode GEMV with exact fixed-point arithmetic: x as
+                                      * 32-bit fixed point per 32-k chunk, codes times x by
+                                      * dp4a; chosen when its CTAs take >= 2 row blocks each */
+    Q4LIN_KERNEL_TC_SMALL = 8   /* tcgen05 GEMM for 2 <= M <= 16 (Q4LIN_PATH_TC_SMALL), tf32 */
 } q4lin_kernel_t;
 
 /* The kernel q4lin_run would launch for these arguments (no launch, no device access);

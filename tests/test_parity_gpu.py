@@ -16,6 +16,7 @@ from tests._gpu import TOL_FP32, TOL_TC, assert_parity, run_q4lin
 pytestmark = pytest.mark.gpu
 
 GEMV, FFMA, TC, AUTO = 1, 2, 3, 0
+TC_SMALL = 4
 
 
 @pytest.fixture(scope="module")
@@ -29,7 +30,7 @@ def handle():
 
 
 def tol_for(path):
-    return TOL_TC if path == TC else TOL_FP32
+    return TOL_TC if path in (TC, TC_SMALL) else TOL_FP32
 
 
 def check_case(handle, case, path=AUTO, even_high=False):

@@ -1,0 +1,216 @@
+"""Parity of the tensor-core GEMM for 2 <= M <= 16 activation rows (Q4LIN_PATH_TC_SMALL,
+bit_weight_quantized_int4_gb300/csrc/tc_small.cu) with the fp64 oracle, through the C ABI.
+
+Every element of out[M, N] is checked at the tensor-core tolerance (4e-3 * sum_k|x*w| +
+1e-6); dyadic inputs and all-8 codes must come out bit-exact.  Covered: every M from 2 to
+16, ragged N (rows past N in the last 128-row block), ragged K (a last 256-k stage that is
+mostly past K), the longest K whose x stays resident, group sizes from 32 to wider than a stage,
+per-channel scales (fp16 and fp32), fp32 and fp16 group scales, bias or none, the
+even-high nibble order, persistent CTAs over many blocks (more blocks than SMs), repeated
+calls bit-identical, and a bounded wait that runs out cleanly.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from bit_weight_quantized_int4_gb300 import synth
+from tests._gpu import TOL_TC, assert_parity, run_q4lin
+
+pytestmark = pytest.mark.gpu
+
+TC_SMALL = 4
+
+
+@pytest.fixture(scope="module")
+def handle():
+    import torch
+    from bit_weight_quantized_int4_gb300 import q4lin as q
+    assert torch.cuda.is_available()
+    h = q.q4lin_create(0)
+    yield h
+    q.q4lin_destroy(h)
+
+
+def check(handle, case, even_high=False):
+    out, used = run_q4lin(handle, case, TC_SMALL, even_high)
+    assert used == TC_SMALL
+    ref, mag = oracle.linear(case.x, case.qweight, case.scales, case.bias, case.K,
+                             case.group_size, even_high=even_high)
+    assert_parity(out, ref, mag, TOL_TC)
+    return out
+
+
+@pytest.mark.parametrize("M", list(range(2, 17)))
+def test_every_m(handle, M):
+    check(handle, synth.make_case(M, 1000, 2048, 32, scale_f16=True, bias=True, seed=M))
+
+
+@pytest.mark.parametrize("N,K,gs,f16,bias", [
+    (128, 512, 32, True, True),        # one block, two stages
+    (200, 1056, 32, False, True),      # ragged N and K (the last stage mostly past K)
+    (4104, 2048, 64, True, False),     # ragged N over 33 blocks
+    (2600, 2560, 128, False, True),    # the longest K that 16 resident rows of x allow
+    (1024, 2048, 1024, True, True),    # group wider than a stage
+    (520, 2048, 2048, False, True),    # per channel, fp32
+    (136, 1536, 1536, True, False),    # per channel, fp16
+])
+def test_shapes(handle, N, K, gs, f16, bias):
+    for M in (2, 7, 16):
+        check(handle, synth.make_case(M, N, K, gs, scale_f16=f16, bias=bias, seed=N + K + M))
+
+
+@pytest.mark.parametrize("N,K,gs,f16", [(384, 5120, 32, True), (1000, 4096, 64, False)])
+@pytest.mark.parametrize("M", [2, 8])
+def test_long_k_up_to_8_rows(handle, M, N, K, gs, f16):
+    """Up to 8 rows, x is kept as 8-row chunks: K up to 5120 stays resident."""
+    check(handle, synth.make_case(M, N, K, gs, scale_f16=f16, bias=True, seed=N + K + M))
+
+
+@pytest.mark.parametrize("M", [3, 16])
+def test_persistent_over_many_blocks(handle, M):
+    """More 128-row blocks than SMs (the vocabulary-sized head): each CTA takes several
+    blocks with the accumulators double-buffered between them."""
+    check(handle, synth.make_case(M, 128256, 2048, 32, scale_f16=True, bias=True, seed=M))
+
+
+def test_even_high(handle):
+    check(handle, synth.make_case(5, 704, 2048, 64, scale_f16=True, bias=True, seed=3),
+          even_high=True)
+
+
+@pytest.mark.parametrize("M,f16", [(2, True), (9, False), (16, True)])
+def test_dyadic_bit_exact(handle, M, f16):
+    c = synth.make_dyadic_case(M, 264, 1024, 32, scale_f16=f16, bias=True, seed=M)
+    out, used = run_q4lin(handle, c, TC_SMALL)
+    assert used == TC_SMALL
+    ref, _ = oracle.linear(c.x, c.qweight, c.scales, c.bias, c.K, c.group_size)
+    np.testing.assert_array_equal(out.astype(np.float64), ref)
+
+
+def test_all_codes_eight_gives_bias(handle):
+    c = synth.make_case(6, 336, 2048, 32, scale_f16=True, bias=True, seed=9)
+    c.qweight = synth.fill_codes(336, 2048, 8)
+    out, _ = run_q4lin(handle, c, TC_SMALL)
+    np.testing.assert_array_equal(out, np.broadcast_to(c.bias, out.shape))
+
+
+def test_repeated_calls_bit_identical(handle):
+    c = synth.make_case(8, 30000, 2048, 32, scale_f16=True, bias=True, seed=5)
+    a = check(handle, c)
+    b, _ = run_q4lin(handle, c, TC_SMALL)
+    np.testing.assert_array_equal(a, b)
+
+
+def test_ineligible_shapes_are_refused(handle):
+    """M outside 2..16, K not a multiple of 32, a group size that is not a power-of-two
+    multiple of 32, or an x too long to stay resident in shared memory (K > 5120 up to 8
+    rows, K > 2560 above): the forced path reports Q4LIN_ERR_UNSUPPORTED, nothing runs."""
+    import torch
+    from bit_weight_quantized_int4_gb300 import q4lin as q
+    q.q4lin_set_option(handle, q.Q4LIN_OPT_FORCE_PATH, TC_SMALL)
+    try:
+        for M, N, K, gs in [(1, 256, 512, 32), (17, 256, 512, 32), (4, 256, 528, 48),
+                            (4, 256, 1024, 96), (4, 256, 5376, 32), (12, 256, 2816, 32)]:
+            c = synth.make_case(M, N, K, gs, scale_f16=False, bias=False, seed=1)
+            x = torch.from_numpy(c.x).cuda()
+            w = torch.from_numpy(c.qweight).cuda()
+            s = torch.from_numpy(c.scales).cuda()
+            out = torch.empty(M * N, device="cuda")
+            st, _ = q.q4lin_plan(handle, x.data_ptr(), w.data_ptr(), s.data_ptr(), None,
+                                 out.data_ptr(), M, N, K, gs, q.Q4LIN_SCALE_F32)
+            assert st == q.Q4LIN_ERR_UNSUPPORTED, (M, N, K, gs)
+    finally:
+        q.q4lin_set_option(handle, q.Q4LIN_OPT_FORCE_PATH, 0)
+
+
+def test_bounded_wait_times_out_cleanly(handle):
+    """The producer skips its first copy (test hook), so the barrier every role waits on
+    first is never completed: the 1 ms bounded waits run out, the kernel records code 1,
+    drains its MMAs, frees its tensor memory and returns; the next call is correct."""
+    from bit_weight_quantized_int4_gb300 import q4lin as q
+    c = synth.make_case(4, 1024, 2048, 32, scale_f16=True, bias=False, seed=77)
+    st, code = q.q4lin_check_device_status(handle, None)
+    assert (st, code) == (q.Q4LIN_OK, 0)
+    q.q4lin_set_option(handle, q.Q4LIN_OPT_WAIT_LIMIT, 1_000_000)
+    q.q4lin_set_option(handle, q.Q4LIN_OPT_TC_SKIP_FIRST_COPY, 1)
+    try:
+        run_q4lin(handle, c, TC_SMALL)
+    except AssertionError:
+        pass  # the output of a timed-out call is undefined (NaN-poisoned here)
+    finally:
+        q.q4lin_set_option(handle, q.Q4LIN_OPT_TC_SKIP_FIRST_COPY, 0)
+        q.q4lin_set_option(handle, q.Q4LIN_OPT_WAIT_LIMIT, 0)
+    st, code = q.q4lin_check_device_status(handle, None)
+    assert st == q.Q4LIN_ERR_TIMEOUT and code == 1
+    st, code = q.q4lin_check_device_status(handle, None)
+    assert (st, code) == (q.Q4LIN_OK, 0)
+    check(handle, c)
+
+
+@pytest.mark.parametrize("pdl", [0, 1])
+@pytest.mark.parametrize("M", [4, 12])
+def test_chain_with_dependent_launch(handle, M, pdl):
+    """Four launches where each output is the next input, with programmatic dependent
+    launch on and off: the weights stream before the dependency wait, x is read after it
+    and out is written after it; each link is checked against the oracle applied to the
+    input it actually received."""
+    import torch
+    from bit_weight_quantized_int4_gb300 import q4lin as q
+    dims = [512, 1024, 256, 768, 2048]
+    links = [synth.make_case(M, dims[i + 1], dims[i], 32, scale_f16=(i % 2 == 1),
+                             bias=(i % 2 == 0), seed=900 + i + M) for i in range(4)]
+    bufs = [torch.from_numpy(np.ascontiguousarray(links[0].x)).cuda()]
+    bufs += [torch.full((M, d), float("nan"), device="cuda") for d in dims[1:]]
+    dev = [tuple(None if a is None else torch.from_numpy(a).cuda()
+                 for a in (c.qweight, c.scales, c.bias)) for c in links]
+    torch.cuda.synchronize()
+    q.q4lin_set_option(handle, q.Q4LIN_OPT_PDL, pdl)
+    q.q4lin_set_option(handle, q.Q4LIN_OPT_FORCE_PATH, TC_SMALL)
+    try:
+        stream = torch.cuda.current_stream().cuda_stream
+        for i, c in enumerate(links):
+            w, s, b = dev[i]
+            sd = q.Q4LIN_SCALE_F16 if c.scales.dtype == np.float16 else q.Q4LIN_SCALE_F32
+            st = q.q4lin_run(handle, bufs[i].data_ptr(), w.data_ptr(), s.data_ptr(),
+                             None if b is None else b.data_ptr(), bufs[i + 1].data_ptr(),
+                             M, c.N, c.K, 32, sd, stream)
+            assert st == q.Q4LIN_OK
+        torch.cuda.synchronize()
+    finally:
+        q.q4lin_set_option(handle, q.Q4LIN_OPT_PDL, 0)
+        q.q4lin_set_option(handle, q.Q4LIN_OPT_FORCE_PATH, 0)
+    host = [b.cpu().numpy() for b in bufs]
+    for i, c in enumerate(links):
+        assert not np.isnan(host[i + 1]).any(), f"link {i} output has NaN"
+        ref, mag = oracle.linear(host[i], c.qweight, c.scales, c.bias, c.K, 32)
+        assert_parity(host[i + 1], ref, mag, TOL_TC)
+
+
+def _auto_kernel(handle, M, N, K, f16=True):
+    import torch
+    from bit_weight_quantized_int4_gb300 import q4lin as q
+    x = torch.zeros(M, K, device="cuda")
+    w = torch.zeros(N, K // 2, dtype=torch.uint8, device="cuda")
+    s = torch.zeros(K // 32, N, dtype=torch.float16 if f16 else torch.float32, device="cuda")
+    out = torch.empty(M, N, device="cuda")
+    st, k = q.q4lin_plan_kernel(handle, x.data_ptr(), w.data_ptr(), s.data_ptr(), None,
+                                out.data_ptr(), M, N, K, 32,
+                                q.Q4LIN_SCALE_F16 if f16 else q.Q4LIN_SCALE_F32)
+    assert st == q.Q4LIN_OK
+    return q.KERNEL_NAMES[k]
+
+
+@pytest.mark.parametrize("M,N,K,kernel", [
+    (2, 128256, 2048, "multirow"),   # two rows: the multi-row GEMV is faster
+    (3, 128256, 2048, "tc_small"),
+    (4, 28672, 4096, "tc_small"),
+    (3, 22016, 4096, "multirow"),    # a last wave of 20 blocks on 152 SMs
+    (4, 8192, 2048, "multirow"),     # 64 blocks at 3-4 rows
+    (8, 8192, 2048, "tc_small"),     # 64 blocks of 8 stages
+    (8, 4096, 4096, "tc"),           # 32 blocks of 16 stages
+    (16, 128256, 2048, "tc_small"),
+    (16, 14336, 4096, "tc"),         # 16 rows of x for K = 4096 do not stay resident
+    (8, 2048, 2048, "rowstream"),    # 16 blocks, 4 M weights
+])
+def test_auto_dispatch(handle, M, N, K, kernel):
+    assert _auto_kernel(handle, M, N, K) == kernel
