@@ -47,10 +47,10 @@ HEADLINE = "8b"
 # one-launch ncu captures (dram__bytes_read.sum + dram__bytes_write.sum; bench.py
 # --profile launch:<model>:<kind>, each launch on its own cold weights).  Valid only for
 # the kernel code they were taken with (gemv_source_sha); any other code reports null.
-LAUNCH_TRAFFIC = {"source_sha256": "0d2bc1909e996a98", "bytes": {
-    "8b:qkv": 14203904, "8b:o": 9482240, "8b:gateup": 66192640, "8b:down": 33116672,
-    "8b:lm_head": 298875136, "1b:qkv": 3575808, "1b:o": 2395904, "1b:gateup": 18919168,
-    "1b:down": 9506816, "1b:lm_head": 150852608}}
+LAUNCH_TRAFFIC = {"source_sha256": "f530a05ba646638e", "bytes": {
+    "8b:qkv": 14203648, "8b:o": 9482240, "8b:gateup": 66401536, "8b:down": 33116672,
+    "8b:lm_head": 298558208, "1b:qkv": 3575808, "1b:o": 2395904, "1b:gateup": 18919168,
+    "1b:down": 9507072, "1b:lm_head": 150955776}}
 
 
 def gemv_source_sha():
