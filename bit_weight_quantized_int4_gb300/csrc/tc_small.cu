@@ -26,17 +26,23 @@
 // ring indices without divisions, and the roles off the issuers' path sleep between polls
 // of their barriers, which together took 93.7 to 85 us.)
 //
-// Roles (800 threads, one CTA per SM, persistent over the row blocks blockIdx.x + k grid):
+// Roles (800 threads, 832 with streamed x; one CTA per SM, persistent over the row blocks
+// blockIdx.x + k grid):
 //   warp 0, one lane:  TMA producer of the weights.  Per 256-k stage of a block: the codes
 //                      [128 rows x 128 B] (128-byte swizzle) and the block's group scales
 //                      [groups of the stage x 128 rows], into a ring of up to seven stages
 //                      (what shared memory leaves next to x).  A stage is released once the
 //                      dequantizing warps have read it.  The weights do not depend on the
 //                      preceding kernel: no dependency wait.
-//   warp 24, one lane: after griddepcontrol.wait, TMA copies of the whole x (resident for
-//                      all the CTA's blocks: K <= 5120 as 8-row chunks when M <= 8, K <= 2560
-//                      as 16-row chunks), one 3D box of 8 chunks [rows x 32 k] per 256-k
-//                      group on its own barrier; then the fourth MMA issuer.
+//   warp 24, one lane: the fourth MMA issuer; when x fits next to three weight stages (K
+//                      <= 5120 as 8-row chunks when M <= 8, K <= 2560 as 16-row chunks) it
+//                      first copies the whole x after griddepcontrol.wait, resident for all
+//                      the CTA's blocks, one 3D box of 8 chunks [rows x 32 k] per 256-k group
+//                      on its own barrier.
+//   warp 25, one lane: (longer K only) streams x instead, one 256-k group per stage of the
+//                      CTA's sequence through a ring of three, released by the MMAs'
+//                      commits: ~5 % slower than resident x (28672 x 4096 at 12 rows 34.1 us
+//                      against 33.0 resident at 8).
 //   warps 1-3, lane 0: MMA issuers; slot i of the CTA's sequence goes to issuer i % 4:
 //                      eight tcgen05.mma.kind::tf32 of K = 8 (A from tensor memory), then a
 //                      commit that frees the A slot; after its last slot of a block, a commit
@@ -89,10 +95,12 @@ constexpr int kWStageBytes = kWBox + kSMax;       // 20 KiB
 constexpr int kMaxWStages = 7;                    // weight ring: up to 140 KiB in flight
 constexpr int kMinWStages = 3;
 constexpr int kMaxXGroups = 20;                   // x resident: K <= 5120 (20 x 256 k)
-constexpr int kWarps = 8 + 4 * kTeams + 1;
+constexpr int kXStages = 3;                       // x streamed: a ring of 256-k groups
+constexpr int kWarps = 8 + 4 * kTeams + 2;
 constexpr int kThreads = 32 * kWarps;
 constexpr int kDeqWarp0 = 8;
-constexpr int kXWarp = 8 + 4 * kTeams;             // the x producer, then an MMA issuer
+constexpr int kIss3Warp = 8 + 4 * kTeams;          // the fourth MMA issuer (resident x: its loader)
+constexpr int kXWarp = kIss3Warp + 1;              // the x producer of streamed x (launched only then)
 constexpr int kBarBytes = 1024;
 constexpr int kSmemCap = 227 * 1024;              // opt-in shared memory of a CTA
 constexpr int64_t kDrainNs = 4000000000LL;
@@ -109,6 +117,7 @@ struct TsArgs {
     int wst;              // stages of the weight ring
     int xrows;            // rows of x per chunk in shared memory: 8 (M <= 8) or 16
     uint32_t x_bytes;     // x region: 8 chunks x xrows x 128 B per 256-k group, + 1 KiB
+    int x_ring;           // 0: all of x resident; 1: streamed through a ring of kXStages
     int skip_first_copy;  // test hook: stage 0's codes are not requested
     int* status;
     int64_t wait_ns;
@@ -158,8 +167,8 @@ __device__ __forceinline__ void dequant_chunk(const uint4 w4, float s, uint32_t 
     }
 }
 
-template <bool EH, bool PC, bool F16>
-__global__ void __launch_bounds__(kThreads, 1)
+template <bool EH, bool PC, bool F16, bool XR>
+__global__ void __launch_bounds__(XR ? kThreads : kThreads - 32, 1)
     tc_small_kernel(const __grid_constant__ CUtensorMap tmw, const __grid_constant__ CUtensorMap tms,
                     const __grid_constant__ CUtensorMap tmx, const TsArgs a) {
     extern __shared__ uint8_t smem_raw[];
@@ -171,11 +180,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t wbase = base + a.x_bytes;
     const uint32_t bar0 = wbase + (uint32_t)(a.wst * kWStageBytes);
     auto wstage = [&](int b) { return wbase + (uint32_t)(b * kWStageBytes); };
-    constexpr int kB0 = 0, kB1 = kB0 + 2 * kMaxWStages, kB2 = kB1 + kMaxXGroups,
-                  kB3 = kB2 + 2 * kASlots, kB4 = kB3 + 4;
+    constexpr int kB0 = 0, kB1 = kB0 + 2 * kMaxWStages, kBx = kB1 + kMaxXGroups,
+                  kB2 = kBx + kXStages, kB3 = kB2 + 2 * kASlots, kB4 = kB3 + 4;
     auto wfull = [&](int b) { return bar0 + 8u * (kB0 + b); };
     auto wempty = [&](int b) { return bar0 + 8u * (kB0 + kMaxWStages + b); };
-    auto xfull = [&](int grp) { return bar0 + 8u * (kB1 + grp); };
+    auto xfull = [&](int grp) { return bar0 + 8u * (kB1 + grp); };   // group, or ring slot
+    auto xempty = [&](int b) { return bar0 + 8u * (kBx + b); };       // ring slot (streamed x)
     auto afull = [&](int p) { return bar0 + 8u * (kB2 + p); };
     auto aempty = [&](int p) { return bar0 + 8u * (kB2 + kASlots + p); };
     auto dfull = [&](int q) { return bar0 + 8u * (kB3 + q); };
@@ -191,7 +201,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(wfull(b), 1);
             mbar_init(wempty(b), kSlotsPerStage * 4);  // the 4 dequantizing warps of each slot
         }
-        for (int grp = 0; grp < a.nst; ++grp) mbar_init(xfull(grp), 1);
+        for (int grp = 0; grp < (XR ? kXStages : a.nst); ++grp) mbar_init(xfull(grp), 1);
+        for (int b = 0; b < kXStages; ++b) mbar_init(xempty(b), kSlotsPerStage);  // MMA commits
         for (int p = 0; p < kASlots; ++p) {
             mbar_init(afull(p), 4);
             mbar_init(aempty(p), 1);
@@ -252,20 +263,44 @@ __global__ void __launch_bounds__(kThreads, 1)
                 wait_bounded(wfull(q % a.wst), (q / a.wst) & 1, kDrainNs, nullptr);
             }
         }
-    } else if (warp <= 3 || warp == kXWarp) {
+    } else if (warp == kXWarp) {
         if (lane == 0) {
-            const int u = warp == kXWarp ? 3 : warp - 1;
-            if (warp == kXWarp) {
-                // --------------------------------------------------- TMA producer of x
-                // x stays resident for all the CTA's blocks: it is read from L2 once per
-                // CTA (every CTA reads the same lines; re-reading them per block made those
-                // L2 lines the bottleneck), in 256-k groups, each on its own barrier.  Then
-                // this thread is the fourth MMA issuer.
+            // ------------------------------------------------- TMA producer of streamed x
+            // One 256-k group per stage of the CTA's sequence through a ring of kXStages,
+            // released by the MMAs' commits (this warp is launched only in that mode).
+            prefetch_tensormap(&tmx);
+            griddep_wait();  // x belongs to the dependency chain
+            const uint32_t gbytes = (uint32_t)(kChunksPerStage * a.xrows * 128);
+            int g = 0;
+            for (; g < n_stages; ++g) {
+                const int b = g % kXStages;
+                if (g >= kXStages && !wait_backoff(xempty(b), ((g / kXStages) - 1) & 1,
+                                                   a.wait_ns, failed, 64)) {
+                    record_failure(a.status, failed);
+                    break;
+                }
+                if (*failed) break;
+                mbar_arrive_expect_tx(xfull(b), gbytes);
+                tma_load_3d(xbase + (uint32_t)b * gbytes, &tmx, 0, 0,
+                            kstage(g % a.nst) * kChunksPerStage, xfull(b));
+            }
+            for (int q = g > kXStages ? g - kXStages : 0; q < g; ++q)
+                wait_bounded(xfull(q % kXStages), (q / kXStages) & 1, kDrainNs, nullptr);
+        }
+    } else if (warp <= 3 || warp == kIss3Warp) {
+        if (lane == 0) {
+            const int u = warp == kIss3Warp ? 3 : warp - 1;
+            if (warp == kIss3Warp && !XR) {
+                // --------------------------------------------------- TMA loads of resident x
+                // All of x, read from L2 once per CTA (every CTA reads the same lines;
+                // re-reading them per block made those L2 lines the bottleneck), in 256-k
+                // groups on their own barriers, in the order of first use; then this thread
+                // is the fourth MMA issuer.
                 prefetch_tensormap(&tmx);
                 griddep_wait();  // x belongs to the dependency chain
                 const uint32_t gbytes = (uint32_t)(kChunksPerStage * a.xrows * 128);
                 for (int q = 0; q < a.nst; ++q) {
-                    const int grp = kstage(q);  // in the order of first use
+                    const int grp = kstage(q);
                     mbar_arrive_expect_tx(xfull(grp), gbytes);
                     tma_load_3d(xbase + (uint32_t)grp * gbytes, &tmx, 0, 0,
                                 grp * kChunksPerStage, xfull(grp));
@@ -277,6 +312,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             // slot p and the parity of its barrier advance without divisions.
             int j = 0, in_blk = u, p = u;
             uint32_t pph = 0;
+            // Streamed x: the ring slot xb and phase xph of the current stage (an issuer
+            // takes one slot of every stage, so they advance by one stage a slot).
+            static_assert(kSlotsPerStage == kIssuers, "one slot of every stage per issuer");
+            int xb = 0;
+            uint32_t xph = 0;
             for (int i = u; i < n_slots; i += kIssuers) {
                 while (in_blk >= slots_per_block) in_blk -= slots_per_block, ++j;
                 const int par = j & 1;
@@ -286,8 +326,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if ((first && j >= 2 &&
                      !wait_bounded(dempty(par), ((j >> 1) - 1) & 1, a.wait_ns, failed)) ||
                     !wait_bounded(afull(p), pph, a.wait_ns, failed) ||
-                    (j == 0 && sl < kIssuers &&
-                     !wait_bounded(xfull(kstage(t)), 0, a.wait_ns, failed))) {
+                    (!XR && j == 0 && sl < kIssuers &&
+                     !wait_bounded(xfull(kstage(t)), 0, a.wait_ns, failed)) ||
+                    (XR && !wait_bounded(xfull(xb), xph, a.wait_ns, failed))) {
                     record_failure(a.status, failed);
                     break;
                 }
@@ -299,7 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // The slot's two x chunks in the resident copy (with 8 rows a chunk, rows 8-15
                 // of the MMA's B read the next chunk: only D columns m >= 8 >= M see them); +2
                 // in the descriptor's address field per 32 bytes (K = 8 tf32) along a row.
-                const int chunk = kstage(t) * kChunksPerStage + sl * (kSlotK / kChunk);
+                const int chunk = (XR ? xb : kstage(t)) * kChunksPerStage + sl * (kSlotK / kChunk);
 #pragma unroll
                 for (int h = 0; h < kSlotK / kChunk; ++h) {
                     const uint64_t bd =
@@ -310,15 +351,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     (first && h == 0 && kk == 0) ? 0u : 1u);
                 }
                 mma_commit(aempty(p));
+                if (XR) mma_commit(xempty(xb));
                 if (last) mma_commit(dfull(par));
                 in_blk += kIssuers;
                 if ((p += kIssuers) >= kASlots) p -= kASlots, pph ^= 1u;
+                if (++xb == kXStages) xb = 0, xph ^= 1u;
             }
             // Every MMA this thread issued completes before the CTA frees tensor memory (and
-            // the copies of x have landed).
+            // the copies of resident x have landed).
             mma_commit(drain(u));
             wait_bounded(drain(u), 0, kDrainNs, nullptr);
-            if (warp == kXWarp)
+            if (warp == kIss3Warp && !XR)
                 for (int grp = 0; grp < a.nst; ++grp) wait_bounded(xfull(grp), 0, kDrainNs, nullptr);
         }
     } else if (warp < kDeqWarp0) {
@@ -417,15 +460,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
-template <bool EH, bool PC, bool F16>
+template <bool EH, bool PC, bool F16, bool XR>
 cudaError_t launch_ts(const CUtensorMap& tw, const CUtensorMap& ts, const CUtensorMap& tx,
                       const TsArgs& a, unsigned grid, int smem, const LaunchCtx& c) {
-    constexpr auto kernel = tc_small_kernel<EH, PC, F16>;
+    constexpr auto kernel = tc_small_kernel<EH, PC, F16, XR>;
     const cudaError_t attr = kernel_smem_once<kernel>(kSmemCap);
     if (attr != cudaSuccess) return attr;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(XR ? kThreads : kThreads - 32);  // the x producer warp: streamed x only
     cfg.dynamicSmemBytes = (size_t)smem;
     cfg.stream = c.stream;
     cudaLaunchAttribute at[1];
@@ -438,22 +481,42 @@ cudaError_t launch_ts(const CUtensorMap& tw, const CUtensorMap& ts, const CUtens
     return cudaLaunchKernelEx(&cfg, kernel, tw, ts, tx, a);
 }
 
+template <bool XR>
+cudaError_t launch_eh(const Problem& p, const CUtensorMap& tw, const CUtensorMap& ts,
+                      const CUtensorMap& tx, const TsArgs& a, unsigned grid, int smem,
+                      const LaunchCtx& c) {
+    const bool pc = p.group_size >= p.K, eh = p.even_high != 0, f16 = p.scale_f16 != 0;
+    if (pc) {
+        if (eh) return f16 ? launch_ts<true, true, true, XR>(tw, ts, tx, a, grid, smem, c)
+                           : launch_ts<true, true, false, XR>(tw, ts, tx, a, grid, smem, c);
+        return f16 ? launch_ts<false, true, true, XR>(tw, ts, tx, a, grid, smem, c)
+                   : launch_ts<false, true, false, XR>(tw, ts, tx, a, grid, smem, c);
+    }
+    if (eh) return f16 ? launch_ts<true, false, true, XR>(tw, ts, tx, a, grid, smem, c)
+                       : launch_ts<true, false, false, XR>(tw, ts, tx, a, grid, smem, c);
+    return f16 ? launch_ts<false, false, true, XR>(tw, ts, tx, a, grid, smem, c)
+               : launch_ts<false, false, false, XR>(tw, ts, tx, a, grid, smem, c);
+}
+
 int log2_pow2(int64_t v) {
     for (int s = 0; s < 62; ++s)
         if ((int64_t(1) << s) == v) return s;
     return -1;
 }
 
-// Shared memory: resident x (8 chunks x rows x 128 B per 256-k group, + 1 KiB that the
+// Shared memory: x (8 chunks x rows x 128 B per 256-k group: all groups when they fit
+// next to at least kMinWStages weight stages, else a ring of kXStages; + 1 KiB that the
 // 8-row layout's MMAs read past the last chunk), then as many weight stages as fit (at
 // most kMaxWStages).  Returns the weight stages (0 if fewer than kMinWStages fit).
-int ts_layout(const Problem& p, int smem_cap, uint32_t* x_bytes, int* xrows, int* smem) {
+int ts_layout(const Problem& p, int smem_cap, uint32_t* x_bytes, int* xrows, int* x_ring,
+              int* smem) {
     const int64_t nst = (p.K + kStageK - 1) / kStageK;
-    if (nst > kMaxXGroups) return 0;
     *xrows = p.M <= 8 ? 8 : 16;
-    *x_bytes = (uint32_t)(nst * kChunksPerStage * *xrows * 128 + 1024);
-    const int64_t room = (int64_t)std::min(smem_cap, kSmemCap) - 1024 - *x_bytes - kBarBytes;
-    const int wst = (int)std::min<int64_t>(kMaxWStages, room / kWStageBytes);
+    const int64_t gbytes = kChunksPerStage * *xrows * 128;
+    const int64_t cap = (int64_t)std::min(smem_cap, kSmemCap) - 1024 - kBarBytes;
+    *x_ring = !(nst <= kMaxXGroups && cap - (nst * gbytes + 1024) >= kMinWStages * kWStageBytes);
+    *x_bytes = (uint32_t)((*x_ring ? kXStages : nst) * gbytes + 1024);
+    const int wst = (int)std::min<int64_t>(kMaxWStages, (cap - *x_bytes) / kWStageBytes);
     if (wst < kMinWStages) return 0;
     *smem = 1024 + (int)*x_bytes + wst * kWStageBytes + kBarBytes;
     return wst;
@@ -474,8 +537,8 @@ bool tc_small_eligible(const Problem& p, const LaunchCtx& c) {
         if (reinterpret_cast<uintptr_t>(p.scales) % 16 || (p.N * esz) % 16 != 0) return false;
     }
     uint32_t xb;
-    int xr, smem;
-    if (ts_layout(p, c.max_smem_optin, &xb, &xr, &smem) == 0) return false;
+    int xr, ring, smem;
+    if (ts_layout(p, c.max_smem_optin, &xb, &xr, &ring, &smem) == 0) return false;
     return tensor_map_encoder() != nullptr;
 }
 
@@ -496,7 +559,7 @@ cudaError_t tc_small_launch(const Problem& p, const LaunchCtx& c) {
     const int gps = pc ? 0 : std::max(1, kStageK >> (a.gs_shift + 5));
     a.w_tx = (uint32_t)(kWBox + gps * kRows * esz);
     int smem = 0;
-    a.wst = ts_layout(p, c.max_smem_optin, &a.x_bytes, &a.xrows, &smem);
+    a.wst = ts_layout(p, c.max_smem_optin, &a.x_bytes, &a.xrows, &a.x_ring, &smem);
     a.skip_first_copy = c.tc_skip_first_copy;
     a.status = c.status_word;
     a.wait_ns = c.wait_limit_ns;
@@ -539,17 +602,8 @@ cudaError_t tc_small_launch(const Problem& p, const LaunchCtx& c) {
             return cudaErrorInvalidValue;
     }
     const unsigned grid = (unsigned)std::min<int64_t>(a.blocks, c.sm_count);
-    const bool eh = p.even_high != 0, f16 = p.scale_f16 != 0;
-    if (pc) {
-        if (eh) return f16 ? launch_ts<true, true, true>(tw, ts, tx, a, grid, smem, c)
-                           : launch_ts<true, true, false>(tw, ts, tx, a, grid, smem, c);
-        return f16 ? launch_ts<false, true, true>(tw, ts, tx, a, grid, smem, c)
-                   : launch_ts<false, true, false>(tw, ts, tx, a, grid, smem, c);
-    }
-    if (eh) return f16 ? launch_ts<true, false, true>(tw, ts, tx, a, grid, smem, c)
-                       : launch_ts<true, false, false>(tw, ts, tx, a, grid, smem, c);
-    return f16 ? launch_ts<false, false, true>(tw, ts, tx, a, grid, smem, c)
-               : launch_ts<false, false, false>(tw, ts, tx, a, grid, smem, c);
+    return a.x_ring ? launch_eh<true>(p, tw, ts, tx, a, grid, smem, c)
+                    : launch_eh<false>(p, tw, ts, tx, a, grid, smem, c);
 }
 
 }  // namespace q4lin

@@ -72,10 +72,10 @@ typedef enum {
     Q4LIN_PATH_TC = 3,      /* tcgen05 tensor-core GEMM (TMEM accumulators)            */
     Q4LIN_PATH_TC_SMALL = 4 /* tcgen05 GEMM for 2 <= M <= 16 activation rows: persistent
                                CTAs over 128-row weight blocks, each weight read once,
-                               x resident in shared memory (K % 32 == 0, K <= 5120 up to
-                               8 rows and K <= 2560 above, 16-byte aligned x and qweight;
-                               grouped scales: a power-of-two multiple of 32 as group
-                               size and a scale row of whole 16-byte units); tensor-core
+                               x resident in shared memory or streamed for long K
+                               (K % 32 == 0, 16-byte aligned x and qweight; grouped
+                               scales: a power-of-two multiple of 32 as group size and a
+                               scale row of whole 16-byte units); tensor-core
                                tolerance.  AUTO takes it for 3..16 rows when the
                                128-row blocks fill the SMs (measured crossover) */
 } q4lin_path_t;

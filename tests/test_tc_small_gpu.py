@@ -4,7 +4,8 @@ bit_weight_quantized_int4_gb300/csrc/tc_small.cu) with the fp64 oracle, through 
 Every element of out[M, N] is checked at the tensor-core tolerance (4e-3 * sum_k|x*w| +
 1e-6); dyadic inputs and all-8 codes must come out bit-exact.  Covered: every M from 2 to
 16, ragged N (rows past N in the last 128-row block), ragged K (a last 256-k stage that is
-mostly past K), the longest K whose x stays resident, group sizes from 32 to wider than a stage,
+mostly past K), the longest K whose x stays resident and longer ones whose x streams,
+group sizes from 32 to wider than a stage,
 per-channel scales (fp16 and fp32), fp32 and fp16 group scales, bias or none, the
 even-high nibble order, persistent CTAs over many blocks (more blocks than SMs), repeated
 calls bit-identical, and a bounded wait that runs out cleanly.
@@ -66,6 +67,26 @@ def test_long_k_up_to_8_rows(handle, M, N, K, gs, f16):
     check(handle, synth.make_case(M, N, K, gs, scale_f16=f16, bias=True, seed=N + K + M))
 
 
+@pytest.mark.parametrize("M,N,K,gs,f16", [
+    (4, 2600, 8192, 32, True),      # 8-row chunks of x, too long to stay resident
+    (12, 1000, 4096, 64, False),    # 16-row chunks, K > 2560
+    (16, 700, 14336, 14336, True),  # per channel, long K
+    (9, 3000, 2592, 32, True),      # just past the resident limit of 16-row chunks, ragged K
+])
+def test_streamed_x(handle, M, N, K, gs, f16):
+    """x too long to stay resident in shared memory: it streams through a ring of three
+    256-k groups per CTA, released by the MMAs' commits."""
+    check(handle, synth.make_case(M, N, K, gs, scale_f16=f16, bias=True, seed=N + K + M))
+
+
+def test_streamed_x_dyadic_bit_exact(handle):
+    c = synth.make_dyadic_case(12, 264, 4096, 32, scale_f16=True, bias=True, seed=12)
+    out, used = run_q4lin(handle, c, TC_SMALL)
+    assert used == TC_SMALL
+    ref, _ = oracle.linear(c.x, c.qweight, c.scales, c.bias, c.K, c.group_size)
+    np.testing.assert_array_equal(out.astype(np.float64), ref)
+
+
 @pytest.mark.parametrize("M", [3, 16])
 def test_persistent_over_many_blocks(handle, M):
     """More 128-row blocks than SMs (the vocabulary-sized head): each CTA takes several
@@ -102,15 +123,14 @@ def test_repeated_calls_bit_identical(handle):
 
 
 def test_ineligible_shapes_are_refused(handle):
-    """M outside 2..16, K not a multiple of 32, a group size that is not a power-of-two
-    multiple of 32, or an x too long to stay resident in shared memory (K > 5120 up to 8
-    rows, K > 2560 above): the forced path reports Q4LIN_ERR_UNSUPPORTED, nothing runs."""
+    """M outside 2..16, K not a multiple of 32, or a group size that is not a power-of-two
+    multiple of 32: the forced path reports Q4LIN_ERR_UNSUPPORTED and nothing runs."""
     import torch
     from bit_weight_quantized_int4_gb300 import q4lin as q
     q.q4lin_set_option(handle, q.Q4LIN_OPT_FORCE_PATH, TC_SMALL)
     try:
         for M, N, K, gs in [(1, 256, 512, 32), (17, 256, 512, 32), (4, 256, 528, 48),
-                            (4, 256, 1024, 96), (4, 256, 5376, 32), (12, 256, 2816, 32)]:
+                            (4, 256, 1024, 96)]:
             c = synth.make_case(M, N, K, gs, scale_f16=False, bias=False, seed=1)
             x = torch.from_numpy(c.x).cuda()
             w = torch.from_numpy(c.qweight).cuda()
@@ -209,7 +229,7 @@ def _auto_kernel(handle, M, N, K, f16=True):
     (8, 8192, 2048, "tc_small"),     # 64 blocks of 8 stages
     (8, 4096, 4096, "tc"),           # 32 blocks of 16 stages
     (16, 128256, 2048, "tc_small"),
-    (16, 14336, 4096, "tc"),         # 16 rows of x for K = 4096 do not stay resident
+    (16, 14336, 4096, "tc_small"),   # 16 rows of x for K = 4096 stream through a ring
     (8, 2048, 2048, "rowstream"),    # 16 blocks, 4 M weights
 ])
 def test_auto_dispatch(handle, M, N, K, kernel):
