@@ -371,7 +371,8 @@ __global__ void __launch_bounds__(XR ? kThreads : kThreads - 32, 1)
         griddep_wait();  // bias, out belong to the dependency chain
         for (int j = 0; j < my_blocks; ++j) {
             const int par = j & 1;
-            if (!wait_backoff(dfull(par), (j >> 1) & 1, a.wait_ns, failed, 256)) {
+            if (!__all_sync(0xffffffffu,
+                            wait_backoff(dfull(par), (j >> 1) & 1, a.wait_ns, failed, 256))) {
                 if (lane == 0) record_failure(a.status, failed);
                 break;
             }
@@ -412,8 +413,10 @@ __global__ void __launch_bounds__(XR ? kThreads : kThreads - 32, 1)
                 sl -= kSlotsPerStage;
                 if (++b == a.wst) b = 0, wph ^= 1u;
             }
-            if ((i >= kASlots && !wait_backoff(aempty(p), pph ^ 1u, a.wait_ns, failed, 32)) ||
-                !wait_backoff(wfull(b), wph, a.wait_ns, failed, 32)) {
+            // Waits are decided for the whole warp (its tcgen05 instructions are collective).
+            if (!__all_sync(0xffffffffu,
+                            (i < kASlots || wait_backoff(aempty(p), pph ^ 1u, a.wait_ns, failed, 32)) &&
+                                wait_backoff(wfull(b), wph, a.wait_ns, failed, 32))) {
                 if (lane == 0) record_failure(a.status, failed);
                 break;
             }
