@@ -1062,9 +1062,24 @@ def main():
         for s in shapes:
             s["frac_of_hbm"] = round(s["GB_s"] / hbm_peak, 4)
         extra["gemv_shapes"] = shapes
-        # A few activation rows (speculative decoding, small batches): the multi-row GEMV.
-        extra["small_m"] = [shape_bandwidth(torch, h, N, K, M) for M in (2, 3, 4)
-                            for N, K in ((8192, 2048), (2048, 8192), (128256, 2048))]
+        # A few activation rows (speculative decoding, small batches): the multi-row GEMV,
+        # and from 3 rows on large matrices the small-M tensor-core GEMM (AUTO's choice;
+        # each row names the kernel that ran).
+        from bit_weight_quantized_int4_gb300 import q4lin as q
+        small = []
+        for M in (2, 3, 4, 8, 16):
+            for N, K in ((8192, 2048), (2048, 8192), (128256, 2048), (28672, 4096)):
+                row = shape_bandwidth(torch, h, N, K, M)
+                x = torch.empty(M, K, device="cuda")
+                w = torch.empty(N, K // 2, dtype=torch.uint8, device="cuda")
+                sc = torch.empty(K // GROUP, N, dtype=torch.float16, device="cuda")
+                o = torch.empty(M, N, device="cuda")
+                st, kern = q.q4lin_plan_kernel(h, x.data_ptr(), w.data_ptr(), sc.data_ptr(), None,
+                                               o.data_ptr(), M, N, K, GROUP, q.Q4LIN_SCALE_F16)
+                row["kernel"] = q.KERNEL_NAMES[kern] if st == q.Q4LIN_OK else None
+                row["frac_of_hbm"] = round(row["GB_s"] / hbm_peak, 4)
+                small.append(row)
+        extra["small_m"] = small
         extra["training"] = ([backward_bandwidth(torch, h, M, N, K)
                               for M in (1, 8) for N, K in ((2048, 2048), (8192, 2048), (2048, 8192))]
                              + [requant_bandwidth(torch, h, N, K)
