@@ -1067,7 +1067,7 @@ def main():
         # each row names the kernel that ran).
         from bit_weight_quantized_int4_gb300 import q4lin as q
         small = []
-        for M in (2, 3, 4, 8, 16):
+        for M in (2, 3, 4, 8, 16, 32):
             for N, K in ((8192, 2048), (2048, 8192), (128256, 2048), (28672, 4096)):
                 row = shape_bandwidth(torch, h, N, K, M)
                 x = torch.empty(M, K, device="cuda")

@@ -61,21 +61,24 @@ bool multirow_preferred(const q4lin::Problem& p) {
     return (double)p.N * (double)p.K >= 1.0e7 && q4lin::gemv_mr_eligible(p);
 }
 
-// 3..16 activation rows: the small-M tensor-core GEMM (one CTA per SM over 128-row weight
+// 3..32 activation rows: the small-M tensor-core GEMM (one CTA per SM over 128-row weight
 // blocks, each weight read once for all rows) where its blocks fill the SMs.  Its time is
-// close to waves x stages of 256 k x ~1.05 us (device time per launch on GB300, HBM-cold
-// weights: 128256 x 2048 57 us, 28672 x 4096 33 us, 14336 x 4096 19 us, 8192 x 2048 9.1 us,
-// flat in M), against, at 3..4 rows, the multi-row GEMV (128256 x 2048: 66 / 79 us at 3 /
-// 4 rows; it stays ahead where a last wave of a few blocks doubles the small-M GEMM's time:
+// close to waves x stages of 256 k x ~1.05 us up to 16 rows (MMA width 16) and ~1.35 us
+// above (width 32), flat in M (device time per launch on GB300, HBM-cold weights: 128256 x
+// 2048 57 / 74 us, 28672 x 4096 33 / 43 us, 14336 x 4096 19 / 23 us, 8192 x 2048 9.1 /
+// 12.0 us), against, at 3..4 rows, the multi-row GEMV (128256 x 2048: 66 / 79 us at 3 / 4
+// rows; it stays ahead where a last wave of a few blocks doubles the small-M GEMM's time:
 // 22016 x 4096 at 3 rows 27 against 33 us) and, from 5 rows, the tile GEMM (128256 x 2048
-// 111 us, 8192 x 2048 11.1 us; it stays ahead on few long blocks: 4096 x 4096 12 against
-// 17 us).  Two rows stay with the multi-row GEMV (50.5 against 57 us on 128256 x 2048).
+// 111-115 us; it stays ahead on few long blocks, 4096 x 4096 12 against 17 us, and above
+// 16 rows on few blocks, 8192 x 2048 11.4 against 12.0 us).  Two rows stay with the
+// multi-row GEMV (50.5 against 57 us on 128256 x 2048).
 bool tc_small_preferred(const q4lin::Problem& p, const q4lin::LaunchCtx& c) {
-    if (p.M < 3 || p.M > 16 || !q4lin::tc_small_eligible(p, c)) return false;
+    if (p.M < 3 || p.M > 32 || !q4lin::tc_small_eligible(p, c)) return false;
     const int64_t blocks = (p.N + 127) / 128, sms = c.sm_count;
     const int64_t stages = (p.K + 255) / 256, tail = blocks % sms;
     if (p.M <= 4) return blocks >= 100 && (tail == 0 || 4 * tail > sms);
-    return blocks >= 100 || (stages <= 8 && blocks >= 40);
+    if (p.M <= 16) return blocks >= 100 || (stages <= 8 && blocks >= 40);
+    return blocks >= 100;
 }
 
 class DeviceGuard {

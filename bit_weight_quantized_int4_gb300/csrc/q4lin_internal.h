@@ -131,7 +131,7 @@ bool tc_eligible(const Problem& p, const LaunchCtx& c);
 bool tc_uses_f16(const Problem& p, const LaunchCtx& c);
 cudaError_t tc_launch(const Problem& p, const LaunchCtx& c);
 
-// tcgen05 GEMM for 2 <= M <= 16 activation rows (tc_small.cu): persistent CTAs over
+// tcgen05 GEMM for 2 <= M <= 32 activation rows (tc_small.cu): persistent CTAs over
 // 128-row weight blocks, x resident in shared memory (or streamed for long K).  Needs
 // K % 32 == 0, 16-byte aligned x and qweight, and for grouped scales a power-of-two
 // multiple of 32 as group size with 16-byte aligned scale rows.

@@ -1,5 +1,5 @@
 // tc_small.cu -- tcgen05 tensor-core GEMM of the 4-bit weight-quantized linear for a few
-// activation rows (2 <= M <= 16: batched or speculative decode), streaming the weights once.
+// activation rows (2 <= M <= 32: batched or speculative decode), streaming the weights once.
 //
 //   out[m, n] = bias[n] + sum_k x[m, k] * (code[n, k] - 8) * scale[k / gs, n]
 //
@@ -8,11 +8,12 @@
 // D[n, m] = sum_k A[n, k] * B[m, k] per block of 128 weight rows, with
 //   A = the block's dequantized weights (c - 8) * scale as fp32, written by CUDA cores into
 //       tensor memory (lane = weight row, one column per k) and read by the MMA as tf32;
-//   B = x, fp32 chunks of 32 k with the 128-byte swizzle, 8 rows a chunk when M <= 8 and
-//       16 otherwise (rows past M are zeros from the copy's out-of-bounds fill; with 8-row
-//       chunks the MMA's rows 8-15 read the next chunk, which only D columns m >= M see),
-//       read as tf32;
-//   D = fp32 accumulators in tensor memory (128 lanes x 16 columns).
+//   B = x, fp32 chunks of 32 k with the 128-byte swizzle, 8 rows a chunk when M <= 8, 16
+//       up to 16 rows and 32 above (rows past M are zeros from the copy's out-of-bounds
+//       fill; with 8-row chunks the MMA's rows 8-15 read the next chunk, which only D
+//       columns m >= M see), read as tf32;
+//   D = fp32 accumulators in tensor memory (128 lanes x BT columns: the MMA width BT is 16
+//       up to 16 rows and 32 above).
 // tf32 keeps 10 explicit mantissa bits of each operand: a product carries a relative error
 // below 2^-9, inside the 4e-3 * sum|x*w| bar of the tensor-core path.
 //
@@ -35,7 +36,8 @@
 //                      dequantizing warps have read it.  The weights do not depend on the
 //                      preceding kernel: no dependency wait.
 //   warp 24, one lane: the fourth MMA issuer; when x fits next to three weight stages (K
-//                      <= 5120 as 8-row chunks when M <= 8, K <= 2560 as 16-row chunks) it
+//                      <= 5120 as 8-row chunks when M <= 8, K <= 2560 as 16-row chunks,
+//                      K <= 1280 as 32-row chunks) it
 //                      first copies the whole x after griddepcontrol.wait, resident for all
 //                      the CTA's blocks, one 3D box of 8 chunks [rows x 32 k] per 256-k group
 //                      on its own barrier.
@@ -62,8 +64,8 @@
 //                      below the tf32 rounding).  Per-channel scales are applied in the
 //                      epilogue instead (A = c - 8 exactly).
 //   Each CTA walks K from its own starting stage (blockIdx.x % stages, wrapping).
-// Tensor memory: accumulators [0, 128) (two blocks in flight x four issuers x 16 columns),
-// the A ring [128, 512) (six slots of 64 columns).  Every wait is bounded in time; a
+// Tensor memory: accumulators [0, 8 BT) (two blocks in flight x four issuers x BT columns),
+// the A ring [8 BT, 512) (six slots of 64 columns at BT = 16, four at BT = 32).  Every wait is bounded in time; a
 // timeout records code 1 in the status word, each role stops, the issuers drain their
 // MMAs, and the CTA frees its tensor memory and returns without storing.
 #include <algorithm>
@@ -76,7 +78,7 @@ namespace {
 using namespace ptx;
 
 constexpr int kRows = 128;                        // weight rows per block (MMA M)
-constexpr int kBt = 16;                           // activation rows per MMA (N); M <= kBt
+constexpr int kBt = 32;                           // most activation rows (MMA N = 16 or 32)
 constexpr int kStageK = 256;                      // k per stage (weights and x alike)
 constexpr int kChunk = 32;                        // k per 16-byte chunk of a code row
 constexpr int kChunksPerStage = kStageK / kChunk; // 8
@@ -84,11 +86,13 @@ constexpr int kSlotK = 64;                        // k per A slot: two chunks, 8
 constexpr int kSlotsPerStage = kStageK / kSlotK;  // 4
 constexpr int kIssuers = 4;                       // warps 1-3 and the x producer's warp
 constexpr int kTeams = 4;
-constexpr int kASlots = 6;                        // A ring: 6 x 64 tensor-memory columns
-static_assert(kASlots >= kIssuers && kASlots >= kTeams && kSlotsPerStage >= kIssuers,
+// Tensor memory for MMA width BT: two blocks' accumulators (2 x issuers x BT columns), then
+// the A ring of 64-k slots: six slots at BT = 16, four at BT = 32.
+__host__ __device__ constexpr int acol0(int bt) { return 2 * kIssuers * bt; }
+__host__ __device__ constexpr int aslots(int bt) { return (512 - acol0(bt)) / kSlotK; }
+constexpr int kMaxASlots = aslots(16);
+static_assert(aslots(32) >= kIssuers && aslots(32) >= kTeams && kSlotsPerStage >= kIssuers,
               "ring positions advance by less than a lap; every issuer has a slot per stage");
-static_assert(2 * kIssuers * kBt <= 128, "two blocks' accumulators fit below the A ring");
-constexpr int kACol0 = 128;
 constexpr int kWBox = kRows * 128;                // codes of a stage: [128 rows x 128 B]
 constexpr int kSMax = 8 * kRows * 4;              // scales: up to 8 groups x 128 rows
 constexpr int kWStageBytes = kWBox + kSMax;       // 20 KiB
@@ -115,7 +119,7 @@ struct TsArgs {
     int gs_shift;         // log2(group_size / 32) (grouped scales)
     uint32_t w_tx;        // bytes of one stage's codes and scales
     int wst;              // stages of the weight ring
-    int xrows;            // rows of x per chunk in shared memory: 8 (M <= 8) or 16
+    int xrows;            // rows of x per chunk in shared memory: 8, 16 or 32 (by M)
     uint32_t x_bytes;     // x region: 8 chunks x xrows x 128 B per 256-k group, + 1 KiB
     int x_ring;           // 0: all of x resident; 1: streamed through a ring of kXStages
     int skip_first_copy;  // test hook: stage 0's codes are not requested
@@ -167,10 +171,11 @@ __device__ __forceinline__ void dequant_chunk(const uint4 w4, float s, uint32_t 
     }
 }
 
-template <bool EH, bool PC, bool F16, bool XR>
+template <bool EH, bool PC, bool F16, bool XR, int BT>
 __global__ void __launch_bounds__(XR ? kThreads : kThreads - 32, 1)
     tc_small_kernel(const __grid_constant__ CUtensorMap tmw, const __grid_constant__ CUtensorMap tms,
                     const __grid_constant__ CUtensorMap tmx, const TsArgs a) {
+    constexpr int kAC0 = acol0(BT), kAS = aslots(BT);
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -181,13 +186,13 @@ __global__ void __launch_bounds__(XR ? kThreads : kThreads - 32, 1)
     const uint32_t bar0 = wbase + (uint32_t)(a.wst * kWStageBytes);
     auto wstage = [&](int b) { return wbase + (uint32_t)(b * kWStageBytes); };
     constexpr int kB0 = 0, kB1 = kB0 + 2 * kMaxWStages, kBx = kB1 + kMaxXGroups,
-                  kB2 = kBx + kXStages, kB3 = kB2 + 2 * kASlots, kB4 = kB3 + 4;
+                  kB2 = kBx + kXStages, kB3 = kB2 + 2 * kMaxASlots, kB4 = kB3 + 4;
     auto wfull = [&](int b) { return bar0 + 8u * (kB0 + b); };
     auto wempty = [&](int b) { return bar0 + 8u * (kB0 + kMaxWStages + b); };
     auto xfull = [&](int grp) { return bar0 + 8u * (kB1 + grp); };   // group, or ring slot
     auto xempty = [&](int b) { return bar0 + 8u * (kBx + b); };       // ring slot (streamed x)
     auto afull = [&](int p) { return bar0 + 8u * (kB2 + p); };
-    auto aempty = [&](int p) { return bar0 + 8u * (kB2 + kASlots + p); };
+    auto aempty = [&](int p) { return bar0 + 8u * (kB2 + kAS + p); };
     auto dfull = [&](int q) { return bar0 + 8u * (kB3 + q); };
     auto dempty = [&](int q) { return bar0 + 8u * (kB3 + 2 + q); };
     auto drain = [&](int u) { return bar0 + 8u * (kB4 + u); };
@@ -203,7 +208,7 @@ __global__ void __launch_bounds__(XR ? kThreads : kThreads - 32, 1)
         }
         for (int grp = 0; grp < (XR ? kXStages : a.nst); ++grp) mbar_init(xfull(grp), 1);
         for (int b = 0; b < kXStages; ++b) mbar_init(xempty(b), kSlotsPerStage);  // MMA commits
-        for (int p = 0; p < kASlots; ++p) {
+        for (int p = 0; p < kAS; ++p) {
             mbar_init(afull(p), 4);
             mbar_init(aempty(p), 1);
         }
@@ -307,7 +312,7 @@ __global__ void __launch_bounds__(XR ? kThreads : kThreads - 32, 1)
                 }
             }
             // ------------------------------------------------------------- MMA issuers
-            const uint32_t idesc = tf32_idesc(kRows, kBt);
+            const uint32_t idesc = tf32_idesc(kRows, BT);
             // Slots u, u + kIssuers, ...: the block j, the slot's place in the block, its A ring
             // slot p and the parity of its barrier advance without divisions.
             int j = 0, in_blk = u, p = u;
@@ -335,8 +340,8 @@ __global__ void __launch_bounds__(XR ? kThreads : kThreads - 32, 1)
                 // A was written by tcgen05.st and fenced by its writers before they arrived;
                 // x came by TMA.  The waits order both.
                 tc_fence_after();
-                const uint32_t d = tmem + (uint32_t)((par * kIssuers + u) * kBt);
-                const uint32_t acol = tmem + (uint32_t)(kACol0 + p * kSlotK);
+                const uint32_t d = tmem + (uint32_t)((par * kIssuers + u) * BT);
+                const uint32_t acol = tmem + (uint32_t)(kAC0 + p * kSlotK);
                 // The slot's two x chunks in the resident copy (with 8 rows a chunk, rows 8-15
                 // of the MMA's B read the next chunk: only D columns m >= 8 >= M see them); +2
                 // in the descriptor's address field per 32 bytes (K = 8 tf32) along a row.
@@ -354,7 +359,7 @@ __global__ void __launch_bounds__(XR ? kThreads : kThreads - 32, 1)
                 if (XR) mma_commit(xempty(xb));
                 if (last) mma_commit(dfull(par));
                 in_blk += kIssuers;
-                if ((p += kIssuers) >= kASlots) p -= kASlots, pph ^= 1u;
+                if ((p += kIssuers) >= kAS) p -= kAS, pph ^= 1u;
                 if (++xb == kXStages) xb = 0, xph ^= 1u;
             }
             // Every MMA this thread issued completes before the CTA frees tensor memory (and
@@ -377,14 +382,17 @@ __global__ void __launch_bounds__(XR ? kThreads : kThreads - 32, 1)
                 break;
             }
             tc_fence_after();
-            float acc[kBt];
+            float acc[BT];
 #pragma unroll
             for (int u = 0; u < kIssuers; ++u) {
-                uint32_t r[kBt];
-                tmem_ld16(lane_base + (uint32_t)((par * kIssuers + u) * kBt), r);
 #pragma unroll
-                for (int m = 0; m < kBt; ++m)
-                    acc[m] = u == 0 ? __uint_as_float(r[m]) : acc[m] + __uint_as_float(r[m]);
+                for (int c = 0; c < BT; c += 16) {
+                    uint32_t r[16];
+                    tmem_ld16(lane_base + (uint32_t)((par * kIssuers + u) * BT + c), r);
+#pragma unroll
+                    for (int m = 0; m < 16; ++m)
+                        acc[c + m] = u == 0 ? __uint_as_float(r[m]) : acc[c + m] + __uint_as_float(r[m]);
+                }
             }
             tc_fence_before();
             __syncwarp();
@@ -394,7 +402,7 @@ __global__ void __launch_bounds__(XR ? kThreads : kThreads - 32, 1)
                 const float cs = PC ? ld_scale(a.scales, F16, n) : 1.f;
                 const float bv = a.bias ? __ldg(a.bias + n) : 0.f;
 #pragma unroll
-                for (int m = 0; m < kBt; ++m)
+                for (int m = 0; m < BT; ++m)
                     if (m < a.M) a.out[(int64_t)m * a.N + n] = fmaf(acc[m], cs, bv);
             }
         }
@@ -415,7 +423,7 @@ __global__ void __launch_bounds__(XR ? kThreads : kThreads - 32, 1)
             }
             // Waits are decided for the whole warp (its tcgen05 instructions are collective).
             if (!__all_sync(0xffffffffu,
-                            (i < kASlots || wait_backoff(aempty(p), pph ^ 1u, a.wait_ns, failed, 32)) &&
+                            (i < kAS || wait_backoff(aempty(p), pph ^ 1u, a.wait_ns, failed, 32)) &&
                                 wait_backoff(wfull(b), wph, a.wait_ns, failed, 32))) {
                 if (lane == 0) record_failure(a.status, failed);
                 break;
@@ -446,14 +454,14 @@ __global__ void __launch_bounds__(XR ? kThreads : kThreads - 32, 1)
             for (int h = 0; h < kCps; ++h) {
                 uint32_t v[32];
                 dequant_chunk<EH>(w[h], sc[h], v);
-                tmem_st32_async(lane_base + (uint32_t)(kACol0 + p * kSlotK + kChunk * h), v);
+                tmem_st32_async(lane_base + (uint32_t)(kAC0 + p * kSlotK + kChunk * h), v);
             }
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(afull(p));
             sl += kTeams;
-            if ((p += kTeams) >= kASlots) p -= kASlots, pph ^= 1u;
+            if ((p += kTeams) >= kAS) p -= kAS, pph ^= 1u;
         }
     }
 
@@ -463,10 +471,10 @@ __global__ void __launch_bounds__(XR ? kThreads : kThreads - 32, 1)
     if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
-template <bool EH, bool PC, bool F16, bool XR>
+template <bool EH, bool PC, bool F16, bool XR, int BT>
 cudaError_t launch_ts(const CUtensorMap& tw, const CUtensorMap& ts, const CUtensorMap& tx,
                       const TsArgs& a, unsigned grid, int smem, const LaunchCtx& c) {
-    constexpr auto kernel = tc_small_kernel<EH, PC, F16, XR>;
+    constexpr auto kernel = tc_small_kernel<EH, PC, F16, XR, BT>;
     const cudaError_t attr = kernel_smem_once<kernel>(kSmemCap);
     if (attr != cudaSuccess) return attr;
     cudaLaunchConfig_t cfg = {};
@@ -484,21 +492,21 @@ cudaError_t launch_ts(const CUtensorMap& tw, const CUtensorMap& ts, const CUtens
     return cudaLaunchKernelEx(&cfg, kernel, tw, ts, tx, a);
 }
 
-template <bool XR>
+template <bool XR, int BT>
 cudaError_t launch_eh(const Problem& p, const CUtensorMap& tw, const CUtensorMap& ts,
                       const CUtensorMap& tx, const TsArgs& a, unsigned grid, int smem,
                       const LaunchCtx& c) {
     const bool pc = p.group_size >= p.K, eh = p.even_high != 0, f16 = p.scale_f16 != 0;
     if (pc) {
-        if (eh) return f16 ? launch_ts<true, true, true, XR>(tw, ts, tx, a, grid, smem, c)
-                           : launch_ts<true, true, false, XR>(tw, ts, tx, a, grid, smem, c);
-        return f16 ? launch_ts<false, true, true, XR>(tw, ts, tx, a, grid, smem, c)
-                   : launch_ts<false, true, false, XR>(tw, ts, tx, a, grid, smem, c);
+        if (eh) return f16 ? launch_ts<true, true, true, XR, BT>(tw, ts, tx, a, grid, smem, c)
+                           : launch_ts<true, true, false, XR, BT>(tw, ts, tx, a, grid, smem, c);
+        return f16 ? launch_ts<false, true, true, XR, BT>(tw, ts, tx, a, grid, smem, c)
+                   : launch_ts<false, true, false, XR, BT>(tw, ts, tx, a, grid, smem, c);
     }
-    if (eh) return f16 ? launch_ts<true, false, true, XR>(tw, ts, tx, a, grid, smem, c)
-                       : launch_ts<true, false, false, XR>(tw, ts, tx, a, grid, smem, c);
-    return f16 ? launch_ts<false, false, true, XR>(tw, ts, tx, a, grid, smem, c)
-               : launch_ts<false, false, false, XR>(tw, ts, tx, a, grid, smem, c);
+    if (eh) return f16 ? launch_ts<true, false, true, XR, BT>(tw, ts, tx, a, grid, smem, c)
+                       : launch_ts<true, false, false, XR, BT>(tw, ts, tx, a, grid, smem, c);
+    return f16 ? launch_ts<false, false, true, XR, BT>(tw, ts, tx, a, grid, smem, c)
+               : launch_ts<false, false, false, XR, BT>(tw, ts, tx, a, grid, smem, c);
 }
 
 int log2_pow2(int64_t v) {
@@ -514,7 +522,7 @@ int log2_pow2(int64_t v) {
 int ts_layout(const Problem& p, int smem_cap, uint32_t* x_bytes, int* xrows, int* x_ring,
               int* smem) {
     const int64_t nst = (p.K + kStageK - 1) / kStageK;
-    *xrows = p.M <= 8 ? 8 : 16;
+    *xrows = p.M <= 8 ? 8 : (p.M <= 16 ? 16 : 32);
     const int64_t gbytes = kChunksPerStage * *xrows * 128;
     const int64_t cap = (int64_t)std::min(smem_cap, kSmemCap) - 1024 - kBarBytes;
     *x_ring = !(nst <= kMaxXGroups && cap - (nst * gbytes + 1024) >= kMinWStages * kWStageBytes);
@@ -605,8 +613,11 @@ cudaError_t tc_small_launch(const Problem& p, const LaunchCtx& c) {
             return cudaErrorInvalidValue;
     }
     const unsigned grid = (unsigned)std::min<int64_t>(a.blocks, c.sm_count);
-    return a.x_ring ? launch_eh<true>(p, tw, ts, tx, a, grid, smem, c)
-                    : launch_eh<false>(p, tw, ts, tx, a, grid, smem, c);
+    if (p.M > 16)
+        return a.x_ring ? launch_eh<true, 32>(p, tw, ts, tx, a, grid, smem, c)
+                        : launch_eh<false, 32>(p, tw, ts, tx, a, grid, smem, c);
+    return a.x_ring ? launch_eh<true, 16>(p, tw, ts, tx, a, grid, smem, c)
+                    : launch_eh<false, 16>(p, tw, ts, tx, a, grid, smem, c);
 }
 
 }  // namespace q4lin

@@ -70,13 +70,13 @@ typedef enum {
                                else the row-streaming kernel (small M)                */
     Q4LIN_PATH_FFMA = 2,    /* generic CUDA-core kernel: any K, group size, alignment  */
     Q4LIN_PATH_TC = 3,      /* tcgen05 tensor-core GEMM (TMEM accumulators)            */
-    Q4LIN_PATH_TC_SMALL = 4 /* tcgen05 GEMM for 2 <= M <= 16 activation rows: persistent
+    Q4LIN_PATH_TC_SMALL = 4 /* tcgen05 GEMM for 2 <= M <= 32 activation rows: persistent
                                CTAs over 128-row weight blocks, each weight read once,
                                x resident in shared memory or streamed for long K
                                (K % 32 == 0, 16-byte aligned x and qweight; grouped
                                scales: a power-of-two multiple of 32 as group size and a
                                scale row of whole 16-byte units); tensor-core
-                               tolerance.  AUTO takes it for 3..16 rows when the
+                               tolerance.  AUTO takes it for 3..32 rows when the
                                128-row blocks fill the SMs (measured crossover) */
 } q4lin_path_t;
 
@@ -271,7 +271,7 @@ typedef enum {
     Q4LIN_KERNEL_GEMV_TMA_FIXED = 7, /* the decode GEMV with exact fixed-point arithmetic: x as
                                       * 32-bit fixed point per 32-k chunk, codes times x by
                                       * dp4a; chosen when its CTAs take >= 2 row blocks each */
-    Q4LIN_KERNEL_TC_SMALL = 8   /* tcgen05 GEMM for 2 <= M <= 16 (Q4LIN_PATH_TC_SMALL), tf32 */
+    Q4LIN_KERNEL_TC_SMALL = 8   /* tcgen05 GEMM for 2 <= M <= 32 (Q4LIN_PATH_TC_SMALL), tf32 */
 } q4lin_kernel_t;
 
 /* The kernel q4lin_run would launch for these arguments (no launch, no device access);

@@ -1,9 +1,9 @@
-"""Parity of the tensor-core GEMM for 2 <= M <= 16 activation rows (Q4LIN_PATH_TC_SMALL,
+"""Parity of the tensor-core GEMM for 2 <= M <= 32 activation rows (Q4LIN_PATH_TC_SMALL,
 bit_weight_quantized_int4_gb300/csrc/tc_small.cu) with the fp64 oracle, through the C ABI.
 
 Every element of out[M, N] is checked at the tensor-core tolerance (4e-3 * sum_k|x*w| +
 1e-6); dyadic inputs and all-8 codes must come out bit-exact.  Covered: every M from 2 to
-16, ragged N (rows past N in the last 128-row block), ragged K (a last 256-k stage that is
+32 (MMA width 16 up to 16 rows, 32 above), ragged N (rows past N in the last 128-row block), ragged K (a last 256-k stage that is
 mostly past K), the longest K whose x stays resident and longer ones whose x streams,
 group sizes from 32 to wider than a stage,
 per-channel scales (fp16 and fp32), fp32 and fp16 group scales, bias or none, the
@@ -41,7 +41,7 @@ def check(handle, case, even_high=False):
     return out
 
 
-@pytest.mark.parametrize("M", list(range(2, 17)))
+@pytest.mark.parametrize("M", list(range(2, 33)))
 def test_every_m(handle, M):
     check(handle, synth.make_case(M, 1000, 2048, 32, scale_f16=True, bias=True, seed=M))
 
@@ -56,7 +56,7 @@ def test_every_m(handle, M):
     (136, 1536, 1536, True, False),    # per channel, fp16
 ])
 def test_shapes(handle, N, K, gs, f16, bias):
-    for M in (2, 7, 16):
+    for M in (2, 7, 16, 17, 32):
         check(handle, synth.make_case(M, N, K, gs, scale_f16=f16, bias=bias, seed=N + K + M))
 
 
@@ -72,6 +72,7 @@ def test_long_k_up_to_8_rows(handle, M, N, K, gs, f16):
     (12, 1000, 4096, 64, False),    # 16-row chunks, K > 2560
     (16, 700, 14336, 14336, True),  # per channel, long K
     (9, 3000, 2592, 32, True),      # just past the resident limit of 16-row chunks, ragged K
+    (24, 1504, 2048, 32, True),     # 32-row chunks (MMA width 32)
 ])
 def test_streamed_x(handle, M, N, K, gs, f16):
     """x too long to stay resident in shared memory: it streams through a ring of three
@@ -87,7 +88,7 @@ def test_streamed_x_dyadic_bit_exact(handle):
     np.testing.assert_array_equal(out.astype(np.float64), ref)
 
 
-@pytest.mark.parametrize("M", [3, 16])
+@pytest.mark.parametrize("M", [3, 16, 32])
 def test_persistent_over_many_blocks(handle, M):
     """More 128-row blocks than SMs (the vocabulary-sized head): each CTA takes several
     blocks with the accumulators double-buffered between them."""
@@ -99,7 +100,7 @@ def test_even_high(handle):
           even_high=True)
 
 
-@pytest.mark.parametrize("M,f16", [(2, True), (9, False), (16, True)])
+@pytest.mark.parametrize("M,f16", [(2, True), (9, False), (16, True), (24, False), (32, True)])
 def test_dyadic_bit_exact(handle, M, f16):
     c = synth.make_dyadic_case(M, 264, 1024, 32, scale_f16=f16, bias=True, seed=M)
     out, used = run_q4lin(handle, c, TC_SMALL)
@@ -123,13 +124,13 @@ def test_repeated_calls_bit_identical(handle):
 
 
 def test_ineligible_shapes_are_refused(handle):
-    """M outside 2..16, K not a multiple of 32, or a group size that is not a power-of-two
+    """M outside 2..32, K not a multiple of 32, or a group size that is not a power-of-two
     multiple of 32: the forced path reports Q4LIN_ERR_UNSUPPORTED and nothing runs."""
     import torch
     from bit_weight_quantized_int4_gb300 import q4lin as q
     q.q4lin_set_option(handle, q.Q4LIN_OPT_FORCE_PATH, TC_SMALL)
     try:
-        for M, N, K, gs in [(1, 256, 512, 32), (17, 256, 512, 32), (4, 256, 528, 48),
+        for M, N, K, gs in [(1, 256, 512, 32), (33, 256, 512, 32), (4, 256, 528, 48),
                             (4, 256, 1024, 96)]:
             c = synth.make_case(M, N, K, gs, scale_f16=False, bias=False, seed=1)
             x = torch.from_numpy(c.x).cuda()
@@ -168,7 +169,7 @@ def test_bounded_wait_times_out_cleanly(handle):
 
 
 @pytest.mark.parametrize("pdl", [0, 1])
-@pytest.mark.parametrize("M", [4, 12])
+@pytest.mark.parametrize("M", [4, 12, 20])
 def test_chain_with_dependent_launch(handle, M, pdl):
     """Four launches where each output is the next input, with programmatic dependent
     launch on and off: the weights stream before the dependency wait, x is read after it
@@ -231,6 +232,8 @@ def _auto_kernel(handle, M, N, K, f16=True):
     (16, 128256, 2048, "tc_small"),
     (16, 14336, 4096, "tc_small"),   # 16 rows of x for K = 4096 stream through a ring
     (8, 2048, 2048, "rowstream"),    # 16 blocks, 4 M weights
+    (24, 128256, 2048, "tc_small"),  # MMA width 32
+    (24, 8192, 2048, "tc"),          # 64 blocks above 16 rows: the tile GEMM
 ])
 def test_auto_dispatch(handle, M, N, K, kernel):
     assert _auto_kernel(handle, M, N, K) == kernel
