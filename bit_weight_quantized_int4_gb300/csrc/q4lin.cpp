@@ -27,6 +27,7 @@ struct q4lin_handle {
     int64_t wait_limit = 0;  // ns; 0: default
     int tc_skip_first_copy = 0;
     int tc_f16 = 0;
+    int tc_small_operands = 0;
     int* d_status = nullptr;
     float* d_ws = nullptr;     // split-K partial sums
     int* d_tickets = nullptr;  // split-K row-block counters (zero between launches)
@@ -161,6 +162,7 @@ q4lin::LaunchCtx make_ctx(q4lin_handle_t h, cudaStream_t stream) {
     c.wait_limit_ns = h->wait_limit > 0 ? h->wait_limit : kDefaultWaitLimit;
     c.tc_skip_first_copy = h->tc_skip_first_copy;
     c.tc_f16 = h->tc_f16;
+    c.tc_small_operands = h->tc_small_operands;
     c.ws = h->d_ws;
     c.ws_floats = kWsFloats;
     c.tickets = h->d_tickets;
@@ -207,7 +209,8 @@ q4lin_status_t plan(q4lin_handle_t h, const q4lin::Problem& p, const q4lin::Laun
 int kernel_of(const q4lin::Problem& p, const q4lin::LaunchCtx& c, int path) {
     switch (path) {
         case Q4LIN_PATH_TC: return q4lin::tc_uses_f16(p, c) ? Q4LIN_KERNEL_TC_F16 : Q4LIN_KERNEL_TC;
-        case Q4LIN_PATH_TC_SMALL: return Q4LIN_KERNEL_TC_SMALL;
+        case Q4LIN_PATH_TC_SMALL:
+            return q4lin::tc_small_uses_bf16(p, c) ? Q4LIN_KERNEL_TC_SMALL_BF16 : Q4LIN_KERNEL_TC_SMALL;
         case Q4LIN_PATH_GEMV:
             if (q4lin::gemv_tma_eligible(p))
                 return q4lin::gemv_tma_fixed_point(p, c) ? Q4LIN_KERNEL_GEMV_TMA_FIXED
@@ -331,7 +334,8 @@ q4lin_status_t q4lin_run(q4lin_handle_t h, const float* x, const uint8_t* qweigh
     switch (kernel_of(p, c, path)) {
         case Q4LIN_KERNEL_TC:
         case Q4LIN_KERNEL_TC_F16: err = q4lin::tc_launch(p, c); break;
-        case Q4LIN_KERNEL_TC_SMALL: err = q4lin::tc_small_launch(p, c); break;
+        case Q4LIN_KERNEL_TC_SMALL:
+        case Q4LIN_KERNEL_TC_SMALL_BF16: err = q4lin::tc_small_launch(p, c); break;
         case Q4LIN_KERNEL_GEMV_TMA:
         case Q4LIN_KERNEL_GEMV_TMA_FIXED: err = q4lin::gemv_tma_launch(p, c); break;
         case Q4LIN_KERNEL_MULTIROW: err = q4lin::gemv_mr_launch(p, c); break;
@@ -529,6 +533,10 @@ q4lin_status_t q4lin_set_option(q4lin_handle_t h, int option, int64_t value) {
             if (value != 0 && value != 1) return Q4LIN_ERR_INVALID_ARG;
             h->tc_f16 = (int)value;
             return Q4LIN_OK;
+        case Q4LIN_OPT_TC_SMALL_OPERANDS:
+            if (value < 0 || value > 2) return Q4LIN_ERR_INVALID_ARG;
+            h->tc_small_operands = (int)value;
+            return Q4LIN_OK;
         default:
             return Q4LIN_ERR_INVALID_ARG;
     }
@@ -545,6 +553,7 @@ q4lin_status_t q4lin_get_option(q4lin_handle_t h, int option, int64_t* value) {
         case Q4LIN_OPT_PDL: *value = h->pdl; return Q4LIN_OK;
         case Q4LIN_OPT_TC_SKIP_FIRST_COPY: *value = h->tc_skip_first_copy; return Q4LIN_OK;
         case Q4LIN_OPT_TC_F16: *value = h->tc_f16; return Q4LIN_OK;
+        case Q4LIN_OPT_TC_SMALL_OPERANDS: *value = h->tc_small_operands; return Q4LIN_OK;
         default: return Q4LIN_ERR_INVALID_ARG;
     }
 }

@@ -58,7 +58,8 @@ struct LaunchCtx {
     int* status_word;        // device int, first nonzero code a kernel records
     int64_t wait_limit_ns;   // time limit of bounded device-side waits
     int tc_skip_first_copy;  // test hook: the TC producer skips stage 0
-    int tc_f16;              // tensor-core GEMM with fp16 operands
+    int tc_f16 = 0;          // tensor-core GEMM with fp16 operands
+    int tc_small_operands = 0;  // small-M GEMM: 0 auto, 1 tf32, 2 bf16 where it applies
     float* ws;               // scratch for split-K partial sums (may be null)
     int64_t ws_floats;
     int* tickets;            // per-row-block counters, zero between launches (may be null)
@@ -136,6 +137,10 @@ cudaError_t tc_launch(const Problem& p, const LaunchCtx& c);
 // K % 32 == 0, 16-byte aligned x and qweight, and for grouped scales a power-of-two
 // multiple of 32 as group size with 16-byte aligned scale rows.
 bool tc_small_eligible(const Problem& p, const LaunchCtx& c);
+// Whether that kernel multiplies bf16 operands (up to 8 rows, x resident, K > 256; x
+// split into bf16(x) and bf16(x - bf16(x)), the dequantized weights rounded to bf16)
+// rather than tf32: by default from 100 row blocks, or as Q4LIN_OPT_TC_SMALL_OPERANDS says.
+bool tc_small_uses_bf16(const Problem& p, const LaunchCtx& c);
 cudaError_t tc_small_launch(const Problem& p, const LaunchCtx& c);
 
 }  // namespace q4lin

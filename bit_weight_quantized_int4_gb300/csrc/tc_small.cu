@@ -17,6 +17,15 @@
 // tf32 keeps 10 explicit mantissa bits of each operand: a product carries a relative error
 // below 2^-9, inside the 4e-3 * sum|x*w| bar of the tensor-core path.
 //
+// bf16 operands (up to 8 rows, x resident, K > 256; by default from 100 row blocks, where
+// they measured 2-5 % faster): A = (c - 8) * s rounded to bf16, two values per tensor-
+// memory column, so that an A slot of 64 columns holds 128 k and an MMA (kind::f16, bf16 A
+// and B) takes 16 k; B = x as 64-k chunks of 16 rows, rows 0-7 bf16(x) and rows 8-15 the
+// remainder bf16(x - bf16(x)), converted by the dequantizing warps into shared memory at
+// the start; the epilogue adds D columns m and m + 8.  A product then carries a relative
+// error below 2^-9 + 2^-16 (the weight's rounding; x keeps 16 bits), and bf16 has fp32's
+// exponent range, so no input range is excluded.
+//
 // At 16 columns an MMA is cheap for the tensor core but not for the thread that issues it:
 // on GB300 one thread issues a tcgen05.mma of 128 x 16 x 8 about every 50-70 cycles
 // whatever its width, and issuers in different warps add up.  So four issuer threads take
@@ -65,7 +74,12 @@
 //                      epilogue instead (A = c - 8 exactly).
 //   Each CTA walks K from its own starting stage (blockIdx.x % stages, wrapping).
 // Tensor memory: accumulators [0, 8 BT) (two blocks in flight x four issuers x BT columns),
-// the A ring [8 BT, 512) (six slots of 64 columns at BT = 16, four at BT = 32).  Every wait is bounded in time; a
+// the A ring [8 BT, 512) (six slots of 64 columns at BT = 16, four at BT = 32).  Slot i of
+// the sequence takes ring position i % slots on lap i / slots, team i % 4 and issuer i % 4;
+// with six positions a position's laps alternate between two teams (and two issuers), so
+// each position has separate barriers for its even and its odd laps: every barrier is then
+// waited on by one role, phase after phase (a parity wait that ran two phases ahead of its
+// barrier would take the phase before the current one for the awaited one).  Every wait is bounded in time; a
 // timeout records code 1 in the status word, each role stops, the issuers drain their
 // MMAs, and the CTA frees its tensor memory and returns without storing.
 #include <algorithm>
@@ -108,8 +122,20 @@ constexpr int kXWarp = kIss3Warp + 1;              // the x producer of streamed
 constexpr int kBarBytes = 1024;
 constexpr int kSmemCap = 227 * 1024;              // opt-in shared memory of a CTA
 constexpr int64_t kDrainNs = 4000000000LL;
+// bf16 operands (up to 8 rows): an A slot holds 128 k as 64 columns of bf16 pairs, two
+// slots a stage; x is kept as 64-k chunks [16 rows x 128 B]: rows 0-7 the bf16 values
+// x_hi = bf16(x), rows 8-15 the remainders x_lo = bf16(x - x_hi).
+constexpr int kSlotKH = 128;
+constexpr int kSlotsPerStageH = kStageK / kSlotKH;  // 2
+constexpr int kChunkXH = 64;                        // k per x chunk (128 B of bf16)
+constexpr int kXChunkBytesH = 16 * 128;
+static_assert(kSlotKH / 2 == kSlotK, "a bf16 slot takes the columns of a tf32 slot");
+static_assert(kStageK / kChunkXH * kXChunkBytesH == kChunksPerStage * 8 * 128,
+              "a stage of bf16 x takes the bytes of a stage of 8-row fp32 x");
 
 struct TsArgs {
+    const float* x;       // bf16 operands: converted by the dequantizing warps
+    int K;
     const void* scales;   // per channel: [N], read by the epilogue
     const float* bias;
     float* out;
@@ -171,11 +197,61 @@ __device__ __forceinline__ void dequant_chunk(const uint4 w4, float s, uint32_t 
     }
 }
 
-template <bool EH, bool PC, bool F16, bool XR, int BT>
+// Two fp32 values as a bf16 pair (round to nearest even), a in the low half.
+__device__ __forceinline__ uint32_t bf16x2(float a, float b) {
+    uint32_t d;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(b), "f"(a));
+    return d;
+}
+// Instruction descriptor of kind::f16 with bf16 A and B (format 1), D fp32, both K-major.
+__device__ __forceinline__ uint32_t bf16_idesc(int m, int n) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) |
+           ((uint32_t)(m >> 4) << 24);
+}
+// Orders this thread's shared-memory stores before later reads by the tensor core.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// bf16 operands: x [M x K] into 64-k chunks [16 rows x 128 B] with the 128-byte swizzle
+// (16-byte unit u of row r at unit u ^ (r % 8)): row m < 8 holds bf16(x), row m + 8 the
+// remainder bf16(x - bf16(x)); rows past M and k past K are zeros.  Thread t of nthr
+// takes units t, t + nthr, ... (8 k of one row each).
+__device__ __forceinline__ void convert_x_bf16(const TsArgs& a, uint32_t xbase, int t, int nthr) {
+    const int units = a.nst * (kStageK / kChunkXH) * 64;
+    for (int e = t; e < units; e += nthr) {
+        const int c = e >> 6, m = (e >> 3) & 7, u = e & 7;
+        const int k0 = c * kChunkXH + u * 8;
+        float v[8];
+        if (m < a.M && k0 < a.K) {
+            const float4* src = reinterpret_cast<const float4*>(a.x + (int64_t)m * a.K + k0);
+            const float4 p = src[0], q = src[1];
+            v[0] = p.x, v[1] = p.y, v[2] = p.z, v[3] = p.w, v[4] = q.x, v[5] = q.y, v[6] = q.z, v[7] = q.w;
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = 0.f;
+        }
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            hi[i] = bf16x2(v[2 * i], v[2 * i + 1]);
+            // bf16 -> fp32 is exact (the top 16 bits); the remainders are exact in fp32.
+            const float h0 = __uint_as_float(hi[i] << 16), h1 = __uint_as_float(hi[i] & 0xFFFF0000u);
+            lo[i] = bf16x2(v[2 * i] - h0, v[2 * i + 1] - h1);
+        }
+        const uint32_t row = xbase + (uint32_t)(c * kXChunkBytesH) + ((uint32_t)(u ^ m) << 4);
+        st_shared_v4(row + (uint32_t)(m * 128), hi[0], hi[1], hi[2], hi[3]);
+        st_shared_v4(row + (uint32_t)((m + 8) * 128), lo[0], lo[1], lo[2], lo[3]);
+    }
+}
+
+template <bool EH, bool PC, bool F16, bool XR, int BT, bool BF>
 __global__ void __launch_bounds__(XR ? kThreads : kThreads - 32, 1)
     tc_small_kernel(const __grid_constant__ CUtensorMap tmw, const __grid_constant__ CUtensorMap tms,
                     const __grid_constant__ CUtensorMap tmx, const TsArgs a) {
     constexpr int kAC0 = acol0(BT), kAS = aslots(BT);
+    static_assert(!BF || (!XR && BT == 16), "bf16 operands: resident x, up to 8 rows");
+    constexpr int SPS = BF ? kSlotsPerStageH : kSlotsPerStage;  // A slots per stage
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -186,13 +262,19 @@ __global__ void __launch_bounds__(XR ? kThreads : kThreads - 32, 1)
     const uint32_t bar0 = wbase + (uint32_t)(a.wst * kWStageBytes);
     auto wstage = [&](int b) { return wbase + (uint32_t)(b * kWStageBytes); };
     constexpr int kB0 = 0, kB1 = kB0 + 2 * kMaxWStages, kBx = kB1 + kMaxXGroups,
-                  kB2 = kBx + kXStages, kB3 = kB2 + 2 * kMaxASlots, kB4 = kB3 + 4;
+                  kB2 = kBx + kXStages, kB3 = kB2 + 4 * kMaxASlots, kB4 = kB3 + 4;
     auto wfull = [&](int b) { return bar0 + 8u * (kB0 + b); };
     auto wempty = [&](int b) { return bar0 + 8u * (kB0 + kMaxWStages + b); };
     auto xfull = [&](int grp) { return bar0 + 8u * (kB1 + grp); };   // group, or ring slot
     auto xempty = [&](int b) { return bar0 + 8u * (kBx + b); };       // ring slot (streamed x)
-    auto afull = [&](int p) { return bar0 + 8u * (kB2 + p); };
-    auto aempty = [&](int p) { return bar0 + 8u * (kB2 + kAS + p); };
+    // A ring position p has one barrier pair for its even laps and one for its odd laps.
+    // The slots go round the positions and the roles (issuers, teams) in turn, six
+    // positions over four roles, so a position's laps alternate between two roles: each
+    // barrier then has one role waiting on it, which takes its phases in order (a parity
+    // wait must never run two phases ahead of its barrier: it would read the phase before
+    // the current one as complete).
+    auto afull = [&](int p, int lap) { return bar0 + 8u * (kB2 + 2 * p + (lap & 1)); };
+    auto aempty = [&](int p, int lap) { return bar0 + 8u * (kB2 + 2 * kMaxASlots + 2 * p + (lap & 1)); };
     auto dfull = [&](int q) { return bar0 + 8u * (kB3 + q); };
     auto dempty = [&](int q) { return bar0 + 8u * (kB3 + 2 + q); };
     auto drain = [&](int u) { return bar0 + 8u * (kB4 + u); };
@@ -204,14 +286,16 @@ __global__ void __launch_bounds__(XR ? kThreads : kThreads - 32, 1)
     if (threadIdx.x == 0) {
         for (int b = 0; b < a.wst; ++b) {
             mbar_init(wfull(b), 1);
-            mbar_init(wempty(b), kSlotsPerStage * 4);  // the 4 dequantizing warps of each slot
+            mbar_init(wempty(b), SPS * 4);  // the 4 dequantizing warps of each slot
         }
-        for (int grp = 0; grp < (XR ? kXStages : a.nst); ++grp) mbar_init(xfull(grp), 1);
+        // bf16 operands: xfull(0) completes once the 16 dequantizing warps converted x.
+        for (int grp = 0; grp < (XR ? kXStages : a.nst); ++grp) mbar_init(xfull(grp), BF ? 16 : 1);
         for (int b = 0; b < kXStages; ++b) mbar_init(xempty(b), kSlotsPerStage);  // MMA commits
-        for (int p = 0; p < kAS; ++p) {
-            mbar_init(afull(p), 4);
-            mbar_init(aempty(p), 1);
-        }
+        for (int p = 0; p < kAS; ++p)
+            for (int e = 0; e < 2; ++e) {
+                mbar_init(afull(p, e), 4);
+                mbar_init(aempty(p, e), 1);
+            }
         for (int q = 0; q < 2; ++q) {
             mbar_init(dfull(q), kIssuers);
             mbar_init(dempty(q), 4);
@@ -231,8 +315,8 @@ __global__ void __launch_bounds__(XR ? kThreads : kThreads - 32, 1)
     // This CTA's blocks: blockIdx.x, + gridDim.x, ...; its stages and 32-k slots in order.
     const int my_blocks = ((int)a.blocks - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
     const int n_stages = my_blocks * a.nst;
-    const int n_slots = n_stages * kSlotsPerStage;
-    const int slots_per_block = a.nst * kSlotsPerStage;
+    const int n_slots = n_stages * SPS;
+    const int slots_per_block = a.nst * SPS;
     // Each CTA walks K from its own starting stage (blockIdx.x % stages, wrapping), so
     // that the CTAs' concurrent weight requests spread over the column offsets of the
     // rows instead of all asking for the same 128 bytes of every row at once.
@@ -295,7 +379,7 @@ __global__ void __launch_bounds__(XR ? kThreads : kThreads - 32, 1)
     } else if (warp <= 3 || warp == kIss3Warp) {
         if (lane == 0) {
             const int u = warp == kIss3Warp ? 3 : warp - 1;
-            if (warp == kIss3Warp && !XR) {
+            if (warp == kIss3Warp && !XR && !BF) {
                 // --------------------------------------------------- TMA loads of resident x
                 // All of x, read from L2 once per CTA (every CTA reads the same lines;
                 // re-reading them per block made those L2 lines the bottleneck), in 256-k
@@ -312,11 +396,10 @@ __global__ void __launch_bounds__(XR ? kThreads : kThreads - 32, 1)
                 }
             }
             // ------------------------------------------------------------- MMA issuers
-            const uint32_t idesc = tf32_idesc(kRows, BT);
+            const uint32_t idesc = BF ? bf16_idesc(kRows, BT) : tf32_idesc(kRows, BT);
             // Slots u, u + kIssuers, ...: the block j, the slot's place in the block, its A ring
-            // slot p and the parity of its barrier advance without divisions.
-            int j = 0, in_blk = u, p = u;
-            uint32_t pph = 0;
+            // slot p and its lap there advance without divisions.
+            int j = 0, in_blk = u, p = u, lap = 0;
             // Streamed x: the ring slot xb and phase xph of the current stage (an issuer
             // takes one slot of every stage, so they advance by one stage a slot).
             static_assert(kSlotsPerStage == kIssuers, "one slot of every stage per issuer");
@@ -325,14 +408,14 @@ __global__ void __launch_bounds__(XR ? kThreads : kThreads - 32, 1)
             for (int i = u; i < n_slots; i += kIssuers) {
                 while (in_blk >= slots_per_block) in_blk -= slots_per_block, ++j;
                 const int par = j & 1;
-                const int t = in_blk / kSlotsPerStage, sl = in_blk % kSlotsPerStage;
+                const int t = in_blk / SPS, sl = in_blk % SPS;
                 const bool first = in_blk < kIssuers;
                 const bool last = in_blk + kIssuers >= slots_per_block;
                 if ((first && j >= 2 &&
                      !wait_bounded(dempty(par), ((j >> 1) - 1) & 1, a.wait_ns, failed)) ||
-                    !wait_bounded(afull(p), pph, a.wait_ns, failed) ||
-                    (!XR && j == 0 && sl < kIssuers &&
-                     !wait_bounded(xfull(kstage(t)), 0, a.wait_ns, failed)) ||
+                    !wait_bounded(afull(p, lap), (lap >> 1) & 1, a.wait_ns, failed) ||
+                    (!XR && !BF && j == 0 && !wait_bounded(xfull(kstage(t)), 0, a.wait_ns, failed)) ||
+                    (BF && j == 0 && in_blk < kIssuers && !wait_bounded(xfull(0), 0, a.wait_ns, failed)) ||
                     (XR && !wait_bounded(xfull(xb), xph, a.wait_ns, failed))) {
                     record_failure(a.status, failed);
                     break;
@@ -345,28 +428,42 @@ __global__ void __launch_bounds__(XR ? kThreads : kThreads - 32, 1)
                 // The slot's two x chunks in the resident copy (with 8 rows a chunk, rows 8-15
                 // of the MMA's B read the next chunk: only D columns m >= 8 >= M see them); +2
                 // in the descriptor's address field per 32 bytes (K = 8 tf32) along a row.
-                const int chunk = (XR ? xb : kstage(t)) * kChunksPerStage + sl * (kSlotK / kChunk);
+                if (BF) {
+                    // bf16: the slot's two 64-k chunks of x [16 rows x 128 B]; an MMA takes
+                    // 16 k (8 columns of A, 32 bytes of a row of x).
+                    const int chunk = kstage(t) * (kStageK / kChunkXH) + sl * (kSlotKH / kChunkXH);
 #pragma unroll
-                for (int h = 0; h < kSlotK / kChunk; ++h) {
-                    const uint64_t bd =
-                        sw128_desc(xbase + (uint32_t)((chunk + h) * a.xrows * 128));
+                    for (int h = 0; h < kSlotKH / kChunkXH; ++h) {
+                        const uint64_t bd = sw128_desc(xbase + (uint32_t)((chunk + h) * kXChunkBytesH));
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        mma_tf32_ts(d, acol + kChunk * h + 8 * kk, bd + (uint64_t)(2 * kk), idesc,
-                                    (first && h == 0 && kk == 0) ? 0u : 1u);
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_f16_ts(d, acol + 32 * h + 8 * kk, bd + (uint64_t)(2 * kk), idesc,
+                                       (first && h == 0 && kk == 0) ? 0u : 1u);
+                    }
+                } else {
+                    const int chunk = (XR ? xb : kstage(t)) * kChunksPerStage + sl * (kSlotK / kChunk);
+#pragma unroll
+                    for (int h = 0; h < kSlotK / kChunk; ++h) {
+                        const uint64_t bd =
+                            sw128_desc(xbase + (uint32_t)((chunk + h) * a.xrows * 128));
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_tf32_ts(d, acol + kChunk * h + 8 * kk, bd + (uint64_t)(2 * kk), idesc,
+                                        (first && h == 0 && kk == 0) ? 0u : 1u);
+                    }
                 }
-                mma_commit(aempty(p));
+                mma_commit(aempty(p, lap));
                 if (XR) mma_commit(xempty(xb));
                 if (last) mma_commit(dfull(par));
                 in_blk += kIssuers;
-                if ((p += kIssuers) >= kAS) p -= kAS, pph ^= 1u;
+                if ((p += kIssuers) >= kAS) p -= kAS, ++lap;
                 if (++xb == kXStages) xb = 0, xph ^= 1u;
             }
             // Every MMA this thread issued completes before the CTA frees tensor memory (and
             // the copies of resident x have landed).
             mma_commit(drain(u));
             wait_bounded(drain(u), 0, kDrainNs, nullptr);
-            if (warp == kIss3Warp && !XR)
+            if (warp == kIss3Warp && !XR && !BF)
                 for (int grp = 0; grp < a.nst; ++grp) wait_bounded(xfull(grp), 0, kDrainNs, nullptr);
         }
     } else if (warp < kDeqWarp0) {
@@ -401,9 +498,16 @@ __global__ void __launch_bounds__(XR ? kThreads : kThreads - 32, 1)
             if (n < a.N && !*failed) {
                 const float cs = PC ? ld_scale(a.scales, F16, n) : 1.f;
                 const float bv = a.bias ? __ldg(a.bias + n) : 0.f;
+                if (BF) {
+                    // Columns m and m + 8: the products with x_hi and with x_lo.
 #pragma unroll
-                for (int m = 0; m < BT; ++m)
-                    if (m < a.M) a.out[(int64_t)m * a.N + n] = fmaf(acc[m], cs, bv);
+                    for (int m = 0; m < 8; ++m)
+                        if (m < a.M) a.out[(int64_t)m * a.N + n] = fmaf(acc[m] + acc[m + 8], cs, bv);
+                } else {
+#pragma unroll
+                    for (int m = 0; m < BT; ++m)
+                        if (m < a.M) a.out[(int64_t)m * a.N + n] = fmaf(acc[m], cs, bv);
+                }
             }
         }
     } else {
@@ -413,17 +517,28 @@ __global__ void __launch_bounds__(XR ? kThreads : kThreads - 32, 1)
         const int r = q * 32 + lane;  // this thread's weight row in the block
         const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
         // Slots team, team + kTeams, ...: stage (ring slot b, parity wph), slot sl in it, A
-        // ring slot p (parity pph), advanced without divisions.
-        int sl = team, b = 0, p = team;
-        uint32_t wph = 0, pph = 0;
+        // ring slot p (and its lap there), advanced without divisions.
+        if (BF) {
+            // x into its bf16 layout once per CTA (it comes from the preceding kernel), then
+            // the tensor core may read it.
+            griddep_wait();
+            convert_x_bf16(a, xbase, (warp - kDeqWarp0) * 32 + lane, 4 * kTeams * 32);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(xfull(0));
+        }
+        int sl = team, b = 0, p = team, lap = 0;
+        uint32_t wph = 0;
         for (int i = team; i < n_slots; i += kTeams) {
-            while (sl >= kSlotsPerStage) {
-                sl -= kSlotsPerStage;
+            while (sl >= SPS) {
+                sl -= SPS;
                 if (++b == a.wst) b = 0, wph ^= 1u;
             }
             // Waits are decided for the whole warp (its tcgen05 instructions are collective).
+            // Lap L of the slot is written once the MMAs of lap L - 1 have completed.
             if (!__all_sync(0xffffffffu,
-                            (i < kAS || wait_backoff(aempty(p), pph ^ 1u, a.wait_ns, failed, 32)) &&
+                            (lap == 0 || wait_backoff(aempty(p, lap - 1), ((lap - 1) >> 1) & 1,
+                                                      a.wait_ns, failed, 32)) &&
                                 wait_backoff(wfull(b), wph, a.wait_ns, failed, 32))) {
                 if (lane == 0) record_failure(a.status, failed);
                 break;
@@ -433,7 +548,7 @@ __global__ void __launch_bounds__(XR ? kThreads : kThreads - 32, 1)
             tc_fence_after();
             // The slot's chunks c of the block row; chunk c sits at chunk c ^ (r % 8)
             // (128-byte swizzle).  Their group scales are in the stage's scale block.
-            constexpr int kCps = kSlotK / kChunk;
+            constexpr int kCps = (BF ? kSlotKH : kSlotK) / kChunk;
             uint4 w[kCps];
             float sc[kCps];
 #pragma unroll
@@ -450,18 +565,35 @@ __global__ void __launch_bounds__(XR ? kThreads : kThreads - 32, 1)
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(wempty(b));  // the warp's reads of the stage are done
+            if (BF) {
+                // Two chunks (64 k) per store of 32 columns of bf16 pairs.
 #pragma unroll
-            for (int h = 0; h < kCps; ++h) {
-                uint32_t v[32];
-                dequant_chunk<EH>(w[h], sc[h], v);
-                tmem_st32_async(lane_base + (uint32_t)(kAC0 + p * kSlotK + kChunk * h), v);
+                for (int h2 = 0; h2 < kCps / 2; ++h2) {
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        uint32_t v[32];
+                        dequant_chunk<EH>(w[2 * h2 + hh], sc[2 * h2 + hh], v);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            pk[16 * hh + i] = bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+                    }
+                    tmem_st32_async(lane_base + (uint32_t)(kAC0 + p * kSlotK + 32 * h2), pk);
+                }
+            } else {
+#pragma unroll
+                for (int h = 0; h < kCps; ++h) {
+                    uint32_t v[32];
+                    dequant_chunk<EH>(w[h], sc[h], v);
+                    tmem_st32_async(lane_base + (uint32_t)(kAC0 + p * kSlotK + kChunk * h), v);
+                }
             }
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(afull(p));
+            if (lane == 0) mbar_arrive(afull(p, lap));
             sl += kTeams;
-            if ((p += kTeams) >= kAS) p -= kAS, pph ^= 1u;
+            if ((p += kTeams) >= kAS) p -= kAS, ++lap;
         }
     }
 
@@ -471,10 +603,10 @@ __global__ void __launch_bounds__(XR ? kThreads : kThreads - 32, 1)
     if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
-template <bool EH, bool PC, bool F16, bool XR, int BT>
+template <bool EH, bool PC, bool F16, bool XR, int BT, bool BF>
 cudaError_t launch_ts(const CUtensorMap& tw, const CUtensorMap& ts, const CUtensorMap& tx,
                       const TsArgs& a, unsigned grid, int smem, const LaunchCtx& c) {
-    constexpr auto kernel = tc_small_kernel<EH, PC, F16, XR, BT>;
+    constexpr auto kernel = tc_small_kernel<EH, PC, F16, XR, BT, BF>;
     const cudaError_t attr = kernel_smem_once<kernel>(kSmemCap);
     if (attr != cudaSuccess) return attr;
     cudaLaunchConfig_t cfg = {};
@@ -492,21 +624,21 @@ cudaError_t launch_ts(const CUtensorMap& tw, const CUtensorMap& ts, const CUtens
     return cudaLaunchKernelEx(&cfg, kernel, tw, ts, tx, a);
 }
 
-template <bool XR, int BT>
+template <bool XR, int BT, bool BF = false>
 cudaError_t launch_eh(const Problem& p, const CUtensorMap& tw, const CUtensorMap& ts,
                       const CUtensorMap& tx, const TsArgs& a, unsigned grid, int smem,
                       const LaunchCtx& c) {
     const bool pc = p.group_size >= p.K, eh = p.even_high != 0, f16 = p.scale_f16 != 0;
     if (pc) {
-        if (eh) return f16 ? launch_ts<true, true, true, XR, BT>(tw, ts, tx, a, grid, smem, c)
-                           : launch_ts<true, true, false, XR, BT>(tw, ts, tx, a, grid, smem, c);
-        return f16 ? launch_ts<false, true, true, XR, BT>(tw, ts, tx, a, grid, smem, c)
-                   : launch_ts<false, true, false, XR, BT>(tw, ts, tx, a, grid, smem, c);
+        if (eh) return f16 ? launch_ts<true, true, true, XR, BT, BF>(tw, ts, tx, a, grid, smem, c)
+                           : launch_ts<true, true, false, XR, BT, BF>(tw, ts, tx, a, grid, smem, c);
+        return f16 ? launch_ts<false, true, true, XR, BT, BF>(tw, ts, tx, a, grid, smem, c)
+                   : launch_ts<false, true, false, XR, BT, BF>(tw, ts, tx, a, grid, smem, c);
     }
-    if (eh) return f16 ? launch_ts<true, false, true, XR, BT>(tw, ts, tx, a, grid, smem, c)
-                       : launch_ts<true, false, false, XR, BT>(tw, ts, tx, a, grid, smem, c);
-    return f16 ? launch_ts<false, false, true, XR, BT>(tw, ts, tx, a, grid, smem, c)
-               : launch_ts<false, false, false, XR, BT>(tw, ts, tx, a, grid, smem, c);
+    if (eh) return f16 ? launch_ts<true, false, true, XR, BT, BF>(tw, ts, tx, a, grid, smem, c)
+                       : launch_ts<true, false, false, XR, BT, BF>(tw, ts, tx, a, grid, smem, c);
+    return f16 ? launch_ts<false, false, true, XR, BT, BF>(tw, ts, tx, a, grid, smem, c)
+               : launch_ts<false, false, false, XR, BT, BF>(tw, ts, tx, a, grid, smem, c);
 }
 
 int log2_pow2(int64_t v) {
@@ -553,12 +685,32 @@ bool tc_small_eligible(const Problem& p, const LaunchCtx& c) {
     return tensor_map_encoder() != nullptr;
 }
 
+// bf16 operands (x split into two bf16 terms) where they apply: up to 8 rows, x resident,
+// at least two 256-k stages (every issuer then has a slot in every block) and an even
+// weight ring of at least four stages.  With two A slots a stage, even stages go to teams
+// 0-1 and odd ones to teams 2-3; an even ring keeps each ring stage with one pair of teams,
+// so that a team waits for every lap of the stages it reads (a parity wait must not run a
+// lap ahead of the barrier).  By default from 100 row blocks of 128, where they were
+// measured 2-5 % faster than tf32 (128256 x 2048 at 4 rows: 55.3 against 58.0 us; 14336 x
+// 4096: 18.7 against 19.4), not on fewer (8192 x 2048: 10.1 against 9.2).
+bool tc_small_uses_bf16(const Problem& p, const LaunchCtx& c) {
+    if (c.tc_small_operands == 1 || p.M > 8 || p.K <= kStageK || !tc_small_eligible(p, c))
+        return false;
+    uint32_t xb;
+    int xr, ring, smem;
+    const int wst = ts_layout(p, c.max_smem_optin, &xb, &xr, &ring, &smem);
+    if (ring || (wst & ~1) < 4) return false;
+    return c.tc_small_operands == 2 || (p.N + kRows - 1) / kRows >= 100;
+}
+
 cudaError_t tc_small_launch(const Problem& p, const LaunchCtx& c) {
     EncodeTiledFn enc = tensor_map_encoder();
     if (!enc || !tc_small_eligible(p, c)) return cudaErrorNotSupported;
     const bool pc = p.group_size >= p.K;
     const int esz = p.scale_f16 ? 2 : 4;
     TsArgs a = {};
+    a.x = p.x;
+    a.K = (int)p.K;
     a.scales = p.scales;
     a.bias = p.bias;
     a.out = p.out;
@@ -613,6 +765,10 @@ cudaError_t tc_small_launch(const Problem& p, const LaunchCtx& c) {
             return cudaErrorInvalidValue;
     }
     const unsigned grid = (unsigned)std::min<int64_t>(a.blocks, c.sm_count);
+    if (tc_small_uses_bf16(p, c)) {
+        a.wst &= ~1;
+        return launch_eh<false, 16, true>(p, tw, ts, tx, a, grid, smem, c);
+    }
     if (p.M > 16)
         return a.x_ring ? launch_eh<true, 32>(p, tw, ts, tx, a, grid, smem, c)
                         : launch_eh<false, 32>(p, tw, ts, tx, a, grid, smem, c);

@@ -435,20 +435,31 @@ __global__ void __launch_bounds__(kBtThreads, 2)
         // tile [MT][256] in its own shared memory (warp 0's slots of `red`: column c was
         // read above by this thread only), and after the cluster barrier CTA rank r adds
         // columns [r * 256 / cluster, (r + 1) * 256 / cluster) of the MT rows over the
-        // ranks in rank order (the result does not depend on timing) and stores them.  No
-        // CTA leaves before the second barrier, so its partial stays readable.
+        // ranks in rank order (the result does not depend on timing) and stores them.
+        // Thread c fetches column r * per + c % per of rank c / per for every row, all MT
+        // remote loads in flight at once, into a local [MT][cluster][per] array (the other
+        // warps' slots of `red`, free after the barrier); the rank-ordered sums then read
+        // that.  No CTA leaves before the second barrier, so its partial stays readable.
 #pragma unroll
         for (int m = 0; m < MT; ++m) red[m * kBtKT + c] = part[m];
         cluster_sync_all();
         const uint32_t rank = cluster_ctarank();
-        const int per = kBtKT / a.cluster;
-        const uint32_t red_addr = base;  // `red` sits at the start of the aligned buffer
+        const int cs = a.cluster, per = kBtKT / cs;
+        const int q = c / per, j = c % per, col = (int)rank * per + j;
+        const uint32_t src = mapa_shared(base + (uint32_t)col * 4u, (uint32_t)q);
+        float got[MT];
+#pragma unroll
+        for (int m = 0; m < MT; ++m) got[m] = ld_dsmem_f32(src + (uint32_t)(m * kBtKT) * 4u);
+        float* stage = red + MT * kBtKT;  // [MT][cs][per]
+#pragma unroll
+        for (int m = 0; m < MT; ++m) stage[m * kBtKT + c] = got[m];
+        asm volatile("bar.sync 1, %0;" ::"r"(kBtCWarps * 32) : "memory");
         for (int e = c; e < MT * per; e += kBtCWarps * 32) {
-            const int m = e / per, col = (int)rank * per + e % per;
-            const uint32_t off = red_addr + (uint32_t)(m * kBtKT + col) * 4u;
+            const int m = e / per, jj = e % per, cc = (int)rank * per + jj;
+            const float* sp = stage + m * kBtKT + jj;
             float v = 0.f;
-            for (int q = 0; q < a.cluster; ++q) v += ld_dsmem_f32(mapa_shared(off, (uint32_t)q));
-            const int64_t kk = (int64_t)kt * kBtKT + col;
+            for (int r = 0; r < cs; ++r) v += sp[r * per];
+            const int64_t kk = (int64_t)kt * kBtKT + cc;
             if (store && m < mt && kk < a.K) a.d_x[(m0 + m) * a.K + kk] = v;
         }
         cluster_sync_all();

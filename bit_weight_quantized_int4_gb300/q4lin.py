@@ -49,8 +49,9 @@ Q4LIN_KERNEL_TC = 5
 Q4LIN_KERNEL_TC_F16 = 6
 Q4LIN_KERNEL_GEMV_TMA_FIXED = 7
 Q4LIN_KERNEL_TC_SMALL = 8
+Q4LIN_KERNEL_TC_SMALL_BF16 = 9
 KERNEL_NAMES = {0: "none", 1: "gemv_tma", 2: "multirow", 3: "rowstream", 4: "generic",
-                5: "tc", 6: "tc_f16", 7: "gemv_tma_fixed", 8: "tc_small"}
+                5: "tc", 6: "tc_f16", 7: "gemv_tma_fixed", 8: "tc_small", 9: "tc_small_bf16"}
 
 Q4LIN_OPT_FORCE_PATH = 1
 Q4LIN_OPT_NIBBLE_EVEN_HIGH = 2
@@ -58,6 +59,7 @@ Q4LIN_OPT_WAIT_LIMIT = 3
 Q4LIN_OPT_PDL = 4
 Q4LIN_OPT_TC_SKIP_FIRST_COPY = 5
 Q4LIN_OPT_TC_F16 = 6
+Q4LIN_OPT_TC_SMALL_OPERANDS = 7
 
 _vp, _i64, _i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
 

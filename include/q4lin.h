@@ -113,7 +113,16 @@ typedef enum {
      * the call record code 2 in the status word; its output is then undefined.  x is
      * first converted into the handle's scratch (M * K * 2 bytes); a problem whose copy
      * does not fit there runs in tf32. */
-    Q4LIN_OPT_TC_F16 = 6
+    Q4LIN_OPT_TC_F16 = 6,
+    /* Operands of the small-M tensor-core GEMM (Q4LIN_PATH_TC_SMALL).  Up to 8 rows, with
+     * x resident in shared memory, K > 256 and room for an even weight ring of >= 4 stages,
+     * it can multiply bf16 operands: the dequantized weights rounded to bf16, and x as the
+     * two bf16 terms bf16(x) and bf16(x - bf16(x)), taken by the same MMA as extra columns;
+     * each product then carries a relative error below 2^-9 + 2^-16, inside the tensor-core
+     * path's 4e-3 * sum|x*w| bar, and bf16 keeps fp32's exponent range.  0 (default): bf16
+     * where it applies and the matrix has >= 100 blocks of 128 rows (measured faster there),
+     * else tf32; 1: tf32 always; 2: bf16 wherever it applies. */
+    Q4LIN_OPT_TC_SMALL_OPERANDS = 7
 } q4lin_option_t;
 
 /* Create a handle for CUDA device `device`.  Queries the SM count and shared-memory
@@ -271,7 +280,9 @@ typedef enum {
     Q4LIN_KERNEL_GEMV_TMA_FIXED = 7, /* the decode GEMV with exact fixed-point arithmetic: x as
                                       * 32-bit fixed point per 32-k chunk, codes times x by
                                       * dp4a; chosen when its CTAs take >= 2 row blocks each */
-    Q4LIN_KERNEL_TC_SMALL = 8   /* tcgen05 GEMM for 2 <= M <= 32 (Q4LIN_PATH_TC_SMALL), tf32 */
+    Q4LIN_KERNEL_TC_SMALL = 8,  /* tcgen05 GEMM for 2 <= M <= 32 (Q4LIN_PATH_TC_SMALL), tf32 */
+    Q4LIN_KERNEL_TC_SMALL_BF16 = 9 /* the same with bf16 operands (up to 8 rows, see
+                                    * Q4LIN_OPT_TC_SMALL_OPERANDS) */
 } q4lin_kernel_t;
 
 /* The kernel q4lin_run would launch for these arguments (no launch, no device access);

@@ -8,7 +8,10 @@ mostly past K), the longest K whose x stays resident and longer ones whose x str
 group sizes from 32 to wider than a stage,
 per-channel scales (fp16 and fp32), fp32 and fp16 group scales, bias or none, the
 even-high nibble order, persistent CTAs over many blocks (more blocks than SMs), repeated
-calls bit-identical, and a bounded wait that runs out cleanly.
+calls bit-identical, and a bounded wait that runs out cleanly.  Up to 8 rows (x resident,
+K > 256) the kernel can multiply bf16 operands (x as bf16(x) + bf16(x - bf16(x))): by
+default from 100 row blocks, forced here with Q4LIN_OPT_TC_SMALL_OPERANDS = 2 on smaller
+matrices; tf32 is forced with 1.
 """
 import numpy as np
 import pytest
@@ -41,9 +44,70 @@ def check(handle, case, even_high=False):
     return out
 
 
+@pytest.fixture
+def bf16(handle):
+    """The handle with bf16 operands wherever they apply, for one test."""
+    from bit_weight_quantized_int4_gb300 import q4lin as q
+    q.q4lin_set_option(handle, q.Q4LIN_OPT_TC_SMALL_OPERANDS, 2)
+    yield handle
+    q.q4lin_set_option(handle, q.Q4LIN_OPT_TC_SMALL_OPERANDS, 0)
+
+
+def kernel_of(handle, case):
+    """The kernel name q4lin_plan_kernel reports for the case on the forced small-M path."""
+    import torch
+    from bit_weight_quantized_int4_gb300 import q4lin as q
+    M, N, K = case.M, case.N, case.K
+    x = torch.zeros(M, K, device="cuda")
+    w = torch.zeros(N, K // 2, dtype=torch.uint8, device="cuda")
+    s = torch.from_numpy(case.scales).cuda()
+    out = torch.empty(M, N, device="cuda")
+    q.q4lin_set_option(handle, q.Q4LIN_OPT_FORCE_PATH, TC_SMALL)
+    try:
+        st, k = q.q4lin_plan_kernel(handle, x.data_ptr(), w.data_ptr(), s.data_ptr(), None,
+                                    out.data_ptr(), M, N, K, case.group_size,
+                                    q.Q4LIN_SCALE_F16 if case.scale_f16 else q.Q4LIN_SCALE_F32)
+    finally:
+        q.q4lin_set_option(handle, q.Q4LIN_OPT_FORCE_PATH, 0)
+    assert st == q.Q4LIN_OK
+    return q.KERNEL_NAMES[k]
+
+
 @pytest.mark.parametrize("M", list(range(2, 33)))
 def test_every_m(handle, M):
-    check(handle, synth.make_case(M, 1000, 2048, 32, scale_f16=True, bias=True, seed=M))
+    c = synth.make_case(M, 1000, 2048, 32, scale_f16=True, bias=True, seed=M)
+    assert kernel_of(handle, c) == "tc_small"  # 8 row blocks: tf32 by default
+    check(handle, c)
+
+
+@pytest.mark.parametrize("M", list(range(2, 9)))
+def test_every_m_bf16_operands(bf16, M):
+    c = synth.make_case(M, 1000, 2048, 32, scale_f16=True, bias=True, seed=M)
+    assert kernel_of(bf16, c) == "tc_small_bf16"
+    check(bf16, c)
+
+
+@pytest.mark.parametrize("M,N,K,gs,f16,kern", [
+    (4, 1000, 256, 32, True, "tc_small"),         # one 256-k stage: tf32
+    (4, 1000, 512, 32, True, "tc_small_bf16"),    # two stages
+    (8, 384, 5120, 32, True, "tc_small"),         # resident, but an even ring < 4 stages
+    (8, 384, 4096, 32, False, "tc_small_bf16"),   # four stages of the ring, fp32 scales
+    (5, 520, 2048, 2048, False, "tc_small_bf16"),  # per channel, fp32
+    (4, 2600, 8192, 32, True, "tc_small"),        # x streamed
+    (9, 1000, 2048, 32, True, "tc_small"),        # more than 8 rows
+])
+def test_where_bf16_operands_apply(bf16, M, N, K, gs, f16, kern):
+    c = synth.make_case(M, N, K, gs, scale_f16=f16, bias=True, seed=M + N + K)
+    assert kernel_of(bf16, c) == kern
+    check(bf16, c)
+
+
+@pytest.mark.parametrize("M,N,kern", [(4, 12800, "tc_small_bf16"), (4, 12672, "tc_small"),
+                                      (8, 12800, "tc_small_bf16"), (9, 12800, "tc_small")])
+def test_default_operands_from_100_blocks(handle, M, N, kern):
+    c = synth.make_case(M, N, 512, 32, scale_f16=True, bias=True, seed=M + N)
+    assert kernel_of(handle, c) == kern
+    check(handle, c)
 
 
 @pytest.mark.parametrize("N,K,gs,f16,bias", [
@@ -88,11 +152,19 @@ def test_streamed_x_dyadic_bit_exact(handle):
     np.testing.assert_array_equal(out.astype(np.float64), ref)
 
 
-@pytest.mark.parametrize("M", [3, 16, 32])
-def test_persistent_over_many_blocks(handle, M):
+@pytest.mark.parametrize("M,mode", [(3, 0), (3, 1), (16, 0), (32, 0)])
+def test_persistent_over_many_blocks(handle, M, mode):
     """More 128-row blocks than SMs (the vocabulary-sized head): each CTA takes several
-    blocks with the accumulators double-buffered between them."""
-    check(handle, synth.make_case(M, 128256, 2048, 32, scale_f16=True, bias=True, seed=M))
+    blocks with the accumulators double-buffered between them (bf16 operands by default
+    at 3 rows, tf32 forced as well)."""
+    from bit_weight_quantized_int4_gb300 import q4lin as q
+    c = synth.make_case(M, 128256, 2048, 32, scale_f16=True, bias=True, seed=M)
+    q.q4lin_set_option(handle, q.Q4LIN_OPT_TC_SMALL_OPERANDS, mode)
+    try:
+        assert kernel_of(handle, c) == ("tc_small_bf16" if M <= 8 and mode == 0 else "tc_small")
+        check(handle, c)
+    finally:
+        q.q4lin_set_option(handle, q.Q4LIN_OPT_TC_SMALL_OPERANDS, 0)
 
 
 def test_even_high(handle):
@@ -100,10 +172,17 @@ def test_even_high(handle):
           even_high=True)
 
 
-@pytest.mark.parametrize("M,f16", [(2, True), (9, False), (16, True), (24, False), (32, True)])
-def test_dyadic_bit_exact(handle, M, f16):
+@pytest.mark.parametrize("M,f16,mode", [(2, True, 2), (5, False, 2), (8, True, 2), (3, True, 0),
+                                        (9, False, 0), (16, True, 0), (24, False, 0), (32, True, 0)])
+def test_dyadic_bit_exact(handle, M, f16, mode):
+    from bit_weight_quantized_int4_gb300 import q4lin as q
     c = synth.make_dyadic_case(M, 264, 1024, 32, scale_f16=f16, bias=True, seed=M)
-    out, used = run_q4lin(handle, c, TC_SMALL)
+    q.q4lin_set_option(handle, q.Q4LIN_OPT_TC_SMALL_OPERANDS, mode)
+    try:
+        assert kernel_of(handle, c) == ("tc_small_bf16" if mode == 2 else "tc_small")
+        out, used = run_q4lin(handle, c, TC_SMALL)
+    finally:
+        q.q4lin_set_option(handle, q.Q4LIN_OPT_TC_SMALL_OPERANDS, 0)
     assert used == TC_SMALL
     ref, _ = oracle.linear(c.x, c.qweight, c.scales, c.bias, c.K, c.group_size)
     np.testing.assert_array_equal(out.astype(np.float64), ref)
@@ -144,14 +223,20 @@ def test_ineligible_shapes_are_refused(handle):
         q.q4lin_set_option(handle, q.Q4LIN_OPT_FORCE_PATH, 0)
 
 
-def test_bounded_wait_times_out_cleanly(handle):
-    """The producer skips its first copy (test hook), so the barrier every role waits on
-    first is never completed: the 1 ms bounded waits run out, the kernel records code 1,
-    drains its MMAs, frees its tensor memory and returns; the next call is correct."""
+@pytest.mark.parametrize("mode", [1, 2])
+def test_bounded_wait_times_out_cleanly(handle, mode):
+    """The producer skips its first copy (test hook), so the barrier the first slots wait on
+    is never completed: the 1 ms bounded waits run out, the kernel records code 1, drains
+    its MMAs, frees its tensor memory and returns; the next call is correct.  With bf16
+    operands (mode 2) a stage holds two A slots, so the teams and issuers of the second
+    stage get through their first slot before everything stops: no role may then run on
+    into ring laps whose previous lap never happened."""
     from bit_weight_quantized_int4_gb300 import q4lin as q
     c = synth.make_case(4, 1024, 2048, 32, scale_f16=True, bias=False, seed=77)
     st, code = q.q4lin_check_device_status(handle, None)
     assert (st, code) == (q.Q4LIN_OK, 0)
+    q.q4lin_set_option(handle, q.Q4LIN_OPT_TC_SMALL_OPERANDS, mode)
+    assert kernel_of(handle, c) == ("tc_small_bf16" if mode == 2 else "tc_small")
     q.q4lin_set_option(handle, q.Q4LIN_OPT_WAIT_LIMIT, 1_000_000)
     q.q4lin_set_option(handle, q.Q4LIN_OPT_TC_SKIP_FIRST_COPY, 1)
     try:
@@ -165,7 +250,10 @@ def test_bounded_wait_times_out_cleanly(handle):
     assert st == q.Q4LIN_ERR_TIMEOUT and code == 1
     st, code = q.q4lin_check_device_status(handle, None)
     assert (st, code) == (q.Q4LIN_OK, 0)
-    check(handle, c)
+    try:
+        check(handle, c)
+    finally:
+        q.q4lin_set_option(handle, q.Q4LIN_OPT_TC_SMALL_OPERANDS, 0)
 
 
 @pytest.mark.parametrize("pdl", [0, 1])
@@ -223,8 +311,8 @@ def _auto_kernel(handle, M, N, K, f16=True):
 
 @pytest.mark.parametrize("M,N,K,kernel", [
     (2, 128256, 2048, "multirow"),   # two rows: the multi-row GEMV is faster
-    (3, 128256, 2048, "tc_small"),
-    (4, 28672, 4096, "tc_small"),
+    (3, 128256, 2048, "tc_small_bf16"),  # bf16 operands from 100 row blocks
+    (4, 28672, 4096, "tc_small_bf16"),
     (3, 22016, 4096, "multirow"),    # a last wave of 20 blocks on 152 SMs
     (4, 8192, 2048, "multirow"),     # 64 blocks at 3-4 rows
     (8, 8192, 2048, "tc_small"),     # 64 blocks of 8 stages
