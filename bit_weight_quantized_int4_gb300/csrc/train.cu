@@ -22,8 +22,9 @@
 //   backward_tma_kernel (the fast path when the tensors suit TMA): the same CTA tile of
 //     256 k, fed by a producer warp that streams per stage the weight tile [64 rows x
 //     128 B], the group scales of those rows [groups of the tile x 64] and d_out
-//     [MT x 64] into a shared-memory ring with one TMA copy each; 8 consumer warps take
-//     every 8th row of a stage (lane = 32-bit word of codes, 8 k).  The weight and scale
+//     [MT x 64] into a shared-memory ring with one TMA copy each; 8 consumer warps (16 for
+//     1-2 rows of d_out on rows of >= 8192 k) take every 8th (16th) row of a stage (lane =
+//     32-bit word of codes, 8 k).  The weight and scale
 //     copies of the first ring of stages go out before the grid-dependency wait, their
 //     d_out copies after it.  The rows are split over CTAs (multiples of 64 rows each);
 //     when each CTA has at most 4 stages, the splits of a k tile are one thread-block
@@ -222,8 +223,10 @@ __global__ void backward_dx_generic_kernel(const BwArgs a) {
 }
 
 // ------------------------------------------------------- TMA-fed input gradient
-constexpr int kBtCWarps = 8;                       // consumer warps
-constexpr int kBtThreads = 32 * kBtCWarps + 32;    // + the producer warp
+// Consumer warps CW: 8, or 16 for tiles of 1-2 rows of d_out on long rows (K >= 8192),
+// where each CTA's loop is long enough for the extra warps to hide its latency (2048 x 8192
+// at M = 1: 8.7 -> 7.1 us); on shorter rows the larger reduction and barriers cost more
+// than they hide (8192 x 2048: 9.1 -> 9.5 us).  One producer warp besides.
 constexpr int kBtKT = 256;                         // k per CTA tile: 128 bytes of a row
 constexpr int kBtRB = 64;                          // weight rows per stage
 constexpr int kBtMaxStages = 8;
@@ -260,15 +263,16 @@ struct BtArgs {
 };
 
 // grid: x = k tile, y = split of the rows, z = tile of MT rows of d_out.
-template <int MT>
-__global__ void __launch_bounds__(kBtThreads, 2)
+template <int MT, int CW>
+__global__ void __launch_bounds__(32 * CW + 32, 2)
     backward_tma_kernel(const __grid_constant__ BtMaps maps, const BtArgs a) {
+    constexpr int kBtCWarps = CW;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* gbase = smem_raw + (base - raw);
     const int S = a.stages;
-    // The partial-tile reduction reuses the ring: max(ring, [8 warps][MT][256] floats).
+    // The partial-tile reduction reuses the ring: max(ring, [warps][MT][256] floats).
     const uint32_t ring = (uint32_t)S * a.stage_bytes;
     const uint32_t red_bytes = (uint32_t)kBtCWarps * MT * kBtKT * 4;
     const uint32_t bar_base = base + (ring > red_bytes ? ring : red_bytes);
@@ -406,10 +410,10 @@ __global__ void __launch_bounds__(kBtThreads, 2)
         if (lane == 0) mbar_arrive(empty(s));
         if (++s == S) s = 0, ph ^= 1u;
     }
-    // The CTA's partial tile: the 8 warps added in warp order through shared memory (the
-    // ring is free once every consumer warp has passed its last stage).
+    // The CTA's partial tile: the consumer warps added in warp order through shared memory
+    // (the ring is free once every consumer warp has passed its last stage).
     asm volatile("bar.sync 1, %0;" ::"r"(kBtCWarps * 32) : "memory");
-    float* red = reinterpret_cast<float*>(gbase);  // [8][MT][256]
+    float* red = reinterpret_cast<float*>(gbase);  // [warps][MT][256]
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
         float4* dst = reinterpret_cast<float4*>(red + (warp * MT + m) * kBtKT + lane * 8);
@@ -418,14 +422,18 @@ __global__ void __launch_bounds__(kBtThreads, 2)
     }
     asm volatile("bar.sync 1, %0;" ::"r"(kBtCWarps * 32) : "memory");
     const int mt = a.M - m0 < MT ? (int)(a.M - m0) : MT;
-    const int c = threadIdx.x;  // consumer thread = column of the tile
+    // Consumer thread c < 256 = column c of the tile (with 16 consumer warps the others
+    // only take part in the barriers).
+    const int c = threadIdx.x;
+    const bool col = kBtCWarps * 32 <= kBtKT || c < kBtKT;  // always, with 8 warps
+    const int cc0 = col ? c : 0;
     const int64_t k = (int64_t)kt * kBtKT + c;
     float part[MT];
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
         float v = 0.f;
 #pragma unroll
-        for (int w = 0; w < kBtCWarps; ++w) v += red[(w * MT + m) * kBtKT + c];
+        for (int w = 0; w < kBtCWarps; ++w) v += red[(w * MT + m) * kBtKT + cc0];
         part[m] = v;
     }
     griddep_wait();  // (long complete: the d_out copies waited for it) before any store
@@ -440,19 +448,22 @@ __global__ void __launch_bounds__(kBtThreads, 2)
         // remote loads in flight at once, into a local [MT][cluster][per] array (the other
         // warps' slots of `red`, free after the barrier); the rank-ordered sums then read
         // that.  No CTA leaves before the second barrier, so its partial stays readable.
+        if (col)
 #pragma unroll
-        for (int m = 0; m < MT; ++m) red[m * kBtKT + c] = part[m];
+            for (int m = 0; m < MT; ++m) red[m * kBtKT + c] = part[m];
         cluster_sync_all();
         const uint32_t rank = cluster_ctarank();
         const int cs = a.cluster, per = kBtKT / cs;
-        const int q = c / per, j = c % per, col = (int)rank * per + j;
-        const uint32_t src = mapa_shared(base + (uint32_t)col * 4u, (uint32_t)q);
-        float got[MT];
-#pragma unroll
-        for (int m = 0; m < MT; ++m) got[m] = ld_dsmem_f32(src + (uint32_t)(m * kBtKT) * 4u);
         float* stage = red + MT * kBtKT;  // [MT][cs][per]
+        if (col) {
+            const int q = c / per, j = c % per, cl = (int)rank * per + j;
+            const uint32_t src = mapa_shared(base + (uint32_t)cl * 4u, (uint32_t)q);
+            float got[MT];
 #pragma unroll
-        for (int m = 0; m < MT; ++m) stage[m * kBtKT + c] = got[m];
+            for (int m = 0; m < MT; ++m) got[m] = ld_dsmem_f32(src + (uint32_t)(m * kBtKT) * 4u);
+#pragma unroll
+            for (int m = 0; m < MT; ++m) stage[m * kBtKT + c] = got[m];
+        }
         asm volatile("bar.sync 1, %0;" ::"r"(kBtCWarps * 32) : "memory");
         for (int e = c; e < MT * per; e += kBtCWarps * 32) {
             const int m = e / per, jj = e % per, cc = (int)rank * per + jj;
@@ -466,7 +477,7 @@ __global__ void __launch_bounds__(kBtThreads, 2)
         return;
     }
     if (a.splits == 1) {
-        if (store && k < a.K)
+        if (store && col && k < a.K)
             for (int m = 0; m < mt; ++m) a.d_x[(m0 + m) * a.K + k] = part[m];
         return;
     }
@@ -474,8 +485,9 @@ __global__ void __launch_bounds__(kBtThreads, 2)
     // them in split order.
     const int64_t item = (int64_t)blockIdx.z * gridDim.x + blockIdx.x;
     float* wsi = a.ws + item * (int64_t)a.splits * MT * kBtKT;
+    if (col)
 #pragma unroll
-    for (int m = 0; m < MT; ++m) wsi[((int64_t)blockIdx.y * MT + m) * kBtKT + c] = part[m];
+        for (int m = 0; m < MT; ++m) wsi[((int64_t)blockIdx.y * MT + m) * kBtKT + c] = part[m];
     // Partials before the ticket: the barrier and one device-scope fence of the thread that
     // takes it; the last CTA's reads after it: that thread's second fence and barrier.
     asm volatile("bar.sync 1, %0;" ::"r"(kBtCWarps * 32) : "memory");
@@ -485,7 +497,7 @@ __global__ void __launch_bounds__(kBtThreads, 2)
         __threadfence();
     }
     asm volatile("bar.sync 1, %0;" ::"r"(kBtCWarps * 32) : "memory");
-    if (!*s_last) return;
+    if (!*s_last || !col) return;
     // The MT rows of the column together, the loads of PB parts of all of them in flight
     // at a time (MT * PB <= 32); every row still added in split order.
     constexpr int PB = MT >= 8 ? 4 : 32 / MT > 8 ? 8 : 32 / MT;
@@ -654,14 +666,14 @@ cudaError_t launch(Kern k, const Args& a, dim3 grid, unsigned block, const Launc
 
 constexpr int kBtSmemLimit = 113 * 1024;  // two CTAs per SM
 
-template <int MT>
+template <int MT, int CW>
 cudaError_t launch_bt(const BtMaps& maps, const BtArgs& a, dim3 grid, int smem,
                       const LaunchCtx& c) {
-    const cudaError_t attr = kernel_smem_once<backward_tma_kernel<MT>>(kBtSmemLimit);
+    const cudaError_t attr = kernel_smem_once<backward_tma_kernel<MT, CW>>(kBtSmemLimit);
     if (attr != cudaSuccess) return attr;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
-    cfg.blockDim = dim3(kBtThreads);
+    cfg.blockDim = dim3(32 * CW + 32);
     cfg.dynamicSmemBytes = (size_t)smem;
     cfg.stream = c.stream;
     cudaLaunchAttribute attrs[2];
@@ -680,13 +692,13 @@ cudaError_t launch_bt(const BtMaps& maps, const BtArgs& a, dim3 grid, int smem,
     }
     cfg.attrs = na ? attrs : nullptr;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, backward_tma_kernel<MT>, maps, a);
+    return cudaLaunchKernelEx(&cfg, backward_tma_kernel<MT, CW>, maps, a);
 }
 
 // Whether clusters of `cs` CTAs (along y) of the MT instance with `smem` bytes can be
 // resident on this device (cs > 8 needs the non-portable cluster size).  Cached per
 // device, instance, cluster size and shared-memory size.
-template <int MT>
+template <int MT, int CW>
 bool bt_cluster_ok(int cs, int smem) {
     static std::mutex mu;
     static std::map<std::tuple<int, int, int>, bool> cache;
@@ -696,15 +708,15 @@ bool bt_cluster_ok(int cs, int smem) {
     std::lock_guard<std::mutex> lock(mu);
     auto it = cache.find(key);
     if (it != cache.end()) return it->second;
-    bool ok = kernel_smem_once<backward_tma_kernel<MT>>(kBtSmemLimit) == cudaSuccess;
+    bool ok = kernel_smem_once<backward_tma_kernel<MT, CW>>(kBtSmemLimit) == cudaSuccess;
     if (ok && cs > 8)
-        ok = cudaFuncSetAttribute(backward_tma_kernel<MT>,
+        ok = cudaFuncSetAttribute(backward_tma_kernel<MT, CW>,
                                   cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
     int n = 0;
     if (ok) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(1, (unsigned)cs, 1);
-        cfg.blockDim = dim3(kBtThreads);
+        cfg.blockDim = dim3(32 * CW + 32);
         cfg.dynamicSmemBytes = (size_t)smem;
         cudaLaunchAttribute at;
         at.id = cudaLaunchAttributeClusterDimension;
@@ -713,7 +725,7 @@ bool bt_cluster_ok(int cs, int smem) {
         at.val.clusterDim.z = 1;
         cfg.attrs = &at;
         cfg.numAttrs = 1;
-        ok = cudaOccupancyMaxActiveClusters(&n, backward_tma_kernel<MT>, &cfg) == cudaSuccess && n > 0;
+        ok = cudaOccupancyMaxActiveClusters(&n, backward_tma_kernel<MT, CW>, &cfg) == cudaSuccess && n > 0;
     }
     if (!ok) cudaGetLastError();
     cache[key] = ok;
@@ -735,6 +747,8 @@ bool bt_eligible(const TrainProblem& p) {
 cudaError_t backward_tma_launch(const TrainProblem& p, const LaunchCtx& c) {
     EncodeTiledFn enc = tensor_map_encoder();
     const int MT = p.M <= 1 ? 1 : p.M <= 2 ? 2 : p.M <= 4 ? 4 : kMT;
+    const bool wide = MT <= 2 && p.K >= 8192;  // 16 consumer warps (see backward_tma_kernel)
+    const int CW = wide ? 16 : 8;
     const int64_t k_tiles = (p.K + kBtKT - 1) / kBtKT;
     const int64_t m_tiles = (p.M + MT - 1) / MT;
     const int64_t tiles = k_tiles * m_tiles;
@@ -792,16 +806,16 @@ cudaError_t backward_tma_launch(const TrainProblem& p, const LaunchCtx& c) {
         while (cs * 2 <= 16 && cs * 2 <= std::max<int64_t>(1, 2LL * c.sm_count / tiles)) cs *= 2;
         const int64_t rows_c = ((p.N + cs - 1) / cs + kBtRB - 1) / kBtRB * kBtRB;
         const int st_c = (int)std::min<int64_t>(kBtMaxStages, rows_c / kBtRB);
-        const int ring_c = st_c * (int)a.stage_bytes, red_c = kBtCWarps * MT * kBtKT * 4;
+        const int ring_c = st_c * (int)a.stage_bytes, red_c = CW * MT * kBtKT * 4;
         const int smem_c = 1024 + (ring_c > red_c ? ring_c : red_c) + 256;
         bool ok = false;
         if (cs >= 2 && (MT <= 2 ? rows_c <= 16 * kBtRB : rows_c <= 4 * kBtRB) &&
             smem_c <= kBtSmemLimit) {
             switch (MT) {
-                case 1: ok = bt_cluster_ok<1>(cs, smem_c); break;
-                case 2: ok = bt_cluster_ok<2>(cs, smem_c); break;
-                case 4: ok = bt_cluster_ok<4>(cs, smem_c); break;
-                default: ok = bt_cluster_ok<kMT>(cs, smem_c); break;
+                case 1: ok = wide ? bt_cluster_ok<1, 16>(cs, smem_c) : bt_cluster_ok<1, 8>(cs, smem_c); break;
+                case 2: ok = wide ? bt_cluster_ok<2, 16>(cs, smem_c) : bt_cluster_ok<2, 8>(cs, smem_c); break;
+                case 4: ok = bt_cluster_ok<4, 8>(cs, smem_c); break;
+                default: ok = bt_cluster_ok<kMT, 8>(cs, smem_c); break;
             }
         }
         if (ok) {
@@ -815,7 +829,7 @@ cudaError_t backward_tma_launch(const TrainProblem& p, const LaunchCtx& c) {
     a.stages = (int)std::min<int64_t>(kBtMaxStages, rows / kBtRB);
     a.sc_rows = p.scale_f16 ? kBtScRows16 : kBtScRows32;
     a.tx = (uint32_t)(kBtRB * kBtKT / 2) + (uint32_t)gt * a.sc_rows * esz + (uint32_t)MT * kBtRB * 4;
-    const int red = kBtCWarps * MT * kBtKT * 4;
+    const int red = CW * MT * kBtKT * 4;
     const int ring = a.stages * (int)a.stage_bytes;
     const int smem = 1024 + (ring > red ? ring : red) + 256;
     if (smem > kBtSmemLimit) return cudaErrorInvalidValue;
@@ -853,10 +867,10 @@ cudaError_t backward_tma_launch(const TrainProblem& p, const LaunchCtx& c) {
     }
     const dim3 grid((unsigned)k_tiles, (unsigned)splits, (unsigned)m_tiles);
     switch (MT) {
-        case 1: return launch_bt<1>(maps, a, grid, smem, c);
-        case 2: return launch_bt<2>(maps, a, grid, smem, c);
-        case 4: return launch_bt<4>(maps, a, grid, smem, c);
-        default: return launch_bt<kMT>(maps, a, grid, smem, c);
+        case 1: return wide ? launch_bt<1, 16>(maps, a, grid, smem, c) : launch_bt<1, 8>(maps, a, grid, smem, c);
+        case 2: return wide ? launch_bt<2, 16>(maps, a, grid, smem, c) : launch_bt<2, 8>(maps, a, grid, smem, c);
+        case 4: return launch_bt<4, 8>(maps, a, grid, smem, c);
+        default: return launch_bt<kMT, 8>(maps, a, grid, smem, c);
     }
 }
 

@@ -97,6 +97,9 @@ BACKWARD_TMA_SHAPES = [
     (1, 8192, 2048, 64, False),    # deep row split, fp32 scales
     (8, 2048, 8192, 32, True),     # the benchmark's M = 8 shape
     (1, 8192, 2048, 32, True),     # the benchmark's M = 1 shape
+    (1, 2048, 8192, 32, True),     # 16 consumer warps (1-2 rows of d_out, K >= 8192), cluster
+    (2, 600, 9216, 64, False),     # 16 consumer warps, MT = 2, ragged N
+    (1, 4096, 14336, 32, True),    # 16 consumer warps, rows split through the workspace
 ]
 
 
