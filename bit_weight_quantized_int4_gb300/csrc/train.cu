@@ -24,7 +24,9 @@
 //     128 B], the group scales of those rows [groups of the tile x 64] and d_out
 //     [MT x 64] into a shared-memory ring with one TMA copy each; 8 consumer warps (16 for
 //     1-2 rows of d_out on rows of >= 8192 k) take every 8th (16th) row of a stage (lane =
-//     32-bit word of codes, 8 k).  The weight and scale
+//     32-bit word of codes, 8 k).  For 1-2 rows of d_out on 2048-k rows of 4096-16384
+//     rows the tile is 128 k (two rows per warp pass), which puts twice the CTAs on the
+//     SMs.  The weight and scale
 //     copies of the first ring of stages go out before the grid-dependency wait, their
 //     d_out copies after it.  The rows are split over CTAs (multiples of 64 rows each);
 //     when each CTA has at most 4 stages, the splits of a k tile are one thread-block
@@ -228,15 +230,16 @@ __global__ void backward_dx_generic_kernel(const BwArgs a) {
 // at M = 1: 8.7 -> 7.1 us); on shorter rows the larger reduction and barriers cost more
 // than they hide (8192 x 2048: 9.1 -> 9.5 us).  One producer warp besides.
 constexpr int kBtKT = 256;                         // k per CTA tile: 128 bytes of a row
+constexpr int kBtKTNarrow = 128;                   // or 64 bytes (more CTAs on short K)
 constexpr int kBtRB = 64;                          // weight rows per stage
 constexpr int kBtMaxStages = 8;
 constexpr int64_t kDrainNs = 4000000000LL;
-constexpr uint32_t kBtScOff = kBtRB * kBtKT / 2;   // 8 KiB of codes, then the scales
+__host__ __device__ constexpr uint32_t bt_sc_off(int kt) { return kBtRB * kt / 2; }  // codes, then scales
 // Scales are copied for 72 rows (fp16: 144-byte box rows) or 68 rows (fp32: 272 bytes): the
 // lanes of a warp read up to 8 groups of one row, and the padded row stride puts them in
 // different banks (a box row must be a multiple of 16 bytes).
 constexpr int kBtScRows16 = kBtRB + 8, kBtScRows32 = kBtRB + 4;
-constexpr uint32_t kBtDoOff = kBtScOff + 2304;  // then d_out [MT x 64]
+__host__ __device__ constexpr uint32_t bt_do_off(int kt) { return bt_sc_off(kt) + 2304; }  // then d_out [MT x 64]
 
 struct BtMaps {
     CUtensorMap w;   // uint8 [N, Kp], box {128, 64}
@@ -263,10 +266,13 @@ struct BtArgs {
 };
 
 // grid: x = k tile, y = split of the rows, z = tile of MT rows of d_out.
-template <int MT, int CW>
+template <int MT, int CW, int KT>
 __global__ void __launch_bounds__(32 * CW + 32, 2)
     backward_tma_kernel(const __grid_constant__ BtMaps maps, const BtArgs a) {
     constexpr int kBtCWarps = CW;
+    constexpr uint32_t kScOff = bt_sc_off(KT), kDoOff = bt_do_off(KT);
+    // Lanes per weight row (one 32-bit word of codes, 8 k, each) and rows per warp pass.
+    constexpr int LPR = KT / 8, RPI = 32 / LPR;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -274,7 +280,7 @@ __global__ void __launch_bounds__(32 * CW + 32, 2)
     const int S = a.stages;
     // The partial-tile reduction reuses the ring: max(ring, [warps][MT][256] floats).
     const uint32_t ring = (uint32_t)S * a.stage_bytes;
-    const uint32_t red_bytes = (uint32_t)kBtCWarps * MT * kBtKT * 4;
+    const uint32_t red_bytes = (uint32_t)kBtCWarps * MT * KT * 4;
     const uint32_t bar_base = base + (ring > red_bytes ? ring : red_bytes);
     volatile int* failed = reinterpret_cast<volatile int*>(gbase + (bar_base + 16 * kBtMaxStages - base));
     volatile int* s_last = failed + 1;
@@ -317,8 +323,8 @@ __global__ void __launch_bounds__(32 * CW + 32, 2)
                 const int n = (int)(n_begin + (int64_t)li * kBtRB);
                 const uint32_t sb = base + (uint32_t)li * a.stage_bytes;
                 mbar_expect_tx(full(li), a.tx - d_bytes);
-                tma_load_2d(sb, &maps.w, kt * (kBtKT / 2), n, full(li));
-                tma_load_2d(sb + kBtScOff, &maps.s, n, g_row, full(li));
+                tma_load_2d(sb, &maps.w, kt * (KT / 2), n, full(li));
+                tma_load_2d(sb + kScOff, &maps.s, n, g_row, full(li));
             }
             griddep_wait();  // d_out comes from the preceding grid
             int li = 0, s = 0;
@@ -335,10 +341,10 @@ __global__ void __launch_bounds__(32 * CW + 32, 2)
                     mbar_arrive_expect_tx(full(s), d_bytes);
                 } else {
                     mbar_arrive_expect_tx(full(s), a.tx);
-                    tma_load_2d(sb, &maps.w, kt * (kBtKT / 2), n, full(s));
-                    tma_load_2d(sb + kBtScOff, &maps.s, n, g_row, full(s));
+                    tma_load_2d(sb, &maps.w, kt * (KT / 2), n, full(s));
+                    tma_load_2d(sb + kScOff, &maps.s, n, g_row, full(s));
                 }
-                tma_load_2d(sb + kBtDoOff, &maps.d, n, (int)m0, full(s));
+                tma_load_2d(sb + kDoOff, &maps.d, n, (int)m0, full(s));
                 if (++s == S) s = 0, ph ^= 1u;
             }
             // After a failure: the stages armed before the wait but not yet arrived on get
@@ -360,9 +366,11 @@ __global__ void __launch_bounds__(32 * CW + 32, 2)
     }
 
     // ------------------------------------------------------------------ consumers
-    // Lane = 32-bit word of codes (k = 256 kt + 8 lane + j), warp = rows warp, warp + 8, ...
-    // of every stage; gl = the lane's group inside the tile.
-    const int gl = a.gs_in_tile ? (lane * 8) / a.gs_in_tile : 0;
+    // Lane = 32-bit word wl of codes (k = KT kt + 8 wl + j) of row hr of a pass: a warp
+    // takes rows RPI (warp + CW i) + hr of every stage (one row per pass with 256-k tiles,
+    // two with 128-k tiles); gl = the lane's group inside the tile.
+    const int wl = lane % LPR, hr = lane / LPR;
+    const int gl = a.gs_in_tile ? (wl * 8) / a.gs_in_tile : 0;
     // acc[m][b] = (k = 2b, k = 2b + 1) of the lane's 8 k: packed fp32x2 FMAs.
     float2 acc[MT][4];
 #pragma unroll
@@ -383,14 +391,14 @@ __global__ void __launch_bounds__(32 * CW + 32, 2)
         }
         if (got) {
             const uint8_t* stage = gbase + (uint32_t)s * a.stage_bytes;
-            const uint32_t* wrow = reinterpret_cast<const uint32_t*>(stage) + lane;
-            const __half* sc16 = reinterpret_cast<const __half*>(stage + kBtScOff) + gl * a.sc_rows;
-            const float* sc32 = reinterpret_cast<const float*>(stage + kBtScOff) + gl * a.sc_rows;
-            const float* dop = reinterpret_cast<const float*>(stage + kBtDoOff);
+            const uint32_t* wrow = reinterpret_cast<const uint32_t*>(stage) + wl;
+            const __half* sc16 = reinterpret_cast<const __half*>(stage + kScOff) + gl * a.sc_rows;
+            const float* sc32 = reinterpret_cast<const float*>(stage + kScOff) + gl * a.sc_rows;
+            const float* dop = reinterpret_cast<const float*>(stage + kDoOff);
 #pragma unroll 4
-            for (int rr = 0; rr < kBtRB / kBtCWarps; ++rr) {
-                const int r = warp + rr * kBtCWarps;
-                const uint32_t word = wrow[r * (kBtKT / 8)];
+            for (int rr = 0; rr < kBtRB / (kBtCWarps * RPI); ++rr) {
+                const int r = (warp + rr * kBtCWarps) * RPI + hr;
+                const uint32_t word = wrow[r * (KT / 8)];
                 const float sc = a.scale_f16 ? __half2float(sc16[r]) : sc32[r];
                 float2 cv[4];  // (c - 8) of k = 2b, 2b + 1, exact
                 if (a.even_high)
@@ -412,28 +420,39 @@ __global__ void __launch_bounds__(32 * CW + 32, 2)
     }
     // The CTA's partial tile: the consumer warps added in warp order through shared memory
     // (the ring is free once every consumer warp has passed its last stage).
-    asm volatile("bar.sync 1, %0;" ::"r"(kBtCWarps * 32) : "memory");
-    float* red = reinterpret_cast<float*>(gbase);  // [warps][MT][256]
+    if (RPI == 2) {
+        // The warp's two rows of a pass are the same columns: half-warp hr = 1 adds onto 0.
 #pragma unroll
-    for (int m = 0; m < MT; ++m) {
-        float4* dst = reinterpret_cast<float4*>(red + (warp * MT + m) * kBtKT + lane * 8);
-        dst[0] = make_float4(acc[m][0].x, acc[m][0].y, acc[m][1].x, acc[m][1].y);
-        dst[1] = make_float4(acc[m][2].x, acc[m][2].y, acc[m][3].x, acc[m][3].y);
+        for (int m = 0; m < MT; ++m)
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+                acc[m][b].x += __shfl_down_sync(0xffffffffu, acc[m][b].x, LPR);
+                acc[m][b].y += __shfl_down_sync(0xffffffffu, acc[m][b].y, LPR);
+            }
     }
     asm volatile("bar.sync 1, %0;" ::"r"(kBtCWarps * 32) : "memory");
+    float* red = reinterpret_cast<float*>(gbase);  // [warps][MT][KT]
+    if (hr == 0)
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            float4* dst = reinterpret_cast<float4*>(red + (warp * MT + m) * KT + wl * 8);
+            dst[0] = make_float4(acc[m][0].x, acc[m][0].y, acc[m][1].x, acc[m][1].y);
+            dst[1] = make_float4(acc[m][2].x, acc[m][2].y, acc[m][3].x, acc[m][3].y);
+        }
+    asm volatile("bar.sync 1, %0;" ::"r"(kBtCWarps * 32) : "memory");
     const int mt = a.M - m0 < MT ? (int)(a.M - m0) : MT;
-    // Consumer thread c < 256 = column c of the tile (with 16 consumer warps the others
-    // only take part in the barriers).
+    // Consumer thread c < KT = column c of the tile (the others only take part in the
+    // barriers).
     const int c = threadIdx.x;
-    const bool col = kBtCWarps * 32 <= kBtKT || c < kBtKT;  // always, with 8 warps
+    const bool col = kBtCWarps * 32 <= KT || c < KT;  // always, with 8 warps and 256-k tiles
     const int cc0 = col ? c : 0;
-    const int64_t k = (int64_t)kt * kBtKT + c;
+    const int64_t k = (int64_t)kt * KT + c;
     float part[MT];
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
         float v = 0.f;
 #pragma unroll
-        for (int w = 0; w < kBtCWarps; ++w) v += red[(w * MT + m) * kBtKT + cc0];
+        for (int w = 0; w < kBtCWarps; ++w) v += red[(w * MT + m) * KT + cc0];
         part[m] = v;
     }
     griddep_wait();  // (long complete: the d_out copies waited for it) before any store
@@ -450,27 +469,27 @@ __global__ void __launch_bounds__(32 * CW + 32, 2)
         // that.  No CTA leaves before the second barrier, so its partial stays readable.
         if (col)
 #pragma unroll
-            for (int m = 0; m < MT; ++m) red[m * kBtKT + c] = part[m];
+            for (int m = 0; m < MT; ++m) red[m * KT + c] = part[m];
         cluster_sync_all();
         const uint32_t rank = cluster_ctarank();
-        const int cs = a.cluster, per = kBtKT / cs;
-        float* stage = red + MT * kBtKT;  // [MT][cs][per]
+        const int cs = a.cluster, per = KT / cs;
+        float* stage = red + MT * KT;  // [MT][cs][per]
         if (col) {
             const int q = c / per, j = c % per, cl = (int)rank * per + j;
             const uint32_t src = mapa_shared(base + (uint32_t)cl * 4u, (uint32_t)q);
             float got[MT];
 #pragma unroll
-            for (int m = 0; m < MT; ++m) got[m] = ld_dsmem_f32(src + (uint32_t)(m * kBtKT) * 4u);
+            for (int m = 0; m < MT; ++m) got[m] = ld_dsmem_f32(src + (uint32_t)(m * KT) * 4u);
 #pragma unroll
-            for (int m = 0; m < MT; ++m) stage[m * kBtKT + c] = got[m];
+            for (int m = 0; m < MT; ++m) stage[m * KT + c] = got[m];
         }
         asm volatile("bar.sync 1, %0;" ::"r"(kBtCWarps * 32) : "memory");
         for (int e = c; e < MT * per; e += kBtCWarps * 32) {
             const int m = e / per, jj = e % per, cc = (int)rank * per + jj;
-            const float* sp = stage + m * kBtKT + jj;
+            const float* sp = stage + m * KT + jj;
             float v = 0.f;
             for (int r = 0; r < cs; ++r) v += sp[r * per];
-            const int64_t kk = (int64_t)kt * kBtKT + cc;
+            const int64_t kk = (int64_t)kt * KT + cc;
             if (store && m < mt && kk < a.K) a.d_x[(m0 + m) * a.K + kk] = v;
         }
         cluster_sync_all();
@@ -484,10 +503,10 @@ __global__ void __launch_bounds__(32 * CW + 32, 2)
     // Split rows: partials to the workspace; the last CTA of this (m tile, k tile) adds
     // them in split order.
     const int64_t item = (int64_t)blockIdx.z * gridDim.x + blockIdx.x;
-    float* wsi = a.ws + item * (int64_t)a.splits * MT * kBtKT;
+    float* wsi = a.ws + item * (int64_t)a.splits * MT * KT;
     if (col)
 #pragma unroll
-        for (int m = 0; m < MT; ++m) wsi[((int64_t)blockIdx.y * MT + m) * kBtKT + c] = part[m];
+        for (int m = 0; m < MT; ++m) wsi[((int64_t)blockIdx.y * MT + m) * KT + c] = part[m];
     // Partials before the ticket: the barrier and one device-scope fence of the thread that
     // takes it; the last CTA's reads after it: that thread's second fence and barrier.
     asm volatile("bar.sync 1, %0;" ::"r"(kBtCWarps * 32) : "memory");
@@ -502,7 +521,7 @@ __global__ void __launch_bounds__(32 * CW + 32, 2)
     // at a time (MT * PB <= 32); every row still added in split order.
     constexpr int PB = MT >= 8 ? 4 : 32 / MT > 8 ? 8 : 32 / MT;
     const float* src = wsi + c;
-    const int64_t stride = (int64_t)MT * kBtKT;
+    const int64_t stride = (int64_t)MT * KT;
     float v[MT];
 #pragma unroll
     for (int m = 0; m < MT; ++m) v[m] = 0.f;
@@ -512,7 +531,7 @@ __global__ void __launch_bounds__(32 * CW + 32, 2)
         for (int u = 0; u < PB; ++u)
 #pragma unroll
             for (int m = 0; m < MT; ++m)
-                t[u][m] = sp + u < a.splits ? __ldcg(src + (int64_t)(sp + u) * stride + m * kBtKT)
+                t[u][m] = sp + u < a.splits ? __ldcg(src + (int64_t)(sp + u) * stride + m * KT)
                                             : 0.f;
 #pragma unroll
         for (int u = 0; u < PB; ++u)
@@ -666,10 +685,10 @@ cudaError_t launch(Kern k, const Args& a, dim3 grid, unsigned block, const Launc
 
 constexpr int kBtSmemLimit = 113 * 1024;  // two CTAs per SM
 
-template <int MT, int CW>
+template <int MT, int CW, int KT>
 cudaError_t launch_bt(const BtMaps& maps, const BtArgs& a, dim3 grid, int smem,
                       const LaunchCtx& c) {
-    const cudaError_t attr = kernel_smem_once<backward_tma_kernel<MT, CW>>(kBtSmemLimit);
+    const cudaError_t attr = kernel_smem_once<backward_tma_kernel<MT, CW, KT>>(kBtSmemLimit);
     if (attr != cudaSuccess) return attr;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
@@ -692,13 +711,13 @@ cudaError_t launch_bt(const BtMaps& maps, const BtArgs& a, dim3 grid, int smem,
     }
     cfg.attrs = na ? attrs : nullptr;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, backward_tma_kernel<MT, CW>, maps, a);
+    return cudaLaunchKernelEx(&cfg, backward_tma_kernel<MT, CW, KT>, maps, a);
 }
 
 // Whether clusters of `cs` CTAs (along y) of the MT instance with `smem` bytes can be
 // resident on this device (cs > 8 needs the non-portable cluster size).  Cached per
 // device, instance, cluster size and shared-memory size.
-template <int MT, int CW>
+template <int MT, int CW, int KT>
 bool bt_cluster_ok(int cs, int smem) {
     static std::mutex mu;
     static std::map<std::tuple<int, int, int>, bool> cache;
@@ -708,9 +727,9 @@ bool bt_cluster_ok(int cs, int smem) {
     std::lock_guard<std::mutex> lock(mu);
     auto it = cache.find(key);
     if (it != cache.end()) return it->second;
-    bool ok = kernel_smem_once<backward_tma_kernel<MT, CW>>(kBtSmemLimit) == cudaSuccess;
+    bool ok = kernel_smem_once<backward_tma_kernel<MT, CW, KT>>(kBtSmemLimit) == cudaSuccess;
     if (ok && cs > 8)
-        ok = cudaFuncSetAttribute(backward_tma_kernel<MT, CW>,
+        ok = cudaFuncSetAttribute(backward_tma_kernel<MT, CW, KT>,
                                   cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
     int n = 0;
     if (ok) {
@@ -725,7 +744,7 @@ bool bt_cluster_ok(int cs, int smem) {
         at.val.clusterDim.z = 1;
         cfg.attrs = &at;
         cfg.numAttrs = 1;
-        ok = cudaOccupancyMaxActiveClusters(&n, backward_tma_kernel<MT, CW>, &cfg) == cudaSuccess && n > 0;
+        ok = cudaOccupancyMaxActiveClusters(&n, backward_tma_kernel<MT, CW, KT>, &cfg) == cudaSuccess && n > 0;
     }
     if (!ok) cudaGetLastError();
     cache[key] = ok;
@@ -733,7 +752,7 @@ bool bt_cluster_ok(int cs, int smem) {
 }
 
 // TMA needs 16-byte aligned bases and row strides (K % 32, N % 8) and a k tile of 256
-// that holds whole groups or lies inside one.
+// that holds whole groups or lies inside one (then so does a tile of 128).
 bool bt_eligible(const TrainProblem& p) {
     auto al16 = [](const void* q) { return reinterpret_cast<uintptr_t>(q) % 16 == 0; };
     if (p.K % 32 != 0 || p.N % 8 != 0) return false;
@@ -749,12 +768,21 @@ cudaError_t backward_tma_launch(const TrainProblem& p, const LaunchCtx& c) {
     const int MT = p.M <= 1 ? 1 : p.M <= 2 ? 2 : p.M <= 4 ? 4 : kMT;
     const bool wide = MT <= 2 && p.K >= 8192;  // 16 consumer warps (see backward_tma_kernel)
     const int CW = wide ? 16 : 8;
-    const int64_t k_tiles = (p.K + kBtKT - 1) / kBtKT;
+    // 128-k tiles (two rows per warp pass) where 256-k tiles in clusters of 16 would leave
+    // SMs idle: 1-2 rows of d_out, fewer than sm_count / 16 tiles of 256 k, and 4-16 stages
+    // of 64 rows per CTA of a 16-CTA cluster (8192 x 2048 at M = 1: 128 CTAs -> 256, 9.2 ->
+    // 8.7 us).  With fewer rows the extra CTAs only add latency (2048 x 2048: 3.6 -> 4.5 us),
+    // with more the clusters do not apply and the workspace hand-off grows (128256 x 2048:
+    // 46.4 -> 51.2 us).
+    const bool narrow = MT <= 2 && !wide && (p.K + kBtKT - 1) / kBtKT * 16 < c.sm_count &&
+                        p.N >= 16 * 4 * kBtRB && p.N <= 16 * 16 * kBtRB;
+    const int KTW = narrow ? kBtKTNarrow : kBtKT;
+    const int64_t k_tiles = (p.K + KTW - 1) / KTW;
     const int64_t m_tiles = (p.M + MT - 1) / MT;
     const int64_t tiles = k_tiles * m_tiles;
     const bool one_group = p.group_size >= p.K;
     const int64_t G = one_group ? 1 : (p.K + p.group_size - 1) / p.group_size;
-    const int gt = one_group || p.group_size >= kBtKT ? 1 : (int)(kBtKT / p.group_size);
+    const int gt = one_group || p.group_size >= KTW ? 1 : (int)(KTW / p.group_size);
     const uint32_t esz = p.scale_f16 ? 2 : 4;
 
     BtArgs a;
@@ -773,11 +801,11 @@ cudaError_t backward_tma_launch(const TrainProblem& p, const LaunchCtx& c) {
     a.tiles_per_group = 1;
     if (one_group) {
         a.tiles_per_group = (int)k_tiles;
-    } else if (p.group_size <= kBtKT) {
+    } else if (p.group_size <= KTW) {
         a.gs_in_tile = (int)p.group_size;
-        while ((kBtKT >> a.gs_shift256) > p.group_size) ++a.gs_shift256;
+        while ((KTW >> a.gs_shift256) > p.group_size) ++a.gs_shift256;
     } else {
-        a.tiles_per_group = (int)(p.group_size / kBtKT);
+        a.tiles_per_group = (int)(p.group_size / KTW);
     }
     a.scale_f16 = p.scale_f16;
     a.even_high = p.even_high;
@@ -786,12 +814,12 @@ cudaError_t backward_tma_launch(const TrainProblem& p, const LaunchCtx& c) {
     // within the workspace and ticket capacity.
     int64_t splits = std::max<int64_t>(1, 2LL * c.sm_count / tiles);
     if (!c.ws || !c.tickets || tiles > c.ticket_count) splits = 1;
-    while (splits > 1 && tiles * splits * MT * kBtKT > c.ws_floats) --splits;
+    while (splits > 1 && tiles * splits * MT * KTW > c.ws_floats) --splits;
     int64_t rows = (p.N + splits - 1) / splits;
     rows = (rows + kBtRB - 1) / kBtRB * kBtRB;
     splits = (p.N + rows - 1) / rows;
     if (splits > 65535 || m_tiles > 65535 || k_tiles > 0x7fffffff) return cudaErrorInvalidValue;
-    a.stage_bytes = (uint32_t)((kBtDoOff + MT * kBtRB * 4 + 1023) / 1024 * 1024);
+    a.stage_bytes = (uint32_t)((bt_do_off(KTW) + MT * kBtRB * 4 + 1023) / 1024 * 1024);
     // When the split above leaves each CTA at most 4 stages of rows, the hand-off through
     // the workspace (partials to L2, two device-scope fences and the ticket atomic, then
     // the last CTA's reads: ~3 us) dominates the launch; then one cluster of up to 16 CTAs
@@ -801,21 +829,27 @@ cudaError_t backward_tma_launch(const TrainProblem& p, const LaunchCtx& c) {
     // 8 rows of d_out over 8 stages, the cluster's fewer CTAs lose more than the hand-off
     // costs, so those keep the workspace.
     a.cluster = 1;
-    if (rows <= 4 * kBtRB) {
+    if (rows <= 4 * kBtRB || narrow) {
         int cs = 1;
         while (cs * 2 <= 16 && cs * 2 <= std::max<int64_t>(1, 2LL * c.sm_count / tiles)) cs *= 2;
         const int64_t rows_c = ((p.N + cs - 1) / cs + kBtRB - 1) / kBtRB * kBtRB;
         const int st_c = (int)std::min<int64_t>(kBtMaxStages, rows_c / kBtRB);
-        const int ring_c = st_c * (int)a.stage_bytes, red_c = CW * MT * kBtKT * 4;
+        const int ring_c = st_c * (int)a.stage_bytes, red_c = CW * MT * KTW * 4;
         const int smem_c = 1024 + (ring_c > red_c ? ring_c : red_c) + 256;
         bool ok = false;
         if (cs >= 2 && (MT <= 2 ? rows_c <= 16 * kBtRB : rows_c <= 4 * kBtRB) &&
             smem_c <= kBtSmemLimit) {
             switch (MT) {
-                case 1: ok = wide ? bt_cluster_ok<1, 16>(cs, smem_c) : bt_cluster_ok<1, 8>(cs, smem_c); break;
-                case 2: ok = wide ? bt_cluster_ok<2, 16>(cs, smem_c) : bt_cluster_ok<2, 8>(cs, smem_c); break;
-                case 4: ok = bt_cluster_ok<4, 8>(cs, smem_c); break;
-                default: ok = bt_cluster_ok<kMT, 8>(cs, smem_c); break;
+                case 1: ok = wide     ? bt_cluster_ok<1, 16, kBtKT>(cs, smem_c)
+                             : narrow ? bt_cluster_ok<1, 8, kBtKTNarrow>(cs, smem_c)
+                                      : bt_cluster_ok<1, 8, kBtKT>(cs, smem_c);
+                        break;
+                case 2: ok = wide     ? bt_cluster_ok<2, 16, kBtKT>(cs, smem_c)
+                             : narrow ? bt_cluster_ok<2, 8, kBtKTNarrow>(cs, smem_c)
+                                      : bt_cluster_ok<2, 8, kBtKT>(cs, smem_c);
+                        break;
+                case 4: ok = bt_cluster_ok<4, 8, kBtKT>(cs, smem_c); break;
+                default: ok = bt_cluster_ok<kMT, 8, kBtKT>(cs, smem_c); break;
             }
         }
         if (ok) {
@@ -828,8 +862,8 @@ cudaError_t backward_tma_launch(const TrainProblem& p, const LaunchCtx& c) {
     a.rows_per_split = rows;
     a.stages = (int)std::min<int64_t>(kBtMaxStages, rows / kBtRB);
     a.sc_rows = p.scale_f16 ? kBtScRows16 : kBtScRows32;
-    a.tx = (uint32_t)(kBtRB * kBtKT / 2) + (uint32_t)gt * a.sc_rows * esz + (uint32_t)MT * kBtRB * 4;
-    const int red = CW * MT * kBtKT * 4;
+    a.tx = (uint32_t)(kBtRB * KTW / 2) + (uint32_t)gt * a.sc_rows * esz + (uint32_t)MT * kBtRB * 4;
+    const int red = CW * MT * KTW * 4;
     const int ring = a.stages * (int)a.stage_bytes;
     const int smem = 1024 + (ring > red ? ring : red) + 256;
     if (smem > kBtSmemLimit) return cudaErrorInvalidValue;
@@ -840,7 +874,7 @@ cudaError_t backward_tma_launch(const TrainProblem& p, const LaunchCtx& c) {
         const int64_t Kp = p.K / 2;
         const cuuint64_t dims[2] = {(cuuint64_t)Kp, (cuuint64_t)p.N};
         const cuuint64_t strides[1] = {(cuuint64_t)Kp};
-        const cuuint32_t box[2] = {(cuuint32_t)(kBtKT / 2), (cuuint32_t)kBtRB};
+        const cuuint32_t box[2] = {(cuuint32_t)(KTW / 2), (cuuint32_t)kBtRB};
         if (enc(&maps.w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(p.qweight), dims,
                 strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
@@ -867,10 +901,14 @@ cudaError_t backward_tma_launch(const TrainProblem& p, const LaunchCtx& c) {
     }
     const dim3 grid((unsigned)k_tiles, (unsigned)splits, (unsigned)m_tiles);
     switch (MT) {
-        case 1: return wide ? launch_bt<1, 16>(maps, a, grid, smem, c) : launch_bt<1, 8>(maps, a, grid, smem, c);
-        case 2: return wide ? launch_bt<2, 16>(maps, a, grid, smem, c) : launch_bt<2, 8>(maps, a, grid, smem, c);
-        case 4: return launch_bt<4, 8>(maps, a, grid, smem, c);
-        default: return launch_bt<kMT, 8>(maps, a, grid, smem, c);
+        case 1: return wide     ? launch_bt<1, 16, kBtKT>(maps, a, grid, smem, c)
+                       : narrow ? launch_bt<1, 8, kBtKTNarrow>(maps, a, grid, smem, c)
+                                : launch_bt<1, 8, kBtKT>(maps, a, grid, smem, c);
+        case 2: return wide     ? launch_bt<2, 16, kBtKT>(maps, a, grid, smem, c)
+                       : narrow ? launch_bt<2, 8, kBtKTNarrow>(maps, a, grid, smem, c)
+                                : launch_bt<2, 8, kBtKT>(maps, a, grid, smem, c);
+        case 4: return launch_bt<4, 8, kBtKT>(maps, a, grid, smem, c);
+        default: return launch_bt<kMT, 8, kBtKT>(maps, a, grid, smem, c);
     }
 }
 

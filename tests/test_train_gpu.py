@@ -100,6 +100,8 @@ BACKWARD_TMA_SHAPES = [
     (1, 2048, 8192, 32, True),     # 16 consumer warps (1-2 rows of d_out, K >= 8192), cluster
     (2, 600, 9216, 64, False),     # 16 consumer warps, MT = 2, ragged N
     (1, 4096, 14336, 32, True),    # 16 consumer warps, rows split through the workspace
+    (2, 4104, 1056, 32, False),    # 128-k tiles (two rows per warp pass), ragged K and N
+    (1, 6000, 512, 256, True),     # 128-k tiles, a group spans two tiles
 ]
 
 
@@ -119,7 +121,8 @@ def test_backward_tma_nibble_even_high_and_repeat(handle):
     np.testing.assert_array_equal(out, run_backward(handle, c, even_high=True))
 
 
-@pytest.mark.parametrize("M,N,K,gs", [(4, 300, 512, 32), (9, 1000, 2048, 128), (1, 77, 40, 8)])
+@pytest.mark.parametrize("M,N,K,gs", [(4, 300, 512, 32), (9, 1000, 2048, 128), (1, 77, 40, 8),
+                                      (1, 4096, 2048, 32), (2, 8192, 1024, 64)])
 def test_backward_dyadic_bit_exact(handle, M, N, K, gs):
     c = synth.make_backward_case(M, N, K, gs, seed=N, dyadic=True)
     ref, _ = oracle.backward_dx(c.d_out, c.qweight, c.scales, K, gs)
