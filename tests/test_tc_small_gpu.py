@@ -93,6 +93,10 @@ def test_every_m_bf16_operands(bf16, M):
     (8, 384, 5120, 32, True, "tc_small"),         # resident, but an even ring < 4 stages
     (8, 384, 4096, 32, False, "tc_small_bf16"),   # four stages of the ring, fp32 scales
     (5, 520, 2048, 2048, False, "tc_small_bf16"),  # per channel, fp32
+    (3, 200, 1056, 32, False, "tc_small_bf16"),   # ragged N and K (last stage mostly past K)
+    (7, 1032, 1536, 1536, True, "tc_small_bf16"),  # per channel, fp16, ragged N
+    (2, 4104, 2048, 64, True, "tc_small_bf16"),   # 33 blocks, group 64
+    (6, 1024, 2048, 1024, True, "tc_small_bf16"),  # group wider than a stage
     (4, 2600, 8192, 32, True, "tc_small"),        # x streamed
     (9, 1000, 2048, 32, True, "tc_small"),        # more than 8 rows
 ])
@@ -169,6 +173,11 @@ def test_persistent_over_many_blocks(handle, M, mode):
 
 def test_even_high(handle):
     check(handle, synth.make_case(5, 704, 2048, 64, scale_f16=True, bias=True, seed=3),
+          even_high=True)
+
+
+def test_even_high_bf16_operands(bf16):
+    check(bf16, synth.make_case(5, 704, 2048, 64, scale_f16=True, bias=True, seed=4),
           even_high=True)
 
 
