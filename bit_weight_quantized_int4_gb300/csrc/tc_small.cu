@@ -49,13 +49,15 @@
 //                      K <= 1280 as 32-row chunks) it
 //                      first copies the whole x after griddepcontrol.wait, resident for all
 //                      the CTA's blocks, one 3D box of 8 chunks [rows x 32 k] per 256-k group
-//                      on its own barrier.
+//                      on its own barrier (with bf16 operands the dequantizing warps convert
+//                      x instead, and this thread only issues MMAs).
 //   warp 25, one lane: (longer K only) streams x instead, one 256-k group per stage of the
 //                      CTA's sequence through a ring of three, released by the MMAs'
 //                      commits: ~5 % slower than resident x (28672 x 4096 at 12 rows 34.1 us
 //                      against 33.0 resident at 8).
 //   warps 1-3, lane 0: MMA issuers; slot i of the CTA's sequence goes to issuer i % 4:
-//                      eight tcgen05.mma.kind::tf32 of K = 8 (A from tensor memory), then a
+//                      eight tcgen05.mma.kind::tf32 of K = 8, or kind::f16 of K = 16 with
+//                      bf16 operands (A from tensor memory), then a
 //                      commit that frees the A slot; after its last slot of a block, a commit
 //                      to the block's "D full".  Warp 1 also allocates and frees the 512
 //                      tensor-memory columns.
