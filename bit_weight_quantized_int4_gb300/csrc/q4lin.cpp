@@ -69,17 +69,30 @@ bool multirow_preferred(const q4lin::Problem& p) {
 // 2048 57 / 74 us, 28672 x 4096 33 / 43 us, 14336 x 4096 19 / 23 us, 8192 x 2048 9.1 /
 // 12.0 us), against, at 3..4 rows, the multi-row GEMV (128256 x 2048: 66 / 79 us at 3 / 4
 // rows; it stays ahead where a last wave of a few blocks doubles the small-M GEMM's time:
-// 22016 x 4096 at 3 rows 27 against 33 us) and, from 5 rows, the tile GEMM (128256 x 2048
-// 111-115 us; it stays ahead on few long blocks, 4096 x 4096 12 against 17 us, and above
-// 16 rows on few blocks, 8192 x 2048 11.4 against 12.0 us).  Two rows stay with the
-// multi-row GEMV (50.5 against 57 us on 128256 x 2048).
+// 22016 x 4096 at 3 rows 27 against 33 us, and at 3 rows on less than one wave, 14336 x
+// 4096 19.1 against 20.0) and, from 5 rows, the tile GEMM (128256 x 2048
+// 111-115 us; above 16 rows it stays ahead on few blocks, 8192 x 2048 11.4 against 12.0 us).
+// On fewer blocks than half the SMs the small-M GEMM splits K (see tc_small_parts): AUTO
+// takes it at 5..8 rows from 4 M weights (8 rows: 4096 x 4096 9.5 against the tile GEMM's
+// 11.8 us, 2048 x 8192 10.9 against 16.1, 2048 x 2048 6.1 against row streaming's 7.3), at
+// 9..16 rows at any size (1000 x 2048 at 12 rows: 6.0 against 7.2), at 4 rows on long
+// rows of >= 4096 rows (4096 x 14336: 19.7 against the multi-row GEMV's 21.9; within 5 %
+// either way on shorter rows, and behind on 2048 x 8192, 10.9 against 10.5) and at
+// 17..32 rows for K >= 8192 (2048 x 8192 15.0
+// against 16.2; shorter rows stay with the tile GEMM, 2048 x 2048 7.3 against 9.2).  Two
+// rows stay with the multi-row GEMV (50.5 against 57 us on 128256 x 2048).
 bool tc_small_preferred(const q4lin::Problem& p, const q4lin::LaunchCtx& c) {
     if (p.M < 3 || p.M > 32 || !q4lin::tc_small_eligible(p, c)) return false;
     const int64_t blocks = (p.N + 127) / 128, sms = c.sm_count;
     const int64_t stages = (p.K + 255) / 256, tail = blocks % sms;
-    if (p.M <= 4) return blocks >= 100 && (tail == 0 || 4 * tail > sms);
-    if (p.M <= 16) return blocks >= 100 || (stages <= 8 && blocks >= 40);
-    return blocks >= 100;
+    const bool split = q4lin::tc_small_parts(p, c) > 1;
+    if (p.M <= 4)
+        return (blocks >= (p.M == 3 ? sms : 100) && (tail == 0 || 4 * tail > sms)) ||
+               (p.M == 4 && split && p.N >= 4096 && p.K >= 8192);
+    if (p.M <= 16)
+        return blocks >= 100 || (stages <= 8 && blocks >= 40) ||
+               (split && (p.M > 8 || p.N * p.K >= (4LL << 20)));
+    return blocks >= 100 || (split && p.K >= 8192);
 }
 
 class DeviceGuard {

@@ -141,6 +141,10 @@ bool tc_small_eligible(const Problem& p, const LaunchCtx& c);
 // split into bf16(x) and bf16(x - bf16(x)), the dequantized weights rounded to bf16)
 // rather than tf32: by default from 100 row blocks, or as Q4LIN_OPT_TC_SMALL_OPERANDS says.
 bool tc_small_uses_bf16(const Problem& p, const LaunchCtx& c);
+// Parts of that kernel's K split (1: none): on matrices with fewer 128-row blocks than half
+// the SMs, the largest of 2, 4 or 8 parts dividing the 256-k stages into runs of >= 2 whose
+// items fit one wave, within the handle's split-K workspace and tickets.
+int tc_small_parts(const Problem& p, const LaunchCtx& c);
 cudaError_t tc_small_launch(const Problem& p, const LaunchCtx& c);
 
 }  // namespace q4lin

@@ -75,6 +75,13 @@
 //                      below the tf32 rounding).  Per-channel scales are applied in the
 //                      epilogue instead (A = c - 8 exactly).
 //   Each CTA walks K from its own starting stage (blockIdx.x % stages, wrapping).
+// K split (matrices with fewer 128-row blocks than half the SMs): each block is 2, 4 or 8
+// work items over consecutive runs of its 256-k stages, one item per CTA; the epilogue
+// writes an item's partial tile [columns x 128 rows] to the split-K workspace, takes the
+// block's ticket, and the last item of the block adds the parts in part order (the sum
+// does not depend on which CTA finishes last), applies the channel scale and bias, stores
+// and resets the ticket.  After a timed-out wait the epilogue still walks every item so
+// that every ticket is counted and reset.
 // Tensor memory: accumulators [0, 8 BT) (two blocks in flight x four issuers x BT columns),
 // the A ring [8 BT, 512) (six slots of 64 columns at BT = 16, four at BT = 32).  Slot i of
 // the sequence takes ring position i % slots on lap i / slots, team i % 4 and issuer i % 4;
@@ -151,6 +158,13 @@ struct TsArgs {
     uint32_t x_bytes;     // x region: 8 chunks x xrows x 128 B per 256-k group, + 1 KiB
     int x_ring;           // 0: all of x resident; 1: streamed through a ring of kXStages
     int skip_first_copy;  // test hook: stage 0's codes are not requested
+    // K split: each 128-row block is `parts` work items of nst / parts stages; CTA c takes
+    // part c % parts of blocks c / parts, c / parts + grid / parts, ... (the grid is a
+    // multiple of parts).  With parts > 1 the items leave their partial tiles in ws and
+    // the last item of a block (ticket count) adds them in part order.
+    int parts;
+    float* ws;            // [blocks][parts][columns][128] partial tiles (parts > 1)
+    int* tickets;         // [blocks], zero between launches (the last item resets its own)
     int* status;
     int64_t wait_ns;
 };
@@ -283,6 +297,7 @@ __global__ void __launch_bounds__(XR ? kThreads : kThreads - 32, 1)
     static_assert(8 * (kB4 + kIssuers) <= 960, "barriers fit below the flags");
     volatile int* failed = reinterpret_cast<volatile int*>(gbase + (bar0 - base) + 960);
     const uint32_t tslot = bar0 + 968;
+    volatile int* s_ticket = reinterpret_cast<volatile int*>(gbase + (bar0 - base) + 976);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
@@ -314,16 +329,20 @@ __global__ void __launch_bounds__(XR ? kThreads : kThreads - 32, 1)
     asm volatile("ld.shared.u32 %0, [%1];" : "=r"(tmem) : "r"(tslot) : "memory");
     griddep_launch_dependents();
 
-    // This CTA's blocks: blockIdx.x, + gridDim.x, ...; its stages and 32-k slots in order.
-    const int my_blocks = ((int)a.blocks - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
-    const int n_stages = my_blocks * a.nst;
+    // This CTA's work items: blockIdx.x, + gridDim.x, ... (item = block * parts + part, the
+    // part the same for all of them); their stages and A slots in order.
+    const int parts = a.parts, tpp = a.nst / parts, my_part = (int)blockIdx.x % parts;
+    const int items = a.blocks * parts;
+    const int my_blocks = (items - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
+    auto blk_of = [&](int j) { return ((int)blockIdx.x + j * (int)gridDim.x) / parts; };
+    const int n_stages = my_blocks * tpp;
     const int n_slots = n_stages * SPS;
-    const int slots_per_block = a.nst * SPS;
+    const int slots_per_block = tpp * SPS;
     // Each CTA walks K from its own starting stage (blockIdx.x % stages, wrapping), so
     // that the CTAs' concurrent weight requests spread over the column offsets of the
     // rows instead of all asking for the same 128 bytes of every row at once.
-    const int rot = (int)(blockIdx.x % (unsigned)a.nst);
-    auto kstage = [&](int t) { return t + rot < a.nst ? t + rot : t + rot - a.nst; };
+    const int rot = (int)((blockIdx.x / (unsigned)parts) % (unsigned)tpp);
+    auto kstage = [&](int t) { return my_part * tpp + (t + rot < tpp ? t + rot : t + rot - tpp); };
 
     if (warp == 0) {
         if (lane == 0) {
@@ -333,8 +352,8 @@ __global__ void __launch_bounds__(XR ? kThreads : kThreads - 32, 1)
             if (!PC) prefetch_tensormap(&tms);
             int g = 0;
             for (; g < n_stages; ++g) {
-                const int b = g % a.wst, t = kstage(g % a.nst);
-                const int row0 = ((int)blockIdx.x + (g / a.nst) * (int)gridDim.x) * kRows;
+                const int b = g % a.wst, t = kstage(g % tpp);
+                const int row0 = blk_of(g / tpp) * kRows;
                 if (g >= a.wst &&
                     !wait_backoff(wempty(b), ((g / a.wst) - 1) & 1, a.wait_ns, failed, 64)) {
                     record_failure(a.status, failed);
@@ -373,7 +392,7 @@ __global__ void __launch_bounds__(XR ? kThreads : kThreads - 32, 1)
                 if (*failed) break;
                 mbar_arrive_expect_tx(xfull(b), gbytes);
                 tma_load_3d(xbase + (uint32_t)b * gbytes, &tmx, 0, 0,
-                            kstage(g % a.nst) * kChunksPerStage, xfull(b));
+                            kstage(g % tpp) * kChunksPerStage, xfull(b));
             }
             for (int q = g > kXStages ? g - kXStages : 0; q < g; ++q)
                 wait_bounded(xfull(q % kXStages), (q / kXStages) & 1, kDrainNs, nullptr);
@@ -390,7 +409,7 @@ __global__ void __launch_bounds__(XR ? kThreads : kThreads - 32, 1)
                 prefetch_tensormap(&tmx);
                 griddep_wait();  // x belongs to the dependency chain
                 const uint32_t gbytes = (uint32_t)(kChunksPerStage * a.xrows * 128);
-                for (int q = 0; q < a.nst; ++q) {
+                for (int q = 0; q < tpp; ++q) {  // the groups of this CTA's part
                     const int grp = kstage(q);
                     mbar_arrive_expect_tx(xfull(grp), gbytes);
                     tma_load_3d(xbase + (uint32_t)grp * gbytes, &tmx, 0, 0,
@@ -466,50 +485,82 @@ __global__ void __launch_bounds__(XR ? kThreads : kThreads - 32, 1)
             mma_commit(drain(u));
             wait_bounded(drain(u), 0, kDrainNs, nullptr);
             if (warp == kIss3Warp && !XR && !BF)
-                for (int grp = 0; grp < a.nst; ++grp) wait_bounded(xfull(grp), 0, kDrainNs, nullptr);
+                for (int q = 0; q < tpp; ++q) wait_bounded(xfull(kstage(q)), 0, kDrainNs, nullptr);
         }
     } else if (warp < kDeqWarp0) {
         // ----------------------------------------------------------------- epilogue
         const int q = warp & 3;
         const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
         griddep_wait();  // bias, out belong to the dependency chain
+        constexpr int MC = BF ? 8 : BT;  // output columns of a row (bf16: x_hi and x_lo added)
+        const int r = q * 32 + lane;
+        // After a timed-out wait the warps still walk every item (K split: every ticket is
+        // counted and reset), without reading tensor memory or storing.
+        bool dead = false;
         for (int j = 0; j < my_blocks; ++j) {
             const int par = j & 1;
-            if (!__all_sync(0xffffffffu,
-                            wait_backoff(dfull(par), (j >> 1) & 1, a.wait_ns, failed, 256))) {
+            if (!dead && !__all_sync(0xffffffffu,
+                                     wait_backoff(dfull(par), (j >> 1) & 1, a.wait_ns, failed, 256))) {
                 if (lane == 0) record_failure(a.status, failed);
-                break;
+                dead = true;
             }
-            tc_fence_after();
+            if (dead && parts == 1) break;
             float acc[BT];
 #pragma unroll
-            for (int u = 0; u < kIssuers; ++u) {
+            for (int m = 0; m < BT; ++m) acc[m] = 0.f;
+            if (!dead) {
+                tc_fence_after();
 #pragma unroll
-                for (int c = 0; c < BT; c += 16) {
-                    uint32_t r[16];
-                    tmem_ld16(lane_base + (uint32_t)((par * kIssuers + u) * BT + c), r);
+                for (int u = 0; u < kIssuers; ++u) {
 #pragma unroll
-                    for (int m = 0; m < 16; ++m)
-                        acc[c + m] = u == 0 ? __uint_as_float(r[m]) : acc[c + m] + __uint_as_float(r[m]);
+                    for (int c = 0; c < BT; c += 16) {
+                        uint32_t rr[16];
+                        tmem_ld16(lane_base + (uint32_t)((par * kIssuers + u) * BT + c), rr);
+#pragma unroll
+                        for (int m = 0; m < 16; ++m)
+                            acc[c + m] = u == 0 ? __uint_as_float(rr[m]) : acc[c + m] + __uint_as_float(rr[m]);
+                    }
                 }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(dempty(par));
+                if (BF)
+#pragma unroll
+                    for (int m = 0; m < 8; ++m) acc[m] += acc[m + 8];  // x_hi and x_lo products
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(dempty(par));
-            const int64_t n = ((int64_t)blockIdx.x + (int64_t)j * gridDim.x) * kRows + q * 32 + lane;
-            if (n < a.N && !*failed) {
+            const int blk = blk_of(j);
+            const int64_t n = (int64_t)blk * kRows + r;
+            if (parts > 1) {
+                // This item's partial tile to the workspace; the last item of the block (ticket)
+                // adds the parts in part order.  The partials are ordered before the ticket by
+                // the epilogue warps' barrier and one device-scope fence of the thread that
+                // takes it; the last item's reads after it by that thread's second fence.
+                float* wp = a.ws + ((int64_t)(blk * parts + my_part) * MC) * kRows + r;
+                if (!dead)
+#pragma unroll
+                    for (int m = 0; m < MC; ++m) wp[(int64_t)m * kRows] = acc[m];
+                asm volatile("bar.sync 1, 128;" ::: "memory");
+                if (q == 0 && lane == 0) {
+                    __threadfence();
+                    *s_ticket = atomicAdd(a.tickets + blk, 1);
+                    __threadfence();
+                }
+                asm volatile("bar.sync 1, 128;" ::: "memory");
+                if (*s_ticket != parts - 1) continue;
+                const float* rp = a.ws + ((int64_t)blk * parts * MC) * kRows + r;
+#pragma unroll
+                for (int m = 0; m < MC; ++m) acc[m] = 0.f;
+                for (int pp = 0; pp < parts; ++pp)
+#pragma unroll
+                    for (int m = 0; m < MC; ++m) acc[m] += __ldcg(rp + ((int64_t)pp * MC + m) * kRows);
+                if (q == 0 && lane == 0) a.tickets[blk] = 0;
+            }
+            if (!dead && n < a.N && !*failed) {
                 const float cs = PC ? ld_scale(a.scales, F16, n) : 1.f;
                 const float bv = a.bias ? __ldg(a.bias + n) : 0.f;
-                if (BF) {
-                    // Columns m and m + 8: the products with x_hi and with x_lo.
 #pragma unroll
-                    for (int m = 0; m < 8; ++m)
-                        if (m < a.M) a.out[(int64_t)m * a.N + n] = fmaf(acc[m] + acc[m + 8], cs, bv);
-                } else {
-#pragma unroll
-                    for (int m = 0; m < BT; ++m)
-                        if (m < a.M) a.out[(int64_t)m * a.N + n] = fmaf(acc[m], cs, bv);
-                }
+                for (int m = 0; m < MC; ++m)
+                    if (m < a.M) a.out[(int64_t)m * a.N + n] = fmaf(acc[m], cs, bv);
             }
         }
     } else {
@@ -687,6 +738,25 @@ bool tc_small_eligible(const Problem& p, const LaunchCtx& c) {
     return tensor_map_encoder() != nullptr;
 }
 
+// K split of the small-M GEMM for matrices with fewer 128-row blocks than SMs: the largest
+// count of parts (2, 4 or 8, dividing the 256-k stages, at least two stages a part; bf16
+// operands need two for every issuer to have a slot in every item) whose items still fit
+// one wave, within the handle's workspace and tickets.  1: no split.  Measured at 8 rows
+// (device time, HBM-cold): 4096 x 4096 17.1 -> 9.5 us (4 parts), 6144 x 4096 -> 12.6 (2),
+// 4096 x 14336 -> 19.7 (4), 2048 x 2048 -> 5.9 (4); not on 8 stages of more than 48
+// blocks (8192 x 2048: 9.1 unsplit, 9.5 in 2 parts).
+int tc_small_parts(const Problem& p, const LaunchCtx& c) {
+    const int64_t blocks = (p.N + kRows - 1) / kRows, nst = (p.K + kStageK - 1) / kStageK;
+    if (!c.ws || !c.tickets || blocks > c.ticket_count || 2 * blocks > c.sm_count) return 1;
+    if (nst <= 8 && blocks > 48) return 1;
+    const int64_t cols = p.M > 16 ? 32 : 16;
+    for (int parts = 8; parts >= 2; parts /= 2)
+        if (nst % parts == 0 && nst / parts >= 2 && blocks * parts <= c.sm_count &&
+            blocks * parts * cols * kRows <= c.ws_floats)
+            return parts;
+    return 1;
+}
+
 // bf16 operands (x split into two bf16 terms) where they apply: up to 8 rows, x resident,
 // at least two 256-k stages (every issuer then has a slot in every block) and an even
 // weight ring of at least four stages.  With two A slots a stage, even stages go to teams
@@ -728,6 +798,9 @@ cudaError_t tc_small_launch(const Problem& p, const LaunchCtx& c) {
     a.skip_first_copy = c.tc_skip_first_copy;
     a.status = c.status_word;
     a.wait_ns = c.wait_limit_ns;
+    a.parts = tc_small_parts(p, c);
+    a.ws = c.ws;
+    a.tickets = c.tickets;
 
     CUtensorMap tw, ts, tx;
     const cuuint32_t e2[2] = {1, 1}, e3[3] = {1, 1, 1};
@@ -766,7 +839,8 @@ cudaError_t tc_small_launch(const Problem& p, const LaunchCtx& c) {
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
-    const unsigned grid = (unsigned)std::min<int64_t>(a.blocks, c.sm_count);
+    const int64_t items = (int64_t)a.blocks * a.parts;
+    const unsigned grid = (unsigned)(std::min<int64_t>(items, c.sm_count) / a.parts * a.parts);
     if (tc_small_uses_bf16(p, c)) {
         a.wst &= ~1;
         return launch_eh<false, 16, true>(p, tw, ts, tx, a, grid, smem, c);

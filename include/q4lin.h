@@ -75,9 +75,12 @@ typedef enum {
                                x resident in shared memory or streamed for long K
                                (K % 32 == 0, 16-byte aligned x and qweight; grouped
                                scales: a power-of-two multiple of 32 as group size and a
-                               scale row of whole 16-byte units); tensor-core
-                               tolerance.  AUTO takes it for 3..32 rows when the
-                               128-row blocks fill the SMs (measured crossover) */
+                               scale row of whole 16-byte units); on fewer blocks
+                               than half the SMs it splits K and adds the parts
+                               through the handle's workspace (deterministic order);
+                               tensor-core tolerance.  AUTO takes it for 3..32 rows
+                               where it measured fastest (large matrices, and with
+                               the K split most smaller ones from 5 rows) */
 } q4lin_path_t;
 
 /* Options for q4lin_set_option / q4lin_get_option. */

@@ -265,6 +265,39 @@ def test_bounded_wait_times_out_cleanly(handle, mode):
         q.q4lin_set_option(handle, q.Q4LIN_OPT_TC_SMALL_OPERANDS, 0)
 
 
+@pytest.mark.parametrize("M,N,K,gs,f16,mode", [
+    (8, 4096, 4096, 32, True, 0),     # 32 blocks: 4 parts of 4 stages
+    (6, 6144, 4096, 64, False, 0),    # 48 blocks: 2 parts, fp32 scales
+    (16, 2048, 8192, 128, True, 0),   # 16 blocks: 8 parts (x streamed through the ring)
+    (5, 1000, 2048, 32, True, 0),     # 8 blocks, ragged N: 4 parts of 2 stages
+    (3, 520, 4096, 4096, True, 0),    # per channel, 5 blocks
+    (24, 1504, 2048, 32, True, 0),    # MMA width 32, 12 blocks
+    (4, 2048, 2048, 32, True, 2),     # bf16 operands, 4 parts of 2 stages
+    (8, 3000, 1024, 32, False, 2),    # bf16 operands, ragged N, 2 parts
+])
+def test_k_split(handle, M, N, K, gs, f16, mode):
+    """Fewer 128-row blocks than half the SMs: each block is split over K into parts whose
+    partial tiles the last part of the block adds (in part order) through the workspace."""
+    from bit_weight_quantized_int4_gb300 import q4lin as q
+    c = synth.make_case(M, N, K, gs, scale_f16=f16, bias=True, seed=M + N + K)
+    q.q4lin_set_option(handle, q.Q4LIN_OPT_TC_SMALL_OPERANDS, mode)
+    try:
+        a = check(handle, c)
+        b, _ = run_q4lin(handle, c, TC_SMALL)
+        np.testing.assert_array_equal(a, b)  # the part order fixes the sum
+    finally:
+        q.q4lin_set_option(handle, q.Q4LIN_OPT_TC_SMALL_OPERANDS, 0)
+
+
+@pytest.mark.parametrize("M,N,K", [(8, 2048, 4096), (4, 1000, 2048)])
+def test_k_split_dyadic_bit_exact(handle, M, N, K):
+    c = synth.make_dyadic_case(M, N, K, 32, scale_f16=True, bias=True, seed=N + K)
+    out, used = run_q4lin(handle, c, TC_SMALL)
+    assert used == TC_SMALL
+    ref, _ = oracle.linear(c.x, c.qweight, c.scales, c.bias, c.K, c.group_size)
+    np.testing.assert_array_equal(out.astype(np.float64), ref)
+
+
 @pytest.mark.parametrize("pdl", [0, 1])
 @pytest.mark.parametrize("M", [4, 12, 20])
 def test_chain_with_dependent_launch(handle, M, pdl):
@@ -323,12 +356,21 @@ def _auto_kernel(handle, M, N, K, f16=True):
     (3, 128256, 2048, "tc_small_bf16"),  # bf16 operands from 100 row blocks
     (4, 28672, 4096, "tc_small_bf16"),
     (3, 22016, 4096, "multirow"),    # a last wave of 20 blocks on 152 SMs
+    (3, 14336, 4096, "multirow"),    # 3 rows on less than one wave (112 blocks)
+    (3, 28672, 4096, "tc_small_bf16"),  # 224 blocks
     (4, 8192, 2048, "multirow"),     # 64 blocks at 3-4 rows
     (8, 8192, 2048, "tc_small"),     # 64 blocks of 8 stages
-    (8, 4096, 4096, "tc"),           # 32 blocks of 16 stages
+    (8, 4096, 4096, "tc_small"),     # 32 blocks of 16 stages: K split in 4 parts
     (16, 128256, 2048, "tc_small"),
     (16, 14336, 4096, "tc_small"),   # 16 rows of x for K = 4096 stream through a ring
-    (8, 2048, 2048, "rowstream"),    # 16 blocks, 4 M weights
+    (8, 2048, 2048, "tc_small"),     # 16 blocks, 4 M weights: K split in 4 parts
+    (8, 1000, 2048, "rowstream"),    # 2 M weights: the CUDA-core path
+    (12, 2048, 8192, "tc_small"),    # 16 blocks of 32 stages: K split in 8 parts
+    (4, 4096, 14336, "tc_small"),    # 4 rows, K split, long rows of >= 4096 rows
+    (4, 4096, 4096, "multirow"),     # 3-4 rows keep the multi-row GEMV below 100 blocks
+    (4, 2048, 8192, "multirow"),     # 4 rows on 2048 rows: the multi-row GEMV
+    (12, 1000, 2048, "tc_small"),    # 9-16 rows: the K split at any size
+    (24, 2048, 8192, "tc_small"),    # 17-32 rows: the K split for K >= 8192
     (24, 128256, 2048, "tc_small"),  # MMA width 32
     (24, 8192, 2048, "tc"),          # 64 blocks above 16 rows: the tile GEMM
 ])
