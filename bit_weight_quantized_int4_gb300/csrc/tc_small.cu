@@ -261,7 +261,7 @@ __device__ __forceinline__ void convert_x_bf16(const TsArgs& a, uint32_t xbase, 
     }
 }
 
-template <bool EH, bool PC, bool F16, bool XR, int BT, bool BF>
+template <bool EH, bool PC, bool F16, bool XR, int BT, bool BF, bool KS>
 __global__ void __launch_bounds__(XR ? kThreads : kThreads - 32, 1)
     tc_small_kernel(const __grid_constant__ CUtensorMap tmw, const __grid_constant__ CUtensorMap tms,
                     const __grid_constant__ CUtensorMap tmx, const TsArgs a) {
@@ -331,7 +331,9 @@ __global__ void __launch_bounds__(XR ? kThreads : kThreads - 32, 1)
 
     // This CTA's work items: blockIdx.x, + gridDim.x, ... (item = block * parts + part, the
     // part the same for all of them); their stages and A slots in order.
-    const int parts = a.parts, tpp = a.nst / parts, my_part = (int)blockIdx.x % parts;
+    // (KS: K split instances; the others compile with one part.)
+    const int parts = KS ? a.parts : 1, tpp = KS ? a.nst / parts : a.nst;
+    const int my_part = KS ? (int)blockIdx.x % parts : 0;
     const int items = a.blocks * parts;
     const int my_blocks = (items - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
     auto blk_of = [&](int j) { return ((int)blockIdx.x + j * (int)gridDim.x) / parts; };
@@ -492,75 +494,117 @@ __global__ void __launch_bounds__(XR ? kThreads : kThreads - 32, 1)
         const int q = warp & 3;
         const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
         griddep_wait();  // bias, out belong to the dependency chain
-        constexpr int MC = BF ? 8 : BT;  // output columns of a row (bf16: x_hi and x_lo added)
-        const int r = q * 32 + lane;
-        // After a timed-out wait the warps still walk every item (K split: every ticket is
-        // counted and reset), without reading tensor memory or storing.
-        bool dead = false;
-        for (int j = 0; j < my_blocks; ++j) {
-            const int par = j & 1;
-            if (!dead && !__all_sync(0xffffffffu,
-                                     wait_backoff(dfull(par), (j >> 1) & 1, a.wait_ns, failed, 256))) {
-                if (lane == 0) record_failure(a.status, failed);
-                dead = true;
-            }
-            if (dead && parts == 1) break;
-            float acc[BT];
-#pragma unroll
-            for (int m = 0; m < BT; ++m) acc[m] = 0.f;
-            if (!dead) {
+        if constexpr (!KS) {
+            for (int j = 0; j < my_blocks; ++j) {
+                const int par = j & 1;
+                if (!__all_sync(0xffffffffu,
+                                wait_backoff(dfull(par), (j >> 1) & 1, a.wait_ns, failed, 256))) {
+                    if (lane == 0) record_failure(a.status, failed);
+                    break;
+                }
                 tc_fence_after();
+                float acc[BT];
 #pragma unroll
                 for (int u = 0; u < kIssuers; ++u) {
 #pragma unroll
                     for (int c = 0; c < BT; c += 16) {
-                        uint32_t rr[16];
-                        tmem_ld16(lane_base + (uint32_t)((par * kIssuers + u) * BT + c), rr);
+                        uint32_t r[16];
+                        tmem_ld16(lane_base + (uint32_t)((par * kIssuers + u) * BT + c), r);
 #pragma unroll
                         for (int m = 0; m < 16; ++m)
-                            acc[c + m] = u == 0 ? __uint_as_float(rr[m]) : acc[c + m] + __uint_as_float(rr[m]);
+                            acc[c + m] = u == 0 ? __uint_as_float(r[m]) : acc[c + m] + __uint_as_float(r[m]);
                     }
                 }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(dempty(par));
-                if (BF)
+                const int64_t n = ((int64_t)blockIdx.x + (int64_t)j * gridDim.x) * kRows + q * 32 + lane;
+                if (n < a.N && !*failed) {
+                    const float cs = PC ? ld_scale(a.scales, F16, n) : 1.f;
+                    const float bv = a.bias ? __ldg(a.bias + n) : 0.f;
+                    if (BF) {
+                        // Columns m and m + 8: the products with x_hi and with x_lo.
 #pragma unroll
-                    for (int m = 0; m < 8; ++m) acc[m] += acc[m + 8];  // x_hi and x_lo products
-            }
-            const int blk = blk_of(j);
-            const int64_t n = (int64_t)blk * kRows + r;
-            if (parts > 1) {
-                // This item's partial tile to the workspace; the last item of the block (ticket)
-                // adds the parts in part order.  The partials are ordered before the ticket by
-                // the epilogue warps' barrier and one device-scope fence of the thread that
-                // takes it; the last item's reads after it by that thread's second fence.
-                float* wp = a.ws + ((int64_t)(blk * parts + my_part) * MC) * kRows + r;
-                if (!dead)
+                        for (int m = 0; m < 8; ++m)
+                            if (m < a.M) a.out[(int64_t)m * a.N + n] = fmaf(acc[m] + acc[m + 8], cs, bv);
+                    } else {
 #pragma unroll
-                    for (int m = 0; m < MC; ++m) wp[(int64_t)m * kRows] = acc[m];
-                asm volatile("bar.sync 1, 128;" ::: "memory");
-                if (q == 0 && lane == 0) {
-                    __threadfence();
-                    *s_ticket = atomicAdd(a.tickets + blk, 1);
-                    __threadfence();
+                        for (int m = 0; m < BT; ++m)
+                            if (m < a.M) a.out[(int64_t)m * a.N + n] = fmaf(acc[m], cs, bv);
+                    }
                 }
-                asm volatile("bar.sync 1, 128;" ::: "memory");
-                if (*s_ticket != parts - 1) continue;
-                const float* rp = a.ws + ((int64_t)blk * parts * MC) * kRows + r;
-#pragma unroll
-                for (int m = 0; m < MC; ++m) acc[m] = 0.f;
-                for (int pp = 0; pp < parts; ++pp)
-#pragma unroll
-                    for (int m = 0; m < MC; ++m) acc[m] += __ldcg(rp + ((int64_t)pp * MC + m) * kRows);
-                if (q == 0 && lane == 0) a.tickets[blk] = 0;
             }
-            if (!dead && n < a.N && !*failed) {
-                const float cs = PC ? ld_scale(a.scales, F16, n) : 1.f;
-                const float bv = a.bias ? __ldg(a.bias + n) : 0.f;
+        } else {
+            constexpr int MC = BF ? 8 : BT;  // output columns of a row (bf16: x_hi and x_lo added)
+            const int r = q * 32 + lane;
+            // After a timed-out wait the warps still walk every item (K split: every ticket is
+            // counted and reset), without reading tensor memory or storing.
+            bool dead = false;
+            for (int j = 0; j < my_blocks; ++j) {
+                const int par = j & 1;
+                if (!dead && !__all_sync(0xffffffffu,
+                                         wait_backoff(dfull(par), (j >> 1) & 1, a.wait_ns, failed, 256))) {
+                    if (lane == 0) record_failure(a.status, failed);
+                    dead = true;
+                }
+                if (dead && !KS) break;
+                float acc[BT];
 #pragma unroll
-                for (int m = 0; m < MC; ++m)
-                    if (m < a.M) a.out[(int64_t)m * a.N + n] = fmaf(acc[m], cs, bv);
+                for (int m = 0; m < BT; ++m) acc[m] = 0.f;
+                if (!dead) {
+                    tc_fence_after();
+#pragma unroll
+                    for (int u = 0; u < kIssuers; ++u) {
+#pragma unroll
+                        for (int c = 0; c < BT; c += 16) {
+                            uint32_t rr[16];
+                            tmem_ld16(lane_base + (uint32_t)((par * kIssuers + u) * BT + c), rr);
+#pragma unroll
+                            for (int m = 0; m < 16; ++m)
+                                acc[c + m] = u == 0 ? __uint_as_float(rr[m]) : acc[c + m] + __uint_as_float(rr[m]);
+                        }
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(dempty(par));
+                    if (BF)
+#pragma unroll
+                        for (int m = 0; m < 8; ++m) acc[m] += acc[m + 8];  // x_hi and x_lo products
+                }
+                const int blk = blk_of(j);
+                const int64_t n = (int64_t)blk * kRows + r;
+                if (KS) {
+                    // This item's partial tile to the workspace; the last item of the block (ticket)
+                    // adds the parts in part order.  The partials are ordered before the ticket by
+                    // the epilogue warps' barrier and one device-scope fence of the thread that
+                    // takes it; the last item's reads after it by that thread's second fence.
+                    float* wp = a.ws + ((int64_t)(blk * parts + my_part) * MC) * kRows + r;
+                    if (!dead)
+#pragma unroll
+                        for (int m = 0; m < MC; ++m) wp[(int64_t)m * kRows] = acc[m];
+                    asm volatile("bar.sync 1, 128;" ::: "memory");
+                    if (q == 0 && lane == 0) {
+                        __threadfence();
+                        *s_ticket = atomicAdd(a.tickets + blk, 1);
+                        __threadfence();
+                    }
+                    asm volatile("bar.sync 1, 128;" ::: "memory");
+                    if (*s_ticket != parts - 1) continue;
+                    const float* rp = a.ws + ((int64_t)blk * parts * MC) * kRows + r;
+#pragma unroll
+                    for (int m = 0; m < MC; ++m) acc[m] = 0.f;
+                    for (int pp = 0; pp < parts; ++pp)
+#pragma unroll
+                        for (int m = 0; m < MC; ++m) acc[m] += __ldcg(rp + ((int64_t)pp * MC + m) * kRows);
+                    if (q == 0 && lane == 0) a.tickets[blk] = 0;
+                }
+                if (!dead && n < a.N && !*failed) {
+                    const float cs = PC ? ld_scale(a.scales, F16, n) : 1.f;
+                    const float bv = a.bias ? __ldg(a.bias + n) : 0.f;
+#pragma unroll
+                    for (int m = 0; m < MC; ++m)
+                        if (m < a.M) a.out[(int64_t)m * a.N + n] = fmaf(acc[m], cs, bv);
+                }
             }
         }
     } else {
@@ -656,10 +700,10 @@ __global__ void __launch_bounds__(XR ? kThreads : kThreads - 32, 1)
     if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
-template <bool EH, bool PC, bool F16, bool XR, int BT, bool BF>
-cudaError_t launch_ts(const CUtensorMap& tw, const CUtensorMap& ts, const CUtensorMap& tx,
-                      const TsArgs& a, unsigned grid, int smem, const LaunchCtx& c) {
-    constexpr auto kernel = tc_small_kernel<EH, PC, F16, XR, BT, BF>;
+template <bool EH, bool PC, bool F16, bool XR, int BT, bool BF, bool KS>
+cudaError_t launch_ts_k(const CUtensorMap& tw, const CUtensorMap& ts, const CUtensorMap& tx,
+                        const TsArgs& a, unsigned grid, int smem, const LaunchCtx& c) {
+    constexpr auto kernel = tc_small_kernel<EH, PC, F16, XR, BT, BF, KS>;
     const cudaError_t attr = kernel_smem_once<kernel>(kSmemCap);
     if (attr != cudaSuccess) return attr;
     cudaLaunchConfig_t cfg = {};
@@ -675,6 +719,13 @@ cudaError_t launch_ts(const CUtensorMap& tw, const CUtensorMap& ts, const CUtens
         cfg.numAttrs = 1;
     }
     return cudaLaunchKernelEx(&cfg, kernel, tw, ts, tx, a);
+}
+
+template <bool EH, bool PC, bool F16, bool XR, int BT, bool BF>
+cudaError_t launch_ts(const CUtensorMap& tw, const CUtensorMap& ts, const CUtensorMap& tx,
+                      const TsArgs& a, unsigned grid, int smem, const LaunchCtx& c) {
+    if (a.parts > 1) return launch_ts_k<EH, PC, F16, XR, BT, BF, true>(tw, ts, tx, a, grid, smem, c);
+    return launch_ts_k<EH, PC, F16, XR, BT, BF, false>(tw, ts, tx, a, grid, smem, c);
 }
 
 template <bool XR, int BT, bool BF = false>
