@@ -77,9 +77,9 @@ bool multirow_preferred(const q4lin::Problem& p) {
 // 11.8 us, 2048 x 8192 10.9 against 16.1, 2048 x 2048 6.1 against row streaming's 7.3), at
 // 9..16 rows at any size (1000 x 2048 at 12 rows: 6.0 against 7.2), at 4 rows on long
 // rows of >= 4096 rows (4096 x 14336: 19.7 against the multi-row GEMV's 21.9; within 5 %
-// either way on shorter rows, and behind on 2048 x 8192, 10.9 against 10.5) and at
-// 17..32 rows for K >= 8192 (2048 x 8192 15.0
-// against 16.2; shorter rows stay with the tile GEMM, 2048 x 2048 7.3 against 9.2).  Two
+// either way on shorter rows, and behind on 2048 x 8192, 10.9 against 10.5); above 16
+// rows the split is within a few per cent of the tile GEMM either way (2048 x 8192 at 24
+// rows 17.1 against 16.2; 2048 x 2048 10.2 against 7.3) and AUTO keeps the tile GEMM.  Two
 // rows stay with the multi-row GEMV (50.5 against 57 us on 128256 x 2048).
 bool tc_small_preferred(const q4lin::Problem& p, const q4lin::LaunchCtx& c) {
     if (p.M < 3 || p.M > 32 || !q4lin::tc_small_eligible(p, c)) return false;
@@ -92,7 +92,7 @@ bool tc_small_preferred(const q4lin::Problem& p, const q4lin::LaunchCtx& c) {
     if (p.M <= 16)
         return blocks >= 100 || (stages <= 8 && blocks >= 40) ||
                (split && (p.M > 8 || p.N * p.K >= (4LL << 20)));
-    return blocks >= 100 || (split && p.K >= 8192);
+    return blocks >= 100;
 }
 
 class DeviceGuard {

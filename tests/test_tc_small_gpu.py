@@ -370,7 +370,7 @@ def _auto_kernel(handle, M, N, K, f16=True):
     (4, 4096, 4096, "multirow"),     # 3-4 rows keep the multi-row GEMV below 100 blocks
     (4, 2048, 8192, "multirow"),     # 4 rows on 2048 rows: the multi-row GEMV
     (12, 1000, 2048, "tc_small"),    # 9-16 rows: the K split at any size
-    (24, 2048, 8192, "tc_small"),    # 17-32 rows: the K split for K >= 8192
+    (24, 2048, 8192, "tc"),          # 17-32 rows on few blocks: the tile GEMM
     (24, 128256, 2048, "tc_small"),  # MMA width 32
     (24, 8192, 2048, "tc"),          # 64 blocks above 16 rows: the tile GEMM
 ])
