@@ -1063,12 +1063,13 @@ def main():
             s["frac_of_hbm"] = round(s["GB_s"] / hbm_peak, 4)
         extra["gemv_shapes"] = shapes
         # A few activation rows (speculative decoding, small batches): the multi-row GEMV,
-        # and from 3 rows on large matrices the small-M tensor-core GEMM (AUTO's choice;
-        # each row names the kernel that ran).
+        # and from 3 rows on large matrices (on few row blocks with its K split) the small-M
+        # tensor-core GEMM (AUTO's choice; each row names the kernel that ran).
         from bit_weight_quantized_int4_gb300 import q4lin as q
         small = []
         for M in (2, 3, 4, 8, 16, 32):
-            for N, K in ((8192, 2048), (2048, 8192), (128256, 2048), (28672, 4096)):
+            for N, K in ((8192, 2048), (2048, 8192), (128256, 2048), (28672, 4096), (4096, 4096),
+                         (4096, 14336)):
                 row = shape_bandwidth(torch, h, N, K, M)
                 x = torch.empty(M, K, device="cuda")
                 w = torch.empty(N, K // 2, dtype=torch.uint8, device="cuda")
