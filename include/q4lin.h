@@ -22,8 +22,8 @@
  *     synchronizes the device and only enqueues kernels on the given stream.  A handle
  *     owns its options, a 4-byte device status word and 64 MiB of device scratch plus
  *     64 KiB of counters (partial sums of launches that split K or the rows across CTAs:
- *     decode GEMV, tensor-core GEMM, input gradient; the fp16 copy of x of the fp16
- *     tensor-core path), all allocated by q4lin_create.
+ *     decode GEMV, tensor-core GEMM, small-M tensor-core GEMM, input gradient; the fp16
+ *     copy of x of the fp16 tensor-core path), all allocated by q4lin_create.
  *   - Status codes, never exceptions, aborts or prints.  Arguments are validated before
  *     any launch: a non-OK status from validation means nothing was enqueued.
  *   - All device pointers must be device-accessible memory of the handle's device.
